@@ -1,0 +1,363 @@
+"""Pins of the CPU oracle against things other than itself: library
+rounding routines, closed forms, a hand-worked example, pure-Python brute
+force, torch float64 references and finite differences.
+
+Each test is chosen so that a plausible slip in the oracle (a dropped term, a
+wrong sign, index or transposition, a wrong rounding point) fails one of them.
+"""
+import collections
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_case(T=37, H=64, F=96, E=5, k=2, seed=1, empty=(3,), wstd=0.15):
+    rng = np.random.default_rng(seed)
+    x = orc.bf16(rng.standard_normal((T, H)))
+    live = [e for e in range(E) if e not in empty]
+    ids = np.stack([rng.choice(live, size=k, replace=False) for _ in range(T)]).astype(np.int64)
+    logits = rng.standard_normal((T, k))
+    probs = (np.exp(logits) / np.exp(logits).sum(1, keepdims=True)).astype(np.float32).astype(np.float64)
+    wg = orc.bf16(rng.standard_normal((E, H, F)) * wstd)
+    wu = orc.bf16(rng.standard_normal((E, H, F)) * wstd)
+    wd = orc.bf16(rng.standard_normal((E, F, H)) * wstd)
+    return x, wg, wu, wd, ids, probs
+
+
+# ---------------------------------------------------------------- rounding
+
+def test_bf16_matches_torch_rne():
+    rng = np.random.default_rng(0)
+    # float32 values over a wide exponent range, plus exact ties and subnormals
+    mant = rng.integers(0, 1 << 23, 20000)
+    expo = rng.integers(1, 254, 20000)
+    sign = rng.integers(0, 2, 20000)
+    bits = (sign << 31) | (expo << 23) | mant
+    vals = bits.astype(np.uint32).view(np.float32)
+    ties = (np.arange(1, 4000, dtype=np.uint32) << 16 | 0x8000).view(np.float32)
+    subn = (rng.integers(1, 1 << 23, 2000).astype(np.uint32)).view(np.float32)
+    for v in (vals, ties, subn, -ties):
+        want = torch.from_numpy(v.copy()).to(torch.bfloat16).float().numpy().astype(np.float64)
+        got = orc.bf16(v.astype(np.float64))
+        np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_overflow_and_zero():
+    assert orc.bf16(0.0) == 0.0
+    assert np.isinf(orc.bf16(3.5e38))
+    assert orc.bf16(float.fromhex("0x1.fep127")) == float.fromhex("0x1.fep127")
+
+
+def test_e4m3_decode_all_codes_vs_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    got = orc.e4m3_decode(codes)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], want[~nan])
+    assert got[0x7E] == 448.0 and got[0x08] == 2.0 ** -6 and got[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_vs_torch():
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([
+        rng.uniform(-448, 448, 20000),
+        rng.standard_normal(20000) * 0.01,
+        rng.standard_normal(5000) * 2.0 ** -8,
+    ]).astype(np.float32)
+    # exact midpoints between neighbouring codes (ties to even)
+    pos = orc.e4m3_decode(np.arange(0, 0x7F))
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    vals = np.concatenate([vals, mids, -mids])
+    want = torch.from_numpy(vals.copy()).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = orc.e4m3_encode(vals.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_e4m3_satfinite():
+    got = orc.e4m3_encode(np.array([448.0, 463.9, 464.0, 480.0, 1e6, -1e6]))
+    np.testing.assert_array_equal(got, [0x7E, 0x7E, 0x7E, 0x7E, 0x7E, 0xFE])
+
+
+def test_e8m0_scale_closed_forms():
+    # X = 2^(floor(log2 amax) - 8), code = exponent + 127
+    cases = {1.0: 119, 1.5: 119, 2.0: 120, 448.0: 127, 511.0: 127, 2.0 ** -10: 109, 0.0: 0,
+             2.0 ** 140: 254, 2.0 ** -140: 0}
+    for amax, code in cases.items():
+        assert int(orc.e8m0_scale_code(amax)) == code, amax
+
+
+def test_mxfp8_power_of_two_blocks_are_exact():
+    rng = np.random.default_rng(5)
+    ex = rng.integers(-20, 20, (4, 64))
+    sgn = rng.choice([-1.0, 1.0], (4, 64))
+    a = sgn * np.ldexp(1.0, ex)
+    # within a block every value must lie within 2^-9..2^8 of the block max
+    a = np.clip(a, None, None)
+    blocks = a.reshape(4, 2, 32)
+    m = np.abs(blocks).max(-1, keepdims=True)
+    blocks = np.where(np.abs(blocks) < m * 2.0 ** -14, np.sign(blocks) * m * 2.0 ** -14, blocks)
+    a = blocks.reshape(4, 64)
+    q, s = orc.quantize_mxfp8(a)
+    np.testing.assert_array_equal(orc.dequantize_mxfp8(q, s), a)
+
+
+def test_mxfp8_block_max_lands_in_top_binade():
+    rng = np.random.default_rng(6)
+    a = orc.bf16(rng.standard_normal((8, 128)) * 3.0)
+    q, s = orc.quantize_mxfp8(a)
+    vals = orc.e4m3_decode(q).reshape(8, 4, 32)
+    top = np.abs(vals).max(-1)
+    assert np.all((top >= 256) & (top <= 448))
+    err = np.abs(orc.dequantize_mxfp8(q, s) - a).reshape(8, 4, 32)
+    scale = np.ldexp(1.0, s.astype(int) - 127)[..., None]
+    scaled = np.abs(a).reshape(8, 4, 32) / scale
+    # round to nearest: at most half an E4M3 ulp (2^5 at the top binade) in
+    # scaled units; beyond 448 the floor-based scale makes satfinite clamp
+    bound = np.maximum(16.0, scaled - 448.0) * scale
+    assert np.all(err <= bound)
+
+
+# ---------------------------------------------------------------- counts / permute
+
+def test_counts_bruteforce():
+    rng = np.random.default_rng(7)
+    ids = rng.integers(0, 13, (211, 3))
+    c = collections.Counter(ids.reshape(-1).tolist())
+    got = orc.expert_counts(ids, 13)
+    assert got.tolist() == [c.get(e, 0) for e in range(13)]
+    assert got.sum() == ids.size
+    off = orc.expert_offsets(got)
+    assert off[0] == 0 and off[-1] == ids.size and np.all(np.diff(off) == got)
+
+
+def test_counts_rejects_out_of_range():
+    with pytest.raises(ValueError):
+        orc.expert_counts(np.array([[0, 5]]), 5)
+    with pytest.raises(ValueError):
+        orc.expert_counts(np.array([[-1, 0]]), 5)
+
+
+def test_permute_matches_stable_sort():
+    rng = np.random.default_rng(8)
+    T, k, E = 173, 4, 9
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    row_of, token_of, slot_of = orc.permute_map(ids, E)
+    order = sorted(range(T * k), key=lambda i: (ids.reshape(-1)[i], i))   # Python's sort is stable
+    for r, i in enumerate(order):
+        assert token_of[r] == i // k and slot_of[r] == i % k
+        assert row_of.reshape(-1)[i] == r
+
+
+def test_permute_rows_carry_token_and_prob():
+    x, wg, wu, wd, ids, probs = _rand_case()
+    xp, row_of, token_of, prob_of = orc.permute(x, ids, probs, 5)
+    for t in range(x.shape[0]):
+        for j in range(ids.shape[1]):
+            r = row_of[t, j]
+            assert np.array_equal(xp[r], x[t]) and prob_of[r] == probs[t, j]
+
+
+def test_unpermute_unit_probs_gives_k_times_x():
+    rng = np.random.default_rng(9)
+    for k in (1, 2, 4, 6, 8):
+        T, E = 50, 8
+        x = orc.bf16(rng.standard_normal((T, 24)))
+        ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+        xp, row_of, _, _ = orc.permute(x, ids, None, E)
+        y = orc.unpermute(xp, row_of, None)
+        np.testing.assert_array_equal(y, orc.bf16(k * x))
+        if k in (1, 2, 4, 8):
+            np.testing.assert_array_equal(y, k * x)
+
+
+# ---------------------------------------------------------------- forward
+
+def test_worked_example_golden():
+    g = json.load(open(os.path.join(GOLDEN, "tiny_worked_example.json")))
+    y, st = orc.expert_forward(np.array(g["x"]), np.array(g["w_gate"]), np.array(g["w_up"]),
+                               np.array(g["w_down"]), np.array(g["expert_ids"]),
+                               np.array(g["probs"]), keep=True)
+    np.testing.assert_array_equal(y, np.array(g["y"]))
+    np.testing.assert_array_equal(st["h"][st["row_of"][0, 0]], g["h_expert0"])
+
+
+def test_grouped_equals_per_token_dense():
+    x, wg, wu, wd, ids, probs = _rand_case()
+    y1 = orc.expert_forward(x, wg, wu, wd, ids, probs)
+    y2 = orc.dense_forward(x, wg, wu, wd, ids, probs)
+    # same dot products in float64; only BLAS summation order can differ, which
+    # can move a bf16 rounding by one step in rare elements
+    np.testing.assert_allclose(y1, y2, rtol=2 ** -7, atol=1e-6)
+    assert np.mean(y1 == y2) > 0.999
+
+
+def test_forward_pure_python_bruteforce():
+    rng = np.random.default_rng(11)
+    T, H, F, E, k = 4, 6, 5, 3, 2
+    x = rng.standard_normal((T, H))
+    wg, wu = rng.standard_normal((E, H, F)), rng.standard_normal((E, H, F))
+    wd = rng.standard_normal((E, F, H))
+    ids = np.array([[0, 2], [1, 0], [2, 1], [0, 1]])
+    probs = rng.uniform(0.1, 1.0, (T, k))
+    want = [[0.0] * H for _ in range(T)]
+    for t in range(T):
+        for j in range(k):
+            e = ids[t][j]
+            h = []
+            for f in range(F):
+                g = sum(x[t][i] * wg[e][i][f] for i in range(H))
+                u = sum(x[t][i] * wu[e][i][f] for i in range(H))
+                h.append(g / (1.0 + math.exp(-g)) * u)
+            for c in range(H):
+                want[t][c] += probs[t][j] * sum(h[f] * wd[e][f][c] for f in range(F))
+    got = orc.expert_forward(x, wg, wu, wd, ids, probs, rounding=False)
+    np.testing.assert_allclose(got, np.array(want), rtol=1e-12, atol=1e-12)
+
+
+def test_single_expert_is_dense_swiglu_mlp_torch():
+    rng = np.random.default_rng(12)
+    T, H, F = 9, 16, 24
+    x = rng.standard_normal((T, H))
+    wg, wu, wd = (rng.standard_normal((1, H, F)), rng.standard_normal((1, H, F)),
+                  rng.standard_normal((1, F, H)))
+    ids = np.zeros((T, 1), np.int64)
+    probs = np.ones((T, 1))
+    tx = torch.from_numpy(x)
+    want = (torch.nn.functional.silu(tx @ torch.from_numpy(wg[0])) * (tx @ torch.from_numpy(wu[0]))
+            ) @ torch.from_numpy(wd[0])
+    got = orc.expert_forward(x, wg, wu, wd, ids, probs, rounding=False)
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-12, atol=1e-12)
+    # with rounding the only change is bf16 at h, O and y
+    got_r = orc.expert_forward(x, wg, wu, wd, ids, probs)
+    h = orc.bf16((torch.nn.functional.silu(tx @ torch.from_numpy(wg[0])) * (tx @ torch.from_numpy(wu[0]))).numpy())
+    np.testing.assert_allclose(got_r, orc.bf16(orc.bf16(h @ wd[0])), rtol=2 ** -7, atol=1e-9)
+
+
+def test_zero_weights_give_zero():
+    x, wg, wu, wd, ids, probs = _rand_case()
+    assert np.all(orc.expert_forward(x, wg, np.zeros_like(wu), wd, ids, probs) == 0)
+    assert np.all(orc.expert_forward(np.zeros_like(x), wg, wu, wd, ids, probs) == 0)
+    assert np.all(orc.expert_forward(x, np.zeros_like(wg), wu, wd, ids, probs) == 0)
+
+
+def test_probs_weight_linearly():
+    x, wg, wu, wd, ids, probs = _rand_case(k=1)
+    y1 = orc.expert_forward(x, wg, wu, wd, ids, np.ones_like(probs), rounding=False)
+    y2 = orc.expert_forward(x, wg, wu, wd, ids, probs, rounding=False)
+    np.testing.assert_allclose(y2, probs * y1, rtol=1e-12, atol=1e-14)
+
+
+def test_microbatch_split_forward_equal():
+    x, wg, wu, wd, ids, probs = _rand_case(T=64, k=2)
+    y = orc.expert_forward(x, wg, wu, wd, ids, probs)
+    for s in (1, 2, 4, 8):
+        ys = orc.microbatched_forward(x, wg, wu, wd, ids, probs, s)
+        np.testing.assert_allclose(ys, y, rtol=2 ** -7, atol=1e-6)
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(dy, *a):
+    return float(np.sum(dy * orc.expert_forward(*a, rounding=False)))
+
+
+def test_backward_finite_differences():
+    x, wg, wu, wd, ids, probs = _rand_case(T=6, H=5, F=7, E=3, k=2, empty=(), wstd=0.7)
+    rng = np.random.default_rng(13)
+    dy = rng.standard_normal(x.shape)
+    g = orc.expert_backward(dy, x, wg, wu, wd, ids, probs, rounding=False)
+    eps = 1e-6
+
+    def fd(arr, idx, build):
+        a1 = arr.copy(); a1[idx] += eps
+        a2 = arr.copy(); a2[idx] -= eps
+        return (_loss(dy, *build(a1)) - _loss(dy, *build(a2))) / (2 * eps)
+
+    checks = [
+        ("dx", x, lambda a: (a, wg, wu, wd, ids, probs)),
+        ("dw_gate", wg, lambda a: (x, a, wu, wd, ids, probs)),
+        ("dw_up", wu, lambda a: (x, wg, a, wd, ids, probs)),
+        ("dw_down", wd, lambda a: (x, wg, wu, a, ids, probs)),
+        ("dprobs", probs, lambda a: (x, wg, wu, wd, ids, a)),
+    ]
+    for name, arr, build in checks:
+        for idx in np.ndindex(arr.shape):
+            want = fd(arr, idx, build)
+            assert abs(g[name][idx] - want) <= 1e-6 * (1 + abs(want)), (name, idx, g[name][idx], want)
+
+
+def test_backward_matches_torch_autograd():
+    x, wg, wu, wd, ids, probs = _rand_case(T=11, H=8, F=12, E=4, k=2, empty=(2,), wstd=0.5)
+    dy = np.random.default_rng(14).standard_normal(x.shape)
+    g = orc.expert_backward(dy, x, wg, wu, wd, ids, probs, rounding=False)
+    tx, tg, tu, td, tp = (torch.tensor(a, requires_grad=True) for a in (x, wg, wu, wd, probs))
+    y = torch.zeros_like(tx)
+    for t in range(x.shape[0]):
+        for j in range(ids.shape[1]):
+            e = int(ids[t, j])
+            hh = torch.nn.functional.silu(tx[t] @ tg[e]) * (tx[t] @ tu[e])
+            y = y.index_add(0, torch.tensor([t]), (tp[t, j] * (hh @ td[e]))[None])
+    (y * torch.from_numpy(dy)).sum().backward()
+    for name, tt in (("dx", tx), ("dw_gate", tg), ("dw_up", tu), ("dw_down", td), ("dprobs", tp)):
+        np.testing.assert_allclose(g[name], tt.grad.numpy(), rtol=1e-10, atol=1e-12, err_msg=name)
+
+
+def test_backward_sampled_helpers_agree():
+    x, wg, wu, wd, ids, probs = _rand_case(T=20, H=16, F=24, E=4, k=2, empty=(1,), wstd=0.3)
+    dy = orc.bf16(np.random.default_rng(15).standard_normal(x.shape))
+    g = orc.expert_backward(dy, x, wg, wu, wd, ids, probs)
+    toks = [0, 3, 7, 19]
+    dx, dp = orc.backward_rows(dy, x, wg, wu, wd, ids, probs, toks)
+    np.testing.assert_allclose(dx, g["dx"][toks], rtol=2 ** -7, atol=1e-9)
+    np.testing.assert_allclose(dp, g["dprobs"][toks], rtol=1e-9, atol=1e-12)
+    for e in (0, 2):
+        c = orc.weight_grad_columns(dy, x, wg, wu, wd, ids, probs, e, [1, 5], [0, 9])
+        np.testing.assert_allclose(c["dw_gate"], g["dw_gate"][e][:, [1, 5]], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(c["dw_up"], g["dw_up"][e][:, [1, 5]], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(c["dw_down"], g["dw_down"][e][:, [0, 9]], rtol=1e-9, atol=1e-12)
+    assert np.all(g["dw_gate"][1] == 0) and np.all(g["dw_down"][1] == 0)
+
+
+def test_microbatch_split_backward():
+    x, wg, wu, wd, ids, probs = _rand_case(T=32, H=16, F=24, E=4, k=2, empty=(), wstd=0.3)
+    dy = orc.bf16(np.random.default_rng(16).standard_normal(x.shape))
+    g = orc.expert_backward(dy, x, wg, wu, wd, ids, probs)
+    for s in (1, 4, 8):
+        gs = orc.microbatched_backward(dy, x, wg, wu, wd, ids, probs, s)
+        np.testing.assert_allclose(gs["dx"], g["dx"], rtol=2 ** -7, atol=1e-9)
+        np.testing.assert_allclose(gs["dprobs"], g["dprobs"], rtol=1e-9, atol=1e-12)
+        for key in ("dw_gate", "dw_up", "dw_down"):
+            np.testing.assert_allclose(gs[key], g[key], rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------- MXFP8 forward
+
+def test_mxfp8_grouped_equals_per_token():
+    rng = np.random.default_rng(17)
+    T, H, F, E, k = 24, 64, 96, 5, 3
+    x = orc.bf16(rng.standard_normal((T, H)))
+    wg = orc.bf16(rng.standard_normal((E, F, H)) * 0.1)
+    wu = orc.bf16(rng.standard_normal((E, F, H)) * 0.1)
+    wd = orc.bf16(rng.standard_normal((E, H, F)) * 0.1)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    probs = rng.dirichlet(np.ones(k), T)
+    xq, xs = orc.quantize_mxfp8(x)
+    qg = [orc.quantize_mxfp8(wg[e]) for e in range(E)]
+    qu = [orc.quantize_mxfp8(wu[e]) for e in range(E)]
+    qd = [orc.quantize_mxfp8(wd[e]) for e in range(E)]
+    y1 = orc.expert_forward_mxfp8(xq, xs, qg, qu, qd, ids, probs, E)
+    y2 = np.stack([orc.token_forward_mxfp8(xq[t], xs[t], qg, qu, qd, ids[t], probs[t]) for t in range(T)])
+    np.testing.assert_allclose(y1, y2, rtol=2 ** -6, atol=1e-6)
+    # against the unquantised block: MXFP8 is an approximation of it
+    wgt = np.transpose(wg, (0, 2, 1)); wut = np.transpose(wu, (0, 2, 1)); wdt = np.transpose(wd, (0, 2, 1))
+    yb = orc.expert_forward(x, wgt, wut, wdt, ids, probs)
+    assert np.max(np.abs(y1 - yb)) <= 0.1 * np.max(np.abs(yb))
