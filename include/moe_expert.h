@@ -1,0 +1,240 @@
+/*
+ * moe_expert.h - C ABI of the GB300 MoE expert-block library
+ * (libmoe_gb300.so, built from moe_expert_dispatch_gb300/csrc).
+ *
+ * The library computes, on one GPU, the expert block of an MoE layer as the
+ * ep_mc2_forward data flow of "NPU Training Operators - MC2" (section
+ * "execution path", steps 2-10) states it: per-expert token counts (histc),
+ * the offset scan, the stable permute of routed rows into expert-contiguous
+ * order, grouped GEMM fc1 (gate and up) with a SwiGLU epilogue, grouped GEMM
+ * fc2 and the probability-weighted unpermute; plus the backward of the same
+ * block and an MXFP8 variant of the forward. On one GPU the two AllToAllv of
+ * the MC2 fusion collapse into the permute gather and the unpermute gather.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers are DEVICE pointers unless stated otherwise, owned by the
+ *    caller, and at least 16-byte aligned (the grouped GEMMs read them with
+ *    TMA). The library allocates no device memory: scratch space comes from
+ *    a caller-provided workspace whose size the *_workspace_size calls give.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t passed as void*,
+ *    NULL = the legacy default stream) and never synchronises the host.
+ *  - Matrices are row-major. bf16 is IEEE-style bfloat16 (2 bytes). Rounding
+ *    to bf16 is round-to-nearest-even.
+ *  - Host-detectable errors (null pointer, bad size, small workspace,
+ *    unsupported shape) return a status immediately and launch nothing.
+ *    Errors found on the device (an expert id outside [0, E), an in-kernel
+ *    wait that ran out of time) set a device error word and the affected work
+ *    stops early; moe_get_error() reports them. Nothing traps.
+ *  - T = 0 (no tokens) is valid and launches nothing.
+ */
+#ifndef MOE_EXPERT_H
+#define MOE_EXPERT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, k > E, ...            */
+  MOE_ERR_UNSUPPORTED = 2,   /* a shape the kernels do not handle (H, F % 128)      */
+  MOE_ERR_BAD_EXPERT_ID = 3, /* device: an expert id outside [0, E)                 */
+  MOE_ERR_WORKSPACE = 4,     /* workspace pointer null or smaller than required     */
+  MOE_ERR_TIMEOUT = 5,       /* device: an in-kernel pipeline wait hit its limit    */
+  MOE_ERR_CUDA = 6           /* a CUDA runtime call failed (launch, attribute, ...) */
+} moe_status;
+
+typedef enum moe_precision { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
+
+/* Tuning and debug knobs of the fused path. moe_config_init() fills the
+ * defaults; a NULL config pointer means the defaults. */
+typedef struct moe_config {
+  int ring_stages;         /* depth of the shared-memory ring that feeds the tensor
+                              cores, 1..4 (default 4; 1 = no overlap, the serial
+                              baseline of the "tileCnt = 1" knob in "MC2 通算融合架构总览"
+                              section 6)                                              */
+  int save_for_backward;   /* forward keeps Xp, A_g, A_u, h and O in its workspace
+                              and zero-fills the padding rows (default 0)              */
+  int num_sms;             /* persistent grid size of the grouped GEMMs; 0 = all SMs   */
+  int fuse_gather;         /* 1: fc1 gathers routed rows of x itself instead of reading
+                              a materialised permuted copy (default 0)                  */
+  long long wait_limit_ns; /* bound of every in-kernel wait (default 0 = 2 s)           */
+  void** step_events;      /* optional: array of MOE_STEP_EVENTS cudaEvent_t (as void*),
+                              recorded on `stream` before the first step and after each
+                              step of moe_expert_forward: routing (counts, row map,
+                              permute), fc1+SwiGLU, fc2, unpermute. NULL = none.      */
+} moe_config;
+
+#define MOE_STEP_EVENTS 5
+
+void moe_config_init(moe_config* cfg);
+
+/* Readable name of a status. Never NULL. */
+const char* moe_status_string(moe_status s);
+
+/* Synchronises `stream`, then returns and clears the device error word
+ * (MOE_OK when no kernel reported an error). The word is per device and is
+ * shared by every stream, so concurrent users see each other's errors. */
+moe_status moe_get_error(void* stream);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int moe_num_sms(void);
+
+/* ------------------------------------------------------------------------
+ * moe_counts - per-expert token counts and the offset scan.
+ * Follows steps 2 and 4-5 of ep_mc2_forward ("NPU Training Operators - MC2",
+ * section "execution path"): torch.histc(selected_experts, bins=E, min=0,
+ * max=E), with send_counts = recv_counts = the local counts on one GPU.
+ *
+ *  expert_ids  int32 [n_ids]   flattened [T, k] routing ids (t-major)
+ *  counts      int32 [E]       out: c_e = #{i : expert_ids[i] == e}
+ *  offsets     int32 [E + 1]   out: offsets[0] = 0, offsets[e+1] = offsets[e] + c_e
+ *  workspace   >= moe_counts_workspace_size(n_ids, E) bytes of scratch
+ *              (per-chunk histograms); every call overwrites all of it, so
+ *              nothing needs clearing and one workspace may serve every call
+ *              on a stream.
+ * Ids outside [0, E) are not counted and raise MOE_ERR_BAD_EXPERT_ID on the
+ * device. Requires 1 <= E <= 1024 and n_ids < 2^31.
+ * ------------------------------------------------------------------------ */
+size_t moe_counts_workspace_size(int64_t n_ids, int E);
+moe_status moe_counts(const int32_t* expert_ids, int64_t n_ids, int E, int32_t* counts,
+                      int32_t* offsets, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_permute - gather routed rows into expert-contiguous order.
+ * Step 6 of ep_mc2_forward, permute(hidden_states, selected_experts): on one
+ * GPU this is also the dispatch AllToAllv of all2all_grouped_matmul.
+ * Rows of one expert keep the order of their flat slot index t*k + j.
+ *
+ *  x           [T, row_bytes]  token rows (any element type; row_bytes % 16 == 0)
+ *  expert_ids  int32 [T, k]    routing ids
+ *  probs       float [T, k]    routing weights, or NULL
+ *  row_align   1 = dense rows (row of slot = offsets[e] + rank); 128 = each
+ *              expert's segment starts at a multiple of 128 rows (the layout
+ *              the grouped GEMMs tile), padding rows are left untouched
+ *  x_perm      [R_cap, row_bytes] out: permuted rows, R_cap = T*k for
+ *              row_align 1, else moe_padded_rows(T*k, E, row_align)
+ *  row_of      int32 [T, k]    out: row of slot (t, j)
+ *  token_of    int32 [R_cap]   out: token of each row (padding rows untouched)
+ *  prob_of     float [R_cap]   out: probs[t, j] of each row (may be NULL)
+ *  offsets     int32 [E + 1]   out: first row of each expert (aligned when
+ *              row_align > 1; offsets[E] is then the padded row total)
+ *  counts      int32 [E]       out: c_e
+ * ------------------------------------------------------------------------ */
+int64_t moe_padded_rows(int64_t n_rows, int E, int row_align);
+size_t moe_permute_workspace_size(int64_t T, int k, int E);
+moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_t* expert_ids,
+                       const float* probs, int k, int E, int row_align, void* x_perm,
+                       int32_t* row_of, int32_t* token_of, float* prob_of, int32_t* offsets,
+                       int32_t* counts, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_unpermute - probability-weighted combine back to token order.
+ * Step 10 of ep_mc2_forward, unpermute(hidden_states, unpermute_indices,
+ * probs=routing_weights); on one GPU also the combine AllToAllv of
+ * grouped_matmul_all2all.
+ *   y[t] = bf16( sum_{j<k} probs[t, j] * o_perm[row_of[t, j]] ), j in order,
+ * accumulated in float. probs NULL means 1. Rows < 0 contribute nothing.
+ *  o_perm  bf16 [*, H]    y  bf16 [T, H]    H % 8 == 0
+ * ------------------------------------------------------------------------ */
+moe_status moe_unpermute(const void* o_perm, const int32_t* row_of, const float* probs, int64_t T,
+                         int k, int H, void* y, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_quantize_mxfp8 - MXFP8 quantisation of bf16 rows.
+ * The quantised AllToAll+Matmul of "MC2 通算融合架构总览" (section 1; scales
+ * in a buffer of their own, section 5), in the OCP Microscaling (MX) v1.0
+ * form: per 32 consecutive elements of a row, the shared scale
+ * X = 2^(floor(log2(amax)) - 8) as an E8M0 code (exponent + 127, clamped to
+ * [0, 254]; an all-zero block gets code 0), and each element E4M3(v / X),
+ * round-to-nearest-even, saturating at +-448.
+ *  in      bf16 [rows, K]   q  uint8 [rows, K]   scales  uint8 [rows, K/32]
+ *  K % 32 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, uint8_t* scales,
+                              void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_forward - the whole block in one call:
+ *   y = unpermute(fc2(swiglu(fc1(permute(x)))), probs)
+ * with, per expert e over its rows, A_g = Xp_e W1g_e, A_u = Xp_e W1u_e
+ * (float accumulation), h = bf16(silu(A_g) * A_u), O = bf16(h_e W2_e).
+ * The argument order follows torch_npu.npu.mc2_fused_expert of the MC2 for
+ * MoE All-to-All article (section "usage"), without its communication
+ * group, plus the routing weights of unpermute.
+ *
+ *  x        bf16 [T, H]
+ *  w_gate   bf16 [E, H, F]   (N contiguous, as the pages' weights_gate)
+ *  w_up     bf16 [E, H, F]
+ *  w_down   bf16 [E, F, H]
+ *  expert_ids int32 [T, k],  probs float [T, k]
+ *  y        bf16 [T, H]      out
+ *  workspace >= moe_workspace_size(T, H, F, E, k, cfg, 0) bytes. With
+ *           cfg->save_for_backward the workspace afterwards holds what
+ *           moe_expert_backward needs; keep it unchanged until then.
+ * Requires H % 128 == 0, F % 128 == 0, 1 <= k <= E <= 1024.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_config* cfg,
+                          int for_backward);
+moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_up,
+                              const void* w_down, const int32_t* expert_ids, const float* probs,
+                              int64_t T, int H, int F, int E, int k, void* y, void* workspace,
+                              size_t ws_bytes, const moe_config* cfg, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_backward - gradients of moe_expert_forward.
+ * The autograd Functions AllToAllGroupedMatmul / GroupedMatmulAllToAll of
+ * "NPU Training Operators - MC2" (section "PR changes") wrap forward and
+ * backward; its section "validation items" compares the fc1/fc2 gradients.
+ *   dO_r  = bf16(p_r dY_t(r));          dprobs[t,j] = <dY_t, O_row(t,j)>
+ *   dH    = dO_e W2_e^T (float);        dA_g = bf16(dH A_u silu'(A_g)),
+ *   dA_u  = bf16(dH silu(A_g));         dXp = bf16(dA_g W1g_e^T + dA_u W1u_e^T)
+ *   dW2_e = h_e^T dO_e, dW1g_e = Xp_e^T dA_g, dW1u_e = Xp_e^T dA_u (float)
+ *   dX_t  = bf16(sum_j dXp[row_of[t, j]])
+ * A_g and A_u enter as saved by the forward (bf16).
+ *
+ *  dy          bf16 [T, H]
+ *  fwd_ws      the workspace of a forward call made with save_for_backward=1
+ *              on the same inputs
+ *  dx          bf16 [T, H]         out
+ *  dw_gate     float [E, H, F]     out (accumulated into when accumulate_dw)
+ *  dw_up       float [E, H, F]     out
+ *  dw_down     float [E, F, H]     out
+ *  dprobs      float [T, k]        out
+ *  workspace   >= moe_workspace_size(T, H, F, E, k, cfg, 1) bytes
+ * Experts that receive no token get dW = 0 (or are left as they were when
+ * accumulate_dw).
+ * ------------------------------------------------------------------------ */
+moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate, const void* w_up,
+                               const void* w_down, const int32_t* expert_ids, const float* probs,
+                               int64_t T, int H, int F, int E, int k, const void* fwd_ws,
+                               size_t fwd_ws_bytes, void* dx, float* dw_gate, float* dw_up,
+                               float* dw_down, float* dprobs, int accumulate_dw, void* workspace,
+                               size_t ws_bytes, const moe_config* cfg, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_forward_mxfp8 - the block with MXFP8 operands.
+ * x arrives in bf16 and is quantised on the fly (per 32 along H) while it is
+ * permuted; the weights arrive already quantised (moe_quantize_mxfp8) in a
+ * K-contiguous layout so that each 32-block lies along the reduction:
+ *  wg_q, wu_q  uint8 [E, F, H], wg_s, wu_s  uint8 [E, F, H/32]
+ *  wd_q        uint8 [E, H, F], wd_s        uint8 [E, H, F/32]
+ * fc1 accumulates in float, h = bf16(silu(A_g) A_u) is quantised per 32
+ * along F for fc2, O = bf16(fc2) and y = bf16(combine), as in BF16 mode.
+ * Requires H % 128 == 0, F % 128 == 0.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_size_mxfp8(int64_t T, int H, int F, int E, int k, const moe_config* cfg);
+moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
+                                    const uint8_t* wu_q, const uint8_t* wu_s, const uint8_t* wd_q,
+                                    const uint8_t* wd_s, const int32_t* expert_ids,
+                                    const float* probs, int64_t T, int H, int F, int E, int k,
+                                    void* y, void* workspace, size_t ws_bytes,
+                                    const moe_config* cfg, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_EXPERT_H */

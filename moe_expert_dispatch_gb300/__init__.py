@@ -1,0 +1,289 @@
+"""GB300 MoE expert block: thin Python binding of libmoe_gb300.so.
+
+Every function here marshals torch tensors (device memory) and the current
+CUDA stream into the C ABI of include/moe_expert.h and raises on a non-OK
+status. All computation runs in the library's CUDA kernels; there is no
+fallback: importing this package without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m moe_expert_dispatch_gb300.build` "
+        "(the expert block has no CPU or eager fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MOE_OK = 0
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "expert id outside [0, E)",
+          4: "workspace missing or too small", 5: "in-kernel wait timed out", 6: "CUDA error"}
+MOE_BF16, MOE_MXFP8 = 0, 1
+TILE_M = 128
+
+_vp, _i64, _i32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+
+
+class moe_config(ctypes.Structure):
+    _fields_ = [("ring_stages", ctypes.c_int), ("save_for_backward", ctypes.c_int),
+                ("num_sms", ctypes.c_int), ("fuse_gather", ctypes.c_int),
+                ("wait_limit_ns", ctypes.c_longlong),
+                ("step_events", ctypes.POINTER(ctypes.c_void_p))]
+
+STEP_EVENTS = 5   # routing, fc1+SwiGLU, fc2, unpermute: MOE_STEP_EVENTS boundaries
+
+
+def _sig(name, res, *args):
+    f = getattr(_lib, name)
+    f.restype = res
+    f.argtypes = list(args)
+    return f
+
+
+_sig("moe_config_init", None, ctypes.POINTER(moe_config))
+_sig("moe_status_string", ctypes.c_char_p, _i32)
+_sig("moe_get_error", _i32, _vp)
+_sig("moe_num_sms", _i32)
+_sig("moe_padded_rows", _i64, _i64, _i32, _i32)
+_sig("moe_counts_workspace_size", _sz, _i64, _i32)
+_sig("moe_counts", _i32, _vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp)
+_sig("moe_permute_workspace_size", _sz, _i64, _i32, _i32)
+_sig("moe_permute", _i32, _vp, _i64, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
+     _vp, _vp, _sz, _vp)
+_sig("moe_unpermute", _i32, _vp, _vp, _vp, _i64, _i32, _i32, _vp, _vp)
+_sig("moe_quantize_mxfp8", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
+_sig("moe_workspace_size", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config), _i32)
+_sig("moe_expert_forward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp,
+     _vp, _sz, ctypes.POINTER(moe_config), _vp)
+_sig("moe_expert_backward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+     _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, ctypes.POINTER(moe_config), _vp)
+_sig("moe_workspace_size_mxfp8", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config))
+_sig("moe_expert_forward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32,
+     _i32, _i32, _i32, _vp, _vp, _sz, ctypes.POINTER(moe_config), _vp)
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+def _check(status: int, where: str):
+    if status != MOE_OK:
+        raise MoeError(status, where)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cuda(t, name, dtype=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def config(ring_stages=4, save_for_backward=False, num_sms=0, fuse_gather=False,
+           wait_limit_ns=0, step_events=None) -> moe_config:
+    """A moe_config; step_events: optional list of MOE_STEP_EVENTS torch.cuda.Event
+    (already recorded once, so that their CUDA events exist)."""
+    c = moe_config()
+    _lib.moe_config_init(ctypes.byref(c))
+    c.ring_stages = ring_stages
+    c.save_for_backward = int(bool(save_for_backward))
+    c.num_sms = num_sms
+    c.fuse_gather = int(bool(fuse_gather))
+    if wait_limit_ns:
+        c.wait_limit_ns = wait_limit_ns
+    if step_events is not None:
+        assert len(step_events) == STEP_EVENTS
+        arr = (ctypes.c_void_p * STEP_EVENTS)(*[ev.cuda_event for ev in step_events])
+        c._events_keepalive = arr
+        c.step_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    return c
+
+
+def moe_get_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error status."""
+    return _lib.moe_get_error(_stream(stream))
+
+
+def moe_num_sms() -> int:
+    return _lib.moe_num_sms()
+
+
+def moe_padded_rows(n_rows: int, E: int, row_align: int = TILE_M) -> int:
+    return _lib.moe_padded_rows(n_rows, E, row_align)
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def moe_counts(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=None,
+               workspace=None, stream=None):
+    """(counts int32 [E], offsets int32 [E+1]) of the flattened ids."""
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    dev = expert_ids.device
+    n = expert_ids.numel()
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+               if offsets is None else offsets)
+    need = _lib.moe_counts_workspace_size(n, num_experts)
+    ws = _workspace(need, dev) if workspace is None else workspace
+    _check(_lib.moe_counts(_p(expert_ids), n, num_experts, _p(counts), _p(offsets), _p(ws),
+                           ws.numel(), _stream(stream)), "moe_counts")
+    return counts, offsets
+
+
+def moe_permute(x: torch.Tensor, expert_ids: torch.Tensor, probs, num_experts: int,
+                row_align: int = 1, stream=None):
+    """Stable permute of token rows into expert-contiguous rows.
+
+    Returns dict(x_perm, row_of, token_of, prob_of, offsets, counts). With
+    row_align > 1 every expert segment starts at a multiple of row_align rows
+    and the padding rows of x_perm/token_of/prob_of are left uninitialised.
+    """
+    _cuda(x, "x")
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    T, k = expert_ids.shape
+    dev = x.device
+    row_bytes = x[0].numel() * x.element_size() if T else x.element_size()
+    cap = _lib.moe_padded_rows(T * k, num_experts, row_align)
+    out = dict(
+        x_perm=torch.empty((cap,) + tuple(x.shape[1:]), dtype=x.dtype, device=dev),
+        row_of=torch.empty((T, k), dtype=torch.int32, device=dev),
+        token_of=torch.empty(cap, dtype=torch.int32, device=dev),
+        prob_of=torch.empty(cap, dtype=torch.float32, device=dev),
+        offsets=torch.empty(num_experts + 1, dtype=torch.int32, device=dev),
+        counts=torch.empty(num_experts, dtype=torch.int32, device=dev),
+    )
+    ws = _workspace(_lib.moe_permute_workspace_size(T, k, num_experts), dev)
+    _check(_lib.moe_permute(_p(x), T, row_bytes, _p(expert_ids), _p(probs), k, num_experts,
+                            row_align, _p(out["x_perm"]), _p(out["row_of"]), _p(out["token_of"]),
+                            _p(out["prob_of"]), _p(out["offsets"]), _p(out["counts"]), _p(ws),
+                            ws.numel(), _stream(stream)), "moe_permute")
+    return out
+
+
+def moe_unpermute(o_perm: torch.Tensor, row_of: torch.Tensor, probs=None, y=None, stream=None):
+    """y[t] = bf16(sum_j probs[t, j] * o_perm[row_of[t, j]])."""
+    _cuda(o_perm, "o_perm", torch.bfloat16)
+    _cuda(row_of, "row_of", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    T, k = row_of.shape
+    H = o_perm.shape[-1]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=o_perm.device) if y is None else y
+    _check(_lib.moe_unpermute(_p(o_perm), _p(row_of), _p(probs), T, k, H, _p(y), _stream(stream)),
+           "moe_unpermute")
+    return y
+
+
+def moe_quantize_mxfp8(a: torch.Tensor, stream=None):
+    """(codes uint8 [..., K], scales uint8 [..., K/32]) of a bf16 tensor along its last axis."""
+    _cuda(a, "a", torch.bfloat16)
+    K = a.shape[-1]
+    rows = a.numel() // K if K else 0
+    q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
+    s = torch.empty(a.shape[:-1] + (K // 32,), dtype=torch.uint8, device=a.device)
+    _check(_lib.moe_quantize_mxfp8(_p(a), rows, K, _p(q), _p(s), _stream(stream)),
+           "moe_quantize_mxfp8")
+    return q, s
+
+
+def moe_workspace_size(T, H, F, E, k, cfg: moe_config | None = None, for_backward=False) -> int:
+    c = cfg if cfg is not None else config()
+    return _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), int(for_backward))
+
+
+def moe_expert_forward(x, w_gate, w_up, w_down, expert_ids, probs, y=None, workspace=None,
+                       cfg: moe_config | None = None, stream=None):
+    """y = the MoE expert block (counts, permute, fc1+SwiGLU, fc2, unpermute).
+
+    Returns (y, workspace); with cfg.save_for_backward the workspace holds
+    what moe_expert_backward needs."""
+    for t, n in ((x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    T, H = x.shape
+    E, _, F = w_gate.shape
+    k = expert_ids.shape[1]
+    c = cfg if cfg is not None else config()
+    need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 0)
+    if need == 0 and T > 0:
+        raise MoeError(1, "moe_workspace_size")
+    ws = _workspace(need, x.device) if workspace is None else workspace
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(_lib.moe_expert_forward(_p(x), _p(w_gate), _p(w_up), _p(w_down), _p(expert_ids),
+                                   _p(probs), T, H, F, E, k, _p(y), _p(ws), ws.numel(),
+                                   ctypes.byref(c), _stream(stream)), "moe_expert_forward")
+    return y, ws
+
+
+def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_workspace,
+                        dx=None, dw_gate=None, dw_up=None, dw_down=None, dprobs=None,
+                        accumulate_dw=False, workspace=None, cfg: moe_config | None = None,
+                        stream=None):
+    """Gradients (dx, dw_gate, dw_up, dw_down, dprobs) of moe_expert_forward."""
+    for t, n in ((dy, "dy"), (x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _cuda(t, n, torch.bfloat16)
+    T, H = x.shape
+    E, _, F = w_gate.shape
+    k = expert_ids.shape[1]
+    dev = x.device
+    c = cfg if cfg is not None else config(save_for_backward=True)
+    dx = torch.empty_like(x) if dx is None else dx
+    dw_gate = torch.empty((E, H, F), dtype=torch.float32, device=dev) if dw_gate is None else dw_gate
+    dw_up = torch.empty((E, H, F), dtype=torch.float32, device=dev) if dw_up is None else dw_up
+    dw_down = torch.empty((E, F, H), dtype=torch.float32, device=dev) if dw_down is None else dw_down
+    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
+    need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 1)
+    ws = _workspace(need, dev) if workspace is None else workspace
+    _check(_lib.moe_expert_backward(_p(dy), _p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                    _p(expert_ids), _p(probs), T, H, F, E, k, _p(fwd_workspace),
+                                    fwd_workspace.numel(), _p(dx), _p(dw_gate), _p(dw_up),
+                                    _p(dw_down), _p(dprobs), int(bool(accumulate_dw)), _p(ws),
+                                    ws.numel(), ctypes.byref(c), _stream(stream)),
+           "moe_expert_backward")
+    return dict(dx=dx, dw_gate=dw_gate, dw_up=dw_up, dw_down=dw_down, dprobs=dprobs)
+
+
+def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, probs, y=None,
+                             workspace=None, cfg: moe_config | None = None, stream=None):
+    """The block with MXFP8 operands (x quantised on the fly; weights pre-quantised,
+    K-contiguous: wg/wu [E, F, H], wd [E, H, F], scales [..., K/32])."""
+    _cuda(x, "x", torch.bfloat16)
+    for t, n in ((wg_q, "wg_q"), (wg_s, "wg_s"), (wu_q, "wu_q"), (wu_s, "wu_s"), (wd_q, "wd_q"),
+                 (wd_s, "wd_s")):
+        _cuda(t, n, torch.uint8)
+    T, H = x.shape
+    E, F, _ = wg_q.shape
+    k = expert_ids.shape[1]
+    c = cfg if cfg is not None else config()
+    need = _lib.moe_workspace_size_mxfp8(T, H, F, E, k, ctypes.byref(c))
+    ws = _workspace(need, x.device) if workspace is None else workspace
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _check(_lib.moe_expert_forward_mxfp8(_p(x), _p(wg_q), _p(wg_s), _p(wu_q), _p(wu_s), _p(wd_q),
+                                         _p(wd_s), _p(expert_ids), _p(probs), T, H, F, E, k,
+                                         _p(y), _p(ws), ws.numel(), ctypes.byref(c),
+                                         _stream(stream)), "moe_expert_forward_mxfp8")
+    return y, ws

@@ -1,0 +1,375 @@
+// capi.cu - the extern "C" entry points of include/moe_expert.h: argument
+// checks, workspace layout, tensor-map encoding and the launch sequence of
+// each call. No device memory is allocated here; every call is asynchronous.
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// The device error word (one per device that loads the library). Kernels
+// OR error bits into it; moe_get_error() reads and clears it.
+__device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int d = 0;
+  cudaGetDevice(&d);
+  return d;
+}
+
+int* error_word() {
+  static int* ptrs[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  if (!ptrs[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    ptrs[d] = static_cast<int*>(p);
+  }
+  return ptrs[d];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+size_t up256(size_t b) { return (b + 255) / 256 * 256; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Forward workspace: byte offsets of every buffer.
+struct FwdLayout {
+  int64_t R, cap;
+  size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xp, h, o, ag, au, total;
+};
+
+FwdLayout fwd_layout(int64_t T, int H, int F, int E, int k, bool save) {
+  FwdLayout L;
+  L.R = T * k;
+  L.cap = moe_padded_rows(L.R, E, kTileM);
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = cur;
+    cur += up256(bytes);
+    return at;
+  };
+  L.route = take(route_scratch_bytes(L.R, E));
+  L.counts = take(E * sizeof(int32_t));
+  L.offsets = take((E + 1) * sizeof(int32_t));
+  L.off_al = take((E + 1) * sizeof(int32_t));
+  L.row_of = take(L.R * sizeof(int32_t));
+  L.token_of = take(L.cap * sizeof(int32_t));
+  L.prob_of = take(L.cap * sizeof(float));
+  L.xp = take(static_cast<size_t>(L.cap) * H * 2);
+  L.h = take(static_cast<size_t>(L.cap) * F * 2);
+  L.o = take(static_cast<size_t>(L.cap) * H * 2);
+  L.ag = save ? take(static_cast<size_t>(L.cap) * F * 2) : 0;
+  L.au = save ? take(static_cast<size_t>(L.cap) * F * 2) : 0;
+  L.total = cur;
+  return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+moe_config cfg_or_default(const moe_config* c) {
+  moe_config d;
+  moe_config_init(&d);
+  if (!c) return d;
+  d = *c;
+  if (d.ring_stages < 1 || d.ring_stages > 4) d.ring_stages = 4;
+  if (d.wait_limit_ns <= 0) d.wait_limit_ns = static_cast<long long>(kDefaultWaitNs);
+  return d;
+}
+
+moe_status check_block_args(int64_t T, int H, int F, int E, int k) {
+  if (T < 0 || H <= 0 || F <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK)
+    return MOE_ERR_INVALID_ARG;
+  if (T * static_cast<int64_t>(k) >= (static_cast<int64_t>(1) << 31) - kTileM * kMaxExperts)
+    return MOE_ERR_INVALID_ARG;
+  if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int grid_size(const moe_config& c) {
+  const int sms = device_sm_count();
+  return (c.num_sms > 0 && c.num_sms < sms) ? c.num_sms : sms;
+}
+
+}  // namespace
+
+int device_sm_count() {
+  static int counts[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 1;
+  if (!counts[d]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    counts[d] = n > 0 ? n : 1;
+  }
+  return counts[d];
+}
+
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+void moe_config_init(moe_config* cfg) {
+  if (!cfg) return;
+  memset(cfg, 0, sizeof(*cfg));
+  cfg->ring_stages = 4;
+  cfg->wait_limit_ns = static_cast<long long>(kDefaultWaitNs);
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id outside [0, E)";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case MOE_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+moe_status moe_get_error(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (v && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v & kErrBadId) return MOE_ERR_BAD_EXPERT_ID;
+  if (v & kErrTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+int moe_num_sms(void) { return device_sm_count(); }
+
+int64_t moe_padded_rows(int64_t n_rows, int E, int row_align) {
+  if (row_align <= 1) return n_rows;
+  const int64_t worst = n_rows + static_cast<int64_t>(E) * (row_align - 1);
+  return (worst + row_align - 1) / row_align * row_align;
+}
+
+size_t moe_counts_workspace_size(int64_t n_ids, int E) {
+  if (n_ids < 0 || E < 1) return 0;
+  return route_scratch_bytes(n_ids, E);
+}
+
+moe_status moe_counts(const int32_t* ids, int64_t n_ids, int E, int32_t* counts, int32_t* offsets,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  if (n_ids < 0 || E < 1 || E > kMaxExperts || n_ids >= (static_cast<int64_t>(1) << 31))
+    return MOE_ERR_INVALID_ARG;
+  if ((n_ids > 0 && !ids) || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < route_scratch_bytes(n_ids, E)) return MOE_ERR_WORKSPACE;
+  RouteScratch s = route_scratch(workspace, n_ids, E);
+  return from_cuda(launch_counts(ids, n_ids, E, 1, counts, offsets, nullptr, s, error_word(),
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_permute_workspace_size(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return route_scratch_bytes(T * k, E);
+}
+
+moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_t* ids,
+                       const float* probs, int k, int E, int row_align, void* x_perm,
+                       int32_t* row_of, int32_t* token_of, float* prob_of, int32_t* offsets,
+                       int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || k > E || E > kMaxExperts || row_bytes <= 0 ||
+      row_bytes % 16 != 0 || row_align < 1 || T * k >= (static_cast<int64_t>(1) << 31))
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !ids || !x_perm || !row_of || !token_of || !offsets || !counts)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < route_scratch_bytes(T * k, E)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RouteScratch s = route_scratch(workspace, T * k, E);
+  int* err = error_word();
+  // dense offsets are wanted when row_align == 1; otherwise the padded ones
+  cudaError_t e;
+  if (row_align == 1)
+    e = launch_counts(ids, T * k, E, 1, counts, offsets, nullptr, s, err, st);
+  else
+    e = launch_counts(ids, T * k, E, row_align, counts, nullptr, offsets, s, err, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = launch_rowmap(ids, probs, T * k, k, E, s, row_of, token_of, prob_of, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return from_cuda(launch_permute_copy(x, T, row_bytes, k, row_of, x_perm, st));
+}
+
+moe_status moe_unpermute(const void* o_perm, const int32_t* row_of, const float* probs, int64_t T,
+                         int k, int H, void* y, void* stream) {
+  if (T < 0 || k < 1 || k > kMaxTopK || H <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!o_perm || !row_of || !y || !aligned16(o_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_unpermute(static_cast<const __nv_bfloat16*>(o_perm), row_of, probs, T, k,
+                                    H, static_cast<__nv_bfloat16*>(y),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, uint8_t* scales,
+                              void* stream) {
+  if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!in || !q || !scales || !aligned16(in) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_mxfp8(static_cast<const __nv_bfloat16*>(in), rows, K, q, scales,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_config* cfg,
+                          int for_backward) {
+  if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;
+  const moe_config c = cfg_or_default(cfg);
+  if (for_backward) return 0;  // the backward workspace is added with the backward kernels
+  return fwd_layout(T, H, F, E, k, c.save_for_backward != 0).total;
+}
+
+moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_up,
+                              const void* w_down, const int32_t* expert_ids, const float* probs,
+                              int64_t T, int H, int F, int E, int k, void* y, void* workspace,
+                              size_t ws_bytes, const moe_config* cfg, void* stream) {
+  moe_status s = check_block_args(T, H, F, E, k);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_gate || !w_up || !w_down || !expert_ids || !probs || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
+      !aligned16(y))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c = cfg_or_default(cfg);
+  const bool save = c.save_for_backward != 0;
+  const FwdLayout L = fwd_layout(T, H, F, E, k, save);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = error_word();
+  auto mark = [&](int i) {
+    if (c.step_events) cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+  };
+  mark(0);
+  const RouteScratch rs = route_scratch(at<char>(workspace, L.route), L.R, E);
+  int32_t* counts = at<int32_t>(workspace, L.counts);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  int32_t* off_al = at<int32_t>(workspace, L.off_al);
+  int32_t* row_of = at<int32_t>(workspace, L.row_of);
+  int32_t* token_of = at<int32_t>(workspace, L.token_of);
+  float* prob_of = at<float>(workspace, L.prob_of);
+  __nv_bfloat16* xp = at<__nv_bfloat16>(workspace, L.xp);
+  __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
+  __nv_bfloat16* o = at<__nv_bfloat16>(workspace, L.o);
+
+  // counts -> offsets -> row map -> permute (the dispatch)
+  if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (save && launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, xp, token_of,
+                                  prob_of, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  mark(1);
+  // fc1 + SwiGLU
+  CUtensorMap ta, tg, tu, th, td;
+  if (!make_tmap_bf16_2d(&ta, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, kTileM) ||
+      !make_tmap_bf16_2d(&tg, w_gate, F, static_cast<uint64_t>(E) * H,
+                         static_cast<uint64_t>(F) * 2, 64, 64) ||
+      !make_tmap_bf16_2d(&tu, w_up, F, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(F) * 2,
+                         64, 64) ||
+      !make_tmap_bf16_2d(&th, h, F, L.cap, static_cast<uint64_t>(F) * 2, 64, kTileM) ||
+      !make_tmap_bf16_2d(&td, w_down, H, static_cast<uint64_t>(E) * F,
+                         static_cast<uint64_t>(H) * 2, 64, 64))
+    return MOE_ERR_CUDA;
+  GroupedGemmArgs g1{};
+  g1.off_al = off_al;
+  g1.E = E;
+  g1.K = H;
+  g1.N = F;
+  g1.bn = 128;
+  g1.stages = c.ring_stages;
+  g1.out = h;
+  g1.save_g = save ? at<__nv_bfloat16>(workspace, L.ag) : nullptr;
+  g1.save_u = save ? at<__nv_bfloat16>(workspace, L.au) : nullptr;
+  g1.err = err;
+  g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+  const int grid = grid_size(c);
+  if (launch_fc1_swiglu(ta, tg, tu, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2);
+
+  // fc2
+  GroupedGemmArgs g2 = g1;
+  g2.K = F;
+  g2.N = H;
+  g2.bn = (H % 256 == 0) ? 256 : 128;
+  g2.out = o;
+  g2.save_g = g2.save_u = nullptr;
+  if (launch_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(3);
+
+  // unpermute (the combine)
+  const cudaError_t ue =
+      launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
+  mark(4);
+  return from_cuda(ue);
+}
+
+moe_status moe_expert_backward(const void*, const void*, const void*, const void*, const void*,
+                               const int32_t*, const float*, int64_t, int, int, int, int,
+                               const void*, size_t, void*, float*, float*, float*, float*, int,
+                               void*, size_t, const moe_config*, void*) {
+  return MOE_ERR_UNSUPPORTED;
+}
+
+size_t moe_workspace_size_mxfp8(int64_t, int, int, int, int, const moe_config*) { return 0; }
+
+moe_status moe_expert_forward_mxfp8(const void*, const uint8_t*, const uint8_t*, const uint8_t*,
+                                    const uint8_t*, const uint8_t*, const uint8_t*,
+                                    const int32_t*, const float*, int64_t, int, int, int, int,
+                                    void*, void*, size_t, const moe_config*, void*) {
+  return MOE_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

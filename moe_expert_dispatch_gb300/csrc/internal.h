@@ -1,0 +1,89 @@
+// internal.h - launchers shared between the translation units of the
+// library. Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+// Ids handled by one CTA of the histogram and row-map kernels.
+constexpr int kRouteChunk = 2048;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+// Rows of one grouped-GEMM M tile; expert segments are padded to it.
+constexpr int kTileM = 128;
+
+inline int64_t route_chunks(int64_t n_ids) { return (n_ids + kRouteChunk - 1) / kRouteChunk; }
+
+// Scratch of the counting step: per-chunk histograms and per-chunk bases,
+// each [chunks, E] int32.
+struct RouteScratch {
+  int32_t* hist;
+  int32_t* base;
+  int64_t chunks;
+};
+size_t route_scratch_bytes(int64_t n_ids, int E);
+RouteScratch route_scratch(void* ws, int64_t n_ids, int E);
+
+// counts[E], offsets[E+1] (dense) and, when off_al != nullptr, the offsets
+// of expert segments padded to `align` rows; s.base receives for every chunk
+// and expert the first row its ids take (in the padded layout).
+cudaError_t launch_counts(const int32_t* ids, int64_t n, int E, int align, int32_t* counts,
+                          int32_t* offsets, int32_t* off_al, RouteScratch s, int* err,
+                          cudaStream_t st);
+
+// Row of every slot, token and prob of every row (stable within an expert).
+cudaError_t launch_rowmap(const int32_t* ids, const float* probs, int64_t n, int k, int E,
+                          RouteScratch s, int32_t* row_of, int32_t* token_of, float* prob_of,
+                          cudaStream_t st);
+
+// xp[row_of[t, j]] = x[t] for every token (rows of row_bytes, % 16 == 0).
+cudaError_t launch_permute_copy(const void* x, int64_t T, int64_t row_bytes, int k,
+                                const int32_t* row_of, void* xp, cudaStream_t st);
+
+// Zero the padding rows of every expert segment of xp (and mark them in
+// token_of / prob_of with -1 / 0).
+cudaError_t launch_zero_padding(const int32_t* counts, const int32_t* off_al, int E,
+                                int64_t row_bytes, void* xp, int32_t* token_of, float* prob_of,
+                                cudaStream_t st);
+
+cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
+                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st);
+
+cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
+                                  uint8_t* scales, cudaStream_t st);
+
+// ------------------------------------------------------------------ grouped GEMMs
+
+struct GroupedGemmArgs {
+  const int32_t* off_al;   // [E+1] expert row offsets, multiples of kTileM
+  int E;
+  int K;                   // reduction length
+  int N;                   // output columns
+  int bn;                  // N tile (fc1: 128 per gate/up; fc2: 128 or 256)
+  int stages;              // ring depth 1..4
+  __nv_bfloat16* out;      // [rows, N]
+  __nv_bfloat16* save_g;   // fc1: optional bf16 copy of A_g
+  __nv_bfloat16* save_u;   // fc1: optional bf16 copy of A_u
+  int* err;
+  unsigned long long wait_ns;
+};
+
+// Encodes a 2D bf16 tensor map with the 128-byte swizzle (box inner = 64).
+bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// fc1: out = bf16(silu(A W_gate) * (A W_up)), A rows tiled per expert.
+cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                              const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// fc2: out = bf16(A W).
+cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
+                       int grid, cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace moe

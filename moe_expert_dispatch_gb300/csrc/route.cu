@@ -1,0 +1,405 @@
+// route.cu - the data-movement steps of the expert block: per-expert counts
+// (histc), the offset scan, the stable row map, the permute gather, the
+// probability-weighted unpermute and the MXFP8 quantiser. All are bound by
+// HBM bandwidth (or latency, for the tiny count/scan kernels); rows move as
+// 16-byte vectors, one warp per token so that each warp streams whole rows.
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ counts
+
+size_t route_scratch_bytes(int64_t n_ids, int E) {
+  const int64_t c = route_chunks(n_ids > 0 ? n_ids : 1);
+  const size_t one = static_cast<size_t>(c) * E * sizeof(int32_t);
+  return 2 * ((one + 255) / 256 * 256);
+}
+
+RouteScratch route_scratch(void* ws, int64_t n_ids, int E) {
+  RouteScratch s;
+  s.chunks = route_chunks(n_ids > 0 ? n_ids : 1);
+  const size_t one = (static_cast<size_t>(s.chunks) * E * sizeof(int32_t) + 255) / 256 * 256;
+  s.hist = static_cast<int32_t*>(ws);
+  s.base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + one);
+  return s;
+}
+
+// One CTA per chunk of ids: a shared-memory histogram, with the lanes of a
+// warp that hold the same expert folded into one atomic (match.any).
+__global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ ids, int64_t n,
+                                                   int E, int32_t* __restrict__ hist, int* err) {
+  extern __shared__ int sh_count[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh_count[e] = 0;
+  __syncthreads();
+  const int64_t lo = static_cast<int64_t>(blockIdx.x) * kRouteChunk;
+  const int64_t hi = min(n, lo + kRouteChunk);
+  bool bad = false;
+  for (int64_t i0 = lo; i0 < hi; i0 += blockDim.x) {
+    const int64_t i = i0 + threadIdx.x;
+    int e = -1;
+    if (i < hi) {
+      e = __ldg(ids + i);
+      if (e < 0 || e >= E) {
+        bad = true;
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane_id() == __ffs(peers) - 1) atomicAdd(&sh_count[e], __popc(peers));
+  }
+  if (bad) report_error(err, kErrBadId);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_count[e];
+}
+
+// One CTA: per expert the total and each chunk's exclusive prefix; then the
+// dense offsets, the padded offsets and every chunk's first row.
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist,
+                                                    int32_t* __restrict__ base, int64_t chunks,
+                                                    int E, int align, int32_t* counts,
+                                                    int32_t* offsets, int32_t* off_al) {
+  __shared__ int sh_cnt[kMaxExperts];
+  __shared__ int sh_al[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int64_t c = 0; c < chunks; ++c) {
+      const int v = hist[c * E + e];
+      base[c * E + e] = run;
+      run += v;
+    }
+    sh_cnt[e] = run;
+    if (counts) counts[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int o = 0, a = 0;
+    for (int e = 0; e < E; ++e) {
+      if (offsets) offsets[e] = o;
+      if (off_al) off_al[e] = a;
+      sh_al[e] = a;
+      o += sh_cnt[e];
+      a += (sh_cnt[e] + align - 1) / align * align;
+    }
+    if (offsets) offsets[E] = o;
+    if (off_al) off_al[E] = a;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    for (int64_t c = 0; c < chunks; ++c) base[c * E + e] += sh_al[e];
+}
+
+cudaError_t launch_counts(const int32_t* ids, int64_t n, int E, int align, int32_t* counts,
+                          int32_t* offsets, int32_t* off_al, RouteScratch s, int* err,
+                          cudaStream_t st) {
+  const int64_t chunks = route_chunks(n);
+  if (chunks > 0)
+    hist_kernel<<<static_cast<unsigned>(chunks), 256, E * sizeof(int), st>>>(ids, n, E, s.hist,
+                                                                            err);
+  else
+    cudaMemsetAsync(s.hist, 0, E * sizeof(int32_t), st);
+  scan_kernel<<<1, 1024, 0, st>>>(s.hist, s.base, chunks > 0 ? chunks : 1, E, align, counts,
+                                  offsets, off_al);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ row map
+
+// One CTA per chunk; warp w owns 256 consecutive ids, taken 32 at a time, so
+// the order "chunk, warp, step, lane" is the flat-index order. Pass 1 counts
+// per (warp, expert); a scan over warps turns that into each warp's first
+// row; pass 2 gives every id its row = warp base + rank among equal lanes.
+constexpr int kRowmapWarps = 8;
+constexpr int kRowmapPerWarp = kRouteChunk / kRowmapWarps;
+
+__global__ void __launch_bounds__(256) rowmap_kernel(const int32_t* __restrict__ ids,
+                                                     const float* __restrict__ probs, int64_t n,
+                                                     int k, int E,
+                                                     const int32_t* __restrict__ base,
+                                                     int32_t* __restrict__ row_of,
+                                                     int32_t* __restrict__ token_of,
+                                                     float* __restrict__ prob_of) {
+  extern __shared__ int wc[];  // [kRowmapWarps][E]
+  for (int i = threadIdx.x; i < kRowmapWarps * E; i += blockDim.x) wc[i] = 0;
+  __syncthreads();
+  const int w = threadIdx.x >> 5, lane = lane_id();
+  const int64_t start = static_cast<int64_t>(blockIdx.x) * kRouteChunk + w * kRowmapPerWarp;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int s = 0; s < kRowmapPerWarp; s += 32) {
+    const int64_t i = start + s + lane;
+    int e = (i < n) ? __ldg(ids + i) : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) wc[w * E + e] += __popc(peers);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = base[static_cast<int64_t>(blockIdx.x) * E + e];
+    for (int q = 0; q < kRowmapWarps; ++q) {
+      const int v = wc[q * E + e];
+      wc[q * E + e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  for (int s = 0; s < kRowmapPerWarp; s += 32) {
+    const int64_t i = start + s + lane;
+    int e = (i < n) ? __ldg(ids + i) : -1;
+    if (e >= E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int r = -1;
+    if (e >= 0) r = wc[w * E + e] + __popc(peers & lt);
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wc[w * E + e] += __popc(peers);
+    __syncwarp();
+    if (i < n) {
+      row_of[i] = r;
+      if (r >= 0) {
+        token_of[r] = static_cast<int32_t>(i / k);
+        if (prob_of) prob_of[r] = probs ? __ldg(probs + i) : 1.0f;
+      }
+    }
+  }
+}
+
+cudaError_t launch_rowmap(const int32_t* ids, const float* probs, int64_t n, int k, int E,
+                          RouteScratch s, int32_t* row_of, int32_t* token_of, float* prob_of,
+                          cudaStream_t st) {
+  const int64_t chunks = route_chunks(n);
+  if (chunks == 0) return cudaSuccess;
+  rowmap_kernel<<<static_cast<unsigned>(chunks), 256, kRowmapWarps * E * sizeof(int), st>>>(
+      ids, probs, n, k, E, s.base, row_of, token_of, prob_of);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ permute copy
+
+__device__ __forceinline__ int4 ld_stream(const int4* p) {
+  int4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// One warp per token: the token's row is read once and written to its k
+// rows; each warp instruction moves 512 contiguous bytes.
+__global__ void __launch_bounds__(256) permute_copy_kernel(const uint8_t* __restrict__ x,
+                                                           int64_t T, int64_t row_bytes, int k,
+                                                           const int32_t* __restrict__ row_of,
+                                                           uint8_t* __restrict__ xp) {
+  constexpr int U = 4;
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int64_t n16 = row_bytes >> 4;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    const int4* src = reinterpret_cast<const int4*>(x + t * row_bytes);
+    // the trip count is the same for every lane (the shuffles below need the
+    // whole warp); lanes past the row end just skip their vectors
+    for (int64_t base = 0; base < n16; base += 32 * U) {
+      const int64_t c0 = base + lane;
+      int4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c0 + 32 * u < n16) v[u] = ld_stream(src + c0 + 32 * u);
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0) continue;
+        int4* dst = reinterpret_cast<int4*>(xp + static_cast<int64_t>(r) * row_bytes);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+      }
+    }
+  }
+}
+
+static int grid_for_warps(int64_t warps, int warps_per_cta) {
+  const int64_t want = (warps + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+cudaError_t launch_permute_copy(const void* x, int64_t T, int64_t row_bytes, int k,
+                                const int32_t* row_of, void* xp, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  permute_copy_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(
+      static_cast<const uint8_t*>(x), T, row_bytes, k, row_of, static_cast<uint8_t*>(xp));
+  return cudaGetLastError();
+}
+
+// blockIdx.y = expert; the CTA zeroes rows [off_al[e] + c_e, off_al[e+1]).
+__global__ void __launch_bounds__(256) zero_padding_kernel(const int32_t* __restrict__ counts,
+                                                           const int32_t* __restrict__ off_al,
+                                                           int64_t row_bytes, uint8_t* xp,
+                                                           int32_t* token_of, float* prob_of) {
+  const int e = blockIdx.y;
+  const int64_t r0 = off_al[e] + counts[e], r1 = off_al[e + 1];
+  const int64_t n16 = (r1 - r0) * (row_bytes >> 4);
+  int4* base = reinterpret_cast<int4*>(xp + r0 * row_bytes);
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    base[i] = make_int4(0, 0, 0, 0);
+  if (blockIdx.x == 0)
+    for (int64_t r = r0 + threadIdx.x; r < r1; r += blockDim.x) {
+      if (token_of) token_of[r] = -1;
+      if (prob_of) prob_of[r] = 0.0f;
+    }
+}
+
+cudaError_t launch_zero_padding(const int32_t* counts, const int32_t* off_al, int E,
+                                int64_t row_bytes, void* xp, int32_t* token_of, float* prob_of,
+                                cudaStream_t st) {
+  const int64_t per = static_cast<int64_t>(kTileM - 1) * (row_bytes >> 4);
+  const int gx = static_cast<int>((per + 255) / 256 < 64 ? (per + 255) / 256 : 64);
+  zero_padding_kernel<<<dim3(gx > 0 ? gx : 1, E), 256, 0, st>>>(
+      counts, off_al, row_bytes, static_cast<uint8_t*>(xp), token_of, prob_of);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ unpermute
+
+__device__ __forceinline__ void acc_bf16x8(float* acc, const int4& v, float p) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = __bfloat1622float2(h[q]);
+    acc[2 * q] = fmaf(p, f.x, acc[2 * q]);
+    acc[2 * q + 1] = fmaf(p, f.y, acc[2 * q + 1]);
+  }
+}
+
+// One warp per token: y[t] = bf16(sum_j p_j o[row_j]), j in order, float
+// accumulation; 8 bf16 per lane per step.
+__global__ void __launch_bounds__(256) unpermute_kernel(const __nv_bfloat16* __restrict__ o,
+                                                        const int32_t* __restrict__ row_of,
+                                                        const float* __restrict__ probs,
+                                                        int64_t T, int k, int H,
+                                                        __nv_bfloat16* __restrict__ y) {
+  constexpr int U = 2;
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n8 = H >> 3;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    const float my_p = lane < k ? (probs ? __ldg(probs + t * k + lane) : 1.0f) : 0.0f;
+    for (int base = 0; base < n8; base += 32 * U) {   // warp-uniform trip count
+      const int c0 = base + lane;
+      float acc[U][8];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        const float p = __shfl_sync(0xffffffffu, my_p, j);
+        if (r < 0) continue;
+        const int4* src = reinterpret_cast<const int4*>(o + static_cast<int64_t>(r) * H);
+        int4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n8) v[u] = ld_stream(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n8) acc_bf16x8(acc[u], v[u], p);
+      }
+      int4* dst = reinterpret_cast<int4*>(y + t * H);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c0 + 32 * u < n8) {
+          int4 w;
+          w.x = static_cast<int>(pack_bf16x2(acc[u][0], acc[u][1]));
+          w.y = static_cast<int>(pack_bf16x2(acc[u][2], acc[u][3]));
+          w.z = static_cast<int>(pack_bf16x2(acc[u][4], acc[u][5]));
+          w.w = static_cast<int>(pack_bf16x2(acc[u][6], acc[u][7]));
+          dst[c0 + 32 * u] = w;
+        }
+    }
+  }
+}
+
+cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
+                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  unpermute_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(o, row_of, probs, T, k, H, y);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ MXFP8 quantiser
+
+// floor(log2(a)) of a positive finite float, subnormals included.
+__device__ __forceinline__ int floor_log2_pos(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int ex = static_cast<int>((b >> 23) & 0xFF);
+  if (ex != 0) return ex - 127;
+  const uint32_t man = b & 0x7FFFFF;
+  return (31 - __clz(static_cast<int>(man))) - 149;
+}
+
+// One thread per 32-element block: amax -> E8M0 code -> 32 E4M3 codes.
+// v * 2^-s is exact (a power-of-two scaling that stays in the normal range
+// for every value that can round to a non-zero E4M3), so the only rounding
+// is the one of the E4M3 conversion itself (round to nearest even,
+// saturating).
+__global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16* __restrict__ in,
+                                                             int64_t blocks,
+                                                             uint8_t* __restrict__ q,
+                                                             uint8_t* __restrict__ scales) {
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < blocks;
+       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int4* src = reinterpret_cast<const int4*>(in + b * 32);
+    int4 raw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) raw[i] = ld_stream(src + i);
+    float v[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(h[j]);
+        v[8 * i + 2 * j] = f.x;
+        v[8 * i + 2 * j + 1] = f.y;
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+    int s = (amax > 0.0f) ? floor_log2_pos(amax) - 8 : -127;
+    s = max(-127, min(127, s));
+    scales[b] = static_cast<uint8_t>(s + 127);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+    uint32_t words[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_fp8x2_storage_t lo =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv),
+                                   __NV_SATFINITE, __NV_E4M3);
+      const __nv_fp8x2_storage_t hi =
+          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv),
+                                   __NV_SATFINITE, __NV_E4M3);
+      words[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+    }
+    int4* dst = reinterpret_cast<int4*>(q + b * 32);
+    dst[0] = make_int4(words[0], words[1], words[2], words[3]);
+    dst[1] = make_int4(words[4], words[5], words[6], words[7]);
+  }
+}
+
+cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
+                                  uint8_t* scales, cudaStream_t st) {
+  const int64_t blocks = rows * (K / 32);
+  if (blocks == 0) return cudaSuccess;
+  const int64_t want = (blocks + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  quantize_mxfp8_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
+      in, blocks, q, scales);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

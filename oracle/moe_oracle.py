@@ -242,6 +242,34 @@ def dense_forward(x, w_gate, w_up, w_down, expert_ids, probs, tokens=None, round
                      for t in tokens])
 
 
+def sampled_forward(x, w_gate, w_up, w_down, expert_ids, probs, tokens):
+    """token_forward for the listed tokens, visiting one expert at a time so
+    that each expert's weights are converted to float64 once. Every (t, j)
+    slot's O row is the same per-token expression; the combine then sums j
+    in order per token."""
+    x = np.asarray(x)
+    ids = np.asarray(expert_ids)
+    pr = np.asarray(probs)
+    tokens = list(tokens)
+    o_rows = {}
+    for e in sorted(set(int(v) for t in tokens for v in ids[t])):
+        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
+        for t in tokens:
+            for j, ee in enumerate(ids[t].tolist()):
+                if ee == e:
+                    xt = _f64(x[t])
+                    hv = bf16(silu(xt @ wg) * (xt @ wu))
+                    o_rows[(t, j)] = bf16(hv @ wd)
+    out = []
+    for t in tokens:
+        acc = None
+        for j in range(ids.shape[1]):
+            term = float(pr[t, j]) * o_rows[(t, j)]
+            acc = term if acc is None else acc + term
+        out.append(bf16(acc))
+    return np.stack(out)
+
+
 # --------------------------------------------------------------------------
 # backward
 # --------------------------------------------------------------------------

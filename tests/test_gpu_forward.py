@@ -1,0 +1,136 @@
+"""GPU parity of the fused forward (counts -> permute -> fc1+SwiGLU -> fc2 ->
+unpermute) against the CPU oracle, within |y - y_ref| <= 1e-2 + 1e-2 |y_ref|,
+on small ragged shapes, the tiny and skewed workloads in full, the
+Mixtral-shaped workload on sampled tokens, and the invariants (schedule and
+ring-depth independence, micro-batch split, empty experts, error paths)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import synth
+from gpu_util import assert_bf16_close, dev, f32_slices, to_np
+
+pytestmark = pytest.mark.gpu
+m = pytest.importorskip("moe_expert_dispatch_gb300")
+
+
+def _case(T, H, F, E, k, seed=0, empty=(), wstd=0.05, hot=None):
+    rng = np.random.default_rng(seed)
+    live = [e for e in range(E) if e not in empty]
+    if hot is not None:
+        ids = np.stack([[hot] + list(rng.choice([e for e in live if e != hot], k - 1, replace=False))
+                        for _ in range(T)])
+    else:
+        ids = np.stack([rng.choice(live, k, replace=False) for _ in range(T)])
+    ids = torch.from_numpy(ids.astype(np.int32))
+    logits = rng.standard_normal((T, k))
+    probs = torch.from_numpy((np.exp(logits) / np.exp(logits).sum(1, keepdims=True)).astype(np.float32))
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    wg = torch.from_numpy((rng.standard_normal((E, H, F)) * wstd).astype(np.float32)).to(torch.bfloat16)
+    wu = torch.from_numpy((rng.standard_normal((E, H, F)) * wstd).astype(np.float32)).to(torch.bfloat16)
+    wd = torch.from_numpy((rng.standard_normal((E, F, H)) * wstd).astype(np.float32)).to(torch.bfloat16)
+    return x, wg, wu, wd, ids, probs
+
+
+def _oracle(x, wg, wu, wd, ids, probs):
+    return orc.expert_forward(to_np(x), to_np(wg), to_np(wu), to_np(wd), ids.numpy(),
+                              probs.numpy().astype(np.float64))
+
+
+def _gpu(x, wg, wu, wd, ids, probs, **cfg):
+    y, _ = m.moe_expert_forward(dev(x), dev(wg), dev(wu), dev(wd), dev(ids), dev(probs),
+                                cfg=m.config(**cfg))
+    assert m.moe_get_error() == 0
+    return y
+
+
+@pytest.mark.parametrize("T,H,F,E,k,empty", [
+    (300, 256, 384, 5, 2, (3,)),       # several tiles, ragged tails, one empty expert
+    (129, 128, 128, 1, 1, ()),         # one expert: a dense SwiGLU MLP, 2 M tiles
+    (1, 128, 256, 4, 2, ()),           # one token
+    (517, 384, 640, 9, 3, (0, 8)),     # H % 256 != 0: fc2 with 128-wide N tiles
+    (256, 512, 1024, 8, 8, ()),        # k = E: every expert gets every token
+])
+def test_forward_small_ragged(T, H, F, E, k, empty):
+    case = _case(T, H, F, E, k, seed=T, empty=empty)
+    y = _gpu(*case)
+    assert_bf16_close(to_np(y), _oracle(*case), "y")
+
+
+def test_forward_all_tokens_one_expert():
+    case = _case(1000, 256, 256, 16, 2, seed=4, hot=11)
+    assert_bf16_close(to_np(_gpu(*case)), _oracle(*case), "y")
+
+
+def test_forward_tiny_workload():
+    inp = synth.make_inputs(synth.WORKLOADS["tiny_bf16"], 0)
+    case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
+    assert_bf16_close(to_np(_gpu(*case)), _oracle(*case), "y")
+
+
+def test_forward_skewed_workload_full():
+    inp = synth.make_inputs(synth.WORKLOADS["skewed_bf16"], 0)
+    case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
+    y = _gpu(*case)
+    ref = orc.expert_forward(to_np(case[0]), f32_slices(case[1]), f32_slices(case[2]),
+                             f32_slices(case[3]), case[4].numpy(), case[5].numpy().astype(np.float64))
+    assert_bf16_close(to_np(y), ref, "y")
+
+
+def test_forward_mixtral_workload_sampled():
+    inp = synth.make_inputs(synth.WORKLOADS["mixtral_bf16"], 0)
+    case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
+    y = to_np(_gpu(*case))
+    toks = np.random.default_rng(0).choice(4096, 48, replace=False).tolist() + [0, 4095]
+    ref = orc.sampled_forward(to_np(case[0]), f32_slices(case[1]), f32_slices(case[2]),
+                              f32_slices(case[3]), case[4].numpy(), case[5].numpy(), toks)
+    assert_bf16_close(y[toks], ref, "y sampled")
+
+
+def test_forward_independent_of_schedule_and_ring_depth():
+    case = _case(700, 256, 512, 6, 2, seed=9, empty=(2,))
+    y0 = _gpu(*case)
+    for stages in (1, 2, 3):
+        assert torch.equal(_gpu(*case, ring_stages=stages), y0)
+    for sms in (1, 3, 17):
+        assert torch.equal(_gpu(*case, num_sms=sms), y0)
+
+
+@pytest.mark.parametrize("splits", [2, 4, 8])
+def test_forward_microbatch_split_bit_identical(splits):
+    case = _case(512, 256, 384, 8, 2, seed=12)
+    x, wg, wu, wd, ids, probs = case
+    y = _gpu(*case)
+    n = 512 // splits
+    parts = [_gpu(x[i * n:(i + 1) * n], wg, wu, wd, ids[i * n:(i + 1) * n], probs[i * n:(i + 1) * n])
+             for i in range(splits)]
+    assert torch.equal(torch.cat(parts), y)
+
+
+def test_forward_zero_tokens():
+    x, wg, wu, wd, ids, probs = _case(4, 128, 128, 4, 2)
+    y, _ = m.moe_expert_forward(dev(x[:0]), dev(wg), dev(wu), dev(wd), dev(ids[:0]), dev(probs[:0]))
+    assert y.shape == (0, 128)
+
+
+def test_forward_bad_ids_reported():
+    x, wg, wu, wd, ids, probs = _case(64, 128, 128, 4, 2)
+    ids = ids.clone()
+    ids[5, 1] = 4
+    ids[9, 0] = -1
+    y, _ = m.moe_expert_forward(dev(x), dev(wg), dev(wu), dev(wd), dev(ids), dev(probs))
+    assert m.moe_get_error() == 3
+    # the tokens with valid ids are still computed
+    ok = [t for t in range(64) if t not in (5, 9)]
+    ids_ok = ids[ok]
+    ref = _oracle(x[ok], wg, wu, wd, ids_ok, probs[ok])
+    assert_bf16_close(to_np(y)[ok], ref, "y")
+
+
+def test_forward_wait_timeout_reports_and_recovers():
+    case = _case(300, 256, 384, 5, 2, seed=3)
+    y, _ = m.moe_expert_forward(*(dev(t) for t in case), cfg=m.config(wait_limit_ns=1))
+    assert m.moe_get_error() == 5
+    y = _gpu(*case)           # the context is still usable and results are right
+    assert_bf16_close(to_np(y), _oracle(*case), "y")

@@ -361,3 +361,10 @@ def test_mxfp8_grouped_equals_per_token():
     wgt = np.transpose(wg, (0, 2, 1)); wut = np.transpose(wu, (0, 2, 1)); wdt = np.transpose(wd, (0, 2, 1))
     yb = orc.expert_forward(x, wgt, wut, wdt, ids, probs)
     assert np.max(np.abs(y1 - yb)) <= 0.1 * np.max(np.abs(yb))
+
+
+def test_sampled_forward_equals_dense():
+    x, wg, wu, wd, ids, probs = _rand_case(T=23)
+    toks = [0, 5, 22, 7]
+    np.testing.assert_array_equal(orc.sampled_forward(x, wg, wu, wd, ids, probs, toks),
+                                  orc.dense_forward(x, wg, wu, wd, ids, probs, toks))
