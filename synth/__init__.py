@@ -55,6 +55,9 @@ WORKLOADS = {
     "skewed_bf16": Workload("skewed_bf16", 8192, 2048, 768, 128, 8, "zipf", 0.01),
     "mxfp8": Workload("mxfp8", 16384, 7168, 2048, 64, 6, "uniform", 0.02, mxfp8=True),
     "train_bf16": Workload("train_bf16", 16384, 4096, 14336, 8, 2, "gaussian", 0.01, backward=True),
+    # a smaller Mixtral-shaped case (2 experts, every token on both) for
+    # profiler captures that must hold only about 1 GB on the device
+    "mixtral_2experts": Workload("mixtral_2experts", 2048, 4096, 14336, 2, 2, "gaussian", 0.01),
 }
 
 # Zipf exponent and the number of experts given zero popularity in the
