@@ -104,6 +104,29 @@ moe_status moe_counts(const int32_t* expert_ids, int64_t n_ids, int E, int32_t* 
                       int32_t* offsets, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * moe_counts_static - moe_counts without a workspace, for callers that
+ * cannot allocate device memory at call time (a serving runtime that fixes
+ * its memory footprint at start-up and forbids allocation afterwards, or a
+ * plugin interface that hands an operator no scratch buffer). The pages have
+ * no counterpart of this call; it exists for those callers only.
+ *
+ * Same arguments and results as moe_counts minus the workspace. The scratch
+ * (per-chunk histograms and bases) lives in a fixed 512 KB array of device
+ * memory owned by the library, held by every GPU that loads the library
+ * until the process exits. Limits: ceil(n_ids / 2048) * E <= 65536 (16 M ids
+ * at E = 8, 1 M ids at E = 128); larger requests return MOE_ERR_WORKSPACE and
+ * launch nothing. The call allocates nothing. Its first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. Every
+ * call overwrites the whole scratch it uses, so nothing needs clearing
+ * between calls, but all calls on a device share the one array: calls that
+ * overlap on the GPU (other streams, other threads) race and must be
+ * serialised by the caller.
+ * ------------------------------------------------------------------------ */
+moe_status moe_counts_static(const int32_t* expert_ids, int64_t n_ids, int E, int32_t* counts,
+                             int32_t* offsets, void* stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute - gather routed rows into expert-contiguous order.
  * Step 6 of ep_mc2_forward, permute(hidden_states, selected_experts): on one
  * GPU this is also the dispatch AllToAllv of all2all_grouped_matmul.

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m moe_expert_dispatch_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python moe_expert_dispatch_gb300/build.py` "
         "(the expert block has no CPU or eager fallback)")
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -54,6 +54,7 @@ _sig("moe_num_sms", _i32)
 _sig("moe_padded_rows", _i64, _i64, _i32, _i32)
 _sig("moe_counts_workspace_size", _sz, _i64, _i32)
 _sig("moe_counts", _i32, _vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp)
+_sig("moe_counts_static", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
 _sig("moe_permute_workspace_size", _sz, _i64, _i32, _i32)
 _sig("moe_permute", _i32, _vp, _i64, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
      _vp, _vp, _sz, _vp)
@@ -150,6 +151,21 @@ def moe_counts(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=
     ws = _workspace(need, dev) if workspace is None else workspace
     _check(_lib.moe_counts(_p(expert_ids), n, num_experts, _p(counts), _p(offsets), _p(ws),
                            ws.numel(), _stream(stream)), "moe_counts")
+    return counts, offsets
+
+
+def moe_counts_static(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=None,
+                      stream=None):
+    """moe_counts with the library's fixed scratch instead of a workspace: it
+    allocates no device memory (the output tensors are created here only when
+    the caller passes none). Calls that overlap on the GPU race on that scratch."""
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    dev = expert_ids.device
+    counts = torch.empty(num_experts, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+               if offsets is None else offsets)
+    _check(_lib.moe_counts_static(_p(expert_ids), expert_ids.numel(), num_experts, _p(counts),
+                                  _p(offsets), _stream(stream)), "moe_counts_static")
     return counts, offsets
 
 

@@ -3,7 +3,7 @@
 Each .cu file is compiled to an object in parallel, then the objects are
 linked into one shared library (CUDA runtime linked statically, no link to
 libcuda: the tensor-map encoder is fetched through the runtime at first use).
-Run as `python -m moe_expert_dispatch_gb300.build`.
+Run as `python moe_expert_dispatch_gb300/build.py` (or __graft_entry__.build()).
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["route.cu", "gemm_bf16.cu", "capi.cu"]
+SOURCES = ["route.cu", "gemm_bf16.cu", "capi.cu", "counts_static.cu"]
 
 
 def nvcc() -> str:

@@ -121,6 +121,8 @@ int grid_size(const moe_config& c) {
 
 }  // namespace
 
+int* device_error_word() { return error_word(); }
+
 int device_sm_count() {
   static int counts[kMaxDevices] = {};
   const int d = current_device();
