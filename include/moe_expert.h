@@ -214,9 +214,9 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
  * backward; its section "validation items" compares the fc1/fc2 gradients.
  *   dO_r  = bf16(p_r dY_t(r));          dprobs[t,j] = <dY_t, O_row(t,j)>
  *   dH    = dO_e W2_e^T (float);        dA_g = bf16(dH A_u silu'(A_g)),
- *   dA_u  = bf16(dH silu(A_g));         dXp = bf16(dA_g W1g_e^T + dA_u W1u_e^T)
+ *   dA_u  = bf16(dH silu(A_g));         dXp = dA_g W1g_e^T + dA_u W1u_e^T (float)
  *   dW2_e = h_e^T dO_e, dW1g_e = Xp_e^T dA_g, dW1u_e = Xp_e^T dA_u (float)
- *   dX_t  = bf16(sum_j dXp[row_of[t, j]])
+ *   dX_t  = bf16(sum_j dXp[row_of[t, j]]), j in order
  * A_g and A_u enter as saved by the forward (bf16).
  *
  *  dy          bf16 [T, H]

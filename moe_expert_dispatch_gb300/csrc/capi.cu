@@ -90,6 +90,29 @@ FwdLayout fwd_layout(int64_t T, int H, int F, int E, int k, bool save) {
   return L;
 }
 
+// Backward workspace: dO [cap, H] and dA = [dA_g | dA_u] [cap, 2F] in bf16 (GEMM
+// operands), dXp [cap, H] in float (summed into dX, then rounded once).
+struct BwdLayout {
+  int64_t cap;
+  size_t d_o, d_a, d_xp, total;
+};
+
+BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
+  BwdLayout B;
+  B.cap = moe_padded_rows(T * k, E, kTileM);
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = cur;
+    cur += up256(bytes);
+    return at;
+  };
+  B.d_o = take(static_cast<size_t>(B.cap) * H * 2);
+  B.d_a = take(static_cast<size_t>(B.cap) * F * 2 * 2);
+  B.d_xp = take(static_cast<size_t>(B.cap) * H * 4);
+  B.total = cur;
+  return B;
+}
+
 template <typename P>
 P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
@@ -264,7 +287,7 @@ size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_confi
                           int for_backward) {
   if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;
   const moe_config c = cfg_or_default(cfg);
-  if (for_backward) return 0;  // the backward workspace is added with the backward kernels
+  if (for_backward) return bwd_layout(T, H, F, E, k).total;
   return fwd_layout(T, H, F, E, k, c.save_for_backward != 0).total;
 }
 
@@ -330,9 +353,12 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g1.E = E;
   g1.K = H;
   g1.N = F;
-  g1.bn = 128;
+  g1.bn = 256;                 // 128 gate + 128 up columns per N tile
   g1.stages = c.ring_stages;
+  g1.b_rows = H;
+  g1.b_split = 1;
   g1.out = h;
+  g1.ldo = F;
   g1.save_g = save ? at<__nv_bfloat16>(workspace, L.ag) : nullptr;
   g1.save_u = save ? at<__nv_bfloat16>(workspace, L.au) : nullptr;
   g1.err = err;
@@ -346,7 +372,10 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g2.K = F;
   g2.N = H;
   g2.bn = (H % 256 == 0) ? 256 : 128;
+  g2.b_rows = F;
+  g2.b_split = 0;
   g2.out = o;
+  g2.ldo = H;
   g2.save_g = g2.save_u = nullptr;
   if (launch_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
@@ -358,11 +387,134 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   return from_cuda(ue);
 }
 
-moe_status moe_expert_backward(const void*, const void*, const void*, const void*, const void*,
-                               const int32_t*, const float*, int64_t, int, int, int, int,
-                               const void*, size_t, void*, float*, float*, float*, float*, int,
-                               void*, size_t, const moe_config*, void*) {
-  return MOE_ERR_UNSUPPORTED;
+moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate, const void* w_up,
+                               const void* w_down, const int32_t* expert_ids, const float* probs,
+                               int64_t T, int H, int F, int E, int k, const void* fwd_ws,
+                               size_t fwd_ws_bytes, void* dx, float* dw_gate, float* dw_up,
+                               float* dw_down, float* dprobs, int accumulate_dw, void* workspace,
+                               size_t ws_bytes, const moe_config* cfg, void* stream) {
+  moe_status s = check_block_args(T, H, F, E, k);
+  if (s != MOE_OK) return s;
+  if (!w_gate || !w_up || !w_down || !dw_gate || !dw_up || !dw_down) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(dw_gate) ||
+      !aligned16(dw_up) || !aligned16(dw_down))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // no tokens: every expert is empty, so the weight gradients are zero
+    if (accumulate_dw) return MOE_OK;
+    const size_t wb = static_cast<size_t>(E) * H * F * sizeof(float);
+    if (cudaMemsetAsync(dw_gate, 0, wb, st) != cudaSuccess ||
+        cudaMemsetAsync(dw_up, 0, wb, st) != cudaSuccess ||
+        cudaMemsetAsync(dw_down, 0, wb, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  (void)x;
+  (void)expert_ids;
+  if (!dy || !probs || !dx || !dprobs || !fwd_ws || !aligned16(dy) || !aligned16(dx))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c = cfg_or_default(cfg);
+  const FwdLayout L = fwd_layout(T, H, F, E, k, true);
+  if (fwd_ws_bytes < L.total || !aligned16(fwd_ws)) return MOE_ERR_WORKSPACE;
+  const BwdLayout B = bwd_layout(T, H, F, E, k);
+  if (!workspace || ws_bytes < B.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  int* err = error_word();
+  void* fw = const_cast<void*>(fwd_ws);
+  const int32_t* counts = at<int32_t>(fw, L.counts);
+  const int32_t* off_al = at<int32_t>(fw, L.off_al);
+  const int32_t* row_of = at<int32_t>(fw, L.row_of);
+  const __nv_bfloat16* xp = at<__nv_bfloat16>(fw, L.xp);
+  const __nv_bfloat16* h = at<__nv_bfloat16>(fw, L.h);
+  const __nv_bfloat16* o = at<__nv_bfloat16>(fw, L.o);
+  const __nv_bfloat16* ag = at<__nv_bfloat16>(fw, L.ag);
+  const __nv_bfloat16* au = at<__nv_bfloat16>(fw, L.au);
+  __nv_bfloat16* d_o = at<__nv_bfloat16>(workspace, B.d_o);
+  __nv_bfloat16* d_a = at<__nv_bfloat16>(workspace, B.d_a);
+  float* d_xp = at<float>(workspace, B.d_xp);
+  const int grid = grid_size(c);
+  const int bnF = (F % 256 == 0) ? 256 : 128;
+  const int bnH = (H % 256 == 0) ? 256 : 128;
+
+  // dO = p dY (gather-scale) and dprobs = <dY, O>; padding rows of dO are zero
+  if (launch_dout(static_cast<const __nv_bfloat16*>(dy), o, row_of, probs, T, k, H, d_o, dprobs,
+                  st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, d_o, nullptr, nullptr,
+                          st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  CUtensorMap t_do, t_w2k, t_da, t_wgk, t_wuk, t_xp_mn, t_da_mn, t_h_mn, t_do_mn;
+  if (!make_tmap_bf16_2d(&t_do, d_o, H, B.cap, static_cast<uint64_t>(H) * 2, 64, kTileM) ||
+      !make_tmap_bf16_2d(&t_w2k, w_down, H, static_cast<uint64_t>(E) * F,
+                         static_cast<uint64_t>(H) * 2, 64, bnF) ||
+      !make_tmap_bf16_2d(&t_da, d_a, 2 * static_cast<uint64_t>(F), B.cap,
+                         static_cast<uint64_t>(F) * 4, 64, kTileM) ||
+      !make_tmap_bf16_2d(&t_wgk, w_gate, F, static_cast<uint64_t>(E) * H,
+                         static_cast<uint64_t>(F) * 2, 64, bnH) ||
+      !make_tmap_bf16_2d(&t_wuk, w_up, F, static_cast<uint64_t>(E) * H,
+                         static_cast<uint64_t>(F) * 2, 64, bnH) ||
+      !make_tmap_bf16_2d(&t_xp_mn, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, 64) ||
+      !make_tmap_bf16_2d(&t_da_mn, d_a, 2 * static_cast<uint64_t>(F), B.cap,
+                         static_cast<uint64_t>(F) * 4, 64, 64) ||
+      !make_tmap_bf16_2d(&t_h_mn, h, F, L.cap, static_cast<uint64_t>(F) * 2, 64, 64) ||
+      !make_tmap_bf16_2d(&t_do_mn, d_o, H, B.cap, static_cast<uint64_t>(H) * 2, 64, 64))
+    return MOE_ERR_CUDA;
+
+  // dH = dO W2^T, then dA_g, dA_u from the saved A_g, A_u
+  GroupedGemmArgs g{};
+  g.off_al = off_al;
+  g.E = E;
+  g.stages = c.ring_stages;
+  g.err = err;
+  g.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+  GroupedGemmArgs gh = g;
+  gh.K = H;
+  gh.N = F;
+  gh.bn = bnF;
+  gh.b_rows = F;
+  gh.out = d_a;
+  gh.ldo = 2 * static_cast<int64_t>(F);
+  gh.out_split = F;
+  gh.act_g = ag;
+  gh.act_u = au;
+  gh.ld_act = F;
+  if (launch_dh_swiglu_bwd(t_do, t_w2k, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // dXp = dA_g W1g^T + dA_u W1u^T (one reduction over 2F), then dX = sum_j dXp[row_of]
+  GroupedGemmArgs gx = g;
+  gx.K = 2 * F;
+  gx.N = H;
+  gx.bn = bnH;
+  gx.b_rows = H;
+  gx.b_split = 2;
+  gx.k_split = F / 64;
+  gx.outf = d_xp;
+  gx.ldo = H;
+  if (launch_dxp(t_da, t_wgk, t_wuk, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+
+  // dW1g | dW1u = Xp_e^T [dA_g | dA_u] and dW2 = h_e^T dO_e over each expert's rows
+  GroupedGemmArgs gw1 = g;
+  gw1.M = H;
+  gw1.N = 2 * F;
+  gw1.bn = bnF;
+  gw1.out_split = F;
+  gw1.outf = dw_gate;
+  gw1.outf2 = dw_up;
+  gw1.accumulate = accumulate_dw ? 1 : 0;
+  if (launch_wgrad(t_xp_mn, t_da_mn, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  GroupedGemmArgs gw2 = g;
+  gw2.M = F;
+  gw2.N = H;
+  gw2.bn = bnH;
+  gw2.out_split = 0;
+  gw2.outf = dw_down;
+  gw2.accumulate = accumulate_dw ? 1 : 0;
+  if (launch_wgrad(t_h_mn, t_do_mn, gw2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 size_t moe_workspace_size_mxfp8(int64_t, int, int, int, int, const moe_config*) { return 0; }

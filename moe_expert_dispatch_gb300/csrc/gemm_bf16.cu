@@ -1,27 +1,30 @@
 // gemm_bf16.cu - persistent grouped GEMMs of the expert block on the
-// 5th-generation tensor cores (tcgen05) of sm_103a.
+// 5th-generation tensor cores (tcgen05) of sm_103a, forward and backward.
 //
 // Structure (one CTA per SM, 6 warps):
-//   warp 0      TMA producer: streams the A tile (128 routed rows x 64 of K)
-//               and the B tile (64 of K x 256 weight columns) of every
-//               k-block into a ring of `stages` shared-memory slots.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
-//               K=16) on each slot and releases it with tcgen05.commit;
+//   warp 0      TMA producer: streams the A tile (128 x 64 of K) and the B
+//               tile (64 of K x bn) of every k-block into a ring of
+//               `stages` shared-memory slots of 48 KB.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=bn,
+//               K=16) on each slot and releases it with tcgen05.commit; it
 //               accumulates a tile in one of two TMEM buffers (2 x 256
 //               columns) so that the epilogue of tile i overlaps tile i+1.
-//   warps 2-5   epilogue: tcgen05.ld the accumulator, apply SwiGLU (fc1) or
-//               round (fc2), store bf16 rows.
+//   warps 2-5   epilogue: tcgen05.ld the accumulator and finish the tile.
 // This is the in-kernel counterpart of the MC2 ring of "MC2 通算融合架构总览"
 // (sections 3-4): the producer's TMA loads stand where the AIV's UDMA puts
-// stood, the mbarrier pair full/empty where the CrossCore set/wait flags
+// stood, the full/empty mbarrier pair where the CrossCore set/wait flags
 // stood, and slot = k-block mod stages as bufferId = mLoopIdx mod bufferSize.
 //
-// Tiles: expert e owns rows [off_al[e], off_al[e+1]) of the permuted
-// activations, a multiple of 128 (padded), i.e. (off_al[e+1]-off_al[e])/128
-// M tiles, times N/bn N tiles. The persistent scheduler numbers the tiles of
-// all experts consecutively (M fastest, so CTAs that run at the same time
-// share one weight tile through L2) and CTA b takes tiles b, b+grid, ...
-// Experts without rows own no tile. Counts never leave the device.
+// Two schedules share the kernel:
+//  * Rows (fc1, fc2, dH, dXp): expert e owns rows [off_al[e], off_al[e+1])
+//    of the permuted activations, a multiple of 128 (padded), i.e. one M
+//    tile per 128 rows, times N/bn N tiles; the reduction is a fixed K.
+//  * WGrad (dW1, dW2): expert e owns (M/128) x (N/bn) tiles of its weight
+//    gradient and the reduction runs over its (zero-padded) rows.
+// Tiles of all experts are numbered consecutively, M fastest (so CTAs that
+// run at the same time share one B tile through L2), and CTA b takes tiles
+// b, b + grid, ...; experts without rows own no Rows tile. Counts never
+// leave the device.
 #include "common.cuh"
 #include "internal.h"
 
@@ -48,21 +51,67 @@ struct Smem {
   int zero;
 };
 
-__device__ __forceinline__ void decode_tile(int t, const int* ts, const int32_t* off_al, int E,
-                                            int& e, int& m, int& n) {
-  int lo = 0, hi = E - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ts[mid] <= t) lo = mid; else hi = mid - 1;
+struct Tile {
+  int e, m, n;
+  int row0;      // Rows: first A row; WGrad: first reduction row
+  int kblocks;
+};
+
+template <Sched kSched>
+__device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedGemmArgs& p) {
+  Tile tl;
+  if (kSched == Sched::Rows) {
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ts[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    tl.e = lo;
+    const int mt = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int local = t - ts[tl.e];
+    tl.n = local / mt;
+    tl.m = local - tl.n * mt;
+    tl.row0 = p.off_al[tl.e] + tl.m * kTileM;
+    tl.kblocks = p.K / BK;
+  } else {
+    const int mt = p.M / kTileM;
+    const int per = mt * (p.N / p.bn);
+    tl.e = t / per;
+    const int local = t - tl.e * per;
+    tl.n = local / mt;
+    tl.m = local - tl.n * mt;
+    tl.row0 = p.off_al[tl.e];
+    tl.kblocks = (p.off_al[tl.e + 1] - tl.row0) / BK;
   }
-  e = lo;
-  const int mt = (off_al[e + 1] - off_al[e]) / kTileM;
-  const int local = t - ts[e];
-  n = local / mt;
-  m = local - n * mt;
+  return tl;
 }
 
-template <bool kSwiglu>
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    st_global_v4(dst + 8 * i,
+                 pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                 pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                 pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                 pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f) {
+  const int4* s = reinterpret_cast<const int4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int4 v = s[i];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 ff = __bfloat1622float2(h[q]);
+      f[8 * i + 2 * q] = ff.x;
+      f[8 * i + 2 * q + 1] = ff.y;
+    }
+  }
+}
+
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -72,12 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   Smem* sm = reinterpret_cast<Smem*>(ring + S * kStageBytes);
-  int* ts = reinterpret_cast<int*>(sm + 1);  // [E+1] first tile of each expert
+  int* ts = reinterpret_cast<int*>(sm + 1);  // [E+1] first tile of each expert (Rows)
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int E = p.E;
-  const int n_tiles = p.N / p.bn;
-  const int kblocks = p.K / BK;
-  const int bn = kSwiglu ? 256 : p.bn;       // MMA N (fc1: gate 128 + up 128)
+  const int bn = p.bn;
+  const int n_tiles = p.N / (kEpi == Epi::SwigluFwd ? bn / 2 : bn);
   const uint32_t stage_tx = kABytes + (bn / 64) * kBBox;
 
   if (threadIdx.x == 0) {
@@ -97,24 +145,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
-    if (kSwiglu) tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  for (int e = threadIdx.x; e < E; e += kThreads)
-    ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ts[0] = 0;
-    for (int e = 0; e < E; ++e) ts[e + 1] += ts[e];
+  int total;
+  if (kSched == Sched::Rows) {
+    for (int e = threadIdx.x; e < E; e += kThreads)
+      ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ts[0] = 0;
+      for (int e = 0; e < E; ++e) ts[e + 1] += ts[e];
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
-  const int total = ts[E];
+  if (kSched == Sched::Rows) total = ts[E];
+  else total = E * (p.M / kTileM) * n_tiles;
   volatile int* abort_flag = &sm->abort;
 
   if (warp == 0) {
@@ -125,32 +177,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t last_par[4] = {0, 0, 0, 0};
       bool used[4] = {false, false, false, false};
       bool ok = true;
-      // the routed rows are re-read by every N tile of their expert: keep them in L2
-      const uint64_t pol_a = l2_policy_evict_last();
+      // operands re-read by many tiles of their expert stay in L2 longer
+      const uint64_t pol_keep = l2_policy_evict_last();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int e, m, n;
-        decode_tile(t, ts, p.off_al, E, e, m, n);
-        const int a_row = p.off_al[e] + m * kTileM;
-        const int b_row = e * p.K;
-        const int n0 = n * p.bn;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const Tile tl = decode_tile<kSched>(t, ts, p);
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
           const uint32_t full = smem_u32(&sm->full[stage]);
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full, stage_tx);
-          uint8_t* sa = ring + stage * kStageBytes;
-          uint8_t* sb = sa + kABytes;
-          tma_load_2d_hint(smem_u32(sa), &tmA, full, kb * BK, a_row, pol_a);
-          if (kSwiglu) {
-            tma_load_2d(smem_u32(sb), &tmB0, full, n0, b_row + kb * BK);
-            tma_load_2d(smem_u32(sb + kBBox), &tmB0, full, n0 + 64, b_row + kb * BK);
-            tma_load_2d(smem_u32(sb + 2 * kBBox), &tmB1, full, n0, b_row + kb * BK);
-            tma_load_2d(smem_u32(sb + 3 * kBBox), &tmB1, full, n0 + 64, b_row + kb * BK);
+          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          // ---- A
+          if (!kAmn) {
+            tma_load_2d_hint(sa, &tmA, full, kb * BK, tl.row0, pol_keep);
           } else {
-            for (int j = 0; j < bn / 64; ++j)
-              tma_load_2d(smem_u32(sb + j * kBBox), &tmB0, full, n0 + 64 * j, b_row + kb * BK);
+            const int kr = tl.row0 + kb * BK;
+            tma_load_2d_hint(sa, &tmA, full, tl.m * kTileM, kr, pol_keep);
+            tma_load_2d_hint(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr, pol_keep);
+          }
+          // ---- B
+          if (kBmn) {
+            const int krow = (kSched == Sched::Rows) ? tl.e * p.b_rows + kb * BK
+                                                      : tl.row0 + kb * BK;
+            if (p.b_split == 1) {            // gate / up halves of one N tile
+              const int n0 = tl.n * (bn / 2);
+              for (int j = 0; j < bn / 128; ++j) {
+                tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow);
+                tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, n0 + 64 * j, krow);
+              }
+            } else {
+              const int n0 = tl.n * bn;
+              for (int j = 0; j < bn / 64; ++j)
+                tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow);
+            }
+          } else {                           // K-major B: one box of bn rows
+            const int nrow = tl.e * p.b_rows + tl.n * bn;
+            if (p.b_split == 2 && kb >= p.k_split)
+              tma_load_2d(sb, &tmB1, full, (kb - p.k_split) * BK, nrow);
+            else
+              tma_load_2d(sb, &tmB0, full, kb * BK, nrow);
           }
           last_par[stage] = phase;
           used[stage] = true;
@@ -171,20 +239,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kTileM, bn, false, true);
+      const uint32_t idesc = idesc_bf16(kTileM, bn, kAmn, kBmn);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<kSched>(t, ts, p);
         if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * 256;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
           if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.wait_ns, abort_flag)) {
             ok = false;
             break;
@@ -194,11 +263,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = a0 + kABytes;
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
-            // A: K-major, 128B swizzle, 8-row groups 1024 B apart; +32 B per K=16.
-            const uint64_t ad = sdesc_sw128(a0 + ks * 32, 16, 1024);
-            // B: N-major, 128B swizzle; 64-column atoms 8 KB apart (LBO),
-            // 8-row K groups 1024 B apart (SBO); +16 rows = 2 KB per K=16.
-            const uint64_t bd = sdesc_sw128(b0 + ks * 2048, kBBox, 1024);
+            // K-major, 128B swizzle: 8-row groups 1024 B apart, +32 B per K=16.
+            // MN-major, 128B swizzle: 64-wide atoms 8 KB apart (LBO), 8-row K
+            // groups 1024 B apart (SBO), +16 rows = 2 KB per K=16.
+            const uint64_t ad = kAmn ? sdesc_sw128(a0 + ks * 2048, kBBox, 1024)
+                                     : sdesc_sw128(a0 + ks * 32, 16, 1024);
+            const uint64_t bd = kBmn ? sdesc_sw128(b0 + ks * 2048, kBBox, 1024)
+                                     : sdesc_sw128(b0 + ks * 32, 16, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | ks) ? 1u : 0u);
           }
           umma_commit(smem_u32(&sm->empty[stage]));
@@ -209,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&sm->tfull[acc]));
+        umma_commit(smem_u32(&sm->tfull[acc]));   // also for a tile with no k-block
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
@@ -229,9 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, m, n;
-      decode_tile(t, ts, p.off_al, E, e, m, n);
-      const int64_t grow = p.off_al[e] + m * kTileM + row_in_tile;
+      const Tile tl = decode_tile<kSched>(t, ts, p);
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       // tcgen05.ld is warp-collective: the whole warp goes on or stops together
       if (!__all_sync(0xffffffffu, got)) {
@@ -241,13 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
-      if (kSwiglu) {
-        __nv_bfloat16* out = p.out + grow * p.N + n * p.bn;
+      if (kEpi == Epi::SwigluFwd) {
+        const int64_t grow = tl.row0 + row_in_tile;
+        const int n0 = tl.n * (bn / 2);
+        __nv_bfloat16* out = p.out + grow * p.ldo + n0;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 0; c < bn / 2; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(taddr + c, g);
-          tmem_ld_32x32b_x32(taddr + 128 + c, u);
+          tmem_ld_32x32b_x32(taddr + bn / 2 + c, u);
           tmem_ld_wait();
           uint32_t hw[16];
 #pragma unroll
@@ -260,37 +331,99 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 4; ++i)
             st_global_v4(out + c + 8 * i, hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
           if (p.save_g) {
-            __nv_bfloat16* og = p.save_g + grow * p.N + n * p.bn + c;
-            __nv_bfloat16* ou = p.save_u + grow * p.N + n * p.bn + c;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              st_global_v4(og + 8 * i,
-                           pack_bf16x2(__uint_as_float(g[8 * i]), __uint_as_float(g[8 * i + 1])),
-                           pack_bf16x2(__uint_as_float(g[8 * i + 2]), __uint_as_float(g[8 * i + 3])),
-                           pack_bf16x2(__uint_as_float(g[8 * i + 4]), __uint_as_float(g[8 * i + 5])),
-                           pack_bf16x2(__uint_as_float(g[8 * i + 6]), __uint_as_float(g[8 * i + 7])));
-              st_global_v4(ou + 8 * i,
-                           pack_bf16x2(__uint_as_float(u[8 * i]), __uint_as_float(u[8 * i + 1])),
-                           pack_bf16x2(__uint_as_float(u[8 * i + 2]), __uint_as_float(u[8 * i + 3])),
-                           pack_bf16x2(__uint_as_float(u[8 * i + 4]), __uint_as_float(u[8 * i + 5])),
-                           pack_bf16x2(__uint_as_float(u[8 * i + 6]), __uint_as_float(u[8 * i + 7])));
-            }
+            store_bf16x32(p.save_g + grow * p.ldo + n0 + c, g);
+            store_bf16x32(p.save_u + grow * p.ldo + n0 + c, u);
           }
         }
-      } else {
-        __nv_bfloat16* out = p.out + grow * p.N + n * p.bn;
+      } else if (kEpi == Epi::Bf16) {
+        const int64_t grow = tl.row0 + row_in_tile;
+        __nv_bfloat16* out = p.out + grow * p.ldo + tl.n * bn;
 #pragma unroll 1
         for (int c = 0; c < bn; c += 32) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c, r);
           tmem_ld_wait();
+          store_bf16x32(out + c, r);
+        }
+      } else if (kEpi == Epi::SwigluBwd) {
+        // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s), s = sigmoid(A_g)
+        const int64_t grow = tl.row0 + row_in_tile;
+        const int f0 = tl.n * bn;
+        const __nv_bfloat16* ag = p.act_g + grow * p.ld_act + f0;
+        const __nv_bfloat16* au = p.act_u + grow * p.ld_act + f0;
+        __nv_bfloat16* dg = p.out + grow * p.ldo + f0;
+        __nv_bfloat16* du = p.out + grow * p.ldo + p.out_split + f0;
+#pragma unroll 1
+        for (int c = 0; c < bn; c += 32) {
+          uint32_t r[32];
+          float fg[32], fu[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          load_bf16x32(ag + c, fg);
+          load_bf16x32(au + c, fu);
+          tmem_ld_wait();
+          uint32_t wg[16], wu[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_global_v4(out + c + 8 * i,
-                         pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+          for (int i = 0; i < 16; ++i) {
+            float vg[2], vu[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float dh = __uint_as_float(r[2 * i + h]);
+              const float a = fg[2 * i + h], b = fu[2 * i + h];
+              const float s = 1.0f / (1.0f + __expf(-a));
+              vg[h] = dh * b * s * (1.0f + a * (1.0f - s));
+              vu[h] = dh * a * s;
+            }
+            wg[i] = pack_bf16x2(vg[0], vg[1]);
+            wu[i] = pack_bf16x2(vu[0], vu[1]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            st_global_v4(dg + c + 8 * i, wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
+            st_global_v4(du + c + 8 * i, wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
+          }
+        }
+      } else {  // Epi::F32: float rows (Rows) or weight-gradient rows (WGrad)
+        float* out;
+        if (kSched == Sched::Rows) {
+          out = p.outf + (tl.row0 + row_in_tile) * p.ldo + tl.n * bn;
+        } else {
+          const int64_t wrow = static_cast<int64_t>(tl.m) * kTileM + row_in_tile;
+          int col = tl.n * bn;
+          float* base = p.outf;
+          int ldn = p.N;
+          if (p.out_split > 0) {             // two outputs side by side along N
+            ldn = p.out_split;
+            if (col >= p.out_split) {
+              base = p.outf2;
+              col -= p.out_split;
+            }
+          }
+          out = base + (static_cast<int64_t>(tl.e) * p.M + wrow) * ldn + col;
+        }
+#pragma unroll 1
+        for (int c = 0; c < bn; c += 32) {
+          uint32_t r[32];
+          if (tl.kblocks > 0) {
+            tmem_ld_32x32b_x32(taddr + c, r);
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = 0u;   // an expert without rows
+          }
+          float4* o4 = reinterpret_cast<float4*>(out + c);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            if (p.accumulate) {
+              const float4 old = o4[i];
+              v.x += old.x;
+              v.y += old.y;
+              v.z += old.z;
+              v.w += old.w;
+            }
+            o4[i] = v;
+          }
         }
       }
       tc_fence_before();
@@ -313,21 +446,21 @@ size_t gemm_smem_bytes(int stages, int E) {
          static_cast<size_t>(E + 1) * sizeof(int);
 }
 
-template <bool kSwiglu>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const GroupedGemmArgs& p, int grid, cudaStream_t st) {
   // always the 4-stage size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
-  const size_t smem = gemm_smem_bytes(4, p.E);
-  static size_t configured = 0;
-  if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<kSwiglu>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(gemm_smem_bytes(4, kMaxExperts)));
+  const size_t smem = gemm_smem_bytes(4, kMaxExperts);
+  static bool configured = false;
+  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched>;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = gemm_smem_bytes(4, kMaxExperts);
+    configured = true;
   }
-  grouped_gemm_kernel<kSwiglu><<<grid, kThreads, smem, st>>>(a, b0, b1, p);
+  kern<<<grid, kThreads, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -335,12 +468,27 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                               const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_impl<true>(a, wg, wu, p, grid, st);
+  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows>(a, wg, wu, p, grid, st);
 }
 
 cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
                        int grid, cudaStream_t st) {
-  return launch_impl<false>(a, w, w, p, grid, st);
+  return launch_impl<Epi::Bf16, false, true, Sched::Rows>(a, w, w, p, grid, st);
+}
+
+cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2,
+                                 const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::SwigluBwd, false, false, Sched::Rows>(a, w2, w2, p, grid, st);
+}
+
+cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                       const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::F32, false, false, Sched::Rows>(a, wg, wu, p, grid, st);
+}
+
+cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GroupedGemmArgs& p,
+                         int grid, cudaStream_t st) {
+  return launch_impl<Epi::F32, true, true, Sched::WGrad>(a, b, b, p, grid, st);
 }
 
 }  // namespace moe

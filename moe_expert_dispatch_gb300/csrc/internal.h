@@ -54,21 +54,49 @@ cudaError_t launch_zero_padding(const int32_t* counts, const int32_t* off_al, in
 cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
                              int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st);
 
+// dX[t] = bf16(sum_j dxp[row_of[t, j]]) over float rows (j in order).
+cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_t T, int k, int H,
+                                 __nv_bfloat16* dx, cudaStream_t st);
+
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
                                   uint8_t* scales, cudaStream_t st);
 
 // ------------------------------------------------------------------ grouped GEMMs
 
+// Epilogue of a grouped GEMM.
+enum class Epi {
+  SwigluFwd,  // fc1: out = bf16(silu(gate) * up); gate/up are the two halves of the N tile
+  Bf16,       // out = bf16(acc)
+  SwigluBwd,  // dH -> dA_g, dA_u (bf16) from the saved A_g, A_u
+  F32,        // float output: rows (Rows schedule) or weight gradients (WGrad), optionally
+              // accumulated
+};
+// Tile schedule: M tiles over the routed rows of each expert (fixed K), or
+// over the rows of each expert's weight gradient (K = the expert's rows).
+enum class Sched { Rows, WGrad };
+
 struct GroupedGemmArgs {
   const int32_t* off_al;   // [E+1] expert row offsets, multiples of kTileM
   int E;
-  int K;                   // reduction length
-  int N;                   // output columns
-  int bn;                  // N tile (fc1: 128 per gate/up; fc2: 128 or 256)
+  int K;                   // Rows: reduction length
+  int M;                   // WGrad: rows of one expert's output (H or F)
+  int N;                   // output columns (logical)
+  int bn;                  // MMA N: 128 or 256
   int stages;              // ring depth 1..4
-  __nv_bfloat16* out;      // [rows, N]
-  __nv_bfloat16* save_g;   // fc1: optional bf16 copy of A_g
+  int64_t b_rows;          // rows of one expert in B's 2D view
+  int b_split;             // 0; 1: N tile = [B0 cols | B1 cols] (gate | up); 2: K split at k_split
+  int k_split;             // k-blocks read from B0 when b_split == 2
+  __nv_bfloat16* out;      // bf16 output
+  int64_t ldo;             // row stride of out (elements)
+  __nv_bfloat16* save_g;   // fc1: optional bf16 copy of A_g (stride ldo)
   __nv_bfloat16* save_u;   // fc1: optional bf16 copy of A_u
+  const __nv_bfloat16* act_g;  // SwigluBwd: saved A_g
+  const __nv_bfloat16* act_u;  // SwigluBwd: saved A_u
+  int64_t ld_act;
+  int out_split;           // SwigluBwd: column offset of dA_u in out; F32: columns of outf
+  float* outf;             // F32 output: Rows [rows, ldo]; WGrad [E, M, N or out_split]
+  float* outf2;            // F32 second output (columns >= out_split)
+  int accumulate;          // F32: add to the existing values
   int* err;
   unsigned long long wait_ns;
 };
@@ -83,6 +111,20 @@ cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const
 // fc2: out = bf16(A W).
 cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
                        int grid, cudaStream_t st);
+// backward: dH = dO W2^T with the SwiGLU-backward epilogue (W2 read K-major).
+cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2,
+                                 const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// backward: dXp = [dA_g | dA_u] [W1g ; W1u]^T in float (K split between the two weights).
+cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                       const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// backward: dW_e = A_e^T B_e over each expert's rows, both operands MN-major.
+cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GroupedGemmArgs& p,
+                         int grid, cudaStream_t st);
+
+// backward: dO[r] = bf16(prob_of[r] dY[token_of[r]]) and dprobs[t, j] = <dY_t, O[row_of[t, j]]>.
+cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const int32_t* row_of,
+                        const float* probs, int64_t T, int k, int H, __nv_bfloat16* d_o,
+                        float* dprobs, cudaStream_t st);
 
 int device_sm_count();
 

@@ -331,6 +331,126 @@ cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, cons
   return cudaGetLastError();
 }
 
+// One warp per token over float rows: dx[t] = bf16(sum_j dxp[row_j]), j in
+// order; 4 floats per lane per step.
+__global__ void __launch_bounds__(256) unpermute_f32_kernel(const float* __restrict__ dxp,
+                                                            const int32_t* __restrict__ row_of,
+                                                            int64_t T, int k, int H,
+                                                            __nv_bfloat16* __restrict__ dx) {
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n4 = H >> 2;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    for (int base = 0; base < n4; base += 32) {     // warp-uniform trip count
+      const int c = base + lane;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0 || c >= n4) continue;
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r) * H) + c);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      if (c < n4) {
+        uint2 w;
+        w.x = pack_bf16x2(acc.x, acc.y);
+        w.y = pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2*>(dx + t * H)[c] = w;
+      }
+    }
+  }
+}
+
+cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_t T, int k, int H,
+                                 __nv_bfloat16* dx, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  unpermute_f32_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(dxp, row_of, T, k, H, dx);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ backward: dO, dprobs
+
+// One warp per token t: for each of its slots j (8 at a time) the warp
+// streams dY_t once and O[row_j]: dO[row_j] = bf16(p_tj dY_t) and
+// dprobs[t, j] = <dY_t, O[row_j]> (float, reduced across the warp).
+__global__ void __launch_bounds__(256) dout_kernel(const __nv_bfloat16* __restrict__ dy,
+                                                   const __nv_bfloat16* __restrict__ o,
+                                                   const int32_t* __restrict__ row_of,
+                                                   const float* __restrict__ probs, int64_t T,
+                                                   int k, int H, __nv_bfloat16* __restrict__ d_o,
+                                                   float* __restrict__ dprobs) {
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int n8 = H >> 3;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    const float my_p = lane < k ? __ldg(probs + t * k + lane) : 0.0f;
+    const int4* g4 = reinterpret_cast<const int4*>(dy + t * H);
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      float dot[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dot[q] = 0.0f;
+      for (int base = 0; base < n8; base += 32) {   // warp-uniform trip count
+        const int c = base + lane;
+        float gf[8];
+        if (c < n8) {
+          const int4 g = ld_stream(g4 + c);
+          const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(h[q]);
+            gf[2 * q] = f.x;
+            gf[2 * q + 1] = f.y;
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          const int j = j0 + jj;
+          if (j >= k) break;
+          const int r = __shfl_sync(0xffffffffu, my_row, j);
+          const float p = __shfl_sync(0xffffffffu, my_p, j);
+          if (r < 0 || c >= n8) continue;
+          const int4 ov = ld_stream(reinterpret_cast<const int4*>(o + static_cast<int64_t>(r) * H) + c);
+          const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&ov);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 f = __bfloat1622float2(oh[q]);
+            dot[jj] = fmaf(gf[2 * q], f.x, dot[jj]);
+            dot[jj] = fmaf(gf[2 * q + 1], f.y, dot[jj]);
+          }
+          int4 w;
+          w.x = static_cast<int>(pack_bf16x2(p * gf[0], p * gf[1]));
+          w.y = static_cast<int>(pack_bf16x2(p * gf[2], p * gf[3]));
+          w.z = static_cast<int>(pack_bf16x2(p * gf[4], p * gf[5]));
+          w.w = static_cast<int>(pack_bf16x2(p * gf[6], p * gf[7]));
+          reinterpret_cast<int4*>(d_o + static_cast<int64_t>(r) * H)[c] = w;
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        float v = dot[jj];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        const int j = j0 + jj;
+        if (lane == 0 && j < k) dprobs[t * k + j] = v;
+      }
+    }
+  }
+}
+
+cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const int32_t* row_of,
+                        const float* probs, int64_t T, int k, int H, __nv_bfloat16* d_o,
+                        float* dprobs, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  dout_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(dy, o, row_of, probs, T, k, H, d_o, dprobs);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ MXFP8 quantiser
 
 // floor(log2(a)) of a positive finite float, subnormals included.

@@ -38,8 +38,9 @@ the definition:
 Readings where the pages are silent (listed with the rest in the design
 notes): h rounded to bf16 (A_g, A_u not rounded in the forward); O rounded to
 bf16 before the combine; the combine sums j in order, then rounds once;
-backward uses A_g, A_u as saved in bf16; dW is float (here float64, on the
-GPU float32); in MXFP8 mode h is first rounded to bf16 then quantised per 32
+backward uses A_g, A_u as saved in bf16 and keeps dXp unrounded (it feeds no
+further matmul; dX = bf16 of its k-way sum); dW is float (here float64, on
+the GPU float32); in MXFP8 mode h is first rounded to bf16 then quantised per 32
 along F.
 
 Every function here is pinned by tests against something other than itself
@@ -283,7 +284,7 @@ def expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, rounding: bo
       dH     = dO_e W2_e^T
       dA_g   = bf16(dH * A_u * sigma(A_g) (1 + A_g (1 - sigma(A_g))))
       dA_u   = bf16(dH * silu(A_g))
-      dXp    = bf16(dA_g W1g_e^T + dA_u W1u_e^T)
+      dXp    = dA_g W1g_e^T + dA_u W1u_e^T        (not rounded)
       dW2_e  = h_e^T dO_e,  dW1g_e = Xp_e^T dA_g,e,  dW1u_e = Xp_e^T dA_u,e
       dX_t   = bf16(sum_j dXp[row_of[t, j]])
 
@@ -319,7 +320,7 @@ def expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, rounding: bo
         sg = sigmoid(a_g[lo:hi])
         da_g = rnd(dh * a_u[lo:hi] * sg * (1.0 + a_g[lo:hi] * (1.0 - sg)))
         da_u = rnd(dh * a_g[lo:hi] * sg)
-        dxp[lo:hi] = rnd(da_g @ _f64(w_gate[e]).T + da_u @ _f64(w_up[e]).T)
+        dxp[lo:hi] = da_g @ _f64(w_gate[e]).T + da_u @ _f64(w_up[e]).T
         dw_down[e] = h[lo:hi].T @ d_o[lo:hi]
         dw_gate[e] = xp[lo:hi].T @ da_g
         dw_up[e] = xp[lo:hi].T @ da_u
@@ -332,45 +333,51 @@ def backward_rows(dy, x, w_gate, w_up, w_down, expert_ids, probs, tokens):
 
     Each token's gradient depends only on its own rows, so this is the same
     arithmetic as expert_backward restricted to those rows; it lets the
-    full-size workloads be checked on a sample of tokens.
+    full-size workloads be checked on a sample of tokens. Experts are
+    visited one at a time so that each expert's weights are converted once.
     """
     dy = _f64(dy)
     x = np.asarray(x)
     ids = np.asarray(expert_ids)
     pr = np.asarray(probs)
-    dx = []
-    dp = []
+    tokens = list(tokens)
+    dxr, dpt = {}, {}
+    for e in sorted(set(int(v) for t in tokens for v in ids[t])):
+        wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
+        for t in tokens:
+            for j, ee in enumerate(ids[t].tolist()):
+                if ee != e:
+                    continue
+                xt = _f64(x[t])
+                g = xt @ wg
+                u = xt @ wu
+                hv = bf16(silu(g) * u)
+                ov = bf16(hv @ wd)
+                dpt[(t, j)] = float(np.dot(dy[t], ov))
+                d_o = bf16(float(pr[t, j]) * dy[t])
+                dh = wd @ d_o
+                ga, ua = bf16(g), bf16(u)
+                sg = sigmoid(ga)
+                da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
+                da_u = bf16(dh * ga * sg)
+                dxr[(t, j)] = wg @ da_g + wu @ da_u
+    k = ids.shape[1]
+    dx, dp = [], []
     for t in tokens:
-        acc = None
-        dpt = []
-        for j, e in enumerate(ids[t].tolist()):
-            xt = _f64(x[t])
-            g = xt @ _f64(w_gate[e])
-            u = xt @ _f64(w_up[e])
-            hv = bf16(silu(g) * u)
-            ov = bf16(hv @ _f64(w_down[e]))
-            dpt.append(float(np.dot(dy[t], ov)))
-            d_o = bf16(float(pr[t, j]) * dy[t])
-            dh = _f64(w_down[e]) @ d_o
-            ga, ua = bf16(g), bf16(u)
-            sg = sigmoid(ga)
-            da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
-            da_u = bf16(dh * ga * sg)
-            dxr = bf16(_f64(w_gate[e]) @ da_g + _f64(w_up[e]) @ da_u)
-            acc = dxr if acc is None else acc + dxr
+        acc = dxr[(t, 0)]
+        for j in range(1, k):
+            acc = acc + dxr[(t, j)]
         dx.append(bf16(acc))
-        dp.append(dpt)
+        dp.append([dpt[(t, j)] for j in range(k)])
     return np.stack(dx), np.array(dp)
 
 
-def weight_grad_columns(dy, x, w_gate, w_up, w_down, expert_ids, probs, e, f_cols, h_cols):
-    """Exact columns of the weight gradients of expert e:
-    dW1g_e[:, f], dW1u_e[:, f] for f in f_cols (each over all H), and
-    dW2_e[:, h] for h in h_cols (each over all F).
-
-    Each column needs only the rows routed to e, so this is expert_backward's
-    arithmetic restricted to those columns.
-    """
+def weight_grad_columns(dy, x, w_gate, w_up, w_down, expert_ids, probs, e, f_cols):
+    """Exact slices of the weight gradients of expert e for each f in f_cols:
+    the columns dW1g_e[:, f] and dW1u_e[:, f] (over all H) and the row
+    dW2_e[f, :] (over all H). Each needs only column f of A_g, A_u and dH
+    over the rows routed to e, so this is expert_backward's arithmetic
+    restricted to those columns."""
     ids = np.asarray(expert_ids)
     pr = np.asarray(probs)
     dy = _f64(dy)
@@ -378,27 +385,23 @@ def weight_grad_columns(dy, x, w_gate, w_up, w_down, expert_ids, probs, e, f_col
     slots = np.nonzero(flat == e)[0]
     k = ids.shape[1]
     toks, js = slots // k, slots % k
-    xe = _f64(np.asarray(x)[toks])                       # rows of expert e in permuted order
+    cols = list(f_cols)
+    xe = _f64(np.asarray(x)[toks])                        # rows of expert e
     p = pr[toks, js].astype(np.float64)
     d_o = bf16(p[:, None] * dy[toks])
-    wg, wu, wd = _f64(w_gate[e]), _f64(w_up[e]), _f64(w_down[e])
-    a_g = xe @ wg
+    wg, wu, wd = _f64(np.asarray(w_gate[e])[:, cols]), _f64(np.asarray(w_up[e])[:, cols]), \
+        _f64(np.asarray(w_down[e])[cols])
+    a_g = xe @ wg                                         # [c_e, len(cols)]
     a_u = xe @ wu
-    out = {}
-    cols = list(f_cols)
-    if cols:
-        dh = d_o @ wd[cols].T                             # [c_e, len(cols)]
-        ga, ua = bf16(a_g[:, cols]), bf16(a_u[:, cols])
-        sg = sigmoid(ga)
-        da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
-        da_u = bf16(dh * ga * sg)
-        out["dw_gate"] = xe.T @ da_g                     # [H, len(cols)]
-        out["dw_up"] = xe.T @ da_u
-    hc = list(h_cols)
-    if hc:
-        h = bf16(silu(a_g) * a_u)
-        out["dw_down"] = h.T @ d_o[:, hc]                # [F, len(hc)]
-    return out
+    dh = d_o @ wd.T
+    ga, ua = bf16(a_g), bf16(a_u)
+    sg = sigmoid(ga)
+    da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
+    da_u = bf16(dh * ga * sg)
+    h = bf16(silu(a_g) * a_u)
+    return {"dw_gate": xe.T @ da_g,                       # [H, len(cols)]
+            "dw_up": xe.T @ da_u,
+            "dw_down": h.T @ d_o}                         # [len(cols), H]
 
 
 # --------------------------------------------------------------------------

@@ -320,10 +320,10 @@ def test_backward_sampled_helpers_agree():
     np.testing.assert_allclose(dx, g["dx"][toks], rtol=2 ** -7, atol=1e-9)
     np.testing.assert_allclose(dp, g["dprobs"][toks], rtol=1e-9, atol=1e-12)
     for e in (0, 2):
-        c = orc.weight_grad_columns(dy, x, wg, wu, wd, ids, probs, e, [1, 5], [0, 9])
-        np.testing.assert_allclose(c["dw_gate"], g["dw_gate"][e][:, [1, 5]], rtol=1e-9, atol=1e-12)
-        np.testing.assert_allclose(c["dw_up"], g["dw_up"][e][:, [1, 5]], rtol=1e-9, atol=1e-12)
-        np.testing.assert_allclose(c["dw_down"], g["dw_down"][e][:, [0, 9]], rtol=1e-9, atol=1e-12)
+        c = orc.weight_grad_columns(dy, x, wg, wu, wd, ids, probs, e, [1, 5, 23])
+        np.testing.assert_allclose(c["dw_gate"], g["dw_gate"][e][:, [1, 5, 23]], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(c["dw_up"], g["dw_up"][e][:, [1, 5, 23]], rtol=1e-9, atol=1e-12)
+        np.testing.assert_allclose(c["dw_down"], g["dw_down"][e][[1, 5, 23], :], rtol=1e-9, atol=1e-12)
     assert np.all(g["dw_gate"][1] == 0) and np.all(g["dw_down"][1] == 0)
 
 
