@@ -1,11 +1,19 @@
 """Benchmark of the GB300 MoE expert block.
 
-One step = one pass of the whole forward hot path (counts, offsets, row map,
-permute, grouped fc1 + SwiGLU, grouped fc2, unpermute) over one batch of the
-Mixtral-8x7B-shaped workload (T=4096 tokens, H=4096, F=14336, 8 experts,
-top-2), seeded synthetic inputs resident in HBM. L2 is flushed (a 512 MB
-write, untimed) before every timed step; each step is bracketed by CUDA
-events on the launching stream.
+One step = one pass of the whole hot path over one batch of a workload, with
+seeded synthetic inputs resident in HBM:
+  * BF16 forward (default: the Mixtral-8x7B-shaped layer, T=4096 tokens,
+    H=4096, F=14336, 8 experts, top-2): counts, offsets, row map, permute,
+    grouped fc1 + SwiGLU, grouped fc2, unpermute;
+  * MXFP8 forward (--workload mxfp8): the same with x quantised while it is
+    permuted, block-scaled GEMMs and h quantised in fc1's epilogue (weights
+    quantised once, outside the timed region, as a deployment would);
+  * BF16 training step (--workload train_bf16): forward (saving what the
+    backward needs) + backward (dX, dW1gate, dW1up, dW2, dprobs).
+L2 is flushed (a 512 MB write, untimed) before every timed step; each step
+is bracketed by CUDA events on the launching stream, and the library records
+events at its own step boundaries on the same stream (moe_config.step_events)
+for the per-kernel times and the roofline.
 
 Prints ONE JSON line (rank 0). `--impl reference` times the CPU oracle on a
 bounded sample of the same workload instead.
@@ -27,15 +35,17 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-# DRAM bytes (read + write) of one fc1 launch on the default workload, from
-# the ncu capture summarised in profiles/; null once the kernel source changes.
-FC1_TRAFFIC = {"bytes": None, "src_sha": None}
+# DRAM bytes (read + write) per launch of the dominant kernel on a workload,
+# from the ncu captures summarised in profiles/, with the hash of the kernel
+# source they were taken on; reported as null once that source changes.
+TRAFFIC = {}
+FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
 def _sha_of_kernel_sources():
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_bf16.cu", "common.cuh"):
+    for f in ("gemm_bf16.cu", "gemm_mxfp8.cu", "common.cuh", "mx.cuh"):
         with open(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -45,9 +55,9 @@ def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained"), "measured"
+        return p["hbm_gbs"], p["bf16_tflops"], "measured"
     except Exception:
-        return 6800.0, 1900.0, 1700.0, "fallback"
+        return 6800.0, 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -73,7 +83,7 @@ class ClockSampler:
                     self.samples.append([v.strip() for v in out.split(",")])
             except Exception:
                 pass
-            self._stop.wait(0.1)
+            self._stop.wait(0.05)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
@@ -87,8 +97,9 @@ class ClockSampler:
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        num = lambda v: v.replace(".", "", 1).isdigit()  # noqa: E731
+        sm = [float(s[0]) for s in self.samples if num(s[0])]
+        mx = [float(s[1]) for s in self.samples if num(s[1])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in self.samples for i in range(4)
                           if len(s) > 3 + i and s[3 + i].lower() == "active"})
@@ -98,10 +109,8 @@ class ClockSampler:
 
 
 def _dist():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def _max_over_ranks(v: float, ws: int, device):
@@ -120,32 +129,43 @@ def _barrier(ws):
         dist.barrier()
 
 
+# ---------------------------------------------------------------- CPU oracle sample
+
 def cpu_oracle_sample(w, inp, n_tokens: int):
     """Time the oracle (as it stands) on n_tokens sampled tokens of the workload."""
     import oracle as orc
     toks = list(range(n_tokens))
+    f32 = synth.F32Slices
     t0 = time.perf_counter()
-    orc.sampled_forward(inp["x"].float().numpy(), synth.F32Slices(inp["w_gate"]),
-                        synth.F32Slices(inp["w_up"]), synth.F32Slices(inp["w_down"]),
-                        inp["expert_ids"].numpy(), inp["probs"].numpy(), toks)
+    if w.mxfp8:
+        orc.sampled_forward_mxfp8(inp["x"].float().numpy(), f32(inp["w_gate_t"]),
+                                  f32(inp["w_up_t"]), f32(inp["w_down_t"]),
+                                  inp["expert_ids"].numpy(), inp["probs"].numpy(), toks)
+        what = "MXFP8 forward"
+    elif w.backward:
+        orc.backward_rows(inp["dy"].float().numpy(), inp["x"].float().numpy(),
+                          f32(inp["w_gate"]), f32(inp["w_up"]), f32(inp["w_down"]),
+                          inp["expert_ids"].numpy(), inp["probs"].numpy(), toks)
+        what = "forward + backward (dX, dprobs)"
+    else:
+        orc.sampled_forward(inp["x"].float().numpy(), f32(inp["w_gate"]), f32(inp["w_up"]),
+                            f32(inp["w_down"]), inp["expert_ids"].numpy(), inp["probs"].numpy(),
+                            toks)
+        what = "forward"
     dt = time.perf_counter() - t0
     return {"value": n_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
             "kind": "oracle", "seconds": dt,
-            "sample": f"{n_tokens} tokens of {w.name} (T={w.T}), per-token float64 loop, "
-                      "NumPy BLAS threads"}
+            "sample": f"{what} of {n_tokens} tokens of {w.name} (T={w.T}), float64, "
+                      "one expert's weights converted at a time, NumPy BLAS threads"}
 
 
 def run_reference(args, w):
-    ws, rank, _ = _dist()
+    _, rank, _ = _dist()
     if rank != 0:
         return 0
     inp = synth.make_inputs(w, 0)
-    times = []
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state worth discarding beyond the first call
-    for _ in range(args.steps):
-        r = cpu_oracle_sample(w, inp, args.ref_tokens)
-        times.append(r["seconds"])
+    times = [cpu_oracle_sample(w, inp, args.ref_tokens)["seconds"]
+             for _ in range(max(1, args.steps))]
     sec_per_token = float(np.mean(times)) / args.ref_tokens
     value = 1.0 / sec_per_token
     line = {"impl": "reference", "metric": "MoE expert-block tokens/s", "value": value,
@@ -162,6 +182,94 @@ def run_reference(args, w):
     return 0
 
 
+# ---------------------------------------------------------------- GPU runs
+
+class Runner:
+    """The timed step of one workload kind, its per-kernel events and FLOPs."""
+
+    def __init__(self, m, w, inp, device):
+        import torch
+        self.m, self.w, self.dev = m, w, device
+        T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
+        R = T * k
+        self.x = inp["x"].to(device)
+        self.ids, self.probs = inp["expert_ids"].to(device), inp["probs"].to(device)
+        self.y = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+        self.stream = torch.cuda.current_stream()
+        mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]  # noqa: E731
+        self.fev = mk(m.STEP_EVENTS)
+        self.bev = mk(m.BWD_STEP_EVENTS) if w.backward else []
+        for e in self.fev + self.bev:
+            e.record(self.stream)
+        if w.mxfp8:
+            self.wq = []
+            for key in ("w_gate_t", "w_up_t", "w_down_t"):
+                q, s = m.moe_quantize_mxfp8(inp[key].to(device))
+                self.wq += [q, s]
+            self.cfg = m.config()
+            self.cfg_ev = m.config(step_events=self.fev)
+            nbytes = m.moe_workspace_size_mxfp8(T, H, F, E, k, self.cfg)
+            self.dtype = "mxfp8 (e4m3 + e8m0 per 32; bf16 out)"
+            self.launches = 9
+        else:
+            self.wg, self.wu, self.wd = (inp[key].to(device) for key in ("w_gate", "w_up", "w_down"))
+            save = bool(w.backward)
+            self.cfg = m.config(save_for_backward=save)
+            self.cfg_ev = m.config(save_for_backward=save, step_events=self.fev)
+            nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
+            self.dtype = "bf16"
+            self.launches = 7
+            if w.backward:
+                self.dy = inp["dy"].to(device)
+                self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev)
+                self.bws = torch.empty(m.moe_workspace_size(T, H, F, E, k, self.cfg, True),
+                                       dtype=torch.uint8, device=device)
+                self.grads = dict(
+                    dx=torch.empty_like(self.x),
+                    dw_gate=torch.empty((E, H, F), dtype=torch.float32, device=device),
+                    dw_up=torch.empty((E, H, F), dtype=torch.float32, device=device),
+                    dw_down=torch.empty((E, F, H), dtype=torch.float32, device=device),
+                    dprobs=torch.empty((T, k), dtype=torch.float32, device=device))
+                self.launches = 8 + 7
+        self.work = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        # per-kernel FLOPs of the grouped GEMMs (algorithmic: routed rows only)
+        self.flops = {"fc1_swiglu": 4.0 * R * H * F, "fc2": 2.0 * R * F * H}
+        if w.backward:
+            self.flops.update({"dH_swiglu_bwd": 2.0 * R * H * F, "dXp": 4.0 * R * H * F,
+                               "dW1": 4.0 * R * H * F, "dW2": 2.0 * R * F * H})
+
+    def step(self, events: bool, x=None, ids=None, probs=None, dy=None):
+        m = self.m
+        x = self.x if x is None else x
+        ids = self.ids if ids is None else ids
+        probs = self.probs if probs is None else probs
+        if self.w.mxfp8:
+            m.moe_expert_forward_mxfp8(x, *self.wq, ids, probs, y=self.y, workspace=self.work,
+                                       cfg=self.cfg_ev if events else self.cfg)
+            return
+        m.moe_expert_forward(x, self.wg, self.wu, self.wd, ids, probs, y=self.y,
+                             workspace=self.work, cfg=self.cfg_ev if events else self.cfg)
+        if self.w.backward:
+            g = self.grads
+            m.moe_expert_backward(self.dy if dy is None else dy, x, self.wg, self.wu, self.wd,
+                                  ids, probs, self.work, dx=g["dx"], dw_gate=g["dw_gate"],
+                                  dw_up=g["dw_up"], dw_down=g["dw_down"], dprobs=g["dprobs"],
+                                  workspace=self.bws,
+                                  cfg=self.cfg_bev if events else self.cfg)
+
+    def parts(self):
+        """Per-kernel milliseconds of the last event-recorded step."""
+        f = self.fev
+        out = {"routing": f[0].elapsed_time(f[1]), "fc1_swiglu": f[1].elapsed_time(f[2]),
+               "fc2": f[2].elapsed_time(f[3]), "unpermute": f[3].elapsed_time(f[4])}
+        if self.bev:
+            b = self.bev
+            names = ["dO_dprobs", "dH_swiglu_bwd", "dXp", "dX", "dW1", "dW2"]
+            for i, n in enumerate(names):
+                out[n] = b[i].elapsed_time(b[i + 1])
+        return out
+
+
 def run_ours(args, w):
     import torch
     ws, rank, local = _dist()
@@ -173,26 +281,13 @@ def run_ours(args, w):
     import moe_expert_dispatch_gb300 as m
 
     inp = synth.make_inputs(w, 0)
-    x = inp["x"].to(device)
-    wg, wu, wd = (inp[k].to(device) for k in ("w_gate", "w_up", "w_down"))
-    ids, probs = inp["expert_ids"].to(device), inp["probs"].to(device)
-    stream = torch.cuda.current_stream()
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.STEP_EVENTS)]
-    for e in evs:
-        e.record(stream)
-    cfg = m.config()
-    cfg_ev = m.config(step_events=evs)
-    nbytes = m.moe_workspace_size(w.T, w.H, w.F, w.E, w.k, cfg)
-    work = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    y = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=device)
+    run = Runner(m, w, inp, device)
+    stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
-
-    def step(c):
-        m.moe_expert_forward(x, wg, wu, wd, ids, probs, y=y, workspace=work, cfg=c)
-
-    for _ in range(max(3, args.warmup)):
+    warm = max(3, args.warmup)
+    for _ in range(warm):
         flush.zero_()
-        step(cfg)
+        run.step(False)
     torch.cuda.synchronize()
     st = m.moe_get_error()
     if st != 0:
@@ -200,77 +295,90 @@ def run_ours(args, w):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    parts = np.zeros(m.STEP_EVENTS - 1)
+    parts = {}
     _barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
-            step(cfg_ev)
+            run.step(True)
             ends[i].record(stream)
-            evs[-1].synchronize()
-            parts += [evs[j].elapsed_time(evs[j + 1]) for j in range(m.STEP_EVENTS - 1)]
+            ends[i].synchronize()
+            for key, v in run.parts().items():
+                parts[key] = parts.get(key, 0.0) + v
         torch.cuda.synchronize()
     _barrier(ws)
-    ms = float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)]))
-    ms = _max_over_ranks(ms, ws, device)
-    parts /= args.steps
+    ms = _max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)])), ws,
+                         device)
+    parts = {key: v / args.steps for key, v in parts.items()}
     if m.moe_get_error() != 0:
         raise RuntimeError("device error during the timed region")
 
-    # end to end through the public call, host buffers: H2D of x/ids/probs,
-    # the block, D2H of y, every step
-    hx = inp["x"].pin_memory()
-    hids = inp["expert_ids"].pin_memory()
-    hprobs = inp["probs"].pin_memory()
-    hy = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
-    dx = torch.empty_like(x)
-    dids = torch.empty_like(ids)
-    dprobs = torch.empty_like(probs)
+    # end to end through the public calls with host buffers: H2D of the step's
+    # inputs, the block, D2H of its result, every step
+    pin = lambda t: t.pin_memory()  # noqa: E731
+    hx, hids, hprobs = pin(inp["x"]), pin(inp["expert_ids"]), pin(inp["probs"])
+    dx_, dids, dprobs = torch.empty_like(run.x), torch.empty_like(run.ids), torch.empty_like(run.probs)
     h2d = hx.numel() * 2 + hids.numel() * 4 + hprobs.numel() * 4
-    d2h = hy.numel() * 2
+    if w.backward:
+        hdy = pin(inp["dy"])
+        ddy = torch.empty_like(run.dy)
+        h2d += hdy.numel() * 2
+        hres = [torch.empty_like(run.grads["dx"], device="cpu").pin_memory(),
+                torch.empty_like(run.grads["dprobs"], device="cpu").pin_memory()]
+        dres = [run.grads["dx"], run.grads["dprobs"]]
+    else:
+        hres = [torch.empty_like(run.y, device="cpu").pin_memory()]
+        dres = [run.y]
+    d2h = sum(t.numel() * t.element_size() for t in hres)
     e2e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e2e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     for i in range(args.steps + 2):
         flush.zero_()
         if i >= 2:
             e2e_s[i - 2].record(stream)
-        dx.copy_(hx, non_blocking=True)
+        dx_.copy_(hx, non_blocking=True)
         dids.copy_(hids, non_blocking=True)
         dprobs.copy_(hprobs, non_blocking=True)
-        m.moe_expert_forward(dx, wg, wu, wd, dids, dprobs, y=y, workspace=work, cfg=cfg)
-        hy.copy_(y, non_blocking=True)
+        if w.backward:
+            ddy.copy_(hdy, non_blocking=True)
+        run.step(False, x=dx_, ids=dids, probs=dprobs, dy=ddy if w.backward else None)
+        for h, d in zip(hres, dres):
+            h.copy_(d, non_blocking=True)
         if i >= 2:
             e2e_e[i - 2].record(stream)
     torch.cuda.synchronize()
     e2e_ms = _max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e2e_s, e2e_e)])),
                              ws, device)
 
-    hbm, bf16_burst, bf16_sus, peak_src = _peaks()
-    R = w.T * w.k
-    fc1_flop = 4.0 * R * w.H * w.F
-    fc2_flop = 2.0 * R * w.F * w.H
-    fc1_tflops = fc1_flop / (parts[1] * 1e-3) / 1e12
-    traffic = FC1_TRAFFIC["bytes"] if FC1_TRAFFIC["src_sha"] == _sha_of_kernel_sources() else None
+    hbm, bf16_peak, peak_src = _peaks()
+    peak = bf16_peak * (FP8_OVER_BF16 if w.mxfp8 else 1.0)
+    tflops = {key: run.flops[key] / (parts[key] * 1e-3) / 1e12 for key in run.flops}
+    dominant = max(run.flops, key=lambda key: parts[key])
+    tr = TRAFFIC.get((w.name, dominant))
+    traffic = tr["bytes"] if tr and tr["src_sha"] == _sha_of_kernel_sources() else None
+    gemm_ms = sum(parts[key] for key in run.flops)
     line = {
         "metric": "MoE expert-block tokens/s", "value": ws * w.T / (ms * 1e-3),
-        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": max(3, args.warmup),
+        "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": warm,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": run.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
+                   "step": "forward + backward" if w.backward else "forward",
                    "l2": "flushed before every step (512 MB write)",
                    "parallelism": "replicas" if ws > 1 else "single"},
-        "roofline": {"bound": "tensor", "kernel": "fc1_swiglu (grouped GEMM)",
-                     "achieved": fc1_tflops, "peak": bf16_burst, "unit": "TFLOP/s",
-                     "frac": fc1_tflops / bf16_burst, "traffic": traffic,
-                     "peak_source": f"{peak_src} bf16 burst"},
-        "steps_ms": {"routing": parts[0], "fc1_swiglu": parts[1], "fc2": parts[2],
-                     "unpermute": parts[3]},
-        "grouped_gemm_tflops": (fc1_flop + fc2_flop) / ((parts[1] + parts[2]) * 1e-3) / 1e12,
+        "roofline": {"bound": "tensor", "kernel": f"{dominant} (grouped GEMM)",
+                     "achieved": tflops[dominant], "peak": peak, "unit": "TFLOP/s",
+                     "frac": tflops[dominant] / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} bf16 burst" + (" x 2 (nominal FP8/BF16)"
+                                                                 if w.mxfp8 else "")},
+        "steps_ms": parts,
+        "gemm_tflops": tflops,
+        "grouped_gemm_tflops": sum(run.flops.values()) / (gemm_ms * 1e-3) / 1e12,
         "e2e": {"value": ws * w.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": run.launches * args.steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -62,13 +62,17 @@ typedef struct moe_config {
   int fuse_gather;         /* 1: fc1 gathers routed rows of x itself instead of reading
                               a materialised permuted copy (default 0)                  */
   long long wait_limit_ns; /* bound of every in-kernel wait (default 0 = 2 s)           */
-  void** step_events;      /* optional: array of MOE_STEP_EVENTS cudaEvent_t (as void*),
-                              recorded on `stream` before the first step and after each
-                              step of moe_expert_forward: routing (counts, row map,
-                              permute), fc1+SwiGLU, fc2, unpermute. NULL = none.      */
+  void** step_events;      /* optional: array of num_step_events cudaEvent_t (as void*)
+                              recorded on `stream` at step boundaries; NULL = none.
+                              Forward (5): start, after routing (counts, row map,
+                              permute), fc1+SwiGLU, fc2, unpermute.
+                              Backward (7): start, after dO+dprobs, dH+SwiGLU
+                              backward, dXp, dX, dW1, dW2.                            */
+  int num_step_events;     /* entries of step_events (events past it are not recorded) */
 } moe_config;
 
 #define MOE_STEP_EVENTS 5
+#define MOE_BWD_STEP_EVENTS 7
 
 void moe_config_init(moe_config* cfg);
 

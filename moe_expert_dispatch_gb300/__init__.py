@@ -35,9 +35,11 @@ class moe_config(ctypes.Structure):
     _fields_ = [("ring_stages", ctypes.c_int), ("save_for_backward", ctypes.c_int),
                 ("num_sms", ctypes.c_int), ("fuse_gather", ctypes.c_int),
                 ("wait_limit_ns", ctypes.c_longlong),
-                ("step_events", ctypes.POINTER(ctypes.c_void_p))]
+                ("step_events", ctypes.POINTER(ctypes.c_void_p)),
+                ("num_step_events", ctypes.c_int)]
 
-STEP_EVENTS = 5   # routing, fc1+SwiGLU, fc2, unpermute: MOE_STEP_EVENTS boundaries
+STEP_EVENTS = 5       # forward: start, routing, fc1+SwiGLU, fc2, unpermute
+BWD_STEP_EVENTS = 7   # backward: start, dO+dprobs, dH, dXp, dX, dW1, dW2
 
 
 def _sig(name, res, *args):
@@ -114,10 +116,11 @@ def config(ring_stages=4, save_for_backward=False, num_sms=0, fuse_gather=False,
     if wait_limit_ns:
         c.wait_limit_ns = wait_limit_ns
     if step_events is not None:
-        assert len(step_events) == STEP_EVENTS
-        arr = (ctypes.c_void_p * STEP_EVENTS)(*[ev.cuda_event for ev in step_events])
+        n = len(step_events)
+        arr = (ctypes.c_void_p * n)(*[ev.cuda_event for ev in step_events])
         c._events_keepalive = arr
         c.step_events = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+        c.num_step_events = n
     return c
 
 
@@ -281,6 +284,11 @@ def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_work
                                     ws.numel(), ctypes.byref(c), _stream(stream)),
            "moe_expert_backward")
     return dict(dx=dx, dw_gate=dw_gate, dw_up=dw_up, dw_down=dw_down, dprobs=dprobs)
+
+
+def moe_workspace_size_mxfp8(T, H, F, E, k, cfg: moe_config | None = None) -> int:
+    c = cfg if cfg is not None else config()
+    return _lib.moe_workspace_size_mxfp8(T, H, F, E, k, ctypes.byref(c))
 
 
 def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, probs, y=None,

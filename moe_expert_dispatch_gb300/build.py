@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["route.cu", "gemm_bf16.cu", "capi.cu", "counts_static.cu"]
+SOURCES = ["route.cu", "gemm_bf16.cu", "gemm_mxfp8.cu", "capi.cu", "counts_static.cu"]
 
 
 def nvcc() -> str:

@@ -113,6 +113,43 @@ BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
   return B;
 }
 
+// MXFP8 forward workspace: the routing buffers of the BF16 layout, then the
+// codes and tiled scales of x, the tiled scales of the weights, the codes
+// and tiled scales of h, and O.
+struct MxLayout {
+  int64_t R, cap;
+  size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xq, xs, wgu_s, wd_s, hq, hs, o,
+      total;
+};
+
+MxLayout mx_layout(int64_t T, int H, int F, int E, int k) {
+  MxLayout L;
+  L.R = T * k;
+  L.cap = moe_padded_rows(L.R, E, kTileM);
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = cur;
+    cur += up256(bytes);
+    return at;
+  };
+  L.route = take(route_scratch_bytes(L.R, E));
+  L.counts = take(E * sizeof(int32_t));
+  L.offsets = take((E + 1) * sizeof(int32_t));
+  L.off_al = take((E + 1) * sizeof(int32_t));
+  L.row_of = take(L.R * sizeof(int32_t));
+  L.token_of = take(L.cap * sizeof(int32_t));
+  L.prob_of = take(L.cap * sizeof(float));
+  L.xq = take(static_cast<size_t>(L.cap) * H);
+  L.xs = take(static_cast<size_t>(L.cap) * H / 32);
+  L.wgu_s = take(static_cast<size_t>(E) * 2 * F * H / 32);
+  L.wd_s = take(static_cast<size_t>(E) * H * F / 32);
+  L.hq = take(static_cast<size_t>(L.cap) * F);
+  L.hs = take(static_cast<size_t>(L.cap) * F / 32);
+  L.o = take(static_cast<size_t>(L.cap) * H * 2);
+  L.total = cur;
+  return L;
+}
+
 template <typename P>
 P* at(void* ws, size_t off) {
   return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
@@ -167,6 +204,19 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
   const cuuint32_t box[2] = {box_inner, box_outer};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -309,7 +359,8 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* err = error_word();
   auto mark = [&](int i) {
-    if (c.step_events) cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+    if (c.step_events && i < c.num_step_events)
+      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
   };
   mark(0);
   const RouteScratch rs = route_scratch(at<char>(workspace, L.route), L.R, E);
@@ -435,6 +486,11 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   const int grid = grid_size(c);
   const int bnF = (F % 256 == 0) ? 256 : 128;
   const int bnH = (H % 256 == 0) ? 256 : 128;
+  auto mark = [&](int i) {
+    if (c.step_events && i < c.num_step_events)
+      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+  };
+  mark(0);
 
   // dO = p dY (gather-scale) and dprobs = <dY, O>; padding rows of dO are zero
   if (launch_dout(static_cast<const __nv_bfloat16*>(dy), o, row_of, probs, T, k, H, d_o, dprobs,
@@ -443,6 +499,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   if (launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, d_o, nullptr, nullptr,
                           st) != cudaSuccess)
     return MOE_ERR_CUDA;
+  mark(1);
 
   CUtensorMap t_do, t_w2k, t_da, t_wgk, t_wuk, t_xp_mn, t_da_mn, t_h_mn, t_do_mn;
   if (!make_tmap_bf16_2d(&t_do, d_o, H, B.cap, static_cast<uint64_t>(H) * 2, 64, kTileM) ||
@@ -480,6 +537,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gh.act_u = au;
   gh.ld_act = F;
   if (launch_dh_swiglu_bwd(t_do, t_w2k, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2);
 
   // dXp = dA_g W1g^T + dA_u W1u^T (one reduction over 2F), then dX = sum_j dXp[row_of]
   GroupedGemmArgs gx = g;
@@ -492,9 +550,11 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gx.outf = d_xp;
   gx.ldo = H;
   if (launch_dxp(t_da, t_wgk, t_wuk, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(3);
   if (launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
+  mark(4);
 
   // dW1g | dW1u = Xp_e^T [dA_g | dA_u] and dW2 = h_e^T dO_e over each expert's rows
   GroupedGemmArgs gw1 = g;
@@ -506,6 +566,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw1.outf2 = dw_up;
   gw1.accumulate = accumulate_dw ? 1 : 0;
   if (launch_wgrad(t_xp_mn, t_da_mn, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(5);
   GroupedGemmArgs gw2 = g;
   gw2.M = F;
   gw2.N = H;
@@ -514,16 +575,112 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw2.outf = dw_down;
   gw2.accumulate = accumulate_dw ? 1 : 0;
   if (launch_wgrad(t_h_mn, t_do_mn, gw2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(6);
   return MOE_OK;
 }
 
-size_t moe_workspace_size_mxfp8(int64_t, int, int, int, int, const moe_config*) { return 0; }
+size_t moe_workspace_size_mxfp8(int64_t T, int H, int F, int E, int k, const moe_config* cfg) {
+  (void)cfg;
+  if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;
+  return mx_layout(T, H, F, E, k).total;
+}
 
-moe_status moe_expert_forward_mxfp8(const void*, const uint8_t*, const uint8_t*, const uint8_t*,
-                                    const uint8_t*, const uint8_t*, const uint8_t*,
-                                    const int32_t*, const float*, int64_t, int, int, int, int,
-                                    void*, void*, size_t, const moe_config*, void*) {
-  return MOE_ERR_UNSUPPORTED;
+moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
+                                    const uint8_t* wu_q, const uint8_t* wu_s, const uint8_t* wd_q,
+                                    const uint8_t* wd_s, const int32_t* expert_ids,
+                                    const float* probs, int64_t T, int H, int F, int E, int k,
+                                    void* y, void* workspace, size_t ws_bytes,
+                                    const moe_config* cfg, void* stream) {
+  moe_status s = check_block_args(T, H, F, E, k);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!x || !wg_q || !wg_s || !wu_q || !wu_s || !wd_q || !wd_s || !expert_ids || !probs || !y)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(wg_q) || !aligned16(wu_q) || !aligned16(wd_q) ||
+      !aligned16(y) || (reinterpret_cast<uintptr_t>(wg_s) & 3) ||
+      (reinterpret_cast<uintptr_t>(wu_s) & 3) || (reinterpret_cast<uintptr_t>(wd_s) & 3))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c = cfg_or_default(cfg);
+  const MxLayout L = mx_layout(T, H, F, E, k);
+  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int* err = error_word();
+  auto mark = [&](int i) {
+    if (c.step_events && i < c.num_step_events)
+      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+  };
+  mark(0);
+  const RouteScratch rs = route_scratch(at<char>(workspace, L.route), L.R, E);
+  int32_t* counts = at<int32_t>(workspace, L.counts);
+  int32_t* offsets = at<int32_t>(workspace, L.offsets);
+  int32_t* off_al = at<int32_t>(workspace, L.off_al);
+  int32_t* row_of = at<int32_t>(workspace, L.row_of);
+  int32_t* token_of = at<int32_t>(workspace, L.token_of);
+  float* prob_of = at<float>(workspace, L.prob_of);
+  uint8_t* xq = at<uint8_t>(workspace, L.xq);
+  uint8_t* xs = at<uint8_t>(workspace, L.xs);
+  uint8_t* wgu_s = at<uint8_t>(workspace, L.wgu_s);
+  uint8_t* wd_st = at<uint8_t>(workspace, L.wd_s);
+  uint8_t* hq = at<uint8_t>(workspace, L.hq);
+  uint8_t* hs = at<uint8_t>(workspace, L.hs);
+  __nv_bfloat16* o = at<__nv_bfloat16>(workspace, L.o);
+
+  // counts -> offsets -> row map -> permute + quantise x (the dispatch)
+  if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
+          cudaSuccess ||
+      launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
+          cudaSuccess ||
+      launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of, xq, xs,
+                              st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // the weights' scales in the layout the block-scaled MMA reads
+  if (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, 1, wgu_s, st) !=
+          cudaSuccess ||
+      launch_tile_scales(wd_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0, wd_st, st) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  mark(1);
+
+  CUtensorMap ta, tg, tu, th, td;
+  if (!make_tmap_u8_2d(&ta, xq, H, L.cap, H, 128, kTileM) ||
+      !make_tmap_u8_2d(&tg, wg_q, H, static_cast<uint64_t>(E) * F, H, 128, 64) ||
+      !make_tmap_u8_2d(&tu, wu_q, H, static_cast<uint64_t>(E) * F, H, 128, 64) ||
+      !make_tmap_u8_2d(&th, hq, F, L.cap, F, 128, kTileM) ||
+      !make_tmap_u8_2d(&td, wd_q, F, static_cast<uint64_t>(E) * H, F, 128, 128))
+    return MOE_ERR_CUDA;
+  const int grid = grid_size(c);
+  MxGemmArgs g1{};
+  g1.off_al = off_al;
+  g1.E = E;
+  g1.K = H;
+  g1.N = F;
+  g1.stages = c.ring_stages;
+  g1.b_rows = F;
+  g1.sfb_rows = 2 * static_cast<int64_t>(F);
+  g1.sfa = xs;
+  g1.sfb = wgu_s;
+  g1.hq = hq;
+  g1.hs = hs;
+  g1.err = err;
+  g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+  if (launch_mx_fc1(ta, tg, tu, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(2);
+  MxGemmArgs g2 = g1;
+  g2.K = F;
+  g2.N = H;
+  g2.b_rows = H;
+  g2.sfb_rows = H;
+  g2.sfa = hs;
+  g2.sfb = wd_st;
+  g2.hq = nullptr;
+  g2.hs = nullptr;
+  g2.out = o;
+  if (launch_mx_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(3);
+  const cudaError_t ue =
+      launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
+  mark(4);
+  return from_cuda(ue);
 }
 
 }  // extern "C"

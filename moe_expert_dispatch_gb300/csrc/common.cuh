@@ -228,6 +228,63 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ block-scaled (MXFP8)
+
+// Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Shared-memory descriptor without swizzle (core matrices of 8 rows x 16 B).
+__device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFF) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFF) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFF) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Copy 32 rows x 128 bits from shared memory into tensor memory at taddr,
+// replicated into all four 32-lane quadrants (4 columns).
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale with E4M3
+// A and B (both K-major), E8M0 scales (bit 23), float accumulation, and the
+// byte (scale-factor id, 0..3) of the 32-bit tensor-memory scale words that
+// this instruction reads for A (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, uint32_t a_sf_id,
+                                                  uint32_t b_sf_id) {
+  return ((b_sf_id & 3u) << 4)                     // B scale-factor id
+         | (0u << 7) | (0u << 10)                  // A, B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (1u << 23)                              // scale type: UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)   // M / 16
+         | ((a_sf_id & 3u) << 29);                 // A scale-factor id
+}
+
+// D[tmem] (+)= (A * 2^sfA) (B * 2^sfB), M x N x 32 of E4M3 with per-32 E8M0 scales.
+__device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -1,0 +1,324 @@
+// gemm_mxfp8.cu - persistent grouped GEMMs of the MXFP8 expert block on the
+// block-scaled tensor cores of sm_103a (tcgen05.mma.kind::mxf8f6f4 with one
+// E8M0 scale per 32 elements of K on both operands).
+//
+// The structure is the one of gemm_bf16.cu (TMA producer warp, single-thread
+// MMA issuer, double-buffered TMEM accumulators, four epilogue warps, a ring
+// of `stages` shared-memory slots), with these differences:
+//   * a k-block is 128 E4M3 elements (128 bytes, one 128B-swizzle row);
+//     A (128 rows) and B (128 rows) are both K-major;
+//   * the scales of a k-block, one 512-byte atom for A and one for B, arrive
+//     by 1D bulk copies into the same slot and are moved into tensor memory
+//     with tcgen05.cp (32x128b, replicated over the four lane quadrants);
+//     each of the four MMAs of the k-block (K = 32) picks its byte of the
+//     32-bit scale words through the instruction's scale-factor id;
+//   * accumulators are 128 columns wide (2 x 128), and 8 columns per slot
+//     hold that slot's scales, all inside one 512-column allocation;
+//   * fc1's epilogue rounds h to bf16 and quantises it per 32 along F (codes
+//     + tiled scales for fc2); fc2's epilogue rounds O to bf16.
+// Tiles follow the Rows schedule: expert segments padded to 128 rows, tiles
+// numbered M fastest, CTA b takes tiles b, b + grid, ...
+#include "common.cuh"
+#include "internal.h"
+#include "mx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BK = 128;                    // E4M3 elements (bytes) per k-block
+constexpr int kTileN = 128;                // MMA N
+constexpr int kABytes = kTileM * BK;       // 16 KB
+constexpr int kBBytes = kTileN * BK;       // 16 KB
+constexpr int kSfBytes = 512;              // one scale atom
+constexpr int kStageBytes = 34 * 1024;     // A | B | SFA | SFB, padded to 1 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol = 256;           // first TMEM column of the per-slot scales
+constexpr unsigned long long kDrainNs = 1000000000ull;
+
+struct Smem {
+  uint64_t full[4];
+  uint64_t empty[4];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int zero;
+};
+
+template <bool kFc1>
+__global__ void __launch_bounds__(kThreads, 1)
+    mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, MxGemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  Smem* sm = reinterpret_cast<Smem*>(ring + S * kStageBytes);
+  int* ts = reinterpret_cast<int*>(sm + 1);
+  const int warp = threadIdx.x >> 5, lane = lane_id();
+  const int E = p.E;
+  const int n_cols = kFc1 ? kTileN / 2 : kTileN;   // output columns per N tile
+  const int n_tiles = p.N / n_cols;
+  const int kblocks = p.K / BK;
+  const int kgroups = p.K >> 7;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&sm->full[s]), 1);
+      mbar_init(smem_u32(&sm->empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&sm->tfull[a]), 1);
+      mbar_init(smem_u32(&sm->tempty[a]), 4 * 32);
+    }
+    mbar_init(smem_u32(&sm->drain), 1);
+    sm->abort = 0;
+    sm->zero = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB0);
+    tma_prefetch_desc(&tmB1);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+    tmem_relinquish();
+  }
+  for (int e = threadIdx.x; e < E; e += kThreads)
+    ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ts[0] = 0;
+    for (int e = 0; e < E; ++e) ts[e + 1] += ts[e];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = sm->tmem_base;
+  const int total = ts[E];
+  volatile int* abort_flag = &sm->abort;
+
+  auto decode = [&](int t, int& e, int& m, int& n) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (ts[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int mt = (p.off_al[e + 1] - p.off_al[e]) / kTileM;
+    const int local = t - ts[e];
+    n = local / mt;
+    m = local - n * mt;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_par[4] = {0, 0, 0, 0};
+      bool used[4] = {false, false, false, false};
+      bool ok = true;
+      const uint64_t pol_keep = l2_policy_evict_last();
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int e, m, n;
+        decode(t, e, m, n);
+        const int row0 = p.off_al[e] + m * kTileM;
+        const int64_t vrow = static_cast<int64_t>(e) * p.sfb_rows + static_cast<int64_t>(n) * kTileN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          const uint32_t full = smem_u32(&sm->full[stage]);
+          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full, kABytes + kBBytes + 2 * kSfBytes);
+          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t ssf = sb + kBBytes;
+          tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_keep);
+          if (kFc1) {       // 64 gate rows, then 64 up rows, of the same N tile
+            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * 64);
+            tma_load_2d(sb + kBBytes / 2, &tmB1, full, kb * BK, e * p.b_rows + n * 64);
+          } else {
+            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * kTileN);
+          }
+          bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(row0) >> 7) * kgroups + kb) * kSfBytes,
+                        kSfBytes, full);
+          bulk_copy_g2s(ssf + kSfBytes, p.sfb + ((vrow >> 7) * kgroups + kb) * kSfBytes, kSfBytes,
+                        full);
+          last_par[stage] = phase;
+          used[stage] = true;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok) {
+        sm->abort = 1;
+        report_error(p.err, kErrTimeout);
+      }
+      for (int s = 0; s < S; ++s)
+        if (used[s]) mbar_wait(smem_u32(&sm->full[s]), last_par[s], kDrainNs, &sm->zero);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, issued = false;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kTileN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.wait_ns, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sb = sa + kABytes;
+          const uint32_t ssf = sb + kBBytes;
+          // this slot's scales into its own 8 TMEM columns: A at +0..3, B at +4..7
+          const uint32_t sfa_t = tmem_base + kSfCol + stage * 8;
+          const uint32_t sfb_t = sfa_t + 4;
+          tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
+          tmem_cp_32x128b_warpx4(sfb_t, sdesc_noswizzle(ssf + kSfBytes, 16, 128));
+#pragma unroll
+          for (int ks = 0; ks < BK / 32; ++ks) {
+            const uint64_t ad = sdesc_sw128(sa + ks * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sb + ks * 32, 16, 1024);
+            umma_mxf8(d, ad, bd, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t, sfb_t,
+                      (kb | ks) ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&sm->empty[stage]));
+          issued = true;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&sm->tfull[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (!ok) {
+        sm->abort = 1;
+        report_error(p.err, kErrTimeout);
+      }
+      if (issued) {
+        umma_commit(smem_u32(&sm->drain));
+        mbar_wait(smem_u32(&sm->drain), 0, kDrainNs, &sm->zero);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;
+    const int row_in_tile = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      int e, m, n;
+      decode(t, e, m, n);
+      const int64_t grow = p.off_al[e] + m * kTileM + row_in_tile;
+      const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        sm->abort = 1;
+        if (lane == 0) report_error(p.err, kErrTimeout);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
+      if (kFc1) {
+        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F
+#pragma unroll 1
+        for (int c = 0; c < kTileN / 2; c += 32) {
+          uint32_t g[32], u[32];
+          tmem_ld_32x32b_x32(taddr + c, g);
+          tmem_ld_32x32b_x32(taddr + kTileN / 2 + c, u);
+          tmem_ld_wait();
+          float hv[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            hv[i] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(g[i])) *
+                                                         __uint_as_float(u[i])));
+          uint32_t w[8];
+          const uint8_t sc = quantize_block32(hv, w);
+          const int col = n * n_cols + c;
+          int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
+          dst[0] = make_int4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+          p.hs[mx_scale_offset(grow, col >> 5, p.N)] = sc;
+        }
+      } else {
+        __nv_bfloat16* out = p.out + grow * p.N + n * kTileN;
+#pragma unroll 1
+        for (int c = 0; c < kTileN; c += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_global_v4(out + c + 8 * i,
+                         pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
+                         pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sm->tempty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool kFc1>
+cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                      const MxGemmArgs& p, int grid, cudaStream_t st) {
+  const size_t smem = 1024 + 4 * static_cast<size_t>(kStageBytes) + sizeof(Smem) +
+                      static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kFc1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  mx_gemm_kernel<kFc1><<<grid, kThreads, smem, st>>>(a, b0, b1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                          const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx<true>(a, wg, wu, p, grid, st);
+}
+
+cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
+                          int grid, cudaStream_t st) {
+  return launch_mx<false>(a, wd, wd, p, grid, st);
+}
+
+}  // namespace moe

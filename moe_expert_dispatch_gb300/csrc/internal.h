@@ -126,6 +126,44 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
                         const float* probs, int64_t T, int k, int H, __nv_bfloat16* d_o,
                         float* dprobs, cudaStream_t st);
 
+// ------------------------------------------------------------------ MXFP8
+
+// codes of x in permuted rows ([cap, H], uint8) and their tiled scales.
+cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
+                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs,
+                                    cudaStream_t st);
+// row-major scales -> tiled layout (see mx.cuh); `pair` interleaves the gate
+// and up weights' rows per 64 so that one 128-row tile holds both halves.
+cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t out_rows,
+                               int64_t rows_per_e, int K, int pair, uint8_t* dst,
+                               cudaStream_t st);
+
+struct MxGemmArgs {
+  const int32_t* off_al;   // [E+1] padded expert row offsets
+  int E;
+  int K;                   // reduction length (elements = bytes)
+  int N;                   // output columns (fc1: F, fc2: H)
+  int stages;
+  int64_t b_rows;          // rows of one expert in B's 2D view (fc1: F, fc2: H)
+  int64_t sfb_rows;        // rows of one expert in B's tiled scales (fc1: 2F, fc2: H)
+  const uint8_t* sfa;      // tiled scales of A
+  const uint8_t* sfb;      // tiled scales of B
+  uint8_t* hq;             // fc1: codes of h [rows, N]
+  uint8_t* hs;             // fc1: tiled scales of h
+  __nv_bfloat16* out;      // fc2: O [rows, N]
+  int* err;
+  unsigned long long wait_ns;
+};
+
+// Encodes a 2D uint8 tensor map with the 128-byte swizzle.
+bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                     uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+
+cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                          const MxGemmArgs& p, int grid, cudaStream_t st);
+cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
+                          int grid, cudaStream_t st);
+
 int device_sm_count();
 
 }  // namespace moe

@@ -1,0 +1,60 @@
+// mx.cuh - MXFP8 (OCP Microscaling v1.0, E4M3 elements, E8M0 scales) on the
+// device: the block quantiser shared by the standalone quantiser, the fused
+// permute+quantise kernel and the fc1 epilogue, and the tiled scale layout
+// that the block-scaled tensor-core MMA reads.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace moe {
+
+// floor(log2(a)) of a positive finite float, subnormals included.
+__device__ __forceinline__ int floor_log2_pos(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int ex = static_cast<int>((b >> 23) & 0xFF);
+  if (ex != 0) return ex - 127;
+  const uint32_t man = b & 0x7FFFFF;
+  return (31 - __clz(static_cast<int>(man))) - 149;
+}
+
+// One block of 32 values: the E8M0 code of X = 2^(floor(log2 amax) - 8)
+// (clamped to [-127, 127]; an all-zero block gets -127) and the 32 E4M3
+// codes of v / X, round to nearest even, saturating at +-448, packed four to
+// a word (element 4i in the low byte of word i). v * 2^-s is exact (a
+// power-of-two scaling that stays in the normal range for every value that
+// can round to a non-zero E4M3), so the E4M3 conversion is the only rounding.
+__device__ __forceinline__ uint8_t quantize_block32(const float* v, uint32_t* words) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  int s = (amax > 0.0f) ? floor_log2_pos(amax) - 8 : -127;
+  s = max(-127, min(127, s));
+  const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+        make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+        make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
+    words[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+  }
+  return static_cast<uint8_t>(s + 127);
+}
+
+// Tiled scale layout read by the block-scaled MMA. Scales of a [rows, K]
+// operand (rows % 128 == 0, K % 128 == 0) are grouped by 128-row block rb
+// and 128-wide K group kg into 512-byte atoms, atom (rb, kg) at
+// (rb * (K / 128) + kg) * 512; inside an atom the scale of row m
+// (0 <= m < 128) for 32-block kk (0..3) of the group sits at byte
+// (m % 32) * 16 + (m / 32) * 4 + kk. An atom is what one
+// tcgen05.cp.32x128b.warpx4 moves into tensor memory.
+__host__ __device__ __forceinline__ int64_t mx_scale_offset(int64_t row, int64_t kblock32,
+                                                            int64_t K) {
+  const int64_t rb = row >> 7, m = row & 127;
+  const int64_t kg = kblock32 >> 2, kk = kblock32 & 3;
+  return (rb * (K >> 7) + kg) * 512 + (m & 31) * 16 + (m >> 5) * 4 + kk;
+}
+
+}  // namespace moe

@@ -3,10 +3,9 @@
 // probability-weighted unpermute and the MXFP8 quantiser. All are bound by
 // HBM bandwidth (or latency, for the tiny count/scan kernels); rows move as
 // 16-byte vectors, one warp per token so that each warp streams whole rows.
-#include <cuda_fp8.h>
-
 #include "common.cuh"
 #include "internal.h"
+#include "mx.cuh"
 
 namespace moe {
 
@@ -451,63 +450,37 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
   return cudaGetLastError();
 }
 
-// ------------------------------------------------------------------ MXFP8 quantiser
+// ------------------------------------------------------------------ MXFP8
 
-// floor(log2(a)) of a positive finite float, subnormals included.
-__device__ __forceinline__ int floor_log2_pos(float a) {
-  const uint32_t b = __float_as_uint(a);
-  const int ex = static_cast<int>((b >> 23) & 0xFF);
-  if (ex != 0) return ex - 127;
-  const uint32_t man = b & 0x7FFFFF;
-  return (31 - __clz(static_cast<int>(man))) - 149;
+__device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* v) {
+  const int4* s4 = reinterpret_cast<const int4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int4 raw = ld_stream(s4 + i);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[8 * i + 2 * j] = f.x;
+      v[8 * i + 2 * j + 1] = f.y;
+    }
+  }
 }
 
-// One thread per 32-element block: amax -> E8M0 code -> 32 E4M3 codes.
-// v * 2^-s is exact (a power-of-two scaling that stays in the normal range
-// for every value that can round to a non-zero E4M3), so the only rounding
-// is the one of the E4M3 conversion itself (round to nearest even,
-// saturating).
+// One thread per 32-element block, row-major scales [rows, K/32].
 __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16* __restrict__ in,
                                                              int64_t blocks,
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ scales) {
   for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < blocks;
        b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int4* src = reinterpret_cast<const int4*>(in + b * 32);
-    int4 raw[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) raw[i] = ld_stream(src + i);
     float v[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[i]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 f = __bfloat1622float2(h[j]);
-        v[8 * i + 2 * j] = f.x;
-        v[8 * i + 2 * j + 1] = f.y;
-        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-    }
-    int s = (amax > 0.0f) ? floor_log2_pos(amax) - 8 : -127;
-    s = max(-127, min(127, s));
-    scales[b] = static_cast<uint8_t>(s + 127);
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
-    uint32_t words[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __nv_fp8x2_storage_t lo =
-          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * inv, v[4 * i + 1] * inv),
-                                   __NV_SATFINITE, __NV_E4M3);
-      const __nv_fp8x2_storage_t hi =
-          __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv),
-                                   __NV_SATFINITE, __NV_E4M3);
-      words[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-    }
+    load_bf16x32_f(in + b * 32, v);
+    uint32_t w[8];
+    scales[b] = quantize_block32(v, w);
     int4* dst = reinterpret_cast<int4*>(q + b * 32);
-    dst[0] = make_int4(words[0], words[1], words[2], words[3]);
-    dst[1] = make_int4(words[4], words[5], words[6], words[7]);
+    dst[0] = make_int4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_int4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -519,6 +492,89 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, 
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   quantize_mxfp8_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
       in, blocks, q, scales);
+  return cudaGetLastError();
+}
+
+// The dispatch of the MXFP8 path: one warp per token reads the bf16 row once,
+// quantises it per 32 (the same routine as quantize_mxfp8_kernel) and writes
+// the codes to each of the token's k rows and the scales in the tiled layout
+// the block-scaled MMA reads.
+__global__ void __launch_bounds__(256) permute_quantize_kernel(
+    const __nv_bfloat16* __restrict__ x, int64_t T, int H, int k,
+    const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int nb = H >> 5;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
+    for (int base = 0; base < nb; base += 32) {     // warp-uniform trip count
+      const int b = base + lane;
+      float v[32];
+      uint32_t w[8];
+      uint8_t sc = 0;
+      if (b < nb) {
+        load_bf16x32_f(x + t * H + b * 32, v);
+        sc = quantize_block32(v, w);
+      }
+      for (int j = 0; j < k; ++j) {
+        const int r = __shfl_sync(0xffffffffu, my_row, j);
+        if (r < 0 || b >= nb) continue;
+        int4* dst = reinterpret_cast<int4*>(xq + static_cast<int64_t>(r) * H + b * 32);
+        dst[0] = make_int4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+        xs[mx_scale_offset(r, b, H)] = sc;
+      }
+    }
+  }
+}
+
+cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
+                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs,
+                                    cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  permute_quantize_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(x, T, H, k, row_of, xq, xs);
+  return cudaGetLastError();
+}
+
+// Row-major scales [rows, K/32] -> the tiled layout, one thread per (row,
+// 128-wide K group): 4 scale bytes in, 4 contiguous bytes out. With
+// `pair`, output row v of expert e's 2*rows_per_e virtual rows is, within its
+// 128-row tile n, row n*64 + (v % 128) of src0 for v % 128 < 64 and of src1
+// otherwise (the gate | up halves of one fc1 N tile).
+__global__ void __launch_bounds__(256) tile_scales_kernel(const uint8_t* __restrict__ src0,
+                                                          const uint8_t* __restrict__ src1,
+                                                          int64_t out_rows, int64_t rows_per_e,
+                                                          int K, int pair,
+                                                          uint8_t* __restrict__ dst) {
+  const int kgroups = K >> 7;
+  const int64_t n = out_rows * kgroups;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t v = i / kgroups;
+    const int kg = static_cast<int>(i - v * kgroups);
+    const uint8_t* src = src0;
+    int64_t srow = v;
+    if (pair) {
+      const int64_t e = v / (2 * rows_per_e), vr = v - e * 2 * rows_per_e;
+      const int64_t tile = vr >> 7, in = vr & 127;
+      src = in < 64 ? src0 : src1;
+      srow = e * rows_per_e + tile * 64 + (in & 63);
+    }
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + srow * (K >> 5) + kg * 4);
+    *reinterpret_cast<uint32_t*>(dst + mx_scale_offset(v, static_cast<int64_t>(kg) * 4, K)) = w;
+  }
+}
+
+cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t out_rows,
+                               int64_t rows_per_e, int K, int pair, uint8_t* dst,
+                               cudaStream_t st) {
+  const int64_t n = out_rows * (K >> 7);
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  tile_scales_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
+      src0, src1, out_rows, rows_per_e, K, pair, dst);
   return cudaGetLastError();
 }
 

@@ -450,24 +450,42 @@ def e8m0_scale_code(amax) -> np.ndarray:
     return (ex + 127).astype(np.uint8)
 
 
+_E4M3_TABLE = None
+
+
+def _e4m3_table() -> np.ndarray:
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        _E4M3_TABLE = e4m3_decode(np.arange(256))
+    return _E4M3_TABLE
+
+
 def quantize_mxfp8(a):
     """Quantise the last axis in blocks of 32: per block the E8M0 scale code
     from its amax, then each element E4M3(v / X). Returns (codes uint8 of a's
-    shape, scale codes uint8 of shape [..., K/32])."""
+    shape, scale codes uint8 of shape [..., K/32]).
+
+    v / X is a power-of-two scaling, exact for bf16-valued inputs, so the
+    only rounding is the E4M3 one. That rounding step uses torch's
+    float8_e4m3fn conversion (round to nearest even) after clamping to
+    +-448, which together are E4M3 satfinite; e4m3_encode is the same rule
+    written out, and the tests hold the two bit-identical."""
+    import torch
     a = _f64(a)
     K = a.shape[-1]
     assert K % MX_BLOCK == 0
     blocks = a.reshape(a.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     sc = e8m0_scale_code(np.abs(blocks).max(axis=-1))
     x_scale = np.ldexp(1.0, sc.astype(np.int64) - 127)
-    codes = e4m3_encode(blocks / x_scale[..., None])
+    scaled = np.clip(blocks / x_scale[..., None], -E4M3_MAX, E4M3_MAX).astype(np.float32)
+    codes = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return codes.reshape(a.shape), sc
 
 
 def dequantize_mxfp8(codes, scales):
     codes = np.asarray(codes)
     K = codes.shape[-1]
-    vals = e4m3_decode(codes).reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
+    vals = _e4m3_table()[codes].reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     x_scale = np.ldexp(1.0, np.asarray(scales).astype(np.int64) - 127)
     return (vals * x_scale[..., None]).reshape(codes.shape)
 
@@ -515,6 +533,38 @@ def expert_forward_mxfp8(xq, xs, wg, wu, wd, expert_ids, probs, num_experts):
         hq, hs = quantize_mxfp8(h)
         o[lo:hi] = bf16(dequantize_mxfp8(hq, hs) @ dequantize_mxfp8(*wd[e]).T)
     return unpermute(o, row_of, probs)
+
+
+def sampled_forward_mxfp8(x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, tokens):
+    """token_forward_mxfp8 for the listed tokens from bf16-valued inputs:
+    x [T, H] and the K-contiguous weights W1g, W1u [E, F, H], W2 [E, H, F]
+    (indexable by expert) are quantised here, one expert at a time, so that
+    only the experts the sampled tokens use are quantised."""
+    x = np.asarray(x)
+    ids = np.asarray(expert_ids)
+    pr = np.asarray(probs)
+    tokens = list(tokens)
+    xq, xs = quantize_mxfp8(x[tokens])
+    xd = {t: dequantize_mxfp8(xq[i], xs[i]) for i, t in enumerate(tokens)}
+    o_rows = {}
+    for e in sorted(set(int(v) for t in tokens for v in ids[t])):
+        wg = dequantize_mxfp8(*quantize_mxfp8(w_gate_t[e]))
+        wu = dequantize_mxfp8(*quantize_mxfp8(w_up_t[e]))
+        wd = dequantize_mxfp8(*quantize_mxfp8(w_down_t[e]))
+        for t in tokens:
+            for j, ee in enumerate(ids[t].tolist()):
+                if ee == e:
+                    h = bf16(silu(wg @ xd[t]) * (wu @ xd[t]))
+                    hq, hs = quantize_mxfp8(h)
+                    o_rows[(t, j)] = bf16(wd @ dequantize_mxfp8(hq, hs))
+    out = []
+    for t in tokens:
+        acc = None
+        for j in range(ids.shape[1]):
+            term = float(pr[t, j]) * o_rows[(t, j)]
+            acc = term if acc is None else acc + term
+        out.append(bf16(acc))
+    return np.stack(out)
 
 
 # --------------------------------------------------------------------------

@@ -1,0 +1,90 @@
+"""GPU parity of the MXFP8 forward (x quantised while permuted, block-scaled
+fc1 with h quantised in its epilogue, block-scaled fc2, bf16 combine)
+against the CPU oracle under max|y - y_ref| <= 3e-2 max|y_ref|. The oracle
+quantises its own inputs; the GPU's weight quantisation is first checked
+bit-exact against it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+import synth
+from gpu_util import assert_rel_to_max, dev, to_np
+
+pytestmark = pytest.mark.gpu
+m = pytest.importorskip("moe_expert_dispatch_gb300")
+
+TOL = 3e-2
+
+
+def _mx_case(T, H, F, E, k, seed=0, empty=(), wstd=0.05):
+    rng = np.random.default_rng(seed)
+    live = [e for e in range(E) if e not in empty]
+    ids = torch.from_numpy(np.stack([rng.choice(live, k, replace=False) for _ in range(T)]).astype(np.int32))
+    ex = rng.exponential(1.0, (T, k))
+    probs = torch.from_numpy((ex / ex.sum(1, keepdims=True)).astype(np.float32))
+    bf = lambda shape, s: torch.from_numpy((rng.standard_normal(shape) * s).astype(np.float32)).to(torch.bfloat16)  # noqa: E731
+    return bf((T, H), 1.0), bf((E, F, H), wstd), bf((E, F, H), wstd), bf((E, H, F), wstd), ids, probs
+
+
+def _gpu_weights(wg, wu, wd):
+    out = []
+    for w in (wg, wu, wd):
+        q, s = m.moe_quantize_mxfp8(dev(w))
+        out += [q, s]
+    return out
+
+
+def _gpu(x, wg, wu, wd, ids, probs, **cfg):
+    wq = _gpu_weights(wg, wu, wd)
+    y, _ = m.moe_expert_forward_mxfp8(dev(x), *wq, dev(ids), dev(probs), cfg=m.config(**cfg))
+    assert m.moe_get_error() == 0
+    return y, wq
+
+
+def _oracle(x, wg, wu, wd, ids, probs):
+    E = wg.shape[0]
+    xq, xs = orc.quantize_mxfp8(to_np(x))
+    qg = [orc.quantize_mxfp8(to_np(wg[e])) for e in range(E)]
+    qu = [orc.quantize_mxfp8(to_np(wu[e])) for e in range(E)]
+    qd = [orc.quantize_mxfp8(to_np(wd[e])) for e in range(E)]
+    return orc.expert_forward_mxfp8(xq, xs, qg, qu, qd, ids.numpy(), probs.numpy().astype(np.float64), E), (qg, qu, qd)
+
+
+@pytest.mark.parametrize("T,H,F,E,k,empty", [
+    (300, 256, 384, 5, 2, (3,)),       # ragged tails, an empty expert
+    (129, 128, 128, 1, 1, ()),         # one expert
+    (517, 384, 640, 9, 3, (0, 8)),     # H, F not multiples of 256
+    (64, 512, 256, 4, 4, ()),          # k = E
+])
+def test_mxfp8_forward_small(T, H, F, E, k, empty):
+    case = _mx_case(T, H, F, E, k, seed=T, empty=empty)
+    y, wq = _gpu(*case)
+    ref, (qg, qu, qd) = _oracle(*case)
+    for e in range(E):       # the GPU's weight codes and scales are the oracle's
+        assert np.array_equal(wq[0][e].cpu().numpy(), qg[e][0])
+        assert np.array_equal(wq[1][e].cpu().numpy(), qg[e][1])
+        assert np.array_equal(wq[4][e].cpu().numpy(), qd[e][0])
+    assert_rel_to_max(to_np(y), ref, TOL, "y")
+
+
+def test_mxfp8_schedule_independent():
+    case = _mx_case(400, 256, 384, 6, 2, seed=4)
+    y0, _ = _gpu(*case)
+    for kw in (dict(ring_stages=1), dict(num_sms=5), dict(ring_stages=2, num_sms=17)):
+        y1, _ = _gpu(*case, **kw)
+        assert torch.equal(y1, y0), kw
+
+
+def test_mxfp8_workload_sampled():
+    w = synth.WORKLOADS["mxfp8"]
+    inp = synth.make_inputs(w, 0)
+    x, wg, wu, wd = inp["x"], inp["w_gate_t"], inp["w_up_t"], inp["w_down_t"]
+    ids, probs = inp["expert_ids"], inp["probs"]
+    y, _ = _gpu(x, wg, wu, wd, ids, probs)
+    y = to_np(y)
+    toks = [0, 7777, w.T - 1]
+    f32 = lambda t: synth.F32Slices(t)  # noqa: E731
+    ref = orc.sampled_forward_mxfp8(to_np(x), f32(wg), f32(wu), f32(wd), ids.numpy(), probs.numpy(), toks)
+    assert_rel_to_max(y[toks], ref, TOL, "y sampled")
+    assert np.all(np.isfinite(y))

@@ -368,3 +368,32 @@ def test_sampled_forward_equals_dense():
     toks = [0, 5, 22, 7]
     np.testing.assert_array_equal(orc.sampled_forward(x, wg, wu, wd, ids, probs, toks),
                                   orc.dense_forward(x, wg, wu, wd, ids, probs, toks))
+
+
+def test_quantizer_rounding_step_equals_definition():
+    # quantize_mxfp8 rounds with torch's float8 conversion; e4m3_encode is the
+    # rule written out: they must agree bit for bit on every block
+    rng = np.random.default_rng(30)
+    a = orc.bf16(rng.standard_normal((40, 256)) * np.exp(rng.uniform(-20, 20, (40, 1))))
+    a[0, :32] = 0.0
+    q, sc = orc.quantize_mxfp8(a)
+    x_scale = np.ldexp(1.0, sc.astype(np.int64) - 127)
+    want = orc.e4m3_encode(a.reshape(40, 8, 32) / x_scale[..., None]).reshape(40, 256)
+    np.testing.assert_array_equal(q, want)
+
+
+def test_sampled_mxfp8_equals_token_forward():
+    rng = np.random.default_rng(31)
+    T, H, F, E, k = 6, 64, 96, 4, 2
+    x = orc.bf16(rng.standard_normal((T, H)))
+    wg, wu = orc.bf16(rng.standard_normal((E, F, H)) * 0.1), orc.bf16(rng.standard_normal((E, F, H)) * 0.1)
+    wd = orc.bf16(rng.standard_normal((E, H, F)) * 0.1)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    probs = rng.dirichlet(np.ones(k), T)
+    xq, xs = orc.quantize_mxfp8(x)
+    qg = [orc.quantize_mxfp8(wg[e]) for e in range(E)]
+    qu = [orc.quantize_mxfp8(wu[e]) for e in range(E)]
+    qd = [orc.quantize_mxfp8(wd[e]) for e in range(E)]
+    toks = [0, 3, 5]
+    want = np.stack([orc.token_forward_mxfp8(xq[t], xs[t], qg, qu, qd, ids[t], probs[t]) for t in toks])
+    np.testing.assert_array_equal(orc.sampled_forward_mxfp8(x, wg, wu, wd, ids, probs, toks), want)
