@@ -187,7 +187,7 @@ def run_reference(args, w):
 class Runner:
     """The timed step of one workload kind, its per-kernel events and FLOPs."""
 
-    def __init__(self, m, w, inp, device):
+    def __init__(self, m, w, inp, device, fuse_gather=False):
         import torch
         self.m, self.w, self.dev = m, w, device
         T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
@@ -214,11 +214,12 @@ class Runner:
         else:
             self.wg, self.wu, self.wd = (inp[key].to(device) for key in ("w_gate", "w_up", "w_down"))
             save = bool(w.backward)
-            self.cfg = m.config(save_for_backward=save)
-            self.cfg_ev = m.config(save_for_backward=save, step_events=self.fev)
+            self.cfg = m.config(save_for_backward=save, fuse_gather=fuse_gather)
+            self.cfg_ev = m.config(save_for_backward=save, fuse_gather=fuse_gather,
+                                   step_events=self.fev)
             nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
             self.dtype = "bf16"
-            self.launches = 7
+            self.launches = 6 if (fuse_gather and not save) else 7
             if w.backward:
                 self.dy = inp["dy"].to(device)
                 self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev)
@@ -281,7 +282,7 @@ def run_ours(args, w):
     import moe_expert_dispatch_gb300 as m
 
     inp = synth.make_inputs(w, 0)
-    run = Runner(m, w, inp, device)
+    run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather)
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
@@ -366,6 +367,9 @@ def run_ours(args, w):
         "dtype": run.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
                    "step": "forward + backward" if w.backward else "forward",
+                   "dispatch": "gathered by fc1's TMA producer" if (args.fuse_gather and not
+                                                                   w.backward and not w.mxfp8)
+                   else "materialised permute",
                    "l2": "flushed before every step (512 MB write)",
                    "parallelism": "replicas" if ws > 1 else "single"},
         "roofline": {"bound": "tensor", "kernel": f"{dominant} (grouped GEMM)",
@@ -401,6 +405,8 @@ def main():
     ap.add_argument("--workload", default="mixtral_bf16", choices=list(synth.WORKLOADS))
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,
+                    help="BF16 forward: fc1 gathers the routed rows itself (no permuted copy)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":

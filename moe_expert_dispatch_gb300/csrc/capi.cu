@@ -381,7 +381,11 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   if (launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  if (launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
+  // with the fused gather, fc1 reads the routed rows straight from x; the
+  // permuted copy is still made when the backward needs it
+  const bool gather = c.fuse_gather != 0;
+  if ((!gather || save) &&
+      launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (save && launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, xp, token_of,
                                   prob_of, st) != cudaSuccess)
@@ -390,7 +394,10 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   mark(1);
   // fc1 + SwiGLU
   CUtensorMap ta, tg, tu, th, td;
-  if (!make_tmap_bf16_2d(&ta, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, kTileM) ||
+  const bool ta_ok =
+      gather ? make_tmap_bf16_2d(&ta, x, H, T, static_cast<uint64_t>(H) * 2, 64, 1)
+             : make_tmap_bf16_2d(&ta, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, kTileM);
+  if (!ta_ok ||
       !make_tmap_bf16_2d(&tg, w_gate, F, static_cast<uint64_t>(E) * H,
                          static_cast<uint64_t>(F) * 2, 64, 64) ||
       !make_tmap_bf16_2d(&tu, w_up, F, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(F) * 2,
@@ -414,8 +421,12 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g1.save_u = save ? at<__nv_bfloat16>(workspace, L.au) : nullptr;
   g1.err = err;
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+  g1.gather_token = token_of;
+  g1.counts = counts;
   const int grid = grid_size(c);
-  if (launch_fc1_swiglu(ta, tg, tu, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, g1, grid, st)
+              : launch_fc1_swiglu(ta, tg, tu, g1, grid, st)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   mark(2);
 
   // fc2

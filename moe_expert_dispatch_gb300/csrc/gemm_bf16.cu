@@ -111,7 +111,7 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f)
   }
 }
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -169,7 +169,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   else total = E * (p.M / kTileM) * n_tiles;
   volatile int* abort_flag = &sm->abort;
 
-  if (warp == 0) {
+  if (kGather && warp == 0) {
+    // ---------------------------------------------------------- gathering producer
+    // The whole warp: lane l gathers rows 4l..4l+3 of the A tile with one TMA
+    // gather4 per k-block (4 token rows of x, 64 columns each, into 4
+    // consecutive 128-byte rows of the slot, swizzled like a tiled load);
+    // lane 0 also loads the weight boxes. This is the dispatch AllToAllv of
+    // all2all_grouped_matmul folded into the GEMM's producer.
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t last_par[4] = {0, 0, 0, 0};
+    bool used[4] = {false, false, false, false};
+    bool ok = true;
+    const uint64_t pol_keep = l2_policy_evict_last();
+    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<kSched>(t, ts, p);
+      const int real_end = p.off_al[tl.e] + p.counts[tl.e];
+      int tok[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = tl.row0 + 4 * lane + i;
+        tok[i] = r < real_end ? __ldg(p.gather_token + r) : 0;   // padding rows: any valid row
+      }
+      const int krow = tl.e * static_cast<int>(p.b_rows);
+      const int n0 = tl.n * (bn / 2);
+      for (int kb = 0; kb < tl.kblocks; ++kb) {
+        const uint32_t full = smem_u32(&sm->full[stage]);
+        const bool got = mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+        const uint32_t sb = sa + kABytes;
+        if (lane == 0) mbar_arrive_expect_tx(full, stage_tx);
+        __syncwarp();
+        tma_gather4(sa + lane * 512, &tmA, full, kb * BK, tok[0], tok[1], tok[2], tok[3]);
+        if (lane == 0) {
+          for (int j = 0; j < bn / 128; ++j) {
+            tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow + kb * BK);
+            tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, n0 + 64 * j, krow + kb * BK);
+          }
+        }
+        last_par[stage] = phase;
+        used[stage] = true;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    (void)pol_keep;
+    if (!ok && lane == 0) {
+      sm->abort = 1;
+      report_error(p.err, kErrTimeout);
+    }
+    if (lane == 0)
+      for (int s = 0; s < S; ++s)
+        if (used[s]) mbar_wait(smem_u32(&sm->full[s]), last_par[s], kDrainNs, &sm->zero);
+  } else if (warp == 0) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
       int stage = 0;
@@ -446,14 +504,14 @@ size_t gemm_smem_bytes(int stages, int E) {
          static_cast<size_t>(E + 1) * sizeof(int);
 }
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const GroupedGemmArgs& p, int grid, cudaStream_t st) {
   // always the 4-stage size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
   const size_t smem = gemm_smem_bytes(4, kMaxExperts);
   static bool configured = false;
-  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched>;
+  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -469,6 +527,12 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                               const GroupedGemmArgs& p, int grid, cudaStream_t st) {
   return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows>(a, wg, wu, p, grid, st);
+}
+
+cudaError_t launch_fc1_swiglu_gather(const CUtensorMap& x_rows, const CUtensorMap& wg,
+                                     const CUtensorMap& wu, const GroupedGemmArgs& p, int grid,
+                                     cudaStream_t st) {
+  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows, true>(x_rows, wg, wu, p, grid, st);
 }
 
 cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,

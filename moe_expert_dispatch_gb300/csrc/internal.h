@@ -97,6 +97,8 @@ struct GroupedGemmArgs {
   float* outf;             // F32 output: Rows [rows, ldo]; WGrad [E, M, N or out_split]
   float* outf2;            // F32 second output (columns >= out_split)
   int accumulate;          // F32: add to the existing values
+  const int32_t* gather_token;  // fc1 with fused gather: token of each padded row
+  const int32_t* counts;        // fc1 with fused gather: rows of each expert
   int* err;
   unsigned long long wait_ns;
 };
@@ -108,6 +110,11 @@ bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint6
 // fc1: out = bf16(silu(A W_gate) * (A W_up)), A rows tiled per expert.
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                               const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// fc1 with the dispatch fused into its producer: A rows are gathered from
+// the token rows of x (tensor map with a one-row box) by TMA gather4.
+cudaError_t launch_fc1_swiglu_gather(const CUtensorMap& x_rows, const CUtensorMap& wg,
+                                     const CUtensorMap& wu, const GroupedGemmArgs& p, int grid,
+                                     cudaStream_t st);
 // fc2: out = bf16(A W).
 cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
                        int grid, cudaStream_t st);

@@ -58,6 +58,10 @@ WORKLOADS = {
     # a smaller Mixtral-shaped case (2 experts, every token on both) for
     # profiler captures that must hold only about 1 GB on the device
     "mixtral_2experts": Workload("mixtral_2experts", 2048, 4096, 14336, 2, 2, "gaussian", 0.01),
+    "mxfp8_16experts": Workload("mxfp8_16experts", 4096, 7168, 2048, 16, 6, "uniform", 0.02,
+                                mxfp8=True),
+    "train_2experts": Workload("train_2experts", 2048, 4096, 14336, 2, 2, "gaussian", 0.01,
+                               backward=True),
 }
 
 # Zipf exponent and the number of experts given zero popularity in the

@@ -134,3 +134,26 @@ def test_forward_wait_timeout_reports_and_recovers():
     assert m.moe_get_error() == 5
     y = _gpu(*case)           # the context is still usable and results are right
     assert_bf16_close(to_np(y), _oracle(*case), "y")
+
+
+@pytest.mark.parametrize("T,H,F,E,k,empty", [
+    (300, 256, 384, 5, 2, (3,)),
+    (1, 128, 256, 4, 2, ()),
+    (517, 384, 640, 9, 3, (0, 8)),
+    (1000, 256, 256, 16, 2, ()),
+])
+def test_fused_gather_bit_identical(T, H, F, E, k, empty):
+    """fc1 gathering the routed rows of x itself (TMA gather4 in its producer)
+    computes exactly what it computes on the materialised permuted copy."""
+    case = _case(T, H, F, E, k, seed=T + 7, empty=empty)
+    y0 = _gpu(*case)
+    y1 = _gpu(*case, fuse_gather=True)
+    assert torch.equal(y1, y0)
+    assert_bf16_close(to_np(y1), _oracle(*case), "y fused gather")
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16", "skewed_bf16", "mixtral_bf16"])
+def test_fused_gather_workloads(name):
+    inp = synth.make_inputs(synth.WORKLOADS[name], 0)
+    case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
+    assert torch.equal(_gpu(*case, fuse_gather=True), _gpu(*case))
