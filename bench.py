@@ -187,7 +187,7 @@ def run_reference(args, w):
 class Runner:
     """The timed step of one workload kind, its per-kernel events and FLOPs."""
 
-    def __init__(self, m, w, inp, device, fuse_gather=False):
+    def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0):
         import torch
         self.m, self.w, self.dev = m, w, device
         T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
@@ -206,8 +206,8 @@ class Runner:
             for key in ("w_gate_t", "w_up_t", "w_down_t"):
                 q, s = m.moe_quantize_mxfp8(inp[key].to(device))
                 self.wq += [q, s]
-            self.cfg = m.config()
-            self.cfg_ev = m.config(step_events=self.fev)
+            self.cfg = m.config(mxfp8_tile_n=mx_tile_n)
+            self.cfg_ev = m.config(step_events=self.fev, mxfp8_tile_n=mx_tile_n)
             nbytes = m.moe_workspace_size_mxfp8(T, H, F, E, k, self.cfg)
             self.dtype = "mxfp8 (e4m3 + e8m0 per 32; bf16 out)"
             self.launches = 9
@@ -282,7 +282,7 @@ def run_ours(args, w):
     import moe_expert_dispatch_gb300 as m
 
     inp = synth.make_inputs(w, 0)
-    run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather)
+    run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather, mx_tile_n=args.mxfp8_tile_n)
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
@@ -405,6 +405,7 @@ def main():
     ap.add_argument("--workload", default="mixtral_bf16", choices=list(synth.WORKLOADS))
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mxfp8-tile-n", type=int, default=0, choices=[0, 128, 256])
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,
                     help="BF16 forward: fc1 gathers the routed rows itself (no permuted copy)")
     args = ap.parse_args()

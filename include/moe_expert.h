@@ -53,9 +53,11 @@ typedef enum moe_precision { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;
  * defaults; a NULL config pointer means the defaults. */
 typedef struct moe_config {
   int ring_stages;         /* depth of the shared-memory ring that feeds the tensor
-                              cores, 1..4 (default 4; 1 = no overlap, the serial
+                              cores: 0 (default) = the deepest that fits, 4 slots of
+                              48 KB for BF16 and 6 slots of 34 KB for MXFP8; 1..6 to
+                              choose (BF16 caps at 4); 1 = no overlap, the serial
                               baseline of the "tileCnt = 1" knob in "MC2 通算融合架构总览"
-                              section 6)                                              */
+                              section 6                                               */
   int save_for_backward;   /* forward keeps Xp, A_g, A_u, h and O in its workspace
                               and zero-fills the padding rows (default 0)              */
   int num_sms;             /* persistent grid size of the grouped GEMMs; 0 = all SMs   */
@@ -69,6 +71,9 @@ typedef struct moe_config {
                               Backward (7): start, after dO+dprobs, dH+SwiGLU
                               backward, dXp, dX, dW1, dW2.                            */
   int num_step_events;     /* entries of step_events (events past it are not recorded) */
+  int mxfp8_tile_n;        /* MMA N of the MXFP8 GEMMs: 128 (two accumulators, the
+                              epilogue overlaps the next tile) or 256 (one accumulator,
+                              half the A traffic per FLOP); 0 (default) = automatic  */
 } moe_config;
 
 #define MOE_STEP_EVENTS 5

@@ -160,7 +160,7 @@ moe_config cfg_or_default(const moe_config* c) {
   moe_config_init(&d);
   if (!c) return d;
   d = *c;
-  if (d.ring_stages < 1 || d.ring_stages > 4) d.ring_stages = 4;
+  if (d.ring_stages < 0 || d.ring_stages > 6) d.ring_stages = 0;   // 0: the kernel's deepest
   if (d.wait_limit_ns <= 0) d.wait_limit_ns = static_cast<long long>(kDefaultWaitNs);
   return d;
 }
@@ -230,7 +230,7 @@ extern "C" {
 void moe_config_init(moe_config* cfg) {
   if (!cfg) return;
   memset(cfg, 0, sizeof(*cfg));
-  cfg->ring_stages = 4;
+  cfg->ring_stages = 0;
   cfg->wait_limit_ns = static_cast<long long>(kDefaultWaitNs);
 }
 
@@ -412,7 +412,7 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g1.K = H;
   g1.N = F;
   g1.bn = 256;                 // 128 gate + 128 up columns per N tile
-  g1.stages = c.ring_stages;
+  g1.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
   g1.b_rows = H;
   g1.b_split = 1;
   g1.out = h;
@@ -533,7 +533,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   GroupedGemmArgs g{};
   g.off_al = off_al;
   g.E = E;
-  g.stages = c.ring_stages;
+  g.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
   g.err = err;
   g.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
   GroupedGemmArgs gh = g;
@@ -644,8 +644,11 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
       launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of, xq, xs,
                               st) != cudaSuccess)
     return MOE_ERR_CUDA;
+  // MMA N: 256 halves the A traffic per FLOP; 128 keeps two accumulators
+  const int mx_bn = c.mxfp8_tile_n == 128 ? 128
+                    : (c.mxfp8_tile_n == 256 || (F % 128 == 0 && H % 256 == 0)) ? 256 : 128;
   // the weights' scales in the layout the block-scaled MMA reads
-  if (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, 1, wgu_s, st) !=
+  if (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, mx_bn / 2, wgu_s, st) !=
           cudaSuccess ||
       launch_tile_scales(wd_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0, wd_st, st) !=
           cudaSuccess)
@@ -654,8 +657,8 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
 
   CUtensorMap ta, tg, tu, th, td;
   if (!make_tmap_u8_2d(&ta, xq, H, L.cap, H, 128, kTileM) ||
-      !make_tmap_u8_2d(&tg, wg_q, H, static_cast<uint64_t>(E) * F, H, 128, 64) ||
-      !make_tmap_u8_2d(&tu, wu_q, H, static_cast<uint64_t>(E) * F, H, 128, 64) ||
+      !make_tmap_u8_2d(&tg, wg_q, H, static_cast<uint64_t>(E) * F, H, 128, mx_bn / 2) ||
+      !make_tmap_u8_2d(&tu, wu_q, H, static_cast<uint64_t>(E) * F, H, 128, mx_bn / 2) ||
       !make_tmap_u8_2d(&th, hq, F, L.cap, F, 128, kTileM) ||
       !make_tmap_u8_2d(&td, wd_q, F, static_cast<uint64_t>(E) * H, F, 128, 128))
     return MOE_ERR_CUDA;
@@ -665,7 +668,8 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.E = E;
   g1.K = H;
   g1.N = F;
-  g1.stages = c.ring_stages;
+  g1.stages = c.ring_stages == 0 ? 6 : c.ring_stages;
+  g1.bn = mx_bn;
   g1.b_rows = F;
   g1.sfb_rows = 2 * static_cast<int64_t>(F);
   g1.sfa = xs;

@@ -21,10 +21,11 @@
 //    tile per 128 rows, times N/bn N tiles; the reduction is a fixed K.
 //  * WGrad (dW1, dW2): expert e owns (M/128) x (N/bn) tiles of its weight
 //    gradient and the reduction runs over its (zero-padded) rows.
-// Tiles of all experts are numbered consecutively, M fastest (so CTAs that
-// run at the same time share one B tile through L2), and CTA b takes tiles
-// b, b + grid, ...; experts without rows own no Rows tile. Counts never
-// leave the device.
+// Tiles of all experts are numbered consecutively and CTA b takes tiles b,
+// b + grid, ...; within an expert M runs fastest (CTAs that run at the same
+// time share one weight tile through L2) unless the expert has more M tiles
+// than N tiles, where N runs fastest so that its rows stay in L2 instead.
+// Experts without rows own no Rows tile. Counts never leave the device.
 #include "common.cuh"
 #include "internal.h"
 
@@ -68,9 +69,15 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
     }
     tl.e = lo;
     const int mt = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int nt = p.N / (p.b_split == 1 ? p.bn / 2 : p.bn);
     const int local = t - ts[tl.e];
-    tl.n = local / mt;
-    tl.m = local - tl.n * mt;
+    if (mt > nt) {            // tall expert: its row panel is the larger operand, keep it in L2
+      tl.m = local / nt;
+      tl.n = local - tl.m * nt;
+    } else {                  // the weight panel is larger: M fastest shares it between CTAs
+      tl.n = local / mt;
+      tl.m = local - tl.n * mt;
+    }
     tl.row0 = p.off_al[tl.e] + tl.m * kTileM;
     tl.kblocks = p.K / BK;
   } else {

@@ -14,10 +14,13 @@
 //     32-bit scale words through the instruction's scale-factor id;
 //   * accumulators are 128 columns wide (2 x 128), and 8 columns per slot
 //     hold that slot's scales, all inside one 512-column allocation;
+//   * slots are smaller (34 KB), so the ring is up to 6 deep: at the FP8 rate
+//     4 slots in flight per SM do not cover the L2 latency;
 //   * fc1's epilogue rounds h to bf16 and quantises it per 32 along F (codes
 //     + tiled scales for fc2); fc2's epilogue rounds O to bf16.
-// Tiles follow the Rows schedule: expert segments padded to 128 rows, tiles
-// numbered M fastest, CTA b takes tiles b, b + grid, ...
+// Tiles follow the Rows schedule of gemm_bf16.cu: expert segments padded to
+// 128 rows, M fastest within an expert unless it has more M tiles than N
+// tiles, CTA b takes tiles b, b + grid, ...
 #include "common.cuh"
 #include "internal.h"
 #include "mx.cuh"
@@ -27,19 +30,34 @@ namespace moe {
 namespace {
 
 constexpr int BK = 128;                    // E4M3 elements (bytes) per k-block
-constexpr int kTileN = 128;                // MMA N
 constexpr int kABytes = kTileM * BK;       // 16 KB
-constexpr int kBBytes = kTileN * BK;       // 16 KB
-constexpr int kSfBytes = 512;              // one scale atom
-constexpr int kStageBytes = 34 * 1024;     // A | B | SFA | SFB, padded to 1 KB
+constexpr int kSfBytes = 512;              // one scale atom (128 rows x 4 blocks of 32)
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSfCol = 256;           // first TMEM column of the per-slot scales
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
+constexpr int kMaxStages = 6;
+
+// Tile geometry for an MMA N of 128 or 256. N=128: two accumulators of 128
+// columns (the epilogue of a tile overlaps the next tile) and 34 KB slots;
+// N=256: one accumulator of 256 columns (no overlap, but half the A reads
+// per FLOP) and 50 KB slots. Scales take 4 + N/32 columns per slot after the
+// accumulators.
+template <int kN>
+struct MxGeo {
+  static constexpr int kBBytes = kN * BK;
+  static constexpr int kSfbAtoms = kN / 128;
+  static constexpr int kStageBytes = ((kABytes + kBBytes + (1 + kSfbAtoms) * kSfBytes) + 1023) /
+                                     1024 * 1024;
+  static constexpr int kAccBufs = kN == 128 ? 2 : 1;
+  static constexpr uint32_t kSfCol = kAccBufs * kN;
+  static constexpr uint32_t kSfColsPerStage = 4 + 4 * kSfbAtoms;
+  static constexpr int kStages = kN == 128 ? 6 : 4;   // what fits in shared memory
+};
+
 struct Smem {
-  uint64_t full[4];
-  uint64_t empty[4];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -48,14 +66,17 @@ struct Smem {
   int zero;
 };
 
-template <bool kFc1>
+template <bool kFc1, int kTileN>
 __global__ void __launch_bounds__(kThreads, 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, MxGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int S = p.stages;
+  using G = MxGeo<kTileN>;
+  constexpr int kBBytes = G::kBBytes;
+  constexpr int kStageBytes = G::kStageBytes;
+  const int S = p.stages < G::kStages ? p.stages : G::kStages;
   Smem* sm = reinterpret_cast<Smem*>(ring + S * kStageBytes);
   int* ts = reinterpret_cast<int*>(sm + 1);
   const int warp = threadIdx.x >> 5, lane = lane_id();
@@ -111,8 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     e = lo;
     const int mt = (p.off_al[e + 1] - p.off_al[e]) / kTileM;
     const int local = t - ts[e];
-    n = local / mt;
-    m = local - n * mt;
+    if (mt > n_tiles) {       // tall expert: keep its row panel in L2
+      m = local / n_tiles;
+      n = local - m * n_tiles;
+    } else {
+      n = local / mt;
+      m = local - n * mt;
+    }
   };
 
   if (warp == 0) {
@@ -120,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t last_par[4] = {0, 0, 0, 0};
-      bool used[4] = {false, false, false, false};
+      uint32_t last_par[kMaxStages] = {};
+      bool used[kMaxStages] = {};
       bool ok = true;
       const uint64_t pol_keep = l2_policy_evict_last();
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
@@ -135,21 +161,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full, kABytes + kBBytes + 2 * kSfBytes);
+          mbar_arrive_expect_tx(full, kABytes + kBBytes + (1 + G::kSfbAtoms) * kSfBytes);
           const uint32_t sa = smem_u32(ring + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
           tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_keep);
-          if (kFc1) {       // 64 gate rows, then 64 up rows, of the same N tile
-            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * 64);
-            tma_load_2d(sb + kBBytes / 2, &tmB1, full, kb * BK, e * p.b_rows + n * 64);
+          if (kFc1) {       // N/2 gate rows, then N/2 up rows, of the same N tile
+            const int half = kTileN / 2;
+            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * half);
+            tma_load_2d(sb + half * BK, &tmB1, full, kb * BK, e * p.b_rows + n * half);
           } else {
-            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * kTileN);
+            for (int j = 0; j < kTileN; j += 128)
+              tma_load_2d(sb + j * BK, &tmB0, full, kb * BK, e * p.b_rows + n * kTileN + j);
           }
           bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(row0) >> 7) * kgroups + kb) * kSfBytes,
                         kSfBytes, full);
-          bulk_copy_g2s(ssf + kSfBytes, p.sfb + ((vrow >> 7) * kgroups + kb) * kSfBytes, kSfBytes,
-                        full);
+#pragma unroll
+          for (int j = 0; j < G::kSfbAtoms; ++j)
+            bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
+                          p.sfb + (((vrow >> 7) + j) * kgroups + kb) * kSfBytes, kSfBytes, full);
           last_par[stage] = phase;
           used[stage] = true;
           if (++stage == S) {
@@ -189,11 +219,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(ring + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
-          // this slot's scales into its own 8 TMEM columns: A at +0..3, B at +4..7
-          const uint32_t sfa_t = tmem_base + kSfCol + stage * 8;
+          // this slot's scales into its own TMEM columns: A at +0..3, B's
+          // 128-row atoms at +4..7 (and +8..11 for N = 256)
+          const uint32_t sfa_t = tmem_base + G::kSfCol + stage * G::kSfColsPerStage;
           const uint32_t sfb_t = sfa_t + 4;
           tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
-          tmem_cp_32x128b_warpx4(sfb_t, sdesc_noswizzle(ssf + kSfBytes, 16, 128));
+#pragma unroll
+          for (int j = 0; j < G::kSfbAtoms; ++j)
+            tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                   sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
 #pragma unroll
           for (int ks = 0; ks < BK / 32; ++ks) {
             const uint64_t ad = sdesc_sw128(sa + ks * 32, 16, 1024);
@@ -210,8 +244,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         umma_commit(smem_u32(&sm->tfull[acc]));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
+        if (++acc == G::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
       }
       if (!ok) {
         sm->abort = 1;
@@ -279,8 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&sm->tempty[acc]));
-      acc ^= 1;
-      if (acc == 0) acc_phase ^= 1;
+      if (++acc == G::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
     }
   }
 
@@ -292,20 +330,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <bool kFc1>
+template <bool kFc1, int kN>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                       const MxGemmArgs& p, int grid, cudaStream_t st) {
-  const size_t smem = 1024 + 4 * static_cast<size_t>(kStageBytes) + sizeof(Smem) +
+  using G = MxGeo<kN>;
+  const size_t smem = 1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + sizeof(Smem) +
                       static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kFc1>,
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kFc1, kN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mx_gemm_kernel<kFc1><<<grid, kThreads, smem, st>>>(a, b0, b1, p);
+  mx_gemm_kernel<kFc1, kN><<<grid, kThreads, smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
@@ -313,12 +352,14 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx<true>(a, wg, wu, p, grid, st);
+  return p.bn == 256 ? launch_mx<true, 256>(a, wg, wu, p, grid, st)
+                     : launch_mx<true, 128>(a, wg, wu, p, grid, st);
 }
 
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
                           int grid, cudaStream_t st) {
-  return launch_mx<false>(a, wd, wd, p, grid, st);
+  return p.bn == 256 ? launch_mx<false, 256>(a, wd, wd, p, grid, st)
+                     : launch_mx<false, 128>(a, wd, wd, p, grid, st);
 }
 
 }  // namespace moe

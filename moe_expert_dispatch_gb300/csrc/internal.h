@@ -139,10 +139,11 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
 cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
                                     const int32_t* row_of, uint8_t* xq, uint8_t* xs,
                                     cudaStream_t st);
-// row-major scales -> tiled layout (see mx.cuh); `pair` interleaves the gate
-// and up weights' rows per 64 so that one 128-row tile holds both halves.
+// row-major scales -> tiled layout (see mx.cuh); pair_half > 0 interleaves
+// the gate and up weights' rows per pair_half so that one N tile of
+// 2*pair_half rows holds both halves.
 cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t out_rows,
-                               int64_t rows_per_e, int K, int pair, uint8_t* dst,
+                               int64_t rows_per_e, int K, int pair_half, uint8_t* dst,
                                cudaStream_t st);
 
 struct MxGemmArgs {
@@ -151,6 +152,7 @@ struct MxGemmArgs {
   int K;                   // reduction length (elements = bytes)
   int N;                   // output columns (fc1: F, fc2: H)
   int stages;
+  int bn;                  // MMA N: 128 or 256
   int64_t b_rows;          // rows of one expert in B's 2D view (fc1: F, fc2: H)
   int64_t sfb_rows;        // rows of one expert in B's tiled scales (fc1: 2F, fc2: H)
   const uint8_t* sfa;      // tiled scales of A

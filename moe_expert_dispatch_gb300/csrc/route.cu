@@ -539,13 +539,13 @@ cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, in
 
 // Row-major scales [rows, K/32] -> the tiled layout, one thread per (row,
 // 128-wide K group): 4 scale bytes in, 4 contiguous bytes out. With
-// `pair`, output row v of expert e's 2*rows_per_e virtual rows is, within its
-// 128-row tile n, row n*64 + (v % 128) of src0 for v % 128 < 64 and of src1
-// otherwise (the gate | up halves of one fc1 N tile).
+// pair_half = P > 0, expert e has 2*rows_per_e virtual rows cut into tiles of
+// 2P: row i of tile n is row n*P + i of src0 for i < P and row n*P + i - P of
+// src1 otherwise (the gate | up halves of one fc1 N tile).
 __global__ void __launch_bounds__(256) tile_scales_kernel(const uint8_t* __restrict__ src0,
                                                           const uint8_t* __restrict__ src1,
                                                           int64_t out_rows, int64_t rows_per_e,
-                                                          int K, int pair,
+                                                          int K, int pair_half,
                                                           uint8_t* __restrict__ dst) {
   const int kgroups = K >> 7;
   const int64_t n = out_rows * kgroups;
@@ -555,11 +555,11 @@ __global__ void __launch_bounds__(256) tile_scales_kernel(const uint8_t* __restr
     const int kg = static_cast<int>(i - v * kgroups);
     const uint8_t* src = src0;
     int64_t srow = v;
-    if (pair) {
+    if (pair_half > 0) {
       const int64_t e = v / (2 * rows_per_e), vr = v - e * 2 * rows_per_e;
-      const int64_t tile = vr >> 7, in = vr & 127;
-      src = in < 64 ? src0 : src1;
-      srow = e * rows_per_e + tile * 64 + (in & 63);
+      const int64_t tile = vr / (2 * pair_half), in = vr - tile * 2 * pair_half;
+      src = in < pair_half ? src0 : src1;
+      srow = e * rows_per_e + tile * pair_half + (in < pair_half ? in : in - pair_half);
     }
     const uint32_t w = *reinterpret_cast<const uint32_t*>(src + srow * (K >> 5) + kg * 4);
     *reinterpret_cast<uint32_t*>(dst + mx_scale_offset(v, static_cast<int64_t>(kg) * 4, K)) = w;
@@ -567,14 +567,14 @@ __global__ void __launch_bounds__(256) tile_scales_kernel(const uint8_t* __restr
 }
 
 cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t out_rows,
-                               int64_t rows_per_e, int K, int pair, uint8_t* dst,
+                               int64_t rows_per_e, int K, int pair_half, uint8_t* dst,
                                cudaStream_t st) {
   const int64_t n = out_rows * (K >> 7);
   if (n == 0) return cudaSuccess;
   const int64_t want = (n + 255) / 256;
   const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
   tile_scales_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
-      src0, src1, out_rows, rows_per_e, K, pair, dst);
+      src0, src1, out_rows, rows_per_e, K, pair_half, dst);
   return cudaGetLastError();
 }
 

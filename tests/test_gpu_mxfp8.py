@@ -51,15 +51,16 @@ def _oracle(x, wg, wu, wd, ids, probs):
     return orc.expert_forward_mxfp8(xq, xs, qg, qu, qd, ids.numpy(), probs.numpy().astype(np.float64), E), (qg, qu, qd)
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("T,H,F,E,k,empty", [
     (300, 256, 384, 5, 2, (3,)),       # ragged tails, an empty expert
-    (129, 128, 128, 1, 1, ()),         # one expert
-    (517, 384, 640, 9, 3, (0, 8)),     # H, F not multiples of 256
+    (129, 256, 128, 1, 1, ()),         # one expert
+    (517, 512, 640, 9, 3, (0, 8)),     # F not a multiple of 256
     (64, 512, 256, 4, 4, ()),          # k = E
 ])
-def test_mxfp8_forward_small(T, H, F, E, k, empty):
+def test_mxfp8_forward_small(T, H, F, E, k, empty, tile_n):
     case = _mx_case(T, H, F, E, k, seed=T, empty=empty)
-    y, wq = _gpu(*case)
+    y, wq = _gpu(*case, mxfp8_tile_n=tile_n)
     ref, (qg, qu, qd) = _oracle(*case)
     for e in range(E):       # the GPU's weight codes and scales are the oracle's
         assert np.array_equal(wq[0][e].cpu().numpy(), qg[e][0])
@@ -68,12 +69,28 @@ def test_mxfp8_forward_small(T, H, F, E, k, empty):
     assert_rel_to_max(to_np(y), ref, TOL, "y")
 
 
-def test_mxfp8_schedule_independent():
+def test_mxfp8_h_not_multiple_of_256_uses_128_tiles():
+    case = _mx_case(300, 384, 256, 4, 2, seed=8)
+    y, _ = _gpu(*case)
+    ref, _ = _oracle(*case)
+    assert_rel_to_max(to_np(y), ref, TOL, "y")
+
+
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_mxfp8_schedule_independent(tile_n):
     case = _mx_case(400, 256, 384, 6, 2, seed=4)
-    y0, _ = _gpu(*case)
+    y0, _ = _gpu(*case, mxfp8_tile_n=tile_n)
     for kw in (dict(ring_stages=1), dict(num_sms=5), dict(ring_stages=2, num_sms=17)):
-        y1, _ = _gpu(*case, **kw)
+        y1, _ = _gpu(*case, mxfp8_tile_n=tile_n, **kw)
         assert torch.equal(y1, y0), kw
+
+
+def test_mxfp8_tile_widths_agree():
+    # both tile widths run the same per-row reduction order over K
+    case = _mx_case(300, 512, 384, 5, 2, seed=11)
+    y128, _ = _gpu(*case, mxfp8_tile_n=128)
+    y256, _ = _gpu(*case, mxfp8_tile_n=256)
+    assert torch.equal(y128, y256)
 
 
 def test_mxfp8_workload_sampled():
