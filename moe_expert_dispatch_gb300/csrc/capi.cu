@@ -118,8 +118,8 @@ BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
 // and tiled scales of h, and O.
 struct MxLayout {
   int64_t R, cap;
-  size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xq, xs, wgu_s, wd_s, hq, hs, o,
-      total;
+  size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xq, xs_tok, xs, wgu_s, wd_s,
+      hq, hs, o, total;
 };
 
 MxLayout mx_layout(int64_t T, int H, int F, int E, int k) {
@@ -140,6 +140,7 @@ MxLayout mx_layout(int64_t T, int H, int F, int E, int k) {
   L.token_of = take(L.cap * sizeof(int32_t));
   L.prob_of = take(L.cap * sizeof(float));
   L.xq = take(static_cast<size_t>(L.cap) * H);
+  L.xs_tok = take(static_cast<size_t>(T) * H / 32);
   L.xs = take(static_cast<size_t>(L.cap) * H / 32);
   L.wgu_s = take(static_cast<size_t>(E) * 2 * F * H / 32);
   L.wd_s = take(static_cast<size_t>(E) * H * F / 32);
@@ -173,6 +174,12 @@ moe_status check_block_args(int64_t T, int H, int F, int E, int k) {
   if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
+
+// Operands at most this large are kept in L2 (evict_last) while a GEMM re-reads
+// them across its N tiles; larger ones would only push the weights out.
+constexpr uint64_t kKeepInL2Bytes = 96ull << 20;
+
+int keep(uint64_t bytes) { return bytes <= kKeepInL2Bytes ? 1 : 0; }
 
 int grid_size(const moe_config& c) {
   const int sms = device_sm_count();
@@ -423,6 +430,7 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
   g1.gather_token = token_of;
   g1.counts = counts;
+  g1.keep_a = keep(static_cast<uint64_t>(L.R) * H * 2);
   const int grid = grid_size(c);
   if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, g1, grid, st)
               : launch_fc1_swiglu(ta, tg, tu, g1, grid, st)) != cudaSuccess)
@@ -439,6 +447,7 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g2.out = o;
   g2.ldo = H;
   g2.save_g = g2.save_u = nullptr;
+  g2.keep_a = keep(static_cast<uint64_t>(L.R) * F * 2);
   if (launch_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
 
@@ -547,6 +556,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gh.act_g = ag;
   gh.act_u = au;
   gh.ld_act = F;
+  gh.keep_a = keep(static_cast<uint64_t>(T) * k * H * 2);
   if (launch_dh_swiglu_bwd(t_do, t_w2k, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
 
@@ -560,6 +570,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gx.k_split = F / 64;
   gx.outf = d_xp;
   gx.ldo = H;
+  gx.keep_a = keep(static_cast<uint64_t>(T) * k * F * 4);
   if (launch_dxp(t_da, t_wgk, t_wuk, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
   if (launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
@@ -576,6 +587,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw1.outf = dw_gate;
   gw1.outf2 = dw_up;
   gw1.accumulate = accumulate_dw ? 1 : 0;
+  gw1.keep_a = keep(static_cast<uint64_t>(T) * k * H * 2);
   if (launch_wgrad(t_xp_mn, t_da_mn, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(5);
   GroupedGemmArgs gw2 = g;
@@ -585,6 +597,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw2.out_split = 0;
   gw2.outf = dw_down;
   gw2.accumulate = accumulate_dw ? 1 : 0;
+  gw2.keep_a = keep(static_cast<uint64_t>(T) * k * F * 2);
   if (launch_wgrad(t_h_mn, t_do_mn, gw2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(6);
   return MOE_OK;
@@ -629,6 +642,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   int32_t* token_of = at<int32_t>(workspace, L.token_of);
   float* prob_of = at<float>(workspace, L.prob_of);
   uint8_t* xq = at<uint8_t>(workspace, L.xq);
+  uint8_t* xs_tok = at<uint8_t>(workspace, L.xs_tok);
   uint8_t* xs = at<uint8_t>(workspace, L.xs);
   uint8_t* wgu_s = at<uint8_t>(workspace, L.wgu_s);
   uint8_t* wd_st = at<uint8_t>(workspace, L.wd_s);
@@ -641,8 +655,10 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
           cudaSuccess ||
       launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
           cudaSuccess ||
-      launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of, xq, xs,
-                              st) != cudaSuccess)
+      launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of, xq, xs_tok,
+                              st) != cudaSuccess ||
+      launch_gather_tile_scales(xs_tok, token_of, off_al, counts, E, H, L.cap, xs, st) !=
+          cudaSuccess)
     return MOE_ERR_CUDA;
   // MMA N: 256 halves the A traffic per FLOP; 128 keeps two accumulators
   const int mx_bn = c.mxfp8_tile_n == 128 ? 128
@@ -670,6 +686,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.N = F;
   g1.stages = c.ring_stages == 0 ? 6 : c.ring_stages;
   g1.bn = mx_bn;
+  g1.keep_a = keep(static_cast<uint64_t>(L.R) * H);
   g1.b_rows = F;
   g1.sfb_rows = 2 * static_cast<int64_t>(F);
   g1.sfa = xs;
@@ -687,6 +704,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g2.sfb_rows = H;
   g2.sfa = hs;
   g2.sfb = wd_st;
+  g2.keep_a = keep(static_cast<uint64_t>(L.R) * F);
   g2.hq = nullptr;
   g2.hs = nullptr;
   g2.out = o;

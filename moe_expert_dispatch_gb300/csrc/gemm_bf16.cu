@@ -255,13 +255,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full, stage_tx);
           const uint32_t sa = smem_u32(ring + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
-          // ---- A
+          // ---- A (kept in L2 only when all of A fits there: pinning a larger
+          // operand would push the weights out instead)
           if (!kAmn) {
-            tma_load_2d_hint(sa, &tmA, full, kb * BK, tl.row0, pol_keep);
+            if (p.keep_a) tma_load_2d_hint(sa, &tmA, full, kb * BK, tl.row0, pol_keep);
+            else tma_load_2d(sa, &tmA, full, kb * BK, tl.row0);
           } else {
             const int kr = tl.row0 + kb * BK;
-            tma_load_2d_hint(sa, &tmA, full, tl.m * kTileM, kr, pol_keep);
-            tma_load_2d_hint(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr, pol_keep);
+            if (p.keep_a) {
+              tma_load_2d_hint(sa, &tmA, full, tl.m * kTileM, kr, pol_keep);
+              tma_load_2d_hint(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr, pol_keep);
+            } else {
+              tma_load_2d(sa, &tmA, full, tl.m * kTileM, kr);
+              tma_load_2d(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr);
+            }
           }
           // ---- B
           if (kBmn) {

@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = smem_u32(ring + stage * kStageBytes);
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
-          tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_keep);
+          if (p.keep_a) tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_keep);
+          else tma_load_2d(sa, &tmA, full, kb * BK, row0);
           if (kFc1) {       // N/2 gate rows, then N/2 up rows, of the same N tile
             const int half = kTileN / 2;
             tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * half);
@@ -277,7 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
       if (kFc1) {
-        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F
+        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F. The tile's
+        // N/64 scale bytes of this row are adjacent in the tiled layout (one
+        // 128-wide K group of fc2): they leave in one store.
+        uint32_t packed = 0;
 #pragma unroll 1
         for (int c = 0; c < kTileN / 2; c += 32) {
           uint32_t g[32], u[32];
@@ -295,8 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
           dst[0] = make_int4(w[0], w[1], w[2], w[3]);
           dst[1] = make_int4(w[4], w[5], w[6], w[7]);
-          p.hs[mx_scale_offset(grow, col >> 5, p.N)] = sc;
+          packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
         }
+        uint8_t* hs = p.hs + mx_scale_offset(grow, (n * n_cols) >> 5, p.N);
+        if (kTileN == 256)
+          *reinterpret_cast<uint32_t*>(hs) = packed;
+        else
+          *reinterpret_cast<uint16_t*>(hs) = static_cast<uint16_t>(packed);
       } else {
         __nv_bfloat16* out = p.out + grow * p.N + n * kTileN;
 #pragma unroll 1

@@ -97,6 +97,7 @@ struct GroupedGemmArgs {
   float* outf;             // F32 output: Rows [rows, ldo]; WGrad [E, M, N or out_split]
   float* outf2;            // F32 second output (columns >= out_split)
   int accumulate;          // F32: add to the existing values
+  int keep_a;              // L2 evict_last hint on A loads (A small enough to stay resident)
   const int32_t* gather_token;  // fc1 with fused gather: token of each padded row
   const int32_t* counts;        // fc1 with fused gather: rows of each expert
   int* err;
@@ -135,10 +136,15 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
 
 // ------------------------------------------------------------------ MXFP8
 
-// codes of x in permuted rows ([cap, H], uint8) and their tiled scales.
+// codes of x in permuted rows ([cap, H], uint8) and its scales in token
+// order ([T, H/32], uint8).
 cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
-                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs,
+                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs_tok,
                                     cudaStream_t st);
+// token-order scales -> the tiled layout over the padded permuted rows.
+cudaError_t launch_gather_tile_scales(const uint8_t* xs_tok, const int32_t* token_of,
+                                      const int32_t* off_al, const int32_t* counts, int E, int K,
+                                      int64_t cap, uint8_t* xs_tiled, cudaStream_t st);
 // row-major scales -> tiled layout (see mx.cuh); pair_half > 0 interleaves
 // the gate and up weights' rows per pair_half so that one N tile of
 // 2*pair_half rows holds both halves.
@@ -155,6 +161,7 @@ struct MxGemmArgs {
   int bn;                  // MMA N: 128 or 256
   int64_t b_rows;          // rows of one expert in B's 2D view (fc1: F, fc2: H)
   int64_t sfb_rows;        // rows of one expert in B's tiled scales (fc1: 2F, fc2: H)
+  int keep_a;              // L2 evict_last hint on A loads
   const uint8_t* sfa;      // tiled scales of A
   const uint8_t* sfb;      // tiled scales of B
   uint8_t* hq;             // fc1: codes of h [rows, N]

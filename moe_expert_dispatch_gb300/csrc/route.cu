@@ -496,12 +496,13 @@ cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, 
 }
 
 // The dispatch of the MXFP8 path: one warp per token reads the bf16 row once,
-// quantises it per 32 (the same routine as quantize_mxfp8_kernel) and writes
-// the codes to each of the token's k rows and the scales in the tiled layout
-// the block-scaled MMA reads.
+// quantises it per 32 (the same routine as quantize_mxfp8_kernel), writes the
+// codes to each of the token's k rows and the scales once, in token order
+// (row-major [T, H/32]); gather_tile_scales_kernel then lays the scales out
+// per permuted row in the tiled layout.
 __global__ void __launch_bounds__(256) permute_quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t T, int H, int k,
-    const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs) {
+    const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_tok) {
   const int lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int nb = H >> 5;
@@ -512,10 +513,9 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
       const int b = base + lane;
       float v[32];
       uint32_t w[8];
-      uint8_t sc = 0;
       if (b < nb) {
         load_bf16x32_f(x + t * H + b * 32, v);
-        sc = quantize_block32(v, w);
+        xs_tok[t * nb + b] = quantize_block32(v, w);
       }
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, my_row, j);
@@ -523,58 +523,112 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
         int4* dst = reinterpret_cast<int4*>(xq + static_cast<int64_t>(r) * H + b * 32);
         dst[0] = make_int4(w[0], w[1], w[2], w[3]);
         dst[1] = make_int4(w[4], w[5], w[6], w[7]);
-        xs[mx_scale_offset(r, b, H)] = sc;
       }
     }
   }
 }
 
 cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
-                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs,
+                                    const int32_t* row_of, uint8_t* xq, uint8_t* xs_tok,
                                     cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  permute_quantize_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(x, T, H, k, row_of, xq, xs);
+  permute_quantize_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(x, T, H, k, row_of, xq, xs_tok);
   return cudaGetLastError();
 }
 
-// Row-major scales [rows, K/32] -> the tiled layout, one thread per (row,
-// 128-wide K group): 4 scale bytes in, 4 contiguous bytes out. With
+// One CTA per 128 permuted rows (one row block of the tiled layout): thread
+// i gathers the token-order scale row of permuted row i (zeros for padding
+// rows), drops its words into the block's atoms in shared memory, and the CTA
+// writes the K/128 atoms (K/32 x 128 bytes) out contiguously.
+__global__ void __launch_bounds__(128) gather_tile_scales_kernel(
+    const uint8_t* __restrict__ xs_tok, const int32_t* __restrict__ token_of,
+    const int32_t* __restrict__ off_al, const int32_t* __restrict__ counts, int E, int K,
+    uint8_t* __restrict__ xs_tiled) {
+  extern __shared__ uint32_t atoms[];        // [K/128][128] words
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileM;
+  if (r0 >= off_al[E]) return;               // capacity beyond the padded rows
+  int lo = 0, hi = E - 1;                    // the expert that owns this row block
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off_al[mid] <= r0) lo = mid; else hi = mid - 1;
+  }
+  const int64_t real_end = static_cast<int64_t>(off_al[lo]) + counts[lo];
+  const int i = threadIdx.x;
+  const int64_t r = r0 + i;
+  const int tok = r < real_end ? __ldg(token_of + r) : -1;
+  const int kgroups = K >> 7, nb = K >> 5;
+  const uint32_t* src = reinterpret_cast<const uint32_t*>(xs_tok + static_cast<int64_t>(tok) * nb);
+  const int word = (i & 31) * 4 + (i >> 5);  // (m % 32) * 16 + (m / 32) * 4 bytes
+  for (int kg = 0; kg < kgroups; ++kg) atoms[kg * 128 + word] = tok >= 0 ? __ldg(src + kg) : 0u;
+  __syncthreads();
+  int4* dst = reinterpret_cast<int4*>(xs_tiled + static_cast<int64_t>(blockIdx.x) * kgroups * 512);
+  const int4* s4 = reinterpret_cast<const int4*>(atoms);
+  for (int j = i; j < kgroups * 32; j += blockDim.x) dst[j] = s4[j];
+}
+
+cudaError_t launch_gather_tile_scales(const uint8_t* xs_tok, const int32_t* token_of,
+                                      const int32_t* off_al, const int32_t* counts, int E, int K,
+                                      int64_t cap, uint8_t* xs_tiled, cudaStream_t st) {
+  const int smem = (K >> 5) * kTileM;
+  static int configured = 0;
+  if (smem > 48 * 1024 && configured < smem) {
+    cudaError_t e = cudaFuncSetAttribute(gather_tile_scales_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  gather_tile_scales_kernel<<<static_cast<unsigned>(cap / kTileM), kTileM, smem, st>>>(
+      xs_tok, token_of, off_al, counts, E, K, xs_tiled);
+  return cudaGetLastError();
+}
+
+// Row-major scales [rows, K/32] -> the tiled layout. One CTA per 128 output
+// rows (one row block of atoms): thread i reads output row i's scale row
+// (4 bytes at a time), drops the words into the block's atoms in shared
+// memory, and the CTA writes the K/128 atoms out contiguously. With
 // pair_half = P > 0, expert e has 2*rows_per_e virtual rows cut into tiles of
 // 2P: row i of tile n is row n*P + i of src0 for i < P and row n*P + i - P of
 // src1 otherwise (the gate | up halves of one fc1 N tile).
-__global__ void __launch_bounds__(256) tile_scales_kernel(const uint8_t* __restrict__ src0,
+__global__ void __launch_bounds__(128) tile_scales_kernel(const uint8_t* __restrict__ src0,
                                                           const uint8_t* __restrict__ src1,
-                                                          int64_t out_rows, int64_t rows_per_e,
-                                                          int K, int pair_half,
+                                                          int64_t rows_per_e, int K,
+                                                          int pair_half,
                                                           uint8_t* __restrict__ dst) {
-  const int kgroups = K >> 7;
-  const int64_t n = out_rows * kgroups;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t v = i / kgroups;
-    const int kg = static_cast<int>(i - v * kgroups);
-    const uint8_t* src = src0;
-    int64_t srow = v;
-    if (pair_half > 0) {
-      const int64_t e = v / (2 * rows_per_e), vr = v - e * 2 * rows_per_e;
-      const int64_t tile = vr / (2 * pair_half), in = vr - tile * 2 * pair_half;
-      src = in < pair_half ? src0 : src1;
-      srow = e * rows_per_e + tile * pair_half + (in < pair_half ? in : in - pair_half);
-    }
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + srow * (K >> 5) + kg * 4);
-    *reinterpret_cast<uint32_t*>(dst + mx_scale_offset(v, static_cast<int64_t>(kg) * 4, K)) = w;
+  extern __shared__ uint32_t atoms[];        // [K/128][128] words
+  const int i = threadIdx.x;
+  const int64_t v = static_cast<int64_t>(blockIdx.x) * kTileM + i;
+  const uint8_t* src = src0;
+  int64_t srow = v;
+  if (pair_half > 0) {
+    const int64_t e = v / (2 * rows_per_e), vr = v - e * 2 * rows_per_e;
+    const int64_t tile = vr / (2 * pair_half), in = vr - tile * 2 * pair_half;
+    src = in < pair_half ? src0 : src1;
+    srow = e * rows_per_e + tile * pair_half + (in < pair_half ? in : in - pair_half);
   }
+  const int kgroups = K >> 7;
+  const uint32_t* s32 = reinterpret_cast<const uint32_t*>(src + srow * (K >> 5));
+  const int word = (i & 31) * 4 + (i >> 5);
+  for (int kg = 0; kg < kgroups; ++kg) atoms[kg * 128 + word] = __ldg(s32 + kg);
+  __syncthreads();
+  int4* out = reinterpret_cast<int4*>(dst + static_cast<int64_t>(blockIdx.x) * kgroups * 512);
+  const int4* s4 = reinterpret_cast<const int4*>(atoms);
+  for (int j = i; j < kgroups * 32; j += blockDim.x) out[j] = s4[j];
 }
 
 cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t out_rows,
                                int64_t rows_per_e, int K, int pair_half, uint8_t* dst,
                                cudaStream_t st) {
-  const int64_t n = out_rows * (K >> 7);
-  if (n == 0) return cudaSuccess;
-  const int64_t want = (n + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-  tile_scales_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
-      src0, src1, out_rows, rows_per_e, K, pair_half, dst);
+  if (out_rows == 0) return cudaSuccess;
+  const int smem = (K >> 5) * kTileM;
+  static int configured = 0;
+  if (smem > 48 * 1024 && configured < smem) {
+    cudaError_t e = cudaFuncSetAttribute(tile_scales_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  tile_scales_kernel<<<static_cast<unsigned>(out_rows / kTileM), kTileM, smem, st>>>(
+      src0, src1, rows_per_e, K, pair_half, dst);
   return cudaGetLastError();
 }
 
