@@ -228,6 +228,20 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_out_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, bool f32) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_stride_bytes};
+  const cuuint32_t box[2] = {f32 ? 16u : 32u, 32u};   // one epilogue warp's 32 rows
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -432,8 +446,19 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g1.counts = counts;
   g1.keep_a = keep(static_cast<uint64_t>(L.R) * H * 2);
   const int grid = grid_size(c);
-  if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, g1, grid, st)
-              : launch_fc1_swiglu(ta, tg, tu, g1, grid, st)) != cudaSuccess)
+  GemmOut o1, o2;
+  if (!make_out_tmap(&o1.map[0], h, F, L.cap, static_cast<uint64_t>(F) * 2, false) ||
+      !make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
+    return MOE_ERR_CUDA;
+  o1.map[1] = o1.map[2] = o1.map[0];
+  if (save && (!make_out_tmap(&o1.map[1], g1.save_g, F, L.cap, static_cast<uint64_t>(F) * 2,
+                              false) ||
+               !make_out_tmap(&o1.map[2], g1.save_u, F, L.cap, static_cast<uint64_t>(F) * 2,
+                              false)))
+    return MOE_ERR_CUDA;
+  o2.map[1] = o2.map[2] = o2.map[0];
+  if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, o1, g1, grid, st)
+              : launch_fc1_swiglu(ta, tg, tu, o1, g1, grid, st)) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(2);
 
@@ -448,7 +473,7 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   g2.ldo = H;
   g2.save_g = g2.save_u = nullptr;
   g2.keep_a = keep(static_cast<uint64_t>(L.R) * F * 2);
-  if (launch_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
 
   // unpermute (the combine)
@@ -557,7 +582,22 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gh.act_u = au;
   gh.ld_act = F;
   gh.keep_a = keep(static_cast<uint64_t>(T) * k * H * 2);
-  if (launch_dh_swiglu_bwd(t_do, t_w2k, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  GemmOut oh, ox, ow1, ow2;
+  if (!make_out_tmap(&oh.map[0], d_a, 2 * static_cast<uint64_t>(F), B.cap,
+                     static_cast<uint64_t>(F) * 4, false) ||
+      !make_out_tmap(&ox.map[0], d_xp, H, B.cap, static_cast<uint64_t>(H) * 4, true) ||
+      !make_out_tmap(&ow1.map[0], dw_gate, F, static_cast<uint64_t>(E) * H,
+                     static_cast<uint64_t>(F) * 4, true) ||
+      !make_out_tmap(&ow1.map[1], dw_up, F, static_cast<uint64_t>(E) * H,
+                     static_cast<uint64_t>(F) * 4, true) ||
+      !make_out_tmap(&ow2.map[0], dw_down, H, static_cast<uint64_t>(E) * F,
+                     static_cast<uint64_t>(H) * 4, true))
+    return MOE_ERR_CUDA;
+  oh.map[1] = oh.map[2] = oh.map[0];
+  ox.map[1] = ox.map[2] = ox.map[0];
+  ow1.map[2] = ow1.map[0];
+  ow2.map[1] = ow2.map[2] = ow2.map[0];
+  if (launch_dh_swiglu_bwd(t_do, t_w2k, oh, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
 
   // dXp = dA_g W1g^T + dA_u W1u^T (one reduction over 2F), then dX = sum_j dXp[row_of]
@@ -571,7 +611,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gx.outf = d_xp;
   gx.ldo = H;
   gx.keep_a = keep(static_cast<uint64_t>(T) * k * F * 4);
-  if (launch_dxp(t_da, t_wgk, t_wuk, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_dxp(t_da, t_wgk, t_wuk, ox, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
   if (launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
       cudaSuccess)
@@ -588,7 +628,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw1.outf2 = dw_up;
   gw1.accumulate = accumulate_dw ? 1 : 0;
   gw1.keep_a = keep(static_cast<uint64_t>(T) * k * H * 2);
-  if (launch_wgrad(t_xp_mn, t_da_mn, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_wgrad(t_xp_mn, t_da_mn, ow1, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(5);
   GroupedGemmArgs gw2 = g;
   gw2.M = F;
@@ -598,7 +638,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gw2.outf = dw_down;
   gw2.accumulate = accumulate_dw ? 1 : 0;
   gw2.keep_a = keep(static_cast<uint64_t>(T) * k * F * 2);
-  if (launch_wgrad(t_h_mn, t_do_mn, gw2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_wgrad(t_h_mn, t_do_mn, ow2, gw2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(6);
   return MOE_OK;
 }

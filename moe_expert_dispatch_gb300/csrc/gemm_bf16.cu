@@ -118,16 +118,30 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f)
   }
 }
 
+// Epilogue output pieces: each epilogue warp finishes its 32 rows of the
+// tile in pieces of 32 rows x 64 bytes (32 bf16 or 16 float columns), staged
+// in its own shared-memory slots with the 64-byte swizzle (16-byte chunk j
+// of row r at chunk j ^ ((r >> 1) & 3): a warp's row writes take 4
+// wavefronts, the minimum for 512 bytes) and stored by its lane 0 with a TMA
+// tensor store. Warps never wait for each other.
+constexpr int kPieceBytes = 32 * 64;       // 2 KB
+constexpr int kSlotsPerWarp = 3;
+constexpr int kPieceArea = 4 * kSlotsPerWarp * kPieceBytes;   // 24 KB
+
 template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
-                        const __grid_constant__ CUtensorMap tmB1, GroupedGemmArgs p) {
+                        const __grid_constant__ CUtensorMap tmB1,
+                        const __grid_constant__ CUtensorMap tmO0,
+                        const __grid_constant__ CUtensorMap tmO1,
+                        const __grid_constant__ CUtensorMap tmO2, GroupedGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  Smem* sm = reinterpret_cast<Smem*>(ring + S * kStageBytes);
+  uint8_t* pieces = ring + 4 * kStageBytes;  // after the largest ring, 1 KB aligned
+  Smem* sm = reinterpret_cast<Smem*>(pieces + kPieceArea);
   int* ts = reinterpret_cast<int*>(sm + 1);  // [E+1] first tile of each expert (Rows)
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int E = p.E;
@@ -153,6 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB0);
     tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmO0);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
@@ -368,7 +383,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
-    const int row_in_tile = q * 32 + lane;
+    const int r = q * 32 + lane;              // row of the tile this thread finishes
+    const uint32_t slot0 = smem_u32(pieces) + q * kSlotsPerWarp * kPieceBytes;
+    const uint32_t my_row = lane * 64;
+    const uint32_t sw = (lane >> 1) & 3;
+    int npiece = 0;
+    // a piece: wait for the warp's next slot, fill this lane's row, store it
+    auto piece_slot = [&]() -> uint32_t {
+      if (lane == 0) bulk_wait_group_read<kSlotsPerWarp - 1>();
+      __syncwarp();
+      return slot0 + (npiece % kSlotsPerWarp) * kPieceBytes;
+    };
+    auto put_row = [&](uint32_t slot, const uint32_t* w16) {   // 16 words = 64 bytes
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + my_row +
+                                                                       ((j ^ sw) << 4)),
+                     "r"(w16[4 * j]), "r"(w16[4 * j + 1]), "r"(w16[4 * j + 2]),
+                     "r"(w16[4 * j + 3])
+                     : "memory");
+    };
+    auto piece_out = [&](uint32_t slot, const CUtensorMap* map, int x, int y, bool add) {
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (add) tma_reduce_add_2d(map, slot, x, y + q * 32);
+        else tma_store_2d(map, slot, x, y + q * 32);
+        bulk_commit_group();
+      }
+      ++npiece;
+    };
+    auto bf16_piece = [&](const uint32_t* f32x32, const CUtensorMap* map, int x, int y) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(f32x32[2 * i]), __uint_as_float(f32x32[2 * i + 1]));
+      const uint32_t slot = piece_slot();
+      put_row(slot, w);
+      piece_out(slot, map, x, y, false);
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
@@ -383,9 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
       if (kEpi == Epi::SwigluFwd) {
-        const int64_t grow = tl.row0 + row_in_tile;
         const int n0 = tl.n * (bn / 2);
-        __nv_bfloat16* out = p.out + grow * p.ldo + n0;
 #pragma unroll 1
         for (int c = 0; c < bn / 2; c += 32) {
           uint32_t g[32], u[32];
@@ -399,37 +450,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
             hw[i] = pack_bf16x2(silu_f(g0) * u0, silu_f(g1) * u1);
           }
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_global_v4(out + c + 8 * i, hw[4 * i], hw[4 * i + 1], hw[4 * i + 2], hw[4 * i + 3]);
+          const uint32_t slot = piece_slot();
+          put_row(slot, hw);
+          piece_out(slot, &tmO0, n0 + c, tl.row0, false);
           if (p.save_g) {
-            store_bf16x32(p.save_g + grow * p.ldo + n0 + c, g);
-            store_bf16x32(p.save_u + grow * p.ldo + n0 + c, u);
+            bf16_piece(g, &tmO1, n0 + c, tl.row0);
+            bf16_piece(u, &tmO2, n0 + c, tl.row0);
           }
         }
       } else if (kEpi == Epi::Bf16) {
-        const int64_t grow = tl.row0 + row_in_tile;
-        __nv_bfloat16* out = p.out + grow * p.ldo + tl.n * bn;
 #pragma unroll 1
         for (int c = 0; c < bn; c += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c, r);
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(taddr + c, v);
           tmem_ld_wait();
-          store_bf16x32(out + c, r);
+          bf16_piece(v, &tmO0, tl.n * bn + c, tl.row0);
         }
       } else if (kEpi == Epi::SwigluBwd) {
         // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s), s = sigmoid(A_g)
-        const int64_t grow = tl.row0 + row_in_tile;
+        const int64_t grow = tl.row0 + r;
         const int f0 = tl.n * bn;
         const __nv_bfloat16* ag = p.act_g + grow * p.ld_act + f0;
         const __nv_bfloat16* au = p.act_u + grow * p.ld_act + f0;
-        __nv_bfloat16* dg = p.out + grow * p.ldo + f0;
-        __nv_bfloat16* du = p.out + grow * p.ldo + p.out_split + f0;
 #pragma unroll 1
         for (int c = 0; c < bn; c += 32) {
-          uint32_t r[32];
+          uint32_t v[32];
           float fg[32], fu[32];
-          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_32x32b_x32(taddr + c, v);
           load_bf16x32(ag + c, fg);
           load_bf16x32(au + c, fu);
           tmem_ld_wait();
@@ -439,62 +486,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             float vg[2], vu[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const float dh = __uint_as_float(r[2 * i + h]);
+              const float dh = __uint_as_float(v[2 * i + h]);
               const float a = fg[2 * i + h], b = fu[2 * i + h];
-              const float s = 1.0f / (1.0f + __expf(-a));
-              vg[h] = dh * b * s * (1.0f + a * (1.0f - s));
-              vu[h] = dh * a * s;
+              const float sg = 1.0f / (1.0f + __expf(-a));
+              vg[h] = dh * b * sg * (1.0f + a * (1.0f - sg));
+              vu[h] = dh * a * sg;
             }
             wg[i] = pack_bf16x2(vg[0], vg[1]);
             wu[i] = pack_bf16x2(vu[0], vu[1]);
           }
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            st_global_v4(dg + c + 8 * i, wg[4 * i], wg[4 * i + 1], wg[4 * i + 2], wg[4 * i + 3]);
-            st_global_v4(du + c + 8 * i, wu[4 * i], wu[4 * i + 1], wu[4 * i + 2], wu[4 * i + 3]);
-          }
+          uint32_t slot = piece_slot();
+          put_row(slot, wg);
+          piece_out(slot, &tmO0, f0 + c, tl.row0, false);
+          slot = piece_slot();
+          put_row(slot, wu);
+          piece_out(slot, &tmO0, p.out_split + f0 + c, tl.row0, false);
         }
       } else {  // Epi::F32: float rows (Rows) or weight-gradient rows (WGrad)
-        float* out;
-        if (kSched == Sched::Rows) {
-          out = p.outf + (tl.row0 + row_in_tile) * p.ldo + tl.n * bn;
-        } else {
-          const int64_t wrow = static_cast<int64_t>(tl.m) * kTileM + row_in_tile;
-          int col = tl.n * bn;
-          float* base = p.outf;
-          int ldn = p.N;
-          if (p.out_split > 0) {             // two outputs side by side along N
-            ldn = p.out_split;
-            if (col >= p.out_split) {
-              base = p.outf2;
-              col -= p.out_split;
-            }
+        const CUtensorMap* map = &tmO0;
+        int col = tl.n * bn;
+        int y = tl.row0;
+        if (kSched == Sched::WGrad) {
+          y = tl.e * p.M + tl.m * kTileM;
+          if (p.out_split > 0 && col >= p.out_split) {   // second output, same layout
+            map = &tmO1;
+            col -= p.out_split;
           }
-          out = base + (static_cast<int64_t>(tl.e) * p.M + wrow) * ldn + col;
         }
+        const bool add = p.accumulate != 0;
+        if (tl.kblocks == 0 && add) {
+          // an expert without rows adds nothing to the gradients
+        } else {
 #pragma unroll 1
-        for (int c = 0; c < bn; c += 32) {
-          uint32_t r[32];
-          if (tl.kblocks > 0) {
-            tmem_ld_32x32b_x32(taddr + c, r);
-            tmem_ld_wait();
-          } else {
+          for (int c = 0; c < bn; c += 32) {
+            uint32_t v[32];
+            if (tl.kblocks > 0) {
+              tmem_ld_32x32b_x32(taddr + c, v);
+              tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;   // an expert without rows
-          }
-          float4* o4 = reinterpret_cast<float4*>(out + c);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-            if (p.accumulate) {
-              const float4 old = o4[i];
-              v.x += old.x;
-              v.y += old.y;
-              v.z += old.z;
-              v.w += old.w;
+              for (int i = 0; i < 32; ++i) v[i] = 0u;      // an expert without rows
             }
-            o4[i] = v;
+            uint32_t slot = piece_slot();
+            put_row(slot, v);
+            piece_out(slot, map, col + c, y, add);
+            slot = piece_slot();
+            put_row(slot, v + 16);
+            piece_out(slot, map, col + c + 16, y, add);
           }
         }
       }
@@ -503,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_group_all();     // every store has landed before exit
   }
 
   tc_fence_before();
@@ -513,17 +552,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-size_t gemm_smem_bytes(int stages, int E) {
-  return 1024 + static_cast<size_t>(stages) * kStageBytes + sizeof(Smem) +
+size_t gemm_smem_bytes(int E) {
+  return 1024 + 4 * static_cast<size_t>(kStageBytes) + kPieceArea + sizeof(Smem) +
          static_cast<size_t>(E + 1) * sizeof(int);
 }
 
 template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+                        const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
   // always the 4-stage size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
-  const size_t smem = gemm_smem_bytes(4, kMaxExperts);
+  const size_t smem = gemm_smem_bytes(kMaxExperts);
   static bool configured = false;
   auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather>;
   if (!configured) {
@@ -532,41 +571,43 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUten
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  kern<<<grid, kThreads, smem, st>>>(a, b0, b1, p);
+  kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                              const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows>(a, wg, wu, p, grid, st);
+                              const GemmOut& o, const GroupedGemmArgs& p, int grid,
+                              cudaStream_t st) {
+  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows>(a, wg, wu, o, p, grid, st);
 }
 
 cudaError_t launch_fc1_swiglu_gather(const CUtensorMap& x_rows, const CUtensorMap& wg,
-                                     const CUtensorMap& wu, const GroupedGemmArgs& p, int grid,
-                                     cudaStream_t st) {
-  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows, true>(x_rows, wg, wu, p, grid, st);
+                                     const CUtensorMap& wu, const GemmOut& o,
+                                     const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::SwigluFwd, false, true, Sched::Rows, true>(x_rows, wg, wu, o, p, grid,
+                                                                     st);
 }
 
-cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
-                       int grid, cudaStream_t st) {
-  return launch_impl<Epi::Bf16, false, true, Sched::Rows>(a, w, w, p, grid, st);
+cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GemmOut& o,
+                       const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::Bf16, false, true, Sched::Rows>(a, w, w, o, p, grid, st);
 }
 
-cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2,
+cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
                                  const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_impl<Epi::SwigluBwd, false, false, Sched::Rows>(a, w2, w2, p, grid, st);
+  return launch_impl<Epi::SwigluBwd, false, false, Sched::Rows>(a, w2, w2, o, p, grid, st);
 }
 
 cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                       const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_impl<Epi::F32, false, false, Sched::Rows>(a, wg, wu, p, grid, st);
+                       const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::F32, false, false, Sched::Rows>(a, wg, wu, o, p, grid, st);
 }
 
-cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GroupedGemmArgs& p,
-                         int grid, cudaStream_t st) {
-  return launch_impl<Epi::F32, true, true, Sched::WGrad>(a, b, b, p, grid, st);
+cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
+                         const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_impl<Epi::F32, true, true, Sched::WGrad>(a, b, b, o, p, grid, st);
 }
 
 }  // namespace moe

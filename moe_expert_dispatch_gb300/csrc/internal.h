@@ -108,26 +108,42 @@ struct GroupedGemmArgs {
 bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
+// Output tensor maps of a grouped GEMM's epilogue: boxes of 32 rows x 64
+// bytes with the 64-byte swizzle (see make_out_tmap). Unused maps may repeat
+// a used one.
+struct GemmOut {
+  CUtensorMap map[3];
+};
+// A 2D output map over a row-major [outer, inner] tensor of bf16 (f32 = false)
+// or float elements.
+bool make_out_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_stride_bytes, bool f32);
+
 // fc1: out = bf16(silu(A W_gate) * (A W_up)), A rows tiled per expert.
+// Outputs: h (map 0) and, with save_g, A_g and A_u (maps 1, 2).
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                              const GroupedGemmArgs& p, int grid, cudaStream_t st);
+                              const GemmOut& o, const GroupedGemmArgs& p, int grid,
+                              cudaStream_t st);
 // fc1 with the dispatch fused into its producer: A rows are gathered from
 // the token rows of x (tensor map with a one-row box) by TMA gather4.
 cudaError_t launch_fc1_swiglu_gather(const CUtensorMap& x_rows, const CUtensorMap& wg,
-                                     const CUtensorMap& wu, const GroupedGemmArgs& p, int grid,
-                                     cudaStream_t st);
-// fc2: out = bf16(A W).
-cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GroupedGemmArgs& p,
-                       int grid, cudaStream_t st);
-// backward: dH = dO W2^T with the SwiGLU-backward epilogue (W2 read K-major).
-cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2,
+                                     const CUtensorMap& wu, const GemmOut& o,
+                                     const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// fc2: out = bf16(A W) (map 0).
+cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GemmOut& o,
+                       const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// backward: dH = dO W2^T with the SwiGLU-backward epilogue (W2 read K-major);
+// dA_g and dA_u into one [rows, 2F] tensor (map 0, columns [0, F) and [F, 2F)).
+cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
                                  const GroupedGemmArgs& p, int grid, cudaStream_t st);
 // backward: dXp = [dA_g | dA_u] [W1g ; W1u]^T in float (K split between the two weights).
 cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                       const GroupedGemmArgs& p, int grid, cudaStream_t st);
-// backward: dW_e = A_e^T B_e over each expert's rows, both operands MN-major.
-cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GroupedGemmArgs& p,
-                         int grid, cudaStream_t st);
+                       const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st);
+// backward: dW_e = A_e^T B_e over each expert's rows, both operands MN-major;
+// float rows of [E*M, N] (map 0; map 1 for columns >= out_split), stored or,
+// with accumulate, added (TMA reduce-add).
+cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
+                         const GroupedGemmArgs& p, int grid, cudaStream_t st);
 
 // backward: dO[r] = bf16(prob_of[r] dY[token_of[r]]) and dprobs[t, j] = <dY_t, O[row_of[t, j]]>.
 cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const int32_t* row_of,
