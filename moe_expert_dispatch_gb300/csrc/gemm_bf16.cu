@@ -128,7 +128,7 @@ constexpr int kPieceBytes = 32 * 64;       // 2 KB
 constexpr int kSlotsPerWarp = 3;
 constexpr int kPieceArea = 4 * kSlotsPerWarp * kPieceBytes;   // 24 KB
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -145,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   int* ts = reinterpret_cast<int*>(sm + 1);  // [E+1] first tile of each expert (Rows)
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int E = p.E;
-  const int bn = p.bn;
+  constexpr int bn = kBN;                     // MMA N
   const int n_tiles = p.N / (kEpi == Epi::SwigluFwd ? bn / 2 : bn);
-  const uint32_t stage_tx = kABytes + (bn / 64) * kBBox;
+  constexpr uint32_t stage_tx = kABytes + (bn / 64) * kBBox;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -200,10 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // all2all_grouped_matmul folded into the GEMM's producer.
     int stage = 0;
     uint32_t phase = 0;
-    uint32_t last_par[4] = {0, 0, 0, 0};
-    bool used[4] = {false, false, false, false};
+    uint32_t fills = 0;
     bool ok = true;
-    const uint64_t pol_keep = l2_policy_evict_last();
     for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
       const Tile tl = decode_tile<kSched>(t, ts, p);
       const int real_end = p.off_al[tl.e] + p.counts[tl.e];
@@ -233,34 +231,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, n0 + 64 * j, krow + kb * BK);
           }
         }
-        last_par[stage] = phase;
-        used[stage] = true;
+        ++fills;
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
         }
       }
     }
-    (void)pol_keep;
     if (!ok && lane == 0) {
       sm->abort = 1;
       report_error(p.err, kErrTimeout);
     }
+    // every issued copy must land before the CTA may exit: the last S fills
+    // (fill i went to slot i % S with phase parity (i / S) & 1)
     if (lane == 0)
-      for (int s = 0; s < S; ++s)
-        if (used[s]) mbar_wait(smem_u32(&sm->full[s]), last_par[s], kDrainNs, &sm->zero);
+      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
+        mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
   } else if (warp == 0) {
     // ---------------------------------------------------------- producer
+    // One thread; it is on the critical path of every k-block, so the loop
+    // body is straight-line: box counts are compile-time, the L2 policy of A
+    // is a value chosen once (operands re-read by many tiles of their expert
+    // stay in L2 longer when all of A fits there; pinning a larger operand
+    // would push the weights out instead).
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t last_par[4] = {0, 0, 0, 0};
-      bool used[4] = {false, false, false, false};
+      uint32_t fills = 0;
       bool ok = true;
-      // operands re-read by many tiles of their expert stay in L2 longer
-      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
+      const uint32_t ring0 = smem_u32(ring);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         const Tile tl = decode_tile<kSched>(t, ts, p);
+        // per-tile coordinates
+        const int a_x0 = kAmn ? tl.m * kTileM : 0;
+        const int a_y0 = tl.row0;
+        const int b_row0 = (kSched == Sched::Rows) ? tl.e * static_cast<int>(p.b_rows) : tl.row0;
+        const int b_n0 = (kEpi == Epi::SwigluFwd) ? tl.n * (bn / 2) : tl.n * bn;
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           const uint32_t full = smem_u32(&sm->full[stage]);
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
@@ -268,47 +275,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full, stage_tx);
-          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sa = ring0 + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
-          // ---- A (kept in L2 only when all of A fits there: pinning a larger
-          // operand would push the weights out instead)
+          const int k0 = kb * BK;
           if (!kAmn) {
-            if (p.keep_a) tma_load_2d_hint(sa, &tmA, full, kb * BK, tl.row0, pol_keep);
-            else tma_load_2d(sa, &tmA, full, kb * BK, tl.row0);
+            tma_load_2d_hint(sa, &tmA, full, k0, a_y0, pol_a);
           } else {
-            const int kr = tl.row0 + kb * BK;
-            if (p.keep_a) {
-              tma_load_2d_hint(sa, &tmA, full, tl.m * kTileM, kr, pol_keep);
-              tma_load_2d_hint(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr, pol_keep);
-            } else {
-              tma_load_2d(sa, &tmA, full, tl.m * kTileM, kr);
-              tma_load_2d(sa + kBBox, &tmA, full, tl.m * kTileM + 64, kr);
-            }
+            tma_load_2d_hint(sa, &tmA, full, a_x0, a_y0 + k0, pol_a);
+            tma_load_2d_hint(sa + kBBox, &tmA, full, a_x0 + 64, a_y0 + k0, pol_a);
           }
-          // ---- B
           if (kBmn) {
-            const int krow = (kSched == Sched::Rows) ? tl.e * p.b_rows + kb * BK
-                                                      : tl.row0 + kb * BK;
-            if (p.b_split == 1) {            // gate / up halves of one N tile
-              const int n0 = tl.n * (bn / 2);
+            const int krow = b_row0 + k0;
+            if (kEpi == Epi::SwigluFwd) {    // gate | up halves of one N tile
+#pragma unroll
               for (int j = 0; j < bn / 128; ++j) {
-                tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow);
-                tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, n0 + 64 * j, krow);
+                tma_load_2d(sb + j * kBBox, &tmB0, full, b_n0 + 64 * j, krow);
+                tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, b_n0 + 64 * j, krow);
               }
             } else {
-              const int n0 = tl.n * bn;
+#pragma unroll
               for (int j = 0; j < bn / 64; ++j)
-                tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow);
+                tma_load_2d(sb + j * kBBox, &tmB0, full, b_n0 + 64 * j, krow);
             }
           } else {                           // K-major B: one box of bn rows
-            const int nrow = tl.e * p.b_rows + tl.n * bn;
+            const int nrow = b_row0 + b_n0;
             if (p.b_split == 2 && kb >= p.k_split)
-              tma_load_2d(sb, &tmB1, full, (kb - p.k_split) * BK, nrow);
+              tma_load_2d(sb, &tmB1, full, k0 - p.k_split * BK, nrow);
             else
-              tma_load_2d(sb, &tmB0, full, kb * BK, nrow);
+              tma_load_2d(sb, &tmB0, full, k0, nrow);
           }
-          last_par[stage] = phase;
-          used[stage] = true;
+          ++fills;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -319,14 +315,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->abort = 1;
         report_error(p.err, kErrTimeout);
       }
-      // every issued copy must land before the CTA may exit
-      for (int s = 0; s < S; ++s)
-        if (used[s]) mbar_wait(smem_u32(&sm->full[s]), last_par[s], kDrainNs, &sm->zero);
+      // every issued copy must land before the CTA may exit: the last S fills
+      // (fill i went to slot i % S with phase parity (i / S) & 1)
+      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
+        mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kTileM, bn, kAmn, kBmn);
+      // descriptors of slot 0; a slot adds kStageBytes, a K=16 step adds 32 B
+      // (K-major) or 16 rows = 2 KB (MN-major) to the 16-byte start field
+      const uint32_t ring0 = smem_u32(ring);
+      const uint64_t adesc0 = kAmn ? sdesc_sw128(ring0, kBBox, 1024) : sdesc_sw128(ring0, 16, 1024);
+      const uint64_t bdesc0 = kBmn ? sdesc_sw128(ring0 + kABytes, kBBox, 1024)
+                                   : sdesc_sw128(ring0 + kABytes, 16, 1024);
+      constexpr uint64_t kAStep = kAmn ? (2048 >> 4) : (32 >> 4);
+      constexpr uint64_t kBStep = kBmn ? (2048 >> 4) : (32 >> 4);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -346,19 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(ring + stage * kStageBytes);
-          const uint32_t b0 = a0 + kABytes;
+          // K-major, 128B swizzle: 8-row groups 1024 B apart, +32 B per K=16.
+          // MN-major, 128B swizzle: 64-wide atoms 8 KB apart (LBO), 8-row K
+          // groups 1024 B apart (SBO), +16 rows = 2 KB per K=16.
+          const uint64_t soff = static_cast<uint64_t>(stage) * (kStageBytes >> 4);
+          const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            // K-major, 128B swizzle: 8-row groups 1024 B apart, +32 B per K=16.
-            // MN-major, 128B swizzle: 64-wide atoms 8 KB apart (LBO), 8-row K
-            // groups 1024 B apart (SBO), +16 rows = 2 KB per K=16.
-            const uint64_t ad = kAmn ? sdesc_sw128(a0 + ks * 2048, kBBox, 1024)
-                                     : sdesc_sw128(a0 + ks * 32, 16, 1024);
-            const uint64_t bd = kBmn ? sdesc_sw128(b0 + ks * 2048, kBBox, 1024)
-                                     : sdesc_sw128(b0 + ks * 32, 16, 1024);
-            umma_bf16(d, ad, bd, idesc, (kb | ks) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_bf16(d, ad + ks * kAStep, bd + ks * kBStep, idesc, (kb | ks) ? 1u : 0u);
           umma_commit(smem_u32(&sm->empty[stage]));
           issued = true;
           if (++stage == S) {
@@ -557,14 +557,14 @@ size_t gemm_smem_bytes(int E) {
          static_cast<size_t>(E + 1) * sizeof(int);
 }
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
-cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                        const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN>
+cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                      const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
   // always the 4-stage size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
   const size_t smem = gemm_smem_bytes(kMaxExperts);
   static bool configured = false;
-  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather>;
+  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather, kBN>;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -573,6 +573,14 @@ cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUten
   }
   kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
   return cudaGetLastError();
+}
+
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
+cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                        const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  if (kEpi == Epi::SwigluFwd || p.bn == 256)
+    return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 256>(a, b0, b1, o, p, grid, st);
+  return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 128>(a, b0, b1, o, p, grid, st);
 }
 
 }  // namespace

@@ -146,10 +146,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t last_par[kMaxStages] = {};
-      bool used[kMaxStages] = {};
+      uint32_t fills = 0;
       bool ok = true;
-      const uint64_t pol_keep = l2_policy_evict_last();
+      const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
+      const uint32_t ring0 = smem_u32(ring);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
         int e, m, n;
         decode(t, e, m, n);
@@ -162,11 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full, kABytes + kBBytes + (1 + G::kSfbAtoms) * kSfBytes);
-          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sa = ring0 + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
-          if (p.keep_a) tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_keep);
-          else tma_load_2d(sa, &tmA, full, kb * BK, row0);
+          tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_a);
           if (kFc1) {       // N/2 gate rows, then N/2 up rows, of the same N tile
             const int half = kTileN / 2;
             tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * half);
@@ -181,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < G::kSfbAtoms; ++j)
             bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
                           p.sfb + (((vrow >> 7) + j) * kgroups + kb) * kSfBytes, kSfBytes, full);
-          last_par[stage] = phase;
-          used[stage] = true;
+          ++fills;
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -193,8 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm->abort = 1;
         report_error(p.err, kErrTimeout);
       }
-      for (int s = 0; s < S; ++s)
-        if (used[s]) mbar_wait(smem_u32(&sm->full[s]), last_par[s], kDrainNs, &sm->zero);
+      // the last S fills must land before exit (fill i: slot i % S, parity (i / S) & 1)
+      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
+        mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -217,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(ring + stage * kStageBytes);
+          const uint32_t sa = smem_u32(ring) + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
           // this slot's scales into its own TMEM columns: A at +0..3, B's
@@ -229,13 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < G::kSfbAtoms; ++j)
             tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
                                    sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
+          const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < BK / 32; ++ks) {
-            const uint64_t ad = sdesc_sw128(sa + ks * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(sb + ks * 32, 16, 1024);
-            umma_mxf8(d, ad, bd, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t, sfb_t,
-                      (kb | ks) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < BK / 32; ++ks)      // +32 B of K per MMA
+            umma_mxf8(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t,
+                      sfb_t, (kb | ks) ? 1u : 0u);
           umma_commit(smem_u32(&sm->empty[stage]));
           issued = true;
           if (++stage == S) {
