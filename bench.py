@@ -38,7 +38,12 @@ import synth  # noqa: E402
 # DRAM bytes (read + write) per launch of the dominant kernel on a workload,
 # from the ncu captures summarised in profiles/, with the hash of the kernel
 # source they were taken on; reported as null once that source changes.
-TRAFFIC = {}
+TRAFFIC = {
+    # fc1 on the Mixtral-shaped workload: the 2-expert capture (610.2 MB for
+    # 620.8 MB algorithmic) scaled by the algorithmic bytes of the full launch
+    # (2181 MB); see profiles/grouped_gemm_mixtral_2experts_ncu_full.md
+    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2144e6, "src_sha": "da34c7a85b08ac65"},
+}
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
