@@ -32,7 +32,15 @@ namespace {
 constexpr int BK = 128;                    // E4M3 elements (bytes) per k-block
 constexpr int kABytes = kTileM * BK;       // 16 KB
 constexpr int kSfBytes = 512;              // one scale atom (128 rows x 4 blocks of 32)
-constexpr int kThreads = 192;
+// warp 0 producer, warp 1 MMA issuer, then the epilogue warps. fc1's
+// epilogue (SwiGLU + quantisation) is heavy: 8 warps, two per TMEM lane
+// quadrant, each finishing half of the tile's columns, halve its exposed
+// part. fc2's (bf16 stores) is light: 4 warps (more only take issue slots
+// from the producer and MMA threads).
+template <bool kFc1>
+constexpr int epi_warps() { return kFc1 ? 8 : 4; }
+template <bool kFc1>
+constexpr int num_threads() { return 64 + 32 * epi_warps<kFc1>(); }
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
@@ -67,7 +75,7 @@ struct Smem {
 };
 
 template <bool kFc1, int kTileN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(num_threads<kFc1>(), 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, MxGemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -93,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm->tfull[a]), 1);
-      mbar_init(smem_u32(&sm->tempty[a]), 4 * 32);
+      mbar_init(smem_u32(&sm->tempty[a]), epi_warps<kFc1>() * 32);
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort = 0;
@@ -109,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  for (int e = threadIdx.x; e < E; e += kThreads)
+  for (int e = threadIdx.x; e < E; e += num_threads<kFc1>())
     ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -258,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ---------------------------------------------------------- epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;                   // TMEM lane quadrant of this warp
+    const int half = (warp - 2) >> 2;         // fc1: which half of the tile's columns
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
@@ -274,53 +283,65 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
+      // The whole accumulator row is read into registers (packed bf16, or
+      // the finished E4M3 codes for fc1) and the accumulator is released
+      // before any global store, so that with a single accumulator the
+      // stores still overlap the next tile's MMAs.
       if (kFc1) {
         // h = bf16(silu(gate) * up), then MXFP8 per 32 along F. The tile's
         // N/64 scale bytes of this row are adjacent in the tiled layout (one
         // 128-wide K group of fc2): they leave in one store.
+        // this warp's half of the tile's h columns: kTileN / 4 of them
+        constexpr int kHalf = kTileN / 4;
+        const int c0 = half * kHalf;
+        uint32_t codes[kHalf / 4];
         uint32_t packed = 0;
-#pragma unroll 1
-        for (int c = 0; c < kTileN / 2; c += 32) {
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 32) {
           uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(taddr + c, g);
-          tmem_ld_32x32b_x32(taddr + kTileN / 2 + c, u);
+          tmem_ld_32x32b_x32(taddr + c0 + c, g);
+          tmem_ld_32x32b_x32(taddr + kTileN / 2 + c0 + c, u);
           tmem_ld_wait();
           float hv[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             hv[i] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(g[i])) *
                                                          __uint_as_float(u[i])));
-          uint32_t w[8];
-          const uint8_t sc = quantize_block32(hv, w);
-          const int col = n * n_cols + c;
-          int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
-          dst[0] = make_int4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+          const uint8_t sc = quantize_block32(hv, &codes[c / 4]);
           packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
         }
-        uint8_t* hs = p.hs + mx_scale_offset(grow, (n * n_cols) >> 5, p.N);
-        if (kTileN == 256)
-          *reinterpret_cast<uint32_t*>(hs) = packed;
-        else
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        const int col = n * n_cols + c0;
+        int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
+#pragma unroll
+        for (int i = 0; i < kHalf / 16; ++i)
+          dst[i] = make_int4(codes[4 * i], codes[4 * i + 1], codes[4 * i + 2], codes[4 * i + 3]);
+        uint8_t* hs = p.hs + mx_scale_offset(grow, col >> 5, p.N);
+        if (kHalf == 64)
           *reinterpret_cast<uint16_t*>(hs) = static_cast<uint16_t>(packed);
+        else
+          *hs = static_cast<uint8_t>(packed);
       } else {
-        __nv_bfloat16* out = p.out + grow * p.N + n * kTileN;
-#pragma unroll 1
-        for (int c = 0; c < kTileN; c += 32) {
+        constexpr int kHalf = kTileN;           // this warp's columns: all of them
+        const int c0 = 0;
+        uint32_t w[kHalf / 2];
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 32) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c, r);
+          tmem_ld_32x32b_x32(taddr + c0 + c, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_global_v4(out + c + 8 * i,
-                         pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                         pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
+          for (int i = 0; i < 16; ++i)
+            w[c / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
         }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        __nv_bfloat16* out = p.out + grow * p.N + n * kTileN + c0;
+#pragma unroll
+        for (int i = 0; i < kHalf / 8; ++i)
+          st_global_v4(out + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&sm->tempty[acc]));
       if (++acc == G::kAccBufs) {
         acc = 0;
         acc_phase ^= 1;
@@ -350,7 +371,7 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mx_gemm_kernel<kFc1, kN><<<grid, kThreads, smem, st>>>(a, b0, b1, p);
+  mx_gemm_kernel<kFc1, kN><<<grid, num_threads<kFc1>(), smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
 }
 
