@@ -302,17 +302,47 @@ def run_ours(args, w):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     parts = {}
+    graph = None
+    if args.graph:
+        # the whole step (every kernel of the block, launched through the C
+        # ABI) captured once into a CUDA graph and replayed; step times come
+        # from events on the launching stream around each replay, per-kernel
+        # times from the ordinary stream launches below (events recorded
+        # inside a graph cannot be timed)
+        gstream = torch.cuda.Stream()
+        gstream.wait_stream(stream)
+        with torch.cuda.stream(gstream):
+            run.step(False)                   # warm the capture stream
+            torch.cuda.current_stream().synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gstream):
+                run.step(False)
+        stream.wait_stream(gstream)
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.zero_()
+            run.step(True)
+            run.fev[-1].synchronize()
+            if run.bev:
+                run.bev[-1].synchronize()
+            for key, v in run.parts().items():
+                parts[key] = parts.get(key, 0.0) + v
+        torch.cuda.synchronize()
     _barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
-            run.step(True)
+            if graph is not None:
+                graph.replay()
+            else:
+                run.step(True)
             ends[i].record(stream)
             ends[i].synchronize()
-            for key, v in run.parts().items():
-                parts[key] = parts.get(key, 0.0) + v
+            if graph is None:
+                for key, v in run.parts().items():
+                    parts[key] = parts.get(key, 0.0) + v
         torch.cuda.synchronize()
     _barrier(ws)
     ms = _max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)])), ws,
@@ -376,6 +406,7 @@ def run_ours(args, w):
                                                                    w.backward and not w.mxfp8)
                    else "materialised permute",
                    "l2": "flushed before every step (512 MB write)",
+                   "launch": "one CUDA graph per step" if args.graph else "stream launches",
                    "parallelism": "replicas" if ws > 1 else "single"},
         "roofline": {"bound": "tensor", "kernel": f"{dominant} (grouped GEMM)",
                      "achieved": tflops[dominant], "peak": peak, "unit": "TFLOP/s",
@@ -411,6 +442,8 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mxfp8-tile-n", type=int, default=0, choices=[0, 128, 256])
+    ap.add_argument("--graph", action="store_true",
+                    help="capture each step once into a CUDA graph and replay it")
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,
                     help="BF16 forward: fc1 gathers the routed rows itself (no permuted copy)")
     args = ap.parse_args()

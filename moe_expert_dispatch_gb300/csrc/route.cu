@@ -273,101 +273,156 @@ __device__ __forceinline__ void acc_bf16x8(float* acc, const int4& v, float p) {
   }
 }
 
-// One warp per token: y[t] = bf16(sum_j p_j o[row_j]), j in order, float
-// accumulation; 8 bf16 per lane per step.
+// y[t] = bf16(sum_j p_j o[row_j]), j in order, float accumulation. One warp
+// per (token, column chunk of 32 lanes x kUnpermU 16-byte vectors): a short
+// row count still gives every SM a full set of warps. Slot pairs are loaded
+// together so two rows are in flight before either is accumulated.
+constexpr int kUnpermU = 2;
+
 __global__ void __launch_bounds__(256) unpermute_kernel(const __nv_bfloat16* __restrict__ o,
                                                         const int32_t* __restrict__ row_of,
                                                         const float* __restrict__ probs,
                                                         int64_t T, int k, int H,
                                                         __nv_bfloat16* __restrict__ y) {
-  constexpr int U = 2;
+  constexpr int U = kUnpermU;
   const int lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n8 = H >> 3;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       t < T; t += warps) {
+  const int chunks = (n8 + 32 * U - 1) / (32 * U);
+  const int64_t tasks = T * chunks;
+  for (int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       task < tasks; task += warps) {
+    const int64_t t = task / chunks;
+    const int c0 = static_cast<int>(task - t * chunks) * 32 * U + lane;
     const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
     const float my_p = lane < k ? (probs ? __ldg(probs + t * k + lane) : 1.0f) : 0.0f;
-    for (int base = 0; base < n8; base += 32 * U) {   // warp-uniform trip count
-      const int c0 = base + lane;
-      float acc[U][8];
+    float acc[U][8];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
+    for (int u = 0; u < U; ++u)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my_row, j);
-        const float p = __shfl_sync(0xffffffffu, my_p, j);
-        if (r < 0) continue;
-        const int4* src = reinterpret_cast<const int4*>(o + static_cast<int64_t>(r) * H);
-        int4 v[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (c0 + 32 * u < n8) v[u] = ld_stream(src + c0 + 32 * u);
+      for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
+    for (int j = 0; j < k; j += 2) {            // warp-uniform trip count
+      const int r0 = __shfl_sync(0xffffffffu, my_row, j);
+      const float p0 = __shfl_sync(0xffffffffu, my_p, j);
+      const int r1 = __shfl_sync(0xffffffffu, my_row, (j + 1) & 31);
+      const float p1 = __shfl_sync(0xffffffffu, my_p, (j + 1) & 31);
+      const bool has1 = j + 1 < k && r1 >= 0;
+      int4 v0[U], v1[U];
+      if (r0 >= 0) {
+        const int4* src = reinterpret_cast<const int4*>(o + static_cast<int64_t>(r0) * H);
 #pragma unroll
         for (int u = 0; u < U; ++u)
-          if (c0 + 32 * u < n8) acc_bf16x8(acc[u], v[u], p);
+          if (c0 + 32 * u < n8) v0[u] = ld_stream(src + c0 + 32 * u);
       }
-      int4* dst = reinterpret_cast<int4*>(y + t * H);
+      if (has1) {
+        const int4* src = reinterpret_cast<const int4*>(o + static_cast<int64_t>(r1) * H);
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (c0 + 32 * u < n8) {
-          int4 w;
-          w.x = static_cast<int>(pack_bf16x2(acc[u][0], acc[u][1]));
-          w.y = static_cast<int>(pack_bf16x2(acc[u][2], acc[u][3]));
-          w.z = static_cast<int>(pack_bf16x2(acc[u][4], acc[u][5]));
-          w.w = static_cast<int>(pack_bf16x2(acc[u][6], acc[u][7]));
-          dst[c0 + 32 * u] = w;
-        }
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n8) v1[u] = ld_stream(src + c0 + 32 * u);
+      }
+      if (r0 >= 0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n8) acc_bf16x8(acc[u], v0[u], p0);
+      }
+      if (has1) {
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n8) acc_bf16x8(acc[u], v1[u], p1);
+      }
     }
+    int4* dst = reinterpret_cast<int4*>(y + t * H);
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (c0 + 32 * u < n8) {
+        int4 w;
+        w.x = static_cast<int>(pack_bf16x2(acc[u][0], acc[u][1]));
+        w.y = static_cast<int>(pack_bf16x2(acc[u][2], acc[u][3]));
+        w.z = static_cast<int>(pack_bf16x2(acc[u][4], acc[u][5]));
+        w.w = static_cast<int>(pack_bf16x2(acc[u][6], acc[u][7]));
+        dst[c0 + 32 * u] = w;
+      }
   }
 }
 
 cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
                              int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  unpermute_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(o, row_of, probs, T, k, H, y);
+  const int64_t chunks = ((H >> 3) + 32 * kUnpermU - 1) / (32 * kUnpermU);
+  unpermute_kernel<<<grid_for_warps(T * chunks, 8), 256, 0, st>>>(o, row_of, probs, T, k, H, y);
   return cudaGetLastError();
 }
 
-// One warp per token over float rows: dx[t] = bf16(sum_j dxp[row_j]), j in
-// order; 4 floats per lane per step.
+// dx[t] = bf16(sum_j dxp[row_j]), j in order, over float rows. One warp per
+// (token, column chunk of 32 lanes x kUnpermU 16-byte vectors); slot pairs
+// are loaded together as in the forward combine.
 __global__ void __launch_bounds__(256) unpermute_f32_kernel(const float* __restrict__ dxp,
                                                             const int32_t* __restrict__ row_of,
                                                             int64_t T, int k, int H,
                                                             __nv_bfloat16* __restrict__ dx) {
+  constexpr int U = kUnpermU;
   const int lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int n4 = H >> 2;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       t < T; t += warps) {
+  const int chunks = (n4 + 32 * U - 1) / (32 * U);
+  const int64_t tasks = T * chunks;
+  for (int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       task < tasks; task += warps) {
+    const int64_t t = task / chunks;
+    const int c0 = static_cast<int>(task - t * chunks) * 32 * U + lane;
     const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
-    for (int base = 0; base < n4; base += 32) {     // warp-uniform trip count
-      const int c = base + lane;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j < k; ++j) {
-        const int r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0 || c >= n4) continue;
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r) * H) + c);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
+    float4 acc[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; j += 2) {            // warp-uniform trip count
+      const int r0 = __shfl_sync(0xffffffffu, my_row, j);
+      const int r1 = __shfl_sync(0xffffffffu, my_row, (j + 1) & 31);
+      const bool has1 = j + 1 < k && r1 >= 0;
+      float4 v0[U], v1[U];
+      if (r0 >= 0) {
+        const float4* src = reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r0) * H);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n4) v0[u] = __ldcs(src + c0 + 32 * u);
       }
-      if (c < n4) {
-        uint2 w;
-        w.x = pack_bf16x2(acc.x, acc.y);
-        w.y = pack_bf16x2(acc.z, acc.w);
-        reinterpret_cast<uint2*>(dx + t * H)[c] = w;
+      if (has1) {
+        const float4* src = reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r1) * H);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + 32 * u < n4) v1[u] = __ldcs(src + c0 + 32 * u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (r0 >= 0 && c0 + 32 * u < n4) {
+          acc[u].x += v0[u].x;
+          acc[u].y += v0[u].y;
+          acc[u].z += v0[u].z;
+          acc[u].w += v0[u].w;
+        }
+        if (has1 && c0 + 32 * u < n4) {
+          acc[u].x += v1[u].x;
+          acc[u].y += v1[u].y;
+          acc[u].z += v1[u].z;
+          acc[u].w += v1[u].w;
+        }
       }
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (c0 + 32 * u < n4) {
+        uint2 w;
+        w.x = pack_bf16x2(acc[u].x, acc[u].y);
+        w.y = pack_bf16x2(acc[u].z, acc[u].w);
+        reinterpret_cast<uint2*>(dx + t * H)[c0 + 32 * u] = w;
+      }
   }
 }
 
 cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_t T, int k, int H,
                                  __nv_bfloat16* dx, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  unpermute_f32_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(dxp, row_of, T, k, H, dx);
+  const int64_t chunks = ((H >> 2) + 32 * kUnpermU - 1) / (32 * kUnpermU);
+  unpermute_f32_kernel<<<grid_for_warps(T * chunks, 8), 256, 0, st>>>(dxp, row_of, T, k, H, dx);
   return cudaGetLastError();
 }
 
