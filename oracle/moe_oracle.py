@@ -16,6 +16,8 @@ the definition:
                 swap from bincount to histc).
   * offsets     the exclusive scan of the counts; on one device the send and
                 receive counts of steps 4-5 are both the local counts.
+  * route_topk  the gate ahead of the block: top-k experts of the router
+                logits with a softmax over the chosen k, and their counts.
   * permute     step 6: routed rows gathered into expert-contiguous order,
                 stable by flat index t*k+j within an expert.
   * fc1+SwiGLU  steps 7-8: A_g = Xp_e W1g_e, A_u = Xp_e W1u_e,
@@ -113,6 +115,45 @@ def expert_offsets(counts) -> np.ndarray:
     for e in range(counts.size):
         off[e + 1] = off[e] + counts[e]
     return off
+
+
+def route_topk(logits, k: int):
+    """Top-k routing from router logits: the gate step just ahead of the block.
+
+    The block takes the routing weights and selected experts that the
+    dispatcher call of "NPU Training Operators - MC2" (section "suggested
+    configuration") passes in; they come from the gate computation that the
+    MC2 for MoE All-to-All article counts as the first part of a step
+    (section on why communication is the bottleneck). The pages do not spell
+    the gate out. Reading used here:
+
+      * ids[t] are the k experts with the largest logits, in descending order
+        of logit; equal logits rank the lower expert index first (so -0.0 and
+        +0.0 tie); a NaN logit ranks as -inf.
+      * probs[t, j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) over the chosen k,
+        l_0 the largest: a softmax over all E restricted to the top k and
+        renormalised.
+      * counts and offsets are those of the chosen ids (expert_counts,
+        expert_offsets).
+
+    logits: float32 [T, E]. The order is decided on those float32 values
+    (exact in float64); the weights are computed in float64.
+    Returns ids int32 [T, k], probs float64 [T, k], counts [E], offsets [E+1].
+    """
+    lg = np.asarray(logits, dtype=np.float32).astype(np.float64)
+    T, E = lg.shape
+    if not 1 <= k <= E:
+        raise ValueError("need 1 <= k <= E")
+    lg = np.where(np.isnan(lg), -np.inf, lg)
+    index = np.broadcast_to(np.arange(E), lg.shape)
+    order = np.lexsort((index, -lg), axis=1)[:, :k]      # primary -logit, then index
+    chosen = np.take_along_axis(lg, order, axis=1)
+    with np.errstate(invalid="ignore"):
+        ex = np.exp(chosen - chosen[:, :1])
+        probs = ex / ex.sum(axis=1, keepdims=True)
+    ids = order.astype(np.int32)
+    counts = expert_counts(ids, E)
+    return ids, probs, counts, expert_offsets(counts)
 
 
 def permute_map(expert_ids, num_experts: int):

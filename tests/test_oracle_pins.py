@@ -397,3 +397,85 @@ def test_sampled_mxfp8_equals_token_forward():
     toks = [0, 3, 5]
     want = np.stack([orc.token_forward_mxfp8(xq[t], xs[t], qg, qu, qd, ids[t], probs[t]) for t in toks])
     np.testing.assert_array_equal(orc.sampled_forward_mxfp8(x, wg, wu, wd, ids, probs, toks), want)
+
+
+# ---------------------------------------------------------------- router (gate ahead of the block)
+
+def test_route_topk_worked_example_golden():
+    g = json.load(open(os.path.join(GOLDEN, "router_worked_example.json")))
+    logits = np.array([[float(v) for v in row] for row in g["logits"]], dtype=np.float32)  # "-inf", "nan", "-0.0"
+    assert np.signbit(logits[3, 0]) and not np.signbit(logits[3, 1])
+    ids, probs, counts, offsets = orc.route_topk(logits, g["k"])
+    assert ids.tolist() == g["expert_ids"]
+    np.testing.assert_allclose(probs, np.array(g["probs"]), rtol=1e-15, atol=0)
+    assert counts.tolist() == g["counts"] and offsets.tolist() == g["offsets"]
+
+
+def _beats(a, b, ea, eb):
+    """a (expert ea) ranks before b (expert eb); NaN as -inf."""
+    a = -math.inf if math.isnan(a) else a
+    b = -math.inf if math.isnan(b) else b
+    return a > b or (a == b and ea < eb)
+
+
+def test_route_topk_order_bruteforce():
+    # values from a small set so that ties, signed zeros, -inf and NaN all occur
+    rng = np.random.default_rng(21)
+    pool = np.array([-0.0, 0.0, 1.0, -1.0, 2.5, -np.inf, np.nan, 0.5], dtype=np.float32)
+    for E, k in ((7, 3), (5, 5), (9, 1), (12, 4)):
+        logits = pool[rng.integers(0, pool.size, (60, E))]
+        ids, _, counts, offsets = orc.route_topk(logits, k)
+        for t in range(60):
+            row = [float(v) for v in logits[t]]
+            chosen = ids[t].tolist()
+            assert len(set(chosen)) == k
+            for a, b in zip(chosen, chosen[1:]):              # in rank order
+                assert _beats(row[a], row[b], a, b)
+            for a in chosen:                                   # beats every expert left out
+                for b in set(range(E)) - set(chosen):
+                    assert _beats(row[a], row[b], a, b)
+        assert counts.tolist() == np.bincount(ids.reshape(-1), minlength=E).tolist()
+        assert offsets.tolist() == [0] + np.cumsum(counts).tolist()
+
+
+def test_route_topk_softmax_closed_forms():
+    rng = np.random.default_rng(22)
+    logits = rng.standard_normal((200, 16)).astype(np.float32)
+    l64 = logits.astype(np.float64)
+    # k = 2: the first weight is the logistic function of the logit gap
+    ids, p, _, _ = orc.route_topk(logits, 2)
+    gap = np.take_along_axis(l64, ids[:, :1], 1) - np.take_along_axis(l64, ids[:, 1:], 1)
+    np.testing.assert_allclose(p[:, :1], 1.0 / (1.0 + np.exp(-gap)), rtol=1e-14)
+    # k = 1: weight one
+    _, p1, _, _ = orc.route_topk(logits, 1)
+    assert np.all(p1 == 1.0)
+    # k = E: a full softmax over the row (scipy's), in rank order
+    from scipy.special import softmax
+    ids, p, _, _ = orc.route_topk(logits, 16)
+    np.testing.assert_allclose(p, np.take_along_axis(softmax(l64, axis=1), ids, 1), rtol=1e-13)
+    # any k: the softmax over all E restricted to the top k and renormalised
+    for k in (3, 6):
+        ids, p, _, _ = orc.route_topk(logits, k)
+        full = np.take_along_axis(softmax(l64, axis=1), ids, 1)
+        np.testing.assert_allclose(p, full / full.sum(1, keepdims=True), rtol=1e-13)
+
+
+def test_route_topk_shift_and_ties():
+    # integer logits shifted by an integer: exact in float32 and float64, so
+    # neither the order nor the weights may change
+    rng = np.random.default_rng(23)
+    logits = rng.integers(-4, 5, (100, 10)).astype(np.float32)
+    ids0, p0, _, _ = orc.route_topk(logits, 4)
+    ids1, p1, _, _ = orc.route_topk(logits + 37.0, 4)
+    assert np.array_equal(ids0, ids1)
+    np.testing.assert_allclose(p0, p1, rtol=1e-15)
+    # a row of equal logits: experts 0..k-1, weight 1/k each
+    ids, p, _, _ = orc.route_topk(np.full((3, 8), 1.25, np.float32), 4)
+    assert ids.tolist() == [[0, 1, 2, 3]] * 3 and np.all(p == 0.25)
+
+
+def test_route_topk_rejects_bad_k():
+    with pytest.raises(ValueError):
+        orc.route_topk(np.zeros((2, 4), np.float32), 5)
+    with pytest.raises(ValueError):
+        orc.route_topk(np.zeros((2, 4), np.float32), 0)
