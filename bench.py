@@ -36,21 +36,25 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 # DRAM bytes (read + write) per launch of the dominant kernel on a workload,
-# from the ncu captures summarised in profiles/, with the hash of the kernel
-# source they were taken on; reported as null once that source changes.
+# from the ncu captures summarised in profiles/, with the kernel's source
+# files and their hash when the counters were taken; reported as null once
+# any of those files changes.
+BF16_GEMM_SOURCES = ("gemm_bf16.cu", "common.cuh", "internal.h")
+MXFP8_GEMM_SOURCES = ("gemm_mxfp8.cu", "mx.cuh", "common.cuh", "internal.h")
 TRAFFIC = {
     # fc1 on the Mixtral-shaped workload: the 2-expert capture (610.2 MB for
     # 620.8 MB algorithmic) scaled by the algorithmic bytes of the full launch
     # (2181 MB); see profiles/grouped_gemm_mixtral_2experts_ncu_full.md
-    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2144e6, "src_sha": "da34c7a85b08ac65"},
+    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2144e6, "sources": BF16_GEMM_SOURCES,
+                                     "src_sha": "8d789a30e6aa6668"},
 }
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
-def _sha_of_kernel_sources():
+def _sha_of_sources(files):
     import hashlib
     h = hashlib.sha256()
-    for f in ("gemm_bf16.cu", "gemm_mxfp8.cu", "common.cuh", "mx.cuh"):
+    for f in files:
         with open(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -192,9 +196,15 @@ def run_reference(args, w):
 class Runner:
     """The timed step of one workload kind, its per-kernel events and FLOPs."""
 
-    def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0):
+    def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0, gate=False):
         import torch
         self.m, self.w, self.dev = m, w, device
+        self.gate = gate
+        if gate:
+            if w.mxfp8 or w.routing not in ("router", "gaussian"):
+                raise SystemExit(f"--gate needs a BF16 workload routed from logits, not {w.name}")
+            # router logits in, routing out: the fused gate replaces the counting step
+            self.logits = synth.router_logits(w, 0, inp["x"]).to(device)
         T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
         R = T * k
         self.x = inp["x"].to(device)
@@ -225,6 +235,8 @@ class Runner:
             nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
             self.dtype = "bf16"
             self.launches = 6 if (fuse_gather and not save) else 7
+            if gate:
+                self.launches -= 1          # one gate kernel for the histogram and scan pair
             if w.backward:
                 self.dy = inp["dy"].to(device)
                 self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev)
@@ -236,7 +248,7 @@ class Runner:
                     dw_up=torch.empty((E, H, F), dtype=torch.float32, device=device),
                     dw_down=torch.empty((E, F, H), dtype=torch.float32, device=device),
                     dprobs=torch.empty((T, k), dtype=torch.float32, device=device))
-                self.launches = 8 + 7
+                self.launches = (7 if gate else 8) + 7
         self.work = torch.empty(nbytes, dtype=torch.uint8, device=device)
         # per-kernel FLOPs of the grouped GEMMs (algorithmic: routed rows only)
         self.flops = {"fc1_swiglu": 4.0 * R * H * F, "fc2": 2.0 * R * F * H}
@@ -244,7 +256,7 @@ class Runner:
             self.flops.update({"dH_swiglu_bwd": 2.0 * R * H * F, "dXp": 4.0 * R * H * F,
                                "dW1": 4.0 * R * H * F, "dW2": 2.0 * R * F * H})
 
-    def step(self, events: bool, x=None, ids=None, probs=None, dy=None):
+    def step(self, events: bool, x=None, ids=None, probs=None, dy=None, logits=None):
         m = self.m
         x = self.x if x is None else x
         ids = self.ids if ids is None else ids
@@ -253,8 +265,15 @@ class Runner:
             m.moe_expert_forward_mxfp8(x, *self.wq, ids, probs, y=self.y, workspace=self.work,
                                        cfg=self.cfg_ev if events else self.cfg)
             return
-        m.moe_expert_forward(x, self.wg, self.wu, self.wd, ids, probs, y=self.y,
-                             workspace=self.work, cfg=self.cfg_ev if events else self.cfg)
+        if self.gate:                       # ids and probs are the gate's outputs
+            m.moe_expert_forward_from_logits(x, self.wg, self.wu, self.wd,
+                                             self.logits if logits is None else logits, self.w.k,
+                                             y=self.y, expert_ids=ids, probs=probs,
+                                             workspace=self.work,
+                                             cfg=self.cfg_ev if events else self.cfg)
+        else:
+            m.moe_expert_forward(x, self.wg, self.wu, self.wd, ids, probs, y=self.y,
+                                 workspace=self.work, cfg=self.cfg_ev if events else self.cfg)
         if self.w.backward:
             g = self.grads
             m.moe_expert_backward(self.dy if dy is None else dy, x, self.wg, self.wu, self.wd,
@@ -287,7 +306,8 @@ def run_ours(args, w):
     import moe_expert_dispatch_gb300 as m
 
     inp = synth.make_inputs(w, 0)
-    run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather, mx_tile_n=args.mxfp8_tile_n)
+    run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather, mx_tile_n=args.mxfp8_tile_n,
+                 gate=args.gate)
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
@@ -357,6 +377,10 @@ def run_ours(args, w):
     hx, hids, hprobs = pin(inp["x"]), pin(inp["expert_ids"]), pin(inp["probs"])
     dx_, dids, dprobs = torch.empty_like(run.x), torch.empty_like(run.ids), torch.empty_like(run.probs)
     h2d = hx.numel() * 2 + hids.numel() * 4 + hprobs.numel() * 4
+    if run.gate:                            # logits in; ids and probs come from the gate
+        hlogits = pin(run.logits.cpu())
+        dlogits = torch.empty_like(run.logits)
+        h2d = hx.numel() * 2 + hlogits.numel() * 4
     if w.backward:
         hdy = pin(inp["dy"])
         ddy = torch.empty_like(run.dy)
@@ -375,11 +399,15 @@ def run_ours(args, w):
         if i >= 2:
             e2e_s[i - 2].record(stream)
         dx_.copy_(hx, non_blocking=True)
-        dids.copy_(hids, non_blocking=True)
-        dprobs.copy_(hprobs, non_blocking=True)
+        if run.gate:
+            dlogits.copy_(hlogits, non_blocking=True)
+        else:
+            dids.copy_(hids, non_blocking=True)
+            dprobs.copy_(hprobs, non_blocking=True)
         if w.backward:
             ddy.copy_(hdy, non_blocking=True)
-        run.step(False, x=dx_, ids=dids, probs=dprobs, dy=ddy if w.backward else None)
+        run.step(False, x=dx_, ids=dids, probs=dprobs, dy=ddy if w.backward else None,
+                 logits=dlogits if run.gate else None)
         for h, d in zip(hres, dres):
             h.copy_(d, non_blocking=True)
         if i >= 2:
@@ -393,7 +421,7 @@ def run_ours(args, w):
     tflops = {key: run.flops[key] / (parts[key] * 1e-3) / 1e12 for key in run.flops}
     dominant = max(run.flops, key=lambda key: parts[key])
     tr = TRAFFIC.get((w.name, dominant))
-    traffic = tr["bytes"] if tr and tr["src_sha"] == _sha_of_kernel_sources() else None
+    traffic = tr["bytes"] if tr and tr["src_sha"] == _sha_of_sources(tr["sources"]) else None
     gemm_ms = sum(parts[key] for key in run.flops)
     line = {
         "metric": "MoE expert-block tokens/s", "value": ws * w.T / (ms * 1e-3),
@@ -407,6 +435,8 @@ def run_ours(args, w):
                    else "materialised permute",
                    "l2": "flushed before every step (512 MB write)",
                    "launch": "one CUDA graph per step" if args.graph else "stream launches",
+                   "routing": ("fused top-k gate from float32 router logits [T, E]" if run.gate
+                               else "expert ids and weights given"),
                    "parallelism": "replicas" if ws > 1 else "single"},
         "roofline": {"bound": "tensor", "kernel": f"{dominant} (grouped GEMM)",
                      "achieved": tflops[dominant], "peak": peak, "unit": "TFLOP/s",
@@ -442,6 +472,9 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--mxfp8-tile-n", type=int, default=0, choices=[0, 128, 256])
+    ap.add_argument("--gate", action="store_true",
+                    help="BF16 forward from router logits: the fused top-k gate replaces the "
+                         "counting step")
     ap.add_argument("--graph", action="store_true",
                     help="capture each step once into a CUDA graph and replay it")
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,

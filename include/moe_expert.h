@@ -136,6 +136,38 @@ moe_status moe_counts_static(const int32_t* expert_ids, int64_t n_ids, int E, in
                              int32_t* offsets, void* stream);
 
 /* ------------------------------------------------------------------------
+ * moe_route_topk - the gate ahead of the block, fused with its counts.
+ * The block's routing weights and selected experts (arguments of the
+ * dispatcher call in "NPU Training Operators - MC2", section "suggested
+ * configuration") come from the gate computation that the MC2 for MoE
+ * All-to-All article lists as the first part of a training step (section on
+ * why communication is the bottleneck). The pages do not spell the gate
+ * out; this call computes the usual top-k softmax gate. One kernel (after
+ * one memset of its scratch) picks every token's experts and weights and,
+ * for the batch, the per-expert counts and the offset scan.
+ *
+ *  logits      float [T, E]  router logits, row-major
+ *  expert_ids  int32 [T, k]  out: the k experts with the largest logits in
+ *                            descending order; equal logits rank the lower
+ *                            index first (-0.0 equals +0.0); a NaN logit
+ *                            ranks as -inf
+ *  probs       float [T, k]  out: exp(l_j - l_0) / sum_i exp(l_i - l_0) over
+ *                            the chosen k, l_0 the largest (float arithmetic);
+ *                            NaN when l_0 is infinite
+ *  counts      int32 [E]     out: as moe_counts of expert_ids
+ *  offsets     int32 [E + 1] out: as moe_counts
+ *  workspace   >= moe_route_topk_workspace_size(T, k, E) bytes, 16-byte
+ *              aligned; the call clears what it uses, so one workspace may
+ *              serve consecutive calls on a stream (not overlapping ones).
+ * Requires 1 <= k <= E <= 1024, k <= 32 and T*k < 2^31; T = 0 gives zero
+ * counts and offsets. Never reports a device error.
+ * ------------------------------------------------------------------------ */
+size_t moe_route_topk_workspace_size(int64_t T, int k, int E);
+moe_status moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* expert_ids,
+                          float* probs, int32_t* counts, int32_t* offsets, void* workspace,
+                          size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * moe_permute - gather routed rows into expert-contiguous order.
  * Step 6 of ep_mc2_forward, permute(hidden_states, selected_experts): on one
  * GPU this is also the dispatch AllToAllv of all2all_grouped_matmul.
@@ -215,6 +247,25 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
                               const void* w_down, const int32_t* expert_ids, const float* probs,
                               int64_t T, int H, int F, int E, int k, void* y, void* workspace,
                               size_t ws_bytes, const moe_config* cfg, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_forward_from_logits - moe_expert_forward with the gate fused
+ * in front: the routing comes from router logits through the kernel of
+ * moe_route_topk, whose counts and offsets replace the block's own counting
+ * step. y equals moe_expert_forward's on the expert_ids / probs written
+ * here, bit for bit.
+ *
+ *  router_logits  float [T, E]
+ *  expert_ids     int32 [T, k]  out (as moe_route_topk; the backward needs it)
+ *  probs          float [T, k]  out (as moe_route_topk)
+ *  everything else as moe_expert_forward, with the same workspace size.
+ * ------------------------------------------------------------------------ */
+moe_status moe_expert_forward_from_logits(const void* x, const void* w_gate, const void* w_up,
+                                          const void* w_down, const float* router_logits,
+                                          int64_t T, int H, int F, int E, int k,
+                                          int32_t* expert_ids, float* probs, void* y,
+                                          void* workspace, size_t ws_bytes,
+                                          const moe_config* cfg, void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_expert_backward - gradients of moe_expert_forward.

@@ -58,6 +58,8 @@ _sig("moe_padded_rows", _i64, _i64, _i32, _i32)
 _sig("moe_counts_workspace_size", _sz, _i64, _i32)
 _sig("moe_counts", _i32, _vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp)
 _sig("moe_counts_static", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
+_sig("moe_route_topk_workspace_size", _sz, _i64, _i32, _i32)
+_sig("moe_route_topk", _i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp)
 _sig("moe_permute_workspace_size", _sz, _i64, _i32, _i32)
 _sig("moe_permute", _i32, _vp, _i64, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp,
      _vp, _vp, _sz, _vp)
@@ -66,6 +68,8 @@ _sig("moe_quantize_mxfp8", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
 _sig("moe_workspace_size", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config), _i32)
 _sig("moe_expert_forward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp,
      _vp, _sz, ctypes.POINTER(moe_config), _vp)
+_sig("moe_expert_forward_from_logits", _i32, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+     _i32, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(moe_config), _vp)
 _sig("moe_expert_backward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
      _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, ctypes.POINTER(moe_config), _vp)
 _sig("moe_workspace_size_mxfp8", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config))
@@ -157,6 +161,27 @@ def moe_counts(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=
     _check(_lib.moe_counts(_p(expert_ids), n, num_experts, _p(counts), _p(offsets), _p(ws),
                            ws.numel(), _stream(stream)), "moe_counts")
     return counts, offsets
+
+
+def moe_route_topk(logits: torch.Tensor, k: int, expert_ids=None, probs=None, counts=None,
+                   offsets=None, workspace=None, stream=None):
+    """The top-k softmax gate fused with the counts: (expert_ids int32 [T, k],
+    probs float32 [T, k], counts int32 [E], offsets int32 [E+1]) of float32
+    router logits [T, E]."""
+    _cuda(logits, "logits", torch.float32)
+    T, E = logits.shape
+    dev = logits.device
+    expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
+                  if expert_ids is None else expert_ids)
+    probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    need = _lib.moe_route_topk_workspace_size(T, k, E)
+    ws = _workspace(need, dev) if workspace is None else workspace
+    _check(_lib.moe_route_topk(_p(logits), T, E, k, _p(expert_ids), _p(probs), _p(counts),
+                               _p(offsets), _p(ws), ws.numel(), _stream(stream)),
+           "moe_route_topk")
+    return expert_ids, probs, counts, offsets
 
 
 def moe_counts_static(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=None,
@@ -258,6 +283,34 @@ def moe_expert_forward(x, w_gate, w_up, w_down, expert_ids, probs, y=None, works
                                    _p(probs), T, H, F, E, k, _p(y), _p(ws), ws.numel(),
                                    ctypes.byref(c), _stream(stream)), "moe_expert_forward")
     return y, ws
+
+
+def moe_expert_forward_from_logits(x, w_gate, w_up, w_down, router_logits, k, y=None,
+                                   expert_ids=None, probs=None, workspace=None,
+                                   cfg: moe_config | None = None, stream=None):
+    """moe_expert_forward with the fused gate in front: returns
+    (y, expert_ids, probs, workspace), the routing as moe_route_topk gives it."""
+    for t, n in ((x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(router_logits, "router_logits", torch.float32)
+    T, H = x.shape
+    E, _, F = w_gate.shape
+    dev = x.device
+    c = cfg if cfg is not None else config()
+    need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 0)
+    if need == 0 and T > 0:
+        raise MoeError(1, "moe_workspace_size")
+    ws = _workspace(need, dev) if workspace is None else workspace
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+    expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
+                  if expert_ids is None else expert_ids)
+    probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
+    _check(_lib.moe_expert_forward_from_logits(_p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                               _p(router_logits), T, H, F, E, k, _p(expert_ids),
+                                               _p(probs), _p(y), _p(ws), ws.numel(),
+                                               ctypes.byref(c), _stream(stream)),
+           "moe_expert_forward_from_logits")
+    return y, expert_ids, probs, ws
 
 
 def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_workspace,

@@ -303,6 +303,26 @@ moe_status moe_counts(const int32_t* ids, int64_t n_ids, int E, int32_t* counts,
                                  static_cast<cudaStream_t>(stream)));
 }
 
+size_t moe_route_topk_workspace_size(int64_t T, int k, int E) {
+  if (T < 0 || k < 1 || E < 1) return 0;
+  return route_scratch_bytes(T * k, E);
+}
+
+moe_status moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* expert_ids,
+                          float* probs, int32_t* counts, int32_t* offsets, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK ||
+      T * static_cast<int64_t>(k) >= (static_cast<int64_t>(1) << 31))
+    return MOE_ERR_INVALID_ARG;
+  if ((T > 0 && (!logits || !expert_ids || !probs)) || !counts || !offsets)
+    return MOE_ERR_INVALID_ARG;
+  if (!workspace || ws_bytes < route_scratch_bytes(T * k, E) || !aligned16(workspace))
+    return MOE_ERR_WORKSPACE;
+  RouteScratch s = route_scratch(workspace, T * k, E);
+  return from_cuda(launch_route_topk(logits, T, E, k, 1, expert_ids, probs, counts, offsets,
+                                     nullptr, s, static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_permute_workspace_size(int64_t T, int k, int E) {
   if (T < 0 || k < 1 || E < 1) return 0;
   return route_scratch_bytes(T * k, E);
@@ -362,14 +382,19 @@ size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_confi
   return fwd_layout(T, H, F, E, k, c.save_for_backward != 0).total;
 }
 
-moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_up,
-                              const void* w_down, const int32_t* expert_ids, const float* probs,
-                              int64_t T, int H, int F, int E, int k, void* y, void* workspace,
-                              size_t ws_bytes, const moe_config* cfg, void* stream) {
+// The BF16 forward. Routing comes either from expert_ids / probs, or, when
+// logits is given, from the fused gate, which writes ids_out / probs_out.
+static moe_status expert_forward_impl(const void* x, const void* w_gate, const void* w_up,
+                                      const void* w_down, const int32_t* expert_ids,
+                                      const float* probs, const float* logits, int32_t* ids_out,
+                                      float* probs_out, int64_t T, int H, int F, int E, int k,
+                                      void* y, void* workspace, size_t ws_bytes,
+                                      const moe_config* cfg, void* stream) {
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
-  if (!x || !w_gate || !w_up || !w_down || !expert_ids || !probs || !y) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_gate || !w_up || !w_down || !y) return MOE_ERR_INVALID_ARG;
+  if (logits ? (!ids_out || !probs_out) : (!expert_ids || !probs)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
       !aligned16(y))
     return MOE_ERR_INVALID_ARG;
@@ -395,10 +420,17 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
   __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
   __nv_bfloat16* o = at<__nv_bfloat16>(workspace, L.o);
 
-  // counts -> offsets -> row map -> permute (the dispatch)
-  if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
-      cudaSuccess)
+  // (gate ->) counts -> offsets -> row map -> permute (the dispatch)
+  if (logits) {
+    if (launch_route_topk(logits, T, E, k, kTileM, ids_out, probs_out, counts, offsets, off_al, rs,
+                          st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    expert_ids = ids_out;
+    probs = probs_out;
+  } else if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
+             cudaSuccess) {
     return MOE_ERR_CUDA;
+  }
   if (launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
@@ -481,6 +513,25 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
       launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
   mark(4);
   return from_cuda(ue);
+}
+
+moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_up,
+                              const void* w_down, const int32_t* expert_ids, const float* probs,
+                              int64_t T, int H, int F, int E, int k, void* y, void* workspace,
+                              size_t ws_bytes, const moe_config* cfg, void* stream) {
+  return expert_forward_impl(x, w_gate, w_up, w_down, expert_ids, probs, nullptr, nullptr, nullptr,
+                             T, H, F, E, k, y, workspace, ws_bytes, cfg, stream);
+}
+
+moe_status moe_expert_forward_from_logits(const void* x, const void* w_gate, const void* w_up,
+                                          const void* w_down, const float* router_logits,
+                                          int64_t T, int H, int F, int E, int k,
+                                          int32_t* expert_ids, float* probs, void* y,
+                                          void* workspace, size_t ws_bytes,
+                                          const moe_config* cfg, void* stream) {
+  if (T > 0 && !router_logits) return MOE_ERR_INVALID_ARG;
+  return expert_forward_impl(x, w_gate, w_up, w_down, nullptr, nullptr, router_logits, expert_ids,
+                             probs, T, H, F, E, k, y, workspace, ws_bytes, cfg, stream);
 }
 
 moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate, const void* w_up,

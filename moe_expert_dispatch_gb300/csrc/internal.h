@@ -20,11 +20,15 @@ constexpr int kTileM = 128;
 inline int64_t route_chunks(int64_t n_ids) { return (n_ids + kRouteChunk - 1) / kRouteChunk; }
 
 // Scratch of the counting step: per-chunk histograms and per-chunk bases,
-// each [chunks, E] int32.
+// each [chunks, E] int32, after a 256-byte head whose first word is the
+// completion ticket of the fused gate (route_topk); the head and the
+// histograms are contiguous so that one memset clears both.
+constexpr size_t kRouteHeadBytes = 256;
 struct RouteScratch {
-  int32_t* hist;
-  int32_t* base;
-  int64_t chunks;
+  int32_t* hist = nullptr;
+  int32_t* base = nullptr;
+  int64_t chunks = 0;
+  unsigned int* ticket = nullptr;
 };
 size_t route_scratch_bytes(int64_t n_ids, int E);
 RouteScratch route_scratch(void* ws, int64_t n_ids, int E);
@@ -35,6 +39,15 @@ RouteScratch route_scratch(void* ws, int64_t n_ids, int E);
 cudaError_t launch_counts(const int32_t* ids, int64_t n, int E, int align, int32_t* counts,
                           int32_t* offsets, int32_t* off_al, RouteScratch s, int* err,
                           cudaStream_t st);
+
+// The gate ahead of the block from float logits [T, E]: ids[t] = the k
+// largest logits in descending order (ties to the lower index, NaN as
+// -inf), probs[t] = softmax over the chosen k; then, in the same launch,
+// counts, offsets (and off_al, s.base as launch_counts). Clears the ticket
+// and histograms of s itself (one memset).
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int align,
+                              int32_t* ids, float* probs, int32_t* counts, int32_t* offsets,
+                              int32_t* off_al, RouteScratch s, cudaStream_t st);
 
 // Row of every slot, token and prob of every row (stable within an expert).
 cudaError_t launch_rowmap(const int32_t* ids, const float* probs, int64_t n, int k, int E,

@@ -3,6 +3,8 @@
 // probability-weighted unpermute and the MXFP8 quantiser. All are bound by
 // HBM bandwidth (or latency, for the tiny count/scan kernels); rows move as
 // 16-byte vectors, one warp per token so that each warp streams whole rows.
+#include <climits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "mx.cuh"
@@ -14,16 +16,25 @@ namespace moe {
 size_t route_scratch_bytes(int64_t n_ids, int E) {
   const int64_t c = route_chunks(n_ids > 0 ? n_ids : 1);
   const size_t one = static_cast<size_t>(c) * E * sizeof(int32_t);
-  return 2 * ((one + 255) / 256 * 256);
+  return kRouteHeadBytes + 2 * ((one + 255) / 256 * 256);
 }
 
 RouteScratch route_scratch(void* ws, int64_t n_ids, int E) {
   RouteScratch s;
   s.chunks = route_chunks(n_ids > 0 ? n_ids : 1);
   const size_t one = (static_cast<size_t>(s.chunks) * E * sizeof(int32_t) + 255) / 256 * 256;
-  s.hist = static_cast<int32_t*>(ws);
-  s.base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + one);
+  s.ticket = static_cast<unsigned int*>(ws);
+  s.hist = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kRouteHeadBytes);
+  s.base = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + kRouteHeadBytes + one);
   return s;
+}
+
+// CTAs of warps_per_cta warps for one warp per work item, capped at 16 per SM
+// (the kernels loop over the rest).
+static int grid_for_warps(int64_t warps, int warps_per_cta) {
+  const int64_t want = (warps + warps_per_cta - 1) / warps_per_cta;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 // One CTA per chunk of ids: a shared-memory histogram, with the lanes of a
@@ -55,20 +66,25 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
     hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_count[e];
 }
 
-// One CTA: per expert the total and each chunk's exclusive prefix; then the
-// dense offsets, the padded offsets and every chunk's first row.
-__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist,
-                                                    int32_t* __restrict__ base, int64_t chunks,
-                                                    int E, int align, int32_t* counts,
-                                                    int32_t* offsets, int32_t* off_al) {
-  __shared__ int sh_cnt[kMaxExperts];
-  __shared__ int sh_al[kMaxExperts];
+// Run by one CTA: per expert the total and each chunk's exclusive prefix;
+// then the dense offsets, the padded offsets and every chunk's first row.
+// hist is read through L2 (other CTAs of the same launch may have written it).
+__device__ void scan_chunks(const int32_t* hist, int32_t* base, int64_t chunks, int E, int align,
+                            int32_t* counts, int32_t* offsets, int32_t* off_al, int* sh_cnt,
+                            int* sh_al) {
+  constexpr int U = 8;                     // independent loads in flight per expert
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int run = 0;
-    for (int64_t c = 0; c < chunks; ++c) {
-      const int v = hist[c * E + e];
-      base[c * E + e] = run;
-      run += v;
+    for (int64_t c0 = 0; c0 < chunks; c0 += U) {
+      int v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = c0 + u < chunks ? __ldcg(hist + (c0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (c0 + u < chunks) {
+          base[(c0 + u) * E + e] = run;
+          run += v[u];
+        }
     }
     sh_cnt[e] = run;
     if (counts) counts[e] = run;
@@ -91,6 +107,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     for (int64_t c = 0; c < chunks; ++c) base[c * E + e] += sh_al[e];
 }
 
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist,
+                                                    int32_t* __restrict__ base, int64_t chunks,
+                                                    int E, int align, int32_t* counts,
+                                                    int32_t* offsets, int32_t* off_al) {
+  __shared__ int sh_cnt[kMaxExperts];
+  __shared__ int sh_al[kMaxExperts];
+  scan_chunks(hist, base, chunks, E, align, counts, offsets, off_al, sh_cnt, sh_al);
+}
+
 cudaError_t launch_counts(const int32_t* ids, int64_t n, int E, int align, int32_t* counts,
                           int32_t* offsets, int32_t* off_al, RouteScratch s, int* err,
                           cudaStream_t st) {
@@ -102,6 +127,128 @@ cudaError_t launch_counts(const int32_t* ids, int64_t n, int E, int align, int32
     cudaMemsetAsync(s.hist, 0, E * sizeof(int32_t), st);
   scan_kernel<<<1, 1024, 0, st>>>(s.hist, s.base, chunks > 0 ? chunks : 1, E, align, counts,
                                   offsets, off_al);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gate (top-k + softmax + counts)
+
+// Rank order of the gate: the larger logit first, equal logits (-0.0 and
+// +0.0 included) to the lower expert index.
+__device__ __forceinline__ bool ranks_before(float a, int ea, float b, int eb) {
+  return a > b || (a == b && ea < eb);
+}
+
+// One warp per token. Lane l holds logits l, l + 32, ... (kEPL of them, NaN
+// entered as -inf); k rounds of a warp arg-max in rank order pick the
+// experts, lane j keeping the j-th pick. The weights are a float softmax
+// over the chosen k. Every slot adds one to the histogram row of its
+// 2048-id chunk (global atomics on rows cleared before the launch), so the
+// row map and its chunk bases work as after launch_counts; the CTA that
+// takes the last ticket runs the offset scan.
+template <int kEPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits,
+                                                         int64_t T, int E, int k, int align,
+                                                         int32_t* __restrict__ ids,
+                                                         float* __restrict__ probs, RouteScratch s,
+                                                         int32_t* counts, int32_t* offsets,
+                                                         int32_t* off_al) {
+  __shared__ int sh_cnt[kMaxExperts];
+  __shared__ int sh_al[kMaxExperts];
+  __shared__ int is_last;
+  const int lane = lane_id();
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       t < T; t += warps) {
+    const float* row = logits + t * E;
+    float v[kEPL];
+    unsigned open = 0;                               // bit i: logit lane + 32 i not yet taken
+#pragma unroll
+    for (int i = 0; i < kEPL; ++i) {
+      const int e = lane + 32 * i;
+      float x = -INFINITY;
+      if (e < E) {
+        x = __ldg(row + e);
+        if (isnan(x)) x = -INFINITY;
+        open |= 1u << i;
+      }
+      v[i] = x;
+    }
+    float mine_v = 0.0f;
+    int mine_e = 0;
+    for (int j = 0; j < k; ++j) {
+      float bv = -INFINITY;
+      int be = INT_MAX;                              // ranks after every real expert
+#pragma unroll
+      for (int i = 0; i < kEPL; ++i)
+        if (((open >> i) & 1u) && ranks_before(v[i], lane + 32 * i, bv, be)) {
+          bv = v[i];
+          be = lane + 32 * i;
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ranks_before(ov, oe, bv, be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      // k <= E, so every round finds an open expert: 0 <= be < E
+      if ((be & 31) == lane) open &= ~(1u << (be >> 5));
+      if (lane == j) {
+        mine_v = bv;
+        mine_e = be;
+      }
+    }
+    const float top = __shfl_sync(0xffffffffu, mine_v, 0);
+    const float ex = lane < k ? expf(mine_v - top) : 0.0f;
+    float sum = ex;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (lane < k) {
+      const int64_t i = t * k + lane;
+      ids[i] = mine_e;
+      probs[i] = ex / sum;
+      atomicAdd(s.hist + (i / kRouteChunk) * E + mine_e, 1);
+    }
+  }
+  // the last CTA to finish sees every histogram row
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(s.ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  scan_chunks(s.hist, s.base, s.chunks, E, align, counts, offsets, off_al, sh_cnt, sh_al);
+  if (threadIdx.x == 0) *s.ticket = 0;
+}
+
+template <int kEPL>
+static void launch_route_topk_epl(const float* logits, int64_t T, int E, int k, int align,
+                                  int32_t* ids, float* probs, RouteScratch s, int32_t* counts,
+                                  int32_t* offsets, int32_t* off_al, cudaStream_t st) {
+  route_topk_kernel<kEPL><<<grid_for_warps(T, 8), 256, 0, st>>>(logits, T, E, k, align, ids, probs,
+                                                                s, counts, offsets, off_al);
+}
+
+cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int align,
+                              int32_t* ids, float* probs, int32_t* counts, int32_t* offsets,
+                              int32_t* off_al, RouteScratch s, cudaStream_t st) {
+  const size_t hist_bytes = static_cast<size_t>(s.chunks) * E * sizeof(int32_t);
+  cudaError_t e = cudaMemsetAsync(s.ticket, 0, kRouteHeadBytes + hist_bytes, st);
+  if (e != cudaSuccess) return e;
+  if (E <= 32)
+    launch_route_topk_epl<1>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
+  else if (E <= 64)
+    launch_route_topk_epl<2>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
+  else if (E <= 128)
+    launch_route_topk_epl<4>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
+  else if (E <= 256)
+    launch_route_topk_epl<8>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
+  else if (E <= 512)
+    launch_route_topk_epl<16>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
+  else
+    launch_route_topk_epl<32>(logits, T, E, k, align, ids, probs, s, counts, offsets, off_al, st);
   return cudaGetLastError();
 }
 
@@ -216,12 +363,6 @@ __global__ void __launch_bounds__(256) permute_copy_kernel(const uint8_t* __rest
       }
     }
   }
-}
-
-static int grid_for_warps(int64_t warps, int warps_per_cta) {
-  const int64_t want = (warps + warps_per_cta - 1) / warps_per_cta;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
 cudaError_t launch_permute_copy(const void* x, int64_t T, int64_t row_bytes, int k,

@@ -166,6 +166,22 @@ def routing(w: Workload, seed: int, x: torch.Tensor | None = None):
             torch.from_numpy(np.ascontiguousarray(probs.astype(np.float32))))
 
 
+def router_logits(w: Workload, seed: int, x: torch.Tensor | None = None) -> torch.Tensor | None:
+    """float32 router logits [T, E] of the 'router' and 'gaussian' routings
+    (the same draws routing() ranks, rounded to float32); None for the
+    routings that sample experts directly ('zipf', 'uniform')."""
+    g = _gen(seed, 100, 0)
+    if w.routing == "router":
+        assert x is not None
+        wr = normal_f32(seed, 101, w.H * w.E, 0.02).astype(np.float64).reshape(w.H, w.E)
+        logits = x.float().numpy().astype(np.float64) @ wr
+    elif w.routing == "gaussian":
+        logits = g.standard_normal((w.T, w.E))
+    else:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(logits.astype(np.float32)))
+
+
 def make_inputs(w: Workload, seed: int = 0, with_dy: bool | None = None) -> dict:
     """All host inputs of one workload.
 

@@ -1,8 +1,10 @@
 """The seeded generators give the workloads' structure (checked on CPU with
 reduced token counts where the full size is not needed)."""
 import numpy as np
+import pytest
 import torch
 
+import oracle as orc
 import synth
 
 
@@ -58,3 +60,17 @@ def test_uniform_dirichlet_routing():
     ids, probs = synth.routing(w, 0)
     c = _check_routing(w, ids, probs)
     assert c.min() > 0.8 * c.mean()
+
+
+@pytest.mark.parametrize("name", ["tiny_bf16", "mixtral_bf16"])
+def test_router_logits_reproduce_workload_routing(name):
+    # the workloads' routing ranks float64 draws with its own top-k; the
+    # oracle's gate on the same draws rounded to float32 picks the same
+    # experts with the same weights (to float32 rounding)
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w, 0)
+    logits = synth.router_logits(w, 0, inp["x"])
+    ids, probs, _, _ = orc.route_topk(logits.numpy(), w.k)
+    assert np.array_equal(ids, inp["expert_ids"].numpy())
+    np.testing.assert_allclose(probs, inp["probs"].numpy(), rtol=1e-6, atol=1e-7)
+    assert synth.router_logits(synth.WORKLOADS["skewed_bf16"], 0) is None
