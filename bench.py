@@ -196,10 +196,14 @@ def run_reference(args, w):
 class Runner:
     """The timed step of one workload kind, its per-kernel events and FLOPs."""
 
-    def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0, gate=False):
+    def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0, gate=False, chunks=0,
+                 gemm_sms=0):
         import torch
         self.m, self.w, self.dev = m, w, device
         self.gate = gate
+        self.chunks = chunks
+        if chunks and (w.mxfp8 or w.backward or gate):
+            raise SystemExit("--chunks pipelines the BF16 forward from given ids only")
         if gate:
             if w.mxfp8 or w.routing not in ("router", "gaussian"):
                 raise SystemExit(f"--gate needs a BF16 workload routed from logits, not {w.name}")
@@ -229,14 +233,18 @@ class Runner:
         else:
             self.wg, self.wu, self.wd = (inp[key].to(device) for key in ("w_gate", "w_up", "w_down"))
             save = bool(w.backward)
-            self.cfg = m.config(save_for_backward=save, fuse_gather=fuse_gather)
+            self.cfg = m.config(save_for_backward=save, fuse_gather=fuse_gather, num_sms=gemm_sms)
             self.cfg_ev = m.config(save_for_backward=save, fuse_gather=fuse_gather,
-                                   step_events=self.fev)
+                                   num_sms=gemm_sms, step_events=self.fev)
             nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
+            if chunks:
+                nbytes = max(nbytes, m._lib.moe_workspace_size_pipelined(T, H, F, E, k, chunks))
             self.dtype = "bf16"
             self.launches = 6 if (fuse_gather and not save) else 7
             if gate:
                 self.launches -= 1          # one gate kernel for the histogram and scan pair
+            if chunks:
+                self.launches = 7 * min(chunks, T)   # the whole forward once per chunk
             if w.backward:
                 self.dy = inp["dy"].to(device)
                 self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev)
@@ -256,7 +264,10 @@ class Runner:
             self.flops.update({"dH_swiglu_bwd": 2.0 * R * H * F, "dXp": 4.0 * R * H * F,
                                "dW1": 4.0 * R * H * F, "dW2": 2.0 * R * F * H})
 
-    def step(self, events: bool, x=None, ids=None, probs=None, dy=None, logits=None):
+    def step(self, events: bool, x=None, ids=None, probs=None, dy=None, logits=None,
+             plain=False):
+        """One step; with --chunks the pipelined forward unless plain (the
+        single-stream forward that records the per-kernel events)."""
         m = self.m
         x = self.x if x is None else x
         ids = self.ids if ids is None else ids
@@ -265,7 +276,10 @@ class Runner:
             m.moe_expert_forward_mxfp8(x, *self.wq, ids, probs, y=self.y, workspace=self.work,
                                        cfg=self.cfg_ev if events else self.cfg)
             return
-        if self.gate:                       # ids and probs are the gate's outputs
+        if self.chunks and not plain:
+            m.moe_expert_forward_pipelined(x, self.wg, self.wu, self.wd, ids, probs, self.chunks,
+                                           y=self.y, workspace=self.work, cfg=self.cfg)
+        elif self.gate:                     # ids and probs are the gate's outputs
             m.moe_expert_forward_from_logits(x, self.wg, self.wu, self.wd,
                                              self.logits if logits is None else logits, self.w.k,
                                              y=self.y, expert_ids=ids, probs=probs,
@@ -307,7 +321,7 @@ def run_ours(args, w):
 
     inp = synth.make_inputs(w, 0)
     run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather, mx_tile_n=args.mxfp8_tile_n,
-                 gate=args.gate)
+                 gate=args.gate, chunks=args.chunks, gemm_sms=args.gemm_sms)
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
@@ -339,9 +353,11 @@ def run_ours(args, w):
                 run.step(False)
         stream.wait_stream(gstream)
         torch.cuda.synchronize()
+    separate_parts = graph is not None or run.chunks > 0
+    if separate_parts:
         for _ in range(args.steps):
             flush.zero_()
-            run.step(True)
+            run.step(True, plain=True)
             run.fev[-1].synchronize()
             if run.bev:
                 run.bev[-1].synchronize()
@@ -360,7 +376,7 @@ def run_ours(args, w):
                 run.step(True)
             ends[i].record(stream)
             ends[i].synchronize()
-            if graph is None:
+            if not separate_parts:
                 for key, v in run.parts().items():
                     parts[key] = parts.get(key, 0.0) + v
         torch.cuda.synchronize()
@@ -435,6 +451,10 @@ def run_ours(args, w):
                    else "materialised permute",
                    "l2": "flushed before every step (512 MB write)",
                    "launch": "one CUDA graph per step" if args.graph else "stream launches",
+                   "pipeline": (f"{run.chunks} token chunks, routing and combine on a second "
+                                "stream (per-kernel times from unpipelined steps)"
+                                if run.chunks else "none"),
+                   "gemm_ctas": args.gemm_sms or "one per SM",
                    "routing": ("fused top-k gate from float32 router logits [T, E]" if run.gate
                                else "expert ids and weights given"),
                    "parallelism": "replicas" if ws > 1 else "single"},
@@ -475,6 +495,10 @@ def main():
     ap.add_argument("--gate", action="store_true",
                     help="BF16 forward from router logits: the fused top-k gate replaces the "
                          "counting step")
+    ap.add_argument("--chunks", type=int, default=0,
+                    help="BF16 forward: micro-batch pipeline over this many token chunks")
+    ap.add_argument("--gemm-sms", type=int, default=0,
+                    help="persistent GEMM grid size (default: one CTA per SM)")
     ap.add_argument("--graph", action="store_true",
                     help="capture each step once into a CUDA graph and replay it")
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,

@@ -268,6 +268,39 @@ moe_status moe_expert_forward_from_logits(const void* x, const void* w_gate, con
                                           const moe_config* cfg, void* stream);
 
 /* ------------------------------------------------------------------------
+ * moe_expert_forward_pipelined - moe_expert_forward over n_chunks
+ * contiguous token chunks of ceil(T / n_chunks) tokens (the last one
+ * ragged), pipelined over two streams: the routing (counts, row map,
+ * permute) of chunk c+1 and the combine of chunk c run on aux_stream while
+ * the grouped GEMMs run on stream. This is the micro-batch pipeline of the
+ * MC2 for MoE All-to-All article (section "pipeline design"), where the
+ * dispatch of the next micro-batch overlaps the expert compute of the
+ * current one; on one GPU the dispatch is the permute gather. Each chunk is
+ * an independent forward, and the block's result does not depend on the
+ * split, so y equals moe_expert_forward's bit for bit.
+ *
+ *  arguments as moe_expert_forward, plus
+ *  n_chunks    >= 1 (n_chunks = 1 still runs routing and combine on aux)
+ *  workspace   >= moe_workspace_size_pipelined(T, H, F, E, k, n_chunks)
+ *              bytes: two per-chunk workspaces, used alternately
+ *  aux_stream  a second stream, not equal to stream. It first waits for the
+ *              work already queued on stream, and stream waits for all of
+ *              the call's work on it before anything queued later, so the
+ *              call is ordered on stream like any other.
+ * cfg->save_for_backward is not supported (MOE_ERR_UNSUPPORTED): the
+ * backward reads one whole-batch workspace. cfg->step_events are ignored.
+ * The first call on a host thread and device creates six CUDA events that
+ * the library keeps for the life of the process; make that call outside
+ * stream capture. Later calls create nothing and may be captured.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_size_pipelined(int64_t T, int H, int F, int E, int k, int n_chunks);
+moe_status moe_expert_forward_pipelined(const void* x, const void* w_gate, const void* w_up,
+                                        const void* w_down, const int32_t* expert_ids,
+                                        const float* probs, int64_t T, int H, int F, int E, int k,
+                                        void* y, int n_chunks, void* workspace, size_t ws_bytes,
+                                        const moe_config* cfg, void* stream, void* aux_stream);
+
+/* ------------------------------------------------------------------------
  * moe_expert_backward - gradients of moe_expert_forward.
  * The autograd Functions AllToAllGroupedMatmul / GroupedMatmulAllToAll of
  * "NPU Training Operators - MC2" (section "PR changes") wrap forward and

@@ -70,6 +70,9 @@ _sig("moe_expert_forward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32,
      _vp, _sz, ctypes.POINTER(moe_config), _vp)
 _sig("moe_expert_forward_from_logits", _i32, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
      _i32, _vp, _vp, _vp, _vp, _sz, ctypes.POINTER(moe_config), _vp)
+_sig("moe_workspace_size_pipelined", _sz, _i64, _i32, _i32, _i32, _i32, _i32)
+_sig("moe_expert_forward_pipelined", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
+     _i32, _vp, _i32, _vp, _sz, ctypes.POINTER(moe_config), _vp, _vp)
 _sig("moe_expert_backward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
      _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, ctypes.POINTER(moe_config), _vp)
 _sig("moe_workspace_size_mxfp8", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config))
@@ -311,6 +314,41 @@ def moe_expert_forward_from_logits(x, w_gate, w_up, w_down, router_logits, k, y=
                                                ctypes.byref(c), _stream(stream)),
            "moe_expert_forward_from_logits")
     return y, expert_ids, probs, ws
+
+
+_aux_streams = {}
+
+
+def moe_expert_forward_pipelined(x, w_gate, w_up, w_down, expert_ids, probs, n_chunks, y=None,
+                                 workspace=None, cfg: moe_config | None = None, stream=None,
+                                 aux_stream=None):
+    """moe_expert_forward over n_chunks token chunks, the routing of the next
+    chunk and the combine of the last overlapping the GEMMs on a second
+    stream (one cached per device unless aux_stream is given). Returns
+    (y, workspace)."""
+    for t, n in ((x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
+        _cuda(t, n, torch.bfloat16)
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    T, H = x.shape
+    E, _, F = w_gate.shape
+    k = expert_ids.shape[1]
+    c = cfg if cfg is not None else config()
+    need = _lib.moe_workspace_size_pipelined(T, H, F, E, k, n_chunks)
+    if need == 0 and T > 0:
+        raise MoeError(1, "moe_workspace_size_pipelined")
+    ws = _workspace(need, x.device) if workspace is None else workspace
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
+    if aux_stream is None:
+        aux_stream = _aux_streams.get(x.device)
+        if aux_stream is None:
+            aux_stream = _aux_streams[x.device] = torch.cuda.Stream(device=x.device)
+    _check(_lib.moe_expert_forward_pipelined(_p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                             _p(expert_ids), _p(probs), T, H, F, E, k, _p(y),
+                                             n_chunks, _p(ws), ws.numel(), ctypes.byref(c),
+                                             _stream(stream), _stream(aux_stream)),
+           "moe_expert_forward_pipelined")
+    return y, ws
 
 
 def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_workspace,

@@ -181,6 +181,24 @@ constexpr uint64_t kKeepInL2Bytes = 96ull << 20;
 
 int keep(uint64_t bytes) { return bytes <= kKeepInL2Bytes ? 1 : 0; }
 
+// Six events of the micro-batch pipeline, per thread and device, created on
+// the first pipelined call and kept for the life of the process; a call
+// re-records them, which leaves the waits of an earlier call untouched.
+cudaEvent_t* pipeline_events() {
+  constexpr int kMaxDevices = 64;
+  static thread_local cudaEvent_t pool[kMaxDevices][6];
+  static thread_local bool made[kMaxDevices];
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return nullptr;
+  if (!made[d]) {
+    for (int i = 0; i < 6; ++i)
+      if (cudaEventCreateWithFlags(&pool[d][i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    made[d] = true;
+  }
+  return pool[d];
+}
+
 int grid_size(const moe_config& c) {
   const int sms = device_sm_count();
   return (c.num_sms > 0 && c.num_sms < sms) ? c.num_sms : sms;
@@ -382,14 +400,143 @@ size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_confi
   return fwd_layout(T, H, F, E, k, c.save_for_backward != 0).total;
 }
 
-// The BF16 forward. Routing comes either from expert_ids / probs, or, when
-// logits is given, from the fused gate, which writes ids_out / probs_out.
-static moe_status expert_forward_impl(const void* x, const void* w_gate, const void* w_up,
-                                      const void* w_down, const int32_t* expert_ids,
-                                      const float* probs, const float* logits, int32_t* ids_out,
-                                      float* probs_out, int64_t T, int H, int F, int E, int k,
-                                      void* y, void* workspace, size_t ws_bytes,
-                                      const moe_config* cfg, void* stream) {
+// One BF16 forward over T tokens in one workspace, in three phases that
+// may run on different streams: route (gate or counts, row map, permute),
+// gemms (fc1 + SwiGLU, fc2) and combine (unpermute). Routing comes either
+// from expert_ids / probs, or, when logits is given, from the fused gate,
+// which writes ids_out / probs_out.
+struct FwdRun {
+  const void *x, *w_gate, *w_up, *w_down;
+  const int32_t* expert_ids;
+  const float* probs;
+  const float* logits;
+  int32_t* ids_out;
+  float* probs_out;
+  int64_t T;
+  int H, F, E, k;
+  void* y;
+  void* ws;
+  moe_config c;
+  bool save;
+  FwdLayout L;
+
+  void mark(int i, cudaStream_t st) const {
+    if (c.step_events && i < c.num_step_events)
+      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+  }
+  const int32_t* ids() const { return logits ? ids_out : expert_ids; }
+  const float* weights() const { return logits ? probs_out : probs; }
+
+  moe_status route(cudaStream_t st) const {
+    const RouteScratch rs = route_scratch(at<char>(ws, L.route), L.R, E);
+    int32_t* counts = at<int32_t>(ws, L.counts);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* off_al = at<int32_t>(ws, L.off_al);
+    int32_t* row_of = at<int32_t>(ws, L.row_of);
+    int32_t* token_of = at<int32_t>(ws, L.token_of);
+    float* prob_of = at<float>(ws, L.prob_of);
+    __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
+    // (gate ->) counts -> offsets -> row map -> permute (the dispatch)
+    if (logits) {
+      if (launch_route_topk(logits, T, E, k, kTileM, ids_out, probs_out, counts, offsets, off_al,
+                            rs, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    } else if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs,
+                             error_word(), st) != cudaSuccess) {
+      return MOE_ERR_CUDA;
+    }
+    if (launch_rowmap(ids(), weights(), L.R, k, E, rs, row_of, token_of, prob_of, st) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    // with the fused gather, fc1 reads the routed rows straight from x; the
+    // permuted copy is still made when the backward needs it
+    const bool gather = c.fuse_gather != 0;
+    if ((!gather || save) &&
+        launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (save && launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, xp, token_of,
+                                    prob_of, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+
+  moe_status gemms(cudaStream_t st) const {
+    const bool gather = c.fuse_gather != 0;
+    __nv_bfloat16* xp = at<__nv_bfloat16>(ws, L.xp);
+    __nv_bfloat16* h = at<__nv_bfloat16>(ws, L.h);
+    __nv_bfloat16* o = at<__nv_bfloat16>(ws, L.o);
+    CUtensorMap ta, tg, tu, th, td;
+    const bool ta_ok =
+        gather ? make_tmap_bf16_2d(&ta, x, H, T, static_cast<uint64_t>(H) * 2, 64, 1)
+               : make_tmap_bf16_2d(&ta, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, kTileM);
+    if (!ta_ok ||
+        !make_tmap_bf16_2d(&tg, w_gate, F, static_cast<uint64_t>(E) * H,
+                           static_cast<uint64_t>(F) * 2, 64, 64) ||
+        !make_tmap_bf16_2d(&tu, w_up, F, static_cast<uint64_t>(E) * H,
+                           static_cast<uint64_t>(F) * 2, 64, 64) ||
+        !make_tmap_bf16_2d(&th, h, F, L.cap, static_cast<uint64_t>(F) * 2, 64, kTileM) ||
+        !make_tmap_bf16_2d(&td, w_down, H, static_cast<uint64_t>(E) * F,
+                           static_cast<uint64_t>(H) * 2, 64, 64))
+      return MOE_ERR_CUDA;
+    GroupedGemmArgs g1{};
+    g1.off_al = at<int32_t>(ws, L.off_al);
+    g1.E = E;
+    g1.K = H;
+    g1.N = F;
+    g1.bn = 256;                 // 128 gate + 128 up columns per N tile
+    g1.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
+    g1.b_rows = H;
+    g1.b_split = 1;
+    g1.out = h;
+    g1.ldo = F;
+    g1.save_g = save ? at<__nv_bfloat16>(ws, L.ag) : nullptr;
+    g1.save_u = save ? at<__nv_bfloat16>(ws, L.au) : nullptr;
+    g1.err = error_word();
+    g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+    g1.gather_token = at<int32_t>(ws, L.token_of);
+    g1.counts = at<int32_t>(ws, L.counts);
+    g1.keep_a = keep(static_cast<uint64_t>(L.R) * H * 2);
+    const int grid = grid_size(c);
+    GemmOut o1, o2;
+    if (!make_out_tmap(&o1.map[0], h, F, L.cap, static_cast<uint64_t>(F) * 2, false) ||
+        !make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
+      return MOE_ERR_CUDA;
+    o1.map[1] = o1.map[2] = o1.map[0];
+    if (save && (!make_out_tmap(&o1.map[1], g1.save_g, F, L.cap, static_cast<uint64_t>(F) * 2,
+                                false) ||
+                 !make_out_tmap(&o1.map[2], g1.save_u, F, L.cap, static_cast<uint64_t>(F) * 2,
+                                false)))
+      return MOE_ERR_CUDA;
+    o2.map[1] = o2.map[2] = o2.map[0];
+    if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, o1, g1, grid, st)
+                : launch_fc1_swiglu(ta, tg, tu, o1, g1, grid, st)) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    mark(2, st);
+    GroupedGemmArgs g2 = g1;
+    g2.K = F;
+    g2.N = H;
+    g2.bn = (H % 256 == 0) ? 256 : 128;
+    g2.b_rows = F;
+    g2.b_split = 0;
+    g2.out = o;
+    g2.ldo = H;
+    g2.save_g = g2.save_u = nullptr;
+    g2.keep_a = keep(static_cast<uint64_t>(L.R) * F * 2);
+    if (launch_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+
+  moe_status combine(cudaStream_t st) const {
+    return from_cuda(launch_unpermute(at<__nv_bfloat16>(ws, L.o), at<int32_t>(ws, L.row_of),
+                                      weights(), T, k, H, static_cast<__nv_bfloat16*>(y), st));
+  }
+};
+
+// Argument checks shared by the forward entry points; fills r but its layout.
+static moe_status fwd_prepare(FwdRun& r, const void* x, const void* w_gate, const void* w_up,
+                              const void* w_down, const int32_t* expert_ids, const float* probs,
+                              const float* logits, int32_t* ids_out, float* probs_out, int64_t T,
+                              int H, int F, int E, int k, void* y, const moe_config* cfg) {
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
@@ -398,121 +545,48 @@ static moe_status expert_forward_impl(const void* x, const void* w_gate, const v
   if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) ||
       !aligned16(y))
     return MOE_ERR_INVALID_ARG;
-  const moe_config c = cfg_or_default(cfg);
-  const bool save = c.save_for_backward != 0;
-  const FwdLayout L = fwd_layout(T, H, F, E, k, save);
-  if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  r.x = x;
+  r.w_gate = w_gate;
+  r.w_up = w_up;
+  r.w_down = w_down;
+  r.expert_ids = expert_ids;
+  r.probs = probs;
+  r.logits = logits;
+  r.ids_out = ids_out;
+  r.probs_out = probs_out;
+  r.T = T;
+  r.H = H;
+  r.F = F;
+  r.E = E;
+  r.k = k;
+  r.y = y;
+  r.c = cfg_or_default(cfg);
+  r.save = r.c.save_for_backward != 0;
+  return MOE_OK;
+}
+
+static moe_status expert_forward_impl(const void* x, const void* w_gate, const void* w_up,
+                                      const void* w_down, const int32_t* expert_ids,
+                                      const float* probs, const float* logits, int32_t* ids_out,
+                                      float* probs_out, int64_t T, int H, int F, int E, int k,
+                                      void* y, void* workspace, size_t ws_bytes,
+                                      const moe_config* cfg, void* stream) {
+  FwdRun r{};
+  moe_status s = fwd_prepare(r, x, w_gate, w_up, w_down, expert_ids, probs, logits, ids_out,
+                             probs_out, T, H, F, E, k, y, cfg);
+  if (s != MOE_OK || T == 0) return s;
+  r.L = fwd_layout(T, H, F, E, k, r.save);
+  if (!workspace || ws_bytes < r.L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  r.ws = workspace;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int* err = error_word();
-  auto mark = [&](int i) {
-    if (c.step_events && i < c.num_step_events)
-      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
-  };
-  mark(0);
-  const RouteScratch rs = route_scratch(at<char>(workspace, L.route), L.R, E);
-  int32_t* counts = at<int32_t>(workspace, L.counts);
-  int32_t* offsets = at<int32_t>(workspace, L.offsets);
-  int32_t* off_al = at<int32_t>(workspace, L.off_al);
-  int32_t* row_of = at<int32_t>(workspace, L.row_of);
-  int32_t* token_of = at<int32_t>(workspace, L.token_of);
-  float* prob_of = at<float>(workspace, L.prob_of);
-  __nv_bfloat16* xp = at<__nv_bfloat16>(workspace, L.xp);
-  __nv_bfloat16* h = at<__nv_bfloat16>(workspace, L.h);
-  __nv_bfloat16* o = at<__nv_bfloat16>(workspace, L.o);
-
-  // (gate ->) counts -> offsets -> row map -> permute (the dispatch)
-  if (logits) {
-    if (launch_route_topk(logits, T, E, k, kTileM, ids_out, probs_out, counts, offsets, off_al, rs,
-                          st) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    expert_ids = ids_out;
-    probs = probs_out;
-  } else if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
-             cudaSuccess) {
-    return MOE_ERR_CUDA;
-  }
-  if (launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
-  // with the fused gather, fc1 reads the routed rows straight from x; the
-  // permuted copy is still made when the backward needs it
-  const bool gather = c.fuse_gather != 0;
-  if ((!gather || save) &&
-      launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (save && launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, xp, token_of,
-                                  prob_of, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-
-  mark(1);
-  // fc1 + SwiGLU
-  CUtensorMap ta, tg, tu, th, td;
-  const bool ta_ok =
-      gather ? make_tmap_bf16_2d(&ta, x, H, T, static_cast<uint64_t>(H) * 2, 64, 1)
-             : make_tmap_bf16_2d(&ta, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, kTileM);
-  if (!ta_ok ||
-      !make_tmap_bf16_2d(&tg, w_gate, F, static_cast<uint64_t>(E) * H,
-                         static_cast<uint64_t>(F) * 2, 64, 64) ||
-      !make_tmap_bf16_2d(&tu, w_up, F, static_cast<uint64_t>(E) * H, static_cast<uint64_t>(F) * 2,
-                         64, 64) ||
-      !make_tmap_bf16_2d(&th, h, F, L.cap, static_cast<uint64_t>(F) * 2, 64, kTileM) ||
-      !make_tmap_bf16_2d(&td, w_down, H, static_cast<uint64_t>(E) * F,
-                         static_cast<uint64_t>(H) * 2, 64, 64))
-    return MOE_ERR_CUDA;
-  GroupedGemmArgs g1{};
-  g1.off_al = off_al;
-  g1.E = E;
-  g1.K = H;
-  g1.N = F;
-  g1.bn = 256;                 // 128 gate + 128 up columns per N tile
-  g1.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
-  g1.b_rows = H;
-  g1.b_split = 1;
-  g1.out = h;
-  g1.ldo = F;
-  g1.save_g = save ? at<__nv_bfloat16>(workspace, L.ag) : nullptr;
-  g1.save_u = save ? at<__nv_bfloat16>(workspace, L.au) : nullptr;
-  g1.err = err;
-  g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
-  g1.gather_token = token_of;
-  g1.counts = counts;
-  g1.keep_a = keep(static_cast<uint64_t>(L.R) * H * 2);
-  const int grid = grid_size(c);
-  GemmOut o1, o2;
-  if (!make_out_tmap(&o1.map[0], h, F, L.cap, static_cast<uint64_t>(F) * 2, false) ||
-      !make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
-    return MOE_ERR_CUDA;
-  o1.map[1] = o1.map[2] = o1.map[0];
-  if (save && (!make_out_tmap(&o1.map[1], g1.save_g, F, L.cap, static_cast<uint64_t>(F) * 2,
-                              false) ||
-               !make_out_tmap(&o1.map[2], g1.save_u, F, L.cap, static_cast<uint64_t>(F) * 2,
-                              false)))
-    return MOE_ERR_CUDA;
-  o2.map[1] = o2.map[2] = o2.map[0];
-  if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, o1, g1, grid, st)
-              : launch_fc1_swiglu(ta, tg, tu, o1, g1, grid, st)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  mark(2);
-
-  // fc2
-  GroupedGemmArgs g2 = g1;
-  g2.K = F;
-  g2.N = H;
-  g2.bn = (H % 256 == 0) ? 256 : 128;
-  g2.b_rows = F;
-  g2.b_split = 0;
-  g2.out = o;
-  g2.ldo = H;
-  g2.save_g = g2.save_u = nullptr;
-  g2.keep_a = keep(static_cast<uint64_t>(L.R) * F * 2);
-  if (launch_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
-  mark(3);
-
-  // unpermute (the combine)
-  const cudaError_t ue =
-      launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
-  mark(4);
-  return from_cuda(ue);
+  r.mark(0, st);
+  if ((s = r.route(st)) != MOE_OK) return s;
+  r.mark(1, st);
+  if ((s = r.gemms(st)) != MOE_OK) return s;
+  r.mark(3, st);
+  s = r.combine(st);
+  r.mark(4, st);
+  return s;
 }
 
 moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_up,
@@ -532,6 +606,77 @@ moe_status moe_expert_forward_from_logits(const void* x, const void* w_gate, con
   if (T > 0 && !router_logits) return MOE_ERR_INVALID_ARG;
   return expert_forward_impl(x, w_gate, w_up, w_down, nullptr, nullptr, router_logits, expert_ids,
                              probs, T, H, F, E, k, y, workspace, ws_bytes, cfg, stream);
+}
+
+size_t moe_workspace_size_pipelined(int64_t T, int H, int F, int E, int k, int n_chunks) {
+  if (check_block_args(T, H, F, E, k) != MOE_OK || n_chunks < 1) return 0;
+  const int64_t tc = T > 0 ? (T + n_chunks - 1) / n_chunks : 0;
+  return 2 * up256(fwd_layout(tc, H, F, E, k, false).total);
+}
+
+moe_status moe_expert_forward_pipelined(const void* x, const void* w_gate, const void* w_up,
+                                        const void* w_down, const int32_t* expert_ids,
+                                        const float* probs, int64_t T, int H, int F, int E, int k,
+                                        void* y, int n_chunks, void* workspace, size_t ws_bytes,
+                                        const moe_config* cfg, void* stream, void* aux_stream) {
+  FwdRun base{};
+  moe_status s = fwd_prepare(base, x, w_gate, w_up, w_down, expert_ids, probs, nullptr, nullptr,
+                             nullptr, T, H, F, E, k, y, cfg);
+  if (s != MOE_OK) return s;
+  if (n_chunks < 1 || !aux_stream || aux_stream == stream) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (base.save) return MOE_ERR_UNSUPPORTED;   // the backward reads one whole-batch workspace
+  const int64_t tc = (T + n_chunks - 1) / n_chunks;
+  const int64_t chunks = (T + tc - 1) / tc;
+  const size_t slot = up256(fwd_layout(tc, H, F, E, k, false).total);
+  if (!workspace || ws_bytes < 2 * slot || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  cudaEvent_t* ev = pipeline_events();
+  if (!ev) return MOE_ERR_CUDA;
+  cudaEvent_t start = ev[0], ready[2] = {ev[1], ev[2]}, gemms_done[2] = {ev[3], ev[4]},
+              aux_done = ev[5];
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t aux = static_cast<cudaStream_t>(aux_stream);
+  base.c.step_events = nullptr;
+  base.c.num_step_events = 0;
+  auto chunk = [&](int64_t c) {
+    FwdRun r = base;
+    const int64_t t0 = c * tc;
+    r.T = (T - t0 < tc) ? T - t0 : tc;
+    r.x = static_cast<const char*>(x) + t0 * H * 2;
+    r.expert_ids = expert_ids + t0 * k;
+    r.probs = probs + t0 * k;
+    r.y = static_cast<char*>(y) + t0 * H * 2;
+    r.ws = static_cast<char*>(workspace) + (c & 1) * slot;
+    r.L = fwd_layout(r.T, H, F, E, k, false);
+    return r;
+  };
+  // aux: route(0) | route(c+1) while st runs the GEMMs of c | combine(c)
+  // while st runs the GEMMs of c+1. Chunk c uses workspace slot c % 2; the
+  // route of c+1 waits for the GEMMs of c-1 (the slot's last reader on st),
+  // and the combine of c-1 precedes it on aux.
+  if (cudaEventRecord(start, st) != cudaSuccess || cudaStreamWaitEvent(aux, start, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if ((s = chunk(0).route(aux)) != MOE_OK) return s;
+  if (cudaEventRecord(ready[0], aux) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int64_t c = 0; c < chunks; ++c) {
+    const FwdRun r = chunk(c);
+    if (cudaStreamWaitEvent(st, ready[c & 1], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((s = r.gemms(st)) != MOE_OK) return s;
+    if (cudaEventRecord(gemms_done[c & 1], st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (c + 1 < chunks) {
+      const FwdRun next = chunk(c + 1);
+      if (c >= 1 && cudaStreamWaitEvent(aux, gemms_done[(c + 1) & 1], 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if ((s = next.route(aux)) != MOE_OK) return s;
+      if (cudaEventRecord(ready[(c + 1) & 1], aux) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (cudaStreamWaitEvent(aux, gemms_done[c & 1], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if ((s = r.combine(aux)) != MOE_OK) return s;
+  }
+  if (cudaEventRecord(aux_done, aux) != cudaSuccess ||
+      cudaStreamWaitEvent(st, aux_done, 0) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate, const void* w_up,

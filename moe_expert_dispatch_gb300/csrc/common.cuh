@@ -345,7 +345,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) and the logistic sigmoid, with the hardware
+// reciprocal-based division (__fdividef, 2 ulp; the denominator is >= 1, and
+// above 2^126 the quotient is 0 as the true value all but is). An IEEE-rounded
+// division costs several times more per element, most of all on the exact
+// zeros of the padding rows every expert segment carries, and in the SwiGLU
+// epilogues that cost showed up in the grouped GEMMs' own time.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+__device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {

@@ -488,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h) {
               const float dh = __uint_as_float(v[2 * i + h]);
               const float a = fg[2 * i + h], b = fu[2 * i + h];
-              const float sg = 1.0f / (1.0f + __expf(-a));
+              const float sg = sigmoid_f(a);
               vg[h] = dh * b * sg * (1.0f + a * (1.0f - sg));
               vu[h] = dh * a * sg;
             }
