@@ -32,7 +32,8 @@ the definition:
   * MXFP8       the quantised AllToAll+Matmul of "MC2 通算融合架构总览"
                 (section 1, and the scale buffers of section 5): E4M3 values
                 with one E8M0 scale per 32 K-contiguous elements, following the
-                OCP Microscaling Formats (MX) v1.0 specification.
+                OCP Microscaling Formats (MX) v1.0 specification; its backward
+                quantises every GEMM operand along that GEMM's reduction.
   * micro-batch the split of the MC2 for MoE All-to-All article (section
                 "pipeline design"): chunks processed independently and
                 reassembled in token order.
@@ -606,6 +607,122 @@ def sampled_forward_mxfp8(x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, toke
             acc = term if acc is None else acc + term
         out.append(bf16(acc))
     return np.stack(out)
+
+
+def quantized_along_rows(a, quantize: bool = True) -> np.ndarray:
+    """deq(quant(a)) with blocks of 32 along the last axis (the rule of
+    quantize_mxfp8), or a itself when quantize is False."""
+    a = _f64(a)
+    if not quantize:
+        return a
+    return dequantize_mxfp8(*quantize_mxfp8(a))
+
+
+def quantized_along_columns(a, quantize: bool = True) -> np.ndarray:
+    """deq(quant(a)) of a [n, C] with blocks of 32 along axis 0: rows
+    32 i .. 32 i + 31 of each column share a scale, the blocks start at row 0
+    and the last one is completed with zero rows. Returned as [n, C]."""
+    a = _f64(a)
+    if not quantize:
+        return a
+    n = a.shape[0]
+    pad = (-n) % MX_BLOCK
+    if pad:
+        a = np.concatenate([a, np.zeros((pad,) + a.shape[1:])])
+    return dequantize_mxfp8(*quantize_mxfp8(a.T)).T[:n]
+
+
+def expert_backward_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs,
+                          quantize: bool = True, keep: bool = False):
+    """Gradients of the MXFP8 block (FP8 training of the expert block, the
+    quantised AllToAll+Matmul of "MC2 通算融合架构总览" section 1 carried to
+    the backward). The pages fix no rule for the backward. Reading used
+    here: every GEMM runs on MXFP8 operands, each quantised by the
+    forward's rule per 32 elements along that GEMM's reduction dimension,
+    with the rounding points of expert_backward:
+
+      forward   x quantised along H; W1g_e, W1u_e [F, H] along H;
+                A_g = deq(x) deq(W1g_e)^T, A_u likewise; h = bf16(silu(A_g) A_u);
+                O = bf16(deq(h quantised along F) deq(W2_e [H, F] along F)^T)
+      dO        bf16(p dY_t), one row per routed slot; dp_tj = <dY_t, O_row>
+      dH        deq(dO along H) deq(W2_e as [F, H], along H)^T
+      dA_g, dA_u  the SwiGLU backward of dH on A_g, A_u as saved (bf16)
+      dXp       deq(dA_g along F) deq(W1g_e as [H, F], along F)^T + the same for up
+      dX        bf16(sum_j dXp[row_of[t, j]])
+      dW1g_e^T  deq(dA_g,e along rows)^T deq(Xp_e along rows)   [F, H]
+      dW1u_e^T  the same with dA_u,e
+      dW2_e^T   deq(dO_e along rows)^T deq(h_e along rows)       [H, F]
+
+    "Along rows" quantises the expert's routed rows (in permuted order) in
+    blocks of 32 starting at its first row (quantized_along_columns). Xp_e
+    are the bf16 rows of x, h_e the bf16 h. Weights come in the MXFP8
+    forward's K-contiguous layout, w_gate_t / w_up_t [E, F, H] and
+    w_down_t [E, H, F], and the weight gradients are returned in that
+    layout: dw_gate_t, dw_up_t [E, F, H], dw_down_t [E, H, F].
+
+    With quantize=False every deq(quant(.)) is the identity and the result
+    is expert_backward's on the same bf16 values. keep=True adds the
+    intermediates (row maps, offsets, A_g, A_u, h, O, dO, dH, dA_g, dA_u, dXp)
+    under "state".
+    """
+    q_rows = lambda a: quantized_along_rows(a, quantize)      # noqa: E731
+    q_cols = lambda a: quantized_along_columns(a, quantize)   # noqa: E731
+    E = len(w_gate_t)
+    x, dy = _f64(x), _f64(dy)
+    ids = np.asarray(expert_ids)
+    pr = _f64(probs)
+    T, k = ids.shape
+    counts = expert_counts(ids, E)
+    off = expert_offsets(counts)
+    row_of, token_of, slot_of = permute_map(ids, E)
+    prob_of = pr[token_of, slot_of]
+    H = x.shape[1]
+    F = np.asarray(w_gate_t[0]).shape[0]
+    R = T * k
+    xd = q_rows(x)[token_of]
+    xp = x[token_of]
+    a_g, a_u, h = np.zeros((R, F)), np.zeros((R, F)), np.zeros((R, F))
+    o = np.zeros((R, H))
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        a_g[lo:hi] = xd[lo:hi] @ q_rows(w_gate_t[e]).T
+        a_u[lo:hi] = xd[lo:hi] @ q_rows(w_up_t[e]).T
+        h[lo:hi] = bf16(silu(a_g[lo:hi]) * a_u[lo:hi])
+        o[lo:hi] = bf16(q_rows(h[lo:hi]) @ q_rows(w_down_t[e]).T)
+    y = unpermute(o, row_of, pr)
+    d_o = bf16(prob_of[:, None] * dy[token_of])
+    dprobs = np.zeros((T, k))
+    for j in range(k):
+        dprobs[:, j] = np.sum(dy * o[row_of[:, j]], axis=1)
+    ag_s, au_s = bf16(a_g), bf16(a_u)
+    dxp = np.zeros((R, H))
+    dw_gate_t, dw_up_t = np.zeros((E, F, H)), np.zeros((E, F, H))
+    dw_down_t = np.zeros((E, H, F))
+    dh_all, dag_all, dau_all = np.zeros((R, F)), np.zeros((R, F)), np.zeros((R, F))
+    for e in range(E):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        dh = q_rows(d_o[lo:hi]) @ q_rows(_f64(w_down_t[e]).T).T
+        sg = sigmoid(ag_s[lo:hi])
+        da_g = bf16(dh * au_s[lo:hi] * sg * (1.0 + ag_s[lo:hi] * (1.0 - sg)))
+        da_u = bf16(dh * ag_s[lo:hi] * sg)
+        dxp[lo:hi] = (q_rows(da_g) @ q_rows(_f64(w_gate_t[e]).T).T +
+                      q_rows(da_u) @ q_rows(_f64(w_up_t[e]).T).T)
+        xq_e = q_cols(xp[lo:hi])
+        dw_gate_t[e] = q_cols(da_g).T @ xq_e
+        dw_up_t[e] = q_cols(da_u).T @ xq_e
+        dw_down_t[e] = q_cols(d_o[lo:hi]).T @ q_cols(h[lo:hi])
+        dh_all[lo:hi], dag_all[lo:hi], dau_all[lo:hi] = dh, da_g, da_u
+    dx = unpermute(dxp, row_of, None)
+    out = dict(dx=dx, dw_gate_t=dw_gate_t, dw_up_t=dw_up_t, dw_down_t=dw_down_t,
+               dprobs=dprobs, y=y)
+    if keep:
+        out["state"] = dict(row_of=row_of, token_of=token_of, off=off, a_g=a_g, a_u=a_u, h=h,
+                            o=o, d_o=d_o, dh=dh_all, da_g=dag_all, da_u=dau_all, dxp=dxp)
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -479,3 +479,99 @@ def test_route_topk_rejects_bad_k():
         orc.route_topk(np.zeros((2, 4), np.float32), 5)
     with pytest.raises(ValueError):
         orc.route_topk(np.zeros((2, 4), np.float32), 0)
+
+
+# ---------------------------------------------------------------- MXFP8 backward
+
+def _mx_bwd_case(T=60, H=64, F=96, E=4, k=2, seed=31, wstd=0.1):
+    rng = np.random.default_rng(seed)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)])
+    ex = rng.exponential(1.0, (T, k))
+    probs = ex / ex.sum(1, keepdims=True)
+    b = lambda *s_, sd=1.0: orc.bf16(rng.standard_normal(s_) * sd)  # noqa: E731
+    return (b(T, H), b(T, H), b(E, F, H, sd=wstd), b(E, F, H, sd=wstd), b(E, H, F, sd=wstd),
+            ids, probs)
+
+
+def test_quantized_along_columns_blocks_by_hand():
+    # blocks of 32 rows per column, the last one zero-completed; each block
+    # worked with the pinned element rules (e8m0_scale_code, e4m3 codes)
+    rng = np.random.default_rng(32)
+    a = orc.bf16(rng.standard_normal((70, 3)) * np.array([1e-3, 1.0, 300.0]))
+    a[40:64, 1] *= 1e-4                         # a block far below its neighbours
+    got = orc.quantized_along_columns(a)
+    for c in range(3):
+        col = np.concatenate([a[:, c], np.zeros(26)])
+        for b in range(3):
+            blk = col[32 * b:32 * b + 32]
+            code = int(orc.e8m0_scale_code(np.abs(blk).max()))
+            scale = 2.0 ** (code - 127)
+            want = orc.e4m3_decode(orc.e4m3_encode(blk / scale)) * scale
+            rows = slice(32 * b, min(32 * b + 32, 70))
+            np.testing.assert_array_equal(got[rows, c], want[:rows.stop - rows.start])
+    np.testing.assert_array_equal(orc.quantized_along_columns(a, quantize=False), a)
+
+
+def test_mxfp8_backward_unquantized_is_bf16_backward():
+    dy, x, wgt, wut, wdt, ids, probs = _mx_bwd_case()
+    mx = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs, quantize=False)
+    ref = orc.expert_backward(dy, x, wgt.transpose(0, 2, 1), wut.transpose(0, 2, 1),
+                              wdt.transpose(0, 2, 1), ids, probs)
+    pairs = [("dx", "dx", None), ("dprobs", "dprobs", None), ("y", "y", None),
+             ("dw_gate_t", "dw_gate", (0, 2, 1)), ("dw_up_t", "dw_up", (0, 2, 1)),
+             ("dw_down_t", "dw_down", (0, 2, 1))]
+    for a, b, perm in pairs:
+        want = ref[b] if perm is None else ref[b].transpose(perm)
+        # the same products in float64; only BLAS summation order differs,
+        # which can move a bf16 rounding of h, dA or y by one step
+        scale = np.abs(want).max()
+        np.testing.assert_allclose(mx[a], want, rtol=2 ** -6, atol=2 ** -6 * scale, err_msg=a)
+        assert np.mean(np.isclose(mx[a], want, rtol=1e-9, atol=1e-12 * scale)) > 0.97, a
+
+
+def test_mxfp8_backward_elements_by_definition():
+    # single elements of every quantised GEMM rebuilt from the kept
+    # intermediates with explicit per-block quantisation
+    dy, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=40, E=2, k=1, seed=33)
+    out = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs, keep=True)
+    st = out["state"]
+
+    def q_vec(v):                     # one vector, blocks of 32 from its start
+        v = np.concatenate([v, np.zeros((-len(v)) % 32)])
+        res = np.zeros_like(v)
+        for b in range(0, len(v), 32):
+            blk = v[b:b + 32]
+            sc = 2.0 ** (int(orc.e8m0_scale_code(np.abs(blk).max())) - 127)
+            res[b:b + 32] = orc.e4m3_decode(orc.e4m3_encode(blk / sc)) * sc
+        return res
+
+    off = st["off"]
+    for e in range(2):
+        lo, hi = int(off[e]), int(off[e + 1])
+        n = hi - lo
+        r, f, hh = lo + n // 2, 17, 9
+        # dH[r, f] = sum_h q(dO[r, :])[h] q(W2[f, :])[h]  (W2 = w_down_t^T, along H)
+        dh = np.dot(q_vec(st["d_o"][r]), q_vec(wdt[e][:, f]))
+        np.testing.assert_allclose(st["dh"][r, f], dh, rtol=1e-12)
+        # dXp[r, hh] = q(dA_g[r])·q(W1g[hh, :]) + q(dA_u[r])·q(W1u[hh, :])  (along F)
+        dxp = (np.dot(q_vec(st["da_g"][r]), q_vec(wgt[e][:, hh])) +
+               np.dot(q_vec(st["da_u"][r]), q_vec(wut[e][:, hh])))
+        np.testing.assert_allclose(st["dxp"][r, hh], dxp, rtol=1e-12)
+        # dW1g^T[f, hh] = sum_r q(dA_g[:, f])[r] q(Xp[:, hh])[r]  (along the expert's rows)
+        xp_col = x[st["token_of"][lo:hi], hh]
+        want = np.dot(q_vec(st["da_g"][lo:hi, f]), q_vec(xp_col))[()]
+        np.testing.assert_allclose(out["dw_gate_t"][e][f, hh], want, rtol=1e-12, atol=1e-300)
+        # dW2^T[hh, f] = sum_r q(dO[:, hh])[r] q(h[:, f])[r]
+        want = np.dot(q_vec(st["d_o"][lo:hi, hh]), q_vec(st["h"][lo:hi, f]))
+        np.testing.assert_allclose(out["dw_down_t"][e][hh, f], want, rtol=1e-12, atol=1e-300)
+
+
+def test_mxfp8_backward_close_to_unquantized():
+    # each operand carries at most 2^-4 relative E4M3 rounding: the
+    # quantised gradients stay within a few percent of the unquantised ones
+    dy, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(seed=34)
+    mx = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs)
+    ex = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs, quantize=False)
+    for key in ("dx", "dw_gate_t", "dw_up_t", "dw_down_t", "dprobs"):
+        err = np.abs(mx[key] - ex[key]).max() / np.abs(ex[key]).max()
+        assert err < 0.15, (key, err)
