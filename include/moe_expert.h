@@ -340,7 +340,10 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
  *  wd_q        uint8 [E, H, F], wd_s        uint8 [E, H, F/32]
  * fc1 accumulates in float, h = bf16(silu(A_g) A_u) is quantised per 32
  * along F for fc2, O = bf16(fc2) and y = bf16(combine), as in BF16 mode.
- * Requires H % 128 == 0, F % 128 == 0.
+ * With cfg->save_for_backward the workspace (moe_workspace_size_mxfp8 with
+ * the same cfg) also keeps A_g, A_u and h in bf16 for
+ * moe_expert_backward_mxfp8, and the padding rows of the quantised x are
+ * zeroed. Requires H % 128 == 0, F % 128 == 0.
  * ------------------------------------------------------------------------ */
 size_t moe_workspace_size_mxfp8(int64_t T, int H, int F, int E, int k, const moe_config* cfg);
 moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
@@ -349,6 +352,64 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
                                     const float* probs, int64_t T, int H, int F, int E, int k,
                                     void* y, void* workspace, size_t ws_bytes,
                                     const moe_config* cfg, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_quantize_mxfp8_t - MXFP8 quantisation along the rows of a batch of
+ * bf16 matrices (the transposed orientation of moe_quantize_mxfp8): for each
+ * z < batch and column c of in[z] [rows, cols], the 32-row blocks of the
+ * column become 32 consecutive codes of q[z][c] and one scale, by the rule
+ * of moe_quantize_mxfp8. It turns the forward-layout weights into the
+ * backward's: W1g, W1u [E, F, H] -> [E, H, F] quantised along F, and
+ * W2 [E, H, F] -> [E, F, H] quantised along H.
+ *  in      bf16 [batch, rows, cols]
+ *  q       uint8 [batch, cols, rows]        out (16-byte aligned)
+ *  scales  uint8 [batch, cols, rows / 32]   out
+ *  rows % 32 == 0.
+ * ------------------------------------------------------------------------ */
+moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int cols, uint8_t* q,
+                                uint8_t* scales, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_expert_backward_mxfp8 - gradients of moe_expert_forward_mxfp8: FP8
+ * training of the expert block, the quantised AllToAll+Matmul of "MC2
+ * 通算融合架构总览" (section 1) carried to the backward. Every GEMM runs on the
+ * block-scaled tensor cores with both operands quantised per 32 along its
+ * own reduction, and the rounding points are those of moe_expert_backward:
+ *   dO_r = bf16(p_r dY_t(r)), dprobs[t,j] = <dY_t, O_row(t,j)> (float)
+ *   dH   = deq(dO along H) deq(W2 as [F, H], along H)^T (float)
+ *   dA_g, dA_u = the SwiGLU backward of dH on A_g, A_u as saved (bf16)
+ *   dXp  = deq(dA_g along F) deq(W1g as [H, F], along F)^T + the same for up
+ *   dX_t = bf16(sum_j dXp[row_of[t, j]]), j in order
+ *   dW1g^T_e = deq(dA_g,e)^T deq(Xp_e), dW1u^T_e likewise, dW2^T_e =
+ *   deq(dO_e)^T deq(h_e) (float), where the routed rows of expert e
+ *   (Xp = bf16 x, h, dO, dA) are quantised along the rows in blocks of 32
+ *   from the expert's first row.
+ *
+ *  dy               bf16 [T, H];  x  bf16 [T, H] (the forward's input)
+ *  w1g_q, w1u_q     uint8 [E, H, F], scales [E, H, F/32] (moe_quantize_mxfp8_t
+ *                   of the forward's wg, wu in bf16)
+ *  w2_q             uint8 [E, F, H], scales [E, F, H/32] (of the forward's wd)
+ *  fwd_ws           the workspace of a moe_expert_forward_mxfp8 call made with
+ *                   save_for_backward on the same inputs
+ *  dx               bf16 [T, H]       out
+ *  dw_gate_t, dw_up_t  float [E, F, H] out, the layout of the forward's wg, wu
+ *  dw_down_t        float [E, H, F]   out, the layout of the forward's wd
+ *  dprobs           float [T, k]      out
+ *  workspace        >= moe_workspace_size_mxfp8_backward(T, H, F, E, k) bytes
+ * Experts that receive no token get dW = 0 (or are left as they were when
+ * accumulate_dw). cfg->mxfp8_tile_n picks the MMA N (default 256 where it
+ * divides the output width). Requires H % 128 == 0, F % 128 == 0.
+ * ------------------------------------------------------------------------ */
+size_t moe_workspace_size_mxfp8_backward(int64_t T, int H, int F, int E, int k);
+moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_t* w1g_q,
+                                     const uint8_t* w1g_s, const uint8_t* w1u_q,
+                                     const uint8_t* w1u_s, const uint8_t* w2_q,
+                                     const uint8_t* w2_s, const int32_t* expert_ids,
+                                     const float* probs, int64_t T, int H, int F, int E, int k,
+                                     const void* fwd_ws, size_t fwd_ws_bytes, void* dx,
+                                     float* dw_gate_t, float* dw_up_t, float* dw_down_t,
+                                     float* dprobs, int accumulate_dw, void* workspace,
+                                     size_t ws_bytes, const moe_config* cfg, void* stream);
 
 #ifdef __cplusplus
 }

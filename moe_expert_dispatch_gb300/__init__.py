@@ -76,6 +76,11 @@ _sig("moe_expert_forward_pipelined", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _
 _sig("moe_expert_backward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32,
      _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, ctypes.POINTER(moe_config), _vp)
 _sig("moe_workspace_size_mxfp8", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config))
+_sig("moe_workspace_size_mxfp8_backward", _sz, _i64, _i32, _i32, _i32, _i32)
+_sig("moe_quantize_mxfp8_t", _i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp)
+_sig("moe_expert_backward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
+     _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz,
+     ctypes.POINTER(moe_config), _vp)
 _sig("moe_expert_forward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32,
      _i32, _i32, _i32, _vp, _vp, _sz, ctypes.POINTER(moe_config), _vp)
 
@@ -258,6 +263,21 @@ def moe_quantize_mxfp8(a: torch.Tensor, stream=None):
     return q, s
 
 
+def moe_quantize_mxfp8_t(a: torch.Tensor, stream=None):
+    """MXFP8 along the rows of each matrix of a bf16 [batch, rows, cols] (or
+    [rows, cols]) tensor: (codes uint8 [batch, cols, rows], scales uint8
+    [batch, cols, rows/32])."""
+    _cuda(a, "a", torch.bfloat16)
+    squeeze = a.dim() == 2
+    a3 = a.unsqueeze(0) if squeeze else a
+    B, rows, cols = a3.shape
+    q = torch.empty((B, cols, rows), dtype=torch.uint8, device=a.device)
+    s = torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device)
+    _check(_lib.moe_quantize_mxfp8_t(_p(a3), B, rows, cols, _p(q), _p(s), _stream(stream)),
+           "moe_quantize_mxfp8_t")
+    return (q[0], s[0]) if squeeze else (q, s)
+
+
 def moe_workspace_size(T, H, F, E, k, cfg: moe_config | None = None, for_backward=False) -> int:
     c = cfg if cfg is not None else config()
     return _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), int(for_backward))
@@ -404,3 +424,41 @@ def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, 
                                          _p(y), _p(ws), ws.numel(), ctypes.byref(c),
                                          _stream(stream)), "moe_expert_forward_mxfp8")
     return y, ws
+
+
+def moe_expert_backward_mxfp8(dy, x, w1g_q, w1g_s, w1u_q, w1u_s, w2_q, w2_s, expert_ids, probs,
+                              fwd_workspace, dx=None, dw_gate_t=None, dw_up_t=None,
+                              dw_down_t=None, dprobs=None, accumulate_dw=False, workspace=None,
+                              cfg: moe_config | None = None, stream=None):
+    """Gradients of moe_expert_forward_mxfp8 (run with save_for_backward):
+    dict(dx, dw_gate_t [E, F, H], dw_up_t [E, F, H], dw_down_t [E, H, F],
+    dprobs). The weights come in the backward orientation of
+    moe_quantize_mxfp8_t: w1g/w1u [E, H, F], w2 [E, F, H]."""
+    for t, n in ((dy, "dy"), (x, "x")):
+        _cuda(t, n, torch.bfloat16)
+    for t, n in ((w1g_q, "w1g_q"), (w1g_s, "w1g_s"), (w1u_q, "w1u_q"), (w1u_s, "w1u_s"),
+                 (w2_q, "w2_q"), (w2_s, "w2_s")):
+        _cuda(t, n, torch.uint8)
+    T, H = x.shape
+    E, _, F = w1g_q.shape
+    k = expert_ids.shape[1]
+    dev = x.device
+    c = cfg if cfg is not None else config(save_for_backward=True)
+    dx = torch.empty_like(x) if dx is None else dx
+    dw_gate_t = (torch.empty((E, F, H), dtype=torch.float32, device=dev)
+                 if dw_gate_t is None else dw_gate_t)
+    dw_up_t = torch.empty((E, F, H), dtype=torch.float32, device=dev) if dw_up_t is None else dw_up_t
+    dw_down_t = (torch.empty((E, H, F), dtype=torch.float32, device=dev)
+                 if dw_down_t is None else dw_down_t)
+    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
+    need = _lib.moe_workspace_size_mxfp8_backward(T, H, F, E, k)
+    ws = _workspace(need, dev) if workspace is None else workspace
+    _check(_lib.moe_expert_backward_mxfp8(_p(dy), _p(x), _p(w1g_q), _p(w1g_s), _p(w1u_q),
+                                          _p(w1u_s), _p(w2_q), _p(w2_s), _p(expert_ids),
+                                          _p(probs), T, H, F, E, k, _p(fwd_workspace),
+                                          fwd_workspace.numel(), _p(dx), _p(dw_gate_t),
+                                          _p(dw_up_t), _p(dw_down_t), _p(dprobs),
+                                          int(bool(accumulate_dw)), _p(ws), ws.numel(),
+                                          ctypes.byref(c), _stream(stream)),
+           "moe_expert_backward_mxfp8")
+    return dict(dx=dx, dw_gate_t=dw_gate_t, dw_up_t=dw_up_t, dw_down_t=dw_down_t, dprobs=dprobs)

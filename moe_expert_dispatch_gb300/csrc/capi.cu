@@ -116,13 +116,15 @@ BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
 // MXFP8 forward workspace: the routing buffers of the BF16 layout, then the
 // codes and tiled scales of x, the tiled scales of the weights, the codes
 // and tiled scales of h, and O.
+// MXFP8 forward workspace; with save_for_backward also A_g, A_u and h in
+// bf16 [cap, F] (the backward's SwiGLU and weight-gradient operands).
 struct MxLayout {
   int64_t R, cap;
   size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xq, xs_tok, xs, wgu_s, wd_s,
-      hq, hs, o, total;
+      hq, hs, o, ag, au, hb, total;
 };
 
-MxLayout mx_layout(int64_t T, int H, int F, int E, int k) {
+MxLayout mx_layout(int64_t T, int H, int F, int E, int k, bool save = false) {
   MxLayout L;
   L.R = T * k;
   L.cap = moe_padded_rows(L.R, E, kTileM);
@@ -147,6 +149,51 @@ MxLayout mx_layout(int64_t T, int H, int F, int E, int k) {
   L.hq = take(static_cast<size_t>(L.cap) * F);
   L.hs = take(static_cast<size_t>(L.cap) * F / 32);
   L.o = take(static_cast<size_t>(L.cap) * H * 2);
+  L.ag = save ? take(static_cast<size_t>(L.cap) * F * 2) : 0;
+  L.au = save ? take(static_cast<size_t>(L.cap) * F * 2) : 0;
+  L.hb = save ? take(static_cast<size_t>(L.cap) * F * 2) : 0;
+  L.total = cur;
+  return L;
+}
+
+// MXFP8 backward workspace. Row-quantised operands of the data-gradient GEMMs
+// (dO along H, dA along 2F) and column-quantised operands of the weight
+// gradients ([C, cap], K = the padded rows), each with tiled scales; dXp in
+// float; the weights' backward-orientation scales in the tiled layout.
+struct MxBwdLayout {
+  int64_t cap;
+  size_t d_o, doq, dos, doT, dots, d_a, daq, das, daT, dats, d_xp, xpT, xpts, hT, hts, w2_st,
+      w1g_st, w1u_st, total;
+};
+
+MxBwdLayout mx_bwd_layout(int64_t T, int H, int F, int E, int k) {
+  MxBwdLayout L;
+  L.cap = moe_padded_rows(T * k, E, kTileM);
+  const size_t cap = static_cast<size_t>(L.cap);
+  size_t cur = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = cur;
+    cur += up256(bytes);
+    return at;
+  };
+  L.d_o = take(cap * H * 2);
+  L.doq = take(cap * H);
+  L.dos = take(cap * H / 32);
+  L.doT = take(cap * H);
+  L.dots = take(cap * H / 32);
+  L.d_a = take(cap * 2 * F * 2);
+  L.daq = take(cap * 2 * F);
+  L.das = take(cap * 2 * F / 32);
+  L.daT = take(cap * 2 * F);
+  L.dats = take(cap * 2 * F / 32);
+  L.d_xp = take(cap * H * 4);
+  L.xpT = take(cap * H);
+  L.xpts = take(cap * H / 32);
+  L.hT = take(cap * F);
+  L.hts = take(cap * F / 32);
+  L.w2_st = take(static_cast<size_t>(E) * F * H / 32);
+  L.w1g_st = take(static_cast<size_t>(E) * H * F / 32);
+  L.w1u_st = take(static_cast<size_t>(E) * H * F / 32);
   L.total = cur;
   return L;
 }
@@ -840,9 +887,25 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
 }
 
 size_t moe_workspace_size_mxfp8(int64_t T, int H, int F, int E, int k, const moe_config* cfg) {
-  (void)cfg;
   if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;
-  return mx_layout(T, H, F, E, k).total;
+  const moe_config c = cfg_or_default(cfg);
+  return mx_layout(T, H, F, E, k, c.save_for_backward != 0).total;
+}
+
+size_t moe_workspace_size_mxfp8_backward(int64_t T, int H, int F, int E, int k) {
+  if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;
+  return mx_bwd_layout(T, H, F, E, k).total;
+}
+
+moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int cols, uint8_t* q,
+                                uint8_t* scales, void* stream) {
+  if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (batch == 0) return MOE_OK;
+  if (!in || !q || !scales || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_cols(static_cast<const __nv_bfloat16*>(in), cols, batch,
+                                        static_cast<int64_t>(rows) * cols, rows, cols, nullptr, 0,
+                                        nullptr, false, q, scales,
+                                        static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
@@ -861,7 +924,8 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
       (reinterpret_cast<uintptr_t>(wu_s) & 3) || (reinterpret_cast<uintptr_t>(wd_s) & 3))
     return MOE_ERR_INVALID_ARG;
   const moe_config c = cfg_or_default(cfg);
-  const MxLayout L = mx_layout(T, H, F, E, k);
+  const bool save = c.save_for_backward != 0;
+  const MxLayout L = mx_layout(T, H, F, E, k, save);
   if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* err = error_word();
@@ -896,6 +960,10 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
       launch_gather_tile_scales(xs_tok, token_of, off_al, counts, E, H, L.cap, xs, st) !=
           cudaSuccess)
     return MOE_ERR_CUDA;
+  // the backward reads the padding rows as zeros (their h is then zero) and
+  // marks them in token_of
+  if (save && launch_zero_padding(counts, off_al, E, H, xq, token_of, prob_of, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   // MMA N: 256 halves the A traffic per FLOP; 128 keeps two accumulators
   const int mx_bn = c.mxfp8_tile_n == 128 ? 128
                     : (c.mxfp8_tile_n == 256 || (F % 128 == 0 && H % 256 == 0)) ? 256 : 128;
@@ -929,6 +997,11 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.sfb = wgu_s;
   g1.hq = hq;
   g1.hs = hs;
+  if (save) {
+    g1.save_g = at<__nv_bfloat16>(workspace, L.ag);
+    g1.save_u = at<__nv_bfloat16>(workspace, L.au);
+    g1.save_h = at<__nv_bfloat16>(workspace, L.hb);
+  }
   g1.err = err;
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
   if (launch_mx_fc1(ta, tg, tu, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
@@ -943,6 +1016,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g2.keep_a = keep(static_cast<uint64_t>(L.R) * F);
   g2.hq = nullptr;
   g2.hs = nullptr;
+  g2.save_g = g2.save_u = g2.save_h = nullptr;
   g2.out = o;
   if (launch_mx_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
@@ -950,6 +1024,197 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
       launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
   mark(4);
   return from_cuda(ue);
+}
+
+moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_t* w1g_q,
+                                     const uint8_t* w1g_s, const uint8_t* w1u_q,
+                                     const uint8_t* w1u_s, const uint8_t* w2_q,
+                                     const uint8_t* w2_s, const int32_t* expert_ids,
+                                     const float* probs, int64_t T, int H, int F, int E, int k,
+                                     const void* fwd_ws, size_t fwd_ws_bytes, void* dx,
+                                     float* dw_gate_t, float* dw_up_t, float* dw_down_t,
+                                     float* dprobs, int accumulate_dw, void* workspace,
+                                     size_t ws_bytes, const moe_config* cfg, void* stream) {
+  moe_status s = check_block_args(T, H, F, E, k);
+  if (s != MOE_OK) return s;
+  if (!dw_gate_t || !dw_up_t || !dw_down_t || !aligned16(dw_gate_t) || !aligned16(dw_up_t) ||
+      !aligned16(dw_down_t))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // no tokens: every expert is empty, so the weight gradients are zero
+    if (accumulate_dw) return MOE_OK;
+    const size_t wb = static_cast<size_t>(E) * H * F * sizeof(float);
+    if (cudaMemsetAsync(dw_gate_t, 0, wb, st) != cudaSuccess ||
+        cudaMemsetAsync(dw_up_t, 0, wb, st) != cudaSuccess ||
+        cudaMemsetAsync(dw_down_t, 0, wb, st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  (void)expert_ids;
+  if (!dy || !x || !probs || !dx || !dprobs || !fwd_ws || !w1g_q || !w1g_s || !w1u_q || !w1u_s ||
+      !w2_q || !w2_s)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(dx) || !aligned16(w1g_q) ||
+      !aligned16(w1u_q) || !aligned16(w2_q))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c = cfg_or_default(cfg);
+  const MxLayout L = mx_layout(T, H, F, E, k, true);
+  if (fwd_ws_bytes < L.total || !aligned16(fwd_ws)) return MOE_ERR_WORKSPACE;
+  const MxBwdLayout B = mx_bwd_layout(T, H, F, E, k);
+  if (!workspace || ws_bytes < B.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  void* fw = const_cast<void*>(fwd_ws);
+  void* ws = workspace;
+  const int32_t* counts = at<int32_t>(fw, L.counts);
+  const int32_t* off_al = at<int32_t>(fw, L.off_al);
+  const int32_t* row_of = at<int32_t>(fw, L.row_of);
+  const int32_t* token_of = at<int32_t>(fw, L.token_of);
+  const int32_t* row_end = off_al + E;          // rows past it are unused capacity
+  const __nv_bfloat16* o = at<__nv_bfloat16>(fw, L.o);
+  const __nv_bfloat16* ag = at<__nv_bfloat16>(fw, L.ag);
+  const __nv_bfloat16* au = at<__nv_bfloat16>(fw, L.au);
+  const __nv_bfloat16* hb = at<__nv_bfloat16>(fw, L.hb);
+  const int64_t cap = B.cap;
+  __nv_bfloat16* d_o = at<__nv_bfloat16>(ws, B.d_o);
+  __nv_bfloat16* d_a = at<__nv_bfloat16>(ws, B.d_a);
+  float* d_xp = at<float>(ws, B.d_xp);
+  const int grid = grid_size(c);
+  auto bn_for = [&](int n) {      // MMA N: the configured width when it divides n
+    const int want = (c.mxfp8_tile_n == 128 || c.mxfp8_tile_n == 256) ? c.mxfp8_tile_n : 256;
+    return n % want == 0 ? want : 128;
+  };
+  auto mark = [&](int i) {
+    if (c.step_events && i < c.num_step_events)
+      cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
+  };
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  mark(0);
+
+  // dO = bf16(p dY) per routed row and dprobs = <dY, O>; padding rows of dO
+  // are zero. dO quantised along H (dH's K) and along the rows (dW2's K).
+  if (!ok(launch_dout(static_cast<const __nv_bfloat16*>(dy), o, row_of, probs, T, k, H, d_o,
+                      dprobs, st)) ||
+      !ok(launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, d_o, nullptr,
+                              nullptr, st)) ||
+      !ok(launch_quantize_mxfp8_tiled(d_o, cap, H, row_end, at<uint8_t>(ws, B.doq),
+                                      at<uint8_t>(ws, B.dos), st)) ||
+      !ok(launch_quantize_cols(d_o, H, 1, 0, static_cast<int>(cap), H, nullptr, 0, row_end, true,
+                               at<uint8_t>(ws, B.doT), at<uint8_t>(ws, B.dots), st)) ||
+      // the weights' backward-orientation scales in the MMA's tiled layout
+      !ok(launch_tile_scales(w2_s, nullptr, static_cast<int64_t>(E) * F, F, H, 0,
+                             at<uint8_t>(ws, B.w2_st), st)) ||
+      !ok(launch_tile_scales(w1g_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0,
+                             at<uint8_t>(ws, B.w1g_st), st)) ||
+      !ok(launch_tile_scales(w1u_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0,
+                             at<uint8_t>(ws, B.w1u_st), st)))
+    return MOE_ERR_CUDA;
+  mark(1);
+
+  const int bnF = bn_for(F), bnH = bn_for(H);
+  CUtensorMap t_doq, t_w2, t_daq, t_w1g, t_w1u, t_daT, t_xpT, t_doT, t_hT;
+  if (!make_tmap_u8_2d(&t_doq, at<uint8_t>(ws, B.doq), H, cap, H, 128, kTileM) ||
+      !make_tmap_u8_2d(&t_w2, w2_q, H, static_cast<uint64_t>(E) * F, H, 128, 128) ||
+      !make_tmap_u8_2d(&t_daq, at<uint8_t>(ws, B.daq), 2 * static_cast<uint64_t>(F), cap,
+                       2 * static_cast<uint64_t>(F), 128, kTileM) ||
+      !make_tmap_u8_2d(&t_w1g, w1g_q, F, static_cast<uint64_t>(E) * H, F, 128, 128) ||
+      !make_tmap_u8_2d(&t_w1u, w1u_q, F, static_cast<uint64_t>(E) * H, F, 128, 128) ||
+      !make_tmap_u8_2d(&t_daT, at<uint8_t>(ws, B.daT), cap, 2 * static_cast<uint64_t>(F), cap,
+                       128, kTileM) ||
+      !make_tmap_u8_2d(&t_xpT, at<uint8_t>(ws, B.xpT), cap, H, cap, 128, 128) ||
+      !make_tmap_u8_2d(&t_doT, at<uint8_t>(ws, B.doT), cap, H, cap, 128, kTileM) ||
+      !make_tmap_u8_2d(&t_hT, at<uint8_t>(ws, B.hT), cap, F, cap, 128, 128))
+    return MOE_ERR_CUDA;
+  MxGemmArgs base{};
+  base.off_al = off_al;
+  base.E = E;
+  base.stages = c.ring_stages == 0 ? 6 : c.ring_stages;
+  base.err = error_word();
+  base.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
+
+  // dH = deq(dO) deq(W2)^T over K = H, then the SwiGLU backward on the
+  // saved A_g, A_u -> dA = [dA_g | dA_u] in bf16
+  MxGemmArgs g = base;
+  g.K = H;
+  g.N = F;
+  g.bn = bnF;
+  g.b_rows = F;
+  g.sfb_rows = F;
+  g.sfa = at<uint8_t>(ws, B.dos);
+  g.sfb = at<uint8_t>(ws, B.w2_st);
+  g.act_g = ag;
+  g.act_u = au;
+  g.out = d_a;
+  g.keep_a = keep(static_cast<uint64_t>(cap) * H);
+  if (!ok(launch_mx_dh(t_doq, t_w2, g, grid, st))) return MOE_ERR_CUDA;
+  mark(2);
+
+  // dA quantised along 2F (dXp's K) and along the rows (dW1's K)
+  if (!ok(launch_quantize_mxfp8_tiled(d_a, cap, 2 * F, row_end, at<uint8_t>(ws, B.daq),
+                                      at<uint8_t>(ws, B.das), st)) ||
+      !ok(launch_quantize_cols(d_a, 2 * static_cast<int64_t>(F), 1, 0, static_cast<int>(cap),
+                               2 * F, nullptr, 0, row_end, true, at<uint8_t>(ws, B.daT),
+                               at<uint8_t>(ws, B.dats), st)))
+    return MOE_ERR_CUDA;
+
+  // dXp = deq(dA_g) deq(W1g)^T + deq(dA_u) deq(W1u)^T: K = 2F, the first F
+  // from W1g, the second from W1u; float rows
+  g = base;
+  g.K = 2 * F;
+  g.N = H;
+  g.bn = bnH;
+  g.b_rows = H;
+  g.sfb_rows = H;
+  g.k_split = F / 128;
+  g.kgroups_b = F / 128;
+  g.sfa = at<uint8_t>(ws, B.das);
+  g.sfb = at<uint8_t>(ws, B.w1g_st);
+  g.sfb1 = at<uint8_t>(ws, B.w1u_st);
+  g.outf = d_xp;
+  g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
+  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, g, grid, st))) return MOE_ERR_CUDA;
+  mark(3);
+  if (!ok(launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
+    return MOE_ERR_CUDA;
+  mark(4);
+
+  // weight gradients: x's routed rows and h quantised along the rows, then
+  // dW1^T = deq(dA)^T deq(Xp) (rows 0..F-1 -> dw_gate_t, F..2F-1 -> dw_up_t)
+  // and dW2^T = deq(dO)^T deq(h), K = each expert's padded rows
+  if (!ok(launch_quantize_cols(static_cast<const __nv_bfloat16*>(x), H, 1, 0,
+                               static_cast<int>(cap), H, token_of, T, row_end, true,
+                               at<uint8_t>(ws, B.xpT), at<uint8_t>(ws, B.xpts), st)) ||
+      !ok(launch_quantize_cols(hb, F, 1, 0, static_cast<int>(cap), F, nullptr, 0, row_end, true,
+                               at<uint8_t>(ws, B.hT), at<uint8_t>(ws, B.hts), st)))
+    return MOE_ERR_CUDA;
+  const int kg_cap = static_cast<int>(cap / 128);
+  g = base;
+  g.M = 2 * F;
+  g.N = H;
+  g.bn = bnH;
+  g.kgroups_a = kg_cap;
+  g.kgroups_b = kg_cap;
+  g.sfa = at<uint8_t>(ws, B.dats);
+  g.sfb = at<uint8_t>(ws, B.xpts);
+  g.outf = dw_gate_t;
+  g.outf2 = dw_up_t;
+  g.out_split = F;
+  g.accumulate = accumulate_dw;
+  if (!ok(launch_mx_wgrad(t_daT, t_xpT, g, grid, st))) return MOE_ERR_CUDA;
+  mark(5);
+  g = base;
+  g.M = H;
+  g.N = F;
+  g.bn = bnF;
+  g.kgroups_a = kg_cap;
+  g.kgroups_b = kg_cap;
+  g.sfa = at<uint8_t>(ws, B.dots);
+  g.sfb = at<uint8_t>(ws, B.hts);
+  g.outf = dw_down_t;
+  g.out_split = 0;
+  g.accumulate = accumulate_dw;
+  if (!ok(launch_mx_wgrad(t_doT, t_hT, g, grid, st))) return MOE_ERR_CUDA;
+  mark(6);
+  return MOE_OK;
 }
 
 }  // extern "C"

@@ -354,6 +354,21 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float sigmoid_f(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f) {
+  const int4* s = reinterpret_cast<const int4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int4 v = s[i];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 ff = __bfloat1622float2(h[q]);
+      f[8 * i + 2 * q] = ff.x;
+      f[8 * i + 2 * q + 1] = ff.y;
+    }
+  }
+}
+
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),

@@ -103,21 +103,6 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t
                  pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
 }
 
-__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* src, float* f) {
-  const int4* s = reinterpret_cast<const int4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int4 v = s[i];
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 ff = __bfloat1622float2(h[q]);
-      f[8 * i + 2 * q] = ff.x;
-      f[8 * i + 2 * q + 1] = ff.y;
-    }
-  }
-}
-
 // Epilogue output pieces: each epilogue warp finishes its 32 rows of the
 // tile in pieces of 32 rows x 64 bytes (32 bf16 or 16 float columns), staged
 // in its own shared-memory slots with the 64-byte swizzle (16-byte chunk j

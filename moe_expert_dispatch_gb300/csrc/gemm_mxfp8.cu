@@ -1,26 +1,28 @@
 // gemm_mxfp8.cu - persistent grouped GEMMs of the MXFP8 expert block on the
 // block-scaled tensor cores of sm_103a (tcgen05.mma.kind::mxf8f6f4 with one
-// E8M0 scale per 32 elements of K on both operands).
+// E8M0 scale per 32 elements of K on both operands), forward and backward.
 //
 // The structure is the one of gemm_bf16.cu (TMA producer warp, single-thread
-// MMA issuer, double-buffered TMEM accumulators, four epilogue warps, a ring
-// of `stages` shared-memory slots), with these differences:
+// MMA issuer, TMEM accumulators, epilogue warps, a ring of `stages`
+// shared-memory slots), with these differences:
 //   * a k-block is 128 E4M3 elements (128 bytes, one 128B-swizzle row);
-//     A (128 rows) and B (128 rows) are both K-major;
-//   * the scales of a k-block, one 512-byte atom for A and one for B, arrive
-//     by 1D bulk copies into the same slot and are moved into tensor memory
-//     with tcgen05.cp (32x128b, replicated over the four lane quadrants);
-//     each of the four MMAs of the k-block (K = 32) picks its byte of the
-//     32-bit scale words through the instruction's scale-factor id;
-//   * accumulators are 128 columns wide (2 x 128), and 8 columns per slot
-//     hold that slot's scales, all inside one 512-column allocation;
-//   * slots are smaller (34 KB), so the ring is up to 6 deep: at the FP8 rate
-//     4 slots in flight per SM do not cover the L2 latency;
-//   * fc1's epilogue rounds h to bf16 and quantises it per 32 along F (codes
-//     + tiled scales for fc2); fc2's epilogue rounds O to bf16.
-// Tiles follow the Rows schedule of gemm_bf16.cu: expert segments padded to
-// 128 rows, M fastest within an expert unless it has more M tiles than N
-// tiles, CTA b takes tiles b, b + grid, ...
+//     A (128 rows) and B (128 rows per box) are both K-major;
+//   * the scales of a k-block, one 512-byte atom for A and one per 128 rows
+//     of B, arrive by 1D bulk copies into the same slot and are moved into
+//     tensor memory with tcgen05.cp (32x128b, replicated over the four lane
+//     quadrants); each of the four MMAs of the k-block (K = 32) picks its
+//     byte of the 32-bit scale words through the instruction's scale-factor id;
+//   * slots are smaller than BF16 ones, so the ring is up to 6 deep: at the
+//     FP8 rate 4 slots in flight per SM do not cover the L2 latency.
+// Epilogues (MxEpi): fc1 rounds h to bf16 and quantises it per 32 along F
+// (codes + tiled scales for fc2), optionally saving A_g, A_u and h in bf16
+// for the backward; fc2 rounds O to bf16; dH applies the SwiGLU backward to
+// the saved A_g, A_u; F32 writes float rows (dXp) or weight-gradient rows.
+// Schedules: Rows (expert segments padded to 128 rows; M fastest within an
+// expert unless it has more M tiles than N tiles) and WGrad (K runs over one
+// expert's padded rows; every expert owns M/128 x N/bn output tiles, N
+// fastest, and an expert without rows writes zeros). CTA b takes tiles b,
+// b + grid, ...
 #include "common.cuh"
 #include "internal.h"
 #include "mx.cuh"
@@ -32,15 +34,15 @@ namespace {
 constexpr int BK = 128;                    // E4M3 elements (bytes) per k-block
 constexpr int kABytes = kTileM * BK;       // 16 KB
 constexpr int kSfBytes = 512;              // one scale atom (128 rows x 4 blocks of 32)
-// warp 0 producer, warp 1 MMA issuer, then the epilogue warps. fc1's
-// epilogue (SwiGLU + quantisation) is heavy: 8 warps, two per TMEM lane
-// quadrant, each finishing half of the tile's columns, halve its exposed
-// part. fc2's (bf16 stores) is light: 4 warps (more only take issue slots
-// from the producer and MMA threads).
-template <bool kFc1>
-constexpr int epi_warps() { return kFc1 ? 8 : 4; }
-template <bool kFc1>
-constexpr int num_threads() { return 64 + 32 * epi_warps<kFc1>(); }
+// warp 0 producer, warp 1 MMA issuer, then the epilogue warps. The fc1 and
+// dH epilogues (SwiGLU forward + quantisation, SwiGLU backward) are heavy:
+// 8 warps, two per TMEM lane quadrant, each finishing half of the tile's
+// columns, halve their exposed part. The fc2 and float epilogues are light:
+// 4 warps (more only take issue slots from the producer and MMA threads).
+template <MxEpi kEpi>
+constexpr int epi_warps() { return (kEpi == MxEpi::Fc1 || kEpi == MxEpi::SwigluBwd) ? 8 : 4; }
+template <MxEpi kEpi>
+constexpr int num_threads() { return 64 + 32 * epi_warps<kEpi>(); }
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
@@ -74,10 +76,24 @@ struct Smem {
   int zero;
 };
 
-template <bool kFc1, int kTileN>
-__global__ void __launch_bounds__(num_threads<kFc1>(), 1)
+// One output tile: expert, M tile, N tile, its k-blocks and the first
+// k-block's K offset (WGrad: the expert's first padded row).
+struct MxTile {
+  int e, m, n, kblocks, k0;
+};
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t* w) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) st_global_v4(dst + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+template <MxEpi kEpi, Sched kSched, int kTileN>
+__global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, MxGemmArgs p) {
+  constexpr bool kFc1 = kEpi == MxEpi::Fc1;
+  constexpr bool kWGrad = kSched == Sched::WGrad;
+  constexpr int kThreads = num_threads<kEpi>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -91,8 +107,9 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
   const int E = p.E;
   const int n_cols = kFc1 ? kTileN / 2 : kTileN;   // output columns per N tile
   const int n_tiles = p.N / n_cols;
-  const int kblocks = p.K / BK;
-  const int kgroups = p.K >> 7;
+  const int kgroups_a = p.kgroups_a > 0 ? p.kgroups_a : (p.K >> 7);
+  const int kgroups_b = p.kgroups_b > 0 ? p.kgroups_b : (p.K >> 7);
+  const int m_tiles_w = kWGrad ? p.M / kTileM : 0;   // WGrad: M tiles of every expert
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -101,7 +118,7 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm->tfull[a]), 1);
-      mbar_init(smem_u32(&sm->tempty[a]), epi_warps<kFc1>() * 32);
+      mbar_init(smem_u32(&sm->tempty[a]), epi_warps<kEpi>() * 32);
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort = 0;
@@ -117,10 +134,12 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
     tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
     tmem_relinquish();
   }
-  for (int e = threadIdx.x; e < E; e += num_threads<kFc1>())
-    ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+  if (!kWGrad) {
+    for (int e = threadIdx.x; e < E; e += kThreads)
+      ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (!kWGrad && threadIdx.x == 0) {
     ts[0] = 0;
     for (int e = 0; e < E; ++e) ts[e + 1] += ts[e];
   }
@@ -128,25 +147,39 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
-  const int total = ts[E];
+  const int total = kWGrad ? E * m_tiles_w * n_tiles : ts[E];
   volatile int* abort_flag = &sm->abort;
 
-  auto decode = [&](int t, int& e, int& m, int& n) {
+  auto decode = [&](int t) {
+    MxTile tl;
+    if (kWGrad) {
+      const int per = m_tiles_w * n_tiles;
+      tl.e = t / per;
+      const int local = t - tl.e * per;
+      tl.m = local / n_tiles;                 // N fastest: the expert's B panel stays in L2
+      tl.n = local - tl.m * n_tiles;
+      tl.k0 = p.off_al[tl.e];
+      tl.kblocks = (p.off_al[tl.e + 1] - tl.k0) / BK;
+      return tl;
+    }
     int lo = 0, hi = E - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (ts[mid] <= t) lo = mid; else hi = mid - 1;
     }
-    e = lo;
-    const int mt = (p.off_al[e + 1] - p.off_al[e]) / kTileM;
-    const int local = t - ts[e];
+    tl.e = lo;
+    const int mt = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int local = t - ts[tl.e];
     if (mt > n_tiles) {       // tall expert: keep its row panel in L2
-      m = local / n_tiles;
-      n = local - m * n_tiles;
+      tl.m = local / n_tiles;
+      tl.n = local - tl.m * n_tiles;
     } else {
-      n = local / mt;
-      m = local - n * mt;
+      tl.n = local / mt;
+      tl.m = local - tl.n * mt;
     }
+    tl.k0 = 0;
+    tl.kblocks = p.K / BK;
+    return tl;
   };
 
   if (warp == 0) {
@@ -159,11 +192,17 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
       const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
       const uint32_t ring0 = smem_u32(ring);
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int e, m, n;
-        decode(t, e, m, n);
-        const int row0 = p.off_al[e] + m * kTileM;
-        const int64_t vrow = static_cast<int64_t>(e) * p.sfb_rows + static_cast<int64_t>(n) * kTileN;
-        for (int kb = 0; kb < kblocks; ++kb) {
+        const MxTile tl = decode(t);
+        // A rows and the first 128-row block of B's scale atoms
+        const int a_row = kWGrad ? tl.m * kTileM : p.off_al[tl.e] + tl.m * kTileM;
+        const int64_t b_row =
+            kWGrad ? static_cast<int64_t>(tl.n) * kTileN
+                   : static_cast<int64_t>(tl.e) * p.b_rows + static_cast<int64_t>(tl.n) * (kFc1 ? kTileN / 2 : kTileN);
+        const int64_t vrow = kWGrad ? b_row
+                                    : static_cast<int64_t>(tl.e) * p.sfb_rows +
+                                          static_cast<int64_t>(tl.n) * kTileN;
+        const int kg0 = tl.k0 >> 7;
+        for (int kb = 0; kb < tl.kblocks; ++kb) {
           const uint32_t full = smem_u32(&sm->full[stage]);
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
@@ -173,21 +212,29 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
           const uint32_t sa = ring0 + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
           const uint32_t ssf = sb + kBBytes;
-          tma_load_2d_hint(sa, &tmA, full, kb * BK, row0, pol_a);
-          if (kFc1) {       // N/2 gate rows, then N/2 up rows, of the same N tile
+          const int kx = tl.k0 + kb * BK;
+          tma_load_2d_hint(sa, &tmA, full, kx, a_row, pol_a);
+          // B: fc1 takes N/2 gate rows and N/2 up rows of the same N tile;
+          // a K-split GEMM takes its k-blocks from B0, then from B1
+          const bool second = !kFc1 && !kWGrad && p.k_split > 0 && kb >= p.k_split;
+          const int kbb = second ? kb - p.k_split : kb;
+          if (kFc1) {
             const int half = kTileN / 2;
-            tma_load_2d(sb, &tmB0, full, kb * BK, e * p.b_rows + n * half);
-            tma_load_2d(sb + half * BK, &tmB1, full, kb * BK, e * p.b_rows + n * half);
+            tma_load_2d(sb, &tmB0, full, kx, static_cast<int>(b_row));
+            tma_load_2d(sb + half * BK, &tmB1, full, kx, static_cast<int>(b_row));
           } else {
+            const CUtensorMap* mb = second ? &tmB1 : &tmB0;
             for (int j = 0; j < kTileN; j += 128)
-              tma_load_2d(sb + j * BK, &tmB0, full, kb * BK, e * p.b_rows + n * kTileN + j);
+              tma_load_2d(sb + j * BK, mb, full, kbb * BK + tl.k0, static_cast<int>(b_row + j));
           }
-          bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(row0) >> 7) * kgroups + kb) * kSfBytes,
+          bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(a_row) >> 7) * kgroups_a + kg0 + kb) * kSfBytes,
                         kSfBytes, full);
+          const uint8_t* sfb = second ? p.sfb1 : p.sfb;
 #pragma unroll
           for (int j = 0; j < G::kSfbAtoms; ++j)
             bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
-                          p.sfb + (((vrow >> 7) + j) * kgroups + kb) * kSfBytes, kSfBytes, full);
+                          sfb + (((vrow >> 7) + j) * kgroups_b + kg0 + kbb) * kSfBytes, kSfBytes,
+                          full);
           ++fills;
           if (++stage == S) {
             stage = 0;
@@ -212,6 +259,7 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const int kblocks = decode(t).kblocks;
         if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
@@ -249,7 +297,10 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
           }
         }
         if (!ok) break;
+        // a tile without k-blocks (WGrad, an expert without rows) issued no
+        // MMA: the commit only hands the (unwritten) accumulator on
         umma_commit(smem_u32(&sm->tfull[acc]));
+        issued = true;
         if (++acc == G::kAccBufs) {
           acc = 0;
           acc_phase ^= 1;
@@ -267,14 +318,13 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
-    const int half = (warp - 2) >> 2;         // fc1: which half of the tile's columns
+    const int half = (warp - 2) >> 2;         // 8 warps: which half of the tile's columns
     const int row_in_tile = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      int e, m, n;
-      decode(t, e, m, n);
-      const int64_t grow = p.off_al[e] + m * kTileM + row_in_tile;
+      const MxTile tl = decode(t);
+      const int64_t grow = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + row_in_tile;
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         sm->abort = 1;
@@ -283,17 +333,18 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
-      // The whole accumulator row is read into registers (packed bf16, or
-      // the finished E4M3 codes for fc1) and the accumulator is released
-      // before any global store, so that with a single accumulator the
-      // stores still overlap the next tile's MMAs.
       if (kFc1) {
-        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F. The tile's
-        // N/64 scale bytes of this row are adjacent in the tiled layout (one
-        // 128-wide K group of fc2): they leave in one store.
-        // this warp's half of the tile's h columns: kTileN / 4 of them
+        // The whole accumulator row is read into registers (the finished
+        // E4M3 codes) and the accumulator is released before any global
+        // store, so that with a single accumulator the stores still overlap
+        // the next tile's MMAs. h = bf16(silu(gate) * up), then MXFP8 per 32
+        // along F. The tile's N/64 scale bytes of this row are adjacent in
+        // the tiled layout (one 128-wide K group of fc2): they leave in one
+        // store. This warp's half of the tile's h columns: kTileN / 4.
         constexpr int kHalf = kTileN / 4;
         const int c0 = half * kHalf;
+        const int col = tl.n * n_cols + c0;
+        const bool save = p.save_h != nullptr;
         uint32_t codes[kHalf / 4];
         uint32_t packed = 0;
 #pragma unroll
@@ -307,12 +358,26 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
           for (int i = 0; i < 32; ++i)
             hv[i] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(g[i])) *
                                                          __uint_as_float(u[i])));
+          if (save) {           // A_g, A_u and h for the backward, in bf16
+            uint32_t w[16];
+            const int64_t o = grow * p.N + col + c;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+            store_bf16x32(p.save_g + o, w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            store_bf16x32(p.save_u + o, w);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+            store_bf16x32(p.save_h + o, w);
+          }
           const uint8_t sc = quantize_block32(hv, &codes[c / 4]);
           packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
-        const int col = n * n_cols + c0;
         int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
 #pragma unroll
         for (int i = 0; i < kHalf / 16; ++i)
@@ -322,14 +387,15 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
           *reinterpret_cast<uint16_t*>(hs) = static_cast<uint16_t>(packed);
         else
           *hs = static_cast<uint8_t>(packed);
-      } else {
-        constexpr int kHalf = kTileN;           // this warp's columns: all of them
-        const int c0 = 0;
-        uint32_t w[kHalf / 2];
+      } else if (kEpi == MxEpi::Bf16) {
+        // O = bf16: the row is packed into registers, the accumulator
+        // released, then stored
+        constexpr int kCols = kTileN;
+        uint32_t w[kCols / 2];
 #pragma unroll
-        for (int c = 0; c < kHalf; c += 32) {
+        for (int c = 0; c < kCols; c += 32) {
           uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + c0 + c, r);
+          tmem_ld_32x32b_x32(taddr + c, r);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -337,10 +403,91 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
-        __nv_bfloat16* out = p.out + grow * p.N + n * kTileN + c0;
+        __nv_bfloat16* out = p.out + grow * p.N + tl.n * kTileN;
 #pragma unroll
-        for (int i = 0; i < kHalf / 8; ++i)
+        for (int i = 0; i < kCols / 8; ++i)
           st_global_v4(out + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      } else if (kEpi == MxEpi::SwigluBwd) {
+        // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s),
+        // s = sigmoid(A_g), over this warp's half of the tile's columns
+        constexpr int kHalf = kTileN / 2;
+        const int f0 = tl.n * kTileN + half * kHalf;
+        const __nv_bfloat16* ag = p.act_g + grow * p.N + f0;
+        const __nv_bfloat16* au = p.act_u + grow * p.N + f0;
+        __nv_bfloat16* dg = p.out + grow * 2 * p.N + f0;
+        __nv_bfloat16* du = dg + p.N;
+#pragma unroll 1
+        for (int c = 0; c < kHalf; c += 32) {
+          uint32_t v[32];
+          float fg[32], fu[32];
+          tmem_ld_32x32b_x32(taddr + half * kHalf + c, v);
+          load_bf16x32(ag + c, fg);
+          load_bf16x32(au + c, fu);
+          tmem_ld_wait();
+          uint32_t wg[16], wu[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float vg[2], vu[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float dh = __uint_as_float(v[2 * i + h]);
+              const float a = fg[2 * i + h], b = fu[2 * i + h];
+              const float sg = sigmoid_f(a);
+              vg[h] = dh * b * sg * (1.0f + a * (1.0f - sg));
+              vu[h] = dh * a * sg;
+            }
+            wg[i] = pack_bf16x2(vg[0], vg[1]);
+            wu[i] = pack_bf16x2(vu[0], vu[1]);
+          }
+          store_bf16x32(dg + c, wg);
+          store_bf16x32(du + c, wu);
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
+      } else {
+        // float rows: dXp (Rows) or a weight-gradient row (WGrad; the
+        // expert's rows below out_split go to outf, the rest to outf2)
+        float* dst;
+        if (kWGrad) {
+          const int r = tl.m * kTileM + row_in_tile;
+          const int split = p.out_split > 0 ? p.out_split : p.M;
+          dst = r < split ? p.outf + (static_cast<int64_t>(tl.e) * split + r) * p.N
+                          : p.outf2 + (static_cast<int64_t>(tl.e) * (p.M - split) + (r - split)) * p.N;
+        } else {
+          dst = p.outf + grow * p.N;
+        }
+        dst += tl.n * kTileN;
+        const bool empty = tl.kblocks == 0;     // WGrad: an expert without rows
+        const bool add = kWGrad && p.accumulate != 0;
+        if (!(empty && add)) {
+#pragma unroll 1
+          for (int c = 0; c < kTileN; c += 32) {
+            uint32_t r[32];
+            if (!empty) {
+              tmem_ld_32x32b_x32(taddr + c, r);
+              tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) r[i] = 0u;
+            }
+            float4* o4 = reinterpret_cast<float4*>(dst + c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                     __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+              if (add) {
+                const float4 old = o4[i];
+                v.x += old.x;
+                v.y += old.y;
+                v.z += old.z;
+                v.w += old.w;
+              }
+              o4[i] = v;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
       }
       if (++acc == G::kAccBufs) {
         acc = 0;
@@ -357,7 +504,7 @@ __global__ void __launch_bounds__(num_threads<kFc1>(), 1)
   }
 }
 
-template <bool kFc1, int kN>
+template <MxEpi kEpi, Sched kSched, int kN>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                       const MxGemmArgs& p, int grid, cudaStream_t st) {
   using G = MxGeo<kN>;
@@ -365,28 +512,48 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                       static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kFc1, kN>,
+    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kEpi, kSched, kN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mx_gemm_kernel<kFc1, kN><<<grid, num_threads<kFc1>(), smem, st>>>(a, b0, b1, p);
+  mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(a, b0, b1, p);
   return cudaGetLastError();
+}
+
+template <MxEpi kEpi, Sched kSched>
+cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                         const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return p.bn == 256 ? launch_mx<kEpi, kSched, 256>(a, b0, b1, p, grid, st)
+                     : launch_mx<kEpi, kSched, 128>(a, b0, b1, p, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return p.bn == 256 ? launch_mx<true, 256>(a, wg, wu, p, grid, st)
-                     : launch_mx<true, 128>(a, wg, wu, p, grid, st);
+  return launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, p, grid, st);
 }
 
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
                           int grid, cudaStream_t st) {
-  return p.bn == 256 ? launch_mx<false, 256>(a, wd, wd, p, grid, st)
-                     : launch_mx<false, 128>(a, wd, wd, p, grid, st);
+  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, p, grid, st);
+}
+
+cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const MxGemmArgs& p,
+                         int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, p, grid, st);
+}
+
+cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
+                          const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::F32, Sched::Rows>(a, w1g, w1u, p, grid, st);
+}
+
+cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const MxGemmArgs& p,
+                            int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, p, grid, st);
 }
 
 }  // namespace moe

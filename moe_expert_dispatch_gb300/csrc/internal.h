@@ -73,6 +73,21 @@ cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_
 
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
                                   uint8_t* scales, cudaStream_t st);
+// The same with the scales in the MMA's tiled layout (rows % 128 == 0,
+// K % 128 == 0); rows at or past *row_end (when given) are skipped.
+cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, int K,
+                                        const int32_t* row_end, uint8_t* q, uint8_t* scales,
+                                        cudaStream_t st);
+// Quantisation along the rows of in[z] [rows, cols] (z < batch; element
+// (r, c) at in + z * batch_stride + r * ld + c): q[z] [cols, rows] codes,
+// scales row-major [batch, cols, rows/32] or tiled for batch * cols rows and
+// K = rows. rows % 32 == 0 (tiled: cols % 128 == 0, rows % 128 == 0). With
+// gather, row r reads row gather[r] of in (zero when outside [0, src_rows));
+// row blocks at or past *row_end (when given) are skipped.
+cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
+                                 int64_t batch_stride, int rows, int cols, const int32_t* gather,
+                                 int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
+                                 uint8_t* scales, cudaStream_t st);
 
 // ------------------------------------------------------------------ grouped GEMMs
 
@@ -181,21 +196,41 @@ cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t
                                int64_t rows_per_e, int K, int pair_half, uint8_t* dst,
                                cudaStream_t st);
 
+// Epilogues of the MXFP8 GEMMs: Fc1 = SwiGLU, h to bf16 and MXFP8 (codes +
+// tiled scales), optionally saving A_g, A_u and h in bf16; Bf16 = rows of
+// bf16 (fc2); SwigluBwd = dA_g, dA_u in bf16 from dH and the saved A_g, A_u;
+// F32 = float rows (dXp) or weight-gradient rows (WGrad schedule).
+enum class MxEpi { Fc1, Bf16, SwigluBwd, F32 };
+
 struct MxGemmArgs {
   const int32_t* off_al;   // [E+1] padded expert row offsets
   int E;
-  int K;                   // reduction length (elements = bytes)
-  int N;                   // output columns (fc1: F, fc2: H)
+  int K;                   // Rows: reduction length (elements = bytes)
+  int N;                   // output columns (fc1: F, fc2: H, dH: F, dXp: H, WGrad: cols of B)
+  int M;                   // WGrad: output rows per expert (rows of A)
   int stages;
   int bn;                  // MMA N: 128 or 256
-  int64_t b_rows;          // rows of one expert in B's 2D view (fc1: F, fc2: H)
-  int64_t sfb_rows;        // rows of one expert in B's tiled scales (fc1: 2F, fc2: H)
+  int64_t b_rows;          // Rows: rows of one expert in B's 2D view (fc1: F, fc2: H)
+  int64_t sfb_rows;        // Rows: rows of one expert in B's tiled scales (fc1: 2F, fc2: H)
+  int k_split;             // Rows: k-blocks taken from B0 before B1 (0: B0 only)
+  int kgroups_a;           // 128-wide K groups in A's tiled scales (0: K / 128)
+  int kgroups_b;           // 128-wide K groups in B's (and B1's) tiled scales (0: K / 128)
   int keep_a;              // L2 evict_last hint on A loads
   const uint8_t* sfa;      // tiled scales of A
-  const uint8_t* sfb;      // tiled scales of B
+  const uint8_t* sfb;      // tiled scales of B (B0)
+  const uint8_t* sfb1;     // tiled scales of B1 (k_split)
   uint8_t* hq;             // fc1: codes of h [rows, N]
   uint8_t* hs;             // fc1: tiled scales of h
-  __nv_bfloat16* out;      // fc2: O [rows, N]
+  __nv_bfloat16* save_g;   // fc1, optional: A_g, A_u and h in bf16 [rows, N]
+  __nv_bfloat16* save_u;
+  __nv_bfloat16* save_h;
+  __nv_bfloat16* out;      // Bf16: [rows, N]; SwigluBwd: [rows, 2N] = dA_g | dA_u
+  const __nv_bfloat16* act_g;   // SwigluBwd: saved A_g, A_u [rows, N]
+  const __nv_bfloat16* act_u;
+  float* outf;             // F32 Rows: [rows, N]; WGrad: rows r < out_split of each expert
+  float* outf2;            // WGrad: rows r >= out_split (at r - out_split)
+  int out_split;           // WGrad: 0 means M (all rows to outf)
+  int accumulate;          // WGrad: add to the outputs instead of overwriting
   int* err;
   unsigned long long wait_ns;
 };
@@ -206,6 +241,15 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const MxGemmArgs& p, int grid, cudaStream_t st);
+// dH with the SwiGLU backward epilogue (Rows; B = W2 as [E*F, H] along H).
+cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const MxGemmArgs& p,
+                         int grid, cudaStream_t st);
+// dXp = dA_g W1g^T + dA_u W1u^T in float (Rows; K = 2F split over B0, B1).
+cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
+                          const MxGemmArgs& p, int grid, cudaStream_t st);
+// Weight gradients (WGrad: K = each expert's padded rows), float out.
+cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const MxGemmArgs& p,
+                            int grid, cudaStream_t st);
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
                           int grid, cudaStream_t st);
 

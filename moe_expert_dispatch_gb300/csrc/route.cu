@@ -663,31 +663,119 @@ __device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* 
   }
 }
 
-// One thread per 32-element block, row-major scales [rows, K/32].
+// One thread per 32-element block along the rows. Scales row-major
+// [rows, K/32], or (kTiled) in the tiled layout of the block-scaled MMA
+// (rows % 128 == 0, K % 128 == 0); with row_end, rows at or past *row_end
+// are skipped (the unused tail of a padded row layout).
+template <bool kTiled>
 __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16* __restrict__ in,
-                                                             int64_t blocks,
+                                                             int64_t blocks, int K,
+                                                             const int32_t* __restrict__ row_end,
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ scales) {
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < blocks;
+  const int nb = K >> 5;
+  const int64_t limit = row_end ? static_cast<int64_t>(*row_end) * nb : blocks;
+  const int64_t end = limit < blocks ? limit : blocks;
+  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < end;
        b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float v[32];
     load_bf16x32_f(in + b * 32, v);
     uint32_t w[8];
-    scales[b] = quantize_block32(v, w);
+    const uint8_t sc = quantize_block32(v, w);
+    if (kTiled)
+      scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
+    else
+      scales[b] = sc;
     int4* dst = reinterpret_cast<int4*>(q + b * 32);
     dst[0] = make_int4(w[0], w[1], w[2], w[3]);
     dst[1] = make_int4(w[4], w[5], w[6], w[7]);
   }
 }
 
+static unsigned grid_for_blocks(int64_t blocks) {
+  const int64_t want = (blocks + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+  return static_cast<unsigned>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
                                   uint8_t* scales, cudaStream_t st) {
   const int64_t blocks = rows * (K / 32);
   if (blocks == 0) return cudaSuccess;
-  const int64_t want = (blocks + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
-  quantize_mxfp8_kernel<<<static_cast<unsigned>(want < cap ? want : cap), 256, 0, st>>>(
-      in, blocks, q, scales);
+  quantize_mxfp8_kernel<false><<<grid_for_blocks(blocks), 256, 0, st>>>(in, blocks, K, nullptr, q,
+                                                                        scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, int K,
+                                        const int32_t* row_end, uint8_t* q, uint8_t* scales,
+                                        cudaStream_t st) {
+  const int64_t blocks = rows * (K / 32);
+  if (blocks == 0) return cudaSuccess;
+  quantize_mxfp8_kernel<true><<<grid_for_blocks(blocks), 256, 0, st>>>(in, blocks, K, row_end, q,
+                                                                       scales);
+  return cudaGetLastError();
+}
+
+// Quantisation along the rows (the transposed orientation): for each batch z
+// and column c of in[z] [rows, cols], the 32-row blocks of that column become
+// 32 K-contiguous codes of q[z] [cols, rows] and one scale, row-major
+// [z, cols, rows/32] or (kTiled) tiled for an operand of batch * cols rows
+// and K = rows. One thread per column and 32-row block; a CTA covers 32 rows
+// of 256 columns. With gather, row r of in is in[gather[r]] (a routed row of
+// x), and a row whose gather index is outside [0, src_rows) is zero (padding).
+// With row_end, row blocks at or past *row_end are skipped.
+template <bool kTiled>
+__global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ in,
+                                                            int64_t ld, int64_t batch_stride,
+                                                            int rows, int cols,
+                                                            const int32_t* __restrict__ gather,
+                                                            int64_t src_rows,
+                                                            const int32_t* __restrict__ row_end,
+                                                            uint8_t* __restrict__ q,
+                                                            uint8_t* __restrict__ scales) {
+  const int rb = blockIdx.x;
+  if (row_end && rb * 32 >= *row_end) return;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  const int z = blockIdx.z;
+  const __nv_bfloat16* src = in + static_cast<int64_t>(z) * batch_stride + c;
+  float v[32];
+#pragma unroll 8
+  for (int i = 0; i < 32; ++i) {
+    int64_t r = rb * 32 + i;
+    bool live = true;
+    if (gather) {
+      r = __ldg(gather + r);
+      live = r >= 0 && r < src_rows;
+    }
+    v[i] = live ? __bfloat162float(src[r * ld]) : 0.0f;
+  }
+  uint32_t w[8];
+  const uint8_t sc = quantize_block32(v, w);
+  const int64_t orow = static_cast<int64_t>(z) * cols + c;
+  int4* dst = reinterpret_cast<int4*>(q + orow * rows + rb * 32);
+  dst[0] = make_int4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+  if (kTiled)
+    scales[mx_scale_offset(orow, rb, rows)] = sc;
+  else
+    scales[orow * (rows >> 5) + rb] = sc;
+}
+
+cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
+                                 int64_t batch_stride, int rows, int cols, const int32_t* gather,
+                                 int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
+                                 uint8_t* scales, cudaStream_t st) {
+  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(rows / 32), static_cast<unsigned>((cols + 255) / 256),
+                  static_cast<unsigned>(batch));
+  if (tiled)
+    quantize_cols_kernel<true><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
+                                                     src_rows, row_end, q, scales);
+  else
+    quantize_cols_kernel<false><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
+                                                      src_rows, row_end, q, scales);
   return cudaGetLastError();
 }
 
