@@ -159,7 +159,12 @@ def cpu_oracle_sample(w, inp, n_tokens: int):
     toks = list(range(n_tokens))
     f32 = synth.F32Slices
     t0 = time.perf_counter()
-    if w.mxfp8:
+    if w.mxfp8 and w.backward:
+        orc.backward_rows_mxfp8(inp["dy"].float().numpy(), inp["x"].float().numpy(),
+                                f32(inp["w_gate_t"]), f32(inp["w_up_t"]), f32(inp["w_down_t"]),
+                                inp["expert_ids"].numpy(), inp["probs"].numpy(), toks)
+        what = "MXFP8 forward + backward (dX, dprobs)"
+    elif w.mxfp8:
         orc.sampled_forward_mxfp8(inp["x"].float().numpy(), f32(inp["w_gate_t"]),
                                   f32(inp["w_up_t"]), f32(inp["w_down_t"]),
                                   inp["expert_ids"].numpy(), inp["probs"].numpy(), toks)
@@ -230,19 +235,44 @@ class Runner:
         self.stream = torch.cuda.current_stream()
         mk = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]  # noqa: E731
         self.fev = mk(m.STEP_EVENTS)
-        self.bev = mk(m.BWD_STEP_EVENTS) if w.backward else []
-        for e in self.fev + self.bev:
+        self.bev = (mk(m.MX_BWD_STEP_EVENTS if w.mxfp8 else m.BWD_STEP_EVENTS) if w.backward
+                    else [])
+        self.qev = mk(1)
+        for e in self.fev + self.bev + self.qev:
             e.record(self.stream)
         if w.mxfp8:
             self.wq = []
-            for key in ("w_gate_t", "w_up_t", "w_down_t"):
-                q, s = m.moe_quantize_mxfp8(inp[key].to(device))
+            self.w_bf16 = [inp[key].to(device) for key in ("w_gate_t", "w_up_t", "w_down_t")]
+            for wt in self.w_bf16:
+                q, s = m.moe_quantize_mxfp8(wt)
                 self.wq += [q, s]
-            self.cfg = m.config(mxfp8_tile_n=mx_tile_n)
-            self.cfg_ev = m.config(step_events=self.fev, mxfp8_tile_n=mx_tile_n)
+            save = bool(w.backward)
+            self.cfg = m.config(mxfp8_tile_n=mx_tile_n, save_for_backward=save)
+            self.cfg_ev = m.config(step_events=self.fev, mxfp8_tile_n=mx_tile_n,
+                                   save_for_backward=save)
             nbytes = m.moe_workspace_size_mxfp8(T, H, F, E, k, self.cfg)
             self.dtype = "mxfp8 (e4m3 + e8m0 per 32; bf16 out)"
-            self.launches = 9
+            self.launches = 10
+            if w.backward:
+                # training re-quantises its weights every step, in the forward's
+                # orientation and in the backward's (along the other axis)
+                self.wq_b = [None] * 6
+                for i, wt in enumerate(self.w_bf16):
+                    self.wq_b[2 * i], self.wq_b[2 * i + 1] = m.moe_quantize_mxfp8_t(wt)
+                self.dy = inp["dy"].to(device)
+                self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev,
+                                        mxfp8_tile_n=mx_tile_n)
+                self.bws = torch.empty(m.moe_workspace_size_mxfp8_backward(T, H, F, E, k),
+                                       dtype=torch.uint8, device=device)
+                self.grads = dict(
+                    dx=torch.empty_like(self.x),
+                    dw_gate_t=torch.empty((E, F, H), dtype=torch.float32, device=device),
+                    dw_up_t=torch.empty((E, F, H), dtype=torch.float32, device=device),
+                    dw_down_t=torch.empty((E, H, F), dtype=torch.float32, device=device),
+                    dprobs=torch.empty((T, k), dtype=torch.float32, device=device))
+                # weights 3 (both orientations each), forward 10 + zero padding,
+                # backward 14
+                self.launches = 3 + 11 + 14
         else:
             self.wg, self.wu, self.wd = (inp[key].to(device) for key in ("w_gate", "w_up", "w_down"))
             save = bool(w.backward)
@@ -286,8 +316,22 @@ class Runner:
         ids = self.ids if ids is None else ids
         probs = self.probs if probs is None else probs
         if self.w.mxfp8:
+            if self.w.backward:
+                if events:
+                    self.qev[0].record(self.stream)
+                for i, wt in enumerate(self.w_bf16):
+                    m.moe_quantize_mxfp8_dual(wt, out=(self.wq[2 * i], self.wq[2 * i + 1],
+                                                       self.wq_b[2 * i], self.wq_b[2 * i + 1]))
             m.moe_expert_forward_mxfp8(x, *self.wq, ids, probs, y=self.y, workspace=self.work,
                                        cfg=self.cfg_ev if events else self.cfg)
+            if self.w.backward:
+                g = self.grads
+                m.moe_expert_backward_mxfp8(self.dy if dy is None else dy, x, *self.wq_b, ids,
+                                            probs, self.work, dx=g["dx"],
+                                            dw_gate_t=g["dw_gate_t"], dw_up_t=g["dw_up_t"],
+                                            dw_down_t=g["dw_down_t"], dprobs=g["dprobs"],
+                                            workspace=self.bws,
+                                            cfg=self.cfg_bev if events else self.cfg)
             return
         if self.chunks and not plain:
             m.moe_expert_forward_pipelined(x, self.wg, self.wu, self.wd, ids, probs, self.chunks,
@@ -314,7 +358,14 @@ class Runner:
         f = self.fev
         out = {"routing": f[0].elapsed_time(f[1]), "fc1_swiglu": f[1].elapsed_time(f[2]),
                "fc2": f[2].elapsed_time(f[3]), "unpermute": f[3].elapsed_time(f[4])}
-        if self.bev:
+        if self.bev and self.w.mxfp8:
+            out["quantise_weights"] = self.qev[0].elapsed_time(f[0])
+            b = self.bev
+            names = ["dO_dprobs_quantise", "dH_swiglu_bwd", "quantise_dA", "dXp", "dX",
+                     "quantise_x_h", "dW1", "dW2"]
+            for i, n in enumerate(names):
+                out[n] = b[i].elapsed_time(b[i + 1])
+        elif self.bev:
             b = self.bev
             names = ["dO_dprobs", "dH_swiglu_bwd", "dXp", "dX", "dW1", "dW2"]
             for i, n in enumerate(names):

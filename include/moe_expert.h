@@ -69,7 +69,8 @@ typedef struct moe_config {
                               Forward (5): start, after routing (counts, row map,
                               permute), fc1+SwiGLU, fc2, unpermute.
                               Backward (7): start, after dO+dprobs, dH+SwiGLU
-                              backward, dXp, dX, dW1, dW2.                            */
+                              backward, dXp, dX, dW1, dW2. MXFP8 backward (9): see
+                              moe_expert_backward_mxfp8.                               */
   int num_step_events;     /* entries of step_events (events past it are not recorded) */
   int mxfp8_tile_n;        /* MMA N of the MXFP8 GEMMs: 128 (two accumulators, the
                               epilogue overlaps the next tile) or 256 (one accumulator,
@@ -78,6 +79,7 @@ typedef struct moe_config {
 
 #define MOE_STEP_EVENTS 5
 #define MOE_BWD_STEP_EVENTS 7
+#define MOE_MX_BWD_STEP_EVENTS 9
 
 void moe_config_init(moe_config* cfg);
 
@@ -364,10 +366,22 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
  *  in      bf16 [batch, rows, cols]
  *  q       uint8 [batch, cols, rows]        out (16-byte aligned)
  *  scales  uint8 [batch, cols, rows / 32]   out
- *  rows % 32 == 0.
+ *  rows % 32 == 0, cols % 8 == 0, in 16-byte aligned.
  * ------------------------------------------------------------------------ */
 moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int cols, uint8_t* q,
                                 uint8_t* scales, void* stream);
+
+/* ------------------------------------------------------------------------
+ * moe_quantize_mxfp8_dual - both orientations of a batch of bf16 matrices
+ * from one read: q_rows [batch, rows, cols] with scales [batch, rows, cols/32]
+ * as moe_quantize_mxfp8 gives them, and q_cols [batch, cols, rows] with
+ * scales [batch, cols, rows/32] as moe_quantize_mxfp8_t gives them. A training
+ * step quantises its weights both ways: the forward's layout and the
+ * backward's. rows % 32 == 0, cols % 128 == 0, 16-byte aligned pointers.
+ * ------------------------------------------------------------------------ */
+moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int cols,
+                                   uint8_t* q_rows, uint8_t* s_rows, uint8_t* q_cols,
+                                   uint8_t* s_cols, void* stream);
 
 /* ------------------------------------------------------------------------
  * moe_expert_backward_mxfp8 - gradients of moe_expert_forward_mxfp8: FP8
@@ -397,8 +411,12 @@ moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int col
  *  dprobs           float [T, k]      out
  *  workspace        >= moe_workspace_size_mxfp8_backward(T, H, F, E, k) bytes
  * Experts that receive no token get dW = 0 (or are left as they were when
- * accumulate_dw). cfg->mxfp8_tile_n picks the MMA N (default 256 where it
- * divides the output width). Requires H % 128 == 0, F % 128 == 0.
+ * accumulate_dw). cfg->mxfp8_tile_n picks the MMA N of every GEMM; by
+ * default dH takes 128 (its heavy epilogue overlaps the next tile) and the
+ * others 256 where it divides the output width. cfg->step_events, when given, receive up to 9
+ * events: start, after dO and its quantisations, dH, dA's quantisations,
+ * dXp, dX, the quantisations of x and h, dW1, dW2.
+ * Requires H % 128 == 0, F % 128 == 0.
  * ------------------------------------------------------------------------ */
 size_t moe_workspace_size_mxfp8_backward(int64_t T, int H, int F, int E, int k);
 moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_t* w1g_q,

@@ -41,6 +41,8 @@ class moe_config(ctypes.Structure):
 
 STEP_EVENTS = 5       # forward: start, routing, fc1+SwiGLU, fc2, unpermute
 BWD_STEP_EVENTS = 7   # backward: start, dO+dprobs, dH, dXp, dX, dW1, dW2
+# MXFP8 backward: start, dO + quantise, dH, quantise dA, dXp, dX, quantise x and h, dW1, dW2
+MX_BWD_STEP_EVENTS = 9
 
 
 def _sig(name, res, *args):
@@ -78,6 +80,7 @@ _sig("moe_expert_backward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32,
 _sig("moe_workspace_size_mxfp8", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config))
 _sig("moe_workspace_size_mxfp8_backward", _sz, _i64, _i32, _i32, _i32, _i32)
 _sig("moe_quantize_mxfp8_t", _i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp)
+_sig("moe_quantize_mxfp8_dual", _i32, _vp, _i64, _i32, _i32, _vp, _vp, _vp, _vp, _vp)
 _sig("moe_expert_backward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64,
      _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz,
      ctypes.POINTER(moe_config), _vp)
@@ -251,31 +254,63 @@ def moe_unpermute(o_perm: torch.Tensor, row_of: torch.Tensor, probs=None, y=None
     return y
 
 
-def moe_quantize_mxfp8(a: torch.Tensor, stream=None):
-    """(codes uint8 [..., K], scales uint8 [..., K/32]) of a bf16 tensor along its last axis."""
+def moe_quantize_mxfp8(a: torch.Tensor, stream=None, out=None):
+    """(codes uint8 [..., K], scales uint8 [..., K/32]) of a bf16 tensor along
+    its last axis, written into out=(codes, scales) when given."""
     _cuda(a, "a", torch.bfloat16)
     K = a.shape[-1]
     rows = a.numel() // K if K else 0
-    q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
-    s = torch.empty(a.shape[:-1] + (K // 32,), dtype=torch.uint8, device=a.device)
+    if out is None:
+        q = torch.empty(a.shape, dtype=torch.uint8, device=a.device)
+        s = torch.empty(a.shape[:-1] + (K // 32,), dtype=torch.uint8, device=a.device)
+    else:
+        q, s = out
+        _cuda(q, "q", torch.uint8)
+        _cuda(s, "scales", torch.uint8)
     _check(_lib.moe_quantize_mxfp8(_p(a), rows, K, _p(q), _p(s), _stream(stream)),
            "moe_quantize_mxfp8")
     return q, s
 
 
-def moe_quantize_mxfp8_t(a: torch.Tensor, stream=None):
+def moe_quantize_mxfp8_t(a: torch.Tensor, stream=None, out=None):
     """MXFP8 along the rows of each matrix of a bf16 [batch, rows, cols] (or
     [rows, cols]) tensor: (codes uint8 [batch, cols, rows], scales uint8
-    [batch, cols, rows/32])."""
+    [batch, cols, rows/32]), written into out=(codes, scales) when given."""
     _cuda(a, "a", torch.bfloat16)
     squeeze = a.dim() == 2
     a3 = a.unsqueeze(0) if squeeze else a
     B, rows, cols = a3.shape
-    q = torch.empty((B, cols, rows), dtype=torch.uint8, device=a.device)
-    s = torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device)
+    if out is None:
+        q = torch.empty((B, cols, rows), dtype=torch.uint8, device=a.device)
+        s = torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device)
+    else:
+        q, s = out
+        _cuda(q, "q", torch.uint8)
+        _cuda(s, "scales", torch.uint8)
+        if squeeze:
+            q, s = q.unsqueeze(0), s.unsqueeze(0)
     _check(_lib.moe_quantize_mxfp8_t(_p(a3), B, rows, cols, _p(q), _p(s), _stream(stream)),
            "moe_quantize_mxfp8_t")
     return (q[0], s[0]) if squeeze else (q, s)
+
+
+def moe_quantize_mxfp8_dual(a: torch.Tensor, stream=None, out=None):
+    """Both orientations of a bf16 [batch, rows, cols] tensor from one read:
+    (q [batch, rows, cols], s [batch, rows, cols/32]) as moe_quantize_mxfp8 and
+    (qt [batch, cols, rows], st [batch, cols, rows/32]) as moe_quantize_mxfp8_t,
+    written into out=(q, s, qt, st) when given."""
+    _cuda(a, "a", torch.bfloat16)
+    B, rows, cols = a.shape
+    if out is None:
+        out = (torch.empty((B, rows, cols), dtype=torch.uint8, device=a.device),
+               torch.empty((B, rows, cols // 32), dtype=torch.uint8, device=a.device),
+               torch.empty((B, cols, rows), dtype=torch.uint8, device=a.device),
+               torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device))
+    for t in out:
+        _cuda(t, "out", torch.uint8)
+    _check(_lib.moe_quantize_mxfp8_dual(_p(a), B, rows, cols, *(_p(t) for t in out),
+                                        _stream(stream)), "moe_quantize_mxfp8_dual")
+    return out
 
 
 def moe_workspace_size(T, H, F, E, k, cfg: moe_config | None = None, for_backward=False) -> int:
@@ -402,6 +437,10 @@ def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_work
 def moe_workspace_size_mxfp8(T, H, F, E, k, cfg: moe_config | None = None) -> int:
     c = cfg if cfg is not None else config()
     return _lib.moe_workspace_size_mxfp8(T, H, F, E, k, ctypes.byref(c))
+
+
+def moe_workspace_size_mxfp8_backward(T, H, F, E, k) -> int:
+    return _lib.moe_workspace_size_mxfp8_backward(T, H, F, E, k)
 
 
 def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, probs, y=None,

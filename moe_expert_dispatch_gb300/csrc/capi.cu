@@ -897,11 +897,27 @@ size_t moe_workspace_size_mxfp8_backward(int64_t T, int H, int F, int E, int k) 
   return mx_bwd_layout(T, H, F, E, k).total;
 }
 
+moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int cols,
+                                   uint8_t* q_rows, uint8_t* s_rows, uint8_t* q_cols,
+                                   uint8_t* s_cols, void* stream) {
+  if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 128 != 0)
+    return MOE_ERR_INVALID_ARG;
+  if (batch == 0) return MOE_OK;
+  if (!in || !q_rows || !s_rows || !q_cols || !s_cols || !aligned16(in) || !aligned16(q_rows) ||
+      !aligned16(q_cols))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_quantize_dual(static_cast<const __nv_bfloat16*>(in), cols, batch,
+                                        static_cast<int64_t>(rows) * cols, rows, cols, nullptr,
+                                        false, q_rows, s_rows, q_cols, s_cols,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int cols, uint8_t* q,
                                 uint8_t* scales, void* stream) {
-  if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0) return MOE_ERR_INVALID_ARG;
+  if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
   if (batch == 0) return MOE_OK;
-  if (!in || !q || !scales || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  if (!in || !q || !scales || !aligned16(in) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
   return from_cuda(launch_quantize_cols(static_cast<const __nv_bfloat16*>(in), cols, batch,
                                         static_cast<int64_t>(rows) * cols, rows, cols, nullptr, 0,
                                         nullptr, false, q, scales,
@@ -1096,9 +1112,8 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
                       dprobs, st)) ||
       !ok(launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, d_o, nullptr,
                               nullptr, st)) ||
-      !ok(launch_quantize_mxfp8_tiled(d_o, cap, H, row_end, at<uint8_t>(ws, B.doq),
-                                      at<uint8_t>(ws, B.dos), st)) ||
-      !ok(launch_quantize_cols(d_o, H, 1, 0, static_cast<int>(cap), H, nullptr, 0, row_end, true,
+      !ok(launch_quantize_dual(d_o, H, 1, 0, static_cast<int>(cap), H, row_end, true,
+                               at<uint8_t>(ws, B.doq), at<uint8_t>(ws, B.dos),
                                at<uint8_t>(ws, B.doT), at<uint8_t>(ws, B.dots), st)) ||
       // the weights' backward-orientation scales in the MMA's tiled layout
       !ok(launch_tile_scales(w2_s, nullptr, static_cast<int64_t>(E) * F, F, H, 0,
@@ -1111,6 +1126,9 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   mark(1);
 
   const int bnF = bn_for(F), bnH = bn_for(H);
+  // dH's SwiGLU-backward epilogue is heavy: by default it takes N = 128, whose
+  // two accumulators let it overlap the next tile's MMAs
+  const int bn_dh = c.mxfp8_tile_n == 0 ? 128 : bnF;
   CUtensorMap t_doq, t_w2, t_daq, t_w1g, t_w1u, t_daT, t_xpT, t_doT, t_hT;
   if (!make_tmap_u8_2d(&t_doq, at<uint8_t>(ws, B.doq), H, cap, H, 128, kTileM) ||
       !make_tmap_u8_2d(&t_w2, w2_q, H, static_cast<uint64_t>(E) * F, H, 128, 128) ||
@@ -1136,7 +1154,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   MxGemmArgs g = base;
   g.K = H;
   g.N = F;
-  g.bn = bnF;
+  g.bn = bn_dh;
   g.b_rows = F;
   g.sfb_rows = F;
   g.sfa = at<uint8_t>(ws, B.dos);
@@ -1149,12 +1167,12 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   mark(2);
 
   // dA quantised along 2F (dXp's K) and along the rows (dW1's K)
-  if (!ok(launch_quantize_mxfp8_tiled(d_a, cap, 2 * F, row_end, at<uint8_t>(ws, B.daq),
-                                      at<uint8_t>(ws, B.das), st)) ||
-      !ok(launch_quantize_cols(d_a, 2 * static_cast<int64_t>(F), 1, 0, static_cast<int>(cap),
-                               2 * F, nullptr, 0, row_end, true, at<uint8_t>(ws, B.daT),
+  if (!ok(launch_quantize_dual(d_a, 2 * static_cast<int64_t>(F), 1, 0, static_cast<int>(cap),
+                               2 * F, row_end, true, at<uint8_t>(ws, B.daq),
+                               at<uint8_t>(ws, B.das), at<uint8_t>(ws, B.daT),
                                at<uint8_t>(ws, B.dats), st)))
     return MOE_ERR_CUDA;
+  mark(3);
 
   // dXp = deq(dA_g) deq(W1g)^T + deq(dA_u) deq(W1u)^T: K = 2F, the first F
   // from W1g, the second from W1u; float rows
@@ -1172,10 +1190,10 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.outf = d_xp;
   g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
   if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, g, grid, st))) return MOE_ERR_CUDA;
-  mark(3);
+  mark(4);
   if (!ok(launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
     return MOE_ERR_CUDA;
-  mark(4);
+  mark(5);
 
   // weight gradients: x's routed rows and h quantised along the rows, then
   // dW1^T = deq(dA)^T deq(Xp) (rows 0..F-1 -> dw_gate_t, F..2F-1 -> dw_up_t)
@@ -1186,6 +1204,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
       !ok(launch_quantize_cols(hb, F, 1, 0, static_cast<int>(cap), F, nullptr, 0, row_end, true,
                                at<uint8_t>(ws, B.hT), at<uint8_t>(ws, B.hts), st)))
     return MOE_ERR_CUDA;
+  mark(6);
   const int kg_cap = static_cast<int>(cap / 128);
   g = base;
   g.M = 2 * F;
@@ -1200,7 +1219,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.out_split = F;
   g.accumulate = accumulate_dw;
   if (!ok(launch_mx_wgrad(t_daT, t_xpT, g, grid, st))) return MOE_ERR_CUDA;
-  mark(5);
+  mark(7);
   g = base;
   g.M = H;
   g.N = F;
@@ -1213,7 +1232,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.out_split = 0;
   g.accumulate = accumulate_dw;
   if (!ok(launch_mx_wgrad(t_doT, t_hT, g, grid, st))) return MOE_ERR_CUDA;
-  mark(6);
+  mark(8);
   return MOE_OK;
 }
 

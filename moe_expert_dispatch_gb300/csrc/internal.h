@@ -81,9 +81,18 @@ cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, i
 // Quantisation along the rows of in[z] [rows, cols] (z < batch; element
 // (r, c) at in + z * batch_stride + r * ld + c): q[z] [cols, rows] codes,
 // scales row-major [batch, cols, rows/32] or tiled for batch * cols rows and
-// K = rows. rows % 32 == 0 (tiled: cols % 128 == 0, rows % 128 == 0). With
+// K = rows. rows % 32 == 0, cols % 8 == 0, ld % 8 == 0 (tiled: batch * cols
+// % 128 == 0, rows % 128 == 0). With
 // gather, row r reads row gather[r] of in (zero when outside [0, src_rows));
 // row blocks at or past *row_end (when given) are skipped.
+// Both orientations of in[z] [rows, cols] from one read: q_row [batch * rows,
+// cols] along the columns (scales [batch * rows, cols/32], or tiled with
+// K = cols) and q_col as launch_quantize_cols. rows % 32 == 0, cols % 128 == 0.
+cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t batch,
+                                 int64_t batch_stride, int rows, int cols,
+                                 const int32_t* row_end, bool tiled, uint8_t* q_row,
+                                 uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                 cudaStream_t st);
 cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
                                  int64_t batch_stride, int rows, int cols, const int32_t* gather,
                                  int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,

@@ -19,27 +19,42 @@ __device__ __forceinline__ int floor_log2_pos(float a) {
   return (31 - __clz(static_cast<int>(man))) - 149;
 }
 
-// One block of 32 values: the E8M0 code of X = 2^(floor(log2 amax) - 8)
-// (clamped to [-127, 127]; an all-zero block gets -127) and the 32 E4M3
-// codes of v / X, round to nearest even, saturating at +-448, packed four to
-// a word (element 4i in the low byte of word i). v * 2^-s is exact (a
-// power-of-two scaling that stays in the normal range for every value that
-// can round to a non-zero E4M3), so the E4M3 conversion is the only rounding.
+// Exponent s of the shared scale X = 2^s of a block whose largest magnitude
+// is amax: floor(log2 amax) - 8, clamped to [-127, 127]; an all-zero block
+// gets -127. The E8M0 code is s + 127.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+  const int s = (amax > 0.0f) ? floor_log2_pos(amax) - 8 : -127;
+  return max(-127, min(127, s));
+}
+
+// 2^-s as a float, exact for s <= 126 (a finite float block has s <= 119).
+__device__ __forceinline__ float mx_inv_scale(int s) {
+  return __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+}
+
+// E4M3 codes of a * inv .. d * inv (round to nearest even, saturating at
+// +-448), a in the low byte. v * 2^-s is exact (a power-of-two scaling that
+// stays in the normal range for every value that can round to a non-zero
+// E4M3), so the E4M3 conversion is the only rounding.
+__device__ __forceinline__ uint32_t mx_encode4(float a, float b, float c, float d, float inv) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(a * inv, b * inv), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(c * inv, d * inv), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+// One block of 32 values: returns the E8M0 code of its scale and packs the
+// 32 E4M3 codes four to a word (element 4i in the low byte of word i).
 __device__ __forceinline__ uint8_t quantize_block32(const float* v, uint32_t* words) {
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  int s = (amax > 0.0f) ? floor_log2_pos(amax) - 8 : -127;
-  s = max(-127, min(127, s));
-  const float inv = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  const int s = mx_block_exp(amax);
+  const float inv = mx_inv_scale(s);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-        make_float2(v[4 * i] * inv, v[4 * i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-        make_float2(v[4 * i + 2] * inv, v[4 * i + 3] * inv), __NV_SATFINITE, __NV_E4M3);
-    words[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-  }
+  for (int i = 0; i < 8; ++i)
+    words[i] = mx_encode4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
   return static_cast<uint8_t>(s + 127);
 }
 

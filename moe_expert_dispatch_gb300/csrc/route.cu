@@ -663,10 +663,12 @@ __device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* 
   }
 }
 
-// One thread per 32-element block along the rows. Scales row-major
-// [rows, K/32], or (kTiled) in the tiled layout of the block-scaled MMA
-// (rows % 128 == 0, K % 128 == 0); with row_end, rows at or past *row_end
-// are skipped (the unused tail of a padded row layout).
+// Quantisation along the rows: four lanes per 32-element block, each with 8
+// consecutive elements (one 16-byte load, one 8-byte store), so a warp reads
+// 512 and writes 256 contiguous bytes; the block's amax is a max over the
+// four lanes. Scales row-major [rows, K/32], or (kTiled) in the tiled layout
+// of the block-scaled MMA (rows % 128 == 0, K % 128 == 0); with row_end,
+// rows at or past *row_end are skipped (the unused tail of a padded layout).
 template <bool kTiled>
 __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16* __restrict__ in,
                                                              int64_t blocks, int K,
@@ -675,20 +677,50 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16
                                                              uint8_t* __restrict__ scales) {
   const int nb = K >> 5;
   const int64_t limit = row_end ? static_cast<int64_t>(*row_end) * nb : blocks;
-  const int64_t end = limit < blocks ? limit : blocks;
-  for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < end;
-       b += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float v[32];
-    load_bf16x32_f(in + b * 32, v);
-    uint32_t w[8];
-    const uint8_t sc = quantize_block32(v, w);
-    if (kTiled)
-      scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
-    else
-      scales[b] = sc;
-    int4* dst = reinterpret_cast<int4*>(q + b * 32);
-    dst[0] = make_int4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+  const int64_t end = 4 * (limit < blocks ? limit : blocks);     // (block, quarter) items
+  const int lane = lane_id();
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // warp-uniform trip count: the shuffles below need every lane
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < end; base += step) {
+    const int64_t item = base + lane;
+    const bool live = item < end;
+    const int64_t b = item >> 2;
+    const int part = lane & 3;
+    float v[8];
+    if (live) {
+      const int4 raw = ld_stream(reinterpret_cast<const int4*>(in + b * 32 + part * 8));
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(h[j]);
+        v[2 * j] = f.x;
+        v[2 * j + 1] = f.y;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int sexp = mx_block_exp(amax);
+    const float inv = mx_inv_scale(sexp);
+    if (live) {
+      uint2 w;
+      w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
+      w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
+      *reinterpret_cast<uint2*>(q + b * 32 + part * 8) = w;
+      if (part == 0) {
+        const uint8_t sc = static_cast<uint8_t>(sexp + 127);
+        if (kTiled)
+          scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
+        else
+          scales[b] = sc;
+      }
+    }
   }
 }
 
@@ -721,10 +753,14 @@ cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, i
 // and column c of in[z] [rows, cols], the 32-row blocks of that column become
 // 32 K-contiguous codes of q[z] [cols, rows] and one scale, row-major
 // [z, cols, rows/32] or (kTiled) tiled for an operand of batch * cols rows
-// and K = rows. One thread per column and 32-row block; a CTA covers 32 rows
-// of 256 columns. With gather, row r of in is in[gather[r]] (a routed row of
-// x), and a row whose gather index is outside [0, src_rows) is zero (padding).
-// With row_end, row blocks at or past *row_end are skipped.
+// and K = rows. A CTA stages a tile of 64 rows x 128 columns in shared memory
+// with 16-byte row loads, then each thread quantises one column's 32-row
+// block out of it and writes its 32 codes as two 16-byte stores. With
+// gather, row r of in is in[gather[r]] (a routed row of x), and a row whose
+// gather index is outside [0, src_rows) is zero (padding). With row_end, row
+// blocks at or past *row_end are skipped. cols % 8 == 0.
+constexpr int kColTileRows = 64, kColTileCols = 128;
+
 template <bool kTiled>
 __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ in,
                                                             int64_t ld, int64_t batch_stride,
@@ -734,33 +770,148 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
                                                             const int32_t* __restrict__ row_end,
                                                             uint8_t* __restrict__ q,
                                                             uint8_t* __restrict__ scales) {
-  const int rb = blockIdx.x;
-  if (row_end && rb * 32 >= *row_end) return;
-  const int c = blockIdx.y * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
+  __shared__ __align__(16) __nv_bfloat16 tile[kColTileRows][kColTileCols];
+  const int r0 = blockIdx.x * kColTileRows;
+  const int live_rows = min(kColTileRows, (row_end ? min(rows, *row_end) : rows) - r0);
+  if (live_rows <= 0) return;
+  const int c0 = blockIdx.y * kColTileCols;
   const int z = blockIdx.z;
-  const __nv_bfloat16* src = in + static_cast<int64_t>(z) * batch_stride + c;
-  float v[32];
-#pragma unroll 8
-  for (int i = 0; i < 32; ++i) {
-    int64_t r = rb * 32 + i;
-    bool live = true;
-    if (gather) {
-      r = __ldg(gather + r);
-      live = r >= 0 && r < src_rows;
+  const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
+  // load: 16 threads per row (8 columns each), 16 rows per pass
+  const int lc = (threadIdx.x & 15) * 8;
+  for (int lr = threadIdx.x >> 4; lr < kColTileRows; lr += 16) {
+    int4 v = make_int4(0, 0, 0, 0);
+    if (lr < live_rows && c0 + lc < cols) {
+      int64_t r = r0 + lr;
+      bool ok = true;
+      if (gather) {
+        r = __ldg(gather + r);
+        ok = r >= 0 && r < src_rows;
+      }
+      if (ok) v = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + lc));
     }
-    v[i] = live ? __bfloat162float(src[r * ld]) : 0.0f;
+    *reinterpret_cast<int4*>(&tile[lr][lc]) = v;
   }
+  __syncthreads();
+  // quantise: thread (column c, 32-row block rb) of the tile
+  const int c = threadIdx.x & (kColTileCols - 1);
+  const int rb = threadIdx.x >> 7;
+  if (rb * 32 >= live_rows || c0 + c >= cols) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[rb * 32 + i][c]);
   uint32_t w[8];
   const uint8_t sc = quantize_block32(v, w);
-  const int64_t orow = static_cast<int64_t>(z) * cols + c;
-  int4* dst = reinterpret_cast<int4*>(q + orow * rows + rb * 32);
+  const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
+  const int64_t kb = (r0 >> 5) + rb;
+  int4* dst = reinterpret_cast<int4*>(q + orow * rows + kb * 32);
   dst[0] = make_int4(w[0], w[1], w[2], w[3]);
   dst[1] = make_int4(w[4], w[5], w[6], w[7]);
   if (kTiled)
-    scales[mx_scale_offset(orow, rb, rows)] = sc;
+    scales[mx_scale_offset(orow, kb, rows)] = sc;
   else
-    scales[orow * (rows >> 5) + rb] = sc;
+    scales[orow * (rows >> 5) + kb] = sc;
+}
+
+// Both orientations from one read: the tile of quantize_cols_kernel also
+// gives its rows' 32-column blocks (four lanes per block, as in
+// quantize_mxfp8_kernel), written to q_row [batch * rows, cols] with scales
+// row-major [batch * rows, cols/32] or tiled (K = cols). The column part is
+// that of quantize_cols_kernel. No gather; rows % 32 == 0, cols % 128 == 0.
+template <bool kTiled>
+__global__ void __launch_bounds__(256) quantize_dual_kernel(const __nv_bfloat16* __restrict__ in,
+                                                            int64_t ld, int64_t batch_stride,
+                                                            int rows, int cols,
+                                                            const int32_t* __restrict__ row_end,
+                                                            uint8_t* __restrict__ q_row,
+                                                            uint8_t* __restrict__ s_row,
+                                                            uint8_t* __restrict__ q_col,
+                                                            uint8_t* __restrict__ s_col) {
+  __shared__ __align__(16) __nv_bfloat16 tile[kColTileRows][kColTileCols];
+  const int r0 = blockIdx.x * kColTileRows;
+  const int live_rows = min(kColTileRows, (row_end ? min(rows, *row_end) : rows) - r0);
+  if (live_rows <= 0) return;
+  const int c0 = blockIdx.y * kColTileCols;
+  const int z = blockIdx.z;
+  const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
+  const int lc = (threadIdx.x & 15) * 8;
+  for (int lr = threadIdx.x >> 4; lr < kColTileRows; lr += 16) {
+    int4 v = make_int4(0, 0, 0, 0);
+    if (lr < live_rows)
+      v = ld_stream(reinterpret_cast<const int4*>(base + static_cast<int64_t>(r0 + lr) * ld + c0 + lc));
+    *reinterpret_cast<int4*>(&tile[lr][lc]) = v;
+  }
+  __syncthreads();
+  // rows: item = (row, 32-column block, quarter); a warp covers two rows
+  const int nbr = cols >> 5;
+  for (int it = threadIdx.x; it < kColTileRows * (kColTileCols / 8); it += blockDim.x) {
+    const int row = it >> 4, blk = (it >> 2) & 3, part = it & 3;
+    const int4 raw = *reinterpret_cast<const int4*>(&tile[row][blk * 32 + part * 8]);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h[j]);
+      v[2 * j] = f.x;
+      v[2 * j + 1] = f.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    if (row >= live_rows) continue;      // whole warps: live_rows is a multiple of 32
+    const int sexp = mx_block_exp(amax);
+    const float inv = mx_inv_scale(sexp);
+    const int64_t grow = static_cast<int64_t>(z) * rows + r0 + row;
+    uint2 w;
+    w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
+    w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
+    *reinterpret_cast<uint2*>(q_row + grow * cols + c0 + blk * 32 + part * 8) = w;
+    if (part == 0) {
+      const int kb = (c0 >> 5) + blk;
+      const uint8_t sc = static_cast<uint8_t>(sexp + 127);
+      if (kTiled)
+        s_row[mx_scale_offset(grow, kb, cols)] = sc;
+      else
+        s_row[grow * nbr + kb] = sc;
+    }
+  }
+  // columns
+  const int c = threadIdx.x & (kColTileCols - 1);
+  const int rb = threadIdx.x >> 7;
+  if (rb * 32 >= live_rows) return;
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[rb * 32 + i][c]);
+  uint32_t w[8];
+  const uint8_t sc = quantize_block32(v, w);
+  const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
+  const int64_t kb = (r0 >> 5) + rb;
+  int4* dst = reinterpret_cast<int4*>(q_col + orow * rows + kb * 32);
+  dst[0] = make_int4(w[0], w[1], w[2], w[3]);
+  dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+  if (kTiled)
+    s_col[mx_scale_offset(orow, kb, rows)] = sc;
+  else
+    s_col[orow * (rows >> 5) + kb] = sc;
+}
+
+cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t batch,
+                                 int64_t batch_stride, int rows, int cols,
+                                 const int32_t* row_end, bool tiled, uint8_t* q_row,
+                                 uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                 cudaStream_t st) {
+  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((rows + kColTileRows - 1) / kColTileRows),
+                  static_cast<unsigned>(cols / kColTileCols), static_cast<unsigned>(batch));
+  if (tiled)
+    quantize_dual_kernel<true><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
+                                                     q_row, s_row, q_col, s_col);
+  else
+    quantize_dual_kernel<false><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
+                                                      q_row, s_row, q_col, s_col);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
@@ -768,7 +919,8 @@ cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t ba
                                  int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
                                  uint8_t* scales, cudaStream_t st) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(rows / 32), static_cast<unsigned>((cols + 255) / 256),
+  const dim3 grid(static_cast<unsigned>((rows + kColTileRows - 1) / kColTileRows),
+                  static_cast<unsigned>((cols + kColTileCols - 1) / kColTileCols),
                   static_cast<unsigned>(batch));
   if (tiled)
     quantize_cols_kernel<true><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, gather,

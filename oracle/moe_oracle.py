@@ -725,6 +725,91 @@ def expert_backward_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs,
     return out
 
 
+def backward_rows_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, tokens):
+    """dX and dprobs of the listed tokens of expert_backward_mxfp8.
+
+    A token's data gradients depend only on its own rows, and every
+    row-quantised operand (x, h, dO, dA, and the weights) is quantised per
+    row, so this is the same arithmetic restricted to those rows. Experts
+    are visited one at a time and their weights quantised once."""
+    dy, x = np.asarray(dy), np.asarray(x)
+    ids = np.asarray(expert_ids)
+    pr = np.asarray(probs)
+    tokens = list(tokens)
+    dxr, dpt = {}, {}
+    for e in sorted(set(int(v) for t in tokens for v in ids[t])):
+        wg = quantized_along_rows(w_gate_t[e])           # [F, H] along H
+        wu = quantized_along_rows(w_up_t[e])
+        wd = quantized_along_rows(w_down_t[e])           # [H, F] along F
+        w2b = quantized_along_rows(_f64(w_down_t[e]).T)  # [F, H] along H
+        w1gb = quantized_along_rows(_f64(w_gate_t[e]).T)  # [H, F] along F
+        w1ub = quantized_along_rows(_f64(w_up_t[e]).T)
+        for t in tokens:
+            for j, ee in enumerate(ids[t].tolist()):
+                if ee != e:
+                    continue
+                xd = quantized_along_rows(x[t])
+                a_g, a_u = wg @ xd, wu @ xd
+                hv = bf16(silu(a_g) * a_u)
+                ov = bf16(wd @ quantized_along_rows(hv))
+                dpt[(t, j)] = float(np.dot(_f64(dy[t]), ov))
+                d_o = bf16(float(pr[t, j]) * _f64(dy[t]))
+                dh = w2b @ quantized_along_rows(d_o)
+                ga, ua = bf16(a_g), bf16(a_u)
+                sg = sigmoid(ga)
+                da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
+                da_u = bf16(dh * ga * sg)
+                dxr[(t, j)] = (w1gb @ quantized_along_rows(da_g) +
+                               w1ub @ quantized_along_rows(da_u))
+    k = ids.shape[1]
+    dx, dp = [], []
+    for t in tokens:
+        acc = dxr[(t, 0)]
+        for j in range(1, k):
+            acc = acc + dxr[(t, j)]
+        dx.append(bf16(acc))
+        dp.append([dpt[(t, j)] for j in range(k)])
+    return np.stack(dx), np.array(dp)
+
+
+def weight_grad_entries_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, e, pairs):
+    """For each (f, h) in pairs, the entries dw_gate_t[e][f, h],
+    dw_up_t[e][f, h] and dw_down_t[e][h, f] of expert_backward_mxfp8.
+
+    Each is a sum over the expert's routed rows of two column-quantised
+    vectors: column f of dA_g (or dA_u, or h) and column h of Xp (or dO).
+    Column f of A_g, A_u and dH over those rows needs only row f of the
+    quantised weights, so the full [rows, F] tensors are never formed."""
+    dy, x = np.asarray(dy), np.asarray(x)
+    ids = np.asarray(expert_ids)
+    pr = np.asarray(probs)
+    E = len(w_gate_t)
+    counts = expert_counts(ids, E)
+    off = expert_offsets(counts)
+    _, token_of, slot_of = permute_map(ids, E)
+    lo, hi = int(off[e]), int(off[e + 1])
+    toks = token_of[lo:hi]
+    q_col = lambda v: quantized_along_columns(np.asarray(v)[:, None])[:, 0]  # noqa: E731
+    xe = _f64(x[toks])
+    xd = quantized_along_rows(xe)
+    d_o = bf16(_f64(pr[toks, slot_of[lo:hi]])[:, None] * _f64(dy[toks]))
+    d_oq = quantized_along_rows(d_o)
+    out = []
+    for f, h in pairs:
+        a_g = xd @ quantized_along_rows(w_gate_t[e][f])
+        a_u = xd @ quantized_along_rows(w_up_t[e][f])
+        hv = bf16(silu(a_g) * a_u)
+        dh = d_oq @ quantized_along_rows(_f64(w_down_t[e])[:, f])
+        ga, ua = bf16(a_g), bf16(a_u)
+        sg = sigmoid(ga)
+        da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
+        da_u = bf16(dh * ga * sg)
+        xh = q_col(xe[:, h])
+        out.append((float(np.dot(q_col(da_g), xh)), float(np.dot(q_col(da_u), xh)),
+                    float(np.dot(q_col(d_o[:, h]), q_col(hv)))))
+    return np.array(out).reshape(len(pairs), 3)
+
+
 # --------------------------------------------------------------------------
 # micro-batch split
 # --------------------------------------------------------------------------

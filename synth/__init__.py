@@ -62,6 +62,12 @@ WORKLOADS = {
                                 mxfp8=True),
     "train_2experts": Workload("train_2experts", 2048, 4096, 14336, 2, 2, "gaussian", 0.01,
                                backward=True),
+    # the training workload in MXFP8 (FP8 training of the expert block), and
+    # its 2-expert profiling case
+    "train_mxfp8": Workload("train_mxfp8", 16384, 4096, 14336, 8, 2, "gaussian", 0.01,
+                            mxfp8=True, backward=True),
+    "train_mxfp8_2experts": Workload("train_mxfp8_2experts", 2048, 4096, 14336, 2, 2, "gaussian",
+                                     0.01, mxfp8=True, backward=True),
 }
 
 # Zipf exponent and the number of experts given zero popularity in the

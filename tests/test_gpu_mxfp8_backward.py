@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle as orc
+import synth
 from gpu_util import assert_rel_to_max, dev, to_np
 
 pytestmark = pytest.mark.gpu
@@ -111,3 +112,47 @@ def test_mxfp8_backward_zero_tokens():
     assert st == 0
     torch.cuda.synchronize()
     assert all(torch.count_nonzero(t) == 0 for t in dw)
+
+
+def test_mxfp8_backward_training_workload_sampled():
+    """The MXFP8 training workload at full size (T=16384, E=8, k=2): dX and
+    dprobs of sampled tokens, and sampled weight-gradient entries (each a sum
+    over all of its expert's rows), against the oracle's sampled forms. The
+    entries' bound is 3e-2 of the GPU tensor's max (the oracle gives no full
+    tensor to take the max of)."""
+    w = synth.WORKLOADS["train_mxfp8"]
+    inp = synth.make_inputs(w, 0)
+    c = dict(dy=inp["dy"], x=inp["x"], wg=inp["w_gate_t"], wu=inp["w_up_t"], wd=inp["w_down_t"],
+             ids=inp["expert_ids"], probs=inp["probs"])
+    g = _gpu(c)
+    f32 = synth.F32Slices
+    args = (to_np(c["dy"]), to_np(c["x"]), f32(c["wg"]), f32(c["wu"]), f32(c["wd"]),
+            c["ids"].numpy(), c["probs"].numpy())
+    # tokens routed to the same two experts as token 0: the oracle quantises
+    # each visited expert's six weight matrices, so fewer experts run faster
+    ids = c["ids"].numpy()
+    same = [t for t in range(1, w.T) if set(ids[t]) == set(ids[0])]
+    toks = [0, same[0], same[-1]]
+    dx, dp = orc.backward_rows_mxfp8(*args, toks)
+    assert_rel_to_max(to_np(g["dx"])[toks], dx, TOL, "dx sampled")
+    assert_rel_to_max(g["dprobs"].cpu().numpy()[toks], dp, TOL, "dprobs sampled")
+    pairs = [(0, 0), (777, 1234), (w.F - 1, w.H - 1), (5000, 3000)]
+    for e in sorted(set(int(v) for v in ids[0])):
+        ref = orc.weight_grad_entries_mxfp8(*args, e, pairs)
+        for i, (f, h) in enumerate(pairs):
+            for j, (key, idx) in enumerate((("dw_gate_t", (f, h)), ("dw_up_t", (f, h)),
+                                            ("dw_down_t", (h, f)))):
+                t = g[key][e]
+                bound = TOL * float(t.abs().max())
+                got = float(t[idx])
+                assert abs(got - ref[i, j]) <= bound, (key, e, f, h, got, ref[i, j], bound)
+
+
+def test_dual_quantiser_equals_both_single_ones():
+    g = torch.Generator().manual_seed(2)
+    w = (torch.randn((2, 160, 384), generator=g) * torch.logspace(-2, 2, 384)).to(torch.bfloat16)
+    q, s, qt, st = m.moe_quantize_mxfp8_dual(dev(w))
+    r = m.moe_quantize_mxfp8(dev(w))
+    rt = m.moe_quantize_mxfp8_t(dev(w))
+    assert torch.equal(q, r[0]) and torch.equal(s, r[1])
+    assert torch.equal(qt, rt[0]) and torch.equal(st, rt[1])

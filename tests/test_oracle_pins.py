@@ -575,3 +575,19 @@ def test_mxfp8_backward_close_to_unquantized():
     for key in ("dx", "dw_gate_t", "dw_up_t", "dw_down_t", "dprobs"):
         err = np.abs(mx[key] - ex[key]).max() / np.abs(ex[key]).max()
         assert err < 0.15, (key, err)
+
+
+def test_mxfp8_backward_sampled_helpers_agree():
+    dy, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=50, E=3, k=2, seed=35)
+    full = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs)
+    toks = [0, 17, 49]
+    dx, dp = orc.backward_rows_mxfp8(dy, x, wgt, wut, wdt, ids, probs, toks)
+    np.testing.assert_allclose(dx, full["dx"][toks], rtol=2 ** -7, atol=1e-12)
+    np.testing.assert_allclose(dp, full["dprobs"][toks], rtol=1e-9, atol=1e-12)
+    pairs = [(0, 0), (5, 63), (95, 17)]
+    for e in range(3):
+        got = orc.weight_grad_entries_mxfp8(dy, x, wgt, wut, wdt, ids, probs, e, pairs)
+        for i, (f, h) in enumerate(pairs):
+            want = (full["dw_gate_t"][e][f, h], full["dw_up_t"][e][f, h],
+                    full["dw_down_t"][e][h, f])
+            np.testing.assert_allclose(got[i], want, rtol=1e-9, atol=1e-12)
