@@ -1013,14 +1013,22 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.sfb = wgu_s;
   g1.hq = hq;
   g1.hs = hs;
-  if (save) {
-    g1.save_g = at<__nv_bfloat16>(workspace, L.ag);
-    g1.save_u = at<__nv_bfloat16>(workspace, L.au);
-    g1.save_h = at<__nv_bfloat16>(workspace, L.hb);
+  GemmOut o1, o2;
+  g1.save = save ? 1 : 0;
+  if (save) {   // A_g, A_u and h in bf16 for the backward
+    if (!make_out_tmap(&o1.map[0], at<void>(workspace, L.ag), F, L.cap,
+                       static_cast<uint64_t>(F) * 2, false) ||
+        !make_out_tmap(&o1.map[1], at<void>(workspace, L.au), F, L.cap,
+                       static_cast<uint64_t>(F) * 2, false) ||
+        !make_out_tmap(&o1.map[2], at<void>(workspace, L.hb), F, L.cap,
+                       static_cast<uint64_t>(F) * 2, false))
+      return MOE_ERR_CUDA;
+  } else {
+    o1.map[0] = o1.map[1] = o1.map[2] = ta;    // unused
   }
   g1.err = err;
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
-  if (launch_mx_fc1(ta, tg, tu, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_mx_fc1(ta, tg, tu, o1, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
   MxGemmArgs g2 = g1;
   g2.K = F;
@@ -1032,9 +1040,11 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g2.keep_a = keep(static_cast<uint64_t>(L.R) * F);
   g2.hq = nullptr;
   g2.hs = nullptr;
-  g2.save_g = g2.save_u = g2.save_h = nullptr;
-  g2.out = o;
-  if (launch_mx_fc2(th, td, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  g2.save = 0;
+  if (!make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
+    return MOE_ERR_CUDA;
+  o2.map[1] = o2.map[2] = o2.map[0];
+  if (launch_mx_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
   const cudaError_t ue =
       launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
@@ -1161,9 +1171,13 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.sfb = at<uint8_t>(ws, B.w2_st);
   g.act_g = ag;
   g.act_u = au;
-  g.out = d_a;
+  GemmOut od;
+  if (!make_out_tmap(&od.map[0], d_a, 2 * static_cast<uint64_t>(F), cap,
+                     static_cast<uint64_t>(F) * 4, false))
+    return MOE_ERR_CUDA;
+  od.map[1] = od.map[2] = od.map[0];
   g.keep_a = keep(static_cast<uint64_t>(cap) * H);
-  if (!ok(launch_mx_dh(t_doq, t_w2, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st))) return MOE_ERR_CUDA;
   mark(2);
 
   // dA quantised along 2F (dXp's K) and along the rows (dW1's K)
@@ -1187,9 +1201,12 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.sfa = at<uint8_t>(ws, B.das);
   g.sfb = at<uint8_t>(ws, B.w1g_st);
   g.sfb1 = at<uint8_t>(ws, B.w1u_st);
-  g.outf = d_xp;
+  GemmOut ox;
+  if (!make_out_tmap(&ox.map[0], d_xp, H, cap, static_cast<uint64_t>(H) * 4, true))
+    return MOE_ERR_CUDA;
+  ox.map[1] = ox.map[2] = ox.map[0];
   g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
-  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st))) return MOE_ERR_CUDA;
   mark(4);
   if (!ok(launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
     return MOE_ERR_CUDA;
@@ -1214,11 +1231,19 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.kgroups_b = kg_cap;
   g.sfa = at<uint8_t>(ws, B.dats);
   g.sfb = at<uint8_t>(ws, B.xpts);
-  g.outf = dw_gate_t;
-  g.outf2 = dw_up_t;
+  GemmOut ow1, ow2;
+  if (!make_out_tmap(&ow1.map[0], dw_gate_t, H, static_cast<uint64_t>(E) * F,
+                     static_cast<uint64_t>(H) * 4, true) ||
+      !make_out_tmap(&ow1.map[1], dw_up_t, H, static_cast<uint64_t>(E) * F,
+                     static_cast<uint64_t>(H) * 4, true) ||
+      !make_out_tmap(&ow2.map[0], dw_down_t, F, static_cast<uint64_t>(E) * H,
+                     static_cast<uint64_t>(F) * 4, true))
+    return MOE_ERR_CUDA;
+  ow1.map[2] = ow1.map[0];
+  ow2.map[1] = ow2.map[2] = ow2.map[0];
   g.out_split = F;
   g.accumulate = accumulate_dw;
-  if (!ok(launch_mx_wgrad(t_daT, t_xpT, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_wgrad(t_daT, t_xpT, ow1, g, grid, st))) return MOE_ERR_CUDA;
   mark(7);
   g = base;
   g.M = H;
@@ -1228,10 +1253,10 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.kgroups_b = kg_cap;
   g.sfa = at<uint8_t>(ws, B.dots);
   g.sfb = at<uint8_t>(ws, B.hts);
-  g.outf = dw_down_t;
+
   g.out_split = 0;
   g.accumulate = accumulate_dw;
-  if (!ok(launch_mx_wgrad(t_doT, t_hT, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_wgrad(t_doT, t_hT, ow2, g, grid, st))) return MOE_ERR_CUDA;
   mark(8);
   return MOE_OK;
 }

@@ -17,7 +17,10 @@
 // Epilogues (MxEpi): fc1 rounds h to bf16 and quantises it per 32 along F
 // (codes + tiled scales for fc2), optionally saving A_g, A_u and h in bf16
 // for the backward; fc2 rounds O to bf16; dH applies the SwiGLU backward to
-// the saved A_g, A_u; F32 writes float rows (dXp) or weight-gradient rows.
+// the saved A_g, A_u; F32 writes float rows (dXp) or weight-gradient rows
+// (reduce-added when accumulating). Rows leave through per-warp shared-memory
+// pieces and TMA tensor stores; only fc1's codes and scales are stored from
+// registers.
 // Schedules: Rows (expert segments padded to 128 rows; M fastest within an
 // expert unless it has more M tiles than N tiles) and WGrad (K runs over one
 // expert's padded rows; every expert owns M/128 x N/bn output tiles, N
@@ -65,6 +68,15 @@ struct MxGeo {
   static constexpr int kStages = kN == 128 ? 6 : 4;   // what fits in shared memory
 };
 
+// Output rows leave as per-warp pieces of 32 rows x 64 bytes (32 bf16 or
+// 16 float columns): each epilogue warp fills its own shared-memory slot,
+// with the 64-byte swizzle of the output maps (16-byte chunk j of row r at
+// chunk j ^ ((r >> 1) & 3)), and its lane 0 writes it with a TMA tensor
+// store (or reduce-add). Whole-row bursts replace per-thread stores that
+// would scatter 32 rows per warp instruction.
+constexpr int kPieceBytes = 32 * 64;                  // 2 KB
+constexpr int kPieceArea = 8 * kPieceBytes;           // one slot per epilogue warp
+
 struct Smem {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
@@ -82,15 +94,13 @@ struct MxTile {
   int e, m, n, kblocks, k0;
 };
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t* w) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) st_global_v4(dst + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-}
-
 template <MxEpi kEpi, Sched kSched, int kTileN>
 __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, MxGemmArgs p) {
+                   const __grid_constant__ CUtensorMap tmB1,
+                   const __grid_constant__ CUtensorMap tmO0,
+                   const __grid_constant__ CUtensorMap tmO1,
+                   const __grid_constant__ CUtensorMap tmO2, MxGemmArgs p) {
   constexpr bool kFc1 = kEpi == MxEpi::Fc1;
   constexpr bool kWGrad = kSched == Sched::WGrad;
   constexpr int kThreads = num_threads<kEpi>();
@@ -101,7 +111,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
   constexpr int kBBytes = G::kBBytes;
   constexpr int kStageBytes = G::kStageBytes;
   const int S = p.stages < G::kStages ? p.stages : G::kStages;
-  Smem* sm = reinterpret_cast<Smem*>(ring + S * kStageBytes);
+  uint8_t* pieces = ring + S * kStageBytes;
+  Smem* sm = reinterpret_cast<Smem*>(pieces + kPieceArea);
   int* ts = reinterpret_cast<int*>(sm + 1);
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int E = p.E;
@@ -320,11 +331,46 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
     const int half = (warp - 2) >> 2;         // 8 warps: which half of the tile's columns
     const int row_in_tile = q * 32 + lane;
+    // 8 slots in all: one per warp of an 8-warp epilogue, two (alternating)
+    // per warp of a 4-warp one
+    constexpr int kSlots = 8 / epi_warps<kEpi>();
+    const uint32_t slot0 = smem_u32(pieces) + (warp - 2) * kSlots * kPieceBytes;
+    const uint32_t my_row = lane * 64;
+    const uint32_t sw = (lane >> 1) & 3;
+    int npiece = 0;
+    // a piece: wait until the warp's next slot has been read by its last
+    // store, fill this lane's 64-byte row, hand the slot to TMA
+    auto put_piece = [&](const uint32_t* w16, const CUtensorMap* map, int x, int y, bool add) {
+      if (lane == 0) bulk_wait_group_read<kSlots - 1>();
+      __syncwarp();
+      const uint32_t slot = slot0 + (npiece % kSlots) * kPieceBytes;
+      ++npiece;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + my_row +
+                                                                       ((j ^ sw) << 4)),
+                     "r"(w16[4 * j]), "r"(w16[4 * j + 1]), "r"(w16[4 * j + 2]),
+                     "r"(w16[4 * j + 3])
+                     : "memory");
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        if (add) tma_reduce_add_2d(map, slot, x, y);
+        else tma_store_2d(map, slot, x, y);
+        bulk_commit_group();
+      }
+    };
+    auto bf16_words = [](const uint32_t* f32x32, uint32_t* w16) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w16[i] = pack_bf16x2(__uint_as_float(f32x32[2 * i]), __uint_as_float(f32x32[2 * i + 1]));
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const MxTile tl = decode(t);
       const int64_t grow = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + row_in_tile;
+      const int wrow0 = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + q * 32;   // warp's first row
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         sm->abort = 1;
@@ -334,17 +380,15 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
       if (kFc1) {
-        // The whole accumulator row is read into registers (the finished
-        // E4M3 codes) and the accumulator is released before any global
-        // store, so that with a single accumulator the stores still overlap
-        // the next tile's MMAs. h = bf16(silu(gate) * up), then MXFP8 per 32
-        // along F. The tile's N/64 scale bytes of this row are adjacent in
-        // the tiled layout (one 128-wide K group of fc2): they leave in one
-        // store. This warp's half of the tile's h columns: kTileN / 4.
+        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F; the codes are
+        // held in registers and stored after the accumulator is released.
+        // The tile's N/64 scale bytes of this row are adjacent in the tiled
+        // layout (one 128-wide K group of fc2): they leave in one store.
+        // With save, A_g, A_u and h leave as bf16 pieces. This warp's half
+        // of the tile's h columns: kTileN / 4.
         constexpr int kHalf = kTileN / 4;
         const int c0 = half * kHalf;
         const int col = tl.n * n_cols + c0;
-        const bool save = p.save_h != nullptr;
         uint32_t codes[kHalf / 4];
         uint32_t packed = 0;
 #pragma unroll
@@ -358,20 +402,15 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           for (int i = 0; i < 32; ++i)
             hv[i] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(g[i])) *
                                                          __uint_as_float(u[i])));
-          if (save) {           // A_g, A_u and h for the backward, in bf16
+          if (p.save) {
             uint32_t w[16];
-            const int64_t o = grow * p.N + col + c;
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
-            store_bf16x32(p.save_g + o, w);
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              w[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
-            store_bf16x32(p.save_u + o, w);
+            bf16_words(g, w);
+            put_piece(w, &tmO0, col + c, wrow0, false);
+            bf16_words(u, w);
+            put_piece(w, &tmO1, col + c, wrow0, false);
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-            store_bf16x32(p.save_h + o, w);
+            put_piece(w, &tmO2, col + c, wrow0, false);
           }
           const uint8_t sc = quantize_block32(hv, &codes[c / 4]);
           packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
@@ -388,34 +427,25 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         else
           *hs = static_cast<uint8_t>(packed);
       } else if (kEpi == MxEpi::Bf16) {
-        // O = bf16: the row is packed into registers, the accumulator
-        // released, then stored
-        constexpr int kCols = kTileN;
-        uint32_t w[kCols / 2];
-#pragma unroll
-        for (int c = 0; c < kCols; c += 32) {
-          uint32_t r[32];
+        // O = bf16, 32 columns per piece
+#pragma unroll 1
+        for (int c = 0; c < kTileN; c += 32) {
+          uint32_t r[32], w[16];
           tmem_ld_32x32b_x32(taddr + c, r);
           tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[c / 2 + i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          bf16_words(r, w);
+          put_piece(w, &tmO0, tl.n * kTileN + c, wrow0, false);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
-        __nv_bfloat16* out = p.out + grow * p.N + tl.n * kTileN;
-#pragma unroll
-        for (int i = 0; i < kCols / 8; ++i)
-          st_global_v4(out + 8 * i, w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       } else if (kEpi == MxEpi::SwigluBwd) {
         // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s),
-        // s = sigmoid(A_g), over this warp's half of the tile's columns
+        // s = sigmoid(A_g), over this warp's half of the tile's columns; dA_g
+        // at column f of [dA_g | dA_u], dA_u at N + f
         constexpr int kHalf = kTileN / 2;
         const int f0 = tl.n * kTileN + half * kHalf;
         const __nv_bfloat16* ag = p.act_g + grow * p.N + f0;
         const __nv_bfloat16* au = p.act_u + grow * p.N + f0;
-        __nv_bfloat16* dg = p.out + grow * 2 * p.N + f0;
-        __nv_bfloat16* du = dg + p.N;
 #pragma unroll 1
         for (int c = 0; c < kHalf; c += 32) {
           uint32_t v[32];
@@ -439,24 +469,28 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             wg[i] = pack_bf16x2(vg[0], vg[1]);
             wu[i] = pack_bf16x2(vu[0], vu[1]);
           }
-          store_bf16x32(dg + c, wg);
-          store_bf16x32(du + c, wu);
+          put_piece(wg, &tmO0, f0 + c, wrow0, false);
+          put_piece(wu, &tmO0, p.N + f0 + c, wrow0, false);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
       } else {
-        // float rows: dXp (Rows) or a weight-gradient row (WGrad; the
-        // expert's rows below out_split go to outf, the rest to outf2)
-        float* dst;
+        // float rows, 16 columns per piece: dXp (Rows) or a weight-gradient
+        // row (WGrad; the expert's rows below out_split go to map 0 at row
+        // e * out_split + r, the rest to map 1 at e * (M - out_split) + r -
+        // out_split; out_split is a multiple of 128, so a tile is on one side)
+        const CUtensorMap* map = &tmO0;
+        int y = wrow0;
         if (kWGrad) {
-          const int r = tl.m * kTileM + row_in_tile;
+          const int r = tl.m * kTileM + q * 32;
           const int split = p.out_split > 0 ? p.out_split : p.M;
-          dst = r < split ? p.outf + (static_cast<int64_t>(tl.e) * split + r) * p.N
-                          : p.outf2 + (static_cast<int64_t>(tl.e) * (p.M - split) + (r - split)) * p.N;
-        } else {
-          dst = p.outf + grow * p.N;
+          if (r < split) {
+            y = tl.e * split + r;
+          } else {
+            map = &tmO1;
+            y = tl.e * (p.M - split) + (r - split);
+          }
         }
-        dst += tl.n * kTileN;
         const bool empty = tl.kblocks == 0;     // WGrad: an expert without rows
         const bool add = kWGrad && p.accumulate != 0;
         if (!(empty && add)) {
@@ -470,20 +504,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) r[i] = 0u;
             }
-            float4* o4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 v = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                     __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-              if (add) {
-                const float4 old = o4[i];
-                v.x += old.x;
-                v.y += old.y;
-                v.z += old.z;
-                v.w += old.w;
-              }
-              o4[i] = v;
-            }
+            put_piece(r, map, tl.n * kTileN + c, y, add);
+            put_piece(r + 16, map, tl.n * kTileN + c + 16, y, add);
           }
         }
         tc_fence_before();
@@ -494,6 +516,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait_group_all();     // every store has landed before exit
   }
 
   tc_fence_before();
@@ -506,10 +529,13 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 
 template <MxEpi kEpi, Sched kSched, int kN>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const MxGemmArgs& p, int grid, cudaStream_t st) {
+                      const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
   using G = MxGeo<kN>;
-  const size_t smem = 1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + sizeof(Smem) +
-                      static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
+  const size_t smem = 1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
+                      sizeof(Smem) + static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
+  static_assert(1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
+                        sizeof(Smem) + (kMaxExperts + 1) * sizeof(int) <= 232448,
+                "shared memory of one CTA");
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kEpi, kSched, kN>,
@@ -518,42 +544,43 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(a, b0, b1, p);
+  mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(
+      a, b0, b1, o.map[0], o.map[1], o.map[2], p);
   return cudaGetLastError();
 }
 
 template <MxEpi kEpi, Sched kSched>
 cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                         const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return p.bn == 256 ? launch_mx<kEpi, kSched, 256>(a, b0, b1, p, grid, st)
-                     : launch_mx<kEpi, kSched, 128>(a, b0, b1, p, grid, st);
+                         const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return p.bn == 256 ? launch_mx<kEpi, kSched, 256>(a, b0, b1, o, p, grid, st)
+                     : launch_mx<kEpi, kSched, 128>(a, b0, b1, o, p, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st);
+}
+
+cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,
                           const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, p, grid, st);
+  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, o, p, grid, st);
 }
 
-cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
-                          int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, p, grid, st);
-}
-
-cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const MxGemmArgs& p,
-                         int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, p, grid, st);
+cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
+                         const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, o, p, grid, st);
 }
 
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
-                          const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::F32, Sched::Rows>(a, w1g, w1u, p, grid, st);
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::F32, Sched::Rows>(a, w1g, w1u, o, p, grid, st);
 }
 
-cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const MxGemmArgs& p,
-                            int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, p, grid, st);
+cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
+                            const MxGemmArgs& p, int grid, cudaStream_t st) {
+  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, o, p, grid, st);
 }
 
 }  // namespace moe

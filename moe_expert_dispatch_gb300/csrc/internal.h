@@ -208,7 +208,10 @@ cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t
 // Epilogues of the MXFP8 GEMMs: Fc1 = SwiGLU, h to bf16 and MXFP8 (codes +
 // tiled scales), optionally saving A_g, A_u and h in bf16; Bf16 = rows of
 // bf16 (fc2); SwigluBwd = dA_g, dA_u in bf16 from dH and the saved A_g, A_u;
-// F32 = float rows (dXp) or weight-gradient rows (WGrad schedule).
+// F32 = float rows (dXp) or weight-gradient rows (WGrad schedule). Rows
+// leave through the output tensor maps (make_out_tmap): fc1's saves
+// (0: A_g, 1: A_u, 2: h), fc2's O (0), dH's [dA_g | dA_u] (0), dXp (0), the
+// weight gradients (0, and 1 past out_split).
 enum class MxEpi { Fc1, Bf16, SwigluBwd, F32 };
 
 struct MxGemmArgs {
@@ -230,15 +233,11 @@ struct MxGemmArgs {
   const uint8_t* sfb1;     // tiled scales of B1 (k_split)
   uint8_t* hq;             // fc1: codes of h [rows, N]
   uint8_t* hs;             // fc1: tiled scales of h
-  __nv_bfloat16* save_g;   // fc1, optional: A_g, A_u and h in bf16 [rows, N]
-  __nv_bfloat16* save_u;
-  __nv_bfloat16* save_h;
-  __nv_bfloat16* out;      // Bf16: [rows, N]; SwigluBwd: [rows, 2N] = dA_g | dA_u
+  int save;                // fc1: also store A_g, A_u and h in bf16 (output maps 0, 1, 2)
   const __nv_bfloat16* act_g;   // SwigluBwd: saved A_g, A_u [rows, N]
   const __nv_bfloat16* act_u;
-  float* outf;             // F32 Rows: [rows, N]; WGrad: rows r < out_split of each expert
-  float* outf2;            // WGrad: rows r >= out_split (at r - out_split)
-  int out_split;           // WGrad: 0 means M (all rows to outf)
+  int out_split;           // WGrad: rows r < out_split of each expert go to output map 0
+                           // (row e * out_split + r), the rest to map 1; 0 means M
   int accumulate;          // WGrad: add to the outputs instead of overwriting
   int* err;
   unsigned long long wait_ns;
@@ -249,18 +248,18 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
                      uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                          const MxGemmArgs& p, int grid, cudaStream_t st);
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st);
 // dH with the SwiGLU backward epilogue (Rows; B = W2 as [E*F, H] along H).
-cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const MxGemmArgs& p,
-                         int grid, cudaStream_t st);
+cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
+                         const MxGemmArgs& p, int grid, cudaStream_t st);
 // dXp = dA_g W1g^T + dA_u W1u^T in float (Rows; K = 2F split over B0, B1).
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
-                          const MxGemmArgs& p, int grid, cudaStream_t st);
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st);
 // Weight gradients (WGrad: K = each expert's padded rows), float out.
-cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const MxGemmArgs& p,
-                            int grid, cudaStream_t st);
-cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const MxGemmArgs& p,
-                          int grid, cudaStream_t st);
+cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
+                            const MxGemmArgs& p, int grid, cudaStream_t st);
+cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,
+                          const MxGemmArgs& p, int grid, cudaStream_t st);
 
 int device_sm_count();
 
