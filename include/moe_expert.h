@@ -411,9 +411,8 @@ moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int 
  *  dprobs           float [T, k]      out
  *  workspace        >= moe_workspace_size_mxfp8_backward(T, H, F, E, k) bytes
  * Experts that receive no token get dW = 0 (or are left as they were when
- * accumulate_dw). cfg->mxfp8_tile_n picks the MMA N of every GEMM; by
- * default dH takes 128 (its heavy epilogue overlaps the next tile) and the
- * others 256 where it divides the output width. cfg->step_events, when given, receive up to 9
+ * accumulate_dw). cfg->mxfp8_tile_n picks the MMA N of every GEMM (default
+ * 256 where it divides the output width). cfg->step_events, when given, receive up to 9
  * events: start, after dO and its quantisations, dH, dA's quantisations,
  * dXp, dX, the quantisations of x and h, dW1, dW2.
  * Requires H % 128 == 0, F % 128 == 0.

@@ -1136,9 +1136,6 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   mark(1);
 
   const int bnF = bn_for(F), bnH = bn_for(H);
-  // dH's SwiGLU-backward epilogue is heavy: by default it takes N = 128, whose
-  // two accumulators let it overlap the next tile's MMAs
-  const int bn_dh = c.mxfp8_tile_n == 0 ? 128 : bnF;
   CUtensorMap t_doq, t_w2, t_daq, t_w1g, t_w1u, t_daT, t_xpT, t_doT, t_hT;
   if (!make_tmap_u8_2d(&t_doq, at<uint8_t>(ws, B.doq), H, cap, H, 128, kTileM) ||
       !make_tmap_u8_2d(&t_w2, w2_q, H, static_cast<uint64_t>(E) * F, H, 128, 128) ||
@@ -1164,7 +1161,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   MxGemmArgs g = base;
   g.K = H;
   g.N = F;
-  g.bn = bn_dh;
+  g.bn = bnF;
   g.b_rows = F;
   g.sfb_rows = F;
   g.sfa = at<uint8_t>(ws, B.dos);
