@@ -371,6 +371,16 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       const MxTile tl = decode(t);
       const int64_t grow = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + row_in_tile;
       const int wrow0 = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + q * 32;   // warp's first row
+      if (kEpi == MxEpi::SwigluBwd) {
+        // while the tile's MMAs run, bring this row's A_g and A_u columns
+        // into L2, so that the epilogue reads them at L2 latency
+        const int64_t o = grow * p.N + tl.n * kTileN + half * (kTileN / 2);
+#pragma unroll
+        for (int b = 0; b < kTileN / 2; b += 64) {   // 128-byte lines of this warp's half
+          prefetch_l2(p.act_g + o + b);
+          prefetch_l2(p.act_u + o + b);
+        }
+      }
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         sm->abort = 1;
