@@ -665,8 +665,8 @@ __device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* 
 
 // Quantisation along the rows: four lanes per 32-element block, each with 8
 // consecutive elements (one 16-byte load, one 8-byte store), so a warp reads
-// 512 and writes 256 contiguous bytes; the block's amax is a max over the
-// four lanes. Scales row-major [rows, K/32], or (kTiled) in the tiled layout
+// 512 and writes 256 contiguous bytes per block group, with four such loads
+// in flight per lane; the block's amax is a max over the four lanes. Scales row-major [rows, K/32], or (kTiled) in the tiled layout
 // of the block-scaled MMA (rows % 128 == 0, K % 128 == 0); with row_end,
 // rows at or past *row_end are skipped (the unused tail of a padded layout).
 template <bool kTiled>
@@ -675,50 +675,57 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16
                                                              const int32_t* __restrict__ row_end,
                                                              uint8_t* __restrict__ q,
                                                              uint8_t* __restrict__ scales) {
+  constexpr int kU = 4;                    // items per lane per pass, loaded together
   const int nb = K >> 5;
   const int64_t limit = row_end ? static_cast<int64_t>(*row_end) * nb : blocks;
   const int64_t end = 4 * (limit < blocks ? limit : blocks);     // (block, quarter) items
   const int lane = lane_id();
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  // warp-uniform trip count: the shuffles below need every lane
-  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
-       base < end; base += step) {
-    const int64_t item = base + lane;
-    const bool live = item < end;
-    const int64_t b = item >> 2;
-    const int part = lane & 3;
-    float v[8];
-    if (live) {
-      const int4 raw = ld_stream(reinterpret_cast<const int4*>(in + b * 32 + part * 8));
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  // warp-uniform trip count: the shuffles below need every lane. A pass of
+  // a warp covers kU consecutive runs of 32 items.
+  for (int64_t base = (static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)) *
+                      (32 * kU);
+       base < end; base += warps * 32 * kU) {
+    int4 raw[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t item = base + 32 * u + lane;
+      raw[u] = item < end ? ld_stream(reinterpret_cast<const int4*>(in + (item >> 2) * 32 +
+                                                                    (lane & 3) * 8))
+                          : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t item = base + 32 * u + lane;
+      const int64_t b = item >> 2;
+      const int part = lane & 3;
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+      float v[8];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 f = __bfloat1622float2(h[j]);
         v[2 * j] = f.x;
         v[2 * j + 1] = f.y;
       }
-    } else {
+      float amax = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-    }
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const int sexp = mx_block_exp(amax);
-    const float inv = mx_inv_scale(sexp);
-    if (live) {
-      uint2 w;
-      w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
-      w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
-      *reinterpret_cast<uint2*>(q + b * 32 + part * 8) = w;
-      if (part == 0) {
-        const uint8_t sc = static_cast<uint8_t>(sexp + 127);
-        if (kTiled)
-          scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
-        else
-          scales[b] = sc;
+      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int sexp = mx_block_exp(amax);
+      const float inv = mx_inv_scale(sexp);
+      if (item < end) {
+        uint2 w;
+        w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
+        w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
+        *reinterpret_cast<uint2*>(q + b * 32 + part * 8) = w;
+        if (part == 0) {
+          const uint8_t sc = static_cast<uint8_t>(sexp + 127);
+          if (kTiled)
+            scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
+          else
+            scales[b] = sc;
+        }
       }
     }
   }
@@ -753,16 +760,19 @@ cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, i
 // and column c of in[z] [rows, cols], the 32-row blocks of that column become
 // 32 K-contiguous codes of q[z] [cols, rows] and one scale, row-major
 // [z, cols, rows/32] or (kTiled) tiled for an operand of batch * cols rows
-// and K = rows. A CTA stages a tile of 64 rows x 128 columns in shared memory
-// with 16-byte row loads, then each thread quantises one column's 32-row
-// block out of it and writes its 32 codes as two 16-byte stores. With
+// and K = rows. A CTA of 128 threads stages a tile of 32 rows x 128 columns
+// in shared memory with 16-byte row loads (all of a thread's loads in flight
+// at once), then each thread quantises one column's 32-row block out of it
+// and writes its 32 codes as two 16-byte stores. Small CTAs let 16 share an
+// SM, so some load while others compute. With
 // gather, row r of in is in[gather[r]] (a routed row of x), and a row whose
 // gather index is outside [0, src_rows) is zero (padding). With row_end, row
 // blocks at or past *row_end are skipped. cols % 8 == 0.
-constexpr int kColTileRows = 64, kColTileCols = 128;
+constexpr int kColTileRows = 32, kColTileCols = 128, kColThreads = 128;
+constexpr int kColRowsPerPass = kColThreads / 16;     // 16 threads load a 256-byte row
 
 template <bool kTiled>
-__global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16* __restrict__ in,
+__global__ void __launch_bounds__(kColThreads) quantize_cols_kernel(const __nv_bfloat16* __restrict__ in,
                                                             int64_t ld, int64_t batch_stride,
                                                             int rows, int cols,
                                                             const int32_t* __restrict__ gather,
@@ -777,10 +787,15 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
   const int c0 = blockIdx.y * kColTileCols;
   const int z = blockIdx.z;
   const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
-  // load: 16 threads per row (8 columns each), 16 rows per pass
+  // load: 16 threads per row (8 columns each); all of a thread's loads are
+  // in flight before any lands in shared memory
+  constexpr int kPasses = kColTileRows / kColRowsPerPass;
   const int lc = (threadIdx.x & 15) * 8;
-  for (int lr = threadIdx.x >> 4; lr < kColTileRows; lr += 16) {
-    int4 v = make_int4(0, 0, 0, 0);
+  int4 v4[kPasses];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {
+    const int lr = (threadIdx.x >> 4) + kColRowsPerPass * i;
+    v4[i] = make_int4(0, 0, 0, 0);
     if (lr < live_rows && c0 + lc < cols) {
       int64_t r = r0 + lr;
       bool ok = true;
@@ -788,14 +803,16 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
         r = __ldg(gather + r);
         ok = r >= 0 && r < src_rows;
       }
-      if (ok) v = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + lc));
+      if (ok) v4[i] = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + lc));
     }
-    *reinterpret_cast<int4*>(&tile[lr][lc]) = v;
   }
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i)
+    *reinterpret_cast<int4*>(&tile[(threadIdx.x >> 4) + kColRowsPerPass * i][lc]) = v4[i];
   __syncthreads();
   // quantise: thread (column c, 32-row block rb) of the tile
   const int c = threadIdx.x & (kColTileCols - 1);
-  const int rb = threadIdx.x >> 7;
+  const int rb = threadIdx.x / kColTileCols;     // 0: one 32-row block per tile
   if (rb * 32 >= live_rows || c0 + c >= cols) return;
   float v[32];
 #pragma unroll
@@ -819,7 +836,7 @@ __global__ void __launch_bounds__(256) quantize_cols_kernel(const __nv_bfloat16*
 // row-major [batch * rows, cols/32] or tiled (K = cols). The column part is
 // that of quantize_cols_kernel. No gather; rows % 32 == 0, cols % 128 == 0.
 template <bool kTiled>
-__global__ void __launch_bounds__(256) quantize_dual_kernel(const __nv_bfloat16* __restrict__ in,
+__global__ void __launch_bounds__(kColThreads) quantize_dual_kernel(const __nv_bfloat16* __restrict__ in,
                                                             int64_t ld, int64_t batch_stride,
                                                             int rows, int cols,
                                                             const int32_t* __restrict__ row_end,
@@ -834,13 +851,19 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(const __nv_bfloat16*
   const int c0 = blockIdx.y * kColTileCols;
   const int z = blockIdx.z;
   const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
+  constexpr int kPasses = kColTileRows / kColRowsPerPass;
   const int lc = (threadIdx.x & 15) * 8;
-  for (int lr = threadIdx.x >> 4; lr < kColTileRows; lr += 16) {
-    int4 v = make_int4(0, 0, 0, 0);
-    if (lr < live_rows)
-      v = ld_stream(reinterpret_cast<const int4*>(base + static_cast<int64_t>(r0 + lr) * ld + c0 + lc));
-    *reinterpret_cast<int4*>(&tile[lr][lc]) = v;
+  int4 v4[kPasses];
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i) {     // all loads in flight before the stores
+    const int lr = (threadIdx.x >> 4) + kColRowsPerPass * i;
+    v4[i] = lr < live_rows ? ld_stream(reinterpret_cast<const int4*>(
+                                 base + static_cast<int64_t>(r0 + lr) * ld + c0 + lc))
+                           : make_int4(0, 0, 0, 0);
   }
+#pragma unroll
+  for (int i = 0; i < kPasses; ++i)
+    *reinterpret_cast<int4*>(&tile[(threadIdx.x >> 4) + kColRowsPerPass * i][lc]) = v4[i];
   __syncthreads();
   // rows: item = (row, 32-column block, quarter); a warp covers two rows
   const int nbr = cols >> 5;
@@ -879,7 +902,7 @@ __global__ void __launch_bounds__(256) quantize_dual_kernel(const __nv_bfloat16*
   }
   // columns
   const int c = threadIdx.x & (kColTileCols - 1);
-  const int rb = threadIdx.x >> 7;
+  const int rb = threadIdx.x / kColTileCols;     // 0: one 32-row block per tile
   if (rb * 32 >= live_rows) return;
   float v[32];
 #pragma unroll
@@ -906,10 +929,10 @@ cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t ba
   const dim3 grid(static_cast<unsigned>((rows + kColTileRows - 1) / kColTileRows),
                   static_cast<unsigned>(cols / kColTileCols), static_cast<unsigned>(batch));
   if (tiled)
-    quantize_dual_kernel<true><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
+    quantize_dual_kernel<true><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
                                                      q_row, s_row, q_col, s_col);
   else
-    quantize_dual_kernel<false><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
+    quantize_dual_kernel<false><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
                                                       q_row, s_row, q_col, s_col);
   return cudaGetLastError();
 }
@@ -923,10 +946,10 @@ cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t ba
                   static_cast<unsigned>((cols + kColTileCols - 1) / kColTileCols),
                   static_cast<unsigned>(batch));
   if (tiled)
-    quantize_cols_kernel<true><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
+    quantize_cols_kernel<true><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
                                                      src_rows, row_end, q, scales);
   else
-    quantize_cols_kernel<false><<<grid, 256, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
+    quantize_cols_kernel<false><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
                                                       src_rows, row_end, q, scales);
   return cudaGetLastError();
 }
