@@ -12,15 +12,13 @@ namespace moe {
 // OR error bits into it; moe_get_error() reads and clears it.
 __device__ int g_error_word;
 
-namespace {
-
-constexpr int kMaxDevices = 64;
-
 int current_device() {
-  int d = 0;
-  cudaGetDevice(&d);
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
   return d;
 }
+
+namespace {
 
 int* error_word() {
   static int* ptrs[kMaxDevices] = {};
@@ -232,7 +230,6 @@ int keep(uint64_t bytes) { return bytes <= kKeepInL2Bytes ? 1 : 0; }
 // the first pipelined call and kept for the life of the process; a call
 // re-records them, which leaves the waits of an earlier call untouched.
 cudaEvent_t* pipeline_events() {
-  constexpr int kMaxDevices = 64;
   static thread_local cudaEvent_t pool[kMaxDevices][6];
   static thread_local bool made[kMaxDevices];
   int d = 0;

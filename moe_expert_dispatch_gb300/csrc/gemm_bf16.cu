@@ -548,13 +548,15 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   // always the 4-stage size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
   const size_t smem = gemm_smem_bytes(kMaxExperts);
-  static bool configured = false;
+  static bool configured[kMaxDevices] = {};    // the attribute is per device
   auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather, kBN>;
-  if (!configured) {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[d]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[d] = true;
   }
   kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
   return cudaGetLastError();

@@ -546,13 +546,15 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   static_assert(1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
                         sizeof(Smem) + (kMaxExperts + 1) * sizeof(int) <= 232448,
                 "shared memory of one CTA");
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevices] = {};    // the attribute is per device
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!configured[d]) {
     cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kEpi, kSched, kN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[d] = true;
   }
   mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(
       a, b0, b1, o.map[0], o.map[1], o.map[2], p);

@@ -262,5 +262,9 @@ cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const Gem
                           const MxGemmArgs& p, int grid, cudaStream_t st);
 
 int device_sm_count();
+// The current CUDA device, or -1; launchers keep per-device state indexed by
+// it (kernel attributes are per device).
+constexpr int kMaxDevices = 64;
+int current_device();
 
 }  // namespace moe

@@ -1029,12 +1029,14 @@ cudaError_t launch_gather_tile_scales(const uint8_t* xs_tok, const int32_t* toke
                                       const int32_t* off_al, const int32_t* counts, int E, int K,
                                       int64_t cap, uint8_t* xs_tiled, cudaStream_t st) {
   const int smem = (K >> 5) * kTileM;
-  static int configured = 0;
-  if (smem > 48 * 1024 && configured < smem) {
+  static int configured[kMaxDevices] = {};    // per device: the largest size set so far
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && configured[d] < smem) {
     cudaError_t e = cudaFuncSetAttribute(gather_tile_scales_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured[d] = smem;
   }
   gather_tile_scales_kernel<<<static_cast<unsigned>(cap / kTileM), kTileM, smem, st>>>(
       xs_tok, token_of, off_al, counts, E, K, xs_tiled);
@@ -1079,12 +1081,14 @@ cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t
                                cudaStream_t st) {
   if (out_rows == 0) return cudaSuccess;
   const int smem = (K >> 5) * kTileM;
-  static int configured = 0;
-  if (smem > 48 * 1024 && configured < smem) {
+  static int configured[kMaxDevices] = {};    // per device: the largest size set so far
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (smem > 48 * 1024 && configured[d] < smem) {
     cudaError_t e = cudaFuncSetAttribute(tile_scales_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    configured = smem;
+    configured[d] = smem;
   }
   tile_scales_kernel<<<static_cast<unsigned>(out_rows / kTileM), kTileM, smem, st>>>(
       src0, src1, rows_per_e, K, pair_half, dst);
