@@ -66,15 +66,153 @@ __global__ void __launch_bounds__(256) hist_kernel(const int32_t* __restrict__ i
     hist[static_cast<int64_t>(blockIdx.x) * E + e] = sh_count[e];
 }
 
-// Run by one CTA: per expert the total and each chunk's exclusive prefix;
-// then the dense offsets, the padded offsets and every chunk's first row.
-// hist is read through L2 (other CTAs of the same launch may have written it).
+// Exclusive prefix sums of v[0..n) (n <= 1024) in place, by warp 0 of the
+// CTA: lane l sums a segment of ceil(n / 32) entries, a warp scan offsets
+// the segments, then each lane writes its segment's prefixes. The total goes
+// to *total.
+__device__ void warp0_exclusive_scan(int* v, int n, int* total) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int seg = (n + 31) >> 5;
+  const int lo = min(n, lane * seg), hi = min(n, lo + seg);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += v[i];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  int run = incl - sum;
+  for (int i = lo; i < hi; ++i) {
+    const int x = v[i];
+    v[i] = run;
+    run += x;
+  }
+  if (lane == 31) *total = incl;
+}
+
+// Run by one CTA: per expert the total over the chunks, the dense and the
+// padded offsets, then every chunk's first row (its padded expert offset
+// plus the expert's ids in earlier chunks). hist is read through L2 (other
+// CTAs of the same launch may have written it), with 8 loads in flight per
+// expert, and is never read back after a write. Up to 32 experts one warp
+// does it all in registers; beyond, warp 0 scans in shared memory.
 __device__ void scan_chunks(const int32_t* hist, int32_t* base, int64_t chunks, int E, int align,
                             int32_t* counts, int32_t* offsets, int32_t* off_al, int* sh_cnt,
                             int* sh_al) {
   constexpr int U = 8;                     // independent loads in flight per expert
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  constexpr int kRegChunks = 32;           // one pass from registers up to this many chunks
+  __shared__ int total_dense, total_al;
+  if (E <= 32) {
+    // one warp, one expert per lane: totals, both scans by shuffles, bases
+    if (threadIdx.x >= 32) return;
+    const int e = threadIdx.x;
     int run = 0;
+    if (e < E) {
+      for (int64_t c0 = 0; c0 < chunks; c0 += U) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = c0 + u < chunks ? __ldcg(hist + (c0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) run += v[u];
+      }
+    }
+    const int al = (run + align - 1) / align * align;
+    int inc = run, inc_al = al;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, inc, o);
+      const int ta = __shfl_up_sync(0xffffffffu, inc_al, o);
+      if (e >= o) {
+        inc += t;
+        inc_al += ta;
+      }
+    }
+    if (e < E) {
+      if (counts) counts[e] = run;
+      if (offsets) offsets[e] = inc - run;
+      if (off_al) off_al[e] = inc_al - al;
+    }
+    if (e == 31) {
+      if (offsets) offsets[E] = inc;
+      if (off_al) off_al[E] = inc_al;
+    }
+    if (e < E) {
+      int b = inc_al - al;
+      for (int64_t c0 = 0; c0 < chunks; c0 += U) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = c0 + u < chunks ? __ldcg(hist + (c0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+          if (c0 + u < chunks) {
+            base[(c0 + u) * E + e] = b;
+            b += v[u];
+          }
+      }
+    }
+    return;
+  }
+  // with one expert per thread and few chunks, the chunk values stay in
+  // registers between the totals and the bases
+  const bool one_pass = chunks <= kRegChunks && E <= static_cast<int>(blockDim.x);
+  int keep[kRegChunks];
+  if (one_pass) {
+    const int e = threadIdx.x;
+    if (e < E) {
+      int run = 0;
+#pragma unroll
+      for (int u = 0; u < kRegChunks; ++u) {
+        keep[u] = u < chunks ? __ldcg(hist + static_cast<int64_t>(u) * E + e) : 0;
+        run += keep[u];
+      }
+      if (counts) counts[e] = run;
+      sh_cnt[e] = run;
+      sh_al[e] = (run + align - 1) / align * align;
+    }
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int64_t c0 = 0; c0 < chunks; c0 += U) {
+        int v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) v[u] = c0 + u < chunks ? __ldcg(hist + (c0 + u) * E + e) : 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) run += v[u];
+      }
+      if (counts) counts[e] = run;
+      sh_cnt[e] = run;
+      sh_al[e] = (run + align - 1) / align * align;
+    }
+  }
+  __syncthreads();
+  warp0_exclusive_scan(sh_al, E, &total_al);
+  if (offsets) warp0_exclusive_scan(sh_cnt, E, &total_dense);    // the same warp, in order
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    if (offsets) offsets[e] = sh_cnt[e];
+    if (off_al) off_al[e] = sh_al[e];
+  }
+  if (threadIdx.x == 0) {
+    if (offsets) offsets[E] = total_dense;
+    if (off_al) off_al[E] = total_al;
+  }
+  if (one_pass) {
+    const int e = threadIdx.x;
+    if (e < E) {
+      int run = sh_al[e];
+#pragma unroll
+      for (int u = 0; u < kRegChunks; ++u)
+        if (u < chunks) {
+          base[static_cast<int64_t>(u) * E + e] = run;
+          run += keep[u];
+        }
+    }
+    return;
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = sh_al[e];
     for (int64_t c0 = 0; c0 < chunks; c0 += U) {
       int v[U];
 #pragma unroll
@@ -86,25 +224,7 @@ __device__ void scan_chunks(const int32_t* hist, int32_t* base, int64_t chunks, 
           run += v[u];
         }
     }
-    sh_cnt[e] = run;
-    if (counts) counts[e] = run;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int o = 0, a = 0;
-    for (int e = 0; e < E; ++e) {
-      if (offsets) offsets[e] = o;
-      if (off_al) off_al[e] = a;
-      sh_al[e] = a;
-      o += sh_cnt[e];
-      a += (sh_cnt[e] + align - 1) / align * align;
-    }
-    if (offsets) offsets[E] = o;
-    if (off_al) off_al[E] = a;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    for (int64_t c = 0; c < chunks; ++c) base[c * E + e] += sh_al[e];
 }
 
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist,
