@@ -156,3 +156,38 @@ def test_dual_quantiser_equals_both_single_ones():
     rt = m.moe_quantize_mxfp8_t(dev(w))
     assert torch.equal(q, r[0]) and torch.equal(s, r[1])
     assert torch.equal(qt, rt[0]) and torch.equal(st, rt[1])
+
+
+@pytest.mark.parametrize("splits", [2, 4])
+def test_mxfp8_microbatch_split(splits):
+    """Micro-batches of the MXFP8 block: y, dX and dprobs are per-row
+    results (every row-quantised operand and every reduction is the row's
+    own), so they are bit-identical to the unsplit call. The weight
+    gradients' 32-row quantisation blocks depend on which rows a chunk gives
+    each expert: their sum over chunks must match the oracle's sum over the
+    same chunks (3e-2 of max), and stays within the quantisation-level
+    distance (0.15 of max, as the oracle's own pins) of the unsplit result."""
+    T = 512
+    c = _case(T, 256, 256, 6, 2, seed=40 + splits)
+    g0 = _gpu(c)
+    n = T // splits
+    acc, ref = None, None
+    for i in range(splits):
+        part = {key: (v[i * n:(i + 1) * n] if key in ("dy", "x", "ids", "probs") else v)
+                for key, v in c.items()}
+        gi = _gpu(part)
+        ri = _oracle(part)
+        for key in ("y", "dx", "dprobs"):
+            assert torch.equal(gi[key], g0[key][i * n:(i + 1) * n]), (key, i)
+        keys = ("dw_gate_t", "dw_up_t", "dw_down_t")
+        if acc is None:
+            acc = {key: gi[key].cpu().numpy().astype(np.float64) for key in keys}
+            ref = {key: ri[key] for key in keys}
+        else:
+            for key in keys:
+                acc[key] += gi[key].cpu().numpy()
+                ref[key] = ref[key] + ri[key]
+    for key in acc:
+        assert_rel_to_max(acc[key], ref[key], TOL, key + " vs the oracle per chunk")
+        assert_rel_to_max(acc[key], g0[key].cpu().numpy().astype(np.float64), 0.15,
+                          key + " vs unsplit")
