@@ -82,11 +82,17 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
     tl.kblocks = p.K / BK;
   } else {
     const int mt = p.M / kTileM;
-    const int per = mt * (p.N / p.bn);
+    const int nt = p.N / p.bn;
+    const int per = mt * nt;
     tl.e = t / per;
     const int local = t - tl.e * per;
-    tl.n = local / mt;
-    tl.m = local - tl.n * mt;
+    if (p.M > p.N) {          // A (M x K) is the larger operand: N fastest keeps B's panels in L2
+      tl.m = local / nt;
+      tl.n = local - tl.m * nt;
+    } else {                  // B is larger: M fastest keeps A's panels in L2
+      tl.n = local / mt;
+      tl.m = local - tl.n * mt;
+    }
     tl.row0 = p.off_al[tl.e];
     tl.kblocks = (p.off_al[tl.e + 1] - tl.row0) / BK;
   }

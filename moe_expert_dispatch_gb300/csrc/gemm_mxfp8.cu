@@ -23,8 +23,9 @@
 // registers.
 // Schedules: Rows (expert segments padded to 128 rows; M fastest within an
 // expert unless it has more M tiles than N tiles) and WGrad (K runs over one
-// expert's padded rows; every expert owns M/128 x N/bn output tiles, N
-// fastest, and an expert without rows writes zeros). CTA b takes tiles b,
+// expert's padded rows; every expert owns M/128 x N/bn output tiles, the
+// larger operand's dimension fastest, and an expert without rows writes
+// zeros). CTA b takes tiles b,
 // b + grid, ...
 #include "common.cuh"
 #include "internal.h"
@@ -167,8 +168,13 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       const int per = m_tiles_w * n_tiles;
       tl.e = t / per;
       const int local = t - tl.e * per;
-      tl.m = local / n_tiles;                 // N fastest: the expert's B panel stays in L2
-      tl.n = local - tl.m * n_tiles;
+      if (p.M > p.N) {        // A is the larger operand: N fastest keeps B's panels in L2
+        tl.m = local / n_tiles;
+        tl.n = local - tl.m * n_tiles;
+      } else {                // B is larger: M fastest keeps A's panels in L2
+        tl.n = local / m_tiles_w;
+        tl.m = local - tl.n * m_tiles_w;
+      }
       tl.k0 = p.off_al[tl.e];
       tl.kblocks = (p.off_al[tl.e + 1] - tl.k0) / BK;
       return tl;
