@@ -46,35 +46,41 @@ TRAFFIC = {
     # 620.8 MB algorithmic) scaled by the algorithmic bytes of the full launch
     # (2181 MB); profiles/grouped_gemm_mixtral_2experts_ncu_full.md
     ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2147e6, "sources": BF16_GEMM_SOURCES,
-                                     "src_sha": "b4a8346c82bb4f87"},
+                                     "src_sha": "91c600ebe389b783"},
     # fc1 on the skewed workload, captured at full size;
     # profiles/grouped_gemm_skewed_bf16_ncu_full.md
     ("skewed_bf16", "fc1_swiglu"): {"bytes": 1175.8e6, "sources": BF16_GEMM_SOURCES,
-                                    "src_sha": "b4a8346c82bb4f87"},
+                                    "src_sha": "91c600ebe389b783"},
     # MXFP8 fc1: the 16-expert capture (727.8 MB for 718.1 MB algorithmic)
     # scaled to the full launch (2871.9 MB); profiles/mx_gemm_mxfp8_16experts_ncu_full.md
     ("mxfp8", "fc1_swiglu"): {"bytes": 2911e6, "sources": MXFP8_GEMM_SOURCES,
-                              "src_sha": "8ad8c98ca2abe3e2"},
+                              "src_sha": "5b9517f870e3c9db"},
     # dW1 of the training step: the 2-expert capture (1165.3 MB for 1208.4 MB
     # algorithmic) scaled to the full launch (5905.5 MB);
     # profiles/grouped_gemm_backward_train_2experts_ncu_full.md
     ("train_bf16", "dW1"): {"bytes": 5695e6, "sources": BF16_GEMM_SOURCES,
-                            "src_sha": "b4a8346c82bb4f87"},
+                            "src_sha": "91c600ebe389b783"},
     # fc1 with its bf16 saves in the MXFP8 training step: the 2-expert capture
     # (629.1 MB for 672.3 MB algorithmic) scaled to the full launch (4410 MB);
     # profiles/mx_gemm_train_mxfp8_2experts_ncu_full.md
     ("train_mxfp8", "fc1_swiglu"): {"bytes": 4127e6, "sources": MXFP8_GEMM_SOURCES,
-                                    "src_sha": "8ad8c98ca2abe3e2"},
+                                    "src_sha": "5b9517f870e3c9db"},
 }
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
 
 def _sha_of_sources(files):
+    """Hash of the kernel sources' code: comments and whitespace are left
+    out, so that only a change to the code itself retires a capture."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

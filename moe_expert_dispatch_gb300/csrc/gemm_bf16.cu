@@ -22,9 +22,11 @@
 //  * WGrad (dW1, dW2): expert e owns (M/128) x (N/bn) tiles of its weight
 //    gradient and the reduction runs over its (zero-padded) rows.
 // Tiles of all experts are numbered consecutively and CTA b takes tiles b,
-// b + grid, ...; within an expert M runs fastest (CTAs that run at the same
-// time share one weight tile through L2) unless the expert has more M tiles
-// than N tiles, where N runs fastest so that its rows stay in L2 instead.
+// b + grid, ...; within an expert the dimension of the larger operand runs
+// fastest, so that the smaller operand's panels are the ones re-read from
+// L2: in Rows, M fastest (CTAs that run at the same time share one weight
+// tile) unless the expert has more M tiles than N tiles; in WGrad, N fastest
+// when M > N (dW2: the h panels stream once) and M fastest otherwise (dW1).
 // Experts without rows own no Rows tile. Counts never leave the device.
 #include "common.cuh"
 #include "internal.h"
