@@ -396,43 +396,54 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
       if (kFc1) {
-        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F; the codes are
-        // held in registers and stored after the accumulator is released.
-        // The tile's N/64 scale bytes of this row are adjacent in the tiled
-        // layout (one 128-wide K group of fc2): they leave in one store.
-        // With save, A_g, A_u and h leave as bf16 pieces. This warp's half
-        // of the tile's h columns: kTileN / 4.
+        // h = bf16(silu(gate) * up), then MXFP8 per 32 along F. h is held
+        // packed in bf16 (it is bf16-valued, so nothing is lost) and the
+        // accumulator is released before the quantisation and the stores,
+        // which then overlap the next tile's MMAs. The tile's N/64 scale
+        // bytes of this row are adjacent in the tiled layout (one 128-wide K
+        // group of fc2): they leave in one store. With save, A_g, A_u and h
+        // leave as bf16 pieces. This warp's half of the tile's h columns:
+        // kTileN / 4.
         constexpr int kHalf = kTileN / 4;
         const int c0 = half * kHalf;
         const int col = tl.n * n_cols + c0;
-        uint32_t codes[kHalf / 4];
-        uint32_t packed = 0;
+        uint32_t hw[kHalf / 2];
 #pragma unroll
         for (int c = 0; c < kHalf; c += 32) {
           uint32_t g[32], u[32];
           tmem_ld_32x32b_x32(taddr + c0 + c, g);
           tmem_ld_32x32b_x32(taddr + kTileN / 2 + c0 + c, u);
           tmem_ld_wait();
-          float hv[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            hv[i] = __bfloat162float(__float2bfloat16_rn(silu_f(__uint_as_float(g[i])) *
-                                                         __uint_as_float(u[i])));
+          for (int i = 0; i < 16; ++i)
+            hw[c / 2 + i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
+                                        silu_f(__uint_as_float(g[2 * i + 1])) *
+                                            __uint_as_float(u[2 * i + 1]));
           if (p.save) {
             uint32_t w[16];
             bf16_words(g, w);
             put_piece(w, &tmO0, col + c, wrow0, false);
             bf16_words(u, w);
             put_piece(w, &tmO1, col + c, wrow0, false);
+            put_piece(&hw[c / 2], &tmO2, col + c, wrow0, false);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        uint32_t codes[kHalf / 4];
+        uint32_t packed = 0;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-            put_piece(w, &tmO2, col + c, wrow0, false);
+        for (int c = 0; c < kHalf; c += 32) {
+          float hv[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[c / 2 + i]));
+            hv[2 * i] = f.x;
+            hv[2 * i + 1] = f.y;
           }
           const uint8_t sc = quantize_block32(hv, &codes[c / 4]);
           packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
         int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);
 #pragma unroll
         for (int i = 0; i < kHalf / 16; ++i)
