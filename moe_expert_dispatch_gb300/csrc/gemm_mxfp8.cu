@@ -454,17 +454,21 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         else
           *hs = static_cast<uint8_t>(packed);
       } else if (kEpi == MxEpi::Bf16) {
-        // O = bf16, 32 columns per piece
-#pragma unroll 1
+        // O = bf16: the row is packed into registers and the accumulator
+        // released before its pieces (32 columns each) go out
+        uint32_t w[kTileN / 2];
+#pragma unroll
         for (int c = 0; c < kTileN; c += 32) {
-          uint32_t r[32], w[16];
+          uint32_t r[32];
           tmem_ld_32x32b_x32(taddr + c, r);
           tmem_ld_wait();
-          bf16_words(r, w);
-          put_piece(w, &tmO0, tl.n * kTileN + c, wrow0, false);
+          bf16_words(r, &w[c / 2]);
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
+#pragma unroll
+        for (int c = 0; c < kTileN; c += 32)
+          put_piece(&w[c / 2], &tmO0, tl.n * kTileN + c, wrow0, false);
       } else if (kEpi == MxEpi::SwigluBwd) {
         // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s),
         // s = sigmoid(A_g), over this warp's half of the tile's columns; dA_g
