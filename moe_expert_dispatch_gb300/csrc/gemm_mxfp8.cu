@@ -39,12 +39,13 @@ constexpr int BK = 128;                    // E4M3 elements (bytes) per k-block
 constexpr int kABytes = kTileM * BK;       // 16 KB
 constexpr int kSfBytes = 512;              // one scale atom (128 rows x 4 blocks of 32)
 // warp 0 producer, warp 1 MMA issuer, then the epilogue warps. The fc1 and
-// dH epilogues (SwiGLU forward + quantisation, SwiGLU backward) are heavy:
-// 8 warps, two per TMEM lane quadrant, each finishing half of the tile's
-// columns, halve their exposed part. The fc2 and float epilogues are light:
-// 4 warps (more only take issue slots from the producer and MMA threads).
+// dH epilogues (SwiGLU forward + quantisation, SwiGLU backward) are heavy,
+// and a float row of 256 columns does not fit one thread's registers: 8
+// warps, two per TMEM lane quadrant, each finishing half of the tile's
+// columns. fc2's bf16 row fits one thread: 4 warps (more only take issue
+// slots from the producer and MMA threads).
 template <MxEpi kEpi>
-constexpr int epi_warps() { return (kEpi == MxEpi::Fc1 || kEpi == MxEpi::SwigluBwd) ? 8 : 4; }
+constexpr int epi_warps() { return kEpi == MxEpi::Bf16 ? 4 : 8; }
 template <MxEpi kEpi>
 constexpr int num_threads() { return 64 + 32 * epi_warps<kEpi>(); }
 constexpr uint32_t kTmemCols = 512;
@@ -524,23 +525,26 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         }
         const bool empty = tl.kblocks == 0;     // WGrad: an expert without rows
         const bool add = kWGrad && p.accumulate != 0;
-        if (!(empty && add)) {
-#pragma unroll 1
-          for (int c = 0; c < kTileN; c += 32) {
-            uint32_t r[32];
-            if (!empty) {
-              tmem_ld_32x32b_x32(taddr + c, r);
-              tmem_ld_wait();
-            } else {
+        // this warp's half of the row, in registers, so that the
+        // accumulator is released before the pieces go out
+        constexpr int kCols = kTileN / 2;
+        const int cbase = half * kCols;
+        uint32_t v[kCols];
+        if (!empty) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) r[i] = 0u;
-            }
-            put_piece(r, map, tl.n * kTileN + c, y, add);
-            put_piece(r + 16, map, tl.n * kTileN + c + 16, y, add);
-          }
+          for (int c = 0; c < kCols; c += 32) tmem_ld_32x32b_x32(taddr + cbase + c, &v[c]);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < kCols; ++i) v[i] = 0u;
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
+        if (!(empty && add)) {
+#pragma unroll
+          for (int c = 0; c < kCols; c += 16)
+            put_piece(&v[c], map, tl.n * kTileN + cbase + c, y, add);
+        }
       }
       if (++acc == G::kAccBufs) {
         acc = 0;
