@@ -876,168 +876,194 @@ cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, i
   return cudaGetLastError();
 }
 
-// Quantisation along the rows (the transposed orientation): for each batch z
-// and column c of in[z] [rows, cols], the 32-row blocks of that column become
-// 32 K-contiguous codes of q[z] [cols, rows] and one scale, row-major
+// Quantisation along the rows (the transposed orientation), alone or with
+// the row orientation from the same read. For each batch z and column c of
+// in[z] [rows, cols], the 32-row blocks of that column become 32
+// K-contiguous codes of q_col[z] [cols, rows] and one scale, row-major
 // [z, cols, rows/32] or (kTiled) tiled for an operand of batch * cols rows
-// and K = rows. A CTA of 128 threads stages a tile of 32 rows x 128 columns
-// in shared memory with 16-byte row loads (all of a thread's loads in flight
-// at once), then each thread quantises one column's 32-row block out of it
-// and writes its 32 codes as two 16-byte stores. Small CTAs let 16 share an
-// SM, so some load while others compute. With
-// gather, row r of in is in[gather[r]] (a routed row of x), and a row whose
-// gather index is outside [0, src_rows) is zero (padding). With row_end, row
-// blocks at or past *row_end are skipped. cols % 8 == 0.
-constexpr int kColTileRows = 32, kColTileCols = 128, kColThreads = 128;
-constexpr int kColRowsPerPass = kColThreads / 16;     // 16 threads load a 256-byte row
+// and K = rows. With kDual, the rows' 32-column blocks also become q_row
+// [batch * rows, cols] with scales row-major [batch * rows, cols/32] or tiled
+// (K = cols), by the rule of quantize_mxfp8_kernel.
+//
+// A CTA of 256 threads takes a tile of 128 rows x 128 columns. Its loads
+// are coalesced 256-byte row pieces, all eight of a thread in flight at
+// once, staged in shared memory with 16-byte chunk j of row r at j ^ (r & 7)
+// so that every access pattern below is free of bank conflicts. Along the
+// rows (kDual) each lane quantises a whole 32-column block (one scale per
+// lane, no shuffles) and writes its 32 codes. Down the columns, each thread
+// quantises two 32-row blocks of one column; the codes gather in shared
+// memory, a column's 128 codes in one 128-byte row, and leave as whole
+// lines, so that the column codes, which land 32 bytes per output row per
+// row block, reach L2 as full-line writes. With gather, row r of in is
+// in[gather[r]] (a routed row of x), and a row whose gather index is outside
+// [0, src_rows) is zero (padding). With row_end, rows at or past *row_end
+// are skipped in whole 32-row blocks; the rest of a live block is zero.
+// rows % 32 == 0; cols % 8 == 0 (kDual: cols % 128 == 0); kTiled: rows and
+// cols % 128 == 0.
+constexpr int kQtRows = 128, kQtCols = 128, kQtThreads = 256;
 
-template <bool kTiled>
-__global__ void __launch_bounds__(kColThreads) quantize_cols_kernel(const __nv_bfloat16* __restrict__ in,
-                                                            int64_t ld, int64_t batch_stride,
-                                                            int rows, int cols,
-                                                            const int32_t* __restrict__ gather,
-                                                            int64_t src_rows,
-                                                            const int32_t* __restrict__ row_end,
-                                                            uint8_t* __restrict__ q,
-                                                            uint8_t* __restrict__ scales) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kColTileRows][kColTileCols];
-  const int r0 = blockIdx.x * kColTileRows;
-  const int live_rows = min(kColTileRows, (row_end ? min(rows, *row_end) : rows) - r0);
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ float absmax8(const float* v) {
+  return fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
+               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+}
+
+template <bool kTiled, bool kDual>
+__global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
+    const __nv_bfloat16* __restrict__ in, int64_t ld, int64_t batch_stride, int rows, int cols,
+    const int32_t* __restrict__ gather, int64_t src_rows, const int32_t* __restrict__ row_end,
+    uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
+    uint8_t* __restrict__ s_col) {
+  __shared__ __align__(16) uint8_t tile[kQtRows][kQtCols * 2];     // bf16, chunk-swizzled
+  __shared__ __align__(16) uint8_t codes[kQtCols][kQtRows];        // column codes, swizzled
+  const int r0 = blockIdx.x * kQtRows, c0 = blockIdx.y * kQtCols, z = blockIdx.z;
+  const int live_rows = min(kQtRows, (row_end ? min(rows, *row_end) : rows) - r0);
   if (live_rows <= 0) return;
-  const int c0 = blockIdx.y * kColTileCols;
-  const int z = blockIdx.z;
+  const int n_rb = (live_rows + 31) >> 5;
   const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
-  // load: 16 threads per row (8 columns each); all of a thread's loads are
-  // in flight before any lands in shared memory
-  constexpr int kPasses = kColTileRows / kColRowsPerPass;
-  const int lc = (threadIdx.x & 15) * 8;
-  int4 v4[kPasses];
+  const int tid = threadIdx.x;
+  const int ch = tid & 15;                     // this thread's 8-column chunk of a row
+  const bool ch_ok = c0 + ch * 8 < cols;
+  int4 v4[kQtRows / 16];
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i) {
-    const int lr = (threadIdx.x >> 4) + kColRowsPerPass * i;
+  for (int i = 0; i < kQtRows / 16; ++i) {
+    const int lr = (tid >> 4) + 16 * i;
     v4[i] = make_int4(0, 0, 0, 0);
-    if (lr < live_rows && c0 + lc < cols) {
+    if (lr < live_rows && ch_ok) {
       int64_t r = r0 + lr;
       bool ok = true;
       if (gather) {
         r = __ldg(gather + r);
         ok = r >= 0 && r < src_rows;
       }
-      if (ok) v4[i] = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + lc));
+      if (ok) v4[i] = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + ch * 8));
     }
   }
 #pragma unroll
-  for (int i = 0; i < kPasses; ++i)
-    *reinterpret_cast<int4*>(&tile[(threadIdx.x >> 4) + kColRowsPerPass * i][lc]) = v4[i];
-  __syncthreads();
-  // quantise: thread (column c, 32-row block rb) of the tile
-  const int c = threadIdx.x & (kColTileCols - 1);
-  const int rb = threadIdx.x / kColTileCols;     // 0: one 32-row block per tile
-  if (rb * 32 >= live_rows || c0 + c >= cols) return;
-  float v[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[rb * 32 + i][c]);
-  uint32_t w[8];
-  const uint8_t sc = quantize_block32(v, w);
-  const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
-  const int64_t kb = (r0 >> 5) + rb;
-  int4* dst = reinterpret_cast<int4*>(q + orow * rows + kb * 32);
-  dst[0] = make_int4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_int4(w[4], w[5], w[6], w[7]);
-  if (kTiled)
-    scales[mx_scale_offset(orow, kb, rows)] = sc;
-  else
-    scales[orow * (rows >> 5) + kb] = sc;
-}
-
-// Both orientations from one read: the tile of quantize_cols_kernel also
-// gives its rows' 32-column blocks (four lanes per block, as in
-// quantize_mxfp8_kernel), written to q_row [batch * rows, cols] with scales
-// row-major [batch * rows, cols/32] or tiled (K = cols). The column part is
-// that of quantize_cols_kernel. No gather; rows % 32 == 0, cols % 128 == 0.
-template <bool kTiled>
-__global__ void __launch_bounds__(kColThreads) quantize_dual_kernel(const __nv_bfloat16* __restrict__ in,
-                                                            int64_t ld, int64_t batch_stride,
-                                                            int rows, int cols,
-                                                            const int32_t* __restrict__ row_end,
-                                                            uint8_t* __restrict__ q_row,
-                                                            uint8_t* __restrict__ s_row,
-                                                            uint8_t* __restrict__ q_col,
-                                                            uint8_t* __restrict__ s_col) {
-  __shared__ __align__(16) __nv_bfloat16 tile[kColTileRows][kColTileCols];
-  const int r0 = blockIdx.x * kColTileRows;
-  const int live_rows = min(kColTileRows, (row_end ? min(rows, *row_end) : rows) - r0);
-  if (live_rows <= 0) return;
-  const int c0 = blockIdx.y * kColTileCols;
-  const int z = blockIdx.z;
-  const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
-  constexpr int kPasses = kColTileRows / kColRowsPerPass;
-  const int lc = (threadIdx.x & 15) * 8;
-  int4 v4[kPasses];
-#pragma unroll
-  for (int i = 0; i < kPasses; ++i) {     // all loads in flight before the stores
-    const int lr = (threadIdx.x >> 4) + kColRowsPerPass * i;
-    v4[i] = lr < live_rows ? ld_stream(reinterpret_cast<const int4*>(
-                                 base + static_cast<int64_t>(r0 + lr) * ld + c0 + lc))
-                           : make_int4(0, 0, 0, 0);
+  for (int i = 0; i < kQtRows / 16; ++i) {
+    const int lr = (tid >> 4) + 16 * i;
+    *reinterpret_cast<int4*>(&tile[lr][(ch ^ (lr & 7)) << 4]) = v4[i];
   }
-#pragma unroll
-  for (int i = 0; i < kPasses; ++i)
-    *reinterpret_cast<int4*>(&tile[(threadIdx.x >> 4) + kColRowsPerPass * i][lc]) = v4[i];
   __syncthreads();
-  // rows: item = (row, 32-column block, quarter); a warp covers two rows
-  const int nbr = cols >> 5;
-  for (int it = threadIdx.x; it < kColTileRows * (kColTileCols / 8); it += blockDim.x) {
-    const int row = it >> 4, blk = (it >> 2) & 3, part = it & 3;
-    const int4 raw = *reinterpret_cast<const int4*>(&tile[row][blk * 32 + part * 8]);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    float v[8];
+  if (kDual) {
+#pragma unroll 1
+    for (int k = 0; k < 2; ++k) {
+      const int r = (tid >> 2) + 64 * k, b = tid & 3;     // row, 32-column block
+      if (r >= live_rows) break;
+      uint32_t w[16];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(h[j]);
-      v[2 * j] = f.x;
-      v[2 * j + 1] = f.y;
-    }
-    float amax = 0.0f;
+      for (int j = 0; j < 4; ++j) {
+        const uint4 q = *reinterpret_cast<const uint4*>(&tile[r][((4 * b + j) ^ (r & 7)) << 4]);
+        w[4 * j] = q.x;
+        w[4 * j + 1] = q.y;
+        w[4 * j + 2] = q.z;
+        w[4 * j + 3] = q.w;
+      }
+      float m[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    if (row >= live_rows) continue;      // whole warps: live_rows is a multiple of 32
-    const int sexp = mx_block_exp(amax);
-    const float inv = mx_inv_scale(sexp);
-    const int64_t grow = static_cast<int64_t>(z) * rows + r0 + row;
-    uint2 w;
-    w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
-    w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
-    *reinterpret_cast<uint2*>(q_row + grow * cols + c0 + blk * 32 + part * 8) = w;
-    if (part == 0) {
-      const int kb = (c0 >> 5) + blk;
+      for (int j = 0; j < 8; ++j)
+        m[j] = fmaxf(fmaxf(fabsf(bf16_lo(w[2 * j])), fabsf(bf16_hi(w[2 * j]))),
+                     fmaxf(fabsf(bf16_lo(w[2 * j + 1])), fabsf(bf16_hi(w[2 * j + 1]))));
+      const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
+                               fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+      const int sexp = mx_block_exp(amax);
+      const float inv = mx_inv_scale(sexp);
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        o[j] = mx_encode4(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]),
+                          bf16_hi(w[2 * j + 1]), inv);
+      const int64_t grow = static_cast<int64_t>(z) * rows + r0 + r;
+      int4* dst = reinterpret_cast<int4*>(q_row + grow * cols + c0 + b * 32);
+      dst[0] = make_int4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_int4(o[4], o[5], o[6], o[7]);
+      const int kb = (c0 >> 5) + b;
       const uint8_t sc = static_cast<uint8_t>(sexp + 127);
       if (kTiled)
         s_row[mx_scale_offset(grow, kb, cols)] = sc;
       else
-        s_row[grow * nbr + kb] = sc;
+        s_row[grow * (cols >> 5) + kb] = sc;
     }
   }
-  // columns
-  const int c = threadIdx.x & (kColTileCols - 1);
-  const int rb = threadIdx.x / kColTileCols;     // 0: one 32-row block per tile
-  if (rb * 32 >= live_rows) return;
-  float v[32];
+  // columns: thread (column c, row blocks 2p and 2p + 1)
+  const int c = tid & (kQtCols - 1), p = tid >> 7;
+  const bool col_ok = c0 + c < cols;
+  uint32_t sc2 = 0;
+  if (col_ok) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(tile[rb * 32 + i][c]);
-  uint32_t w[8];
-  const uint8_t sc = quantize_block32(v, w);
-  const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
-  const int64_t kb = (r0 >> 5) + rb;
-  int4* dst = reinterpret_cast<int4*>(q_col + orow * rows + kb * 32);
-  dst[0] = make_int4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_int4(w[4], w[5], w[6], w[7]);
-  if (kTiled)
-    s_col[mx_scale_offset(orow, kb, rows)] = sc;
+    for (int h = 0; h < 2; ++h) {
+      const int rb = 2 * p + h;
+      if (rb < n_rb) {
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int rr = rb * 32 + i;
+          v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+              &tile[rr][(((c >> 3) ^ (rr & 7)) << 4) + (c & 7) * 2]));
+        }
+        const float amax = fmaxf(fmaxf(absmax8(v), absmax8(v + 8)),
+                                 fmaxf(absmax8(v + 16), absmax8(v + 24)));
+        const int sexp = mx_block_exp(amax);
+        const float inv = mx_inv_scale(sexp);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = mx_encode4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+        *reinterpret_cast<int4*>(&codes[c][((2 * rb) ^ (c & 7)) << 4]) =
+            make_int4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<int4*>(&codes[c][((2 * rb + 1) ^ (c & 7)) << 4]) =
+            make_int4(w[4], w[5], w[6], w[7]);
+        sc2 |= static_cast<uint32_t>(sexp + 127) << (8 * h);
+      }
+    }
+    const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int rb = 2 * p + h;
+      if (rb < n_rb) {
+        const int64_t kb = (r0 >> 5) + rb;
+        const uint8_t sc = static_cast<uint8_t>(sc2 >> (8 * h));
+        if (kTiled)
+          s_col[mx_scale_offset(orow, kb, rows)] = sc;
+        else
+          s_col[orow * (rows >> 5) + kb] = sc;
+      }
+    }
+  }
+  __syncthreads();
+  // the column codes leave as whole rows of q_col: 8 lanes per 128-byte line
+#pragma unroll
+  for (int k = 0; k < (kQtCols * kQtRows / 16) / kQtThreads; ++k) {
+    const int e = tid + kQtThreads * k;
+    const int row = e >> 3, cc = e & 7;
+    if ((cc >> 1) < n_rb && c0 + row < cols) {
+      const int4 val = *reinterpret_cast<const int4*>(&codes[row][(cc ^ (row & 7)) << 4]);
+      *reinterpret_cast<int4*>(q_col + (static_cast<int64_t>(z) * cols + c0 + row) * rows + r0 +
+                               cc * 16) = val;
+    }
+  }
+}
+
+template <bool kDual>
+static cudaError_t launch_quantize_tiles(const __nv_bfloat16* in, int64_t ld, int64_t batch,
+                                         int64_t batch_stride, int rows, int cols,
+                                         const int32_t* gather, int64_t src_rows,
+                                         const int32_t* row_end, bool tiled, uint8_t* q_row,
+                                         uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
+                                         cudaStream_t st) {
+  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>((rows + kQtRows - 1) / kQtRows),
+                  static_cast<unsigned>((cols + kQtCols - 1) / kQtCols),
+                  static_cast<unsigned>(batch));
+  if (tiled)
+    quantize_tile_kernel<true, kDual><<<grid, kQtThreads, 0, st>>>(
+        in, ld, batch_stride, rows, cols, gather, src_rows, row_end, q_row, s_row, q_col, s_col);
   else
-    s_col[orow * (rows >> 5) + kb] = sc;
+    quantize_tile_kernel<false, kDual><<<grid, kQtThreads, 0, st>>>(
+        in, ld, batch_stride, rows, cols, gather, src_rows, row_end, q_row, s_row, q_col, s_col);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t batch,
@@ -1045,33 +1071,16 @@ cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t ba
                                  const int32_t* row_end, bool tiled, uint8_t* q_row,
                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                  cudaStream_t st) {
-  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((rows + kColTileRows - 1) / kColTileRows),
-                  static_cast<unsigned>(cols / kColTileCols), static_cast<unsigned>(batch));
-  if (tiled)
-    quantize_dual_kernel<true><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
-                                                     q_row, s_row, q_col, s_col);
-  else
-    quantize_dual_kernel<false><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, row_end,
-                                                      q_row, s_row, q_col, s_col);
-  return cudaGetLastError();
+  return launch_quantize_tiles<true>(in, ld, batch, batch_stride, rows, cols, nullptr, 0, row_end,
+                                     tiled, q_row, s_row, q_col, s_col, st);
 }
 
 cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
                                  int64_t batch_stride, int rows, int cols, const int32_t* gather,
                                  int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
                                  uint8_t* scales, cudaStream_t st) {
-  if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>((rows + kColTileRows - 1) / kColTileRows),
-                  static_cast<unsigned>((cols + kColTileCols - 1) / kColTileCols),
-                  static_cast<unsigned>(batch));
-  if (tiled)
-    quantize_cols_kernel<true><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
-                                                     src_rows, row_end, q, scales);
-  else
-    quantize_cols_kernel<false><<<grid, kColThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather,
-                                                      src_rows, row_end, q, scales);
-  return cudaGetLastError();
+  return launch_quantize_tiles<false>(in, ld, batch, batch_stride, rows, cols, gather, src_rows,
+                                      row_end, tiled, nullptr, nullptr, q, scales, st);
 }
 
 // The dispatch of the MXFP8 path: one warp per token reads the bf16 row once,

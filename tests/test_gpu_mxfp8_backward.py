@@ -53,11 +53,15 @@ def _oracle(c):
 KEYS = ("dx", "dw_gate_t", "dw_up_t", "dw_down_t", "dprobs", "y")
 
 
-def test_transposed_quantiser_bit_exact():
+@pytest.mark.parametrize("shape", [(3, 96, 256), (2, 64, 264), (1, 32, 8), (2, 128, 392)])
+def test_transposed_quantiser_bit_exact(shape):
+    """Column tiles of 256 with ragged last tiles (264, 392: one or a few
+    8-column chunks past the last full tile; 8: a single chunk)."""
     g = torch.Generator().manual_seed(1)
-    w = (torch.randn((3, 96, 256), generator=g) * torch.logspace(-3, 2, 256)).to(torch.bfloat16)
+    B, R, C = shape
+    w = (torch.randn(shape, generator=g) * torch.logspace(-3, 2, C)).to(torch.bfloat16)
     q, s = m.moe_quantize_mxfp8_t(dev(w))
-    for z in range(3):
+    for z in range(B):
         rq, rs = orc.quantize_mxfp8(to_np(w[z]).T)
         assert np.array_equal(q[z].cpu().numpy(), rq)
         assert np.array_equal(s[z].cpu().numpy(), rs)
@@ -148,14 +152,20 @@ def test_mxfp8_backward_training_workload_sampled():
                 assert abs(got - ref[i, j]) <= bound, (key, e, f, h, got, ref[i, j], bound)
 
 
-def test_dual_quantiser_equals_both_single_ones():
+@pytest.mark.parametrize("shape", [(2, 160, 384), (1, 32, 128), (3, 64, 512)])
+def test_dual_quantiser_equals_both_single_ones(shape):
     g = torch.Generator().manual_seed(2)
-    w = (torch.randn((2, 160, 384), generator=g) * torch.logspace(-2, 2, 384)).to(torch.bfloat16)
+    w = (torch.randn(shape, generator=g) * torch.logspace(-2, 2, shape[2])).to(torch.bfloat16)
     q, s, qt, st = m.moe_quantize_mxfp8_dual(dev(w))
     r = m.moe_quantize_mxfp8(dev(w))
     rt = m.moe_quantize_mxfp8_t(dev(w))
     assert torch.equal(q, r[0]) and torch.equal(s, r[1])
     assert torch.equal(qt, rt[0]) and torch.equal(st, rt[1])
+    for z in range(shape[0]):           # and both against the oracle's rule
+        rq, rs = orc.quantize_mxfp8(to_np(w[z]))
+        assert np.array_equal(q[z].cpu().numpy(), rq) and np.array_equal(s[z].cpu().numpy(), rs)
+        rq, rs = orc.quantize_mxfp8(to_np(w[z]).T)
+        assert np.array_equal(qt[z].cpu().numpy(), rq) and np.array_equal(st[z].cpu().numpy(), rs)
 
 
 @pytest.mark.parametrize("splits", [2, 4])
