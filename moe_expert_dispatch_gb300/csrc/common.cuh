@@ -234,24 +234,6 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// ------------------------------------------------------------------ cp.async (LDGSTS)
-
-// 16 bytes global -> shared, bypassing L1; src_bytes = 0 fills the 16 bytes
-// with zeros and reads nothing.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// this thread's copies: all but the newest N groups have landed
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ------------------------------------------------------------------ block-scaled (MXFP8)
 
 // Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0).

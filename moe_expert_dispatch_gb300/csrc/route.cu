@@ -887,8 +887,8 @@ cudaError_t launch_quantize_mxfp8_tiled(const __nv_bfloat16* in, int64_t rows, i
 //
 // A CTA of 256 threads takes a tile of 128 rows x 128 columns. Its loads
 // are coalesced 256-byte row pieces, all eight of a thread in flight at
-// once, staged in shared memory with 16-byte chunk j of row r at j ^ (r & 7)
-// so that every access pattern below is free of bank conflicts. Along the
+// once, staged in shared memory in swizzled 16-byte chunks so that every
+// access pattern below is free of bank conflicts. Along the
 // rows (kDual) each lane quantises a whole 32-column block (one scale per
 // lane, no shuffles) and writes its 32 codes. Down the columns, each thread
 // quantises two 32-row blocks of one column; the codes gather in shared
@@ -905,17 +905,22 @@ constexpr int kQtRows = 128, kQtCols = 128, kQtThreads = 256;
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// 16-byte chunk j of staged row r sits at chunk j ^ qt_swizzle(r): eight
+// consecutive rows, or rows 64 apart, never share a bank group
+__device__ __forceinline__ int qt_swizzle(int r) { return (r & 7) ^ ((r >> 4) & 4); }
+
 __device__ __forceinline__ float absmax8(const float* v) {
   return fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
                fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
 }
 
-template <bool kTiled, bool kDual>
+template <bool kTiled, bool kDual, bool kGather>
 __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
     const __nv_bfloat16* __restrict__ in, int64_t ld, int64_t batch_stride, int rows, int cols,
     const int32_t* __restrict__ gather, int64_t src_rows, const int32_t* __restrict__ row_end,
     uint8_t* __restrict__ q_row, uint8_t* __restrict__ s_row, uint8_t* __restrict__ q_col,
     uint8_t* __restrict__ s_col) {
+  // 48 KB in all, so that four CTAs share an SM
   __shared__ __align__(16) uint8_t tile[kQtRows][kQtCols * 2];     // bf16, chunk-swizzled
   __shared__ __align__(16) uint8_t codes[kQtCols][kQtRows];        // column codes, swizzled
   const int r0 = blockIdx.x * kQtRows, c0 = blockIdx.y * kQtCols, z = blockIdx.z;
@@ -930,21 +935,19 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
 #pragma unroll
   for (int i = 0; i < kQtRows / 16; ++i) {
     const int lr = (tid >> 4) + 16 * i;
-    v4[i] = make_int4(0, 0, 0, 0);
-    if (lr < live_rows && ch_ok) {
-      int64_t r = r0 + lr;
-      bool ok = true;
-      if (gather) {
-        r = __ldg(gather + r);
-        ok = r >= 0 && r < src_rows;
-      }
-      if (ok) v4[i] = ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + ch * 8));
+    int64_t r = r0 + lr;
+    bool ok = lr < live_rows && ch_ok;
+    if (kGather && ok) {
+      r = __ldg(gather + r);
+      ok = r >= 0 && r < src_rows;
     }
+    v4[i] = ok ? ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + ch * 8))
+               : make_int4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int i = 0; i < kQtRows / 16; ++i) {
     const int lr = (tid >> 4) + 16 * i;
-    *reinterpret_cast<int4*>(&tile[lr][(ch ^ (lr & 7)) << 4]) = v4[i];
+    *reinterpret_cast<int4*>(&tile[lr][(ch ^ qt_swizzle(lr)) << 4]) = v4[i];
   }
   __syncthreads();
   if (kDual) {
@@ -955,7 +958,7 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
       uint32_t w[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint4 q = *reinterpret_cast<const uint4*>(&tile[r][((4 * b + j) ^ (r & 7)) << 4]);
+        const uint4 q = *reinterpret_cast<const uint4*>(&tile[r][((4 * b + j) ^ qt_swizzle(r)) << 4]);
         w[4 * j] = q.x;
         w[4 * j + 1] = q.y;
         w[4 * j + 2] = q.z;
@@ -987,8 +990,11 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
         s_row[grow * (cols >> 5) + kb] = sc;
     }
   }
-  // columns: thread (column c, row blocks 2p and 2p + 1)
-  const int c = tid & (kQtCols - 1), p = tid >> 7;
+  // columns: lane l of warp w takes column c = 16 w + (l & 15) and its row
+  // blocks 2p, 2p + 1, p = l >> 4, so that a column's four scales meet in one
+  // warp (the swizzle keeps the halves, 64 rows apart, on disjoint banks).
+  const int lane = tid & 31;
+  const int c = 16 * (tid >> 5) + (lane & 15), p = lane >> 4;
   const bool col_ok = c0 + c < cols;
   uint32_t sc2 = 0;
   if (col_ok) {
@@ -1001,7 +1007,7 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
         for (int i = 0; i < 32; ++i) {
           const int rr = rb * 32 + i;
           v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-              &tile[rr][(((c >> 3) ^ (rr & 7)) << 4) + (c & 7) * 2]));
+              &tile[rr][(((c >> 3) ^ qt_swizzle(rr)) << 4) + (c & 7) * 2]));
         }
         const float amax = fmaxf(fmaxf(absmax8(v), absmax8(v + 8)),
                                  fmaxf(absmax8(v + 16), absmax8(v + 24)));
@@ -1018,18 +1024,19 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
         sc2 |= static_cast<uint32_t>(sexp + 127) << (8 * h);
       }
     }
+  }
+  // the column's n_rb (<= 4) scales are adjacent bytes in both layouts
+  // (tiled: the 32-blocks kk = 0..3 of one 128-row K group); lane l < 16
+  // writes them, one word when it can
+  sc2 |= __shfl_xor_sync(0xffffffffu, sc2, 16) << 16;
+  if (p == 0 && col_ok) {
     const int64_t orow = static_cast<int64_t>(z) * cols + c0 + c;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int rb = 2 * p + h;
-      if (rb < n_rb) {
-        const int64_t kb = (r0 >> 5) + rb;
-        const uint8_t sc = static_cast<uint8_t>(sc2 >> (8 * h));
-        if (kTiled)
-          s_col[mx_scale_offset(orow, kb, rows)] = sc;
-        else
-          s_col[orow * (rows >> 5) + kb] = sc;
-      }
+    const int64_t kb0 = r0 >> 5;
+    uint8_t* d = kTiled ? s_col + mx_scale_offset(orow, kb0, rows) : s_col + orow * (rows >> 5) + kb0;
+    if (n_rb == 4 && (reinterpret_cast<uintptr_t>(d) & 3) == 0) {
+      *reinterpret_cast<uint32_t*>(d) = sc2;
+    } else {
+      for (int rb = 0; rb < n_rb; ++rb) d[rb] = static_cast<uint8_t>(sc2 >> (8 * rb));
     }
   }
   __syncthreads();
@@ -1057,12 +1064,12 @@ static cudaError_t launch_quantize_tiles(const __nv_bfloat16* in, int64_t ld, in
   const dim3 grid(static_cast<unsigned>((rows + kQtRows - 1) / kQtRows),
                   static_cast<unsigned>((cols + kQtCols - 1) / kQtCols),
                   static_cast<unsigned>(batch));
-  if (tiled)
-    quantize_tile_kernel<true, kDual><<<grid, kQtThreads, 0, st>>>(
-        in, ld, batch_stride, rows, cols, gather, src_rows, row_end, q_row, s_row, q_col, s_col);
-  else
-    quantize_tile_kernel<false, kDual><<<grid, kQtThreads, 0, st>>>(
-        in, ld, batch_stride, rows, cols, gather, src_rows, row_end, q_row, s_row, q_col, s_col);
+  auto kern = gather ? (tiled ? quantize_tile_kernel<true, kDual, true>
+                              : quantize_tile_kernel<false, kDual, true>)
+                     : (tiled ? quantize_tile_kernel<true, kDual, false>
+                              : quantize_tile_kernel<false, kDual, false>);
+  kern<<<grid, kQtThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather, src_rows, row_end,
+                                    q_row, s_row, q_col, s_col);
   return cudaGetLastError();
 }
 
