@@ -1012,14 +1012,13 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.hs = hs;
   GemmOut o1, o2;
   g1.save = save ? 1 : 0;
-  if (save) {   // A_g, A_u and h in bf16 for the backward
-    if (!make_out_tmap(&o1.map[0], at<void>(workspace, L.ag), F, L.cap,
-                       static_cast<uint64_t>(F) * 2, false) ||
-        !make_out_tmap(&o1.map[1], at<void>(workspace, L.au), F, L.cap,
-                       static_cast<uint64_t>(F) * 2, false) ||
-        !make_out_tmap(&o1.map[2], at<void>(workspace, L.hb), F, L.cap,
+  if (save) {   // A_g, A_u (blocked) and h (row-major) in bf16 for the backward
+    g1.save_g = at<__nv_bfloat16>(workspace, L.ag);
+    g1.save_u = at<__nv_bfloat16>(workspace, L.au);
+    if (!make_out_tmap(&o1.map[2], at<void>(workspace, L.hb), F, L.cap,
                        static_cast<uint64_t>(F) * 2, false))
       return MOE_ERR_CUDA;
+    o1.map[0] = o1.map[1] = ta;                // unused
   } else {
     o1.map[0] = o1.map[1] = o1.map[2] = ta;    // unused
   }

@@ -367,6 +367,27 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         bulk_commit_group();
       }
     };
+    // a 32 x 32 bf16 block of A_g or A_u in the blocked layout: lane r's 16
+    // words (its row) land in the four 512-byte slabs, and the 2 KB leave
+    // in one bulk copy
+    auto put_block = [&](const uint32_t* w16, __nv_bfloat16* dst) {
+      if (lane == 0) bulk_wait_group_read<kSlots - 1>();
+      __syncwarp();
+      const uint32_t slot = slot0 + (npiece % kSlots) * kPieceBytes;
+      ++npiece;
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + j * 512 + lane * 16),
+                     "r"(w16[4 * j]), "r"(w16[4 * j + 1]), "r"(w16[4 * j + 2]),
+                     "r"(w16[4 * j + 3])
+                     : "memory");
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_copy_s2g(dst, slot, kPieceBytes);
+        bulk_commit_group();
+      }
+    };
     auto bf16_words = [](const uint32_t* f32x32, uint32_t* w16) {
 #pragma unroll
       for (int i = 0; i < 16; ++i)
@@ -378,15 +399,33 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       const MxTile tl = decode(t);
       const int64_t grow = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + row_in_tile;
       const int wrow0 = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + q * 32;   // warp's first row
-      if (kEpi == MxEpi::SwigluBwd) {
-        // while the tile's MMAs run, bring this row's A_g and A_u columns
-        // into L2, so that the epilogue reads them at L2 latency
-        const int64_t o = grow * p.N + tl.n * kTileN + half * (kTileN / 2);
+      // SwigluBwd: this row's A_g, A_u over the warp's half of the tile, 32
+      // columns at a time as packed bf16 pairs, from the blocked layout (four
+      // coalesced 512-byte loads per 32 x 32 block). The first block of each
+      // arrives while the tile's MMAs run; the rest are brought into L2 now
+      // and into registers one step ahead of their use.
+      constexpr int kActW = 16;                  // words of 32 columns
+      uint32_t ag_w[kActW], au_w[kActW];
+      const int act_c0 = tl.n * kTileN + half * (kTileN / 2);
+      auto act_block = [&](const __nv_bfloat16* act, int c) {   // this lane's row of a block
+        return act + act_block_offset(wrow0, act_c0 + c, p.N) + lane * 8;
+      };
+      auto load_act = [&](const __nv_bfloat16* row, uint32_t* w16) {
 #pragma unroll
-        for (int b = 0; b < kTileN / 2; b += 64) {   // 128-byte lines of this warp's half
-          prefetch_l2(p.act_g + o + b);
-          prefetch_l2(p.act_u + o + b);
+        for (int j = 0; j < 4; ++j) {
+          const int4 v = __ldg(reinterpret_cast<const int4*>(row + j * 256));
+          w16[4 * j] = static_cast<uint32_t>(v.x);
+          w16[4 * j + 1] = static_cast<uint32_t>(v.y);
+          w16[4 * j + 2] = static_cast<uint32_t>(v.z);
+          w16[4 * j + 3] = static_cast<uint32_t>(v.w);
         }
+      };
+      if (kEpi == MxEpi::SwigluBwd) {
+#pragma unroll
+        for (int c = 32; c < kTileN / 2; c += 32)   // 16 lines per block: lanes 0-15 A_g
+          prefetch_l2(act_block(lane < 16 ? p.act_g : p.act_u, c) - lane * 8 + (lane & 15) * 64);
+        load_act(act_block(p.act_g, 0), ag_w);
+        load_act(act_block(p.act_u, 0), au_w);
       }
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
@@ -423,9 +462,9 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           if (p.save) {
             uint32_t w[16];
             bf16_words(g, w);
-            put_piece(w, &tmO0, col + c, wrow0, false);
+            put_block(w, p.save_g + act_block_offset(wrow0, col + c, p.N));
             bf16_words(u, w);
-            put_piece(w, &tmO1, col + c, wrow0, false);
+            put_block(w, p.save_u + act_block_offset(wrow0, col + c, p.N));
             put_piece(&hw[c / 2], &tmO2, col + c, wrow0, false);
           }
         }
@@ -476,15 +515,15 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         // at column f of [dA_g | dA_u], dA_u at N + f
         constexpr int kHalf = kTileN / 2;
         const int f0 = tl.n * kTileN + half * kHalf;
-        const __nv_bfloat16* ag = p.act_g + grow * p.N + f0;
-        const __nv_bfloat16* au = p.act_u + grow * p.N + f0;
-#pragma unroll 1
+#pragma unroll
         for (int c = 0; c < kHalf; c += 32) {
           uint32_t v[32];
-          float fg[32], fu[32];
           tmem_ld_32x32b_x32(taddr + half * kHalf + c, v);
-          load_bf16x32(ag + c, fg);
-          load_bf16x32(au + c, fu);
+          uint32_t ag_n[kActW], au_n[kActW];      // the next 32 columns, in flight
+          if (c + 32 < kHalf) {
+            load_act(act_block(p.act_g, c + 32), ag_n);
+            load_act(act_block(p.act_u, c + 32), au_n);
+          }
           tmem_ld_wait();
           uint32_t wg[16], wu[16];
 #pragma unroll
@@ -493,7 +532,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const float dh = __uint_as_float(v[2 * i + h]);
-              const float a = fg[2 * i + h], b = fu[2 * i + h];
+              const float a = __uint_as_float(h ? (ag_w[i] & 0xFFFF0000u) : (ag_w[i] << 16));
+              const float b = __uint_as_float(h ? (au_w[i] & 0xFFFF0000u) : (au_w[i] << 16));
               const float sg = sigmoid_f(a);
               vg[h] = dh * b * sg * (1.0f + a * (1.0f - sg));
               vu[h] = dh * a * sg;
@@ -503,6 +543,13 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           }
           put_piece(wg, &tmO0, f0 + c, wrow0, false);
           put_piece(wu, &tmO0, p.N + f0 + c, wrow0, false);
+          if (c + 32 < kHalf) {
+#pragma unroll
+            for (int i = 0; i < kActW; ++i) {
+              ag_w[i] = ag_n[i];
+              au_w[i] = au_n[i];
+            }
+          }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));

@@ -233,8 +233,11 @@ struct MxGemmArgs {
   const uint8_t* sfb1;     // tiled scales of B1 (k_split)
   uint8_t* hq;             // fc1: codes of h [rows, N]
   uint8_t* hs;             // fc1: tiled scales of h
-  int save;                // fc1: also store A_g, A_u and h in bf16 (output maps 0, 1, 2)
-  const __nv_bfloat16* act_g;   // SwigluBwd: saved A_g, A_u [rows, N]
+  int save;                // fc1: also store A_g, A_u (blocked, save_g / save_u) and h
+                           // (row-major, output map 2) in bf16
+  __nv_bfloat16* save_g;
+  __nv_bfloat16* save_u;
+  const __nv_bfloat16* act_g;   // SwigluBwd: saved A_g, A_u [rows, N], blocked
   const __nv_bfloat16* act_u;
   int out_split;           // WGrad: rows r < out_split of each expert go to output map 0
                            // (row e * out_split + r), the rest to map 1; 0 means M
@@ -242,6 +245,17 @@ struct MxGemmArgs {
   int* err;
   unsigned long long wait_ns;
 };
+
+// The MXFP8 path keeps A_g and A_u [rows, N] (rows, N % 32 == 0) in 32 x 32
+// blocks of 2 KB, block (row / 32, col / 32) at ((row / 32) * (N / 32) +
+// col / 32) * 1024 elements; inside a block, 8-column slab j of row r at
+// j * 256 + r * 8. A warp that owns 32 rows then moves one 32-column chunk
+// of them with four fully coalesced 512-byte accesses, lane r holding its
+// own row (the TMEM lane layout of the accumulator).
+__host__ __device__ __forceinline__ int64_t act_block_offset(int64_t row, int64_t col, int64_t N) {
+  return ((row >> 5) * (N >> 5) + (col >> 5)) * 1024 + ((col & 31) >> 3) * 256 + (row & 31) * 8 +
+         (col & 7);
+}
 
 // Encodes a 2D uint8 tensor map with the 128-byte swizzle.
 bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
