@@ -545,12 +545,8 @@ struct FwdRun {
     if (!make_out_tmap(&o1.map[0], h, F, L.cap, static_cast<uint64_t>(F) * 2, false) ||
         !make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
       return MOE_ERR_CUDA;
-    o1.map[1] = o1.map[2] = o1.map[0];
-    if (save && (!make_out_tmap(&o1.map[1], g1.save_g, F, L.cap, static_cast<uint64_t>(F) * 2,
-                                false) ||
-                 !make_out_tmap(&o1.map[2], g1.save_u, F, L.cap, static_cast<uint64_t>(F) * 2,
-                                false)))
-      return MOE_ERR_CUDA;
+    o1.map[1] = o1.map[2] = o1.map[0];          // A_g, A_u leave as blocks (save_g, save_u)
+    g1.ld_act = F;
     o2.map[1] = o2.map[2] = o2.map[0];
     if ((gather ? launch_fc1_swiglu_gather(ta, tg, tu, o1, g1, grid, st)
                 : launch_fc1_swiglu(ta, tg, tu, o1, g1, grid, st)) != cudaSuccess)

@@ -101,16 +101,6 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
   return tl;
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const uint32_t* r) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    st_global_v4(dst + 8 * i,
-                 pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1])),
-                 pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3])),
-                 pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5])),
-                 pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7])));
-}
-
 // Epilogue output pieces: each epilogue warp finishes its 32 rows of the
 // tile in pieces of 32 rows x 64 bytes (32 bf16 or 16 float columns), staged
 // in its own shared-memory slots with the 64-byte swizzle (16-byte chunk j
@@ -376,7 +366,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
-    const int r = q * 32 + lane;              // row of the tile this thread finishes
     const uint32_t slot0 = smem_u32(pieces) + q * kSlotsPerWarp * kPieceBytes;
     const uint32_t my_row = lane * 64;
     const uint32_t sw = (lane >> 1) & 3;
@@ -415,10 +404,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       put_row(slot, w);
       piece_out(slot, map, x, y, false);
     };
+    // a 32 x 32 bf16 block of A_g or A_u in the blocked layout
+    // (act_block_offset): lane r's row lands in the four 512-byte slabs and
+    // the 2 KB leave in one bulk copy
+    auto put_block = [&](const uint32_t* f32x32, __nv_bfloat16* dst) {
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        w[i] = pack_bf16x2(__uint_as_float(f32x32[2 * i]), __uint_as_float(f32x32[2 * i + 1]));
+      const uint32_t slot = piece_slot();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + j * 512 + lane * 16),
+                     "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                     : "memory");
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_copy_s2g(dst, slot, kPieceBytes);
+        bulk_commit_group();
+      }
+      ++npiece;
+    };
+    // SwigluBwd: lane r's row of a 32 x 32 block of A_g or A_u, as 16 words
+    auto load_act = [&](const __nv_bfloat16* block, uint32_t* w16) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int4 v = __ldg(reinterpret_cast<const int4*>(block + j * 256 + lane * 8));
+        w16[4 * j] = static_cast<uint32_t>(v.x);
+        w16[4 * j + 1] = static_cast<uint32_t>(v.y);
+        w16[4 * j + 2] = static_cast<uint32_t>(v.z);
+        w16[4 * j + 3] = static_cast<uint32_t>(v.w);
+      }
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile tl = decode_tile<kSched>(t, ts, p);
+      // SwigluBwd: the warp's rows of A_g, A_u for the tile's first 32
+      // columns arrive while its MMAs run; the other blocks go to L2 now
+      uint32_t ag_w[16], au_w[16];
+      const int64_t wrow0 = tl.row0 + q * 32;
+      if (kEpi == Epi::SwigluBwd) {
+#pragma unroll 1
+        for (int c = 32; c < bn; c += 32)       // 16 lines per block: lanes 0-15 A_g
+          prefetch_l2((lane < 16 ? p.act_g : p.act_u) +
+                      act_block_offset(wrow0, tl.n * bn + c, p.ld_act) + (lane & 15) * 64);
+        load_act(p.act_g + act_block_offset(wrow0, tl.n * bn, p.ld_act), ag_w);
+        load_act(p.act_u + act_block_offset(wrow0, tl.n * bn, p.ld_act), au_w);
+      }
       const bool got = mbar_wait(smem_u32(&sm->tfull[acc]), acc_phase, p.wait_ns, abort_flag);
       // tcgen05.ld is warp-collective: the whole warp goes on or stops together
       if (!__all_sync(0xffffffffu, got)) {
@@ -447,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           put_row(slot, hw);
           piece_out(slot, &tmO0, n0 + c, tl.row0, false);
           if (p.save_g) {
-            bf16_piece(g, &tmO1, n0 + c, tl.row0);
-            bf16_piece(u, &tmO2, n0 + c, tl.row0);
+            put_block(g, p.save_g + act_block_offset(tl.row0 + q * 32, n0 + c, p.ld_act));
+            put_block(u, p.save_u + act_block_offset(tl.row0 + q * 32, n0 + c, p.ld_act));
           }
         }
       } else if (kEpi == Epi::Bf16) {
@@ -460,18 +494,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           bf16_piece(v, &tmO0, tl.n * bn + c, tl.row0);
         }
       } else if (kEpi == Epi::SwigluBwd) {
-        // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s), s = sigmoid(A_g)
-        const int64_t grow = tl.row0 + r;
+        // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s), s = sigmoid(A_g);
+        // the next 32 columns of A_g, A_u are loaded one step ahead
         const int f0 = tl.n * bn;
-        const __nv_bfloat16* ag = p.act_g + grow * p.ld_act + f0;
-        const __nv_bfloat16* au = p.act_u + grow * p.ld_act + f0;
 #pragma unroll 1
         for (int c = 0; c < bn; c += 32) {
           uint32_t v[32];
-          float fg[32], fu[32];
           tmem_ld_32x32b_x32(taddr + c, v);
-          load_bf16x32(ag + c, fg);
-          load_bf16x32(au + c, fu);
+          uint32_t ag_n[16], au_n[16];
+          if (c + 32 < bn) {
+            load_act(p.act_g + act_block_offset(wrow0, f0 + c + 32, p.ld_act), ag_n);
+            load_act(p.act_u + act_block_offset(wrow0, f0 + c + 32, p.ld_act), au_n);
+          }
           tmem_ld_wait();
           uint32_t wg[16], wu[16];
 #pragma unroll
@@ -480,7 +514,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const float dh = __uint_as_float(v[2 * i + h]);
-              const float a = fg[2 * i + h], b = fu[2 * i + h];
+              const float a = __uint_as_float(h ? (ag_w[i] & 0xFFFF0000u) : (ag_w[i] << 16));
+              const float b = __uint_as_float(h ? (au_w[i] & 0xFFFF0000u) : (au_w[i] << 16));
               const float sg = sigmoid_f(a);
               vg[h] = dh * b * sg * (1.0f + a * (1.0f - sg));
               vu[h] = dh * a * sg;
@@ -494,6 +529,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           slot = piece_slot();
           put_row(slot, wu);
           piece_out(slot, &tmO0, p.out_split + f0 + c, tl.row0, false);
+          if (c + 32 < bn) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              ag_w[i] = ag_n[i];
+              au_w[i] = au_n[i];
+            }
+          }
         }
       } else {  // Epi::F32: float rows (Rows) or weight-gradient rows (WGrad)
         const CUtensorMap* map = &tmO0;

@@ -125,11 +125,11 @@ struct GroupedGemmArgs {
   int k_split;             // k-blocks read from B0 when b_split == 2
   __nv_bfloat16* out;      // bf16 output
   int64_t ldo;             // row stride of out (elements)
-  __nv_bfloat16* save_g;   // fc1: optional bf16 copy of A_g (stride ldo)
-  __nv_bfloat16* save_u;   // fc1: optional bf16 copy of A_u
-  const __nv_bfloat16* act_g;  // SwigluBwd: saved A_g
-  const __nv_bfloat16* act_u;  // SwigluBwd: saved A_u
-  int64_t ld_act;
+  __nv_bfloat16* save_g;   // fc1: optional bf16 copy of A_g, blocked (act_block_offset)
+  __nv_bfloat16* save_u;   // fc1: optional bf16 copy of A_u, blocked
+  const __nv_bfloat16* act_g;  // SwigluBwd: saved A_g, blocked
+  const __nv_bfloat16* act_u;  // SwigluBwd: saved A_u, blocked
+  int64_t ld_act;          // columns of the saved A_g, A_u (F)
   int out_split;           // SwigluBwd: column offset of dA_u in out; F32: columns of outf
   float* outf;             // F32 output: Rows [rows, ldo]; WGrad [E, M, N or out_split]
   float* outf2;            // F32 second output (columns >= out_split)
@@ -157,7 +157,7 @@ bool make_out_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
                    uint64_t row_stride_bytes, bool f32);
 
 // fc1: out = bf16(silu(A W_gate) * (A W_up)), A rows tiled per expert.
-// Outputs: h (map 0) and, with save_g, A_g and A_u (maps 1, 2).
+// Outputs: h (map 0) and, with save_g, A_g and A_u as blocks (save_g, save_u).
 cudaError_t launch_fc1_swiglu(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                               const GemmOut& o, const GroupedGemmArgs& p, int grid,
                               cudaStream_t st);
@@ -246,7 +246,7 @@ struct MxGemmArgs {
   unsigned long long wait_ns;
 };
 
-// The MXFP8 path keeps A_g and A_u [rows, N] (rows, N % 32 == 0) in 32 x 32
+// The forward keeps A_g and A_u [rows, N] (rows, N % 32 == 0) in 32 x 32
 // blocks of 2 KB, block (row / 32, col / 32) at ((row / 32) * (N / 32) +
 // col / 32) * 1024 elements; inside a block, 8-column slab j of row r at
 // j * 256 + r * 8. A warp that owns 32 rows then moves one 32-column chunk
