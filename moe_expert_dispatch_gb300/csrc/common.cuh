@@ -246,15 +246,6 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
       : "memory");
 }
 
-// Untiled bulk copy shared -> global in the bulk-group of this thread
-// (16-byte aligned, size % 16 == 0).
-__device__ __forceinline__ void bulk_copy_s2g(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   reinterpret_cast<uint64_t>(dst)),
-               "r"(src), "r"(bytes)
-               : "memory");
-}
-
 // Shared-memory descriptor without swizzle (core matrices of 8 rows x 16 B).
 __device__ __forceinline__ uint64_t sdesc_noswizzle(uint32_t saddr, uint32_t lbo_bytes,
                                                     uint32_t sbo_bytes) {

@@ -405,26 +405,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       piece_out(slot, map, x, y, false);
     };
     // a 32 x 32 bf16 block of A_g or A_u in the blocked layout
-    // (act_block_offset): lane r's row lands in the four 512-byte slabs and
-    // the 2 KB leave in one bulk copy
+    // (act_block_offset): lane r's row is its four 16-byte slab pieces, so
+    // each warp store writes 512 contiguous bytes straight from registers
     auto put_block = [&](const uint32_t* f32x32, __nv_bfloat16* dst) {
       uint32_t w[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         w[i] = pack_bf16x2(__uint_as_float(f32x32[2 * i]), __uint_as_float(f32x32[2 * i + 1]));
-      const uint32_t slot = piece_slot();
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + j * 512 + lane * 16),
-                     "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
-                     : "memory");
-      fence_proxy_async_shared();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_copy_s2g(dst, slot, kPieceBytes);
-        bulk_commit_group();
-      }
-      ++npiece;
+        st_global_v4(dst + j * 256 + lane * 8, w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
     };
     // SwigluBwd: lane r's row of a 32 x 32 block of A_g or A_u, as 16 words
     auto load_act = [&](const __nv_bfloat16* block, uint32_t* w16) {

@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
   const int n_tiles = p.N / n_cols;
   const int kgroups_a = p.kgroups_a > 0 ? p.kgroups_a : (p.K >> 7);
   const int kgroups_b = p.kgroups_b > 0 ? p.kgroups_b : (p.K >> 7);
-  const int m_tiles_w = kWGrad ? p.M / kTileM : 0;   // WGrad: M tiles of every expert
+  const int m_tiles_w = kWGrad ? p.M / kTileM : 1;   // WGrad: M tiles of every expert
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -367,26 +367,14 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         bulk_commit_group();
       }
     };
-    // a 32 x 32 bf16 block of A_g or A_u in the blocked layout: lane r's 16
-    // words (its row) land in the four 512-byte slabs, and the 2 KB leave
-    // in one bulk copy
+    // a 32 x 32 bf16 block of A_g or A_u in the blocked layout
+    // (act_block_offset): lane r's row is its four 16-byte slab pieces, so
+    // each warp store writes 512 contiguous bytes straight from registers
     auto put_block = [&](const uint32_t* w16, __nv_bfloat16* dst) {
-      if (lane == 0) bulk_wait_group_read<kSlots - 1>();
-      __syncwarp();
-      const uint32_t slot = slot0 + (npiece % kSlots) * kPieceBytes;
-      ++npiece;
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(slot + j * 512 + lane * 16),
-                     "r"(w16[4 * j]), "r"(w16[4 * j + 1]), "r"(w16[4 * j + 2]),
-                     "r"(w16[4 * j + 3])
-                     : "memory");
-      fence_proxy_async_shared();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_copy_s2g(dst, slot, kPieceBytes);
-        bulk_commit_group();
-      }
+        st_global_v4(dst + j * 256 + lane * 8, w16[4 * j], w16[4 * j + 1], w16[4 * j + 2],
+                     w16[4 * j + 3]);
     };
     auto bf16_words = [](const uint32_t* f32x32, uint32_t* w16) {
 #pragma unroll
