@@ -1008,13 +1008,11 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.hs = hs;
   GemmOut o1, o2;
   g1.save = save ? 1 : 0;
-  if (save) {   // A_g, A_u (blocked) and h (row-major) in bf16 for the backward
+  if (save) {   // A_g, A_u and h in bf16, blocked, for the backward
     g1.save_g = at<__nv_bfloat16>(workspace, L.ag);
     g1.save_u = at<__nv_bfloat16>(workspace, L.au);
-    if (!make_out_tmap(&o1.map[2], at<void>(workspace, L.hb), F, L.cap,
-                       static_cast<uint64_t>(F) * 2, false))
-      return MOE_ERR_CUDA;
-    o1.map[0] = o1.map[1] = ta;                // unused
+    g1.save_h = at<__nv_bfloat16>(workspace, L.hb);
+    o1.map[0] = o1.map[1] = o1.map[2] = ta;    // unused
   } else {
     o1.map[0] = o1.map[1] = o1.map[2] = ta;    // unused
   }
@@ -1160,20 +1158,17 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.sfb = at<uint8_t>(ws, B.w2_st);
   g.act_g = ag;
   g.act_u = au;
+  g.out_b = d_a;                                 // [dA_g | dA_u], blocked
   GemmOut od;
-  if (!make_out_tmap(&od.map[0], d_a, 2 * static_cast<uint64_t>(F), cap,
-                     static_cast<uint64_t>(F) * 4, false))
-    return MOE_ERR_CUDA;
-  od.map[1] = od.map[2] = od.map[0];
+  od.map[0] = od.map[1] = od.map[2] = t_doq;     // unused
   g.keep_a = keep(static_cast<uint64_t>(cap) * H);
   if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st))) return MOE_ERR_CUDA;
   mark(2);
 
   // dA quantised along 2F (dXp's K) and along the rows (dW1's K)
-  if (!ok(launch_quantize_dual(d_a, 2 * static_cast<int64_t>(F), 1, 0, static_cast<int>(cap),
-                               2 * F, row_end, true, at<uint8_t>(ws, B.daq),
-                               at<uint8_t>(ws, B.das), at<uint8_t>(ws, B.daT),
-                               at<uint8_t>(ws, B.dats), st)))
+  if (!ok(launch_quantize_dual_blocked(d_a, static_cast<int>(cap), 2 * F, row_end,
+                                       at<uint8_t>(ws, B.daq), at<uint8_t>(ws, B.das),
+                                       at<uint8_t>(ws, B.daT), at<uint8_t>(ws, B.dats), st)))
     return MOE_ERR_CUDA;
   mark(3);
 
@@ -1207,8 +1202,8 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   if (!ok(launch_quantize_cols(static_cast<const __nv_bfloat16*>(x), H, 1, 0,
                                static_cast<int>(cap), H, token_of, T, row_end, true,
                                at<uint8_t>(ws, B.xpT), at<uint8_t>(ws, B.xpts), st)) ||
-      !ok(launch_quantize_cols(hb, F, 1, 0, static_cast<int>(cap), F, nullptr, 0, row_end, true,
-                               at<uint8_t>(ws, B.hT), at<uint8_t>(ws, B.hts), st)))
+      !ok(launch_quantize_cols_blocked(hb, static_cast<int>(cap), F, row_end,
+                                       at<uint8_t>(ws, B.hT), at<uint8_t>(ws, B.hts), st)))
     return MOE_ERR_CUDA;
   mark(6);
   const int kg_cap = static_cast<int>(cap / 128);

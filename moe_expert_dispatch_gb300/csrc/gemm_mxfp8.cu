@@ -430,8 +430,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         // which then overlap the next tile's MMAs. The tile's N/64 scale
         // bytes of this row are adjacent in the tiled layout (one 128-wide K
         // group of fc2): they leave in one store. With save, A_g, A_u and h
-        // leave as bf16 pieces. This warp's half of the tile's h columns:
-        // kTileN / 4.
+        // also leave in bf16, in the blocked layout, straight from registers.
+        // This warp's half of the tile's h columns: kTileN / 4.
         constexpr int kHalf = kTileN / 4;
         const int c0 = half * kHalf;
         const int col = tl.n * n_cols + c0;
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             put_block(w, p.save_g + act_block_offset(wrow0, col + c, p.N));
             bf16_words(u, w);
             put_block(w, p.save_u + act_block_offset(wrow0, col + c, p.N));
-            put_piece(&hw[c / 2], &tmO2, col + c, wrow0, false);
+            put_block(&hw[c / 2], p.save_h + act_block_offset(wrow0, col + c, p.N));
           }
         }
         tc_fence_before();
@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       } else if (kEpi == MxEpi::SwigluBwd) {
         // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s),
         // s = sigmoid(A_g), over this warp's half of the tile's columns; dA_g
-        // at column f of [dA_g | dA_u], dA_u at N + f
+        // at column f of [dA_g | dA_u], dA_u at N + f, in the blocked layout
+        // (the dual quantiser reads it), straight from registers
         constexpr int kHalf = kTileN / 2;
         const int f0 = tl.n * kTileN + half * kHalf;
 #pragma unroll
@@ -529,8 +530,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             wg[i] = pack_bf16x2(vg[0], vg[1]);
             wu[i] = pack_bf16x2(vu[0], vu[1]);
           }
-          put_piece(wg, &tmO0, f0 + c, wrow0, false);
-          put_piece(wu, &tmO0, p.N + f0 + c, wrow0, false);
+          put_block(wg, p.out_b + act_block_offset(wrow0, f0 + c, 2 * p.N));
+          put_block(wu, p.out_b + act_block_offset(wrow0, p.N + f0 + c, 2 * p.N));
           if (c + 32 < kHalf) {
 #pragma unroll
             for (int i = 0; i < kActW; ++i) {

@@ -97,6 +97,15 @@ cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t ba
                                  int64_t batch_stride, int rows, int cols, const int32_t* gather,
                                  int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
                                  uint8_t* scales, cudaStream_t st);
+// The same two quantisers, tiled scales, reading in [rows, cols] from the
+// 32 x 32 blocked layout of act_block_offset (N = cols): rows % 32 == 0,
+// cols % 128 == 0.
+cudaError_t launch_quantize_dual_blocked(const __nv_bfloat16* in, int rows, int cols,
+                                         const int32_t* row_end, uint8_t* q_row, uint8_t* s_row,
+                                         uint8_t* q_col, uint8_t* s_col, cudaStream_t st);
+cudaError_t launch_quantize_cols_blocked(const __nv_bfloat16* in, int rows, int cols,
+                                         const int32_t* row_end, uint8_t* q, uint8_t* scales,
+                                         cudaStream_t st);
 
 // ------------------------------------------------------------------ grouped GEMMs
 
@@ -233,10 +242,12 @@ struct MxGemmArgs {
   const uint8_t* sfb1;     // tiled scales of B1 (k_split)
   uint8_t* hq;             // fc1: codes of h [rows, N]
   uint8_t* hs;             // fc1: tiled scales of h
-  int save;                // fc1: also store A_g, A_u (blocked, save_g / save_u) and h
-                           // (row-major, output map 2) in bf16
+  int save;                // fc1: also store A_g, A_u and h in bf16, blocked
+                           // (act_block_offset, N = F): save_g, save_u, save_h
   __nv_bfloat16* save_g;
   __nv_bfloat16* save_u;
+  __nv_bfloat16* save_h;
+  __nv_bfloat16* out_b;    // SwigluBwd: [dA_g | dA_u], blocked with N = 2 * N
   const __nv_bfloat16* act_g;   // SwigluBwd: saved A_g, A_u [rows, N], blocked
   const __nv_bfloat16* act_u;
   int out_split;           // WGrad: rows r < out_split of each expert go to output map 0

@@ -914,7 +914,11 @@ __device__ __forceinline__ float absmax8(const float* v) {
                fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
 }
 
-template <bool kTiled, bool kDual, bool kGather>
+// Where the bf16 input comes from: rows of a row-major matrix, gathered
+// rows, or the 32 x 32 blocked layout of act_block_offset (with N = cols).
+enum class QtSrc { Rows, Gather, Blocked };
+
+template <bool kTiled, bool kDual, QtSrc kSrc>
 __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
     const __nv_bfloat16* __restrict__ in, int64_t ld, int64_t batch_stride, int rows, int cols,
     const int32_t* __restrict__ gather, int64_t src_rows, const int32_t* __restrict__ row_end,
@@ -929,24 +933,35 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
   const int n_rb = (live_rows + 31) >> 5;
   const __nv_bfloat16* base = in + static_cast<int64_t>(z) * batch_stride;
   const int tid = threadIdx.x;
-  const int ch = tid & 15;                     // this thread's 8-column chunk of a row
-  const bool ch_ok = c0 + ch * 8 < cols;
+  // load i of this thread: tile row lr(i), 8-column chunk ch(i). Row-major
+  // sources: 16 lanes per 256-byte row piece. Blocked: a warp load is one
+  // 512-byte slab (8 columns of a block's 32 rows, lane = row); the tile's
+  // 16 blocks x 4 slabs are the 8 warps' 8 loads.
+  auto load_row = [&](int i) {
+    return kSrc == QtSrc::Blocked ? (((tid >> 5) * 8 + i) >> 4) * 32 + (tid & 31)
+                                  : (tid >> 4) + 16 * i;
+  };
+  auto load_chunk = [&](int i) {
+    const int q = (tid >> 5) * 8 + i;
+    return kSrc == QtSrc::Blocked ? ((q >> 2) & 3) * 4 + (q & 3) : (tid & 15);
+  };
   int4 v4[kQtRows / 16];
 #pragma unroll
   for (int i = 0; i < kQtRows / 16; ++i) {
-    const int lr = (tid >> 4) + 16 * i;
+    const int lr = load_row(i), ch = load_chunk(i);
     int64_t r = r0 + lr;
-    bool ok = lr < live_rows && ch_ok;
-    if (kGather && ok) {
+    bool ok = lr < live_rows && c0 + ch * 8 < cols;
+    if (kSrc == QtSrc::Gather && ok) {
       r = __ldg(gather + r);
       ok = r >= 0 && r < src_rows;
     }
-    v4[i] = ok ? ld_stream(reinterpret_cast<const int4*>(base + r * ld + c0 + ch * 8))
-               : make_int4(0, 0, 0, 0);
+    const __nv_bfloat16* src = kSrc == QtSrc::Blocked ? base + act_block_offset(r, c0 + ch * 8, cols)
+                                                       : base + r * ld + c0 + ch * 8;
+    v4[i] = ok ? ld_stream(reinterpret_cast<const int4*>(src)) : make_int4(0, 0, 0, 0);
   }
 #pragma unroll
   for (int i = 0; i < kQtRows / 16; ++i) {
-    const int lr = (tid >> 4) + 16 * i;
+    const int lr = load_row(i), ch = load_chunk(i);
     *reinterpret_cast<int4*>(&tile[lr][(ch ^ qt_swizzle(lr)) << 4]) = v4[i];
   }
   __syncthreads();
@@ -1057,17 +1072,19 @@ template <bool kDual>
 static cudaError_t launch_quantize_tiles(const __nv_bfloat16* in, int64_t ld, int64_t batch,
                                          int64_t batch_stride, int rows, int cols,
                                          const int32_t* gather, int64_t src_rows,
-                                         const int32_t* row_end, bool tiled, uint8_t* q_row,
-                                         uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
-                                         cudaStream_t st) {
+                                         const int32_t* row_end, bool tiled, bool blocked,
+                                         uint8_t* q_row, uint8_t* s_row, uint8_t* q_col,
+                                         uint8_t* s_col, cudaStream_t st) {
   if (batch == 0 || rows == 0 || cols == 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>((rows + kQtRows - 1) / kQtRows),
                   static_cast<unsigned>((cols + kQtCols - 1) / kQtCols),
                   static_cast<unsigned>(batch));
-  auto kern = gather ? (tiled ? quantize_tile_kernel<true, kDual, true>
-                              : quantize_tile_kernel<false, kDual, true>)
-                     : (tiled ? quantize_tile_kernel<true, kDual, false>
-                              : quantize_tile_kernel<false, kDual, false>);
+  auto kern = blocked  ? (tiled ? quantize_tile_kernel<true, kDual, QtSrc::Blocked>
+                                : quantize_tile_kernel<false, kDual, QtSrc::Blocked>)
+              : gather ? (tiled ? quantize_tile_kernel<true, kDual, QtSrc::Gather>
+                                : quantize_tile_kernel<false, kDual, QtSrc::Gather>)
+                       : (tiled ? quantize_tile_kernel<true, kDual, QtSrc::Rows>
+                                : quantize_tile_kernel<false, kDual, QtSrc::Rows>);
   kern<<<grid, kQtThreads, 0, st>>>(in, ld, batch_stride, rows, cols, gather, src_rows, row_end,
                                     q_row, s_row, q_col, s_col);
   return cudaGetLastError();
@@ -1079,7 +1096,14 @@ cudaError_t launch_quantize_dual(const __nv_bfloat16* in, int64_t ld, int64_t ba
                                  uint8_t* s_row, uint8_t* q_col, uint8_t* s_col,
                                  cudaStream_t st) {
   return launch_quantize_tiles<true>(in, ld, batch, batch_stride, rows, cols, nullptr, 0, row_end,
-                                     tiled, q_row, s_row, q_col, s_col, st);
+                                     tiled, false, q_row, s_row, q_col, s_col, st);
+}
+
+cudaError_t launch_quantize_dual_blocked(const __nv_bfloat16* in, int rows, int cols,
+                                         const int32_t* row_end, uint8_t* q_row, uint8_t* s_row,
+                                         uint8_t* q_col, uint8_t* s_col, cudaStream_t st) {
+  return launch_quantize_tiles<true>(in, cols, 1, 0, rows, cols, nullptr, 0, row_end, true, true,
+                                     q_row, s_row, q_col, s_col, st);
 }
 
 cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t batch,
@@ -1087,7 +1111,14 @@ cudaError_t launch_quantize_cols(const __nv_bfloat16* in, int64_t ld, int64_t ba
                                  int64_t src_rows, const int32_t* row_end, bool tiled, uint8_t* q,
                                  uint8_t* scales, cudaStream_t st) {
   return launch_quantize_tiles<false>(in, ld, batch, batch_stride, rows, cols, gather, src_rows,
-                                      row_end, tiled, nullptr, nullptr, q, scales, st);
+                                      row_end, tiled, false, nullptr, nullptr, q, scales, st);
+}
+
+cudaError_t launch_quantize_cols_blocked(const __nv_bfloat16* in, int rows, int cols,
+                                         const int32_t* row_end, uint8_t* q, uint8_t* scales,
+                                         cudaStream_t st) {
+  return launch_quantize_tiles<false>(in, cols, 1, 0, rows, cols, nullptr, 0, row_end, true, true,
+                                      nullptr, nullptr, q, scales, st);
 }
 
 // The dispatch of the MXFP8 path: one warp per token reads the bf16 row once,
