@@ -103,7 +103,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
                    const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1,
                    const __grid_constant__ CUtensorMap tmO2, MxGemmArgs p) {
-  constexpr bool kFc1 = kEpi == MxEpi::Fc1;
+  constexpr bool kFc1 = kEpi == MxEpi::Fc1 || kEpi == MxEpi::Fc1Save;
+  constexpr bool kSave = kEpi == MxEpi::Fc1Save;   // fc1 also stores A_g, A_u and h in bf16
   constexpr bool kWGrad = kSched == Sched::WGrad;
   constexpr int kThreads = num_threads<kEpi>();
   extern __shared__ uint8_t smem_raw[];
@@ -429,35 +430,55 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         // accumulator is released before the quantisation and the stores,
         // which then overlap the next tile's MMAs. The tile's N/64 scale
         // bytes of this row are adjacent in the tiled layout (one 128-wide K
-        // group of fc2): they leave in one store. With save, A_g, A_u and h
-        // also leave in bf16, in the blocked layout, straight from registers.
-        // This warp's half of the tile's h columns: kTileN / 4.
+        // group of fc2): they leave in one store. With save, A_g and A_u are
+        // packed too, and A_g, A_u and h leave in bf16 after the release, in
+        // the blocked layout, straight from registers. This warp's half of
+        // the tile's h columns: kTileN / 4.
         constexpr int kHalf = kTileN / 4;
         const int c0 = half * kHalf;
         const int col = tl.n * n_cols + c0;
         uint32_t hw[kHalf / 2];
+        uint32_t gw[kHalf / 2], uw[kHalf / 2];    // with save: A_g, A_u packed
+        auto h_pair = [](uint32_t g0, uint32_t g1, uint32_t u0, uint32_t u1) {
+          return pack_bf16x2(silu_f(__uint_as_float(g0)) * __uint_as_float(u0),
+                             silu_f(__uint_as_float(g1)) * __uint_as_float(u1));
+        };
+        if (kSave) {
 #pragma unroll
-        for (int c = 0; c < kHalf; c += 32) {
-          uint32_t g[32], u[32];
-          tmem_ld_32x32b_x32(taddr + c0 + c, g);
-          tmem_ld_32x32b_x32(taddr + kTileN / 2 + c0 + c, u);
-          tmem_ld_wait();
+          for (int c = 0; c < kHalf; c += 16) {   // 16 columns at a time: few live registers
+            uint32_t g[16], u[16];
+            tmem_ld_32x32b_x16(taddr + c0 + c, g);
+            tmem_ld_32x32b_x16(taddr + kTileN / 2 + c0 + c, u);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            hw[c / 2 + i] = pack_bf16x2(silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
-                                        silu_f(__uint_as_float(g[2 * i + 1])) *
-                                            __uint_as_float(u[2 * i + 1]));
-          if (p.save) {
-            uint32_t w[16];
-            bf16_words(g, w);
-            put_block(w, p.save_g + act_block_offset(wrow0, col + c, p.N));
-            bf16_words(u, w);
-            put_block(w, p.save_u + act_block_offset(wrow0, col + c, p.N));
-            put_block(&hw[c / 2], p.save_h + act_block_offset(wrow0, col + c, p.N));
+            for (int i = 0; i < 8; ++i) {
+              hw[c / 2 + i] = h_pair(g[2 * i], g[2 * i + 1], u[2 * i], u[2 * i + 1]);
+              gw[c / 2 + i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+              uw[c / 2 + i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(taddr + c0 + c, g);
+            tmem_ld_32x32b_x32(taddr + kTileN / 2 + c0 + c, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              hw[c / 2 + i] = h_pair(g[2 * i], g[2 * i + 1], u[2 * i], u[2 * i + 1]);
           }
         }
         tc_fence_before();
         mbar_arrive(smem_u32(&sm->tempty[acc]));
+        if (kSave) {                               // after the release: off the MMAs' path
+#pragma unroll
+          for (int c = 0; c < kHalf; c += 32) {
+            put_block(&gw[c / 2], p.save_g + act_block_offset(wrow0, col + c, p.N));
+            put_block(&uw[c / 2], p.save_u + act_block_offset(wrow0, col + c, p.N));
+            put_block(&hw[c / 2], p.save_h + act_block_offset(wrow0, col + c, p.N));
+          }
+        }
         uint32_t codes[kHalf / 4];
         uint32_t packed = 0;
 #pragma unroll
@@ -633,7 +654,8 @@ cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUte
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st);
+  return p.save ? launch_mx_bn<MxEpi::Fc1Save, Sched::Rows>(a, wg, wu, o, p, grid, st)
+                : launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st);
 }
 
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,

@@ -221,7 +221,7 @@ cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t
 // leave through the output tensor maps (make_out_tmap): fc1's saves
 // (0: A_g, 1: A_u, 2: h), fc2's O (0), dH's [dA_g | dA_u] (0), dXp (0), the
 // weight gradients (0, and 1 past out_split).
-enum class MxEpi { Fc1, Bf16, SwigluBwd, F32 };
+enum class MxEpi { Fc1, Bf16, SwigluBwd, F32, Fc1Save };   // Fc1Save: fc1 with p.save
 
 struct MxGemmArgs {
   const int32_t* off_al;   // [E+1] padded expert row offsets
