@@ -42,29 +42,33 @@ import synth  # noqa: E402
 BF16_GEMM_SOURCES = ("gemm_bf16.cu", "common.cuh", "internal.h")
 MXFP8_GEMM_SOURCES = ("gemm_mxfp8.cu", "mx.cuh", "common.cuh", "internal.h")
 TRAFFIC = {
-    # fc1 on the Mixtral-shaped workload: the 2-expert capture (611.4 MB for
+    # fc1 on the Mixtral-shaped workload: the 2-expert capture (611.1 MB for
     # 620.8 MB algorithmic) scaled by the algorithmic bytes of the full launch
     # (2181 MB); profiles/grouped_gemm_mixtral_2experts_ncu_full.md
-    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2148e6, "sources": BF16_GEMM_SOURCES,
-                                     "src_sha": "1d7db3e5b7490783"},
+    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2147e6, "sources": BF16_GEMM_SOURCES,
+                                     "src_sha": "d2c93375bc1c283b"},
     # fc1 on the skewed workload, captured at full size;
     # profiles/grouped_gemm_skewed_bf16_ncu_full.md
-    ("skewed_bf16", "fc1_swiglu"): {"bytes": 1175.5e6, "sources": BF16_GEMM_SOURCES,
-                                    "src_sha": "1d7db3e5b7490783"},
-    # MXFP8 fc1: the 16-expert capture (727.8 MB for 718.1 MB algorithmic)
+    ("skewed_bf16", "fc1_swiglu"): {"bytes": 1175.0e6, "sources": BF16_GEMM_SOURCES,
+                                    "src_sha": "d2c93375bc1c283b"},
+    # MXFP8 fc1: the 16-expert capture (727.6 MB for 718.1 MB algorithmic)
     # scaled to the full launch (2871.9 MB); profiles/mx_gemm_mxfp8_16experts_ncu_full.md
-    ("mxfp8", "fc1_swiglu"): {"bytes": 2911e6, "sources": MXFP8_GEMM_SOURCES,
-                              "src_sha": "b5f3e113463c3f39"},
-    # dW1 of the training step: the 2-expert capture (1165.5 MB for 1208.4 MB
+    ("mxfp8", "fc1_swiglu"): {"bytes": 2910e6, "sources": MXFP8_GEMM_SOURCES,
+                              "src_sha": "76674f7cbe8666d2"},
+    # dW1 of the training step: the 2-expert capture (1165.0 MB for 1208.4 MB
     # algorithmic) scaled to the full launch (5905.5 MB);
     # profiles/grouped_gemm_backward_train_2experts_ncu_full.md
-    ("train_bf16", "dW1"): {"bytes": 5696e6, "sources": BF16_GEMM_SOURCES,
-                            "src_sha": "1d7db3e5b7490783"},
+    ("train_bf16", "dW1"): {"bytes": 5693e6, "sources": BF16_GEMM_SOURCES,
+                            "src_sha": "d2c93375bc1c283b"},
     # fc1 with its bf16 saves in the MXFP8 training step: the 2-expert capture
     # (626.7 MB for 672.3 MB algorithmic) scaled to the full launch (4410 MB);
     # profiles/mx_gemm_train_mxfp8_2experts_ncu_full.md
     ("train_mxfp8", "fc1_swiglu"): {"bytes": 4111e6, "sources": MXFP8_GEMM_SOURCES,
-                                    "src_sha": "b5f3e113463c3f39"},
+                                    "src_sha": "76674f7cbe8666d2"},
+    # dW1 of the MXFP8 training step: the 2-expert capture (1023.6 MB for
+    # 1077.9 MB algorithmic) scaled to the full launch (4865.4 MB); same file
+    ("train_mxfp8", "dW1"): {"bytes": 4620e6, "sources": MXFP8_GEMM_SOURCES,
+                             "src_sha": "76674f7cbe8666d2"},
 }
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
