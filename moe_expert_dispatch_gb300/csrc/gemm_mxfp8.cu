@@ -46,8 +46,32 @@ constexpr int kSfBytes = 512;              // one scale atom (128 rows x 4 block
 // slots from the producer and MMA threads).
 template <MxEpi kEpi>
 constexpr int epi_warps() { return kEpi == MxEpi::Bf16 ? 4 : 8; }
+// dH also needs its float half-row (128 columns) next to the A_g, A_u blocks
+// it reads, more than 168 registers a thread. Its CTA runs 12 warps: warps
+// 0-3 (producer, MMA issuer and two idle warps that only complete the
+// warpgroup) drop to kRegsControl registers, and the two epilogue
+// warpgroups, warps 4-11, rise to kRegsEpi. setmaxnreg.inc waits until the
+// CTA's pool (its registers at launch) has room, so the split must add up
+// to exactly that pool: the launch checks the kernel's register count.
 template <MxEpi kEpi>
-constexpr int num_threads() { return 64 + 32 * epi_warps<kEpi>(); }
+constexpr bool reg_split() { return kEpi == MxEpi::SwigluBwd; }
+template <MxEpi kEpi>
+constexpr int epi_first_warp() { return reg_split<kEpi>() ? 4 : 2; }
+template <MxEpi kEpi>
+constexpr int num_threads() { return 32 * (epi_first_warp<kEpi>() + epi_warps<kEpi>()); }
+constexpr int kRegsLaunch = 168;    // 65536 / 384 threads, in steps of 8
+constexpr int kRegsControl = 56, kRegsEpi = 224;
+static_assert(4 * kRegsControl + 8 * kRegsEpi == 12 * kRegsLaunch,
+              "the register split must fill the pool of a 12-warp CTA exactly");
+
+template <int kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
@@ -201,148 +225,156 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     return tl;
   };
 
-  if (warp == 0) {
-    // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t fills = 0;
-      bool ok = true;
-      const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
-      const uint32_t ring0 = smem_u32(ring);
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const MxTile tl = decode(t);
-        // A rows and the first 128-row block of B's scale atoms
-        const int a_row = kWGrad ? tl.m * kTileM : p.off_al[tl.e] + tl.m * kTileM;
-        const int64_t b_row =
-            kWGrad ? static_cast<int64_t>(tl.n) * kTileN
-                   : static_cast<int64_t>(tl.e) * p.b_rows + static_cast<int64_t>(tl.n) * (kFc1 ? kTileN / 2 : kTileN);
-        const int64_t vrow = kWGrad ? b_row
-                                    : static_cast<int64_t>(tl.e) * p.sfb_rows +
-                                          static_cast<int64_t>(tl.n) * kTileN;
-        const int kg0 = tl.k0 >> 7;
-        for (int kb = 0; kb < tl.kblocks; ++kb) {
-          const uint32_t full = smem_u32(&sm->full[stage]);
-          if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full, kABytes + kBBytes + (1 + G::kSfbAtoms) * kSfBytes);
-          const uint32_t sa = ring0 + stage * kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          const uint32_t ssf = sb + kBBytes;
-          const int kx = tl.k0 + kb * BK;
-          tma_load_2d_hint(sa, &tmA, full, kx, a_row, pol_a);
-          // B: fc1 takes N/2 gate rows and N/2 up rows of the same N tile;
-          // a K-split GEMM takes its k-blocks from B0, then from B1
-          const bool second = !kFc1 && !kWGrad && p.k_split > 0 && kb >= p.k_split;
-          const int kbb = second ? kb - p.k_split : kb;
-          if (kFc1) {
-            const int half = kTileN / 2;
-            tma_load_2d(sb, &tmB0, full, kx, static_cast<int>(b_row));
-            tma_load_2d(sb + half * BK, &tmB1, full, kx, static_cast<int>(b_row));
-          } else {
-            const CUtensorMap* mb = second ? &tmB1 : &tmB0;
-            for (int j = 0; j < kTileN; j += 128)
-              tma_load_2d(sb + j * BK, mb, full, kbb * BK + tl.k0, static_cast<int>(b_row + j));
-          }
-          bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(a_row) >> 7) * kgroups_a + kg0 + kb) * kSfBytes,
-                        kSfBytes, full);
-          const uint8_t* sfb = second ? p.sfb1 : p.sfb;
+  // warpgroup-uniform role split: the register move, when there is one, is
+  // the first thing each side runs, so all the code after it is compiled
+  // against its new register count
+  if (warp < epi_first_warp<kEpi>()) {
+    if constexpr (reg_split<kEpi>()) regs_dec<kRegsControl>();
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t fills = 0;
+        bool ok = true;
+        const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
+        const uint32_t ring0 = smem_u32(ring);
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          const MxTile tl = decode(t);
+          // A rows and the first 128-row block of B's scale atoms
+          const int a_row = kWGrad ? tl.m * kTileM : p.off_al[tl.e] + tl.m * kTileM;
+          const int64_t b_row =
+              kWGrad ? static_cast<int64_t>(tl.n) * kTileN
+                     : static_cast<int64_t>(tl.e) * p.b_rows + static_cast<int64_t>(tl.n) * (kFc1 ? kTileN / 2 : kTileN);
+          const int64_t vrow = kWGrad ? b_row
+                                      : static_cast<int64_t>(tl.e) * p.sfb_rows +
+                                            static_cast<int64_t>(tl.n) * kTileN;
+          const int kg0 = tl.k0 >> 7;
+          for (int kb = 0; kb < tl.kblocks; ++kb) {
+            const uint32_t full = smem_u32(&sm->full[stage]);
+            if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full, kABytes + kBBytes + (1 + G::kSfbAtoms) * kSfBytes);
+            const uint32_t sa = ring0 + stage * kStageBytes;
+            const uint32_t sb = sa + kABytes;
+            const uint32_t ssf = sb + kBBytes;
+            const int kx = tl.k0 + kb * BK;
+            tma_load_2d_hint(sa, &tmA, full, kx, a_row, pol_a);
+            // B: fc1 takes N/2 gate rows and N/2 up rows of the same N tile;
+            // a K-split GEMM takes its k-blocks from B0, then from B1
+            const bool second = !kFc1 && !kWGrad && p.k_split > 0 && kb >= p.k_split;
+            const int kbb = second ? kb - p.k_split : kb;
+            if (kFc1) {
+              const int half = kTileN / 2;
+              tma_load_2d(sb, &tmB0, full, kx, static_cast<int>(b_row));
+              tma_load_2d(sb + half * BK, &tmB1, full, kx, static_cast<int>(b_row));
+            } else {
+              const CUtensorMap* mb = second ? &tmB1 : &tmB0;
+              for (int j = 0; j < kTileN; j += 128)
+                tma_load_2d(sb + j * BK, mb, full, kbb * BK + tl.k0, static_cast<int>(b_row + j));
+            }
+            bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(a_row) >> 7) * kgroups_a + kg0 + kb) * kSfBytes,
+                          kSfBytes, full);
+            const uint8_t* sfb = second ? p.sfb1 : p.sfb;
 #pragma unroll
-          for (int j = 0; j < G::kSfbAtoms; ++j)
-            bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
-                          sfb + (((vrow >> 7) + j) * kgroups_b + kg0 + kbb) * kSfBytes, kSfBytes,
-                          full);
-          ++fills;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+            for (int j = 0; j < G::kSfbAtoms; ++j)
+              bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
+                            sfb + (((vrow >> 7) + j) * kgroups_b + kg0 + kbb) * kSfBytes, kSfBytes,
+                            full);
+            ++fills;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1;
+            }
           }
         }
-      }
-      if (!ok) {
-        sm->abort = 1;
-        report_error(p.err, kErrTimeout);
-      }
-      // the last S fills must land before exit (fill i: slot i % S, parity (i / S) & 1)
-      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
-        mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
-      bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const int kblocks = decode(t).kblocks;
-        if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
-          ok = false;
-          break;
+        if (!ok) {
+          sm->abort = 1;
+          report_error(p.err, kErrTimeout);
         }
-        tc_fence_after();
-        const uint32_t d = tmem_base + acc * kTileN;
-        for (int kb = 0; kb < kblocks; ++kb) {
-          if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.wait_ns, abort_flag)) {
+        // the last S fills must land before exit (fill i: slot i % S, parity (i / S) & 1)
+        for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
+          mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
+      }
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true, issued = false;
+        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+          const int kblocks = decode(t).kblocks;
+          if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(ring) + stage * kStageBytes;
-          const uint32_t sb = sa + kABytes;
-          const uint32_t ssf = sb + kBBytes;
-          // this slot's scales into its own TMEM columns: A at +0..3, B's
-          // 128-row atoms at +4..7 (and +8..11 for N = 256)
-          const uint32_t sfa_t = tmem_base + G::kSfCol + stage * G::kSfColsPerStage;
-          const uint32_t sfb_t = sfa_t + 4;
-          tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
+          const uint32_t d = tmem_base + acc * kTileN;
+          for (int kb = 0; kb < kblocks; ++kb) {
+            if (!mbar_wait(smem_u32(&sm->full[stage]), phase, p.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sa = smem_u32(ring) + stage * kStageBytes;
+            const uint32_t sb = sa + kABytes;
+            const uint32_t ssf = sb + kBBytes;
+            // this slot's scales into its own TMEM columns: A at +0..3, B's
+            // 128-row atoms at +4..7 (and +8..11 for N = 256)
+            const uint32_t sfa_t = tmem_base + G::kSfCol + stage * G::kSfColsPerStage;
+            const uint32_t sfb_t = sfa_t + 4;
+            tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
 #pragma unroll
-          for (int j = 0; j < G::kSfbAtoms; ++j)
-            tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                   sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
-          const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
+            for (int j = 0; j < G::kSfbAtoms; ++j)
+              tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                     sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
+            const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
 #pragma unroll
-          for (int ks = 0; ks < BK / 32; ++ks)      // +32 B of K per MMA
-            umma_mxf8(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t,
-                      sfb_t, (kb | ks) ? 1u : 0u);
-          umma_commit(smem_u32(&sm->empty[stage]));
+            for (int ks = 0; ks < BK / 32; ++ks)      // +32 B of K per MMA
+              umma_mxf8(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t,
+                        sfb_t, (kb | ks) ? 1u : 0u);
+            umma_commit(smem_u32(&sm->empty[stage]));
+            issued = true;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          // a tile without k-blocks (WGrad, an expert without rows) issued no
+          // MMA: the commit only hands the (unwritten) accumulator on
+          umma_commit(smem_u32(&sm->tfull[acc]));
           issued = true;
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1;
+          if (++acc == G::kAccBufs) {
+            acc = 0;
+            acc_phase ^= 1;
           }
         }
-        if (!ok) break;
-        // a tile without k-blocks (WGrad, an expert without rows) issued no
-        // MMA: the commit only hands the (unwritten) accumulator on
-        umma_commit(smem_u32(&sm->tfull[acc]));
-        issued = true;
-        if (++acc == G::kAccBufs) {
-          acc = 0;
-          acc_phase ^= 1;
+        if (!ok) {
+          sm->abort = 1;
+          report_error(p.err, kErrTimeout);
+        }
+        if (issued) {
+          umma_commit(smem_u32(&sm->drain));
+          mbar_wait(smem_u32(&sm->drain), 0, kDrainNs, &sm->zero);
         }
       }
-      if (!ok) {
-        sm->abort = 1;
-        report_error(p.err, kErrTimeout);
-      }
-      if (issued) {
-        umma_commit(smem_u32(&sm->drain));
-        mbar_wait(smem_u32(&sm->drain), 0, kDrainNs, &sm->zero);
-      }
-    }
+    }      // warps 2 and 3 of a 12-warp CTA have no role
   } else {
+    if constexpr (reg_split<kEpi>()) regs_inc<kRegsEpi>();
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;                   // TMEM lane quadrant of this warp
-    const int half = (warp - 2) >> 2;         // 8 warps: which half of the tile's columns
+    const int ew = warp - epi_first_warp<kEpi>();
+    const int half = ew >> 2;                 // 8 warps: which half of the tile's columns
     const int row_in_tile = q * 32 + lane;
     // 8 slots in all: one per warp of an 8-warp epilogue, two (alternating)
     // per warp of a 4-warp one
     constexpr int kSlots = 8 / epi_warps<kEpi>();
-    const uint32_t slot0 = smem_u32(pieces) + (warp - 2) * kSlots * kPieceBytes;
+    const uint32_t slot0 = smem_u32(pieces) + ew * kSlots * kPieceBytes;
     const uint32_t my_row = lane * 64;
     const uint32_t sw = (lane >> 1) & 3;
     int npiece = 0;
@@ -522,26 +554,31 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         // dA_g = bf16(dH A_u s (1 + A_g (1 - s))), dA_u = bf16(dH A_g s),
         // s = sigmoid(A_g), over this warp's half of the tile's columns; dA_g
         // at column f of [dA_g | dA_u], dA_u at N + f, in the blocked layout
-        // (the dual quantiser reads it), straight from registers
+        // (the dual quantiser reads it), straight from registers. The warp's
+        // whole half-row of dH is loaded and the accumulator released first,
+        // so the next tile's MMAs run under this arithmetic and these stores.
         constexpr int kHalf = kTileN / 2;
         const int f0 = tl.n * kTileN + half * kHalf;
+        uint32_t v[kHalf];
+#pragma unroll
+        for (int c = 0; c < kHalf; c += 32) tmem_ld_32x32b_x32(taddr + half * kHalf + c, &v[c]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&sm->tempty[acc]));
 #pragma unroll
         for (int c = 0; c < kHalf; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(taddr + half * kHalf + c, v);
           uint32_t ag_n[kActW], au_n[kActW];      // the next 32 columns, in flight
           if (c + 32 < kHalf) {
             load_act(act_block(p.act_g, c + 32), ag_n);
             load_act(act_block(p.act_u, c + 32), au_n);
           }
-          tmem_ld_wait();
           uint32_t wg[16], wu[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             float vg[2], vu[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-              const float dh = __uint_as_float(v[2 * i + h]);
+              const float dh = __uint_as_float(v[c + 2 * i + h]);
               const float a = __uint_as_float(h ? (ag_w[i] & 0xFFFF0000u) : (ag_w[i] << 16));
               const float b = __uint_as_float(h ? (au_w[i] & 0xFFFF0000u) : (au_w[i] << 16));
               const float sg = sigmoid_f(a);
@@ -561,8 +598,6 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             }
           }
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
       } else {
         // float rows, 16 columns per piece: dXp (Rows) or a weight-gradient
         // row (WGrad; the expert's rows below out_split go to map 0 at row
@@ -636,6 +671,13 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    if (reg_split<kEpi>()) {
+      // the split's setmaxnreg.inc would wait for good on a smaller pool
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, mx_gemm_kernel<kEpi, kSched, kN>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+    }
     configured[d] = true;
   }
   mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(
