@@ -175,6 +175,22 @@ def _barrier(ws):
 
 # ---------------------------------------------------------------- CPU oracle sample
 
+def _cpu_threads() -> int:
+    """Threads the oracle's NumPy BLAS calls run on: the BLAS pool's size
+    where threadpoolctl can read it, else the cores this process may use."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:   # not installed, or a BLAS it cannot query
+        pass
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def cpu_oracle_sample(w, inp, n_tokens: int):
     """Time the oracle (as it stands) on n_tokens sampled tokens of the workload."""
     import oracle as orc
@@ -202,7 +218,7 @@ def cpu_oracle_sample(w, inp, n_tokens: int):
                             toks)
         what = "forward"
     dt = time.perf_counter() - t0
-    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": os.cpu_count(),
+    return {"value": n_tokens / dt, "unit": "tokens/s", "cores": _cpu_threads(),
             "kind": "oracle", "seconds": dt,
             "sample": f"{what} of {n_tokens} tokens of {w.name} (T={w.T}), float64, "
                       "one expert's weights converted at a time, NumPy BLAS threads"}
@@ -222,7 +238,7 @@ def run_reference(args, w):
             "ms_per_step": sec_per_token * w.T * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": os.cpu_count(),
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cpu_threads(),
                              "kind": "oracle",
                              "sample": f"{args.ref_tokens} tokens per step of {w.name}"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,

@@ -23,6 +23,23 @@ def test_reference_arm_prints_one_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny_bf16"
+    assert 1 <= d["cpu_baseline"]["cores"] <= os.cpu_count()
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    # two ranks: rank 0 alone times the oracle and prints; rank 1 exits 0
+    port = 29000 + os.getpid() % 1000
+    out = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                          "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                          "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+                          "--impl", "reference", "--gpus", "2", "--workload", "tiny_bf16",
+                          "--steps", "1", "--ref-tokens", "2"],
+                         capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
 
 
 def _rank(rank, world, port, q):
