@@ -224,6 +224,25 @@ moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, u
                               void* stream);
 
 /* ------------------------------------------------------------------------
+ * moe_permute_quantize_mxfp8 - the MXFP8 dispatch: each token's bf16 row is
+ * quantised once, by the rule of moe_quantize_mxfp8, and its codes are
+ * written to each of the token's k permuted rows. This is the quantised
+ * AllToAll of "MC2 通算融合架构总览" (section 1) on one GPU, the permute of
+ * moe_permute with MXFP8 rows. The scales are written once per token, in
+ * token order; the block-scaled GEMMs take them per permuted row.
+ *  x       bf16 [T, H]       token rows, 16-byte aligned
+ *  row_of  int32 [T, k]      permuted row of slot (t, j), as moe_permute
+ *                            writes it; a negative row is skipped. Rows are
+ *                            not checked against the size of xq.
+ *  xq      uint8 [rows, H]   out: E4M3 codes of token t at every row_of[t, j];
+ *                            other rows are left untouched
+ *  xs      uint8 [T, H/32]   out: E8M0 scales of token t, row-major
+ *  H % 32 == 0, 1 <= k <= 32. T == 0 does nothing.
+ * ------------------------------------------------------------------------ */
+moe_status moe_permute_quantize_mxfp8(const void* x, int64_t T, int H, const int32_t* row_of,
+                                      int k, uint8_t* xq, uint8_t* xs, void* stream);
+
+/* ------------------------------------------------------------------------
  * moe_expert_forward - the whole block in one call:
  *   y = unpermute(fc2(swiglu(fc1(permute(x)))), probs)
  * with, per expert e over its rows, A_g = Xp_e W1g_e, A_u = Xp_e W1u_e

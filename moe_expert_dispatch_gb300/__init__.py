@@ -67,6 +67,7 @@ _sig("moe_permute", _i32, _vp, _i64, _i64, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
      _vp, _vp, _sz, _vp)
 _sig("moe_unpermute", _i32, _vp, _vp, _vp, _i64, _i32, _i32, _vp, _vp)
 _sig("moe_quantize_mxfp8", _i32, _vp, _i64, _i32, _vp, _vp, _vp)
+_sig("moe_permute_quantize_mxfp8", _i32, _vp, _i64, _i32, _vp, _i32, _vp, _vp, _vp)
 _sig("moe_workspace_size", _sz, _i64, _i32, _i32, _i32, _i32, ctypes.POINTER(moe_config), _i32)
 _sig("moe_expert_forward", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32, _i32, _i32, _i32, _vp,
      _vp, _sz, ctypes.POINTER(moe_config), _vp)
@@ -269,6 +270,29 @@ def moe_quantize_mxfp8(a: torch.Tensor, stream=None, out=None):
         _cuda(s, "scales", torch.uint8)
     _check(_lib.moe_quantize_mxfp8(_p(a), rows, K, _p(q), _p(s), _stream(stream)),
            "moe_quantize_mxfp8")
+    return q, s
+
+
+def moe_permute_quantize_mxfp8(x: torch.Tensor, row_of: torch.Tensor, n_rows: int | None = None,
+                               stream=None, out=None):
+    """The MXFP8 dispatch of bf16 x [T, H]: (codes uint8 [n_rows, H] holding
+    token t's codes at every row_of[t, j] >= 0, scales uint8 [T, H/32] in
+    token order), written into out=(codes, scales) when given. n_rows
+    defaults to T * k; rows that row_of does not name stay zero."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(row_of, "row_of", torch.int32)
+    T, H = x.shape
+    k = row_of.shape[1]
+    if out is None:
+        rows = T * k if n_rows is None else n_rows
+        q = torch.zeros((rows, H), dtype=torch.uint8, device=x.device)
+        s = torch.empty((T, H // 32), dtype=torch.uint8, device=x.device)
+    else:
+        q, s = out
+        _cuda(q, "codes", torch.uint8)
+        _cuda(s, "scales", torch.uint8)
+    _check(_lib.moe_permute_quantize_mxfp8(_p(x), T, H, _p(row_of), k, _p(q), _p(s),
+                                           _stream(stream)), "moe_permute_quantize_mxfp8")
     return q, s
 
 

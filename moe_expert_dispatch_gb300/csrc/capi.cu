@@ -436,6 +436,16 @@ moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, u
                                          static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_permute_quantize_mxfp8(const void* x, int64_t T, int H, const int32_t* row_of,
+                                      int k, uint8_t* xq, uint8_t* xs, void* stream) {
+  if (T < 0 || H <= 0 || H % 32 != 0 || k < 1 || k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !row_of || !xq || !xs || !aligned16(x) || reinterpret_cast<uintptr_t>(xq) % 8 != 0)
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of,
+                                           xq, xs, static_cast<cudaStream_t>(stream)));
+}
+
 size_t moe_workspace_size(int64_t T, int H, int F, int E, int k, const moe_config* cfg,
                           int for_backward) {
   if (check_block_args(T, H, F, E, k) != MOE_OK) return 0;

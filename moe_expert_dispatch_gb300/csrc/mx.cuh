@@ -1,7 +1,8 @@
 // mx.cuh - MXFP8 (OCP Microscaling v1.0, E4M3 elements, E8M0 scales) on the
-// device: the block quantiser shared by the standalone quantiser, the fused
-// permute+quantise kernel and the fc1 epilogue, and the tiled scale layout
-// that the block-scaled tensor-core MMA reads.
+// device: the block quantiser's steps (scale exponent, inverse scale, E4M3
+// encoding) shared by the standalone quantisers, the fused permute+quantise
+// kernel and the fc1 epilogue, and the tiled scale layout that the
+// block-scaled tensor-core MMA reads.
 #pragma once
 
 #include <cuda_bf16.h>

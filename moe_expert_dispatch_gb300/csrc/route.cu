@@ -768,21 +768,6 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
 
 // ------------------------------------------------------------------ MXFP8
 
-__device__ __forceinline__ void load_bf16x32_f(const __nv_bfloat16* src, float* v) {
-  const int4* s4 = reinterpret_cast<const int4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int4 raw = ld_stream(s4 + i);
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = __bfloat1622float2(h[j]);
-      v[8 * i + 2 * j] = f.x;
-      v[8 * i + 2 * j + 1] = f.y;
-    }
-  }
-}
-
 // Quantisation along the rows: four lanes per 32-element block, each with 8
 // consecutive elements (one 16-byte load, one 8-byte store), so a warp reads
 // 512 and writes 256 contiguous bytes per block group, with four such loads
@@ -1122,33 +1107,65 @@ cudaError_t launch_quantize_cols_blocked(const __nv_bfloat16* in, int rows, int 
 }
 
 // The dispatch of the MXFP8 path: one warp per token reads the bf16 row once,
-// quantises it per 32 (the same routine as quantize_mxfp8_kernel), writes the
-// codes to each of the token's k rows and the scales once, in token order
+// quantises it per 32 (the rule of quantize_mxfp8_kernel), writes the codes
+// to each of the token's k rows and the scales once, in token order
 // (row-major [T, H/32]); gather_tile_scales_kernel then lays the scales out
-// per permuted row in the tiled layout.
+// per permuted row in the tiled layout. As in quantize_mxfp8_kernel, four
+// lanes share a 32-element block, 8 consecutive elements each, so every warp
+// load reads 512 contiguous bytes and every store to a row writes 256; a
+// pass covers 32 blocks with four loads in flight per lane.
 __global__ void __launch_bounds__(256) permute_quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t T, int H, int k,
     const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_tok) {
+  constexpr int kU = 4;                      // groups of 8 blocks per pass
   const int lane = lane_id();
+  const int part = lane & 3;                 // which 8 elements of the block
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int nb = H >> 5;
   for (int64_t t = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
        t < T; t += warps) {
     const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
-    for (int base = 0; base < nb; base += 32) {     // warp-uniform trip count
-      const int b = base + lane;
-      float v[32];
-      uint32_t w[8];
-      if (b < nb) {
-        load_bf16x32_f(x + t * H + b * 32, v);
-        xs_tok[t * nb + b] = quantize_block32(v, w);
+    const __nv_bfloat16* src = x + t * H;
+    for (int base = 0; base < nb; base += 8 * kU) {   // warp-uniform trip count
+      int4 raw[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int b = base + 8 * u + (lane >> 2);
+        raw[u] = b < nb ? ld_stream(reinterpret_cast<const int4*>(src + b * 32 + part * 8))
+                        : make_int4(0, 0, 0, 0);
+      }
+      uint2 w[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int b = base + 8 * u + (lane >> 2);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[u]);
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 f = __bfloat1622float2(h[j]);
+          v[2 * j] = f.x;
+          v[2 * j + 1] = f.y;
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int sexp = mx_block_exp(amax);
+        const float inv = mx_inv_scale(sexp);
+        w[u].x = mx_encode4(v[0], v[1], v[2], v[3], inv);
+        w[u].y = mx_encode4(v[4], v[5], v[6], v[7], inv);
+        if (part == 0 && b < nb) xs_tok[t * nb + b] = static_cast<uint8_t>(sexp + 127);
       }
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0 || b >= nb) continue;
-        int4* dst = reinterpret_cast<int4*>(xq + static_cast<int64_t>(r) * H + b * 32);
-        dst[0] = make_int4(w[0], w[1], w[2], w[3]);
-        dst[1] = make_int4(w[4], w[5], w[6], w[7]);
+        if (r < 0) continue;                   // warp-uniform
+        uint8_t* dst = xq + static_cast<int64_t>(r) * H + part * 8;
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int b = base + 8 * u + (lane >> 2);
+          if (b < nb) *reinterpret_cast<uint2*>(dst + b * 32) = w[u];
+        }
       }
     }
   }

@@ -61,3 +61,6 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
     assert st == 2
     assert m._lib.moe_counts(None, 10, 0, None, None, None, 0, None) == 1
     assert m._lib.moe_quantize_mxfp8(None, 4, 33, None, None, None) == 1
+    assert m._lib.moe_permute_quantize_mxfp8(None, 4, 48, None, 2, None, None, None) == 1
+    assert m._lib.moe_permute_quantize_mxfp8(None, 4, 64, None, 33, None, None, None) == 1
+    assert m._lib.moe_permute_quantize_mxfp8(None, 0, 64, None, 2, None, None, None) == 0

@@ -140,6 +140,49 @@ def test_quantize_mxfp8_bitexact():
     np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
 
 
+@pytest.mark.parametrize("T,H,k", [(1, 32, 1), (37, 96, 3), (300, 1056, 8), (64, 4128, 32),
+                                   (513, 7168, 6)])
+def test_permute_quantize_mxfp8_bitexact(T, H, k):
+    # the MXFP8 dispatch: every slot's row holds its token's codes, the
+    # scales are per token; H spans whole and ragged passes of 32 blocks
+    rng = np.random.default_rng(T + H + k)
+    a = rng.standard_normal((T, H)) * np.exp(rng.uniform(-30, 30, (T, 1)))
+    a[0, :32] = 0.0                     # an all-zero block
+    if T > 2:
+        a[2, H - 32:] = 1e-38           # subnormal-range values in the last block
+    x = torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)
+    n_rows = T * k + 5
+    row_of = rng.permutation(n_rows)[:T * k].reshape(T, k).astype(np.int32)
+    row_of[rng.random((T, k)) < 0.1] = -1                  # dropped slots write nothing
+    q, s = m.moe_permute_quantize_mxfp8(dev(x), dev(torch.from_numpy(row_of)), n_rows=n_rows)
+    q_ref, s_ref = orc.quantize_mxfp8(to_np(x))
+    np.testing.assert_array_equal(s.cpu().numpy(), s_ref)
+    want = np.zeros((n_rows, H), np.uint8)
+    for t in range(T):
+        for j in range(k):
+            if row_of[t, j] >= 0:
+                want[row_of[t, j]] = q_ref[t]
+    np.testing.assert_array_equal(q.cpu().numpy(), want)
+
+
+def test_permute_quantize_mxfp8_workload_sampled():
+    # the MXFP8 forward's full workload (T=16384, H=7168, k=6) with the padded
+    # row map the forward uses; 64 sampled tokens checked bit for bit
+    w, ids, probs = _routing("mxfp8")
+    x = synth.normal_bf16(0, 1, (w.T, w.H))
+    out = m.moe_permute(dev(x), dev(ids), dev(probs), w.E, row_align=128)
+    cap = out["x_perm"].shape[0]
+    q, s = m.moe_permute_quantize_mxfp8(dev(x), out["row_of"], n_rows=cap)
+    row_of = out["row_of"].cpu().numpy()
+    toks = np.random.default_rng(5).choice(w.T, 64, replace=False)
+    q_ref, s_ref = orc.quantize_mxfp8(to_np(x[torch.from_numpy(toks)]))
+    np.testing.assert_array_equal(s.cpu().numpy()[toks], s_ref)
+    qn = q.cpu().numpy()
+    for i, t in enumerate(toks):
+        for j in range(w.k):
+            np.testing.assert_array_equal(qn[row_of[t, j]], q_ref[i])
+
+
 def test_quantize_mxfp8_weights_bitexact():
     w = synth.normal_bf16(0, 2, (4, 256, 7168), 0.02)
     q, s = m.moe_quantize_mxfp8(dev(w))
