@@ -7,9 +7,11 @@
  * "execution path", steps 2-10) states it: per-expert token counts (histc),
  * the offset scan, the stable permute of routed rows into expert-contiguous
  * order, grouped GEMM fc1 (gate and up) with a SwiGLU epilogue, grouped GEMM
- * fc2 and the probability-weighted unpermute; plus the backward of the same
- * block and an MXFP8 variant of the forward. On one GPU the two AllToAllv of
- * the MC2 fusion collapse into the permute gather and the unpermute gather.
+ * fc2 and the probability-weighted unpermute. Around that path: a top-k
+ * router fused with the counts, the backward of the block, MXFP8 variants of
+ * the dispatch, the forward and the backward, and a micro-batch pipelined
+ * forward. On one GPU the two AllToAllv of the MC2 fusion collapse into the
+ * permute gather and the unpermute gather.
  *
  * Conventions shared by every entry point:
  *  - Pointers are DEVICE pointers unless stated otherwise, owned by the

@@ -64,3 +64,19 @@ def test_invalid_arguments_rejected_before_any_launch(lib):
     assert m._lib.moe_permute_quantize_mxfp8(None, 4, 48, None, 2, None, None, None) == 1
     assert m._lib.moe_permute_quantize_mxfp8(None, 4, 64, None, 33, None, None, None) == 1
     assert m._lib.moe_permute_quantize_mxfp8(None, 0, 64, None, 2, None, None, None) == 0
+
+
+def test_binding_rejects_host_tensors_before_the_library(lib):
+    # the binding checks device, dtype and layout itself, so no call reaches
+    # the library with a host pointer
+    import torch
+    import moe_expert_dispatch_gb300 as m
+    x = torch.zeros((4, 64), dtype=torch.bfloat16)
+    rows = torch.zeros((4, 2), dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA"):
+        m.moe_permute_quantize_mxfp8(x, rows)
+    with pytest.raises(ValueError, match="CUDA"):
+        m.moe_quantize_mxfp8(x)
+    with pytest.raises(ValueError, match="CUDA"):
+        m.moe_unpermute(x, rows, torch.zeros((4, 2)))
+
