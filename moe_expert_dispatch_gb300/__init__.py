@@ -437,6 +437,9 @@ def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_work
     """Gradients (dx, dw_gate, dw_up, dw_down, dprobs) of moe_expert_forward."""
     for t, n in ((dy, "dy"), (x, "x"), (w_gate, "w_gate"), (w_up, "w_up"), (w_down, "w_down")):
         _cuda(t, n, torch.bfloat16)
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    _cuda(fwd_workspace, "fwd_workspace")
     T, H = x.shape
     E, _, F = w_gate.shape
     k = expert_ids.shape[1]
@@ -502,6 +505,9 @@ def moe_expert_backward_mxfp8(dy, x, w1g_q, w1g_s, w1u_q, w1u_s, w2_q, w2_s, exp
     for t, n in ((w1g_q, "w1g_q"), (w1g_s, "w1g_s"), (w1u_q, "w1u_q"), (w1u_s, "w1u_s"),
                  (w2_q, "w2_q"), (w2_s, "w2_s")):
         _cuda(t, n, torch.uint8)
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
+    _cuda(fwd_workspace, "fwd_workspace")
     T, H = x.shape
     E, _, F = w1g_q.shape
     k = expert_ids.shape[1]
