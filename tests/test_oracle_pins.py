@@ -591,3 +591,59 @@ def test_mxfp8_backward_sampled_helpers_agree():
             want = (full["dw_gate_t"][e][f, h], full["dw_up_t"][e][f, h],
                     full["dw_down_t"][e][h, f])
             np.testing.assert_allclose(got[i], want, rtol=1e-9, atol=1e-12)
+
+
+# ---------------------------------------------------------------- MXFP8 symmetries
+
+def _mx_fwd(x, wgt, wut, wdt, ids, probs):
+    E = len(wgt)
+    xq, xs = orc.quantize_mxfp8(x)
+    q = [[orc.quantize_mxfp8(w[e]) for e in range(E)] for w in (wgt, wut, wdt)]
+    return orc.expert_forward_mxfp8(xq, xs, *q, ids, probs, E)
+
+
+def test_mxfp8_forward_linear_in_probs():
+    # the weights enter only the combine, after every quantisation: doubling
+    # them doubles y exactly (a power of two moves no rounding)
+    _, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=30, seed=40)
+    y1 = _mx_fwd(x, wgt, wut, wdt, ids, probs)
+    y2 = _mx_fwd(x, wgt, wut, wdt, ids, 2.0 * probs)
+    np.testing.assert_array_equal(y2, 2.0 * y1)
+    assert np.abs(y1).max() > 0
+
+
+def test_mxfp8_forward_expert_relabelling():
+    # renaming the experts (ids and weights together) changes nothing:
+    # every routed row meets its own expert's weights
+    _, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=30, E=5, k=3, seed=41)
+    perm = np.array([3, 0, 4, 1, 2])            # expert e is called perm[e]
+    inv = np.argsort(perm)
+    y1 = _mx_fwd(x, wgt, wut, wdt, ids, probs)
+    y2 = _mx_fwd(x, wgt[inv], wut[inv], wdt[inv], perm[ids], probs)
+    np.testing.assert_array_equal(y2, y1)
+
+
+def test_mxfp8_forward_token_order():
+    # tokens are independent: permuting them permutes y's rows
+    _, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=30, seed=42)
+    order = np.random.default_rng(43).permutation(30)
+    y1 = _mx_fwd(x, wgt, wut, wdt, ids, probs)
+    y2 = _mx_fwd(x[order], wgt, wut, wdt, ids[order], probs[order])
+    # a different row order can change BLAS's blocking, so a bf16 rounding
+    # may move by one step
+    np.testing.assert_allclose(y2, y1[order], rtol=2 ** -7, atol=1e-12)
+    assert np.mean(y2 == y1[order]) > 0.99
+
+
+def test_mxfp8_dprobs_is_dy_dot_slot_output():
+    # dprobs[t, j] = <dY_t, O of slot (t, j)>, O from the forward of that
+    # slot alone with weight 1
+    dy, x, wgt, wut, wdt, ids, probs = _mx_bwd_case(T=12, E=3, k=2, seed=44)
+    g = orc.expert_backward_mxfp8(dy, x, wgt, wut, wdt, ids, probs)
+    xq, xs = orc.quantize_mxfp8(x)
+    q = [[orc.quantize_mxfp8(w[e]) for e in range(3)] for w in (wgt, wut, wdt)]
+    for t in (0, 5, 11):
+        for j in range(2):
+            o = orc.token_forward_mxfp8(xq[t], xs[t], *q, ids[t, j:j + 1], [1.0])
+            np.testing.assert_allclose(g["dprobs"][t, j], np.dot(dy[t], o),
+                                       rtol=2 ** -7, atol=1e-9 * np.abs(o).max())
