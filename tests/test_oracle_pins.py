@@ -256,6 +256,27 @@ def test_probs_weight_linearly():
     np.testing.assert_allclose(y2, probs * y1, rtol=1e-12, atol=1e-14)
 
 
+def test_expert_relabelling_changes_nothing():
+    # renaming the experts (ids and weights together) gives the same y, bit
+    # for bit; a weight of the wrong expert anywhere would show
+    x, wg, wu, wd, ids, probs = _rand_case(E=5, empty=(3,))
+    perm = np.array([2, 4, 0, 1, 3])            # expert e is called perm[e]
+    inv = np.argsort(perm)
+    y1 = orc.expert_forward(x, wg, wu, wd, ids, probs)
+    y2 = orc.expert_forward(x, wg[inv], wu[inv], wd[inv], perm[ids], probs)
+    np.testing.assert_array_equal(y2, y1)
+
+
+def test_slot_order_within_a_token_changes_only_rounding():
+    # swapping a token's slots (ids and probs together) reorders one float
+    # sum before its single bf16 rounding
+    x, wg, wu, wd, ids, probs = _rand_case(k=2)
+    y1 = orc.expert_forward(x, wg, wu, wd, ids, probs)
+    y2 = orc.expert_forward(x, wg, wu, wd, ids[:, ::-1].copy(), probs[:, ::-1].copy())
+    np.testing.assert_allclose(y2, y1, rtol=2 ** -7, atol=1e-12)
+    assert np.mean(y2 == y1) > 0.95
+
+
 def test_microbatch_split_forward_equal():
     x, wg, wu, wd, ids, probs = _rand_case(T=64, k=2)
     y = orc.expert_forward(x, wg, wu, wd, ids, probs)
