@@ -651,7 +651,7 @@ def run_ours(args, w):
     return 0
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -672,7 +672,11 @@ def main():
                     help="capture each step once into a CUDA graph and replay it")
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,
                     help="BF16 forward: fc1 gathers the routed rows itself (no permuted copy)")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)

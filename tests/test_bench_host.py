@@ -69,3 +69,22 @@ def test_max_over_ranks_gloo_world_size_2():
     assert [r for r, _, _ in res] == [0, 1]
     assert all(v == 2.5 for _, _, v in res)          # both ranks see the slowest time
     assert res[1][1] == (2, 1, 1)                      # (world size, rank, local rank)
+
+
+def test_profile_commands_run_committed_files_with_valid_options():
+    # every bench command a profile summary names parses with bench.py's own
+    # options and names a workload the generators define
+    import glob
+    import re
+    import shlex
+    sys.path.insert(0, ROOT)
+    import bench
+    ap = bench.build_parser()
+    seen = 0
+    for path in glob.glob(os.path.join(ROOT, "profiles", "*.md")):
+        text = open(path).read().replace("\\\n", " ")
+        for cmd in re.findall(r"python bench\.py[^\n`]*", text):
+            argv = shlex.split(cmd)[2:]
+            ap.parse_args(argv)                      # exits on an unknown option
+            seen += 1
+    assert seen >= 5
