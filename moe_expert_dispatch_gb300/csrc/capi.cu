@@ -113,9 +113,8 @@ BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
 
 // MXFP8 forward workspace: the routing buffers of the BF16 layout, then the
 // codes and tiled scales of x, the tiled scales of the weights, the codes
-// and tiled scales of h, and O.
-// MXFP8 forward workspace; with save_for_backward also A_g, A_u and h in
-// bf16 [cap, F] (the backward's SwiGLU and weight-gradient operands).
+// and tiled scales of h, and O; with save_for_backward also A_g, A_u and h
+// in bf16 [cap, F] (the backward's SwiGLU and weight-gradient operands).
 struct MxLayout {
   int64_t R, cap;
   size_t route, counts, offsets, off_al, row_of, token_of, prob_of, xq, xs_tok, xs, wgu_s, wd_s,
