@@ -80,3 +80,19 @@ def test_binding_rejects_host_tensors_before_the_library(lib):
     with pytest.raises(ValueError, match="CUDA"):
         m.moe_unpermute(x, rows, torch.zeros((4, 2)))
 
+
+
+def test_package_refuses_to_import_without_the_library(tmp_path):
+    # a copy of the package without libmoe_gb300.so: the import fails loudly
+    # instead of falling back to anything else
+    import shutil
+    import subprocess
+    import sys
+    src = os.path.join(ROOT, "moe_expert_dispatch_gb300", "__init__.py")
+    pkg = tmp_path / "moe_expert_dispatch_gb300"
+    pkg.mkdir()
+    shutil.copy(src, pkg / "__init__.py")
+    out = subprocess.run([sys.executable, "-c", "import moe_expert_dispatch_gb300"],
+                         capture_output=True, text=True, cwd=tmp_path, timeout=300)
+    assert out.returncode != 0
+    assert "ImportError" in out.stderr and "no CPU or eager fallback" in out.stderr
