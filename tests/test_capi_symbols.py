@@ -96,3 +96,19 @@ def test_package_refuses_to_import_without_the_library(tmp_path):
                          capture_output=True, text=True, cwd=tmp_path, timeout=300)
     assert out.returncode != 0
     assert "ImportError" in out.stderr and "no CPU or eager fallback" in out.stderr
+
+
+def test_product_and_oracle_share_nothing():
+    # the library and its binding never name the oracle, and the oracle
+    # never names the library: parity compares two independent programs
+    import glob
+    product = [p for ext in ("py", "cu", "cuh", "h")
+               for p in glob.glob(os.path.join(ROOT, "moe_expert_dispatch_gb300", "**", "*." + ext),
+                                  recursive=True)]
+    product += glob.glob(os.path.join(ROOT, "include", "*.h"))
+    assert product
+    for p in product:
+        assert "oracle" not in open(p, encoding="utf-8").read(), p
+    for p in glob.glob(os.path.join(ROOT, "oracle", "**", "*.py"), recursive=True):
+        text = open(p, encoding="utf-8").read()
+        assert "moe_expert_dispatch_gb300" not in text and "libmoe" not in text, p
