@@ -190,6 +190,35 @@ def test_worked_example_golden():
     np.testing.assert_array_equal(st["h"][st["row_of"][0, 0]], g["h_expert0"])
 
 
+def test_mxfp8_worked_example_golden():
+    g = json.load(open(os.path.join(GOLDEN, "mxfp8_worked_example.json")))
+    inp = g["inputs"]
+    H, F, E = inp["H"], inp["F"], inp["E"]
+    ids, probs = np.array(inp["ids"]), np.array(inp["probs"])
+    x = np.zeros((len(ids), H))
+    for t, c, v in inp["x_nonzero"]:
+        x[t, c] = v
+
+    def ones(shape, where):
+        a = np.zeros(shape)
+        for e, r, c in where:
+            a[e, r, c] = 1.0
+        return a
+    wg = ones((E, F, H), inp["w_gate_t_ones"])
+    wu = ones((E, F, H), inp["w_up_t_ones"])
+    wd = ones((E, H, F), inp["w_down_t_ones"])
+    want = np.zeros_like(x)
+    for t, c, v in g["expected"]["y_nonzero"]:
+        want[t, c] = v
+    np.testing.assert_array_equal(_mx_fwd(x, wg, wu, wd, ids, probs), want)
+    xq, xs = orc.quantize_mxfp8(x)
+    q = [[orc.quantize_mxfp8(w[e]) for e in range(E)] for w in (wg, wu, wd)]
+    np.testing.assert_array_equal(orc.token_forward_mxfp8(xq[0], xs[0], *q, ids[0], probs[0]),
+                                  want[0])
+    hq, hs = orc.quantize_mxfp8(np.array([[g["expected"]["h_bf16_0"]] + [0.0] * (F - 1)]))
+    assert orc.dequantize_mxfp8(hq, hs)[0, 0] == g["expected"]["h_dequantised_0"]
+
+
 def test_grouped_equals_per_token_dense():
     x, wg, wu, wd, ids, probs = _rand_case()
     y1 = orc.expert_forward(x, wg, wu, wd, ids, probs)
