@@ -229,6 +229,8 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     inp = synth.make_inputs(w, 0)
+    for _ in range(args.warmup):          # untimed, as the GPU arm's warm-up steps
+        cpu_oracle_sample(w, inp, args.ref_tokens)
     times = [cpu_oracle_sample(w, inp, args.ref_tokens)["seconds"]
              for _ in range(max(1, args.steps))]
     sec_per_token = float(np.mean(times)) / args.ref_tokens
