@@ -120,8 +120,10 @@ moe_status moe_counts(const int32_t* expert_ids, int64_t n_ids, int E, int32_t* 
  * moe_counts_static - moe_counts without a workspace, for callers that
  * cannot allocate device memory at call time (a serving runtime that fixes
  * its memory footprint at start-up and forbids allocation afterwards, or a
- * plugin interface that hands an operator no scratch buffer). The pages have
- * no counterpart of this call; it exists for those callers only.
+ * plugin interface that hands an operator no scratch buffer). It computes
+ * the histc step of ep_mc2_forward ("NPU Training Operators - MC2", section
+ * "execution path", step 2) exactly as moe_counts does; the pages have no
+ * counterpart of the workspace-free form, which exists for those callers.
  *
  * Same arguments and results as moe_counts minus the workspace. The scratch
  * (per-chunk histograms and bases) lives in a fixed 512 KB array of device
@@ -275,8 +277,10 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
  * moe_expert_forward_from_logits - moe_expert_forward with the gate fused
  * in front: the routing comes from router logits through the kernel of
  * moe_route_topk, whose counts and offsets replace the block's own counting
- * step. y equals moe_expert_forward's on the expert_ids / probs written
- * here, bit for bit.
+ * step. This is the gate whose routing_weights and selected_experts the
+ * dispatcher call of "NPU Training Operators - MC2" (section "suggested
+ * configuration") takes. y equals moe_expert_forward's on the expert_ids /
+ * probs written here, bit for bit.
  *
  *  router_logits  float [T, E]
  *  expert_ids     int32 [T, k]  out (as moe_route_topk; the backward needs it)
@@ -355,7 +359,9 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
                                size_t ws_bytes, const moe_config* cfg, void* stream);
 
 /* ------------------------------------------------------------------------
- * moe_expert_forward_mxfp8 - the block with MXFP8 operands.
+ * moe_expert_forward_mxfp8 - the block with MXFP8 operands: the quantised
+ * AllToAll+Matmul of "MC2 通算融合架构总览" (section 1, MX FP8; scales in
+ * buffers of their own, section 5) on one GPU.
  * x arrives in bf16 and is quantised on the fly (per 32 along H) while it is
  * permuted; the weights arrive already quantised (moe_quantize_mxfp8) in a
  * K-contiguous layout so that each 32-block lies along the reduction:
@@ -381,7 +387,8 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
  * bf16 matrices (the transposed orientation of moe_quantize_mxfp8): for each
  * z < batch and column c of in[z] [rows, cols], the 32-row blocks of the
  * column become 32 consecutive codes of q[z][c] and one scale, by the rule
- * of moe_quantize_mxfp8. It turns the forward-layout weights into the
+ * of moe_quantize_mxfp8 (the MX FP8 of "MC2 通算融合架构总览", section 1,
+ * in OCP Microscaling v1.0 form). It turns the forward-layout weights into the
  * backward's: W1g, W1u [E, F, H] -> [E, H, F] quantised along F, and
  * W2 [E, H, F] -> [E, F, H] quantised along H.
  *  in      bf16 [batch, rows, cols]
@@ -396,7 +403,8 @@ moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int col
  * moe_quantize_mxfp8_dual - both orientations of a batch of bf16 matrices
  * from one read: q_rows [batch, rows, cols] with scales [batch, rows, cols/32]
  * as moe_quantize_mxfp8 gives them, and q_cols [batch, cols, rows] with
- * scales [batch, cols, rows/32] as moe_quantize_mxfp8_t gives them. A training
+ * scales [batch, cols, rows/32] as moe_quantize_mxfp8_t gives them, by the
+ * MX FP8 rule of "MC2 通算融合架构总览" (section 1). A training
  * step quantises its weights both ways: the forward's layout and the
  * backward's. rows % 32 == 0, cols % 128 == 0, 16-byte aligned pointers.
  * ------------------------------------------------------------------------ */
