@@ -19,8 +19,11 @@
 // for the backward; fc2 rounds O to bf16; dH applies the SwiGLU backward to
 // the saved A_g, A_u; F32 writes float rows (dXp) or weight-gradient rows
 // (reduce-added when accumulating). Rows leave through per-warp shared-memory
-// pieces and TMA tensor stores; only fc1's codes and scales are stored from
-// registers.
+// pieces and TMA tensor stores, except fc1's codes and scales and the bf16
+// tensors kept in 32 x 32 blocks (fc1's saves, dH's dA), which are stored
+// from registers. dH runs 12 warps with a register split (see reg_split).
+// This is the quantised AllToAll+Matmul (MX FP8) of "MC2 通算融合架构总览",
+// section 1, on one GPU, with its scales in buffers of their own (section 5).
 // Schedules: Rows (expert segments padded to 128 rows; M fastest within an
 // expert unless it has more M tiles than N tiles) and WGrad (K runs over one
 // expert's padded rows; every expert owns M/128 x N/bn output tiles, the

@@ -3,6 +3,12 @@
 // probability-weighted unpermute and the MXFP8 quantiser. All are bound by
 // HBM bandwidth (or latency, for the tiny count/scan kernels); rows move as
 // 16-byte vectors, one warp per token so that each warp streams whole rows.
+// They are the steps of ep_mc2_forward in "NPU Training Operators - MC2"
+// (section "execution path") on one GPU: step 2 histc (hist_kernel), steps
+// 4-5 (scan_kernel, send = receive = the local counts), step 6 permute
+// (rowmap_kernel + permute_copy_kernel) and step 10 unpermute; the gate
+// ahead of them is route_topk_kernel. The MXFP8 dispatch and quantisers
+// follow the MX FP8 of "MC2 通算融合架构总览", section 1.
 #include <climits>
 
 #include "common.cuh"
