@@ -112,3 +112,68 @@ def test_product_and_oracle_share_nothing():
     for p in glob.glob(os.path.join(ROOT, "oracle", "**", "*.py"), recursive=True):
         text = open(p, encoding="utf-8").read()
         assert "moe_expert_dispatch_gb300" not in text and "libmoe" not in text, p
+
+
+def test_host_side_argument_errors_of_every_entry_point(lib):
+    # each call is wrong in one way the host can see; it must answer with
+    # that status at once, before any device work (this machine has no GPU,
+    # so a call that reached the device would answer MOE_ERR_CUDA instead).
+    # P is a fake, aligned device address that no check dereferences; with a
+    # GPU present the test does not run, so a missing check could never hand
+    # such an address to a kernel.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only: the cases carry fake device addresses")
+    import moe_expert_dispatch_gb300 as m
+    L = m._lib
+    P = ctypes.c_void_p(1 << 20)
+    U = ctypes.c_void_p((1 << 20) + 8)      # not 16-byte aligned
+    c = m.config()
+    cs = m.config(save_for_backward=True)
+    INV, UNS, WS = 1, 2, 4
+    cases = [
+        ("counts: E = 0", INV, lambda: L.moe_counts(P, 10, 0, P, P, P, 1 << 20, None)),
+        ("counts: no workspace", WS, lambda: L.moe_counts(P, 10, 4, P, P, None, 0, None)),
+        ("route_topk: k = 0", INV, lambda: L.moe_route_topk(P, 4, 8, 0, P, P, P, P, P, 1 << 20, None)),
+        ("route_topk: k > E", INV, lambda: L.moe_route_topk(P, 4, 4, 5, P, P, P, P, P, 1 << 20, None)),
+        ("route_topk: workspace too small", WS,
+         lambda: L.moe_route_topk(P, 4, 8, 2, P, P, P, P, P, 16, None)),
+        ("permute: unaligned x", INV,
+         lambda: L.moe_permute(U, 4, 64, P, P, 2, 4, 1, P, P, P, P, P, P, P, 1 << 20, None)),
+        ("permute: no workspace", WS,
+         lambda: L.moe_permute(P, 4, 64, P, P, 2, 4, 1, P, P, P, P, P, P, None, 0, None)),
+        ("unpermute: H % 8 != 0", INV, lambda: L.moe_unpermute(P, P, P, 4, 2, 12, P, None)),
+        ("unpermute: k > 32", INV, lambda: L.moe_unpermute(P, P, P, 4, 33, 64, P, None)),
+        ("quantize: unaligned input", INV, lambda: L.moe_quantize_mxfp8(U, 4, 64, P, P, None)),
+        ("quantize_t: rows % 32 != 0", INV, lambda: L.moe_quantize_mxfp8_t(P, 1, 48, 64, P, P, None)),
+        ("quantize_dual: cols % 128 != 0", INV,
+         lambda: L.moe_quantize_mxfp8_dual(P, 1, 64, 96, P, P, P, P, None)),
+        ("permute_quantize: H % 32 != 0", INV,
+         lambda: L.moe_permute_quantize_mxfp8(P, 4, 48, P, 2, P, P, None)),
+        ("forward: F % 128 != 0", UNS,
+         lambda: L.moe_expert_forward(P, P, P, P, P, P, 4, 128, 100, 4, 2, P, P, 1 << 30,
+                                      ctypes.byref(c), None)),
+        ("forward: k > E", INV,
+         lambda: L.moe_expert_forward(P, P, P, P, P, P, 4, 128, 128, 2, 3, P, P, 1 << 30,
+                                      ctypes.byref(c), None)),
+        ("forward: workspace too small", WS,
+         lambda: L.moe_expert_forward(P, P, P, P, P, P, 4, 128, 128, 4, 2, P, P, 256,
+                                      ctypes.byref(c), None)),
+        ("forward_from_logits: no logits", INV,
+         lambda: L.moe_expert_forward_from_logits(P, P, P, P, None, 4, 128, 128, 4, 2, P, P, P,
+                                                  P, 1 << 30, ctypes.byref(c), None)),
+        ("pipelined: zero chunks", INV,
+         lambda: L.moe_expert_forward_pipelined(P, P, P, P, P, P, 4, 128, 128, 4, 2, P, 0, P,
+                                                1 << 30, ctypes.byref(c), P, U)),
+        ("pipelined: aux stream = stream", INV,
+         lambda: L.moe_expert_forward_pipelined(P, P, P, P, P, P, 4, 128, 128, 4, 2, P, 2, P,
+                                                1 << 30, ctypes.byref(c), P, P)),
+        ("backward: no weight gradients", INV,
+         lambda: L.moe_expert_backward(P, P, P, P, P, P, P, 4, 128, 128, 4, 2, P, 1 << 30, P,
+                                       None, None, None, P, 0, P, 1 << 30, ctypes.byref(cs), None)),
+        ("forward_mxfp8: no weights", INV,
+         lambda: L.moe_expert_forward_mxfp8(P, None, None, None, None, None, None, P, P, 4, 128,
+                                            128, 4, 2, P, P, 1 << 30, ctypes.byref(c), None)),
+    ]
+    for name, want, call in cases:
+        assert call() == want, name
