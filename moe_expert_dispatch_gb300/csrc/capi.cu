@@ -52,6 +52,9 @@ EncodeTiledFn encode_fn() {
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
+// T * k < limit for k >= 1, without forming a product that could overflow.
+bool rows_below(int64_t T, int k, int64_t limit) { return T <= (limit - 1) / k; }
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -213,7 +216,7 @@ moe_config cfg_or_default(const moe_config* c) {
 moe_status check_block_args(int64_t T, int H, int F, int E, int k) {
   if (T < 0 || H <= 0 || F <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK)
     return MOE_ERR_INVALID_ARG;
-  if (T * static_cast<int64_t>(k) >= (static_cast<int64_t>(1) << 31) - kTileM * kMaxExperts)
+  if (!rows_below(T, k, (static_cast<int64_t>(1) << 31) - kTileM * kMaxExperts))
     return MOE_ERR_INVALID_ARG;
   if (H % 128 != 0 || F % 128 != 0) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -365,7 +368,7 @@ moe_status moe_counts(const int32_t* ids, int64_t n_ids, int E, int32_t* counts,
 }
 
 size_t moe_route_topk_workspace_size(int64_t T, int k, int E) {
-  if (T < 0 || k < 1 || E < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || !rows_below(T, k, static_cast<int64_t>(1) << 31)) return 0;
   return route_scratch_bytes(T * k, E);
 }
 
@@ -373,7 +376,7 @@ moe_status moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t*
                           float* probs, int32_t* counts, int32_t* offsets, void* workspace,
                           size_t ws_bytes, void* stream) {
   if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK ||
-      T * static_cast<int64_t>(k) >= (static_cast<int64_t>(1) << 31))
+      !rows_below(T, k, static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
   if ((T > 0 && (!logits || !expert_ids || !probs)) || !counts || !offsets)
     return MOE_ERR_INVALID_ARG;
@@ -385,7 +388,7 @@ moe_status moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t*
 }
 
 size_t moe_permute_workspace_size(int64_t T, int k, int E) {
-  if (T < 0 || k < 1 || E < 1) return 0;
+  if (T < 0 || k < 1 || E < 1 || !rows_below(T, k, static_cast<int64_t>(1) << 31)) return 0;
   return route_scratch_bytes(T * k, E);
 }
 
@@ -394,7 +397,7 @@ moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_
                        int32_t* row_of, int32_t* token_of, float* prob_of, int32_t* offsets,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
   if (T < 0 || k < 1 || k > kMaxTopK || k > E || E > kMaxExperts || row_bytes <= 0 ||
-      row_bytes % 16 != 0 || row_align < 1 || T * k >= (static_cast<int64_t>(1) << 31))
+      row_bytes % 16 != 0 || row_align < 1 || !rows_below(T, k, static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !ids || !x_perm || !row_of || !token_of || !offsets || !counts)

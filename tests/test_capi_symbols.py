@@ -48,6 +48,13 @@ def test_host_side_queries(lib):
     assert m.moe_workspace_size(16, 128, 128, 4, 5) == 0     # k > E
     s = m._lib.moe_status_string(3)
     assert b"expert id" in s
+    # T * k past the int32 row space is refused, also where the product
+    # itself would overflow 64 bits
+    assert m._lib.moe_route_topk_workspace_size(1 << 62, 32, 64) == 0
+    assert m._lib.moe_permute_workspace_size(1 << 62, 32, 64) == 0
+    assert m.moe_workspace_size(1 << 62, 4096, 14336, 8, 2) == 0
+    assert m.moe_workspace_size(1 << 30, 4096, 14336, 8, 2) == 0     # 2^31 routed rows
+    assert m._lib.moe_route_topk_workspace_size(4096, 2, 8) > 0
 
 
 def test_invalid_arguments_rejected_before_any_launch(lib):
