@@ -28,6 +28,10 @@
  *    wait that ran out of time) set a device error word and the affected work
  *    stops early; moe_get_error() reports them. Nothing traps.
  *  - T = 0 (no tokens) is valid and launches nothing.
+ *  - Host threads: the first call of each entry point on a device sets that
+ *    kernel's shared-memory attribute and caches device addresses, without a
+ *    lock. Make one call per device from one thread (or before any stream
+ *    capture) before calling from several threads at once.
  */
 #ifndef MOE_EXPERT_H
 #define MOE_EXPERT_H
