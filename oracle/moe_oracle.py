@@ -41,9 +41,11 @@ the definition:
 Readings where the pages are silent (listed with the rest in the design
 notes): h rounded to bf16 (A_g, A_u not rounded in the forward); O rounded to
 bf16 before the combine; the combine sums j in order, then rounds once;
-backward uses A_g, A_u as saved in bf16 and keeps dXp unrounded (it feeds no
-further matmul; dX = bf16 of its k-way sum); dW is float (here float64, on
-the GPU float32); in MXFP8 mode h is first rounded to bf16 then quantised per 32
+backward uses A_g, A_u as saved in bf16 and rounds dXp to bf16, because, like
+O in the forward, it is a tensor of its own between two ops (the grouped
+matmul's backward and the permute's backward); dX = bf16 of the float sum of
+a token's k rows of dXp, rounded once; dW is float (here float64, on the GPU
+float32); in MXFP8 mode h is first rounded to bf16 then quantised per 32
 along F.
 
 Every function here is pinned by tests against something other than itself
@@ -326,14 +328,15 @@ def expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, rounding: bo
       dH     = dO_e W2_e^T
       dA_g   = bf16(dH * A_u * sigma(A_g) (1 + A_g (1 - sigma(A_g))))
       dA_u   = bf16(dH * silu(A_g))
-      dXp    = dA_g W1g_e^T + dA_u W1u_e^T        (not rounded)
+      dXp    = bf16(dA_g W1g_e^T + dA_u W1u_e^T)
       dW2_e  = h_e^T dO_e,  dW1g_e = Xp_e^T dA_g,e,  dW1u_e = Xp_e^T dA_u,e
       dX_t   = bf16(sum_j dXp[row_of[t, j]])
 
     With rounding, A_g and A_u enter as bf16 (as saved by the forward).
     With rounding=False every bf16() is the identity: the exact gradient of
     the unrounded forward, which the finite-difference test checks.
-    Returns dict(dx, dw_gate, dw_up, dw_down, dprobs).
+    Returns dict(dx, dw_gate, dw_up, dw_down, dprobs, y), plus the rows of
+    dXp (dxp, in permuted order) and row_of.
     """
     E = len(w_gate)
     rnd = bf16 if rounding else (lambda v: _f64(v))
@@ -362,16 +365,18 @@ def expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, rounding: bo
         sg = sigmoid(a_g[lo:hi])
         da_g = rnd(dh * a_u[lo:hi] * sg * (1.0 + a_g[lo:hi] * (1.0 - sg)))
         da_u = rnd(dh * a_g[lo:hi] * sg)
-        dxp[lo:hi] = da_g @ _f64(w_gate[e]).T + da_u @ _f64(w_up[e]).T
+        dxp[lo:hi] = rnd(da_g @ _f64(w_gate[e]).T + da_u @ _f64(w_up[e]).T)
         dw_down[e] = h[lo:hi].T @ d_o[lo:hi]
         dw_gate[e] = xp[lo:hi].T @ da_g
         dw_up[e] = xp[lo:hi].T @ da_u
     dx = unpermute(dxp, row_of, None, rounding)
-    return dict(dx=dx, dw_gate=dw_gate, dw_up=dw_up, dw_down=dw_down, dprobs=dprobs, y=y)
+    return dict(dx=dx, dw_gate=dw_gate, dw_up=dw_up, dw_down=dw_down, dprobs=dprobs, y=y,
+                dxp=dxp, row_of=row_of)
 
 
-def backward_rows(dy, x, w_gate, w_up, w_down, expert_ids, probs, tokens):
-    """dX and dprobs of the listed tokens only (rounding as expert_backward).
+def backward_rows(dy, x, w_gate, w_up, w_down, expert_ids, probs, tokens, with_rows=False):
+    """dX and dprobs of the listed tokens only (rounding as expert_backward);
+    with_rows adds their dXp rows, [len(tokens), k, H], slot by slot.
 
     Each token's gradient depends only on its own rows, so this is the same
     arithmetic as expert_backward restricted to those rows; it lets the
@@ -402,7 +407,7 @@ def backward_rows(dy, x, w_gate, w_up, w_down, expert_ids, probs, tokens):
                 sg = sigmoid(ga)
                 da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
                 da_u = bf16(dh * ga * sg)
-                dxr[(t, j)] = wg @ da_g + wu @ da_u
+                dxr[(t, j)] = bf16(wg @ da_g + wu @ da_u)
     k = ids.shape[1]
     dx, dp = [], []
     for t in tokens:
@@ -411,6 +416,9 @@ def backward_rows(dy, x, w_gate, w_up, w_down, expert_ids, probs, tokens):
             acc = acc + dxr[(t, j)]
         dx.append(bf16(acc))
         dp.append([dpt[(t, j)] for j in range(k)])
+    if with_rows:
+        rows = np.stack([np.stack([dxr[(t, j)] for j in range(k)]) for t in tokens])
+        return np.stack(dx), np.array(dp), rows
     return np.stack(dx), np.array(dp)
 
 
@@ -484,12 +492,19 @@ def e4m3_encode(v) -> np.ndarray:
 def e8m0_scale_code(amax) -> np.ndarray:
     """Shared scale of one block: X = 2^(floor(log2(amax)) - 8), the
     exponent clamped to E8M0's [-127, 127]; code = exponent + 127. A block of
-    zeros gets the smallest scale, 2^-127 (code 0)."""
+    zeros gets the smallest scale, 2^-127 (code 0). A block holding an
+    infinity or a NaN (amax not finite) has no such exponent: it gets 255,
+    the E8M0 NaN, so that the whole block decodes to NaN."""
     amax = _f64(amax)
-    with np.errstate(divide="ignore"):
-        ex = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))), -np.inf)
+    live = np.isfinite(amax) & (amax > 0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ex = np.where(live, np.floor(np.log2(np.where(live, amax, 1.0))), -np.inf)
     ex = np.clip(ex - E4M3_EMAX, -127, 127)
-    return (ex + 127).astype(np.uint8)
+    return np.where(np.isfinite(amax), ex + 127, 255).astype(np.uint8)
+
+
+E8M0_NAN = 255
+E4M3_NAN = 0x7F
 
 
 _E4M3_TABLE = None
@@ -505,7 +520,8 @@ def _e4m3_table() -> np.ndarray:
 def quantize_mxfp8(a):
     """Quantise the last axis in blocks of 32: per block the E8M0 scale code
     from its amax, then each element E4M3(v / X). Returns (codes uint8 of a's
-    shape, scale codes uint8 of shape [..., K/32]).
+    shape, scale codes uint8 of shape [..., K/32]). A block holding an
+    infinity or a NaN gets the NaN scale code and E4M3 NaN (0x7F) elements.
 
     v / X is a power-of-two scaling, exact for bf16-valued inputs, so the
     only rounding is the E4M3 one. That rounding step uses torch's
@@ -518,9 +534,12 @@ def quantize_mxfp8(a):
     assert K % MX_BLOCK == 0
     blocks = a.reshape(a.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
     sc = e8m0_scale_code(np.abs(blocks).max(axis=-1))
-    x_scale = np.ldexp(1.0, sc.astype(np.int64) - 127)
-    scaled = np.clip(blocks / x_scale[..., None], -E4M3_MAX, E4M3_MAX).astype(np.float32)
+    bad = sc == E8M0_NAN
+    x_scale = np.ldexp(1.0, np.where(bad, 127, sc.astype(np.int64)) - 127)
+    with np.errstate(invalid="ignore"):
+        scaled = np.clip(blocks / x_scale[..., None], -E4M3_MAX, E4M3_MAX).astype(np.float32)
     codes = torch.from_numpy(scaled).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    codes = np.where(bad[..., None], np.uint8(E4M3_NAN), codes)
     return codes.reshape(a.shape), sc
 
 
@@ -528,7 +547,8 @@ def dequantize_mxfp8(codes, scales):
     codes = np.asarray(codes)
     K = codes.shape[-1]
     vals = _e4m3_table()[codes].reshape(codes.shape[:-1] + (K // MX_BLOCK, MX_BLOCK))
-    x_scale = np.ldexp(1.0, np.asarray(scales).astype(np.int64) - 127)
+    sc = np.asarray(scales).astype(np.int64)
+    x_scale = np.where(sc == E8M0_NAN, np.nan, np.ldexp(1.0, np.minimum(sc, 254) - 127))
     return (vals * x_scale[..., None]).reshape(codes.shape)
 
 
@@ -647,7 +667,7 @@ def expert_backward_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs,
       dO        bf16(p dY_t), one row per routed slot; dp_tj = <dY_t, O_row>
       dH        deq(dO along H) deq(W2_e as [F, H], along H)^T
       dA_g, dA_u  the SwiGLU backward of dH on A_g, A_u as saved (bf16)
-      dXp       deq(dA_g along F) deq(W1g_e as [H, F], along F)^T + the same for up
+      dXp       bf16(deq(dA_g along F) deq(W1g_e as [H, F], along F)^T + the same for up)
       dX        bf16(sum_j dXp[row_of[t, j]])
       dW1g_e^T  deq(dA_g,e along rows)^T deq(Xp_e along rows)   [F, H]
       dW1u_e^T  the same with dA_u,e
@@ -709,8 +729,8 @@ def expert_backward_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs,
         sg = sigmoid(ag_s[lo:hi])
         da_g = bf16(dh * au_s[lo:hi] * sg * (1.0 + ag_s[lo:hi] * (1.0 - sg)))
         da_u = bf16(dh * ag_s[lo:hi] * sg)
-        dxp[lo:hi] = (q_rows(da_g) @ q_rows(_f64(w_gate_t[e]).T).T +
-                      q_rows(da_u) @ q_rows(_f64(w_up_t[e]).T).T)
+        dxp[lo:hi] = bf16(q_rows(da_g) @ q_rows(_f64(w_gate_t[e]).T).T +
+                          q_rows(da_u) @ q_rows(_f64(w_up_t[e]).T).T)
         xq_e = q_cols(xp[lo:hi])
         dw_gate_t[e] = q_cols(da_g).T @ xq_e
         dw_up_t[e] = q_cols(da_u).T @ xq_e
@@ -759,8 +779,8 @@ def backward_rows_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, to
                 sg = sigmoid(ga)
                 da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
                 da_u = bf16(dh * ga * sg)
-                dxr[(t, j)] = (w1gb @ quantized_along_rows(da_g) +
-                               w1ub @ quantized_along_rows(da_u))
+                dxr[(t, j)] = bf16(w1gb @ quantized_along_rows(da_g) +
+                                   w1ub @ quantized_along_rows(da_u))
     k = ids.shape[1]
     dx, dp = [], []
     for t in tokens:
@@ -808,6 +828,47 @@ def weight_grad_entries_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, pro
         out.append((float(np.dot(q_col(da_g), xh)), float(np.dot(q_col(da_u), xh)),
                     float(np.dot(q_col(d_o[:, h]), q_col(hv)))))
     return np.array(out).reshape(len(pairs), 3)
+
+
+def weight_grad_slices_mxfp8(dy, x, w_gate_t, w_up_t, w_down_t, expert_ids, probs, e, f_cols):
+    """Whole slices of expert e's weight gradients in expert_backward_mxfp8,
+    for each f in f_cols: the rows dw_gate_t[e][f, :] and dw_up_t[e][f, :]
+    and the column dw_down_t[e][:, f], each over all H.
+
+    They need column f of A_g, A_u, h and dH over the expert's routed rows
+    (row f of the quantised weights) and the column-quantised Xp_e and dO_e
+    [rows, H], so the [rows, F] tensors are never formed. Returns a dict of
+    [len(f_cols), H] arrays."""
+    dy, x = np.asarray(dy), np.asarray(x)
+    ids = np.asarray(expert_ids)
+    pr = np.asarray(probs)
+    E = len(w_gate_t)
+    counts = expert_counts(ids, E)
+    off = expert_offsets(counts)
+    _, token_of, slot_of = permute_map(ids, E)
+    lo, hi = int(off[e]), int(off[e + 1])
+    toks = token_of[lo:hi]
+    xe = _f64(x[toks])
+    xd = quantized_along_rows(xe)                        # fc1's A: along H
+    xq_cols = quantized_along_columns(xe)                # dW1's B: along the rows
+    d_o = bf16(_f64(pr[toks, slot_of[lo:hi]])[:, None] * _f64(dy[toks]))
+    d_oq = quantized_along_rows(d_o)                     # dH's A: along H
+    do_cols = quantized_along_columns(d_o)               # dW2's A: along the rows
+    q_col = lambda v: quantized_along_columns(np.asarray(v)[:, None])[:, 0]  # noqa: E731
+    out = {"dw_gate_t": [], "dw_up_t": [], "dw_down_t": []}
+    for f in f_cols:
+        a_g = xd @ quantized_along_rows(w_gate_t[e][f])
+        a_u = xd @ quantized_along_rows(w_up_t[e][f])
+        hv = bf16(silu(a_g) * a_u)
+        dh = d_oq @ quantized_along_rows(_f64(w_down_t[e])[:, f])
+        ga, ua = bf16(a_g), bf16(a_u)
+        sg = sigmoid(ga)
+        da_g = bf16(dh * ua * sg * (1.0 + ga * (1.0 - sg)))
+        da_u = bf16(dh * ga * sg)
+        out["dw_gate_t"].append(q_col(da_g) @ xq_cols)
+        out["dw_up_t"].append(q_col(da_u) @ xq_cols)
+        out["dw_down_t"].append(q_col(hv) @ do_cols)
+    return {key: np.array(v) for key, v in out.items()}
 
 
 # --------------------------------------------------------------------------
