@@ -27,7 +27,11 @@
  *    Errors found on the device (an expert id outside [0, E), an in-kernel
  *    wait that ran out of time) set a device error word and the affected work
  *    stops early; moe_get_error() reports them. Nothing traps.
- *  - T = 0 (no tokens) is valid and launches nothing.
+ *  - T = 0 (no tokens) is valid. The block's calls then launch nothing, or
+ *    only what writes outputs that do not depend on the tokens: the counting
+ *    calls (moe_counts, moe_counts_static, moe_route_topk) still write zero
+ *    counts and offsets, and the backward writes zero weight gradients (or
+ *    leaves them as they were when accumulating).
  *  - Host threads: the first call of each entry point on a device sets that
  *    kernel's shared-memory attribute and caches device addresses, without a
  *    lock. Make one call per device from one thread (or before any stream
@@ -338,10 +342,12 @@ moe_status moe_expert_forward_pipelined(const void* x, const void* w_gate, const
  * backward; its section "validation items" compares the fc1/fc2 gradients.
  *   dO_r  = bf16(p_r dY_t(r));          dprobs[t,j] = <dY_t, O_row(t,j)>
  *   dH    = dO_e W2_e^T (float);        dA_g = bf16(dH A_u silu'(A_g)),
- *   dA_u  = bf16(dH silu(A_g));         dXp = dA_g W1g_e^T + dA_u W1u_e^T (float)
+ *   dA_u  = bf16(dH silu(A_g));         dXp = bf16(dA_g W1g_e^T + dA_u W1u_e^T)
  *   dW2_e = h_e^T dO_e, dW1g_e = Xp_e^T dA_g, dW1u_e = Xp_e^T dA_u (float)
- *   dX_t  = bf16(sum_j dXp[row_of[t, j]]), j in order
- * A_g and A_u enter as saved by the forward (bf16).
+ *   dX_t  = bf16(sum_j dXp[row_of[t, j]]), j in order, summed in float
+ * A_g and A_u enter as saved by the forward (bf16). dXp, like O in the
+ * forward, is a tensor of its own between two of the page's ops (the
+ * grouped matmul's backward and the permute's backward), so it is bf16.
  *
  *  dy          bf16 [T, H]
  *  fwd_ws      the workspace of a forward call made with save_for_backward=1
@@ -425,8 +431,8 @@ moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int 
  *   dO_r = bf16(p_r dY_t(r)), dprobs[t,j] = <dY_t, O_row(t,j)> (float)
  *   dH   = deq(dO along H) deq(W2 as [F, H], along H)^T (float)
  *   dA_g, dA_u = the SwiGLU backward of dH on A_g, A_u as saved (bf16)
- *   dXp  = deq(dA_g along F) deq(W1g as [H, F], along F)^T + the same for up
- *   dX_t = bf16(sum_j dXp[row_of[t, j]]), j in order
+ *   dXp  = bf16(deq(dA_g along F) deq(W1g as [H, F], along F)^T + the same for up)
+ *   dX_t = bf16(sum_j dXp[row_of[t, j]]), j in order, summed in float
  *   dW1g^T_e = deq(dA_g,e)^T deq(Xp_e), dW1u^T_e likewise, dW2^T_e =
  *   deq(dO_e)^T deq(h_e) (float), where the routed rows of expert e
  *   (Xp = bf16 x, h, dO, dA) are quantised along the rows in blocks of 32

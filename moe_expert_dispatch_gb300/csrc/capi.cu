@@ -92,7 +92,8 @@ FwdLayout fwd_layout(int64_t T, int H, int F, int E, int k, bool save) {
 }
 
 // Backward workspace: dO [cap, H] and dA = [dA_g | dA_u] [cap, 2F] in bf16 (GEMM
-// operands), dXp [cap, H] in float (summed into dX, then rounded once).
+// operands), dXp [cap, H] in bf16 (a token's k rows summed in float into dX,
+// then rounded once).
 struct BwdLayout {
   int64_t cap;
   size_t d_o, d_a, d_xp, total;
@@ -109,7 +110,7 @@ BwdLayout bwd_layout(int64_t T, int H, int F, int E, int k) {
   };
   B.d_o = take(static_cast<size_t>(B.cap) * H * 2);
   B.d_a = take(static_cast<size_t>(B.cap) * F * 2 * 2);
-  B.d_xp = take(static_cast<size_t>(B.cap) * H * 4);
+  B.d_xp = take(static_cast<size_t>(B.cap) * H * 2);
   B.total = cur;
   return B;
 }
@@ -159,7 +160,7 @@ MxLayout mx_layout(int64_t T, int H, int F, int E, int k, bool save = false) {
 // MXFP8 backward workspace. Row-quantised operands of the data-gradient GEMMs
 // (dO along H, dA along 2F) and column-quantised operands of the weight
 // gradients ([C, cap], K = the padded rows), each with tiled scales; dXp in
-// float; the weights' backward-orientation scales in the tiled layout.
+// bf16; the weights' backward-orientation scales in the tiled layout.
 struct MxBwdLayout {
   int64_t cap;
   size_t d_o, doq, dos, doT, dots, d_a, daq, das, daT, dats, d_xp, xpT, xpts, hT, hts, w2_st,
@@ -186,7 +187,7 @@ MxBwdLayout mx_bwd_layout(int64_t T, int H, int F, int E, int k) {
   L.das = take(cap * 2 * F / 32);
   L.daT = take(cap * 2 * F);
   L.dats = take(cap * 2 * F / 32);
-  L.d_xp = take(cap * H * 4);
+  L.d_xp = take(cap * H * 2);
   L.xpT = take(cap * H);
   L.xpts = take(cap * H / 32);
   L.hT = take(cap * F);
@@ -333,6 +334,7 @@ const char* moe_status_string(moe_status s) {
 }
 
 moe_status moe_get_error(void* stream) {
+  MOE_ENTRY_RANGE();
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
@@ -358,6 +360,7 @@ size_t moe_counts_workspace_size(int64_t n_ids, int E) {
 
 moe_status moe_counts(const int32_t* ids, int64_t n_ids, int E, int32_t* counts, int32_t* offsets,
                       void* workspace, size_t ws_bytes, void* stream) {
+  MOE_ENTRY_RANGE();
   if (n_ids < 0 || E < 1 || E > kMaxExperts || n_ids >= (static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
   if ((n_ids > 0 && !ids) || !counts || !offsets) return MOE_ERR_INVALID_ARG;
@@ -375,6 +378,7 @@ size_t moe_route_topk_workspace_size(int64_t T, int k, int E) {
 moe_status moe_route_topk(const float* logits, int64_t T, int E, int k, int32_t* expert_ids,
                           float* probs, int32_t* counts, int32_t* offsets, void* workspace,
                           size_t ws_bytes, void* stream) {
+  MOE_ENTRY_RANGE();
   if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK ||
       !rows_below(T, k, static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
@@ -396,6 +400,7 @@ moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_
                        const float* probs, int k, int E, int row_align, void* x_perm,
                        int32_t* row_of, int32_t* token_of, float* prob_of, int32_t* offsets,
                        int32_t* counts, void* workspace, size_t ws_bytes, void* stream) {
+  MOE_ENTRY_RANGE();
   if (T < 0 || k < 1 || k > kMaxTopK || k > E || E > kMaxExperts || row_bytes <= 0 ||
       row_bytes % 16 != 0 || row_align < 1 || !rows_below(T, k, static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
@@ -421,6 +426,7 @@ moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_
 
 moe_status moe_unpermute(const void* o_perm, const int32_t* row_of, const float* probs, int64_t T,
                          int k, int H, void* y, void* stream) {
+  MOE_ENTRY_RANGE();
   if (T < 0 || k < 1 || k > kMaxTopK || H <= 0 || H % 8 != 0) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!o_perm || !row_of || !y || !aligned16(o_perm) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
@@ -431,6 +437,7 @@ moe_status moe_unpermute(const void* o_perm, const int32_t* row_of, const float*
 
 moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, uint8_t* scales,
                               void* stream) {
+  MOE_ENTRY_RANGE();
   if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
   if (rows == 0) return MOE_OK;
   if (!in || !q || !scales || !aligned16(in) || !aligned16(q)) return MOE_ERR_INVALID_ARG;
@@ -440,6 +447,7 @@ moe_status moe_quantize_mxfp8(const void* in, int64_t rows, int K, uint8_t* q, u
 
 moe_status moe_permute_quantize_mxfp8(const void* x, int64_t T, int H, const int32_t* row_of,
                                       int k, uint8_t* xq, uint8_t* xs, void* stream) {
+  MOE_ENTRY_RANGE();
   if (T < 0 || H <= 0 || H % 32 != 0 || k < 1 || k > kMaxTopK) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !row_of || !xq || !xs || !aligned16(x) || reinterpret_cast<uintptr_t>(xq) % 8 != 0)
@@ -645,6 +653,7 @@ moe_status moe_expert_forward(const void* x, const void* w_gate, const void* w_u
                               const void* w_down, const int32_t* expert_ids, const float* probs,
                               int64_t T, int H, int F, int E, int k, void* y, void* workspace,
                               size_t ws_bytes, const moe_config* cfg, void* stream) {
+  MOE_ENTRY_RANGE();
   return expert_forward_impl(x, w_gate, w_up, w_down, expert_ids, probs, nullptr, nullptr, nullptr,
                              T, H, F, E, k, y, workspace, ws_bytes, cfg, stream);
 }
@@ -655,6 +664,7 @@ moe_status moe_expert_forward_from_logits(const void* x, const void* w_gate, con
                                           int32_t* expert_ids, float* probs, void* y,
                                           void* workspace, size_t ws_bytes,
                                           const moe_config* cfg, void* stream) {
+  MOE_ENTRY_RANGE();
   if (T > 0 && !router_logits) return MOE_ERR_INVALID_ARG;
   return expert_forward_impl(x, w_gate, w_up, w_down, nullptr, nullptr, router_logits, expert_ids,
                              probs, T, H, F, E, k, y, workspace, ws_bytes, cfg, stream);
@@ -671,6 +681,7 @@ moe_status moe_expert_forward_pipelined(const void* x, const void* w_gate, const
                                         const float* probs, int64_t T, int H, int F, int E, int k,
                                         void* y, int n_chunks, void* workspace, size_t ws_bytes,
                                         const moe_config* cfg, void* stream, void* aux_stream) {
+  MOE_ENTRY_RANGE();
   FwdRun base{};
   moe_status s = fwd_prepare(base, x, w_gate, w_up, w_down, expert_ids, probs, nullptr, nullptr,
                              nullptr, T, H, F, E, k, y, cfg);
@@ -737,6 +748,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
                                size_t fwd_ws_bytes, void* dx, float* dw_gate, float* dw_up,
                                float* dw_down, float* dprobs, int accumulate_dw, void* workspace,
                                size_t ws_bytes, const moe_config* cfg, void* stream) {
+  MOE_ENTRY_RANGE();
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (!w_gate || !w_up || !w_down || !dw_gate || !dw_up || !dw_down) return MOE_ERR_INVALID_ARG;
@@ -775,7 +787,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   const __nv_bfloat16* au = at<__nv_bfloat16>(fw, L.au);
   __nv_bfloat16* d_o = at<__nv_bfloat16>(workspace, B.d_o);
   __nv_bfloat16* d_a = at<__nv_bfloat16>(workspace, B.d_a);
-  float* d_xp = at<float>(workspace, B.d_xp);
+  __nv_bfloat16* d_xp = at<__nv_bfloat16>(workspace, B.d_xp);
   const int grid = grid_size(c);
   const int bnF = (F % 256 == 0) ? 256 : 128;
   const int bnH = (H % 256 == 0) ? 256 : 128;
@@ -833,7 +845,7 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   GemmOut oh, ox, ow1, ow2;
   if (!make_out_tmap(&oh.map[0], d_a, 2 * static_cast<uint64_t>(F), B.cap,
                      static_cast<uint64_t>(F) * 4, false) ||
-      !make_out_tmap(&ox.map[0], d_xp, H, B.cap, static_cast<uint64_t>(H) * 4, true) ||
+      !make_out_tmap(&ox.map[0], d_xp, H, B.cap, static_cast<uint64_t>(H) * 2, false) ||
       !make_out_tmap(&ow1.map[0], dw_gate, F, static_cast<uint64_t>(E) * H,
                      static_cast<uint64_t>(F) * 4, true) ||
       !make_out_tmap(&ow1.map[1], dw_up, F, static_cast<uint64_t>(E) * H,
@@ -848,7 +860,8 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   if (launch_dh_swiglu_bwd(t_do, t_w2k, oh, gh, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(2);
 
-  // dXp = dA_g W1g^T + dA_u W1u^T (one reduction over 2F), then dX = sum_j dXp[row_of]
+  // dXp = bf16(dA_g W1g^T + dA_u W1u^T) (one reduction over 2F), then
+  // dX = bf16(sum_j dXp[row_of]), the combine with unit weights
   GroupedGemmArgs gx = g;
   gx.K = 2 * F;
   gx.N = H;
@@ -856,12 +869,12 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gx.b_rows = H;
   gx.b_split = 2;
   gx.k_split = F / 64;
-  gx.outf = d_xp;
+  gx.out = d_xp;
   gx.ldo = H;
   gx.keep_a = keep(static_cast<uint64_t>(T) * k * F * 4);
   if (launch_dxp(t_da, t_wgk, t_wuk, ox, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
-  if (launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
+  if (launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   mark(4);
@@ -905,6 +918,7 @@ size_t moe_workspace_size_mxfp8_backward(int64_t T, int H, int F, int E, int k) 
 moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int cols,
                                    uint8_t* q_rows, uint8_t* s_rows, uint8_t* q_cols,
                                    uint8_t* s_cols, void* stream) {
+  MOE_ENTRY_RANGE();
   if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 128 != 0)
     return MOE_ERR_INVALID_ARG;
   if (batch == 0) return MOE_OK;
@@ -919,6 +933,7 @@ moe_status moe_quantize_mxfp8_dual(const void* in, int64_t batch, int rows, int 
 
 moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int cols, uint8_t* q,
                                 uint8_t* scales, void* stream) {
+  MOE_ENTRY_RANGE();
   if (batch < 0 || rows <= 0 || cols <= 0 || rows % 32 != 0 || cols % 8 != 0)
     return MOE_ERR_INVALID_ARG;
   if (batch == 0) return MOE_OK;
@@ -935,6 +950,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
                                     const float* probs, int64_t T, int H, int F, int E, int k,
                                     void* y, void* workspace, size_t ws_bytes,
                                     const moe_config* cfg, void* stream) {
+  MOE_ENTRY_RANGE();
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
@@ -1063,6 +1079,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
                                      float* dw_gate_t, float* dw_up_t, float* dw_down_t,
                                      float* dprobs, int accumulate_dw, void* workspace,
                                      size_t ws_bytes, const moe_config* cfg, void* stream) {
+  MOE_ENTRY_RANGE();
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (!dw_gate_t || !dw_up_t || !dw_down_t || !aligned16(dw_gate_t) || !aligned16(dw_up_t) ||
@@ -1105,7 +1122,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   const int64_t cap = B.cap;
   __nv_bfloat16* d_o = at<__nv_bfloat16>(ws, B.d_o);
   __nv_bfloat16* d_a = at<__nv_bfloat16>(ws, B.d_a);
-  float* d_xp = at<float>(ws, B.d_xp);
+  __nv_bfloat16* d_xp = at<__nv_bfloat16>(ws, B.d_xp);
   const int grid = grid_size(c);
   auto bn_for = [&](int n) {      // MMA N: the configured width when it divides n
     const int want = (c.mxfp8_tile_n == 128 || c.mxfp8_tile_n == 256) ? c.mxfp8_tile_n : 256;
@@ -1184,8 +1201,8 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
     return MOE_ERR_CUDA;
   mark(3);
 
-  // dXp = deq(dA_g) deq(W1g)^T + deq(dA_u) deq(W1u)^T: K = 2F, the first F
-  // from W1g, the second from W1u; float rows
+  // dXp = bf16(deq(dA_g) deq(W1g)^T + deq(dA_u) deq(W1u)^T): K = 2F, the
+  // first F from W1g, the second from W1u
   g = base;
   g.K = 2 * F;
   g.N = H;
@@ -1198,13 +1215,13 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   g.sfb = at<uint8_t>(ws, B.w1g_st);
   g.sfb1 = at<uint8_t>(ws, B.w1u_st);
   GemmOut ox;
-  if (!make_out_tmap(&ox.map[0], d_xp, H, cap, static_cast<uint64_t>(H) * 4, true))
+  if (!make_out_tmap(&ox.map[0], d_xp, H, cap, static_cast<uint64_t>(H) * 2, false))
     return MOE_ERR_CUDA;
   ox.map[1] = ox.map[2] = ox.map[0];
   g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
   if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st))) return MOE_ERR_CUDA;
   mark(4);
-  if (!ok(launch_unpermute_f32(d_xp, row_of, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
+  if (!ok(launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
     return MOE_ERR_CUDA;
   mark(5);
 

@@ -50,6 +50,7 @@ using namespace moe;
 
 extern "C" moe_status moe_counts_static(const int32_t* ids, int64_t n_ids, int E, int32_t* counts,
                                         int32_t* offsets, void* stream) {
+  MOE_ENTRY_RANGE();
   if (n_ids < 0 || E < 1 || E > kMaxExperts || n_ids >= (static_cast<int64_t>(1) << 31))
     return MOE_ERR_INVALID_ARG;
   if ((n_ids > 0 && !ids) || !counts || !offsets) return MOE_ERR_INVALID_ARG;

@@ -637,7 +637,7 @@ cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2, co
 
 cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                        const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_impl<Epi::F32, false, false, Sched::Rows>(a, wg, wu, o, p, grid, st);
+  return launch_impl<Epi::Bf16, false, false, Sched::Rows>(a, wg, wu, o, p, grid, st);
 }
 
 cudaError_t launch_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,

@@ -16,8 +16,8 @@
 //     FP8 rate 4 slots in flight per SM do not cover the L2 latency.
 // Epilogues (MxEpi): fc1 rounds h to bf16 and quantises it per 32 along F
 // (codes + tiled scales for fc2), optionally saving A_g, A_u and h in bf16
-// for the backward; fc2 rounds O to bf16; dH applies the SwiGLU backward to
-// the saved A_g, A_u; F32 writes float rows (dXp) or weight-gradient rows
+// for the backward; fc2 and dXp round their rows to bf16; dH applies the
+// SwiGLU backward to the saved A_g, A_u; F32 writes weight-gradient rows
 // (reduce-added when accumulating). Rows leave through per-warp shared-memory
 // pieces and TMA tensor stores, except fc1's codes and scales and the bf16
 // tensors kept in 32 x 32 blocks (fc1's saves, dH's dA), which are stored
@@ -602,8 +602,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           }
         }
       } else {
-        // float rows, 16 columns per piece: dXp (Rows) or a weight-gradient
-        // row (WGrad; the expert's rows below out_split go to map 0 at row
+        // float rows, 16 columns per piece: a weight-gradient row (WGrad;
+        // the expert's rows below out_split go to map 0 at row
         // e * out_split + r, the rest to map 1 at e * (M - out_split) + r -
         // out_split; out_split is a multiple of 128, so a tile is on one side)
         const CUtensorMap* map = &tmO0;
@@ -715,7 +715,7 @@ cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const Gemm
 
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::F32, Sched::Rows>(a, w1g, w1u, o, p, grid, st);
+  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, w1g, w1u, o, p, grid, st);
 }
 
 cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,

@@ -5,10 +5,22 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace moe {
+
+// An NVTX range named after the entry point around each C-ABI call, so that
+// a profiler's timeline groups every launch under the call that made it.
+// Without a tool attached a push or pop costs a few nanoseconds.
+struct ScopedRange {
+  explicit ScopedRange(const char* name) { nvtxRangePushA(name); }
+  ~ScopedRange() { nvtxRangePop(); }
+  ScopedRange(const ScopedRange&) = delete;
+  ScopedRange& operator=(const ScopedRange&) = delete;
+};
+#define MOE_ENTRY_RANGE() ::moe::ScopedRange moe_entry_range_(__func__)
 
 // Ids handled by one CTA of the histogram and row-map kernels.
 constexpr int kRouteChunk = 2048;
@@ -67,10 +79,6 @@ cudaError_t launch_zero_padding(const int32_t* counts, const int32_t* off_al, in
 cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
                              int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st);
 
-// dX[t] = bf16(sum_j dxp[row_of[t, j]]) over float rows (j in order).
-cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_t T, int k, int H,
-                                 __nv_bfloat16* dx, cudaStream_t st);
-
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
                                   uint8_t* scales, cudaStream_t st);
 // The same with the scales in the MMA's tiled layout (rows % 128 == 0,
@@ -114,8 +122,7 @@ enum class Epi {
   SwigluFwd,  // fc1: out = bf16(silu(gate) * up); gate/up are the two halves of the N tile
   Bf16,       // out = bf16(acc)
   SwigluBwd,  // dH -> dA_g, dA_u (bf16) from the saved A_g, A_u
-  F32,        // float output: rows (Rows schedule) or weight gradients (WGrad), optionally
-              // accumulated
+  F32,        // float output: weight gradients (WGrad), optionally accumulated
 };
 // Tile schedule: M tiles over the routed rows of each expert (fixed K), or
 // over the rows of each expert's weight gradient (K = the expert's rows).
@@ -182,7 +189,7 @@ cudaError_t launch_fc2(const CUtensorMap& a, const CUtensorMap& w, const GemmOut
 // dA_g and dA_u into one [rows, 2F] tensor (map 0, columns [0, F) and [F, 2F)).
 cudaError_t launch_dh_swiglu_bwd(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
                                  const GroupedGemmArgs& p, int grid, cudaStream_t st);
-// backward: dXp = [dA_g | dA_u] [W1g ; W1u]^T in float (K split between the two weights).
+// backward: dXp = bf16([dA_g | dA_u] [W1g ; W1u]^T) (K split between the two weights).
 cudaError_t launch_dxp(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                        const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st);
 // backward: dW_e = A_e^T B_e over each expert's rows, both operands MN-major;
@@ -217,9 +224,8 @@ cudaError_t launch_tile_scales(const uint8_t* src0, const uint8_t* src1, int64_t
 // Epilogues of the MXFP8 GEMMs: Fc1 = SwiGLU, h to bf16 and MXFP8 (codes +
 // tiled scales), optionally saving A_g, A_u and h in bf16; Bf16 = rows of
 // bf16 (fc2); SwigluBwd = dA_g, dA_u in bf16 from dH and the saved A_g, A_u;
-// F32 = float rows (dXp) or weight-gradient rows (WGrad schedule). Rows
-// leave through the output tensor maps (make_out_tmap): fc1's saves
-// (0: A_g, 1: A_u, 2: h), fc2's O (0), dH's [dA_g | dA_u] (0), dXp (0), the
+// F32 = weight-gradient rows (WGrad schedule). Rows leave through the
+// output tensor maps (make_out_tmap): fc2's O and dXp (bf16, map 0), the
 // weight gradients (0, and 1 past out_split).
 enum class MxEpi { Fc1, Bf16, SwigluBwd, F32, Fc1Save };   // Fc1Save: fc1 with p.save
 
@@ -277,7 +283,7 @@ cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUt
 // dH with the SwiGLU backward epilogue (Rows; B = W2 as [E*F, H] along H).
 cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
                          const MxGemmArgs& p, int grid, cudaStream_t st);
-// dXp = dA_g W1g^T + dA_u W1u^T in float (Rows; K = 2F split over B0, B1).
+// dXp = bf16(dA_g W1g^T + dA_u W1u^T) (Rows; K = 2F split over B0, B1).
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st);
 // Weight gradients (WGrad: K = each expert's padded rows), float out.

@@ -28,9 +28,30 @@ __device__ __forceinline__ int mx_block_exp(float amax) {
   return max(-127, min(127, s));
 }
 
-// 2^-s as a float, exact for s <= 126 (a finite float block has s <= 119).
-__device__ __forceinline__ float mx_inv_scale(int s) {
-  return __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+// The bits of |v| as a float. Non-negative floats order like their bit
+// patterns read as integers, and every infinity or NaN pattern (0x7F800000
+// and above) lies above every finite one, so the integer maximum of these
+// over a block is the bits of its largest magnitude, or a non-finite
+// pattern when the block holds an infinity or a NaN (which fmaxf would drop).
+__device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
+
+// A block that holds an infinity or a NaN has no finite shared scale: it is
+// given the E8M0 NaN code and E4M3 NaN elements, so that every element of it
+// decodes to NaN.
+constexpr int kMxNanScale = 0xFF;
+constexpr uint32_t kMxNanCodes = 0x7F7F7F7Fu;   // four E4M3 NaNs (S.1111.111, S = 0)
+
+// E8M0 code of the block whose largest magnitude has the bits amax_bits
+// (see abs_bits): mx_block_exp + 127, or kMxNanScale for a non-finite block.
+__device__ __forceinline__ int mx_block_code(uint32_t amax_bits) {
+  return amax_bits >= 0x7F800000u ? kMxNanScale : mx_block_exp(__uint_as_float(amax_bits)) + 127;
+}
+
+// 1 / X of a block's code, X = 2^(code - 127), as a float: exact for the
+// codes of finite float blocks (at most 246); 1 for the NaN code, whose
+// element codes are replaced by kMxNanCodes anyway.
+__device__ __forceinline__ float mx_inv_scale(int code) {
+  return __uint_as_float(static_cast<uint32_t>(code == kMxNanScale ? 127 : 254 - code) << 23);
 }
 
 // E4M3 codes of a * inv .. d * inv (round to nearest even, saturating at
@@ -48,15 +69,17 @@ __device__ __forceinline__ uint32_t mx_encode4(float a, float b, float c, float 
 // One block of 32 values: returns the E8M0 code of its scale and packs the
 // 32 E4M3 codes four to a word (element 4i in the low byte of word i).
 __device__ __forceinline__ uint8_t quantize_block32(const float* v, uint32_t* words) {
-  float amax = 0.0f;
+  uint32_t amax = 0u;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int s = mx_block_exp(amax);
-  const float inv = mx_inv_scale(s);
+  for (int i = 0; i < 32; ++i) amax = max(amax, abs_bits(v[i]));
+  const int code = mx_block_code(amax);
+  const float inv = mx_inv_scale(code);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    words[i] = mx_encode4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
-  return static_cast<uint8_t>(s + 127);
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t w = mx_encode4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+    words[i] = code == kMxNanScale ? kMxNanCodes : w;
+  }
+  return static_cast<uint8_t>(code);
 }
 
 // Tiled scale layout read by the block-scaled MMA. Scales of a [rows, K]

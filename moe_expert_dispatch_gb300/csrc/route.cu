@@ -620,79 +620,6 @@ cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, cons
   return cudaGetLastError();
 }
 
-// dx[t] = bf16(sum_j dxp[row_j]), j in order, over float rows. One warp per
-// (token, column chunk of 32 lanes x kUnpermU 16-byte vectors); slot pairs
-// are loaded together as in the forward combine.
-__global__ void __launch_bounds__(256) unpermute_f32_kernel(const float* __restrict__ dxp,
-                                                            const int32_t* __restrict__ row_of,
-                                                            int64_t T, int k, int H,
-                                                            __nv_bfloat16* __restrict__ dx) {
-  constexpr int U = kUnpermU;
-  const int lane = lane_id();
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
-  const int n4 = H >> 2;
-  const int chunks = (n4 + 32 * U - 1) / (32 * U);
-  const int64_t tasks = T * chunks;
-  for (int64_t task = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
-       task < tasks; task += warps) {
-    const int64_t t = task / chunks;
-    const int c0 = static_cast<int>(task - t * chunks) * 32 * U + lane;
-    const int my_row = lane < k ? __ldg(row_of + t * k + lane) : -1;
-    float4 acc[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; j += 2) {            // warp-uniform trip count
-      const int r0 = __shfl_sync(0xffffffffu, my_row, j);
-      const int r1 = __shfl_sync(0xffffffffu, my_row, (j + 1) & 31);
-      const bool has1 = j + 1 < k && r1 >= 0;
-      float4 v0[U], v1[U];
-      if (r0 >= 0) {
-        const float4* src = reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r0) * H);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (c0 + 32 * u < n4) v0[u] = __ldcs(src + c0 + 32 * u);
-      }
-      if (has1) {
-        const float4* src = reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(r1) * H);
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (c0 + 32 * u < n4) v1[u] = __ldcs(src + c0 + 32 * u);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (r0 >= 0 && c0 + 32 * u < n4) {
-          acc[u].x += v0[u].x;
-          acc[u].y += v0[u].y;
-          acc[u].z += v0[u].z;
-          acc[u].w += v0[u].w;
-        }
-        if (has1 && c0 + 32 * u < n4) {
-          acc[u].x += v1[u].x;
-          acc[u].y += v1[u].y;
-          acc[u].z += v1[u].z;
-          acc[u].w += v1[u].w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (c0 + 32 * u < n4) {
-        uint2 w;
-        w.x = pack_bf16x2(acc[u].x, acc[u].y);
-        w.y = pack_bf16x2(acc[u].z, acc[u].w);
-        reinterpret_cast<uint2*>(dx + t * H)[c0 + 32 * u] = w;
-      }
-  }
-}
-
-cudaError_t launch_unpermute_f32(const float* dxp, const int32_t* row_of, int64_t T, int k, int H,
-                                 __nv_bfloat16* dx, cudaStream_t st) {
-  if (T == 0) return cudaSuccess;
-  const int64_t chunks = ((H >> 2) + 32 * kUnpermU - 1) / (32 * kUnpermU);
-  unpermute_f32_kernel<<<grid_for_warps(T * chunks, 8), 256, 0, st>>>(dxp, row_of, T, k, H, dx);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------------ backward: dO, dprobs
 
 // One warp per token t: for each of its slots j (8 at a time) the warp
@@ -818,20 +745,21 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16
         v[2 * j] = f.x;
         v[2 * j + 1] = f.y;
       }
-      float amax = 0.0f;
+      uint32_t amax = 0u;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      const int sexp = mx_block_exp(amax);
-      const float inv = mx_inv_scale(sexp);
+      for (int j = 0; j < 8; ++j) amax = max(amax, abs_bits(v[j]));
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      const int code = mx_block_code(amax);
+      const float inv = mx_inv_scale(code);
       if (item < end) {
         uint2 w;
         w.x = mx_encode4(v[0], v[1], v[2], v[3], inv);
         w.y = mx_encode4(v[4], v[5], v[6], v[7], inv);
+        if (code == kMxNanScale) w = make_uint2(kMxNanCodes, kMxNanCodes);
         *reinterpret_cast<uint2*>(q + b * 32 + part * 8) = w;
         if (part == 0) {
-          const uint8_t sc = static_cast<uint8_t>(sexp + 127);
+          const uint8_t sc = static_cast<uint8_t>(code);
           if (kTiled)
             scales[mx_scale_offset(b / nb, b % nb, K)] = sc;
           else
@@ -900,9 +828,10 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // consecutive rows, or rows 64 apart, never share a bank group
 __device__ __forceinline__ int qt_swizzle(int r) { return (r & 7) ^ ((r >> 4) & 4); }
 
-__device__ __forceinline__ float absmax8(const float* v) {
-  return fmaxf(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))),
-               fmaxf(fmaxf(fabsf(v[4]), fabsf(v[5])), fmaxf(fabsf(v[6]), fabsf(v[7]))));
+// abs_bits of the largest magnitude of 8 values (non-finite ones included)
+__device__ __forceinline__ uint32_t absmax8(const float* v) {
+  return max(max(max(abs_bits(v[0]), abs_bits(v[1])), max(abs_bits(v[2]), abs_bits(v[3]))),
+             max(max(abs_bits(v[4]), abs_bits(v[5])), max(abs_bits(v[6]), abs_bits(v[7]))));
 }
 
 // Where the bf16 input comes from: rows of a row-major matrix, gathered
@@ -970,26 +899,25 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
         w[4 * j + 2] = q.z;
         w[4 * j + 3] = q.w;
       }
-      float m[8];
+      uint32_t amax = 0u;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        m[j] = fmaxf(fmaxf(fabsf(bf16_lo(w[2 * j])), fabsf(bf16_hi(w[2 * j]))),
-                     fmaxf(fabsf(bf16_lo(w[2 * j + 1])), fabsf(bf16_hi(w[2 * j + 1]))));
-      const float amax = fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])),
-                               fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
-      const int sexp = mx_block_exp(amax);
-      const float inv = mx_inv_scale(sexp);
+      for (int j = 0; j < 16; ++j)
+        amax = max(amax, max(abs_bits(bf16_lo(w[j])), abs_bits(bf16_hi(w[j]))));
+      const int code = mx_block_code(amax);
+      const float inv = mx_inv_scale(code);
       uint32_t o[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < 8; ++j) {
         o[j] = mx_encode4(bf16_lo(w[2 * j]), bf16_hi(w[2 * j]), bf16_lo(w[2 * j + 1]),
                           bf16_hi(w[2 * j + 1]), inv);
+        if (code == kMxNanScale) o[j] = kMxNanCodes;
+      }
       const int64_t grow = static_cast<int64_t>(z) * rows + r0 + r;
       int4* dst = reinterpret_cast<int4*>(q_row + grow * cols + c0 + b * 32);
       dst[0] = make_int4(o[0], o[1], o[2], o[3]);
       dst[1] = make_int4(o[4], o[5], o[6], o[7]);
       const int kb = (c0 >> 5) + b;
-      const uint8_t sc = static_cast<uint8_t>(sexp + 127);
+      const uint8_t sc = static_cast<uint8_t>(code);
       if (kTiled)
         s_row[mx_scale_offset(grow, kb, cols)] = sc;
       else
@@ -1015,19 +943,21 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
           v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
               &tile[rr][(((c >> 3) ^ qt_swizzle(rr)) << 4) + (c & 7) * 2]));
         }
-        const float amax = fmaxf(fmaxf(absmax8(v), absmax8(v + 8)),
-                                 fmaxf(absmax8(v + 16), absmax8(v + 24)));
-        const int sexp = mx_block_exp(amax);
-        const float inv = mx_inv_scale(sexp);
+        const uint32_t amax = max(max(absmax8(v), absmax8(v + 8)),
+                                  max(absmax8(v + 16), absmax8(v + 24)));
+        const int code = mx_block_code(amax);
+        const float inv = mx_inv_scale(code);
         uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < 8; ++i) {
           w[i] = mx_encode4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3], inv);
+          if (code == kMxNanScale) w[i] = kMxNanCodes;
+        }
         *reinterpret_cast<int4*>(&codes[c][((2 * rb) ^ (c & 7)) << 4]) =
             make_int4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<int4*>(&codes[c][((2 * rb + 1) ^ (c & 7)) << 4]) =
             make_int4(w[4], w[5], w[6], w[7]);
-        sc2 |= static_cast<uint32_t>(sexp + 127) << (8 * h);
+        sc2 |= static_cast<uint32_t>(code) << (8 * h);
       }
     }
   }
@@ -1152,16 +1082,17 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
           v[2 * j] = f.x;
           v[2 * j + 1] = f.y;
         }
-        float amax = 0.0f;
+        uint32_t amax = 0u;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[j]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const int sexp = mx_block_exp(amax);
-        const float inv = mx_inv_scale(sexp);
+        for (int j = 0; j < 8; ++j) amax = max(amax, abs_bits(v[j]));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int code = mx_block_code(amax);
+        const float inv = mx_inv_scale(code);
         w[u].x = mx_encode4(v[0], v[1], v[2], v[3], inv);
         w[u].y = mx_encode4(v[4], v[5], v[6], v[7], inv);
-        if (part == 0 && b < nb) xs_tok[t * nb + b] = static_cast<uint8_t>(sexp + 127);
+        if (code == kMxNanScale) w[u] = make_uint2(kMxNanCodes, kMxNanCodes);
+        if (part == 0 && b < nb) xs_tok[t * nb + b] = static_cast<uint8_t>(code);
       }
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, my_row, j);

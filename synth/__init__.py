@@ -215,6 +215,71 @@ def make_inputs(w: Workload, seed: int = 0, with_dy: bool | None = None) -> dict
     return out
 
 
+# Small-integer inputs of the BF16 block whose arithmetic is exact (see
+# exact_inputs): the gate bias, and the nonzero entries per weight column.
+EXACT_GATE_BIAS = 44
+EXACT_GATE_NNZ = 4
+EXACT_UP_NNZ = 6
+EXACT_DOWN_NNZ = 8
+
+
+def _sparse_columns(g: np.random.Generator, E: int, K: int, N: int, nnz: int,
+                    row0: int) -> np.ndarray:
+    """int8 [E, K, N]: in every column (e, :, n), nnz draws of +-1 added at
+    rows drawn uniformly from [row0, K) (two draws may land on one row)."""
+    w = np.zeros((E, K, N), dtype=np.int8)
+    rows = g.integers(row0, K, size=(E, nnz, N))
+    signs = (2 * g.integers(0, 2, size=(E, nnz, N)) - 1).astype(np.int8)
+    e_idx = np.broadcast_to(np.arange(E)[:, None, None], rows.shape)
+    n_idx = np.broadcast_to(np.arange(N)[None, None, :], rows.shape)
+    np.add.at(w, (e_idx, rows, n_idx), signs)
+    return w
+
+
+def exact_inputs(w: Workload, seed: int = 0) -> dict:
+    """Inputs of the BF16 block (with dY) whose arithmetic is exact in float32.
+
+    Shapes and routing are the workload's (routing() draws ids as usual), but
+    every value is a small integer or a dyadic fraction:
+      x     in {-1, 0, 1}, with column 0 fixed at 1 (a bias input);
+      W1g   row 0 = EXACT_GATE_BIAS, plus EXACT_GATE_NNZ draws of +-1 per
+            column in rows 1..H-1, so every gate pre-activation lies in
+            [bias - nnz, bias + nnz] = [40, 48];
+      W1u   row 0 in {-2..2}, plus EXACT_UP_NNZ draws of +-1 per column;
+      W2    EXACT_DOWN_NNZ draws of +-1 per output column, over all F rows;
+      probs dyadic: k positive multiples of 2^-m summing to 1;
+      dY    in {-1, 0, 1}.
+    A gate input of 40 or more puts exp(-z) below half an ulp of 1 in float64
+    (and in float32), so silu(z) = z and the sigmoid is exactly 1 on both the
+    GPU and the oracle, and every product and partial sum of the block and its
+    backward is an integer or a multiple of 2^-m far below 2^24 units. Both
+    sides then round the same real numbers at the same points, and any
+    remaining difference is a mistake, not rounding.
+    """
+    T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
+    g = _gen(seed, 200, 0)
+    x = g.integers(-1, 2, size=(T, H)).astype(np.int8)
+    x[:, 0] = 1
+    wg = _sparse_columns(_gen(seed, 201, 0), E, H, F, EXACT_GATE_NNZ, 1)
+    wg[:, 0, :] = EXACT_GATE_BIAS
+    wu = _sparse_columns(_gen(seed, 202, 0), E, H, F, EXACT_UP_NNZ, 1)
+    wu[:, 0, :] = _gen(seed, 203, 0).integers(-2, 3, size=(E, F))
+    wd = _sparse_columns(_gen(seed, 204, 0), E, F, H, EXACT_DOWN_NNZ, 0)
+    dy = _gen(seed, 205, 0).integers(-1, 2, size=(T, H)).astype(np.int8)
+    # dyadic routing weights: a random composition of 2^m into k positive parts
+    m = max(2, int(np.ceil(np.log2(k))) + 1)
+    gp = _gen(seed, 206, 0)
+    cuts = np.sort(np.stack([gp.choice(np.arange(1, 2 ** m), k - 1, replace=False)
+                             for _ in range(T)]), axis=1) if k > 1 else np.zeros((T, 0), int)
+    edges = np.concatenate([np.zeros((T, 1), int), cuts, np.full((T, 1), 2 ** m)], axis=1)
+    probs = (np.diff(edges, axis=1) / 2.0 ** m).astype(np.float32)
+    ids, _ = routing(w, seed, torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+                     if w.routing == "router" else None)
+    bf = lambda a: torch.from_numpy(a).to(torch.bfloat16)  # noqa: E731
+    return {"workload": w, "x": bf(x), "w_gate": bf(wg), "w_up": bf(wu), "w_down": bf(wd),
+            "expert_ids": ids, "probs": torch.from_numpy(probs), "dy": bf(dy)}
+
+
 class F32Slices:
     """Indexable view that hands out one expert's weights at a time as a
     float32 NumPy array (bf16 -> f32 is exact), so that callers never hold a

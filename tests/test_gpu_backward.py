@@ -1,15 +1,29 @@
 """GPU parity of the backward (dX, dW1gate, dW1up, dW2, dprobs) against the
-CPU oracle under |g - g_ref| <= 1e-2 + 1e-2 |g_ref|: small ragged shapes in
-full, the Mixtral-shaped training workload on sampled tokens and sampled
-weight-gradient columns, empty experts, accumulation and the micro-batch
-split (dX, dprobs bit-identical; dW summed over chunks)."""
+CPU oracle under |g - g_ref| <= 1e-2 + 1e-2 |g_ref|.
+
+Two kinds of inputs:
+  * exact-arithmetic inputs (synth.exact_inputs: small integers, dyadic
+    routing weights, a saturated gate), on which the GPU and the oracle round
+    the same real numbers at the same points: every output is held to the
+    bound elementwise, small ragged shapes in full and the Mixtral-shaped
+    training workload at full size on sampled tokens and weight-gradient
+    columns of every expert;
+  * N(0, sigma) inputs, which also exercise the SwiGLU derivative: dprobs and
+    the small shapes' weight gradients are held to the bound elementwise; dX
+    and the full-size weight gradients can differ by one bf16 step of an
+    intermediate that the two sides round on either side of a boundary, so
+    they are held to a bound widened by exactly that step, with the number of
+    elements that need the widening counted and held to the measured count.
+Also: empty experts, accumulation, ring depth and grid size, and the
+micro-batch split (dX, dprobs bit-identical; dW summed over chunks), at
+T=512 and on the full training workload at splits 1, 4 and 8."""
 import numpy as np
 import pytest
 import torch
 
 import oracle as orc
 import synth
-from gpu_util import assert_bf16_close, dev, f32_slices, to_np
+from gpu_util import assert_bf16_close, check_dx, dev, f32_slices, to_np
 from test_gpu_forward import _case
 
 pytestmark = pytest.mark.gpu
@@ -32,44 +46,83 @@ def _oracle_bwd(x, wg, wu, wd, ids, probs, dy):
                                probs.numpy().astype(np.float64))
 
 
-# Weight scale of the elementwise checks: the workloads' (N(0, 0.01..0.02)).
+# Weight scale of the N(0, sigma) checks: the workloads' (N(0, 0.01..0.02)).
 WSTD = 0.02
 
+# Elements of dX outside the unwidened bound on the N(0, sigma) cases, as
+# measured on a GB300 (both sides are deterministic; check_dx explains each
+# by one bf16 step of a dXp row).
+DX_OUTSIDE = {"small-300": 0, "small-129": 0, "small-517": 0, "small-64": 0, "one-expert": 0,
+              "stress": 2, "train-sampled": 0}
 
-def _compare_all(g, ref):
-    assert_bf16_close(to_np(g["dx"]), ref["dx"], "dx")
+
+def _compare_all(g, ref, case):
+    n = check_dx(to_np(g["dx"]), ref["dx"], ref["dxp"][ref["row_of"]], f"dx ({case})")
+    print(f"{case}: {n} elements of dx outside the unwidened bound")
+    assert n <= DX_OUTSIDE[case], (case, n)
     assert_bf16_close(to_np(g["dprobs"]), ref["dprobs"], "dprobs")
     for key in ("dw_gate", "dw_up", "dw_down"):
         assert_bf16_close(to_np(g[key]), ref[key], key)
 
 
-@pytest.mark.parametrize("T,H,F,E,k,empty", [
+def _compare_exact(g, ref, what):
+    """Exact-arithmetic inputs: every output within the bound and, since both
+    sides round the same real numbers, bit-equal to the oracle."""
+    for key in ("y", "dx", "dprobs", "dw_gate", "dw_up", "dw_down"):
+        got = to_np(g[key])
+        assert_bf16_close(got, ref[key], f"{key} ({what})")
+        assert np.array_equal(got, ref[key]), \
+            f"{what} {key}: {int((got != ref[key]).sum())} of {got.size} not bit-equal"
+
+
+SMALL = [
     (300, 256, 384, 5, 2, (3,)),       # ragged tails, an empty expert
     (129, 128, 256, 1, 1, ()),         # one expert
     (517, 384, 640, 9, 3, (0, 8)),     # H, F not multiples of 256
     (64, 256, 512, 4, 4, ()),          # k = E
-])
+]
+
+
+@pytest.mark.parametrize("T,H,F,E,k,empty", SMALL)
 def test_backward_small(T, H, F, E, k, empty):
     case = _case(T, H, F, E, k, seed=T + 1, empty=empty, wstd=WSTD)
     dy = synth.normal_bf16(7, 5, (T, H))
     g = _gpu_fwd_bwd(*case, dy)
     ref = _oracle_bwd(*case, dy)
-    _compare_all(g, ref)
+    _compare_all(g, ref, f"small-{T}")
     for e in empty:
         assert torch.all(g["dw_gate"][e] == 0) and torch.all(g["dw_down"][e] == 0)
+
+
+def _exact_case(T, H, F, E, k, seed, empty=(), hot=None):
+    """exact_inputs values with _case's routing (empty experts, a hot expert)."""
+    w = synth.WORKLOADS["tiny_bf16"].resized(T=T, H=H, F=F, E=E, k=k, routing="gaussian")
+    inp = synth.exact_inputs(w, seed)
+    ids = _case(T, 128, 128, E, k, seed=seed, empty=empty, hot=hot)[4]
+    return (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], ids, inp["probs"]), inp["dy"]
+
+
+@pytest.mark.parametrize("T,H,F,E,k,empty", SMALL)
+def test_backward_small_exact(T, H, F, E, k, empty):
+    case, dy = _exact_case(T, H, F, E, k, seed=T + 3, empty=empty)
+    g = _gpu_fwd_bwd(*case, dy)
+    _compare_exact(g, _oracle_bwd(*case, dy), f"exact-{T}")
 
 
 def test_backward_large_weights_stress():
     """Weights five times the workloads' scale make dA large, so a one-ulp
     difference in where GPU (float) and oracle (float64) round an element of
-    dA to bf16 moves whole dW columns by ulp(dA) * |Xp|. dX and dprobs stay
-    within the elementwise bound; dW is held to a relative norm bound and
-    to a small count of elements outside the elementwise one."""
+    dA to bf16 moves whole dW columns by ulp(dA) * |Xp|. dX is held as in
+    every N(0, sigma) case and dprobs to the elementwise bound; dW is held to
+    a relative norm bound and to a small count of elements outside the
+    elementwise one."""
     case = _case(300, 256, 384, 5, 2, seed=301, empty=(3,), wstd=0.1)
     dy = synth.normal_bf16(7, 5, (300, 256))
     g = _gpu_fwd_bwd(*case, dy)
     ref = _oracle_bwd(*case, dy)
-    assert_bf16_close(to_np(g["dx"]), ref["dx"], "dx")
+    n = check_dx(to_np(g["dx"]), ref["dx"], ref["dxp"][ref["row_of"]], "dx (stress)")
+    print(f"stress: {n} elements of dx outside the unwidened bound")
+    assert n <= DX_OUTSIDE["stress"], n
     assert_bf16_close(to_np(g["dprobs"]), ref["dprobs"], "dprobs")
     for key in ("dw_gate", "dw_up", "dw_down"):
         got, want = to_np(g[key]), ref[key]
@@ -81,7 +134,12 @@ def test_backward_large_weights_stress():
 def test_backward_all_tokens_one_expert():
     case = _case(700, 256, 256, 16, 2, seed=5, hot=3, wstd=WSTD)
     dy = synth.normal_bf16(7, 6, (700, 256))
-    _compare_all(_gpu_fwd_bwd(*case, dy), _oracle_bwd(*case, dy))
+    _compare_all(_gpu_fwd_bwd(*case, dy), _oracle_bwd(*case, dy), "one-expert")
+
+
+def test_backward_all_tokens_one_expert_exact():
+    case, dy = _exact_case(700, 256, 256, 16, 2, seed=6, hot=3)
+    _compare_exact(_gpu_fwd_bwd(*case, dy), _oracle_bwd(*case, dy), "exact-one-expert")
 
 
 def test_backward_accumulate_and_ring_depth():
@@ -97,16 +155,13 @@ def test_backward_accumulate_and_ring_depth():
         assert torch.equal(g3[key], g1[key]), key
 
 
-@pytest.mark.parametrize("splits", [4, 8])
-def test_backward_microbatch_split(splits):
-    T = 512
-    case = _case(T, 256, 384, 8, 2, seed=13, wstd=WSTD)
-    x, wg, wu, wd, ids, probs = case
-    dy = synth.normal_bf16(7, 8, (T, 256))
-    full = _gpu_fwd_bwd(*case, dy)
+def _split_run(x, wg, wu, wd, ids, probs, dy, splits):
+    """The block over `splits` contiguous token chunks: dX, dprobs and y
+    concatenated, dW accumulated over the chunks in chunk order."""
+    T = x.shape[0]
     n = T // splits
     acc = None
-    dxs, dps = [], []
+    dxs, dps, ys = [], [], []
     for i in range(splits):
         sl = slice(i * n, (i + 1) * n)
         g = _gpu_fwd_bwd(x[sl], wg, wu, wd, ids[sl], probs[sl], dy[sl],
@@ -114,31 +169,98 @@ def test_backward_microbatch_split(splits):
         acc = {k: g[k] for k in ("dw_gate", "dw_up", "dw_down")}
         dxs.append(g["dx"])
         dps.append(g["dprobs"])
-    assert torch.equal(torch.cat(dxs), full["dx"])
-    assert torch.equal(torch.cat(dps), full["dprobs"])
+        ys.append(g["y"])
+    acc.update(dx=torch.cat(dxs), dprobs=torch.cat(dps), y=torch.cat(ys))
+    return acc
+
+
+@pytest.mark.parametrize("splits", [4, 8])
+def test_backward_microbatch_split(splits):
+    T = 512
+    case = _case(T, 256, 384, 8, 2, seed=13, wstd=WSTD)
+    dy = synth.normal_bf16(7, 8, (T, 256))
+    full = _gpu_fwd_bwd(*case, dy)
+    acc = _split_run(*case, dy, splits)
+    for key in ("y", "dx", "dprobs"):
+        assert torch.equal(acc[key], full[key]), key
     for key in ("dw_gate", "dw_up", "dw_down"):
         assert_bf16_close(to_np(acc[key]), to_np(full[key]), key)
 
 
-def test_backward_train_workload_sampled():
+def _train_case(exact):
     w = synth.WORKLOADS["train_bf16"]
-    inp = synth.make_inputs(w, 0)
+    inp = synth.exact_inputs(w, 0) if exact else synth.make_inputs(w, 0)
     case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
-    dy = inp["dy"]
+    return w, case, inp["dy"]
+
+
+def _tokens_of_every_expert(ids, E, per_expert=2, extra=(0,)):
+    """The first and last tokens routed to each expert, plus `extra`."""
+    toks = set(extra)
+    for e in range(E):
+        hit = np.nonzero((ids == e).any(axis=1))[0]
+        if hit.size:
+            toks.update(hit[:per_expert // 2 + per_expert % 2].tolist())
+            toks.update(hit[-(per_expert // 2):].tolist() if per_expert > 1 else [])
+    return sorted(toks)
+
+
+def test_backward_train_workload_exact_full_size():
+    """The Mixtral-shaped training workload at full size (T=16384, H=4096,
+    F=14336, E=8, k=2) on exact-arithmetic inputs: y, dX and dprobs of tokens
+    routed to every expert, and whole columns of every expert's weight
+    gradients (each a sum over all of that expert's rows), elementwise within
+    the BF16 bound and bit-equal to the oracle."""
+    w, case, dy = _train_case(exact=True)
     g = _gpu_fwd_bwd(*case, dy)
+    ids = case[4].numpy()
+    toks = _tokens_of_every_expert(ids, w.E, extra=(0, w.T - 1))
     ws = [f32_slices(t) for t in case[1:4]]
-    toks = np.random.default_rng(1).choice(w.T, 12, replace=False).tolist() + [0, w.T - 1]
-    dx_ref, dp_ref = orc.backward_rows(to_np(dy), to_np(case[0]), *ws, case[4].numpy(),
-                                       case[5].numpy(), toks)
-    assert_bf16_close(to_np(g["dx"])[toks], dx_ref, "dx sampled")
-    assert_bf16_close(to_np(g["dprobs"])[toks], dp_ref, "dprobs sampled")
-    cols = [0, 77, 8191, w.F - 1]
-    for e in (0, 5):
-        ref = orc.weight_grad_columns(to_np(dy), to_np(case[0]), *ws, case[4].numpy(),
-                                      case[5].numpy(), e, cols)
+    args = (to_np(case[0]), *ws, ids, case[5].numpy())
+    y_ref = orc.sampled_forward(*args, toks)
+    dx_ref, dp_ref = orc.backward_rows(to_np(dy), *args, toks)
+    for key, got, ref in (("y", g["y"], y_ref), ("dx", g["dx"], dx_ref),
+                          ("dprobs", g["dprobs"], dp_ref)):
+        got = to_np(got)[toks]
+        assert_bf16_close(got, ref, f"{key} sampled")
+        assert np.array_equal(got, ref), f"{key}: {int((got != ref).sum())} not bit-equal"
+    cols = [0, 1, 4095, 7777, w.F - 1]
+    for e in range(w.E):
+        ref = orc.weight_grad_columns(to_np(dy), *args, e, cols)
         for key, got in (("dw_gate", g["dw_gate"][e][:, cols]), ("dw_up", g["dw_up"][e][:, cols]),
                          ("dw_down", g["dw_down"][e][cols, :])):
-            _check_reduction_over_rows(to_np(got), ref[key], f"{key}[{e}]")
+            got = to_np(got)
+            assert_bf16_close(got, ref[key], f"{key}[{e}]")
+            assert np.array_equal(got, ref[key]), f"{key}[{e}] not bit-equal"
+
+
+# Sampled weight-gradient elements outside the unwidened bound on the
+# N(0, sigma) training workload, as measured (see _check_reduction_over_rows).
+DW_OUTSIDE_TRAIN = 5
+
+
+def test_backward_train_workload_sampled():
+    w, case, dy = _train_case(exact=False)
+    g = _gpu_fwd_bwd(*case, dy)
+    ws = [f32_slices(t) for t in case[1:4]]
+    ids = case[4].numpy()
+    toks = _tokens_of_every_expert(ids, w.E, extra=(0, w.T - 1))
+    dx_ref, dp_ref, rows = orc.backward_rows(to_np(dy), to_np(case[0]), *ws, ids,
+                                             case[5].numpy(), toks, with_rows=True)
+    n = check_dx(to_np(g["dx"])[toks], dx_ref, rows, "dx sampled")
+    print(f"train-sampled: {n} elements of dx outside the unwidened bound")
+    assert n <= DX_OUTSIDE["train-sampled"], n
+    assert_bf16_close(to_np(g["dprobs"])[toks], dp_ref, "dprobs sampled")
+    cols = [0, 77, 8191, w.F - 1]
+    outside = 0
+    for e in (0, 5):
+        ref = orc.weight_grad_columns(to_np(dy), to_np(case[0]), *ws, ids, case[5].numpy(), e,
+                                      cols)
+        for key, got in (("dw_gate", g["dw_gate"][e][:, cols]), ("dw_up", g["dw_up"][e][:, cols]),
+                         ("dw_down", g["dw_down"][e][cols, :])):
+            outside += _check_reduction_over_rows(to_np(got), ref[key], f"{key}[{e}]")
+    print(f"train-sampled: {outside} weight-gradient elements outside the unwidened bound")
+    assert outside <= DW_OUTSIDE_TRAIN, outside
 
 
 def _check_reduction_over_rows(got, ref, what):
@@ -146,13 +268,36 @@ def _check_reduction_over_rows(got, ref, what):
     come from float32 accumulations on the GPU: a few tenths of a percent of
     them round one way on the GPU and the other way in the float64 oracle
     (measured: 0.45 % of h on this workload). Where a sum cancels heavily
-    that can move it past the elementwise bound, so at full size the bound
-    must hold for at least 99.9 % of the sampled elements, and every element
-    must lie within the bound widened by 1e-3 * max|ref| (the scale of those
-    rounding flips summed over the rows)."""
+    that can move it past the elementwise bound. Every element must lie
+    within the bound widened by 1e-3 * max|ref| (the scale of those rounding
+    flips summed over the rows); the count outside the unwidened bound is
+    returned. The exact-arithmetic test above holds the same sums to the
+    unwidened bound."""
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), what
-    inside = err <= 1e-2 + 1e-2 * np.abs(ref)
-    assert inside.mean() >= 0.999, (what, int((~inside).sum()), inside.size)
     widened = err <= 1e-2 + 1e-2 * np.abs(ref) + 1e-3 * np.max(np.abs(ref))
     assert widened.all(), (what, float(err.max()))
+    return int((err > 1e-2 + 1e-2 * np.abs(ref)).sum())
+
+
+def test_backward_train_workload_microbatch_splits():
+    """Micro-batch splits 1, 4 and 8 of the full training workload (T=16384):
+    y, dX and dprobs bit-identical to the unsplit step (1: the step run
+    again), dW summed over the chunks within the BF16 bound of the unsplit
+    dW (only the order of its float sums over rows changes)."""
+    w, case, dy = _train_case(exact=False)
+    full = _gpu_fwd_bwd(*case, dy)
+    full = {k: v.cpu() for k, v in full.items()}
+    torch.cuda.empty_cache()
+    for splits in (1, 4, 8):
+        acc = _split_run(*case, dy, splits)
+        for key in ("y", "dx", "dprobs"):
+            assert torch.equal(acc[key].cpu(), full[key]), (splits, key)
+        for key in ("dw_gate", "dw_up", "dw_down"):
+            got = acc[key].cpu()
+            if splits == 1:
+                assert torch.equal(got, full[key]), key
+            else:
+                assert_bf16_close(to_np(got), to_np(full[key]), f"{key} at {splits} splits")
+        del acc
+        torch.cuda.empty_cache()

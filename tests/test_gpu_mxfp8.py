@@ -93,15 +93,79 @@ def test_mxfp8_tile_widths_agree():
     assert torch.equal(y128, y256)
 
 
+def tokens_covering_experts(ids, E, extra=(), seed=0):
+    """Tokens, in a seeded random order, taken while they route to an expert
+    that no earlier pick reaches, until every expert with a token is reached;
+    then `extra`."""
+    order = np.random.default_rng(seed).permutation(ids.shape[0])
+    seen, toks = set(), []
+    for t in order:
+        new = set(int(e) for e in ids[t]) - seen
+        if new:
+            toks.append(int(t))
+            seen |= new
+        if len(seen) == E:
+            break
+    return sorted(set(toks) | set(extra))
+
+
 def test_mxfp8_workload_sampled():
+    """The MXFP8 workload at full size (T=16384, H=7168, F=2048, E=64, k=6)
+    on sampled tokens that together reach all 64 experts, so that every
+    expert's fc1 and fc2 tiles are compared with the oracle."""
     w = synth.WORKLOADS["mxfp8"]
     inp = synth.make_inputs(w, 0)
     x, wg, wu, wd = inp["x"], inp["w_gate_t"], inp["w_up_t"], inp["w_down_t"]
     ids, probs = inp["expert_ids"], inp["probs"]
     y, _ = _gpu(x, wg, wu, wd, ids, probs)
     y = to_np(y)
-    toks = [0, 7777, w.T - 1]
+    toks = tokens_covering_experts(ids.numpy(), w.E, extra=(0, 7777, w.T - 1))
+    assert set(ids.numpy()[toks].reshape(-1).tolist()) == set(range(w.E))
     f32 = lambda t: synth.F32Slices(t)  # noqa: E731
     ref = orc.sampled_forward_mxfp8(to_np(x), f32(wg), f32(wu), f32(wd), ids.numpy(), probs.numpy(), toks)
+    print(f"{len(toks)} tokens reach all {w.E} experts; max err / max|ref| = "
+          f"{np.abs(y[toks] - ref).max() / np.abs(ref).max():.3e}")
     assert_rel_to_max(y[toks], ref, TOL, "y sampled")
     assert np.all(np.isfinite(y))
+
+
+def _with_nonfinite(shape, seed):
+    """N(0,1) bf16 values with about one element in 400 replaced by +inf,
+    -inf or NaN."""
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn(shape, generator=g)
+    flat = a.view(-1)
+    idx = torch.randperm(flat.numel(), generator=g)[:max(3, flat.numel() // 400)]
+    special = torch.tensor([float("inf"), float("-inf"), float("nan")])
+    flat[idx] = special[torch.arange(idx.numel()) % 3]
+    return a.to(torch.bfloat16)
+
+
+def test_quantisers_nonfinite_blocks_bit_exact():
+    """Blocks holding an infinity or a NaN: every quantiser (along the rows,
+    along the columns, both at once, and fused with the permute) writes the
+    E8M0 NaN scale and E4M3 NaN codes for them, and the oracle's codes and
+    scales elsewhere, bit for bit."""
+    a = _with_nonfinite((3, 96, 256), 3)
+    ref_rows = [orc.quantize_mxfp8(to_np(a[z])) for z in range(3)]
+    ref_cols = [orc.quantize_mxfp8(to_np(a[z]).T) for z in range(3)]
+    assert any((s == 255).any() for _, s in ref_rows)
+    q, s = m.moe_quantize_mxfp8(dev(a))
+    qt, st = m.moe_quantize_mxfp8_t(dev(a))
+    dq, ds, dqt, dst = m.moe_quantize_mxfp8_dual(dev(a))
+    for z in range(3):
+        for got, want in ((q[z], ref_rows[z][0]), (s[z], ref_rows[z][1]), (dq[z], ref_rows[z][0]),
+                          (ds[z], ref_rows[z][1]), (qt[z], ref_cols[z][0]),
+                          (st[z], ref_cols[z][1]), (dqt[z], ref_cols[z][0]),
+                          (dst[z], ref_cols[z][1])):
+            assert np.array_equal(got.cpu().numpy(), want)
+    x = a[0]                                     # [96, 256] as tokens
+    T, k = x.shape[0], 2
+    row_of = torch.arange(T * k, dtype=torch.int32).reshape(T, k).flip(0).contiguous()
+    pq, ps = m.moe_permute_quantize_mxfp8(dev(x), dev(row_of))
+    rq, rs = ref_rows[0]
+    assert np.array_equal(ps.cpu().numpy(), rs)
+    pq = pq.cpu().numpy()
+    for t in range(T):
+        for j in range(k):
+            assert np.array_equal(pq[row_of[t, j]], rq[t]), (t, j)
