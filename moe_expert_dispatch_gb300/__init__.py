@@ -104,12 +104,19 @@ def _p(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream=None):
-    s = torch.cuda.current_stream() if stream is None else stream
+def _stream(stream=None, device=None):
+    """The given stream, or the current stream of `device` (the device that
+    the call's tensors live on); a given stream must belong to that device."""
+    if stream is None:
+        s = torch.cuda.current_stream(device)
+    else:
+        s = stream
+        if device is not None and s.device != device:
+            raise ValueError(f"stream is on {s.device}, the tensors on {device}")
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _cuda(t, name, dtype=None):
+def _cuda(t, name, dtype=None, min_numel=None):
     if t is None:
         return
     if not t.is_cuda:
@@ -118,6 +125,25 @@ def _cuda(t, name, dtype=None):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name} holds {t.numel()} elements, needs at least {min_numel}")
+
+
+def _device(*named):
+    """The one CUDA device of the (name, tensor) pairs given (None tensors
+    skipped). Every kernel of a call runs on the device of its tensors, and
+    a call whose tensors live on two devices is refused before anything is
+    launched."""
+    dev, first = None, None
+    for name, t in named:
+        if t is None:
+            continue
+        if dev is None:
+            dev, first = t.device, name
+        elif t.device != dev:
+            raise ValueError(f"{name} is on {t.device} but {first} is on {dev}: "
+                             "all tensors of a call must share one device")
+    return dev
 
 
 def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
@@ -143,8 +169,12 @@ def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
 
 
 def moe_get_error(stream=None) -> int:
-    """Synchronises the stream and returns (and clears) the device error status."""
-    return _lib.moe_get_error(_stream(stream))
+    """Synchronises the stream (default: the current device's current stream)
+    and returns (and clears) the error status of the stream's device."""
+    if stream is None:
+        return _lib.moe_get_error(_stream(None))
+    with torch.cuda.device(stream.device):
+        return _lib.moe_get_error(_stream(stream))
 
 
 def moe_num_sms() -> int:
@@ -163,15 +193,21 @@ def moe_counts(expert_ids: torch.Tensor, num_experts: int, counts=None, offsets=
                workspace=None, stream=None):
     """(counts int32 [E], offsets int32 [E+1]) of the flattened ids."""
     _cuda(expert_ids, "expert_ids", torch.int32)
-    dev = expert_ids.device
+    _cuda(counts, "counts", torch.int32, num_experts)
+    _cuda(offsets, "offsets", torch.int32, num_experts + 1)
+    _cuda(workspace, "workspace")
+    dev = _device(("expert_ids", expert_ids), ("counts", counts), ("offsets", offsets),
+                  ("workspace", workspace))
     n = expert_ids.numel()
-    counts = torch.empty(num_experts, dtype=torch.int32, device=dev) if counts is None else counts
-    offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
-               if offsets is None else offsets)
-    need = _lib.moe_counts_workspace_size(n, num_experts)
-    ws = _workspace(need, dev) if workspace is None else workspace
-    _check(_lib.moe_counts(_p(expert_ids), n, num_experts, _p(counts), _p(offsets), _p(ws),
-                           ws.numel(), _stream(stream)), "moe_counts")
+    with torch.cuda.device(dev):
+        counts = (torch.empty(num_experts, dtype=torch.int32, device=dev)
+                  if counts is None else counts)
+        offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+                   if offsets is None else offsets)
+        need = _lib.moe_counts_workspace_size(n, num_experts)
+        ws = _workspace(need, dev) if workspace is None else workspace
+        _check(_lib.moe_counts(_p(expert_ids), n, num_experts, _p(counts), _p(offsets), _p(ws),
+                               ws.numel(), _stream(stream, dev)), "moe_counts")
     return counts, offsets
 
 
@@ -182,17 +218,25 @@ def moe_route_topk(logits: torch.Tensor, k: int, expert_ids=None, probs=None, co
     router logits [T, E]."""
     _cuda(logits, "logits", torch.float32)
     T, E = logits.shape
-    dev = logits.device
-    expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
-                  if expert_ids is None else expert_ids)
-    probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
-    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
-    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
-    need = _lib.moe_route_topk_workspace_size(T, k, E)
-    ws = _workspace(need, dev) if workspace is None else workspace
-    _check(_lib.moe_route_topk(_p(logits), T, E, k, _p(expert_ids), _p(probs), _p(counts),
-                               _p(offsets), _p(ws), ws.numel(), _stream(stream)),
-           "moe_route_topk")
+    _cuda(expert_ids, "expert_ids", torch.int32, T * k)
+    _cuda(probs, "probs", torch.float32, T * k)
+    _cuda(counts, "counts", torch.int32, E)
+    _cuda(offsets, "offsets", torch.int32, E + 1)
+    _cuda(workspace, "workspace")
+    dev = _device(("logits", logits), ("expert_ids", expert_ids), ("probs", probs),
+                  ("counts", counts), ("offsets", offsets), ("workspace", workspace))
+    with torch.cuda.device(dev):
+        expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
+                      if expert_ids is None else expert_ids)
+        probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
+        counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+        offsets = (torch.empty(E + 1, dtype=torch.int32, device=dev)
+                   if offsets is None else offsets)
+        need = _lib.moe_route_topk_workspace_size(T, k, E)
+        ws = _workspace(need, dev) if workspace is None else workspace
+        _check(_lib.moe_route_topk(_p(logits), T, E, k, _p(expert_ids), _p(probs), _p(counts),
+                                   _p(offsets), _p(ws), ws.numel(), _stream(stream, dev)),
+               "moe_route_topk")
     return expert_ids, probs, counts, offsets
 
 
@@ -202,12 +246,17 @@ def moe_counts_static(expert_ids: torch.Tensor, num_experts: int, counts=None, o
     allocates no device memory (the output tensors are created here only when
     the caller passes none). Calls that overlap on the GPU race on that scratch."""
     _cuda(expert_ids, "expert_ids", torch.int32)
-    dev = expert_ids.device
-    counts = torch.empty(num_experts, dtype=torch.int32, device=dev) if counts is None else counts
-    offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
-               if offsets is None else offsets)
-    _check(_lib.moe_counts_static(_p(expert_ids), expert_ids.numel(), num_experts, _p(counts),
-                                  _p(offsets), _stream(stream)), "moe_counts_static")
+    _cuda(counts, "counts", torch.int32, num_experts)
+    _cuda(offsets, "offsets", torch.int32, num_experts + 1)
+    dev = _device(("expert_ids", expert_ids), ("counts", counts), ("offsets", offsets))
+    with torch.cuda.device(dev):        # the scratch used is the one of this device
+        counts = (torch.empty(num_experts, dtype=torch.int32, device=dev)
+                  if counts is None else counts)
+        offsets = (torch.empty(num_experts + 1, dtype=torch.int32, device=dev)
+                   if offsets is None else offsets)
+        _check(_lib.moe_counts_static(_p(expert_ids), expert_ids.numel(), num_experts,
+                                      _p(counts), _p(offsets), _stream(stream, dev)),
+               "moe_counts_static")
     return counts, offsets
 
 
@@ -223,7 +272,12 @@ def moe_permute(x: torch.Tensor, expert_ids: torch.Tensor, probs, num_experts: i
     _cuda(expert_ids, "expert_ids", torch.int32)
     _cuda(probs, "probs", torch.float32)
     T, k = expert_ids.shape
-    dev = x.device
+    dev = _device(("x", x), ("expert_ids", expert_ids), ("probs", probs))
+    with torch.cuda.device(dev):
+        return _moe_permute(x, expert_ids, probs, num_experts, row_align, stream, T, k, dev)
+
+
+def _moe_permute(x, expert_ids, probs, num_experts, row_align, stream, T, k, dev):
     row_bytes = x[0].numel() * x.element_size() if T else x.element_size()
     cap = _lib.moe_padded_rows(T * k, num_experts, row_align)
     out = dict(
@@ -238,7 +292,7 @@ def moe_permute(x: torch.Tensor, expert_ids: torch.Tensor, probs, num_experts: i
     _check(_lib.moe_permute(_p(x), T, row_bytes, _p(expert_ids), _p(probs), k, num_experts,
                             row_align, _p(out["x_perm"]), _p(out["row_of"]), _p(out["token_of"]),
                             _p(out["prob_of"]), _p(out["offsets"]), _p(out["counts"]), _p(ws),
-                            ws.numel(), _stream(stream)), "moe_permute")
+                            ws.numel(), _stream(stream, dev)), "moe_permute")
     return out
 
 
@@ -246,12 +300,15 @@ def moe_unpermute(o_perm: torch.Tensor, row_of: torch.Tensor, probs=None, y=None
     """y[t] = bf16(sum_j probs[t, j] * o_perm[row_of[t, j]])."""
     _cuda(o_perm, "o_perm", torch.bfloat16)
     _cuda(row_of, "row_of", torch.int32)
-    _cuda(probs, "probs", torch.float32)
     T, k = row_of.shape
     H = o_perm.shape[-1]
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=o_perm.device) if y is None else y
-    _check(_lib.moe_unpermute(_p(o_perm), _p(row_of), _p(probs), T, k, H, _p(y), _stream(stream)),
-           "moe_unpermute")
+    _cuda(probs, "probs", torch.float32, T * k)
+    _cuda(y, "y", torch.bfloat16, T * H)
+    dev = _device(("o_perm", o_perm), ("row_of", row_of), ("probs", probs), ("y", y))
+    with torch.cuda.device(dev):
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+        _check(_lib.moe_unpermute(_p(o_perm), _p(row_of), _p(probs), T, k, H, _p(y),
+                                  _stream(stream, dev)), "moe_unpermute")
     return y
 
 
@@ -266,10 +323,12 @@ def moe_quantize_mxfp8(a: torch.Tensor, stream=None, out=None):
         s = torch.empty(a.shape[:-1] + (K // 32,), dtype=torch.uint8, device=a.device)
     else:
         q, s = out
-        _cuda(q, "q", torch.uint8)
-        _cuda(s, "scales", torch.uint8)
-    _check(_lib.moe_quantize_mxfp8(_p(a), rows, K, _p(q), _p(s), _stream(stream)),
-           "moe_quantize_mxfp8")
+        _cuda(q, "q", torch.uint8, a.numel())
+        _cuda(s, "scales", torch.uint8, a.numel() // 32)
+    dev = _device(("a", a), ("q", q), ("scales", s))
+    with torch.cuda.device(dev):
+        _check(_lib.moe_quantize_mxfp8(_p(a), rows, K, _p(q), _p(s), _stream(stream, dev)),
+               "moe_quantize_mxfp8")
     return q, s
 
 
@@ -290,9 +349,12 @@ def moe_permute_quantize_mxfp8(x: torch.Tensor, row_of: torch.Tensor, n_rows: in
     else:
         q, s = out
         _cuda(q, "codes", torch.uint8)
-        _cuda(s, "scales", torch.uint8)
-    _check(_lib.moe_permute_quantize_mxfp8(_p(x), T, H, _p(row_of), k, _p(q), _p(s),
-                                           _stream(stream)), "moe_permute_quantize_mxfp8")
+        _cuda(s, "scales", torch.uint8, T * H // 32)
+    dev = _device(("x", x), ("row_of", row_of), ("codes", q), ("scales", s))
+    with torch.cuda.device(dev):
+        _check(_lib.moe_permute_quantize_mxfp8(_p(x), T, H, _p(row_of), k, _p(q), _p(s),
+                                               _stream(stream, dev)),
+               "moe_permute_quantize_mxfp8")
     return q, s
 
 
@@ -309,12 +371,14 @@ def moe_quantize_mxfp8_t(a: torch.Tensor, stream=None, out=None):
         s = torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device)
     else:
         q, s = out
-        _cuda(q, "q", torch.uint8)
-        _cuda(s, "scales", torch.uint8)
+        _cuda(q, "q", torch.uint8, a.numel())
+        _cuda(s, "scales", torch.uint8, a.numel() // 32)
         if squeeze:
             q, s = q.unsqueeze(0), s.unsqueeze(0)
-    _check(_lib.moe_quantize_mxfp8_t(_p(a3), B, rows, cols, _p(q), _p(s), _stream(stream)),
-           "moe_quantize_mxfp8_t")
+    dev = _device(("a", a), ("q", q), ("scales", s))
+    with torch.cuda.device(dev):
+        _check(_lib.moe_quantize_mxfp8_t(_p(a3), B, rows, cols, _p(q), _p(s),
+                                         _stream(stream, dev)), "moe_quantize_mxfp8_t")
     return (q[0], s[0]) if squeeze else (q, s)
 
 
@@ -330,10 +394,12 @@ def moe_quantize_mxfp8_dual(a: torch.Tensor, stream=None, out=None):
                torch.empty((B, rows, cols // 32), dtype=torch.uint8, device=a.device),
                torch.empty((B, cols, rows), dtype=torch.uint8, device=a.device),
                torch.empty((B, cols, rows // 32), dtype=torch.uint8, device=a.device))
-    for t in out:
-        _cuda(t, "out", torch.uint8)
-    _check(_lib.moe_quantize_mxfp8_dual(_p(a), B, rows, cols, *(_p(t) for t in out),
-                                        _stream(stream)), "moe_quantize_mxfp8_dual")
+    for t, n in zip(out, (a.numel(), a.numel() // 32, a.numel(), a.numel() // 32)):
+        _cuda(t, "out", torch.uint8, n)
+    dev = _device(("a", a), *(("out", t) for t in out))
+    with torch.cuda.device(dev):
+        _check(_lib.moe_quantize_mxfp8_dual(_p(a), B, rows, cols, *(_p(t) for t in out),
+                                            _stream(stream, dev)), "moe_quantize_mxfp8_dual")
     return out
 
 
@@ -355,15 +421,22 @@ def moe_expert_forward(x, w_gate, w_up, w_down, expert_ids, probs, y=None, works
     T, H = x.shape
     E, _, F = w_gate.shape
     k = expert_ids.shape[1]
+    _cuda(y, "y", torch.bfloat16, T * H)
+    _cuda(workspace, "workspace")
+    dev = _device(("x", x), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down),
+                  ("expert_ids", expert_ids), ("probs", probs), ("y", y),
+                  ("workspace", workspace))
     c = cfg if cfg is not None else config()
     need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 0)
     if need == 0 and T > 0:
         raise MoeError(1, "moe_workspace_size")
-    ws = _workspace(need, x.device) if workspace is None else workspace
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
-    _check(_lib.moe_expert_forward(_p(x), _p(w_gate), _p(w_up), _p(w_down), _p(expert_ids),
-                                   _p(probs), T, H, F, E, k, _p(y), _p(ws), ws.numel(),
-                                   ctypes.byref(c), _stream(stream)), "moe_expert_forward")
+    with torch.cuda.device(dev):
+        ws = _workspace(need, dev) if workspace is None else workspace
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+        _check(_lib.moe_expert_forward(_p(x), _p(w_gate), _p(w_up), _p(w_down), _p(expert_ids),
+                                       _p(probs), T, H, F, E, k, _p(y), _p(ws), ws.numel(),
+                                       ctypes.byref(c), _stream(stream, dev)),
+               "moe_expert_forward")
     return y, ws
 
 
@@ -377,21 +450,29 @@ def moe_expert_forward_from_logits(x, w_gate, w_up, w_down, router_logits, k, y=
     _cuda(router_logits, "router_logits", torch.float32)
     T, H = x.shape
     E, _, F = w_gate.shape
-    dev = x.device
+    _cuda(y, "y", torch.bfloat16, T * H)
+    _cuda(expert_ids, "expert_ids", torch.int32, T * k)
+    _cuda(probs, "probs", torch.float32, T * k)
+    _cuda(workspace, "workspace")
+    dev = _device(("x", x), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down),
+                  ("router_logits", router_logits), ("y", y), ("expert_ids", expert_ids),
+                  ("probs", probs), ("workspace", workspace))
     c = cfg if cfg is not None else config()
     need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 0)
     if need == 0 and T > 0:
         raise MoeError(1, "moe_workspace_size")
-    ws = _workspace(need, dev) if workspace is None else workspace
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
-    expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
-                  if expert_ids is None else expert_ids)
-    probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
-    _check(_lib.moe_expert_forward_from_logits(_p(x), _p(w_gate), _p(w_up), _p(w_down),
-                                               _p(router_logits), T, H, F, E, k, _p(expert_ids),
-                                               _p(probs), _p(y), _p(ws), ws.numel(),
-                                               ctypes.byref(c), _stream(stream)),
-           "moe_expert_forward_from_logits")
+    with torch.cuda.device(dev):
+        ws = _workspace(need, dev) if workspace is None else workspace
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+        expert_ids = (torch.empty((T, k), dtype=torch.int32, device=dev)
+                      if expert_ids is None else expert_ids)
+        probs = torch.empty((T, k), dtype=torch.float32, device=dev) if probs is None else probs
+        _check(_lib.moe_expert_forward_from_logits(_p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                                   _p(router_logits), T, H, F, E, k,
+                                                   _p(expert_ids), _p(probs), _p(y), _p(ws),
+                                                   ws.numel(), ctypes.byref(c),
+                                                   _stream(stream, dev)),
+               "moe_expert_forward_from_logits")
     return y, expert_ids, probs, ws
 
 
@@ -412,21 +493,27 @@ def moe_expert_forward_pipelined(x, w_gate, w_up, w_down, expert_ids, probs, n_c
     T, H = x.shape
     E, _, F = w_gate.shape
     k = expert_ids.shape[1]
+    _cuda(y, "y", torch.bfloat16, T * H)
+    _cuda(workspace, "workspace")
+    dev = _device(("x", x), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down),
+                  ("expert_ids", expert_ids), ("probs", probs), ("y", y),
+                  ("workspace", workspace))
     c = cfg if cfg is not None else config()
     need = _lib.moe_workspace_size_pipelined(T, H, F, E, k, n_chunks)
     if need == 0 and T > 0:
         raise MoeError(1, "moe_workspace_size_pipelined")
-    ws = _workspace(need, x.device) if workspace is None else workspace
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
-    if aux_stream is None:
-        aux_stream = _aux_streams.get(x.device)
+    with torch.cuda.device(dev):
+        ws = _workspace(need, dev) if workspace is None else workspace
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
         if aux_stream is None:
-            aux_stream = _aux_streams[x.device] = torch.cuda.Stream(device=x.device)
-    _check(_lib.moe_expert_forward_pipelined(_p(x), _p(w_gate), _p(w_up), _p(w_down),
-                                             _p(expert_ids), _p(probs), T, H, F, E, k, _p(y),
-                                             n_chunks, _p(ws), ws.numel(), ctypes.byref(c),
-                                             _stream(stream), _stream(aux_stream)),
-           "moe_expert_forward_pipelined")
+            aux_stream = _aux_streams.get(dev)
+            if aux_stream is None:
+                aux_stream = _aux_streams[dev] = torch.cuda.Stream(device=dev)
+        _check(_lib.moe_expert_forward_pipelined(_p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                                 _p(expert_ids), _p(probs), T, H, F, E, k, _p(y),
+                                                 n_chunks, _p(ws), ws.numel(), ctypes.byref(c),
+                                                 _stream(stream, dev), _stream(aux_stream, dev)),
+               "moe_expert_forward_pipelined")
     return y, ws
 
 
@@ -443,21 +530,32 @@ def moe_expert_backward(dy, x, w_gate, w_up, w_down, expert_ids, probs, fwd_work
     T, H = x.shape
     E, _, F = w_gate.shape
     k = expert_ids.shape[1]
-    dev = x.device
+    _cuda(dx, "dx", torch.bfloat16, T * H)
+    for t, n in ((dw_gate, "dw_gate"), (dw_up, "dw_up"), (dw_down, "dw_down")):
+        _cuda(t, n, torch.float32, E * H * F)
+    _cuda(dprobs, "dprobs", torch.float32, T * k)
+    _cuda(workspace, "workspace")
+    dev = _device(("dy", dy), ("x", x), ("w_gate", w_gate), ("w_up", w_up), ("w_down", w_down),
+                  ("expert_ids", expert_ids), ("probs", probs), ("fwd_workspace", fwd_workspace),
+                  ("dx", dx), ("dw_gate", dw_gate), ("dw_up", dw_up), ("dw_down", dw_down),
+                  ("dprobs", dprobs), ("workspace", workspace))
     c = cfg if cfg is not None else config(save_for_backward=True)
-    dx = torch.empty_like(x) if dx is None else dx
-    dw_gate = torch.empty((E, H, F), dtype=torch.float32, device=dev) if dw_gate is None else dw_gate
-    dw_up = torch.empty((E, H, F), dtype=torch.float32, device=dev) if dw_up is None else dw_up
-    dw_down = torch.empty((E, F, H), dtype=torch.float32, device=dev) if dw_down is None else dw_down
-    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
-    need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 1)
-    ws = _workspace(need, dev) if workspace is None else workspace
-    _check(_lib.moe_expert_backward(_p(dy), _p(x), _p(w_gate), _p(w_up), _p(w_down),
-                                    _p(expert_ids), _p(probs), T, H, F, E, k, _p(fwd_workspace),
-                                    fwd_workspace.numel(), _p(dx), _p(dw_gate), _p(dw_up),
-                                    _p(dw_down), _p(dprobs), int(bool(accumulate_dw)), _p(ws),
-                                    ws.numel(), ctypes.byref(c), _stream(stream)),
-           "moe_expert_backward")
+    with torch.cuda.device(dev):
+        dx = torch.empty_like(x) if dx is None else dx
+        f32 = dict(dtype=torch.float32, device=dev)
+        dw_gate = torch.empty((E, H, F), **f32) if dw_gate is None else dw_gate
+        dw_up = torch.empty((E, H, F), **f32) if dw_up is None else dw_up
+        dw_down = torch.empty((E, F, H), **f32) if dw_down is None else dw_down
+        dprobs = torch.empty((T, k), **f32) if dprobs is None else dprobs
+        need = _lib.moe_workspace_size(T, H, F, E, k, ctypes.byref(c), 1)
+        ws = _workspace(need, dev) if workspace is None else workspace
+        _check(_lib.moe_expert_backward(_p(dy), _p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                        _p(expert_ids), _p(probs), T, H, F, E, k,
+                                        _p(fwd_workspace), fwd_workspace.numel(), _p(dx),
+                                        _p(dw_gate), _p(dw_up), _p(dw_down), _p(dprobs),
+                                        int(bool(accumulate_dw)), _p(ws), ws.numel(),
+                                        ctypes.byref(c), _stream(stream, dev)),
+               "moe_expert_backward")
     return dict(dx=dx, dw_gate=dw_gate, dw_up=dw_up, dw_down=dw_down, dprobs=dprobs)
 
 
@@ -478,17 +576,25 @@ def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, 
     for t, n in ((wg_q, "wg_q"), (wg_s, "wg_s"), (wu_q, "wu_q"), (wu_s, "wu_s"), (wd_q, "wd_q"),
                  (wd_s, "wd_s")):
         _cuda(t, n, torch.uint8)
+    _cuda(expert_ids, "expert_ids", torch.int32)
+    _cuda(probs, "probs", torch.float32)
     T, H = x.shape
     E, F, _ = wg_q.shape
     k = expert_ids.shape[1]
+    _cuda(y, "y", torch.bfloat16, T * H)
+    _cuda(workspace, "workspace")
+    dev = _device(("x", x), ("wg_q", wg_q), ("wg_s", wg_s), ("wu_q", wu_q), ("wu_s", wu_s),
+                  ("wd_q", wd_q), ("wd_s", wd_s), ("expert_ids", expert_ids), ("probs", probs),
+                  ("y", y), ("workspace", workspace))
     c = cfg if cfg is not None else config()
     need = _lib.moe_workspace_size_mxfp8(T, H, F, E, k, ctypes.byref(c))
-    ws = _workspace(need, x.device) if workspace is None else workspace
-    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device) if y is None else y
-    _check(_lib.moe_expert_forward_mxfp8(_p(x), _p(wg_q), _p(wg_s), _p(wu_q), _p(wu_s), _p(wd_q),
-                                         _p(wd_s), _p(expert_ids), _p(probs), T, H, F, E, k,
-                                         _p(y), _p(ws), ws.numel(), ctypes.byref(c),
-                                         _stream(stream)), "moe_expert_forward_mxfp8")
+    with torch.cuda.device(dev):
+        ws = _workspace(need, dev) if workspace is None else workspace
+        y = torch.empty((T, H), dtype=torch.bfloat16, device=dev) if y is None else y
+        _check(_lib.moe_expert_forward_mxfp8(_p(x), _p(wg_q), _p(wg_s), _p(wu_q), _p(wu_s),
+                                             _p(wd_q), _p(wd_s), _p(expert_ids), _p(probs), T, H,
+                                             F, E, k, _p(y), _p(ws), ws.numel(), ctypes.byref(c),
+                                             _stream(stream, dev)), "moe_expert_forward_mxfp8")
     return y, ws
 
 
@@ -511,23 +617,32 @@ def moe_expert_backward_mxfp8(dy, x, w1g_q, w1g_s, w1u_q, w1u_s, w2_q, w2_s, exp
     T, H = x.shape
     E, _, F = w1g_q.shape
     k = expert_ids.shape[1]
-    dev = x.device
+    _cuda(dx, "dx", torch.bfloat16, T * H)
+    for t, n in ((dw_gate_t, "dw_gate_t"), (dw_up_t, "dw_up_t"), (dw_down_t, "dw_down_t")):
+        _cuda(t, n, torch.float32, E * H * F)
+    _cuda(dprobs, "dprobs", torch.float32, T * k)
+    _cuda(workspace, "workspace")
+    dev = _device(("dy", dy), ("x", x), ("w1g_q", w1g_q), ("w1g_s", w1g_s), ("w1u_q", w1u_q),
+                  ("w1u_s", w1u_s), ("w2_q", w2_q), ("w2_s", w2_s), ("expert_ids", expert_ids),
+                  ("probs", probs), ("fwd_workspace", fwd_workspace), ("dx", dx),
+                  ("dw_gate_t", dw_gate_t), ("dw_up_t", dw_up_t), ("dw_down_t", dw_down_t),
+                  ("dprobs", dprobs), ("workspace", workspace))
     c = cfg if cfg is not None else config(save_for_backward=True)
-    dx = torch.empty_like(x) if dx is None else dx
-    dw_gate_t = (torch.empty((E, F, H), dtype=torch.float32, device=dev)
-                 if dw_gate_t is None else dw_gate_t)
-    dw_up_t = torch.empty((E, F, H), dtype=torch.float32, device=dev) if dw_up_t is None else dw_up_t
-    dw_down_t = (torch.empty((E, H, F), dtype=torch.float32, device=dev)
-                 if dw_down_t is None else dw_down_t)
-    dprobs = torch.empty((T, k), dtype=torch.float32, device=dev) if dprobs is None else dprobs
-    need = _lib.moe_workspace_size_mxfp8_backward(T, H, F, E, k)
-    ws = _workspace(need, dev) if workspace is None else workspace
-    _check(_lib.moe_expert_backward_mxfp8(_p(dy), _p(x), _p(w1g_q), _p(w1g_s), _p(w1u_q),
-                                          _p(w1u_s), _p(w2_q), _p(w2_s), _p(expert_ids),
-                                          _p(probs), T, H, F, E, k, _p(fwd_workspace),
-                                          fwd_workspace.numel(), _p(dx), _p(dw_gate_t),
-                                          _p(dw_up_t), _p(dw_down_t), _p(dprobs),
-                                          int(bool(accumulate_dw)), _p(ws), ws.numel(),
-                                          ctypes.byref(c), _stream(stream)),
-           "moe_expert_backward_mxfp8")
+    with torch.cuda.device(dev):
+        dx = torch.empty_like(x) if dx is None else dx
+        f32 = dict(dtype=torch.float32, device=dev)
+        dw_gate_t = torch.empty((E, F, H), **f32) if dw_gate_t is None else dw_gate_t
+        dw_up_t = torch.empty((E, F, H), **f32) if dw_up_t is None else dw_up_t
+        dw_down_t = torch.empty((E, H, F), **f32) if dw_down_t is None else dw_down_t
+        dprobs = torch.empty((T, k), **f32) if dprobs is None else dprobs
+        need = _lib.moe_workspace_size_mxfp8_backward(T, H, F, E, k)
+        ws = _workspace(need, dev) if workspace is None else workspace
+        _check(_lib.moe_expert_backward_mxfp8(_p(dy), _p(x), _p(w1g_q), _p(w1g_s), _p(w1u_q),
+                                              _p(w1u_s), _p(w2_q), _p(w2_s), _p(expert_ids),
+                                              _p(probs), T, H, F, E, k, _p(fwd_workspace),
+                                              fwd_workspace.numel(), _p(dx), _p(dw_gate_t),
+                                              _p(dw_up_t), _p(dw_down_t), _p(dprobs),
+                                              int(bool(accumulate_dw)), _p(ws), ws.numel(),
+                                              ctypes.byref(c), _stream(stream, dev)),
+               "moe_expert_backward_mxfp8")
     return dict(dx=dx, dw_gate_t=dw_gate_t, dw_up_t=dw_up_t, dw_down_t=dw_down_t, dprobs=dprobs)

@@ -89,6 +89,61 @@ def test_binding_rejects_host_tensors_before_the_library(lib):
 
 
 
+class _FakeCuda:
+    """Stands in for a contiguous CUDA tensor on device `index`: enough of
+    the tensor interface for the binding's checks, and a data_ptr that fails
+    the test if a call ever gets as far as the library."""
+
+    def __init__(self, shape, dtype, index=0):
+        import torch
+        self.shape = torch.Size(shape)
+        self.dtype = dtype
+        self.device = torch.device("cuda", index)
+        self.is_cuda = True
+
+    def is_contiguous(self):
+        return True
+
+    def numel(self):
+        n = 1
+        for d in self.shape:
+            n *= d
+        return n
+
+    def data_ptr(self):
+        raise AssertionError("the call reached the library")
+
+
+def test_binding_refuses_tensors_on_two_devices(lib):
+    # every kernel of a call runs on the device of its tensors: a call whose
+    # tensors (inputs, outputs or workspace) span two devices is refused on
+    # the host, and so are outputs of the wrong type or size
+    import torch
+    import moe_expert_dispatch_gb300 as m
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    ids0 = _FakeCuda((4, 2), i32, 0)
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_counts(ids0, 8, counts=_FakeCuda((8,), i32, 1))
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_counts_static(ids0, 8, offsets=_FakeCuda((9,), i32, 1))
+    with pytest.raises(ValueError, match="at least 9"):
+        m.moe_counts_static(ids0, 8, offsets=_FakeCuda((8,), i32, 0))
+    with pytest.raises(ValueError, match="int32"):
+        m.moe_counts(ids0, 8, counts=_FakeCuda((8,), f32, 0))
+    x, wg, wu, wd = (_FakeCuda((4, 128), bf), _FakeCuda((8, 128, 256), bf),
+                     _FakeCuda((8, 128, 256), bf), _FakeCuda((8, 256, 128), bf))
+    probs = _FakeCuda((4, 2), f32, 0)
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_expert_forward(x, wg, wu, _FakeCuda((8, 256, 128), bf, 1), ids0, probs)
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_expert_forward(x, wg, wu, wd, ids0, probs, y=_FakeCuda((4, 128), bf, 1))
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_expert_backward(x, x, wg, wu, wd, ids0, probs, _FakeCuda((1024,), torch.uint8, 0),
+                              dprobs=_FakeCuda((4, 2), f32, 1))
+    with pytest.raises(ValueError, match="one device"):
+        m.moe_unpermute(_FakeCuda((8, 128), bf, 1), ids0, probs)
+
+
 def test_package_refuses_to_import_without_the_library(tmp_path):
     # a copy of the package without libmoe_gb300.so: the import fails loudly
     # instead of falling back to anything else

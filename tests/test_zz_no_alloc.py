@@ -1,7 +1,8 @@
 """moe_counts_static, the counting entry point for callers that cannot
 allocate device memory at call time (its scratch is a fixed array inside the
-library), against moe_counts with a caller workspace: identical counts and
-offsets on two calls in a row, and a clear error past its size limit.
+library), against the CPU oracle and against moe_counts with a caller
+workspace: identical counts and offsets on two calls in a row, no device
+memory taken by a call, and a clear error past its size limit.
 
 Kept in a file that pytest collects last, so that a run stopping at the
 first failure has run every other test before this one."""
@@ -10,6 +11,8 @@ import ctypes
 import numpy as np
 import pytest
 import torch
+
+import oracle as orc
 
 pytestmark = pytest.mark.gpu
 m = pytest.importorskip("moe_expert_dispatch_gb300")
@@ -37,7 +40,31 @@ def test_counts_static_matches_workspace_counts_twice():
         assert m.moe_get_error() == 0
         assert torch.equal(got_c, want_c)
         assert torch.equal(got_o, want_o)
-        assert int(got_c.sum()) == ids.numel()
+        ref_c = orc.expert_counts(ids_np, E)
+        assert np.array_equal(got_c.cpu().numpy(), ref_c)
+        assert np.array_equal(got_o.cpu().numpy(), orc.expert_offsets(ref_c))
+
+
+def test_counts_static_takes_no_device_memory():
+    """After one call on the device (which loads its kernels and looks up
+    the scratch address), a call with preallocated outputs changes neither
+    the device's free memory nor what torch has allocated."""
+    ids = torch.from_numpy(np.random.default_rng(7).integers(0, 64, (4096, 6))
+                           .astype(np.int32)).cuda()
+    _via_c_abi(ids, 64)
+    counts = torch.empty(64, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(65, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    free0, alloc0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+    st = m._lib.moe_counts_static(ctypes.c_void_p(ids.data_ptr()), ids.numel(), 64,
+                                  ctypes.c_void_p(counts.data_ptr()),
+                                  ctypes.c_void_p(offsets.data_ptr()),
+                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert torch.cuda.memory_allocated() == alloc0
+    assert int(counts.sum()) == ids.numel()
 
 
 def test_counts_static_rejects_sizes_past_its_scratch():
