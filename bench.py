@@ -105,7 +105,10 @@ def _peaks(sustained: bool = False):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """SM clock, power and throttle reasons sampled every 20 ms by one
+    nvidia-smi process in loop mode while the GPU runs the settle pass and the
+    timed region; each sample carries its host time, so that the summary can
+    count the samples inside the timed region itself."""
 
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
@@ -113,43 +116,58 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
-        self._stop = threading.Event()
+        self.samples = []          # (host time, fields)
+        self.timed = None          # (start, end) host times of the timed region
+        self._p = None
         self._t = None
 
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                      "--format=csv,noheader,nounits"], capture_output=True,
-                                     text=True, timeout=5).stdout.strip()
-                if out:
-                    self.samples.append([v.strip() for v in out.split(",")])
-            except Exception:
-                pass
-            self._stop.wait(0.05)
+    def _read(self):
+        for line in self._p.stdout:
+            line = line.strip()
+            if line:
+                self.samples.append((time.monotonic(), [v.strip() for v in line.split(",")]))
 
     def __enter__(self):
-        self._t = threading.Thread(target=self._run, daemon=True)
-        self._t.start()
+        try:
+            self._p = subprocess.Popen(["nvidia-smi", "-i", str(self.index),
+                                        "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                        "-lms", "20"], stdout=subprocess.PIPE,
+                                       stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.1)        # the first sample precedes the load
+        except Exception:
+            self._p = None
         return self
 
     def __exit__(self, *a):
-        self._stop.set()
-        self._t.join(timeout=10)
+        if self._p is not None:
+            self._p.terminate()
+            try:
+                self._p.wait(timeout=10)
+            except Exception:
+                self._p.kill()
+            self._t.join(timeout=10)
 
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         num = lambda v: v.replace(".", "", 1).isdigit()  # noqa: E731
-        sm = [float(s[0]) for s in self.samples if num(s[0])]
-        mx = [float(s[1]) for s in self.samples if num(s[1])]
+        rows = [f for _, f in self.samples]
+        sm = [float(f[0]) for f in rows if num(f[0])]
+        mx = [float(f[1]) for f in rows if num(f[1])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4)
-                          if len(s) > 3 + i and s[3 + i].lower() == "active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(self.samples)}
+        reasons = sorted({names[i] for f in rows for i in range(4)
+                          if len(f) > 3 + i and f[3 + i].lower() == "active"})
+        out = {"sm_mhz": float(np.median(sm)) if sm else None,
+               "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+               "samples": len(rows)}
+        if self.timed is not None:
+            t0, t1 = self.timed
+            tsm = [float(f[0]) for t, f in self.samples if t0 <= t <= t1 and num(f[0])]
+            out["samples_timed"] = len(tsm)
+            out["sm_mhz_timed"] = float(np.median(tsm)) if tsm else None
+        return out
 
 
 def _dist():
@@ -229,15 +247,21 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     inp = synth.make_inputs(w, 0)
+    steps = args.steps if args.steps > 0 else 3
     for _ in range(args.warmup):          # untimed, as the GPU arm's warm-up steps
         cpu_oracle_sample(w, inp, args.ref_tokens)
-    times = [cpu_oracle_sample(w, inp, args.ref_tokens)["seconds"]
-             for _ in range(max(1, args.steps))]
+    times = [cpu_oracle_sample(w, inp, args.ref_tokens)["seconds"] for _ in range(steps)]
     sec_per_token = float(np.mean(times)) / args.ref_tokens
     value = 1.0 / sec_per_token
+    # a step of this arm is one sampled step of ref_tokens tokens; its
+    # ms_per_step is that step's measured time. The full batch's time at the
+    # same rate is an extrapolation, reported under its own name.
     line = {"impl": "reference", "metric": "MoE expert-block tokens/s", "value": value,
-            "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": sec_per_token * w.T * 1e3, "higher_is_better": True,
+            "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": float(np.mean(times)) * 1e3,
+            "tokens_per_step": args.ref_tokens,
+            "extrapolated_ms_per_full_batch": sec_per_token * w.T * 1e3,
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _cpu_threads(),
@@ -260,8 +284,10 @@ class Runner:
         self.m, self.w, self.dev = m, w, device
         self.gate = gate
         self.chunks = chunks
-        if chunks and (w.mxfp8 or w.backward or gate):
-            raise SystemExit("--chunks pipelines the BF16 forward from given ids only")
+        if chunks and (w.mxfp8 or gate):
+            raise SystemExit("--chunks runs the BF16 block from given ids only")
+        if chunks and w.T % chunks:
+            raise SystemExit(f"--chunks {chunks} does not divide T = {w.T}")
         if gate:
             if w.mxfp8 or w.routing not in ("router", "gaussian"):
                 raise SystemExit(f"--gate needs a BF16 workload routed from logits, not {w.name}")
@@ -320,7 +346,7 @@ class Runner:
             self.cfg_ev = m.config(save_for_backward=save, fuse_gather=fuse_gather,
                                    num_sms=gemm_sms, step_events=self.fev)
             nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
-            if chunks:
+            if chunks and not w.backward:
                 nbytes = max(nbytes, m._lib.moe_workspace_size_pipelined(T, H, F, E, k, chunks))
             self.dtype = "bf16"
             self.launches = 6 if (fuse_gather and not save) else 7
@@ -340,6 +366,15 @@ class Runner:
                     dw_down=torch.empty((E, F, H), dtype=torch.float32, device=device),
                     dprobs=torch.empty((T, k), dtype=torch.float32, device=device))
                 self.launches = (7 if gate else 8) + 7
+                if chunks:
+                    # micro-batches: the whole step once per chunk, one chunk's
+                    # workspaces reused by every chunk
+                    tc = T // chunks
+                    self.launches = 15 * chunks
+                    self.cwork = torch.empty(m.moe_workspace_size(tc, H, F, E, k, self.cfg),
+                                             dtype=torch.uint8, device=device)
+                    self.cbws = torch.empty(m.moe_workspace_size(tc, H, F, E, k, self.cfg, True),
+                                            dtype=torch.uint8, device=device)
         self.work = torch.empty(nbytes, dtype=torch.uint8, device=device)
         # per-kernel FLOPs of the grouped GEMMs (algorithmic: routed rows only)
         self.flops = {"fc1_swiglu": 4.0 * R * H * F, "fc2": 2.0 * R * F * H}
@@ -372,6 +407,22 @@ class Runner:
                                             dw_down_t=g["dw_down_t"], dprobs=g["dprobs"],
                                             workspace=self.bws,
                                             cfg=self.cfg_bev if events else self.cfg)
+            return
+        if self.chunks and self.w.backward and not plain:
+            # the training step over micro-batches of T / chunks tokens: each
+            # chunk's forward and backward, dX, dprobs and y into the chunk's
+            # rows, the weight gradients accumulated over the chunks
+            g, tc = self.grads, self.w.T // self.chunks
+            dy = self.dy if dy is None else dy
+            for c in range(self.chunks):
+                sl = slice(c * tc, (c + 1) * tc)
+                m.moe_expert_forward(x[sl], self.wg, self.wu, self.wd, ids[sl], probs[sl],
+                                     y=self.y[sl], workspace=self.cwork, cfg=self.cfg)
+                m.moe_expert_backward(dy[sl], x[sl], self.wg, self.wu, self.wd, ids[sl],
+                                      probs[sl], self.cwork, dx=g["dx"][sl], dw_gate=g["dw_gate"],
+                                      dw_up=g["dw_up"], dw_down=g["dw_down"],
+                                      dprobs=g["dprobs"][sl], accumulate_dw=c > 0,
+                                      workspace=self.cbws, cfg=self.cfg)
             return
         if self.chunks and not plain:
             m.moe_expert_forward_pipelined(x, self.wg, self.wu, self.wd, ids, probs, self.chunks,
@@ -429,13 +480,26 @@ def run_ours(args, w):
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
-    for _ in range(warm):
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(warm):
         flush.zero_()
+        if i == warm - 1:
+            w0.record(stream)
         run.step(False)
+        if i == warm - 1:
+            w1.record(stream)
     torch.cuda.synchronize()
     st = m.moe_get_error()
     if st != 0:
         raise RuntimeError(f"device error {st}")
+    step_s = _max_over_ranks(max(w0.elapsed_time(w1), 1e-3) * 1e-3, ws, device)
+    # steps: as asked, else enough for about a second of timed work; a
+    # timed region shorter than that is preceded by untimed settle steps, so
+    # that the clocks are sampled, and the timed steps run, under a load
+    # that has lasted about a second
+    if args.steps <= 0:
+        args.steps = int(min(2000, max(20, np.ceil(1.0 / step_s))))
+    settle = int(max(0, np.ceil((1.0 - args.steps * step_s) / step_s)))
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -471,6 +535,14 @@ def run_ours(args, w):
     _barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        for _ in range(settle):
+            flush.zero_()
+            if graph is not None:
+                graph.replay()
+            else:
+                run.step(False)
+        torch.cuda.synchronize()
+        t_timed0 = time.monotonic()
         for i in range(args.steps):
             flush.zero_()
             starts[i].record(stream)
@@ -484,6 +556,7 @@ def run_ours(args, w):
                 for key, v in run.parts().items():
                     parts[key] = parts.get(key, 0.0) + v
         torch.cuda.synchronize()
+        clk.timed = (t_timed0, time.monotonic())
     _barrier(ws)
     ms = _max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(starts, ends)])), ws,
                          device)
@@ -597,7 +670,10 @@ def run_ours(args, w):
     e2e_loop = "pipelined" if piped_ms <= seq_ms else "sequential"
     e2e_ms = _max_over_ranks(min(piped_ms, seq_ms), ws, device)
 
-    hbm, bf16_peak, peak_src = _peaks(sustained=bool(w.backward))
+    # every timed step follows about a second of load (the settle pass, or the
+    # timed region itself): the kernels run at the clocks of sustained work,
+    # under the power cap, so they are held to the sustained peak
+    hbm, bf16_peak, peak_src = _peaks(sustained=True)
     peak = bf16_peak * (FP8_OVER_BF16 if w.mxfp8 else 1.0)
     tflops = {key: run.flops[key] / (parts[key] * 1e-3) / 1e12 for key in run.flops}
     dominant = max(run.flops, key=lambda key: parts[key])
@@ -623,8 +699,17 @@ def run_ours(args, w):
                            "tokens_per_s": {"pipelined": ws * w.T / (piped_ms * 1e-3),
                                             "sequential": ws * w.T / (seq_ms * 1e-3)}},
                    "launch": "one CUDA graph per step" if args.graph else "stream launches",
-                   "pipeline": (f"{run.chunks} token chunks, routing and combine on a second "
-                                "stream (per-kernel times from unpipelined steps)"
+                   "settle_steps": settle,
+                   "settle": ("untimed steps run right before the timed region, after the "
+                              "warm-up, when the timed region alone is shorter than a second: "
+                              "the clocks are sampled, and the timed steps run, under a load "
+                              "that has lasted about a second"),
+                   "pipeline": (("micro-batch split of the training step into "
+                                 f"{run.chunks} chunks of {w.T // run.chunks} tokens, dW "
+                                 "accumulated (per-kernel times from unsplit steps)")
+                                if run.chunks and w.backward else
+                                (f"{run.chunks} token chunks, routing and combine on a second "
+                                 "stream (per-kernel times from unpipelined steps)")
                                 if run.chunks else "none"),
                    "gemm_ctas": args.gemm_sms or "one per SM",
                    "routing": ("fused top-k gate from float32 router logits [T, E]" if run.gate
@@ -656,7 +741,9 @@ def run_ours(args, w):
 def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps (default: enough for about a second of timed work; "
+                         "3 sampled steps for --impl reference)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mixtral_bf16", choices=list(synth.WORKLOADS))
@@ -667,7 +754,8 @@ def build_parser() -> argparse.ArgumentParser:
                     help="BF16 forward from router logits: the fused top-k gate replaces the "
                          "counting step")
     ap.add_argument("--chunks", type=int, default=0,
-                    help="BF16 forward: micro-batch pipeline over this many token chunks")
+                    help="BF16 forward: micro-batch pipeline over this many token chunks; "
+                         "BF16 training step: run it as this many micro-batches")
     ap.add_argument("--gemm-sms", type=int, default=0,
                     help="persistent GEMM grid size (default: one CTA per SM)")
     ap.add_argument("--graph", action="store_true",

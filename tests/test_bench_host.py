@@ -24,6 +24,10 @@ def test_reference_arm_prints_one_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny_bf16"
     assert 1 <= d["cpu_baseline"]["cores"] <= os.cpu_count()
+    # a step of this arm is the sampled step that was timed, not the full batch
+    assert d["tokens_per_step"] == 2 and d["steps"] == 1
+    assert abs(d["ms_per_step"] - 2 / d["value"] * 1e3) <= 1e-6 * d["ms_per_step"]
+    assert d["extrapolated_ms_per_full_batch"] > d["ms_per_step"]
 
 
 def test_reference_arm_under_torchrun_prints_once():
