@@ -279,7 +279,7 @@ class Runner:
     """The timed step of one workload kind, its per-kernel events and FLOPs."""
 
     def __init__(self, m, w, inp, device, fuse_gather=False, mx_tile_n=0, gate=False, chunks=0,
-                 gemm_sms=0):
+                 gemm_sms=0, cta_pairs=0):
         import torch
         self.m, self.w, self.dev = m, w, device
         self.gate = gate
@@ -342,9 +342,10 @@ class Runner:
         else:
             self.wg, self.wu, self.wd = (inp[key].to(device) for key in ("w_gate", "w_up", "w_down"))
             save = bool(w.backward)
-            self.cfg = m.config(save_for_backward=save, fuse_gather=fuse_gather, num_sms=gemm_sms)
+            self.cfg = m.config(save_for_backward=save, fuse_gather=fuse_gather, num_sms=gemm_sms,
+                                cta_pairs=cta_pairs)
             self.cfg_ev = m.config(save_for_backward=save, fuse_gather=fuse_gather,
-                                   num_sms=gemm_sms, step_events=self.fev)
+                                   num_sms=gemm_sms, step_events=self.fev, cta_pairs=cta_pairs)
             nbytes = m.moe_workspace_size(T, H, F, E, k, self.cfg)
             if chunks and not w.backward:
                 nbytes = max(nbytes, m._lib.moe_workspace_size_pipelined(T, H, F, E, k, chunks))
@@ -356,7 +357,8 @@ class Runner:
                 self.launches = 7 * min(chunks, T)   # the whole forward once per chunk
             if w.backward:
                 self.dy = inp["dy"].to(device)
-                self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev)
+                self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev,
+                                        cta_pairs=cta_pairs)
                 self.bws = torch.empty(m.moe_workspace_size(T, H, F, E, k, self.cfg, True),
                                        dtype=torch.uint8, device=device)
                 self.grads = dict(
@@ -476,7 +478,8 @@ def run_ours(args, w):
 
     inp = synth.make_inputs(w, 0)
     run = Runner(m, w, inp, device, fuse_gather=args.fuse_gather, mx_tile_n=args.mxfp8_tile_n,
-                 gate=args.gate, chunks=args.chunks, gemm_sms=args.gemm_sms)
+                 gate=args.gate, chunks=args.chunks, gemm_sms=args.gemm_sms,
+                 cta_pairs=args.cta_pairs)
     stream = run.stream
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
     warm = max(3, args.warmup)
@@ -712,6 +715,7 @@ def run_ours(args, w):
                                  "stream (per-kernel times from unpipelined steps)")
                                 if run.chunks else "none"),
                    "gemm_ctas": args.gemm_sms or "one per SM",
+                   "cta_pairs": {0: "automatic", 1: "off", 2: "on"}[args.cta_pairs],
                    "routing": ("fused top-k gate from float32 router logits [T, E]" if run.gate
                                else "expert ids and weights given"),
                    "parallelism": "replicas" if ws > 1 else "single"},
@@ -758,6 +762,9 @@ def build_parser() -> argparse.ArgumentParser:
                          "BF16 training step: run it as this many micro-batches")
     ap.add_argument("--gemm-sms", type=int, default=0,
                     help="persistent GEMM grid size (default: one CTA per SM)")
+    ap.add_argument("--cta-pairs", type=int, default=0, choices=[0, 1, 2],
+                    help="BF16 GEMMs over routed rows: 2 = CTA pairs share M = 256 tiles, "
+                         "1 = one CTA per tile, 0 = automatic")
     ap.add_argument("--graph", action="store_true",
                     help="capture each step once into a CUDA graph and replay it")
     ap.add_argument("--fuse-gather", action=argparse.BooleanOptionalAction, default=False,

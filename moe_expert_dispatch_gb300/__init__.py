@@ -37,7 +37,8 @@ class moe_config(ctypes.Structure):
                 ("wait_limit_ns", ctypes.c_longlong),
                 ("step_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("num_step_events", ctypes.c_int),
-                ("mxfp8_tile_n", ctypes.c_int)]
+                ("mxfp8_tile_n", ctypes.c_int),
+                ("cta_pairs", ctypes.c_int)]
 
 STEP_EVENTS = 5       # forward: start, routing, fc1+SwiGLU, fc2, unpermute
 BWD_STEP_EVENTS = 7   # backward: start, dO+dprobs, dH, dXp, dX, dW1, dW2
@@ -147,7 +148,7 @@ def _device(*named):
 
 
 def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
-           wait_limit_ns=0, step_events=None, mxfp8_tile_n=0) -> moe_config:
+           wait_limit_ns=0, step_events=None, mxfp8_tile_n=0, cta_pairs=0) -> moe_config:
     """A moe_config; step_events: optional list of MOE_STEP_EVENTS torch.cuda.Event
     (already recorded once, so that their CUDA events exist)."""
     c = moe_config()
@@ -157,6 +158,7 @@ def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
     c.num_sms = num_sms
     c.fuse_gather = int(bool(fuse_gather))
     c.mxfp8_tile_n = mxfp8_tile_n
+    c.cta_pairs = cta_pairs
     if wait_limit_ns:
         c.wait_limit_ns = wait_limit_ns
     if step_events is not None:

@@ -246,6 +246,22 @@ cudaEvent_t* pipeline_events() {
   return pool[d];
 }
 
+// CTA pairs for the BF16 GEMMs over routed rows: as configured, else when
+// the experts average at least 4 row blocks of 128, where the half-filled
+// last tile of an expert with an odd block count costs little.
+bool use_pairs(const moe_config& c, int64_t R, int E) {
+  if (c.cta_pairs == 1) return false;
+  if (c.cta_pairs == 2) return true;
+  return R >= static_cast<int64_t>(4) * kTileM * E;
+}
+
+// Ring depth of the BF16 GEMMs: the configured one, capped at what fits
+// (4 slots of 48 KB for one CTA per tile, 6 of 32 KB for a CTA of a pair).
+int bf16_stages(const moe_config& c, bool pairs) {
+  const int cap = pairs ? 6 : 4;
+  return (c.ring_stages == 0 || c.ring_stages > cap) ? cap : c.ring_stages;
+}
+
 int grid_size(const moe_config& c) {
   const int sms = device_sm_count();
   return (c.num_sms > 0 && c.num_sms < sms) ? c.num_sms : sms;
@@ -548,7 +564,8 @@ struct FwdRun {
     g1.K = H;
     g1.N = F;
     g1.bn = 256;                 // 128 gate + 128 up columns per N tile
-    g1.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
+    g1.pair = (!gather && use_pairs(c, L.R, E)) ? 1 : 0;
+    g1.stages = bf16_stages(c, g1.pair != 0);
     g1.b_rows = H;
     g1.b_split = 1;
     g1.out = h;
@@ -791,6 +808,10 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   const int grid = grid_size(c);
   const int bnF = (F % 256 == 0) ? 256 : 128;
   const int bnH = (H % 256 == 0) ? 256 : 128;
+  // dH and dXp run on CTA pairs as the forward does; a pair's CTA reads its
+  // half of the K-major B tile, bn / 2 rows
+  const bool pairs = use_pairs(c, T * k, E);
+  const int bF = pairs ? bnF / 2 : bnF, bH = pairs ? bnH / 2 : bnH;
   auto mark = [&](int i) {
     if (c.step_events && i < c.num_step_events)
       cudaEventRecord(static_cast<cudaEvent_t>(c.step_events[i]), st);
@@ -809,13 +830,13 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   CUtensorMap t_do, t_w2k, t_da, t_wgk, t_wuk, t_xp_mn, t_da_mn, t_h_mn, t_do_mn;
   if (!make_tmap_bf16_2d(&t_do, d_o, H, B.cap, static_cast<uint64_t>(H) * 2, 64, kTileM) ||
       !make_tmap_bf16_2d(&t_w2k, w_down, H, static_cast<uint64_t>(E) * F,
-                         static_cast<uint64_t>(H) * 2, 64, bnF) ||
+                         static_cast<uint64_t>(H) * 2, 64, bF) ||
       !make_tmap_bf16_2d(&t_da, d_a, 2 * static_cast<uint64_t>(F), B.cap,
                          static_cast<uint64_t>(F) * 4, 64, kTileM) ||
       !make_tmap_bf16_2d(&t_wgk, w_gate, F, static_cast<uint64_t>(E) * H,
-                         static_cast<uint64_t>(F) * 2, 64, bnH) ||
+                         static_cast<uint64_t>(F) * 2, 64, bH) ||
       !make_tmap_bf16_2d(&t_wuk, w_up, F, static_cast<uint64_t>(E) * H,
-                         static_cast<uint64_t>(F) * 2, 64, bnH) ||
+                         static_cast<uint64_t>(F) * 2, 64, bH) ||
       !make_tmap_bf16_2d(&t_xp_mn, xp, H, L.cap, static_cast<uint64_t>(H) * 2, 64, 64) ||
       !make_tmap_bf16_2d(&t_da_mn, d_a, 2 * static_cast<uint64_t>(F), B.cap,
                          static_cast<uint64_t>(F) * 4, 64, 64) ||
@@ -827,10 +848,12 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   GroupedGemmArgs g{};
   g.off_al = off_al;
   g.E = E;
-  g.stages = (c.ring_stages == 0 || c.ring_stages > 4) ? 4 : c.ring_stages;
+  g.stages = bf16_stages(c, false);
   g.err = err;
   g.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
   GroupedGemmArgs gh = g;
+  gh.pair = pairs ? 1 : 0;
+  gh.stages = bf16_stages(c, pairs);
   gh.K = H;
   gh.N = F;
   gh.bn = bnF;
@@ -863,6 +886,8 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   // dXp = bf16(dA_g W1g^T + dA_u W1u^T) (one reduction over 2F), then
   // dX = bf16(sum_j dXp[row_of]), the combine with unit weights
   GroupedGemmArgs gx = g;
+  gx.pair = pairs ? 1 : 0;
+  gx.stages = bf16_stages(c, pairs);
   gx.K = 2 * F;
   gx.N = H;
   gx.bn = bnH;

@@ -15,6 +15,18 @@
 // stood, the full/empty mbarrier pair where the CrossCore set/wait flags
 // stood, and slot = k-block mod stages as bufferId = mLoopIdx mod bufferSize.
 //
+// CTA pairs (kPair, Rows schedules): the two CTAs of a cluster of two share
+// one tile of M = 256 (tcgen05.mma.cta_group::2). Each CTA loads its own 128
+// rows of A and half of the tile's B columns (gate or up of fc1, one half of
+// the N tile otherwise) into its own ring, so each SM streams half the B
+// bytes of a one-CTA tile for the same FLOPs; the slots (32 KB) are smaller,
+// and the ring is 6 deep. Both CTAs' copies complete on the leader's (rank
+// 0) full barrier, the leader's thread issues the MMAs, and their commits
+// release the slots and hand the accumulators to the epilogues of both CTAs;
+// each CTA finishes its own 128 rows. An expert whose segment has an odd
+// number of 128-row blocks ends in a tile whose second half lies past the
+// expert: there the second CTA loads no A rows and stores nothing.
+//
 // Two schedules share the kernel:
 //  * Rows (fc1, fc2, dH, dXp): expert e owns rows [off_al[e], off_al[e+1])
 //    of the permuted activations, a multiple of 128 (padded), i.e. one M
@@ -38,14 +50,21 @@ namespace {
 constexpr int BK = 64;                         // k-block (128 bytes of bf16)
 constexpr int kABytes = kTileM * BK * 2;       // 16 KB
 constexpr int kBBox = 64 * BK * 2;             // 8 KB: 64 columns x 64 of K
-constexpr int kStageBytes = kABytes + 4 * kBBox;  // 48 KB
+// A slot holds A and the CTA's B columns of the widest tile (N = 256): all of
+// them for one CTA (48 KB, 4 slots), half of them for a CTA of a pair (32 KB,
+// 6 slots).
+template <bool kPair>
+constexpr int stage_bytes() { return kABytes + (kPair ? 2 : 4) * kBBox; }
+template <bool kPair>
+constexpr int max_stages() { return kPair ? 6 : 4; }
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
+constexpr unsigned long long kPairDrainNs = 50000000ull;
 
 struct Smem {
-  uint64_t full[4];
-  uint64_t empty[4];
+  uint64_t full[6];
+  uint64_t empty[6];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -56,13 +75,20 @@ struct Smem {
 
 struct Tile {
   int e, m, n;
-  int row0;      // Rows: first A row; WGrad: first reduction row
+  int row0;      // Rows: first A row (of the pair's tile); WGrad: first reduction row
   int kblocks;
+  int half_rows; // pairs: 128-row blocks of the tile inside the expert (1 or 2)
 };
 
-template <Sched kSched>
+// M tiles of an expert with mt 128-row blocks: one per block, or one per two
+// blocks for CTA pairs (the last one half-filled when mt is odd).
+template <bool kPair>
+__device__ __forceinline__ int m_tiles(int mt) { return kPair ? (mt + 1) >> 1 : mt; }
+
+template <Sched kSched, bool kPair>
 __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedGemmArgs& p) {
   Tile tl;
+  tl.half_rows = 1;
   if (kSched == Sched::Rows) {
     int lo = 0, hi = p.E - 1;
     while (lo < hi) {
@@ -70,7 +96,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
       if (ts[mid] <= t) lo = mid; else hi = mid - 1;
     }
     tl.e = lo;
-    const int mt = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int mb = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int mt = m_tiles<kPair>(mb);
     const int nt = p.N / (p.b_split == 1 ? p.bn / 2 : p.bn);
     const int local = t - ts[tl.e];
     if (mt > nt) {            // tall expert: its row panel is the larger operand, keep it in L2
@@ -80,7 +107,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
       tl.n = local / mt;
       tl.m = local - tl.n * mt;
     }
-    tl.row0 = p.off_al[tl.e] + tl.m * kTileM;
+    tl.row0 = p.off_al[tl.e] + tl.m * (kPair ? 2 * kTileM : kTileM);
+    if (kPair) tl.half_rows = min(2, mb - 2 * tl.m);
     tl.kblocks = p.K / BK;
   } else {
     const int mt = p.M / kTileM;
@@ -111,7 +139,7 @@ constexpr int kPieceBytes = 32 * 64;       // 2 KB
 constexpr int kSlotsPerWarp = 3;
 constexpr int kPieceArea = 4 * kSlotsPerWarp * kPieceBytes;   // 24 KB
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
@@ -122,15 +150,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  static_assert(!kPair || (kSched == Sched::Rows && !kGather && !kAmn),
+                "CTA pairs run the Rows schedule with a K-major A");
+  constexpr int kStageBytes = stage_bytes<kPair>();
   const int S = p.stages;
-  uint8_t* pieces = ring + 4 * kStageBytes;  // after the largest ring, 1 KB aligned
+  uint8_t* pieces = ring + max_stages<kPair>() * kStageBytes;  // after the largest ring
   Smem* sm = reinterpret_cast<Smem*>(pieces + kPieceArea);
   int* ts = reinterpret_cast<int*>(sm + 1);  // [E+1] first tile of each expert (Rows)
   const int warp = threadIdx.x >> 5, lane = lane_id();
   const int E = p.E;
   constexpr int bn = kBN;                     // MMA N
   const int n_tiles = p.N / (kEpi == Epi::SwigluFwd ? bn / 2 : bn);
-  constexpr uint32_t stage_tx = kABytes + (bn / 64) * kBBox;
+  constexpr uint32_t stage_tx = kABytes + (bn / 64) * kBBox;   // one-CTA tile
+  // CTA pairs: this CTA's rank, the tile walk over clusters, and the
+  // leader's barriers as seen from either CTA
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;
+  const int walk0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int walk_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -139,7 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm->tfull[a]), 1);
-      mbar_init(smem_u32(&sm->tempty[a]), 4 * 32);
+      // one arrival per epilogue warp (of both CTAs of a pair: the leader's
+      // MMAs overwrite both CTAs' accumulators)
+      mbar_init(smem_u32(&sm->tempty[a]), kPair ? 8 : 4);
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort = 0;
@@ -153,13 +191,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmO0);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(&sm->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   int total;
   if (kSched == Sched::Rows) {
     for (int e = threadIdx.x; e < E; e += kThreads)
-      ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+      ts[e + 1] = m_tiles<kPair>((p.off_al[e + 1] - p.off_al[e]) / kTileM) * n_tiles;
     __syncthreads();
     if (threadIdx.x == 0) {
       ts[0] = 0;
@@ -168,6 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
   if (kSched == Sched::Rows) total = ts[E];
@@ -185,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t fills = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<kSched>(t, ts, p);
+    for (int t = walk0; t < total && ok; t += walk_step) {
+      const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
       const int real_end = p.off_al[tl.e] + p.counts[tl.e];
       int tok[4];
 #pragma unroll
@@ -243,24 +287,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t fills = 0;
       bool ok = true;
       const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
+      const uint64_t pol_b = l2_policy_evict_normal();
       const uint32_t ring0 = smem_u32(ring);
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<kSched>(t, ts, p);
+      for (int t = walk0; t < total && ok; t += walk_step) {
+        const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
         // per-tile coordinates
         const int a_x0 = kAmn ? tl.m * kTileM : 0;
-        const int a_y0 = tl.row0;
+        const int a_y0 = tl.row0 + static_cast<int>(rank) * kTileM;
         const int b_row0 = (kSched == Sched::Rows) ? tl.e * static_cast<int>(p.b_rows) : tl.row0;
         const int b_n0 = (kEpi == Epi::SwigluFwd) ? tl.n * (bn / 2) : tl.n * bn;
+        // pairs: the second CTA's rows may lie past the expert (odd tail)
+        const bool load_a = !kPair || static_cast<int>(rank) < tl.half_rows;
         for (int kb = 0; kb < tl.kblocks; ++kb) {
           const uint32_t full = smem_u32(&sm->full[stage]);
           if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full, stage_tx);
           const uint32_t sa = ring0 + stage * kStageBytes;
           const uint32_t sb = sa + kABytes;
           const int k0 = kb * BK;
+          if constexpr (kPair) {
+            // both CTAs' copies complete on the leader's full barrier, which
+            // the leader arms with the bytes of the whole pair tile
+            const uint32_t full_l = mapa_shared(full, 0);
+            if (rank == 0)
+              mbar_arrive_expect_tx(full, tl.half_rows * kABytes + (bn / 64) * kBBox);
+            if (load_a) tma_load_2d_pair(sa, &tmA, full_l, k0, a_y0, pol_a);
+            if (kBmn) {       // this CTA's half of the N tile: bn / 128 boxes of 64 columns
+              const int krow = b_row0 + k0;
+              const CUtensorMap* mb = (kEpi == Epi::SwigluFwd && rank == 1) ? &tmB1 : &tmB0;
+              const int n0 = (kEpi == Epi::SwigluFwd) ? b_n0 : b_n0 + static_cast<int>(rank) * (bn / 2);
+#pragma unroll
+              for (int j = 0; j < bn / 128; ++j)
+                tma_load_2d_pair(sb + j * kBBox, mb, full_l, n0 + 64 * j, krow, pol_b);
+            } else {          // K-major B: this CTA's bn / 2 rows in one box
+              const int nrow = b_row0 + b_n0 + static_cast<int>(rank) * (bn / 2);
+              if (p.b_split == 2 && kb >= p.k_split)
+                tma_load_2d_pair(sb, &tmB1, full_l, k0 - p.k_split * BK, nrow, pol_b);
+              else
+                tma_load_2d_pair(sb, &tmB0, full_l, k0, nrow, pol_b);
+            }
+            ++fills;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1;
+            }
+            continue;
+          }
+          mbar_arrive_expect_tx(full, stage_tx);
           if (!kAmn) {
             tma_load_2d_hint(sa, &tmA, full, k0, a_y0, pol_a);
           } else {
@@ -299,14 +374,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_error(p.err, kErrTimeout);
       }
       // every issued copy must land before the CTA may exit: the last S fills
-      // (fill i went to slot i % S with phase parity (i / S) & 1)
-      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
-        mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
+      // (fill i went to slot i % S with phase parity (i / S) & 1). A pair's
+      // copies complete on the leader's barrier; here each CTA waits until
+      // the MMAs that read its last fills released them (a slot is released
+      // only after both CTAs' copies into it landed). After an abort the
+      // MMAs may never come, so those waits are short: a copy lands within
+      // microseconds.
+      for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i) {
+        if (kPair)
+          mbar_wait(smem_u32(&sm->empty[i % S]), (i / S) & 1, kPairDrainNs, &sm->zero);
+        else
+          mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kTileM, bn, kAmn, kBmn);
+    if (lane == 0 && rank == 0) {   // pairs: the leader's thread issues for both CTAs
+      const uint32_t idesc = idesc_bf16(kPair ? 2 * kTileM : kTileM, bn, kAmn, kBmn);
       // descriptors of slot 0; a slot adds kStageBytes, a K=16 step adds 32 B
       // (K-major) or 16 rows = 2 KB (MN-major) to the 16-byte start field
       const uint32_t ring0 = smem_u32(ring);
@@ -320,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true, issued = false;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<kSched>(t, ts, p);
+      for (int t = walk0; t < total && ok; t += walk_step) {
+        const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
         if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
           ok = false;
           break;
@@ -339,10 +423,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           // groups 1024 B apart (SBO), +16 rows = 2 KB per K=16.
           const uint64_t soff = static_cast<uint64_t>(stage) * (kStageBytes >> 4);
           const uint64_t ad = adesc0 + soff, bd = bdesc0 + soff;
+          if constexpr (kPair) {
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks)
-            umma_bf16(d, ad + ks * kAStep, bd + ks * kBStep, idesc, (kb | ks) ? 1u : 0u);
-          umma_commit(smem_u32(&sm->empty[stage]));
+            for (int ks = 0; ks < BK / 16; ++ks)
+              umma_bf16_pair(d, ad + ks * kAStep, bd + ks * kBStep, idesc, (kb | ks) ? 1u : 0u);
+            umma_commit_pair_mc(smem_u32(&sm->empty[stage]), 0x3);   // the slot, in both CTAs
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < BK / 16; ++ks)
+              umma_bf16(d, ad + ks * kAStep, bd + ks * kBStep, idesc, (kb | ks) ? 1u : 0u);
+            umma_commit(smem_u32(&sm->empty[stage]));
+          }
           issued = true;
           if (++stage == S) {
             stage = 0;
@@ -350,7 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&sm->tfull[acc]));   // also for a tile with no k-block
+        if (kPair)
+          umma_commit_pair_mc(smem_u32(&sm->tfull[acc]), 0x3);   // both CTAs' epilogues
+        else
+          umma_commit(smem_u32(&sm->tfull[acc]));   // also for a tile with no k-block
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
@@ -359,7 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_error(p.err, kErrTimeout);
       }
       if (issued) {
-        umma_commit(smem_u32(&sm->drain));
+        if (kPair)
+          umma_commit_pair_mc(smem_u32(&sm->drain), 0x1);
+        else
+          umma_commit(smem_u32(&sm->drain));
         mbar_wait(smem_u32(&sm->drain), 0, kDrainNs, &sm->zero);
       }
     }
@@ -429,13 +526,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile tl = decode_tile<kSched>(t, ts, p);
+    // the accumulator is handed back to the MMA issuer (the leader, for a
+    // pair) by one arrival per warp
+    const uint32_t tempty0 = kPair ? mapa_shared(smem_u32(&sm->tempty[0]), 0) : 0;
+    for (int t = walk0; t < total; t += walk_step) {
+      Tile tl = decode_tile<kSched, kPair>(t, ts, p);
+      tl.row0 += static_cast<int>(rank) * kTileM;   // this CTA's 128 rows
+      const bool live = !kPair || static_cast<int>(rank) < tl.half_rows;
       // SwigluBwd: the warp's rows of A_g, A_u for the tile's first 32
       // columns arrive while its MMAs run; the other blocks go to L2 now
       uint32_t ag_w[16], au_w[16];
       const int64_t wrow0 = tl.row0 + q * 32;
-      if (kEpi == Epi::SwigluBwd) {
+      if (kEpi == Epi::SwigluBwd && live) {
 #pragma unroll 1
         for (int c = 32; c < bn; c += 32)       // 16 lines per block: lanes 0-15 A_g
           prefetch_l2((lane < 16 ? p.act_g : p.act_u) +
@@ -452,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * 256;
-      if (kEpi == Epi::SwigluFwd) {
+      if (!live) {
+        // pairs: rows past the expert; the accumulator holds nothing to keep
+      } else if (kEpi == Epi::SwigluFwd) {
         const int n0 = tl.n * (bn / 2);
 #pragma unroll 1
         for (int c = 0; c < bn / 2; c += 32) {
@@ -562,7 +666,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&sm->tempty[acc]));
+      __syncwarp();
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(tempty0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+        else
+          mbar_arrive(smem_u32(&sm->tempty[acc]));
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -571,43 +681,84 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  // pairs: neither CTA leaves while the other may still signal its barriers,
+  // read its slots (the leader's MMAs) or write its accumulators
+  if (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-size_t gemm_smem_bytes(int E) {
-  return 1024 + 4 * static_cast<size_t>(kStageBytes) + kPieceArea + sizeof(Smem) +
-         static_cast<size_t>(E + 1) * sizeof(int);
+template <bool kPair>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + max_stages<kPair>() * static_cast<size_t>(stage_bytes<kPair>()) + kPieceArea +
+         sizeof(Smem) + static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
 }
+static_assert(gemm_smem_bytes<false>() <= 232448 && gemm_smem_bytes<true>() <= 232448,
+              "shared memory of one CTA");
 
-template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN>
+template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN, bool kPair>
 cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                       const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  // always the 4-stage size: one CTA per SM, so the 512-column TMEM
+  // always the deepest ring's size: one CTA per SM, so the 512-column TMEM
   // allocation never waits on a neighbour
-  const size_t smem = gemm_smem_bytes(kMaxExperts);
+  const size_t smem = gemm_smem_bytes<kPair>();
   static bool configured[kMaxDevices] = {};    // the attribute is per device
-  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather, kBN>;
+  static int max_pairs[kMaxDevices] = {};      // clusters of two that fit at once
+  auto kern = grouped_gemm_kernel<kEpi, kAmn, kBmn, kSched, kGather, kBN, kPair>;
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!configured[d]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    if (kPair) {
+      cfg.gridDim = dim3(2 * kMaxDevices);    // any even size: the query asks how many fit
+      e = cudaOccupancyMaxActiveClusters(&max_pairs[d], kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_pairs[d] < 1) return cudaErrorInvalidConfiguration;
+    }
     configured[d] = true;
   }
-  kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
-  return cudaGetLastError();
+  if (!kPair) {
+    kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
+    return cudaGetLastError();
+  }
+  // a persistent grid of pairs: at most one pair per two of the CTAs asked
+  // for, and no more pairs than fit on the GPU at once
+  const int pairs = grid / 2 < max_pairs[d] ? (grid / 2 > 0 ? grid / 2 : 1) : max_pairs[d];
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, o.map[0], o.map[1], o.map[2], p);
 }
 
 template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
+  if constexpr (kSched == Sched::Rows && !kGather && !kAmn) {
+    if (p.pair) {
+      if (kEpi == Epi::SwigluFwd || p.bn == 256)
+        return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 256, true>(a, b0, b1, o, p, grid, st);
+      return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 128, true>(a, b0, b1, o, p, grid, st);
+    }
+  }
   if (kEpi == Epi::SwigluFwd || p.bn == 256)
-    return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 256>(a, b0, b1, o, p, grid, st);
-  return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 128>(a, b0, b1, o, p, grid, st);
+    return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 256, false>(a, b0, b1, o, p, grid, st);
+  return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 128, false>(a, b0, b1, o, p, grid, st);
 }
 
 }  // namespace

@@ -153,6 +153,8 @@ struct GroupedGemmArgs {
   int keep_a;              // L2 evict_last hint on A loads (A small enough to stay resident)
   const int32_t* gather_token;  // fc1 with fused gather: token of each padded row
   const int32_t* counts;        // fc1 with fused gather: rows of each expert
+  int pair;                // Rows: CTA pairs (cta_group::2) share M = 256 tiles; a
+                           // K-major B map then has boxes of bn/2 rows
   int* err;
   unsigned long long wait_ns;
 };
