@@ -313,9 +313,10 @@ class Runner:
                 q, s = m.moe_quantize_mxfp8(wt)
                 self.wq += [q, s]
             save = bool(w.backward)
-            self.cfg = m.config(mxfp8_tile_n=mx_tile_n, save_for_backward=save)
+            self.cfg = m.config(mxfp8_tile_n=mx_tile_n, save_for_backward=save,
+                                cta_pairs=cta_pairs)
             self.cfg_ev = m.config(step_events=self.fev, mxfp8_tile_n=mx_tile_n,
-                                   save_for_backward=save)
+                                   save_for_backward=save, cta_pairs=cta_pairs)
             nbytes = m.moe_workspace_size_mxfp8(T, H, F, E, k, self.cfg)
             self.dtype = "mxfp8 (e4m3 + e8m0 per 32; bf16 out)"
             self.launches = 10
@@ -327,7 +328,7 @@ class Runner:
                     self.wq_b[2 * i], self.wq_b[2 * i + 1] = m.moe_quantize_mxfp8_t(wt)
                 self.dy = inp["dy"].to(device)
                 self.cfg_bev = m.config(save_for_backward=True, step_events=self.bev,
-                                        mxfp8_tile_n=mx_tile_n)
+                                        mxfp8_tile_n=mx_tile_n, cta_pairs=cta_pairs)
                 self.bws = torch.empty(m.moe_workspace_size_mxfp8_backward(T, H, F, E, k),
                                        dtype=torch.uint8, device=device)
                 self.grads = dict(
@@ -763,7 +764,7 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--gemm-sms", type=int, default=0,
                     help="persistent GEMM grid size (default: one CTA per SM)")
     ap.add_argument("--cta-pairs", type=int, default=0, choices=[0, 1, 2],
-                    help="BF16 GEMMs over routed rows: 2 = CTA pairs share M = 256 tiles, "
+                    help="GEMMs over routed rows: 2 = CTA pairs share M = 256 tiles, "
                          "1 = one CTA per tile, 0 = automatic")
     ap.add_argument("--graph", action="store_true",
                     help="capture each step once into a CUDA graph and replay it")

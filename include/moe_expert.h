@@ -85,12 +85,13 @@ typedef struct moe_config {
   int mxfp8_tile_n;        /* MMA N of the MXFP8 GEMMs: 128 (two accumulators, the
                               epilogue overlaps the next tile) or 256 (one accumulator,
                               half the A traffic per FLOP); 0 (default) = automatic  */
-  int cta_pairs;           /* BF16 grouped GEMMs over routed rows (fc1, fc2, dH, dXp):
-                              2 = pairs of CTAs on two SMs share M = 256 tiles
-                              (tcgen05 cta_group::2, each SM loading half of B);
-                              1 = one CTA per 128-row tile; 0 (default) = pairs when
-                              the experts average at least 512 routed rows. Results
-                              are bit-identical either way.                           */
+  int cta_pairs;           /* grouped GEMMs over routed rows (fc1, fc2, dH, dXp; BF16,
+                              and MXFP8 with 256-wide N tiles): 2 = pairs of CTAs on
+                              two SMs share M = 256 tiles (tcgen05 cta_group::2, each
+                              SM loading half of B); 1 = one CTA per 128-row tile;
+                              0 (default) = pairs for BF16 when the experts average
+                              at least 512 routed rows, one CTA per tile for MXFP8.
+                              Results are bit-identical either way.                   */
 } moe_config;
 
 #define MOE_STEP_EVENTS 5

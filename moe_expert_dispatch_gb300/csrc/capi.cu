@@ -309,6 +309,18 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_scale_rows(CUtensorMap* map, const void* base, uint64_t bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || bytes % 512 != 0 || bytes == 0) return false;
+  const cuuint64_t dims[2] = {256, bytes / 256};
+  const cuuint64_t strides[1] = {256};
+  const cuuint32_t box[2] = {256, 2};   // one 512-byte scale atom
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_out_tmap(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
                    uint64_t row_stride_bytes, bool f32) {
   EncodeTiledFn fn = encode_fn();
@@ -1071,7 +1083,22 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   }
   g1.err = err;
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
-  if (launch_mx_fc1(ta, tg, tu, o1, g1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // CTA pairs (N = 256 tiles) only when asked for: measured on the MXFP8
+  // workloads they are no faster (the block-scaled GEMMs are not bound by
+  // their operand traffic); their scale atoms arrive through tensor maps
+  const bool pairs = mx_bn == 256 && c.cta_pairs == 2;
+  g1.pair = pairs ? 1 : 0;
+  MxScaleMaps s1, s2;
+  if (pairs &&
+      (!make_tmap_scale_rows(&s1.map[0], xs, static_cast<uint64_t>(L.cap) * H / 32) ||
+       !make_tmap_scale_rows(&s1.map[1], wgu_s, static_cast<uint64_t>(E) * 2 * F * H / 32) ||
+       !make_tmap_scale_rows(&s2.map[0], hs, static_cast<uint64_t>(L.cap) * F / 32) ||
+       !make_tmap_scale_rows(&s2.map[1], wd_st, static_cast<uint64_t>(E) * H * F / 32)))
+    return MOE_ERR_CUDA;
+  s1.map[2] = s1.map[1];
+  s2.map[2] = s2.map[1];
+  if (launch_mx_fc1(ta, tg, tu, o1, g1, grid, st, pairs ? &s1 : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
   mark(2);
   MxGemmArgs g2 = g1;
   g2.K = F;
@@ -1087,7 +1114,8 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   if (!make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
     return MOE_ERR_CUDA;
   o2.map[1] = o2.map[2] = o2.map[0];
-  if (launch_mx_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_mx_fc2(th, td, o2, g2, grid, st, pairs ? &s2 : nullptr) != cudaSuccess)
+    return MOE_ERR_CUDA;
   mark(3);
   const cudaError_t ue =
       launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
@@ -1216,7 +1244,26 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   GemmOut od;
   od.map[0] = od.map[1] = od.map[2] = t_doq;     // unused
   g.keep_a = keep(static_cast<uint64_t>(cap) * H);
-  if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st))) return MOE_ERR_CUDA;
+  // dH and dXp on CTA pairs (N = 256 tiles) when asked for, their scale
+  // atoms by tensor map
+  const bool pairs = c.cta_pairs == 2;
+  MxScaleMaps sh, sx;
+  const bool pair_h = pairs && bnF == 256, pair_x = pairs && bnH == 256;
+  if ((pair_h && (!make_tmap_scale_rows(&sh.map[0], at<uint8_t>(ws, B.dos),
+                                        static_cast<uint64_t>(cap) * H / 32) ||
+                  !make_tmap_scale_rows(&sh.map[1], at<uint8_t>(ws, B.w2_st),
+                                        static_cast<uint64_t>(E) * F * H / 32))) ||
+      (pair_x && (!make_tmap_scale_rows(&sx.map[0], at<uint8_t>(ws, B.das),
+                                        static_cast<uint64_t>(cap) * 2 * F / 32) ||
+                  !make_tmap_scale_rows(&sx.map[1], at<uint8_t>(ws, B.w1g_st),
+                                        static_cast<uint64_t>(E) * H * F / 32) ||
+                  !make_tmap_scale_rows(&sx.map[2], at<uint8_t>(ws, B.w1u_st),
+                                        static_cast<uint64_t>(E) * H * F / 32))))
+    return MOE_ERR_CUDA;
+  sh.map[2] = sh.map[1];
+  g.pair = pair_h ? 1 : 0;
+  if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st, pair_h ? &sh : nullptr)))
+    return MOE_ERR_CUDA;
   mark(2);
 
   // dA quantised along 2F (dXp's K) and along the rows (dW1's K)
@@ -1244,7 +1291,9 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
     return MOE_ERR_CUDA;
   ox.map[1] = ox.map[2] = ox.map[0];
   g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
-  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st))) return MOE_ERR_CUDA;
+  g.pair = pair_x ? 1 : 0;
+  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st, pair_x ? &sx : nullptr)))
+    return MOE_ERR_CUDA;
   mark(4);
   if (!ok(launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
     return MOE_ERR_CUDA;

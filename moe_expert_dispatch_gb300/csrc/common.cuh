@@ -387,6 +387,38 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t adesc, uint6
       : "memory");
 }
 
+// The pair forms of tcgen05.cp and of the block-scaled MMA: issued by the
+// leader's thread; the copy moves each CTA's shared-memory atom into the
+// same tensor-memory columns of that CTA, and the MMA scales each CTA's rows
+// of A with its own scale columns and B with the scales of the whole N tile.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+__device__ __forceinline__ void umma_mxf8_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t sfa_tmem,
+                                               uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// 2D tiled TMA load without an L2 hint, completing on an mbarrier of either
+// CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair_plain(uint32_t dst, const CUtensorMap* map,
+                                                       uint32_t bar_cluster, int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::"
+      "bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(x), "r"(y)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ TMA stores
 
 // 2D tiled bulk tensor copy shared -> global (one bulk group per commit).

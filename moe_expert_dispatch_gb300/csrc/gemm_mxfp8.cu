@@ -77,6 +77,7 @@ __device__ __forceinline__ void regs_inc() {
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
+constexpr unsigned long long kPairDrainNs = 50000000ull;
 
 constexpr int kMaxStages = 6;
 
@@ -84,17 +85,20 @@ constexpr int kMaxStages = 6;
 // columns (the epilogue of a tile overlaps the next tile) and 34 KB slots;
 // N=256: one accumulator of 256 columns (no overlap, but half the A reads
 // per FLOP) and 50 KB slots. Scales take 4 + N/32 columns per slot after the
-// accumulators.
-template <int kN>
+// accumulators. A CTA of a pair (kPair, N = 256, M = 256 over the two CTAs)
+// holds half of the N tile's B rows but the scales of the whole N tile (its
+// SM's tensor core scales all N columns of its own 128 rows): 34 KB slots,
+// 6 of them.
+template <int kN, bool kPair = false>
 struct MxGeo {
-  static constexpr int kBBytes = kN * BK;
+  static constexpr int kBBytes = (kPair ? kN / 2 : kN) * BK;
   static constexpr int kSfbAtoms = kN / 128;
   static constexpr int kStageBytes = ((kABytes + kBBytes + (1 + kSfbAtoms) * kSfBytes) + 1023) /
                                      1024 * 1024;
   static constexpr int kAccBufs = kN == 128 ? 2 : 1;
   static constexpr uint32_t kSfCol = kAccBufs * kN;
   static constexpr uint32_t kSfColsPerStage = 4 + 4 * kSfbAtoms;
-  static constexpr int kStages = kN == 128 ? 6 : 4;   // what fits in shared memory
+  static constexpr int kStages = (kPair || kN == 128) ? 6 : 4;   // what fits in shared memory
 };
 
 // Output rows leave as per-warp pieces of 32 rows x 64 bytes (32 bf16 or
@@ -121,15 +125,22 @@ struct Smem {
 // k-block's K offset (WGrad: the expert's first padded row).
 struct MxTile {
   int e, m, n, kblocks, k0;
+  int row0;        // Rows: first A row of the tile (of the pair's tile)
+  int half_rows;   // pairs: 128-row blocks of the tile inside the expert (1 or 2)
 };
 
-template <MxEpi kEpi, Sched kSched, int kTileN>
+template <MxEpi kEpi, Sched kSched, int kTileN, bool kPair>
 __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1,
                    const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1,
-                   const __grid_constant__ CUtensorMap tmO2, MxGemmArgs p) {
+                   const __grid_constant__ CUtensorMap tmO2,
+                   const __grid_constant__ CUtensorMap tmSA,
+                   const __grid_constant__ CUtensorMap tmSB0,
+                   const __grid_constant__ CUtensorMap tmSB1, MxGemmArgs p) {
+  static_assert(!kPair || (kTileN == 256 && kSched == Sched::Rows),
+                "CTA pairs run the Rows schedule with N = 256");
   constexpr bool kFc1 = kEpi == MxEpi::Fc1 || kEpi == MxEpi::Fc1Save;
   constexpr bool kSave = kEpi == MxEpi::Fc1Save;   // fc1 also stores A_g, A_u and h in bf16
   constexpr bool kWGrad = kSched == Sched::WGrad;
@@ -137,7 +148,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  using G = MxGeo<kTileN>;
+  using G = MxGeo<kTileN, kPair>;
   constexpr int kBBytes = G::kBBytes;
   constexpr int kStageBytes = G::kStageBytes;
   const int S = p.stages < G::kStages ? p.stages : G::kStages;
@@ -151,6 +162,10 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
   const int kgroups_a = p.kgroups_a > 0 ? p.kgroups_a : (p.K >> 7);
   const int kgroups_b = p.kgroups_b > 0 ? p.kgroups_b : (p.K >> 7);
   const int m_tiles_w = kWGrad ? p.M / kTileM : 1;   // WGrad: M tiles of every expert
+  // CTA pairs: this CTA's rank and the tile walk over clusters
+  const uint32_t rank = kPair ? cluster_ctarank() : 0;
+  const int walk0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int walk_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -159,7 +174,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&sm->tfull[a]), 1);
-      mbar_init(smem_u32(&sm->tempty[a]), epi_warps<kEpi>() * 32);
+      // one arrival per epilogue warp (of both CTAs of a pair)
+      mbar_init(smem_u32(&sm->tempty[a]), (kPair ? 2 : 1) * epi_warps<kEpi>());
     }
     mbar_init(smem_u32(&sm->drain), 1);
     sm->abort = 0;
@@ -172,12 +188,19 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     tma_prefetch_desc(&tmB1);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(&sm->tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(&sm->tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
   }
   if (!kWGrad) {
-    for (int e = threadIdx.x; e < E; e += kThreads)
-      ts[e + 1] = (p.off_al[e + 1] - p.off_al[e]) / kTileM * n_tiles;
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+      const int mb = (p.off_al[e + 1] - p.off_al[e]) / kTileM;
+      ts[e + 1] = (kPair ? (mb + 1) >> 1 : mb) * n_tiles;
+    }
   }
   __syncthreads();
   if (!kWGrad && threadIdx.x == 0) {
@@ -186,6 +209,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync();   // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
   const int total = kWGrad ? E * m_tiles_w * n_tiles : ts[E];
@@ -193,6 +217,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 
   auto decode = [&](int t) {
     MxTile tl;
+    tl.half_rows = 1;
+    tl.row0 = 0;
     if (kWGrad) {
       const int per = m_tiles_w * n_tiles;
       tl.e = t / per;
@@ -214,7 +240,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       if (ts[mid] <= t) lo = mid; else hi = mid - 1;
     }
     tl.e = lo;
-    const int mt = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int mb = (p.off_al[tl.e + 1] - p.off_al[tl.e]) / kTileM;
+    const int mt = kPair ? (mb + 1) >> 1 : mb;
     const int local = t - ts[tl.e];
     if (mt > n_tiles) {       // tall expert: keep its row panel in L2
       tl.m = local / n_tiles;
@@ -223,6 +250,8 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       tl.n = local / mt;
       tl.m = local - tl.n * mt;
     }
+    tl.row0 = p.off_al[tl.e] + tl.m * (kPair ? 2 * kTileM : kTileM);
+    if (kPair) tl.half_rows = min(2, mb - 2 * tl.m);
     tl.k0 = 0;
     tl.kblocks = p.K / BK;
     return tl;
@@ -241,11 +270,12 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
         uint32_t fills = 0;
         bool ok = true;
         const uint64_t pol_a = p.keep_a ? l2_policy_evict_last() : l2_policy_evict_normal();
+        const uint64_t pol_b = l2_policy_evict_normal();
         const uint32_t ring0 = smem_u32(ring);
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int t = walk0; t < total && ok; t += walk_step) {
           const MxTile tl = decode(t);
           // A rows and the first 128-row block of B's scale atoms
-          const int a_row = kWGrad ? tl.m * kTileM : p.off_al[tl.e] + tl.m * kTileM;
+          const int a_row = kWGrad ? tl.m * kTileM : tl.row0 + static_cast<int>(rank) * kTileM;
           const int64_t b_row =
               kWGrad ? static_cast<int64_t>(tl.n) * kTileN
                      : static_cast<int64_t>(tl.e) * p.b_rows + static_cast<int64_t>(tl.n) * (kFc1 ? kTileN / 2 : kTileN);
@@ -253,11 +283,53 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
                                       : static_cast<int64_t>(tl.e) * p.sfb_rows +
                                             static_cast<int64_t>(tl.n) * kTileN;
           const int kg0 = tl.k0 >> 7;
+          // pairs: the second CTA's rows may lie past the expert (odd tail)
+          const bool load_a = !kPair || static_cast<int>(rank) < tl.half_rows;
           for (int kb = 0; kb < tl.kblocks; ++kb) {
             const uint32_t full = smem_u32(&sm->full[stage]);
             if (!mbar_wait(smem_u32(&sm->empty[stage]), phase ^ 1, p.wait_ns, abort_flag)) {
               ok = false;
               break;
+            }
+            if constexpr (kPair) {
+              // every copy of both CTAs completes on the leader's full barrier,
+              // armed by the leader with the pair tile's bytes: A and its
+              // scale atom per live half, both halves of B, and each CTA's
+              // copy of the N tile's B scales
+              const uint32_t full_l = mapa_shared(full, 0);
+              if (rank == 0)
+                mbar_arrive_expect_tx(full, tl.half_rows * (kABytes + kSfBytes) + kTileN * BK +
+                                                2 * G::kSfbAtoms * kSfBytes);
+              const uint32_t sa = ring0 + stage * kStageBytes;
+              const uint32_t sb = sa + kABytes;
+              const uint32_t ssf = sb + kBBytes;
+              const int kx = kb * BK;
+              const bool second = !kFc1 && p.k_split > 0 && kb >= p.k_split;
+              const int kbb = second ? kb - p.k_split : kb;
+              if (load_a) {
+                tma_load_2d_pair(sa, &tmA, full_l, kx, a_row, pol_a);
+                const int64_t atom = (static_cast<int64_t>(a_row) >> 7) * kgroups_a + kb;
+                tma_load_2d_pair_plain(ssf, &tmSA, full_l, 0, static_cast<int>(2 * atom));
+              }
+              // this CTA's 128 rows of B: fc1's gate rows (rank 0) or up rows
+              // (rank 1), else its half of the N tile
+              if (kFc1)
+                tma_load_2d_pair(sb, rank == 0 ? &tmB0 : &tmB1, full_l, kx, static_cast<int>(b_row),
+                                 pol_b);
+              else
+                tma_load_2d_pair(sb, second ? &tmB1 : &tmB0, full_l, kbb * BK,
+                                 static_cast<int>(b_row) + static_cast<int>(rank) * kTileM, pol_b);
+              const CUtensorMap* msb = second ? &tmSB1 : &tmSB0;
+#pragma unroll
+              for (int j = 0; j < G::kSfbAtoms; ++j)
+                tma_load_2d_pair_plain(ssf + (1 + j) * kSfBytes, msb, full_l, 0,
+                                       static_cast<int>(2 * (((vrow >> 7) + j) * kgroups_b + kbb)));
+              ++fills;
+              if (++stage == S) {
+                stage = 0;
+                phase ^= 1;
+              }
+              continue;
             }
             mbar_arrive_expect_tx(full, kABytes + kBBytes + (1 + G::kSfbAtoms) * kSfBytes);
             const uint32_t sa = ring0 + stage * kStageBytes;
@@ -297,19 +369,27 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           sm->abort = 1;
           report_error(p.err, kErrTimeout);
         }
-        // the last S fills must land before exit (fill i: slot i % S, parity (i / S) & 1)
-        for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i)
-          mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
+        // the last S fills must land before exit (fill i: slot i % S, parity
+        // (i / S) & 1). A pair's copies complete on the leader's barrier: each
+        // CTA waits until the MMAs that read its last fills released them,
+        // briefly after an abort, when they may never come (a copy lands
+        // within microseconds).
+        for (uint32_t i = fills > static_cast<uint32_t>(S) ? fills - S : 0; i < fills; ++i) {
+          if (kPair)
+            mbar_wait(smem_u32(&sm->empty[i % S]), (i / S) & 1, kPairDrainNs, &sm->zero);
+          else
+            mbar_wait(smem_u32(&sm->full[i % S]), (i / S) & 1, kDrainNs, &sm->zero);
+        }
       }
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      if (lane == 0) {
+      if (lane == 0 && rank == 0) {   // pairs: the leader's thread issues for both CTAs
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true, issued = false;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int t = walk0; t < total && ok; t += walk_step) {
           const int kblocks = decode(t).kblocks;
           if (!mbar_wait(smem_u32(&sm->tempty[acc]), acc_phase ^ 1, p.wait_ns, abort_flag)) {
             ok = false;
@@ -330,17 +410,30 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             // 128-row atoms at +4..7 (and +8..11 for N = 256)
             const uint32_t sfa_t = tmem_base + G::kSfCol + stage * G::kSfColsPerStage;
             const uint32_t sfb_t = sfa_t + 4;
-            tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
-#pragma unroll
-            for (int j = 0; j < G::kSfbAtoms; ++j)
-              tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
-                                     sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
             const uint64_t ad = sdesc_sw128(sa, 16, 1024), bd = sdesc_sw128(sb, 16, 1024);
+            if constexpr (kPair) {
+              tmem_cp_32x128b_warpx4_pair(sfa_t, sdesc_noswizzle(ssf, 16, 128));
 #pragma unroll
-            for (int ks = 0; ks < BK / 32; ++ks)      // +32 B of K per MMA
-              umma_mxf8(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t,
-                        sfb_t, (kb | ks) ? 1u : 0u);
-            umma_commit(smem_u32(&sm->empty[stage]));
+              for (int j = 0; j < G::kSfbAtoms; ++j)
+                tmem_cp_32x128b_warpx4_pair(sfb_t + 4 * j,
+                                            sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
+#pragma unroll
+              for (int ks = 0; ks < BK / 32; ++ks)
+                umma_mxf8_pair(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(2 * kTileM, kTileN, ks, ks),
+                               sfa_t, sfb_t, (kb | ks) ? 1u : 0u);
+              umma_commit_pair_mc(smem_u32(&sm->empty[stage]), 0x3);   // the slot, in both CTAs
+            } else {
+              tmem_cp_32x128b_warpx4(sfa_t, sdesc_noswizzle(ssf, 16, 128));
+#pragma unroll
+              for (int j = 0; j < G::kSfbAtoms; ++j)
+                tmem_cp_32x128b_warpx4(sfb_t + 4 * j,
+                                       sdesc_noswizzle(ssf + (1 + j) * kSfBytes, 16, 128));
+#pragma unroll
+              for (int ks = 0; ks < BK / 32; ++ks)      // +32 B of K per MMA
+                umma_mxf8(d, ad + 2 * ks, bd + 2 * ks, idesc_mxf8(kTileM, kTileN, ks, ks), sfa_t,
+                          sfb_t, (kb | ks) ? 1u : 0u);
+              umma_commit(smem_u32(&sm->empty[stage]));
+            }
             issued = true;
             if (++stage == S) {
               stage = 0;
@@ -350,7 +443,10 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           if (!ok) break;
           // a tile without k-blocks (WGrad, an expert without rows) issued no
           // MMA: the commit only hands the (unwritten) accumulator on
-          umma_commit(smem_u32(&sm->tfull[acc]));
+          if (kPair)
+            umma_commit_pair_mc(smem_u32(&sm->tfull[acc]), 0x3);   // both CTAs' epilogues
+          else
+            umma_commit(smem_u32(&sm->tfull[acc]));
           issued = true;
           if (++acc == G::kAccBufs) {
             acc = 0;
@@ -362,7 +458,10 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           report_error(p.err, kErrTimeout);
         }
         if (issued) {
-          umma_commit(smem_u32(&sm->drain));
+          if (kPair)
+            umma_commit_pair_mc(smem_u32(&sm->drain), 0x1);
+          else
+            umma_commit(smem_u32(&sm->drain));
           mbar_wait(smem_u32(&sm->drain), 0, kDrainNs, &sm->zero);
         }
       }
@@ -419,10 +518,26 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
     };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    // the accumulator is handed back to the MMA issuer (the leader, for a
+    // pair) by one arrival per warp, once the warp's reads of it are done
+    const uint32_t tempty0 = kPair ? mapa_shared(smem_u32(&sm->tempty[0]), 0) : 0;
+    auto release_acc = [&](int a) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (kPair)
+          mbar_arrive_cluster(tempty0 + a * static_cast<uint32_t>(sizeof(uint64_t)));
+        else
+          mbar_arrive(smem_u32(&sm->tempty[a]));
+      }
+    };
+    for (int t = walk0; t < total; t += walk_step) {
       const MxTile tl = decode(t);
-      const int64_t grow = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + row_in_tile;
-      const int wrow0 = kWGrad ? 0 : p.off_al[tl.e] + tl.m * kTileM + q * 32;   // warp's first row
+      // this CTA's 128 rows of the tile; pairs: rows past the expert are not live
+      const int my_row0 = tl.row0 + static_cast<int>(rank) * kTileM;
+      const bool live = !kPair || static_cast<int>(rank) < tl.half_rows;
+      const int64_t grow = kWGrad ? 0 : my_row0 + row_in_tile;
+      const int wrow0 = kWGrad ? 0 : my_row0 + q * 32;   // warp's first row
       // SwigluBwd: this row's A_g, A_u over the warp's half of the tile, 32
       // columns at a time as packed bf16 pairs, from the blocked layout (four
       // coalesced 512-byte loads per 32 x 32 block). The first block of each
@@ -444,7 +559,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           w16[4 * j + 3] = static_cast<uint32_t>(v.w);
         }
       };
-      if (kEpi == MxEpi::SwigluBwd) {
+      if (kEpi == MxEpi::SwigluBwd && live) {
 #pragma unroll
         for (int c = 32; c < kTileN / 2; c += 32)   // 16 lines per block: lanes 0-15 A_g
           prefetch_l2(act_block(lane < 16 ? p.act_g : p.act_u, c) - lane * 8 + (lane & 15) * 64);
@@ -459,7 +574,9 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
       }
       tc_fence_after();
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kTileN;
-      if (kFc1) {
+      if (!live) {
+        release_acc(acc);   // pairs: rows past the expert; nothing to keep
+      } else if (kFc1) {
         // h = bf16(silu(gate) * up), then MXFP8 per 32 along F. h is held
         // packed in bf16 (it is bf16-valued, so nothing is lost) and the
         // accumulator is released before the quantisation and the stores,
@@ -504,8 +621,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
               hw[c / 2 + i] = h_pair(g[2 * i], g[2 * i + 1], u[2 * i], u[2 * i + 1]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        release_acc(acc);
         if (kSave) {                               // after the release: off the MMAs' path
 #pragma unroll
           for (int c = 0; c < kHalf; c += 32) {
@@ -548,8 +664,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
           tmem_ld_wait();
           bf16_words(r, &w[c / 2]);
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        release_acc(acc);
 #pragma unroll
         for (int c = 0; c < kTileN; c += 32)
           put_piece(&w[c / 2], &tmO0, tl.n * kTileN + c, wrow0, false);
@@ -566,8 +681,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 #pragma unroll
         for (int c = 0; c < kHalf; c += 32) tmem_ld_32x32b_x32(taddr + half * kHalf + c, &v[c]);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        release_acc(acc);
 #pragma unroll
         for (int c = 0; c < kHalf; c += 32) {
           uint32_t ag_n[kActW], au_n[kActW];      // the next 32 columns, in flight
@@ -633,8 +747,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 #pragma unroll
           for (int i = 0; i < kCols; ++i) v[i] = 0u;
         }
-        tc_fence_before();
-        mbar_arrive(smem_u32(&sm->tempty[acc]));
+        release_acc(acc);
         if (!(empty && add)) {
 #pragma unroll
           for (int c = 0; c < kCols; c += 16)
@@ -651,76 +764,118 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
 
   tc_fence_before();
   __syncthreads();
+  // pairs: neither CTA leaves while the other may still signal its barriers,
+  // read its slots (the leader's MMAs) or write its accumulators
+  if (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (kPair)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-template <MxEpi kEpi, Sched kSched, int kN>
+template <MxEpi kEpi, Sched kSched, int kN, bool kPair>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                      const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  using G = MxGeo<kN>;
-  const size_t smem = 1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
-                      sizeof(Smem) + static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
-  static_assert(1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
-                        sizeof(Smem) + (kMaxExperts + 1) * sizeof(int) <= 232448,
-                "shared memory of one CTA");
+                      const GemmOut& o, const MxScaleMaps& sc, const MxGemmArgs& p, int grid,
+                      cudaStream_t st) {
+  using G = MxGeo<kN, kPair>;
+  constexpr size_t smem = 1024 + G::kStages * static_cast<size_t>(G::kStageBytes) + kPieceArea +
+                          sizeof(Smem) + static_cast<size_t>(kMaxExperts + 1) * sizeof(int);
+  static_assert(smem <= 232448, "shared memory of one CTA");
+  static_assert(G::kSfCol + G::kStages * G::kSfColsPerStage <= kTmemCols,
+                "accumulators and scale columns fit the tensor memory");
   static bool configured[kMaxDevices] = {};    // the attribute is per device
+  static int max_pairs[kMaxDevices] = {};      // clusters of two that fit at once
+  auto kern = mx_gemm_kernel<kEpi, kSched, kN, kPair>;
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  cfg.blockDim = dim3(num_threads<kEpi>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!configured[d]) {
-    cudaError_t e = cudaFuncSetAttribute(mx_gemm_kernel<kEpi, kSched, kN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     if (reg_split<kEpi>()) {
       // the split's setmaxnreg.inc would wait for good on a smaller pool
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mx_gemm_kernel<kEpi, kSched, kN>);
+      e = cudaFuncGetAttributes(&fa, kern);
       if (e != cudaSuccess) return e;
       if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
     }
+    if (kPair) {
+      cfg.gridDim = dim3(2 * kMaxDevices);    // any even size: the query asks how many fit
+      e = cudaOccupancyMaxActiveClusters(&max_pairs[d], kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (max_pairs[d] < 1) return cudaErrorInvalidConfiguration;
+    }
     configured[d] = true;
   }
-  mx_gemm_kernel<kEpi, kSched, kN><<<grid, num_threads<kEpi>(), smem, st>>>(
-      a, b0, b1, o.map[0], o.map[1], o.map[2], p);
-  return cudaGetLastError();
+  if (!kPair) {
+    kern<<<grid, num_threads<kEpi>(), smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2],
+                                                    sc.map[0], sc.map[1], sc.map[2], p);
+    return cudaGetLastError();
+  }
+  const int pairs = grid / 2 < max_pairs[d] ? (grid / 2 > 0 ? grid / 2 : 1) : max_pairs[d];
+  cfg.gridDim = dim3(2 * pairs);
+  return cudaLaunchKernelEx(&cfg, kern, a, b0, b1, o.map[0], o.map[1], o.map[2], sc.map[0],
+                            sc.map[1], sc.map[2], p);
 }
 
+// CTA pairs run N = 256 tiles of the Rows schedule, when asked for and given
+// the scale maps; everything else runs one CTA per tile.
 template <MxEpi kEpi, Sched kSched>
 cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                         const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return p.bn == 256 ? launch_mx<kEpi, kSched, 256>(a, b0, b1, o, p, grid, st)
-                     : launch_mx<kEpi, kSched, 128>(a, b0, b1, o, p, grid, st);
+                         const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
+                         const MxScaleMaps* sc) {
+  MxScaleMaps none;
+  none.map[0] = none.map[1] = none.map[2] = a;   // unused by one-CTA tiles
+  if constexpr (kSched == Sched::Rows) {
+    if (p.pair && p.bn == 256 && sc)
+      return launch_mx<kEpi, kSched, 256, true>(a, b0, b1, o, *sc, p, grid, st);
+  }
+  return p.bn == 256 ? launch_mx<kEpi, kSched, 256, false>(a, b0, b1, o, none, p, grid, st)
+                     : launch_mx<kEpi, kSched, 128, false>(a, b0, b1, o, none, p, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
-                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return p.save ? launch_mx_bn<MxEpi::Fc1Save, Sched::Rows>(a, wg, wu, o, p, grid, st)
-                : launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st);
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
+                          const MxScaleMaps* sc) {
+  return p.save ? launch_mx_bn<MxEpi::Fc1Save, Sched::Rows>(a, wg, wu, o, p, grid, st, sc)
+                : launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,
-                          const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, o, p, grid, st);
+                          const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps* sc) {
+  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
-                         const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, o, p, grid, st);
+                         const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps* sc) {
+  return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
-                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, w1g, w1u, o, p, grid, st);
+                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
+                          const MxScaleMaps* sc) {
+  return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, w1g, w1u, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
                             const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, o, p, grid, st);
+  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, o, p, grid, st, nullptr);
 }
 
 }  // namespace moe
