@@ -918,6 +918,8 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
 
   // dW1g | dW1u = Xp_e^T [dA_g | dA_u] and dW2 = h_e^T dO_e over each expert's rows
   GroupedGemmArgs gw1 = g;
+  gw1.pair = (pairs && H % 256 == 0) ? 1 : 0;      // the gradient's rows in M = 256 tiles
+  gw1.stages = bf16_stages(c, gw1.pair != 0);
   gw1.M = H;
   gw1.N = 2 * F;
   gw1.bn = bnF;
@@ -929,6 +931,8 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   if (launch_wgrad(t_xp_mn, t_da_mn, ow1, gw1, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(5);
   GroupedGemmArgs gw2 = g;
+  gw2.pair = (pairs && F % 256 == 0) ? 1 : 0;
+  gw2.stages = bf16_stages(c, gw2.pair != 0);
   gw2.M = F;
   gw2.N = H;
   gw2.bn = bnH;

@@ -111,7 +111,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
     if (kPair) tl.half_rows = min(2, mb - 2 * tl.m);
     tl.kblocks = p.K / BK;
   } else {
-    const int mt = p.M / kTileM;
+    const int mt = p.M / (kPair ? 2 * kTileM : kTileM);   // pairs: M % 256 == 0
     const int nt = p.N / p.bn;
     const int per = mt * nt;
     tl.e = t / per;
@@ -125,6 +125,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const int* ts, const GroupedG
     }
     tl.row0 = p.off_al[tl.e];
     tl.kblocks = (p.off_al[tl.e + 1] - tl.row0) / BK;
+    if (kPair) tl.half_rows = 2;   // M % 256 == 0: both halves lie inside the gradient
   }
   return tl;
 }
@@ -150,8 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  static_assert(!kPair || (kSched == Sched::Rows && !kGather && !kAmn),
-                "CTA pairs run the Rows schedule with a K-major A");
+  static_assert(!kPair || (!kGather && (kSched == Sched::Rows ? !kAmn : (kAmn && kBmn))),
+                "CTA pairs: the Rows schedule with a K-major A, or WGrad");
   constexpr int kStageBytes = stage_bytes<kPair>();
   const int S = p.stages;
   uint8_t* pieces = ring + max_stages<kPair>() * kStageBytes;  // after the largest ring
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sm->tmem_base;
   if (kSched == Sched::Rows) total = ts[E];
-  else total = E * (p.M / kTileM) * n_tiles;
+  else total = E * (p.M / (kPair ? 2 * kTileM : kTileM)) * n_tiles;
   volatile int* abort_flag = &sm->abort;
 
   if (kGather && warp == 0) {
@@ -291,9 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t ring0 = smem_u32(ring);
       for (int t = walk0; t < total && ok; t += walk_step) {
         const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
-        // per-tile coordinates
-        const int a_x0 = kAmn ? tl.m * kTileM : 0;
-        const int a_y0 = tl.row0 + static_cast<int>(rank) * kTileM;
+        // per-tile coordinates; a CTA of a pair takes the second 128 rows of
+        // the pair's M tile when its rank is 1 (Rows: rows of A; WGrad: the
+        // columns of the MN-major A)
+        const int m128 = kPair ? 2 * tl.m + static_cast<int>(rank) : tl.m;
+        const int a_x0 = kAmn ? m128 * kTileM : 0;
+        const int a_y0 = (kPair && !kAmn) ? tl.row0 + static_cast<int>(rank) * kTileM : tl.row0;
         const int b_row0 = (kSched == Sched::Rows) ? tl.e * static_cast<int>(p.b_rows) : tl.row0;
         const int b_n0 = (kEpi == Epi::SwigluFwd) ? tl.n * (bn / 2) : tl.n * bn;
         // pairs: the second CTA's rows may lie past the expert (odd tail)
@@ -313,7 +317,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full_l = mapa_shared(full, 0);
             if (rank == 0)
               mbar_arrive_expect_tx(full, tl.half_rows * kABytes + (bn / 64) * kBBox);
-            if (load_a) tma_load_2d_pair(sa, &tmA, full_l, k0, a_y0, pol_a);
+            if (load_a) {
+              if (kAmn) {     // MN-major A: two boxes of 64 of M x 64 of K
+                tma_load_2d_pair(sa, &tmA, full_l, a_x0, a_y0 + k0, pol_a);
+                tma_load_2d_pair(sa + kBBox, &tmA, full_l, a_x0 + 64, a_y0 + k0, pol_a);
+              } else {
+                tma_load_2d_pair(sa, &tmA, full_l, k0, a_y0, pol_a);
+              }
+            }
             if (kBmn) {       // this CTA's half of the N tile: bn / 128 boxes of 64 columns
               const int krow = b_row0 + k0;
               const CUtensorMap* mb = (kEpi == Epi::SwigluFwd && rank == 1) ? &tmB1 : &tmB0;
@@ -531,7 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty0 = kPair ? mapa_shared(smem_u32(&sm->tempty[0]), 0) : 0;
     for (int t = walk0; t < total; t += walk_step) {
       Tile tl = decode_tile<kSched, kPair>(t, ts, p);
-      tl.row0 += static_cast<int>(rank) * kTileM;   // this CTA's 128 rows
+      if (kPair && kSched == Sched::Rows)
+        tl.row0 += static_cast<int>(rank) * kTileM;   // this CTA's 128 rows
+      if (kPair && kSched == Sched::WGrad)
+        tl.m = 2 * tl.m + static_cast<int>(rank);     // this CTA's 128 rows of the gradient
       const bool live = !kPair || static_cast<int>(rank) < tl.half_rows;
       // SwigluBwd: the warp's rows of A_g, A_u for the tile's first 32
       // columns arrive while its MMAs run; the other blocks go to L2 now
@@ -749,7 +763,7 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
 template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather = false>
 cudaError_t launch_impl(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                         const GemmOut& o, const GroupedGemmArgs& p, int grid, cudaStream_t st) {
-  if constexpr (kSched == Sched::Rows && !kGather && !kAmn) {
+  if constexpr (!kGather && (kSched == Sched::Rows ? !kAmn : (kAmn && kBmn))) {
     if (p.pair) {
       if (kEpi == Epi::SwigluFwd || p.bn == 256)
         return launch_bn<kEpi, kAmn, kBmn, kSched, kGather, 256, true>(a, b0, b1, o, p, grid, st);

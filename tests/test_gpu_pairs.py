@@ -111,3 +111,17 @@ def test_mxfp8_backward_pairs_bit_identical(T, H, F, E, k, empty):
     g2 = _mxb_gpu(c, mxfp8_tile_n=256, cta_pairs=2)
     for key in ("y", "dx", "dprobs", "dw_gate_t", "dw_up_t", "dw_down_t"):
         assert torch.equal(g2[key], g1[key]), key
+
+
+def test_weight_gradients_on_pairs_accumulate():
+    # dW1 (M = H) and dW2 (M = F) on CTA pairs, stored then added: x + x is
+    # exact in float, and both match one CTA per tile
+    case = _case(300, 256, 512, 5, 2, seed=31, wstd=0.02)
+    dy = synth.normal_bf16(9, 2, (300, 256))
+    g1 = _gpu_fwd_bwd(*case, dy, cta_pairs=2)
+    g2 = _gpu_fwd_bwd(*case, dy, accumulate=True, cta_pairs=2,
+                      grads={k: g1[k].clone() for k in ("dw_gate", "dw_up", "dw_down")})
+    g0 = _gpu_fwd_bwd(*case, dy, cta_pairs=1)
+    for key in ("dw_gate", "dw_up", "dw_down"):
+        assert torch.equal(g1[key], g0[key]), key
+        assert torch.equal(g2[key], 2 * g1[key]), key
