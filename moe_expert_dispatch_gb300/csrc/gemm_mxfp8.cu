@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
             hv[2 * i] = f.x;
             hv[2 * i + 1] = f.y;
           }
-          const uint8_t sc = quantize_block32(hv, &codes[c / 4]);
+          const uint8_t sc = quantize_block32(hv, &hw[c / 2], &codes[c / 4]);
           packed |= static_cast<uint32_t>(sc) << (8 * (c >> 5));
         }
         int4* dst = reinterpret_cast<int4*>(p.hq + grow * p.N + col);

@@ -35,6 +35,18 @@ __device__ __forceinline__ int mx_block_exp(float amax) {
 // pattern when the block holds an infinity or a NaN (which fmaxf would drop).
 __device__ __forceinline__ uint32_t abs_bits(float v) { return __float_as_uint(v) & 0x7FFFFFFFu; }
 
+// abs_bits of the largest magnitude among the 2n bf16 values packed in
+// w[0..n): the sign bits cleared, each word's two halves compared as
+// unsigned 16-bit numbers (which order like the magnitudes, with every
+// infinity or NaN above every finite value), two values per instruction.
+template <int n>
+__device__ __forceinline__ uint32_t bf16x2_absmax_bits(const uint32_t* w) {
+  uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+  for (int j = 1; j < n; ++j) m = __vmaxu2(m, w[j] & 0x7FFF7FFFu);
+  return max(m & 0xFFFFu, m >> 16) << 16;   // bf16 bits to float bits
+}
+
 // A block that holds an infinity or a NaN has no finite shared scale: it is
 // given the E8M0 NaN code and E4M3 NaN elements, so that every element of it
 // decodes to NaN.
@@ -66,13 +78,13 @@ __device__ __forceinline__ uint32_t mx_encode4(float a, float b, float c, float 
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// One block of 32 values: returns the E8M0 code of its scale and packs the
-// 32 E4M3 codes four to a word (element 4i in the low byte of word i).
-__device__ __forceinline__ uint8_t quantize_block32(const float* v, uint32_t* words) {
-  uint32_t amax = 0u;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) amax = max(amax, abs_bits(v[i]));
-  const int code = mx_block_code(amax);
+// One block of 32 values, given as floats v and as the same values packed in
+// bf16 pairs (v2, for the block maximum): returns the E8M0 code of its scale
+// and packs the 32 E4M3 codes four to a word (element 4i in the low byte of
+// word i).
+__device__ __forceinline__ uint8_t quantize_block32(const float* v, const uint32_t* v2,
+                                                    uint32_t* words) {
+  const int code = mx_block_code(bf16x2_absmax_bits<16>(v2));
   const float inv = mx_inv_scale(code);
 #pragma unroll
   for (int i = 0; i < 8; ++i) {

@@ -745,9 +745,7 @@ __global__ void __launch_bounds__(256) quantize_mxfp8_kernel(const __nv_bfloat16
         v[2 * j] = f.x;
         v[2 * j + 1] = f.y;
       }
-      uint32_t amax = 0u;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) amax = max(amax, abs_bits(v[j]));
+      uint32_t amax = bf16x2_absmax_bits<4>(reinterpret_cast<const uint32_t*>(&raw[u]));
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
       const int code = mx_block_code(amax);
@@ -828,11 +826,6 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // consecutive rows, or rows 64 apart, never share a bank group
 __device__ __forceinline__ int qt_swizzle(int r) { return (r & 7) ^ ((r >> 4) & 4); }
 
-// abs_bits of the largest magnitude of 8 values (non-finite ones included)
-__device__ __forceinline__ uint32_t absmax8(const float* v) {
-  return max(max(max(abs_bits(v[0]), abs_bits(v[1])), max(abs_bits(v[2]), abs_bits(v[3]))),
-             max(max(abs_bits(v[4]), abs_bits(v[5])), max(abs_bits(v[6]), abs_bits(v[7]))));
-}
 
 // Where the bf16 input comes from: rows of a row-major matrix, gathered
 // rows, or the 32 x 32 blocked layout of act_block_offset (with N = cols).
@@ -899,11 +892,7 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
         w[4 * j + 2] = q.z;
         w[4 * j + 3] = q.w;
       }
-      uint32_t amax = 0u;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        amax = max(amax, max(abs_bits(bf16_lo(w[j])), abs_bits(bf16_hi(w[j]))));
-      const int code = mx_block_code(amax);
+      const int code = mx_block_code(bf16x2_absmax_bits<16>(w));
       const float inv = mx_inv_scale(code);
       uint32_t o[8];
 #pragma unroll
@@ -937,15 +926,19 @@ __global__ void __launch_bounds__(kQtThreads) quantize_tile_kernel(
       const int rb = 2 * p + h;
       if (rb < n_rb) {
         float v[32];
+        uint32_t v2[16];                     // the same values as bf16 pairs
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 32; i += 2) {
           const int rr = rb * 32 + i;
-          v[i] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-              &tile[rr][(((c >> 3) ^ qt_swizzle(rr)) << 4) + (c & 7) * 2]));
+          const uint32_t lo = *reinterpret_cast<const uint16_t*>(
+              &tile[rr][(((c >> 3) ^ qt_swizzle(rr)) << 4) + (c & 7) * 2]);
+          const uint32_t hi = *reinterpret_cast<const uint16_t*>(
+              &tile[rr + 1][(((c >> 3) ^ qt_swizzle(rr + 1)) << 4) + (c & 7) * 2]);
+          v2[i / 2] = lo | (hi << 16);
+          v[i] = __uint_as_float(lo << 16);
+          v[i + 1] = __uint_as_float(hi << 16);
         }
-        const uint32_t amax = max(max(absmax8(v), absmax8(v + 8)),
-                                  max(absmax8(v + 16), absmax8(v + 24)));
-        const int code = mx_block_code(amax);
+        const int code = mx_block_code(bf16x2_absmax_bits<16>(v2));
         const float inv = mx_inv_scale(code);
         uint32_t w[8];
 #pragma unroll
@@ -1082,9 +1075,7 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
           v[2 * j] = f.x;
           v[2 * j + 1] = f.y;
         }
-        uint32_t amax = 0u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = max(amax, abs_bits(v[j]));
+        uint32_t amax = bf16x2_absmax_bits<4>(reinterpret_cast<const uint32_t*>(&raw[u]));
         amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
         amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const int code = mx_block_code(amax);
