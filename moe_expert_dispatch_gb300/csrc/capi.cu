@@ -1053,12 +1053,18 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
     return MOE_ERR_CUDA;
   mark(1);
 
+  // CTA pairs only when asked for: measured on the MXFP8 workloads with
+  // 256-wide N tiles they are no faster (the block-scaled GEMMs are not
+  // bound by their operand traffic). A pair's CTA reads N / 2 rows of B,
+  // and the pairs' scale atoms arrive through tensor maps.
+  const bool pairs = c.cta_pairs == 2;
+  const uint32_t b_box = (pairs && mx_bn == 128) ? 64 : 128;
   CUtensorMap ta, tg, tu, th, td;
   if (!make_tmap_u8_2d(&ta, xq, H, L.cap, H, 128, kTileM) ||
       !make_tmap_u8_2d(&tg, wg_q, H, static_cast<uint64_t>(E) * F, H, 128, mx_bn / 2) ||
       !make_tmap_u8_2d(&tu, wu_q, H, static_cast<uint64_t>(E) * F, H, 128, mx_bn / 2) ||
       !make_tmap_u8_2d(&th, hq, F, L.cap, F, 128, kTileM) ||
-      !make_tmap_u8_2d(&td, wd_q, F, static_cast<uint64_t>(E) * H, F, 128, 128))
+      !make_tmap_u8_2d(&td, wd_q, F, static_cast<uint64_t>(E) * H, F, 128, b_box))
     return MOE_ERR_CUDA;
   const int grid = grid_size(c);
   MxGemmArgs g1{};
@@ -1087,10 +1093,6 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   }
   g1.err = err;
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
-  // CTA pairs (N = 256 tiles) only when asked for: measured on the MXFP8
-  // workloads they are no faster (the block-scaled GEMMs are not bound by
-  // their operand traffic); their scale atoms arrive through tensor maps
-  const bool pairs = mx_bn == 256 && c.cta_pairs == 2;
   g1.pair = pairs ? 1 : 0;
   MxScaleMaps s1, s2;
   if (pairs &&
@@ -1212,13 +1214,18 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   mark(1);
 
   const int bnF = bn_for(F), bnH = bn_for(H);
+  // dH and dXp on CTA pairs when asked for (a pair's CTA reads N / 2 rows of
+  // B; the scale atoms arrive by tensor map)
+  const bool pairs = c.cta_pairs == 2;
+  const uint32_t box_f = (pairs && bnF == 128) ? 64 : 128;
+  const uint32_t box_h = (pairs && bnH == 128) ? 64 : 128;
   CUtensorMap t_doq, t_w2, t_daq, t_w1g, t_w1u, t_daT, t_xpT, t_doT, t_hT;
   if (!make_tmap_u8_2d(&t_doq, at<uint8_t>(ws, B.doq), H, cap, H, 128, kTileM) ||
-      !make_tmap_u8_2d(&t_w2, w2_q, H, static_cast<uint64_t>(E) * F, H, 128, 128) ||
+      !make_tmap_u8_2d(&t_w2, w2_q, H, static_cast<uint64_t>(E) * F, H, 128, box_f) ||
       !make_tmap_u8_2d(&t_daq, at<uint8_t>(ws, B.daq), 2 * static_cast<uint64_t>(F), cap,
                        2 * static_cast<uint64_t>(F), 128, kTileM) ||
-      !make_tmap_u8_2d(&t_w1g, w1g_q, F, static_cast<uint64_t>(E) * H, F, 128, 128) ||
-      !make_tmap_u8_2d(&t_w1u, w1u_q, F, static_cast<uint64_t>(E) * H, F, 128, 128) ||
+      !make_tmap_u8_2d(&t_w1g, w1g_q, F, static_cast<uint64_t>(E) * H, F, 128, box_h) ||
+      !make_tmap_u8_2d(&t_w1u, w1u_q, F, static_cast<uint64_t>(E) * H, F, 128, box_h) ||
       !make_tmap_u8_2d(&t_daT, at<uint8_t>(ws, B.daT), cap, 2 * static_cast<uint64_t>(F), cap,
                        128, kTileM) ||
       !make_tmap_u8_2d(&t_xpT, at<uint8_t>(ws, B.xpT), cap, H, cap, 128, 128) ||
@@ -1248,11 +1255,8 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   GemmOut od;
   od.map[0] = od.map[1] = od.map[2] = t_doq;     // unused
   g.keep_a = keep(static_cast<uint64_t>(cap) * H);
-  // dH and dXp on CTA pairs (N = 256 tiles) when asked for, their scale
-  // atoms by tensor map
-  const bool pairs = c.cta_pairs == 2;
   MxScaleMaps sh, sx;
-  const bool pair_h = pairs && bnF == 256, pair_x = pairs && bnH == 256;
+  const bool pair_h = pairs, pair_x = pairs;
   if ((pair_h && (!make_tmap_scale_rows(&sh.map[0], at<uint8_t>(ws, B.dos),
                                         static_cast<uint64_t>(cap) * H / 32) ||
                   !make_tmap_scale_rows(&sh.map[1], at<uint8_t>(ws, B.w2_st),

@@ -79,16 +79,18 @@ constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
 constexpr unsigned long long kPairDrainNs = 50000000ull;
 
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
 
 // Tile geometry for an MMA N of 128 or 256. N=128: two accumulators of 128
 // columns (the epilogue of a tile overlaps the next tile) and 34 KB slots;
 // N=256: one accumulator of 256 columns (no overlap, but half the A reads
 // per FLOP) and 50 KB slots. Scales take 4 + N/32 columns per slot after the
-// accumulators. A CTA of a pair (kPair, N = 256, M = 256 over the two CTAs)
-// holds half of the N tile's B rows but the scales of the whole N tile (its
-// SM's tensor core scales all N columns of its own 128 rows): 34 KB slots,
-// 6 of them.
+// accumulators. A CTA of a pair (kPair, M = 256 over the two CTAs) holds
+// half of the N tile's B rows but the scales of the whole N tile (its SM's
+// tensor core scales all N columns of its own 128 rows): 34 KB slots, 6 of
+// them, for N = 256; 25 KB slots, 8 of them, and two accumulators for
+// N = 128, which streams as few operand bytes per SM and FLOP as one CTA
+// with N = 256 while the epilogue of a tile overlaps the next one.
 template <int kN, bool kPair = false>
 struct MxGeo {
   static constexpr int kBBytes = (kPair ? kN / 2 : kN) * BK;
@@ -98,7 +100,8 @@ struct MxGeo {
   static constexpr int kAccBufs = kN == 128 ? 2 : 1;
   static constexpr uint32_t kSfCol = kAccBufs * kN;
   static constexpr uint32_t kSfColsPerStage = 4 + 4 * kSfbAtoms;
-  static constexpr int kStages = (kPair || kN == 128) ? 6 : 4;   // what fits in shared memory
+  // what fits in shared memory
+  static constexpr int kStages = kPair ? (kN == 128 ? 8 : 6) : (kN == 128 ? 6 : 4);
 };
 
 // Output rows leave as per-warp pieces of 32 rows x 64 bytes (32 bf16 or
@@ -139,8 +142,7 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
                    const __grid_constant__ CUtensorMap tmSA,
                    const __grid_constant__ CUtensorMap tmSB0,
                    const __grid_constant__ CUtensorMap tmSB1, MxGemmArgs p) {
-  static_assert(!kPair || (kTileN == 256 && kSched == Sched::Rows),
-                "CTA pairs run the Rows schedule with N = 256");
+  static_assert(!kPair || kSched == Sched::Rows, "CTA pairs run the Rows schedule");
   constexpr bool kFc1 = kEpi == MxEpi::Fc1 || kEpi == MxEpi::Fc1Save;
   constexpr bool kSave = kEpi == MxEpi::Fc1Save;   // fc1 also stores A_g, A_u and h in bf16
   constexpr bool kWGrad = kSched == Sched::WGrad;
@@ -311,14 +313,15 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
                 const int64_t atom = (static_cast<int64_t>(a_row) >> 7) * kgroups_a + kb;
                 tma_load_2d_pair_plain(ssf, &tmSA, full_l, 0, static_cast<int>(2 * atom));
               }
-              // this CTA's 128 rows of B: fc1's gate rows (rank 0) or up rows
-              // (rank 1), else its half of the N tile
+              // this CTA's N / 2 rows of B (one box): fc1's gate rows (rank 0)
+              // or up rows (rank 1), else its half of the N tile
               if (kFc1)
                 tma_load_2d_pair(sb, rank == 0 ? &tmB0 : &tmB1, full_l, kx, static_cast<int>(b_row),
                                  pol_b);
               else
                 tma_load_2d_pair(sb, second ? &tmB1 : &tmB0, full_l, kbb * BK,
-                                 static_cast<int>(b_row) + static_cast<int>(rank) * kTileM, pol_b);
+                                 static_cast<int>(b_row) + static_cast<int>(rank) * (kTileN / 2),
+                                 pol_b);
               const CUtensorMap* msb = second ? &tmSB1 : &tmSB0;
 #pragma unroll
               for (int j = 0; j < G::kSfbAtoms; ++j)
@@ -832,8 +835,9 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                             sc.map[1], sc.map[2], p);
 }
 
-// CTA pairs run N = 256 tiles of the Rows schedule, when asked for and given
-// the scale maps; everything else runs one CTA per tile.
+// CTA pairs run tiles of the Rows schedule when asked for and given the scale
+// maps (a pair's B maps then have boxes of N / 2 rows); everything else runs
+// one CTA per tile.
 template <MxEpi kEpi, Sched kSched>
 cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
@@ -841,8 +845,9 @@ cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUte
   MxScaleMaps none;
   none.map[0] = none.map[1] = none.map[2] = a;   // unused by one-CTA tiles
   if constexpr (kSched == Sched::Rows) {
-    if (p.pair && p.bn == 256 && sc)
-      return launch_mx<kEpi, kSched, 256, true>(a, b0, b1, o, *sc, p, grid, st);
+    if (p.pair && sc)
+      return p.bn == 256 ? launch_mx<kEpi, kSched, 256, true>(a, b0, b1, o, *sc, p, grid, st)
+                         : launch_mx<kEpi, kSched, 128, true>(a, b0, b1, o, *sc, p, grid, st);
   }
   return p.bn == 256 ? launch_mx<kEpi, kSched, 256, false>(a, b0, b1, o, none, p, grid, st)
                      : launch_mx<kEpi, kSched, 128, false>(a, b0, b1, o, none, p, grid, st);

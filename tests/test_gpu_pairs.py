@@ -82,33 +82,37 @@ MX_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("T,H,F,E,k,empty", MX_SHAPES)
-def test_mxfp8_forward_pairs_bit_identical(T, H, F, E, k, empty):
+def test_mxfp8_forward_pairs_bit_identical(T, H, F, E, k, empty, tile_n):
     from test_gpu_mxfp8 import TOL, _gpu as _mx_gpu, _mx_case, _oracle as _mx_oracle
     from gpu_util import assert_rel_to_max
     case = _mx_case(T, H, F, E, k, seed=T + 17, empty=empty)
-    y1, _ = _mx_gpu(*case, mxfp8_tile_n=256, cta_pairs=1)
-    y2, _ = _mx_gpu(*case, mxfp8_tile_n=256, cta_pairs=2)
+    y1, _ = _mx_gpu(*case, mxfp8_tile_n=tile_n, cta_pairs=1)
+    y2, _ = _mx_gpu(*case, mxfp8_tile_n=tile_n, cta_pairs=2)
     assert torch.equal(y2, y1)
     ref, _ = _mx_oracle(*case)
     assert_rel_to_max(to_np(y2), ref, TOL, "y")
 
 
-def test_mxfp8_forward_pairs_ring_depth_and_grid():
+@pytest.mark.parametrize("tile_n", [128, 256])
+def test_mxfp8_forward_pairs_ring_depth_and_grid(tile_n):
     from test_gpu_mxfp8 import _gpu as _mx_gpu, _mx_case
     case = _mx_case(700, 256, 512, 6, 2, seed=23)
-    y0, _ = _mx_gpu(*case, mxfp8_tile_n=256, cta_pairs=1)
-    for kw in (dict(ring_stages=1), dict(ring_stages=4), dict(num_sms=2), dict(num_sms=9)):
-        y1, _ = _mx_gpu(*case, mxfp8_tile_n=256, cta_pairs=2, **kw)
+    y0, _ = _mx_gpu(*case, mxfp8_tile_n=tile_n, cta_pairs=1)
+    for kw in (dict(ring_stages=1), dict(ring_stages=4), dict(ring_stages=8), dict(num_sms=2),
+               dict(num_sms=9)):
+        y1, _ = _mx_gpu(*case, mxfp8_tile_n=tile_n, cta_pairs=2, **kw)
         assert torch.equal(y1, y0), kw
 
 
+@pytest.mark.parametrize("tile_n", [128, 256])
 @pytest.mark.parametrize("T,H,F,E,k,empty", MX_SHAPES[:3])
-def test_mxfp8_backward_pairs_bit_identical(T, H, F, E, k, empty):
+def test_mxfp8_backward_pairs_bit_identical(T, H, F, E, k, empty, tile_n):
     from test_gpu_mxfp8_backward import _case as _mxb_case, _gpu as _mxb_gpu
     c = _mxb_case(T, H, F, E, k, seed=T + 19, empty=empty)
-    g1 = _mxb_gpu(c, mxfp8_tile_n=256, cta_pairs=1)
-    g2 = _mxb_gpu(c, mxfp8_tile_n=256, cta_pairs=2)
+    g1 = _mxb_gpu(c, mxfp8_tile_n=tile_n, cta_pairs=1)
+    g2 = _mxb_gpu(c, mxfp8_tile_n=tile_n, cta_pairs=2)
     for key in ("y", "dx", "dprobs", "dw_gate_t", "dw_up_t", "dw_down_t"):
         assert torch.equal(g2[key], g1[key]), key
 
