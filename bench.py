@@ -313,13 +313,22 @@ class Runner:
                 q, s = m.moe_quantize_mxfp8(wt)
                 self.wq += [q, s]
             save = bool(w.backward)
+            # forward only: the weights are held in MXFP8 across steps, their
+            # scales laid out once for the block-scaled MMAs
+            pretiled = not w.backward
+            if pretiled:
+                self.wq[1], self.wq[5] = m.moe_tile_weight_scales_mxfp8(
+                    self.wq[1], self.wq[3], self.wq[5], cfg=m.config(mxfp8_tile_n=mx_tile_n))
+                self.wq[3] = None
+            self.pretiled = pretiled
+            self.launches = 8 if pretiled else 10
             self.cfg = m.config(mxfp8_tile_n=mx_tile_n, save_for_backward=save,
-                                cta_pairs=cta_pairs)
+                                cta_pairs=cta_pairs, mx_scales_pretiled=pretiled)
             self.cfg_ev = m.config(step_events=self.fev, mxfp8_tile_n=mx_tile_n,
-                                   save_for_backward=save, cta_pairs=cta_pairs)
+                                   save_for_backward=save, cta_pairs=cta_pairs,
+                                   mx_scales_pretiled=pretiled)
             nbytes = m.moe_workspace_size_mxfp8(T, H, F, E, k, self.cfg)
             self.dtype = "mxfp8 (e4m3 + e8m0 per 32; bf16 out)"
-            self.launches = 10
             if w.backward:
                 # training re-quantises its weights every step, in the forward's
                 # orientation and in the backward's (along the other axis)
@@ -717,6 +726,11 @@ def run_ours(args, w):
                                 if run.chunks else "none"),
                    "gemm_ctas": args.gemm_sms or "one per SM",
                    "cta_pairs": {0: "automatic", 1: "off", 2: "on"}[args.cta_pairs],
+                   **({"mx_weight_scales": ("laid out once for the block-scaled MMAs "
+                                            "(weights held in MXFP8 across steps)"
+                                            if run.pretiled else
+                                            "quantised and laid out in every step")}
+                      if w.mxfp8 else {}),
                    "routing": ("fused top-k gate from float32 router logits [T, E]" if run.gate
                                else "expert ids and weights given"),
                    "parallelism": "replicas" if ws > 1 else "single"},

@@ -92,6 +92,13 @@ typedef struct moe_config {
                               0 (default) = pairs for BF16 when the experts average
                               at least 512 routed rows, one CTA per tile for MXFP8.
                               Results are bit-identical either way.                   */
+  int mx_scales_pretiled;  /* moe_expert_forward_mxfp8: 1 = wg_s and wd_s already hold
+                              the weights' scales in the block-scaled MMA's layout,
+                              written by moe_tile_weight_scales_mxfp8 with the same
+                              mxfp8_tile_n and the same H, F, E (wu_s is not read and
+                              may be NULL), so the forward does not re-tile them on
+                              every call; 0 (default) = row-major scales as
+                              moe_quantize_mxfp8 writes them                          */
 } moe_config;
 
 #define MOE_STEP_EVENTS 5
@@ -389,9 +396,36 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
  * With cfg->save_for_backward the workspace (moe_workspace_size_mxfp8 with
  * the same cfg) also keeps A_g, A_u and h in bf16 for
  * moe_expert_backward_mxfp8, and the padding rows of the quantised x are
- * zeroed. Requires H % 128 == 0, F % 128 == 0.
+ * zeroed. Requires H % 128 == 0, F % 128 == 0. With cfg->mx_scales_pretiled
+ * the scales come from moe_tile_weight_scales_mxfp8 (wg_s = its wgu_tiled,
+ * wd_s = its wd_tiled, wu_s unused).
  * ------------------------------------------------------------------------ */
 size_t moe_workspace_size_mxfp8(int64_t T, int H, int F, int E, int k, const moe_config* cfg);
+
+/* ------------------------------------------------------------------------
+ * moe_tile_weight_scales_mxfp8 - the weights' scales of moe_expert_forward_mxfp8
+ * laid out once for its block-scaled MMAs, for a forward run with
+ * cfg->mx_scales_pretiled = 1 (weights held in MXFP8 across calls: the
+ * scales are re-tiled only when the weights change). "MC2 通算融合架构总览"
+ * section 5 keeps the scales in buffers of their own, put once outside the
+ * pipeline; this is that put for the weights.
+ *  wg_s, wu_s  uint8 [E, F, H/32]  in (moe_quantize_mxfp8 of W1g^T, W1u^T)
+ *  wd_s        uint8 [E, H, F/32]  in (moe_quantize_mxfp8 of W2^T)
+ *  wgu_tiled   uint8 [E * 2F * H/32] out: pass as the forward's wg_s
+ *  wd_tiled    uint8 [E * H * F/32]  out: pass as the forward's wd_s
+ * The layout: atoms of 128 rows x 4 blocks of 32 (512 bytes), row blocks of
+ * the gate and up scales interleaved per N tile of fc1 (half of the MMA N
+ * each, which cfg->mxfp8_tile_n and H, F decide as the forward decides
+ * them). The forward must get the same cfg->mxfp8_tile_n. Pointers are
+ * device memory owned by the caller: the inputs 4-byte aligned, the outputs
+ * 16-byte aligned (the forward reads them with bulk copies and requires the
+ * same). Same argument checks as the forward (H % 128 == 0, F % 128 == 0,
+ * 1 <= E <= 1024); MOE_ERR_CUDA if a launch fails.
+ * ------------------------------------------------------------------------ */
+moe_status moe_tile_weight_scales_mxfp8(const uint8_t* wg_s, const uint8_t* wu_s,
+                                        const uint8_t* wd_s, int H, int F, int E,
+                                        const moe_config* cfg, uint8_t* wgu_tiled,
+                                        uint8_t* wd_tiled, void* stream);
 moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
                                     const uint8_t* wu_q, const uint8_t* wu_s, const uint8_t* wd_q,
                                     const uint8_t* wd_s, const int32_t* expert_ids,

@@ -38,7 +38,8 @@ class moe_config(ctypes.Structure):
                 ("step_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("num_step_events", ctypes.c_int),
                 ("mxfp8_tile_n", ctypes.c_int),
-                ("cta_pairs", ctypes.c_int)]
+                ("cta_pairs", ctypes.c_int),
+                ("mx_scales_pretiled", ctypes.c_int)]
 
 STEP_EVENTS = 5       # forward: start, routing, fc1+SwiGLU, fc2, unpermute
 BWD_STEP_EVENTS = 7   # backward: start, dO+dprobs, dH, dXp, dX, dW1, dW2
@@ -88,6 +89,8 @@ _sig("moe_expert_backward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, 
      ctypes.POINTER(moe_config), _vp)
 _sig("moe_expert_forward_mxfp8", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i32,
      _i32, _i32, _i32, _vp, _vp, _sz, ctypes.POINTER(moe_config), _vp)
+_sig("moe_tile_weight_scales_mxfp8", _i32, _vp, _vp, _vp, _i32, _i32, _i32,
+     ctypes.POINTER(moe_config), _vp, _vp, _vp)
 
 
 class MoeError(RuntimeError):
@@ -148,7 +151,8 @@ def _device(*named):
 
 
 def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
-           wait_limit_ns=0, step_events=None, mxfp8_tile_n=0, cta_pairs=0) -> moe_config:
+           wait_limit_ns=0, step_events=None, mxfp8_tile_n=0, cta_pairs=0,
+           mx_scales_pretiled=False) -> moe_config:
     """A moe_config; step_events: optional list of MOE_STEP_EVENTS torch.cuda.Event
     (already recorded once, so that their CUDA events exist)."""
     c = moe_config()
@@ -159,6 +163,7 @@ def config(ring_stages=0, save_for_backward=False, num_sms=0, fuse_gather=False,
     c.fuse_gather = int(bool(fuse_gather))
     c.mxfp8_tile_n = mxfp8_tile_n
     c.cta_pairs = cta_pairs
+    c.mx_scales_pretiled = int(bool(mx_scales_pretiled))
     if wait_limit_ns:
         c.wait_limit_ns = wait_limit_ns
     if step_events is not None:
@@ -570,10 +575,43 @@ def moe_workspace_size_mxfp8_backward(T, H, F, E, k) -> int:
     return _lib.moe_workspace_size_mxfp8_backward(T, H, F, E, k)
 
 
+def moe_tile_weight_scales_mxfp8(wg_s, wu_s, wd_s, cfg: moe_config | None = None, stream=None,
+                                 out=None):
+    """The weights' scales laid out once for the MXFP8 forward's block-scaled
+    MMAs: (wgu_tiled, wd_tiled), to pass as wg_s and wd_s to
+    moe_expert_forward_mxfp8 with config(mx_scales_pretiled=True) and the same
+    mxfp8_tile_n. wg_s, wu_s [E, F, H/32], wd_s [E, H, F/32] as
+    moe_quantize_mxfp8 writes them."""
+    for t, n in ((wg_s, "wg_s"), (wu_s, "wu_s"), (wd_s, "wd_s")):
+        _cuda(t, n, torch.uint8)
+    E, F, H32 = wg_s.shape
+    H = 32 * H32
+    if tuple(wu_s.shape) != (E, F, H32) or tuple(wd_s.shape) != (E, H, F // 32):
+        raise ValueError("wg_s, wu_s [E, F, H/32] and wd_s [E, H, F/32] expected")
+    if out is None:
+        wgu = torch.empty(E * 2 * F * H32, dtype=torch.uint8, device=wg_s.device)
+        wdt = torch.empty(E * H * (F // 32), dtype=torch.uint8, device=wg_s.device)
+    else:
+        wgu, wdt = out
+        _cuda(wgu, "wgu_tiled", torch.uint8, E * 2 * F * H32)
+        _cuda(wdt, "wd_tiled", torch.uint8, E * H * (F // 32))
+    dev = _device(("wg_s", wg_s), ("wu_s", wu_s), ("wd_s", wd_s), ("wgu_tiled", wgu),
+                  ("wd_tiled", wdt))
+    c = cfg if cfg is not None else config()
+    with torch.cuda.device(dev):
+        _check(_lib.moe_tile_weight_scales_mxfp8(_p(wg_s), _p(wu_s), _p(wd_s), H, F, E,
+                                                 ctypes.byref(c), _p(wgu), _p(wdt),
+                                                 _stream(stream, dev)),
+               "moe_tile_weight_scales_mxfp8")
+    return wgu, wdt
+
+
 def moe_expert_forward_mxfp8(x, wg_q, wg_s, wu_q, wu_s, wd_q, wd_s, expert_ids, probs, y=None,
                              workspace=None, cfg: moe_config | None = None, stream=None):
     """The block with MXFP8 operands (x quantised on the fly; weights pre-quantised,
-    K-contiguous: wg/wu [E, F, H], wd [E, H, F], scales [..., K/32])."""
+    K-contiguous: wg/wu [E, F, H], wd [E, H, F], scales [..., K/32]). With
+    cfg.mx_scales_pretiled, wg_s and wd_s are moe_tile_weight_scales_mxfp8's
+    outputs and wu_s may be None."""
     _cuda(x, "x", torch.bfloat16)
     for t, n in ((wg_q, "wg_q"), (wg_s, "wg_s"), (wu_q, "wu_q"), (wu_s, "wu_s"), (wd_q, "wd_q"),
                  (wd_s, "wd_s")):

@@ -214,6 +214,13 @@ moe_config cfg_or_default(const moe_config* c) {
   return d;
 }
 
+// MMA N of the MXFP8 GEMMs: 256 halves the A traffic per FLOP; 128 keeps two
+// accumulators (and is the only width when H is not a multiple of 256)
+int mx_tile_n(const moe_config& c, int H, int F) {
+  return c.mxfp8_tile_n == 128 ? 128
+         : (c.mxfp8_tile_n == 256 || (F % 128 == 0 && H % 256 == 0)) ? 256 : 128;
+}
+
 moe_status check_block_args(int64_t T, int H, int F, int E, int k) {
   if (T < 0 || H <= 0 || F <= 0 || E < 1 || E > kMaxExperts || k < 1 || k > E || k > kMaxTopK)
     return MOE_ERR_INVALID_ARG;
@@ -985,6 +992,27 @@ moe_status moe_quantize_mxfp8_t(const void* in, int64_t batch, int rows, int col
                                         static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_tile_weight_scales_mxfp8(const uint8_t* wg_s, const uint8_t* wu_s,
+                                        const uint8_t* wd_s, int H, int F, int E,
+                                        const moe_config* cfg, uint8_t* wgu_tiled,
+                                        uint8_t* wd_tiled, void* stream) {
+  MOE_ENTRY_RANGE();
+  moe_status s = check_block_args(0, H, F, E, 1);
+  if (s != MOE_OK) return s;
+  if (!wg_s || !wu_s || !wd_s || !wgu_tiled || !wd_tiled) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(wg_s) & 3) || (reinterpret_cast<uintptr_t>(wu_s) & 3) ||
+      (reinterpret_cast<uintptr_t>(wd_s) & 3) || !aligned16(wgu_tiled) || !aligned16(wd_tiled))
+    return MOE_ERR_INVALID_ARG;
+  const moe_config c = cfg_or_default(cfg);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, mx_tile_n(c, H, F) / 2,
+                         wgu_tiled, st) != cudaSuccess ||
+      launch_tile_scales(wd_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0, wd_tiled, st) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
 moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const uint8_t* wg_s,
                                     const uint8_t* wu_q, const uint8_t* wu_s, const uint8_t* wd_q,
                                     const uint8_t* wd_s, const int32_t* expert_ids,
@@ -995,13 +1023,17 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   moe_status s = check_block_args(T, H, F, E, k);
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
-  if (!x || !wg_q || !wg_s || !wu_q || !wu_s || !wd_q || !wd_s || !expert_ids || !probs || !y)
+  const moe_config c = cfg_or_default(cfg);
+  const bool pretiled = c.mx_scales_pretiled != 0;
+  if (!x || !wg_q || !wg_s || !wu_q || (!wu_s && !pretiled) || !wd_q || !wd_s || !expert_ids ||
+      !probs || !y)
     return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(wg_q) || !aligned16(wu_q) || !aligned16(wd_q) ||
       !aligned16(y) || (reinterpret_cast<uintptr_t>(wg_s) & 3) ||
-      (reinterpret_cast<uintptr_t>(wu_s) & 3) || (reinterpret_cast<uintptr_t>(wd_s) & 3))
+      (!pretiled && (reinterpret_cast<uintptr_t>(wu_s) & 3)) ||
+      (reinterpret_cast<uintptr_t>(wd_s) & 3) ||
+      (pretiled && (!aligned16(wg_s) || !aligned16(wd_s))))   // read by bulk copies
     return MOE_ERR_INVALID_ARG;
-  const moe_config c = cfg_or_default(cfg);
   const bool save = c.save_for_backward != 0;
   const MxLayout L = mx_layout(T, H, F, E, k, save);
   if (!workspace || ws_bytes < L.total || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
@@ -1022,8 +1054,9 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   uint8_t* xq = at<uint8_t>(workspace, L.xq);
   uint8_t* xs_tok = at<uint8_t>(workspace, L.xs_tok);
   uint8_t* xs = at<uint8_t>(workspace, L.xs);
-  uint8_t* wgu_s = at<uint8_t>(workspace, L.wgu_s);
-  uint8_t* wd_st = at<uint8_t>(workspace, L.wd_s);
+  // the weights' scales in the block-scaled MMA's layout: given, or tiled here
+  const uint8_t* wgu_s = pretiled ? wg_s : at<uint8_t>(workspace, L.wgu_s);
+  const uint8_t* wd_st = pretiled ? wd_s : at<uint8_t>(workspace, L.wd_s);
   uint8_t* hq = at<uint8_t>(workspace, L.hq);
   uint8_t* hs = at<uint8_t>(workspace, L.hs);
   __nv_bfloat16* o = at<__nv_bfloat16>(workspace, L.o);
@@ -1042,14 +1075,12 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   // marks them in token_of
   if (save && launch_zero_padding(counts, off_al, E, H, xq, token_of, prob_of, st) != cudaSuccess)
     return MOE_ERR_CUDA;
-  // MMA N: 256 halves the A traffic per FLOP; 128 keeps two accumulators
-  const int mx_bn = c.mxfp8_tile_n == 128 ? 128
-                    : (c.mxfp8_tile_n == 256 || (F % 128 == 0 && H % 256 == 0)) ? 256 : 128;
-  // the weights' scales in the layout the block-scaled MMA reads
-  if (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, mx_bn / 2, wgu_s, st) !=
-          cudaSuccess ||
-      launch_tile_scales(wd_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0, wd_st, st) !=
-          cudaSuccess)
+  const int mx_bn = mx_tile_n(c, H, F);
+  if (!pretiled &&
+      (launch_tile_scales(wg_s, wu_s, static_cast<int64_t>(E) * 2 * F, F, H, mx_bn / 2,
+                          at<uint8_t>(workspace, L.wgu_s), st) != cudaSuccess ||
+       launch_tile_scales(wd_s, nullptr, static_cast<int64_t>(E) * H, H, F, 0,
+                          at<uint8_t>(workspace, L.wd_s), st) != cudaSuccess))
     return MOE_ERR_CUDA;
   mark(1);
 

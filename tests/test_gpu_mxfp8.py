@@ -169,3 +169,32 @@ def test_quantisers_nonfinite_blocks_bit_exact():
     for t in range(T):
         for j in range(k):
             assert np.array_equal(pq[row_of[t, j]], rq[t]), (t, j)
+
+
+@pytest.mark.parametrize("tile_n,pairs", [(128, 1), (256, 1), (256, 2), (128, 2)])
+def test_mxfp8_forward_pretiled_scales_bit_identical(tile_n, pairs):
+    """The weights' scales tiled once (moe_tile_weight_scales_mxfp8) and handed
+    to the forward with mx_scales_pretiled give its output bit for bit."""
+    case = _mx_case(300, 256, 384, 5, 2, seed=21, empty=(3,))
+    y0, wq = _gpu(*case, mxfp8_tile_n=tile_n, cta_pairs=pairs)
+    x, _, _, _, ids, probs = case
+    wgu_t, wd_t = m.moe_tile_weight_scales_mxfp8(wq[1], wq[3], wq[5],
+                                                  cfg=m.config(mxfp8_tile_n=tile_n))
+    cfg = m.config(mxfp8_tile_n=tile_n, cta_pairs=pairs, mx_scales_pretiled=True)
+    y1, _ = m.moe_expert_forward_mxfp8(dev(x), wq[0], wgu_t, wq[2], None, wq[4], wd_t, dev(ids),
+                                       dev(probs), cfg=cfg)
+    assert m.moe_get_error() == 0
+    assert torch.equal(y0, y1)
+
+
+def test_mxfp8_pretiled_scales_rejects_unaligned_buffers():
+    case = _mx_case(64, 256, 256, 2, 1, seed=5)
+    _, wq = _gpu(*case)
+    wgu_t, wd_t = m.moe_tile_weight_scales_mxfp8(wq[1], wq[3], wq[5])
+    x, _, _, _, ids, probs = case
+    cfg = m.config(mx_scales_pretiled=True)
+    shifted = torch.empty(wgu_t.numel() + 16, dtype=torch.uint8, device=wgu_t.device)[4:4 + wgu_t.numel()]
+    shifted.copy_(wgu_t)
+    with pytest.raises(m.MoeError):
+        m.moe_expert_forward_mxfp8(dev(x), wq[0], shifted, wq[2], None, wq[4], wd_t, dev(ids),
+                                   dev(probs), cfg=cfg)
