@@ -51,24 +51,24 @@ TRAFFIC = {
     # profiles/grouped_gemm_skewed_bf16_ncu_full.md
     ("skewed_bf16", "fc1_swiglu"): {"bytes": 1179.4e6, "sources": BF16_GEMM_SOURCES,
                                     "src_sha": "e59fc33167276ef4"},
-    # MXFP8 fc1: the 16-expert capture (727.7 MB for 718.1 MB algorithmic)
+    # MXFP8 fc1: the 16-expert capture (727.3 MB for 718.1 MB algorithmic)
     # scaled to the full launch (2871.9 MB); profiles/mx_gemm_mxfp8_16experts_ncu_full.md
-    ("mxfp8", "fc1_swiglu"): {"bytes": 2910e6, "sources": MXFP8_GEMM_SOURCES,
-                              "src_sha": "7e9b384d52e4b0b0"},
+    ("mxfp8", "fc1_swiglu"): {"bytes": 2909e6, "sources": MXFP8_GEMM_SOURCES,
+                              "src_sha": "d2f44ac20132c16e"},
     # dW1 of the training step (CTA pairs): the 2-expert capture (1168.4 MB for
     # 1208.4 MB algorithmic) scaled to the full launch (5905.5 MB);
     # profiles/grouped_gemm_backward_train_2experts_ncu_full.md
     ("train_bf16", "dW1"): {"bytes": 5710e6, "sources": BF16_GEMM_SOURCES,
                             "src_sha": "e59fc33167276ef4"},
     # fc1 with its bf16 saves in the MXFP8 training step: the 2-expert capture
-    # (626.4 MB for 672.3 MB algorithmic) scaled to the full launch (4410 MB);
+    # (626.0 MB for 672.3 MB algorithmic) scaled to the full launch (4410 MB);
     # profiles/mx_gemm_train_mxfp8_2experts_ncu_full.md
-    ("train_mxfp8", "fc1_swiglu"): {"bytes": 4109e6, "sources": MXFP8_GEMM_SOURCES,
-                                    "src_sha": "7e9b384d52e4b0b0"},
-    # dW1 of the MXFP8 training step: the 2-expert capture (1023.6 MB for
+    ("train_mxfp8", "fc1_swiglu"): {"bytes": 4106e6, "sources": MXFP8_GEMM_SOURCES,
+                                    "src_sha": "d2f44ac20132c16e"},
+    # dW1 of the MXFP8 training step: the 2-expert capture (1023.5 MB for
     # 1077.9 MB algorithmic) scaled to the full launch (4865.4 MB); same file
     ("train_mxfp8", "dW1"): {"bytes": 4620e6, "sources": MXFP8_GEMM_SOURCES,
-                             "src_sha": "7e9b384d52e4b0b0"},
+                             "src_sha": "d2f44ac20132c16e"},
 }
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
