@@ -27,6 +27,12 @@
  *    Errors found on the device (an expert id outside [0, E), an in-kernel
  *    wait that ran out of time) set a device error word and the affected work
  *    stops early; moe_get_error() reports them. Nothing traps.
+ *  - The library built with MOE_DEBUG (libmoe_gb300_debug.so) also checks,
+ *    on the device, every row index it takes from a row map against the rows
+ *    of the buffer it indexes, wherever the library knows that count (its
+ *    own workspaces, moe_permute's padded rows); an index outside sets
+ *    MOE_ERR_BOUNDS in the error word and its access is skipped. The release
+ *    build relies on the row maps being right by construction.
  *  - T = 0 (no tokens) is valid. The block's calls then launch nothing, or
  *    only what writes outputs that do not depend on the tokens: the counting
  *    calls (moe_counts, moe_counts_static, moe_route_topk) still write zero
@@ -54,7 +60,10 @@ typedef enum moe_status {
   MOE_ERR_BAD_EXPERT_ID = 3, /* device: an expert id outside [0, E)                 */
   MOE_ERR_WORKSPACE = 4,     /* workspace pointer null or smaller than required     */
   MOE_ERR_TIMEOUT = 5,       /* device: an in-kernel pipeline wait hit its limit    */
-  MOE_ERR_CUDA = 6           /* a CUDA runtime call failed (launch, attribute, ...) */
+  MOE_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...) */
+  MOE_ERR_BOUNDS = 7         /* device, MOE_DEBUG build only: a row index taken from a
+                                row map fell outside the buffer it indexes; the access
+                                was skipped (see moe_get_error)                       */
 } moe_status;
 
 typedef enum moe_precision { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_precision;

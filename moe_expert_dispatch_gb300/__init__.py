@@ -13,7 +13,10 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_gb300.so")
+# MOE_GB300_DEBUG=1 loads the MOE_DEBUG build (device-side bounds checks of
+# the row indices taken from row maps, reported as MOE_ERR_BOUNDS)
+DEBUG = os.environ.get("MOE_GB300_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300_debug.so" if DEBUG else "libmoe_gb300.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
@@ -24,7 +27,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 MOE_OK = 0
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported shape", 3: "expert id outside [0, E)",
-          4: "workspace missing or too small", 5: "in-kernel wait timed out", 6: "CUDA error"}
+          4: "workspace missing or too small", 5: "in-kernel wait timed out", 6: "CUDA error",
+          7: "row index outside its buffer (debug build)"}
 MOE_BF16, MOE_MXFP8 = 0, 1
 TILE_M = 128
 

@@ -1,8 +1,10 @@
-"""Builds libmoe_gb300.so in-tree with nvcc for sm_103a.
+"""Builds libmoe_gb300.so (and libmoe_gb300_debug.so, the same sources with
+MOE_DEBUG's device-side bounds checks) in-tree with nvcc for sm_103a.
 
 Each .cu file is compiled to an object in parallel, then the objects are
-linked into one shared library (CUDA runtime linked statically, no link to
-libcuda: the tensor-map encoder is fetched through the runtime at first use).
+linked into one shared library per variant (CUDA runtime linked statically,
+no link to libcuda: the tensor-map encoder is fetched through the runtime at
+first use).
 Run as `python moe_expert_dispatch_gb300/build.py` (or __graft_entry__.build()).
 """
 from __future__ import annotations
@@ -41,18 +43,32 @@ def _needs(obj: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+VARIANTS = {
+    # release: the product library; debug: the same sources with MOE_DEBUG,
+    # whose kernels bounds-check the row indices they take from row maps
+    "release": (BUILD, LIB, []),
+    "debug": (os.path.join(PKG, "_build_debug"), os.path.join(PKG, "libmoe_gb300_debug.so"),
+              ["-DMOE_DEBUG"]),
+}
+
+
+def build(verbose: bool = False, force: bool = False, variants=("release", "debug")) -> str:
+    """Compiles the named variants (all their translation units in one
+    parallel pool) and links each library; returns the release library's path."""
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "moe_expert.h"))
-    jobs = []
-    objs = []
-    for src in SOURCES:
-        s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
-        objs.append(o)
-        if force or _needs(o, [s] + headers):
-            jobs.append([nvcc(), *_flags(), "-c", s, "-o", o])
+    jobs, links = [], []
+    for v in variants:
+        bdir, lib, extra = VARIANTS[v]
+        os.makedirs(bdir, exist_ok=True)
+        objs = []
+        for src in SOURCES:
+            s = os.path.join(CSRC, src)
+            o = os.path.join(bdir, src.replace(".cu", ".o"))
+            objs.append(o)
+            if force or _needs(o, [s] + headers):
+                jobs.append([nvcc(), *_flags(), *extra, "-c", s, "-o", o])
+        links.append((lib, objs))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,8 +80,9 @@ def build(verbose: bool = False, force: bool = False) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(len(jobs)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _needs(LIB, objs):
-        run([nvcc(), *ARCH, "-shared", "-o", LIB, *objs])
+    for lib, objs in links:
+        if force or _needs(lib, objs):
+            run([nvcc(), *ARCH, "-shared", "-o", lib, *objs])
     return LIB
 
 

@@ -364,6 +364,7 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_WORKSPACE: return "workspace missing or too small";
     case MOE_ERR_TIMEOUT: return "in-kernel wait timed out";
     case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BOUNDS: return "row index outside its buffer (debug build)";
   }
   return "unknown status";
 }
@@ -377,6 +378,7 @@ moe_status moe_get_error(void* stream) {
   if (v && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   if (v & kErrBadId) return MOE_ERR_BAD_EXPERT_ID;
   if (v & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kErrBounds) return MOE_ERR_BOUNDS;
   return MOE_OK;
 }
 
@@ -454,9 +456,11 @@ moe_status moe_permute(const void* x, int64_t T, int64_t row_bytes, const int32_
   else
     e = launch_counts(ids, T * k, E, row_align, counts, nullptr, offsets, s, err, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = launch_rowmap(ids, probs, T * k, k, E, s, row_of, token_of, prob_of, st);
+  // x_perm, token_of and prob_of hold the padded row count (moe_padded_rows)
+  const int64_t cap = moe_padded_rows(T * k, E, row_align);
+  e = launch_rowmap(ids, probs, T * k, k, E, s, row_of, token_of, prob_of, st, cap, err);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return from_cuda(launch_permute_copy(x, T, row_bytes, k, row_of, x_perm, st));
+  return from_cuda(launch_permute_copy(x, T, row_bytes, k, row_of, x_perm, st, cap, err));
 }
 
 moe_status moe_unpermute(const void* o_perm, const int32_t* row_of, const float* probs, int64_t T,
@@ -544,14 +548,15 @@ struct FwdRun {
                              error_word(), st) != cudaSuccess) {
       return MOE_ERR_CUDA;
     }
-    if (launch_rowmap(ids(), weights(), L.R, k, E, rs, row_of, token_of, prob_of, st) !=
-        cudaSuccess)
+    if (launch_rowmap(ids(), weights(), L.R, k, E, rs, row_of, token_of, prob_of, st, L.cap,
+                      error_word()) != cudaSuccess)
       return MOE_ERR_CUDA;
     // with the fused gather, fc1 reads the routed rows straight from x; the
     // permuted copy is still made when the backward needs it
     const bool gather = c.fuse_gather != 0;
     if ((!gather || save) &&
-        launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st) != cudaSuccess)
+        launch_permute_copy(x, T, static_cast<int64_t>(H) * 2, k, row_of, xp, st, L.cap,
+                            error_word()) != cudaSuccess)
       return MOE_ERR_CUDA;
     if (save && launch_zero_padding(counts, off_al, E, static_cast<int64_t>(H) * 2, xp, token_of,
                                     prob_of, st) != cudaSuccess)
@@ -624,7 +629,8 @@ struct FwdRun {
 
   moe_status combine(cudaStream_t st) const {
     return from_cuda(launch_unpermute(at<__nv_bfloat16>(ws, L.o), at<int32_t>(ws, L.row_of),
-                                      weights(), T, k, H, static_cast<__nv_bfloat16*>(y), st));
+                                      weights(), T, k, H, static_cast<__nv_bfloat16*>(y), st,
+                                      L.cap, error_word()));
   }
 };
 
@@ -918,8 +924,8 @@ moe_status moe_expert_backward(const void* dy, const void* x, const void* w_gate
   gx.keep_a = keep(static_cast<uint64_t>(T) * k * F * 4);
   if (launch_dxp(t_da, t_wgk, t_wuk, ox, gx, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
-  if (launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st) !=
-      cudaSuccess)
+  if (launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st, L.cap,
+                       err) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(4);
 
@@ -1064,10 +1070,10 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   // counts -> offsets -> row map -> permute + quantise x (the dispatch)
   if (launch_counts(expert_ids, L.R, E, kTileM, counts, offsets, off_al, rs, err, st) !=
           cudaSuccess ||
-      launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st) !=
-          cudaSuccess ||
+      launch_rowmap(expert_ids, probs, L.R, k, E, rs, row_of, token_of, prob_of, st, L.cap,
+                    err) != cudaSuccess ||
       launch_permute_quantize(static_cast<const __nv_bfloat16*>(x), T, H, k, row_of, xq, xs_tok,
-                              st) != cudaSuccess ||
+                              st, L.cap, err) != cudaSuccess ||
       launch_gather_tile_scales(xs_tok, token_of, off_al, counts, E, H, L.cap, xs, st) !=
           cudaSuccess)
     return MOE_ERR_CUDA;
@@ -1155,7 +1161,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
     return MOE_ERR_CUDA;
   mark(3);
   const cudaError_t ue =
-      launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st);
+      launch_unpermute(o, row_of, probs, T, k, H, static_cast<__nv_bfloat16*>(y), st, L.cap, err);
   mark(4);
   return from_cuda(ue);
 }
@@ -1334,7 +1340,8 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st, pair_x ? &sx : nullptr)))
     return MOE_ERR_CUDA;
   mark(4);
-  if (!ok(launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st)))
+  if (!ok(launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st,
+                           cap, error_word())))
     return MOE_ERR_CUDA;
   mark(5);
 

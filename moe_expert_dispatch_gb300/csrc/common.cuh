@@ -16,6 +16,7 @@ namespace moe {
 enum : int {
   kErrBadId = 1 << 0,
   kErrTimeout = 1 << 1,
+  kErrBounds = 1 << 2,   // MOE_DEBUG builds: a row index outside its buffer
 };
 
 // Default bound of an in-kernel wait: no legitimate wait of these kernels
@@ -24,6 +25,25 @@ constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 __device__ __forceinline__ void report_error(int* err, int bits) {
   if (err) atomicOr(err, bits);
+}
+
+// A bounds check of the MOE_DEBUG build: a row index outside [0, n) sets
+// kErrBounds in the error word and the caller skips the access. The release
+// build compiles it to `true` (the library's row maps hold by construction).
+// n < 0: no bound is known (a row map handed in by the caller of a public
+// call that does not take the buffer's row count).
+__device__ __forceinline__ bool dbg_row_ok(int64_t r, int64_t n, int* err) {
+#ifdef MOE_DEBUG
+  if (n >= 0 && (r < 0 || r >= n)) {
+    report_error(err, kErrBounds);
+    return false;
+  }
+#else
+  (void)r;
+  (void)n;
+  (void)err;
+#endif
+  return true;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -62,13 +62,16 @@ cudaError_t launch_route_topk(const float* logits, int64_t T, int E, int k, int 
                               int32_t* off_al, RouteScratch s, cudaStream_t st);
 
 // Row of every slot, token and prob of every row (stable within an expert).
+// n_rows, err (here and below): the rows of the row-indexed buffers and the
+// error word, for the bounds checks of the MOE_DEBUG build (n_rows < 0: none).
 cudaError_t launch_rowmap(const int32_t* ids, const float* probs, int64_t n, int k, int E,
                           RouteScratch s, int32_t* row_of, int32_t* token_of, float* prob_of,
-                          cudaStream_t st);
+                          cudaStream_t st, int64_t n_rows = -1, int* err = nullptr);
 
 // xp[row_of[t, j]] = x[t] for every token (rows of row_bytes, % 16 == 0).
 cudaError_t launch_permute_copy(const void* x, int64_t T, int64_t row_bytes, int k,
-                                const int32_t* row_of, void* xp, cudaStream_t st);
+                                const int32_t* row_of, void* xp, cudaStream_t st,
+                                int64_t n_rows = -1, int* err = nullptr);
 
 // Zero the padding rows of every expert segment of xp (and mark them in
 // token_of / prob_of with -1 / 0).
@@ -77,7 +80,8 @@ cudaError_t launch_zero_padding(const int32_t* counts, const int32_t* off_al, in
                                 cudaStream_t st);
 
 cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
-                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st);
+                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st,
+                             int64_t n_rows = -1, int* err = nullptr);
 
 cudaError_t launch_quantize_mxfp8(const __nv_bfloat16* in, int64_t rows, int K, uint8_t* q,
                                   uint8_t* scales, cudaStream_t st);
@@ -211,7 +215,7 @@ cudaError_t launch_dout(const __nv_bfloat16* dy, const __nv_bfloat16* o, const i
 // order ([T, H/32], uint8).
 cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
                                     const int32_t* row_of, uint8_t* xq, uint8_t* xs_tok,
-                                    cudaStream_t st);
+                                    cudaStream_t st, int64_t n_rows = -1, int* err = nullptr);
 // token-order scales -> the tiled layout over the padded permuted rows.
 cudaError_t launch_gather_tile_scales(const uint8_t* xs_tok, const int32_t* token_of,
                                       const int32_t* off_al, const int32_t* counts, int E, int K,

@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(256) rowmap_kernel(const int32_t* __restrict__
                                                      const int32_t* __restrict__ base,
                                                      int32_t* __restrict__ row_of,
                                                      int32_t* __restrict__ token_of,
-                                                     float* __restrict__ prob_of) {
+                                                     float* __restrict__ prob_of,
+                                                     int64_t n_rows, int* err) {
   extern __shared__ int wc[];  // [kRowmapWarps][E]
   for (int i = threadIdx.x; i < kRowmapWarps * E; i += blockDim.x) wc[i] = 0;
   __syncthreads();
@@ -429,7 +430,7 @@ __global__ void __launch_bounds__(256) rowmap_kernel(const int32_t* __restrict__
     __syncwarp();
     if (i < n) {
       row_of[i] = r;
-      if (r >= 0) {
+      if (r >= 0 && dbg_row_ok(r, n_rows, err)) {
         token_of[r] = static_cast<int32_t>(i / k);
         if (prob_of) prob_of[r] = probs ? __ldg(probs + i) : 1.0f;
       }
@@ -439,11 +440,11 @@ __global__ void __launch_bounds__(256) rowmap_kernel(const int32_t* __restrict__
 
 cudaError_t launch_rowmap(const int32_t* ids, const float* probs, int64_t n, int k, int E,
                           RouteScratch s, int32_t* row_of, int32_t* token_of, float* prob_of,
-                          cudaStream_t st) {
+                          cudaStream_t st, int64_t n_rows, int* err) {
   const int64_t chunks = route_chunks(n);
   if (chunks == 0) return cudaSuccess;
   rowmap_kernel<<<static_cast<unsigned>(chunks), 256, kRowmapWarps * E * sizeof(int), st>>>(
-      ids, probs, n, k, E, s.base, row_of, token_of, prob_of);
+      ids, probs, n, k, E, s.base, row_of, token_of, prob_of, n_rows, err);
   return cudaGetLastError();
 }
 
@@ -462,7 +463,8 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
 __global__ void __launch_bounds__(256) permute_copy_kernel(const uint8_t* __restrict__ x,
                                                            int64_t T, int64_t row_bytes, int k,
                                                            const int32_t* __restrict__ row_of,
-                                                           uint8_t* __restrict__ xp) {
+                                                           uint8_t* __restrict__ xp,
+                                                           int64_t n_rows, int* err) {
   constexpr int U = 4;
   const int lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -481,7 +483,7 @@ __global__ void __launch_bounds__(256) permute_copy_kernel(const uint8_t* __rest
         if (c0 + 32 * u < n16) v[u] = ld_stream(src + c0 + 32 * u);
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0) continue;
+        if (r < 0 || !dbg_row_ok(r, n_rows, err)) continue;   // warp-uniform
         int4* dst = reinterpret_cast<int4*>(xp + static_cast<int64_t>(r) * row_bytes);
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -492,10 +494,12 @@ __global__ void __launch_bounds__(256) permute_copy_kernel(const uint8_t* __rest
 }
 
 cudaError_t launch_permute_copy(const void* x, int64_t T, int64_t row_bytes, int k,
-                                const int32_t* row_of, void* xp, cudaStream_t st) {
+                                const int32_t* row_of, void* xp, cudaStream_t st, int64_t n_rows,
+                                int* err) {
   if (T == 0) return cudaSuccess;
   permute_copy_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(
-      static_cast<const uint8_t*>(x), T, row_bytes, k, row_of, static_cast<uint8_t*>(xp));
+      static_cast<const uint8_t*>(x), T, row_bytes, k, row_of, static_cast<uint8_t*>(xp), n_rows,
+      err);
   return cudaGetLastError();
 }
 
@@ -550,7 +554,8 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const __nv_bfloat16* __r
                                                         const int32_t* __restrict__ row_of,
                                                         const float* __restrict__ probs,
                                                         int64_t T, int k, int H,
-                                                        __nv_bfloat16* __restrict__ y) {
+                                                        __nv_bfloat16* __restrict__ y,
+                                                        int64_t n_rows, int* err) {
   constexpr int U = kUnpermU;
   const int lane = lane_id();
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
@@ -569,9 +574,11 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const __nv_bfloat16* __r
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[u][q] = 0.0f;
     for (int j = 0; j < k; j += 2) {            // warp-uniform trip count
-      const int r0 = __shfl_sync(0xffffffffu, my_row, j);
+      int r0 = __shfl_sync(0xffffffffu, my_row, j);
       const float p0 = __shfl_sync(0xffffffffu, my_p, j);
-      const int r1 = __shfl_sync(0xffffffffu, my_row, (j + 1) & 31);
+      int r1 = __shfl_sync(0xffffffffu, my_row, (j + 1) & 31);
+      if (r0 >= 0 && !dbg_row_ok(r0, n_rows, err)) r0 = -1;      // warp-uniform
+      if (r1 >= 0 && !dbg_row_ok(r1, n_rows, err)) r1 = -1;
       const float p1 = __shfl_sync(0xffffffffu, my_p, (j + 1) & 31);
       const bool has1 = j + 1 < k && r1 >= 0;
       int4 v0[U], v1[U];
@@ -613,10 +620,12 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const __nv_bfloat16* __r
 }
 
 cudaError_t launch_unpermute(const __nv_bfloat16* o, const int32_t* row_of, const float* probs,
-                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st) {
+                             int64_t T, int k, int H, __nv_bfloat16* y, cudaStream_t st,
+                             int64_t n_rows, int* err) {
   if (T == 0) return cudaSuccess;
   const int64_t chunks = ((H >> 3) + 32 * kUnpermU - 1) / (32 * kUnpermU);
-  unpermute_kernel<<<grid_for_warps(T * chunks, 8), 256, 0, st>>>(o, row_of, probs, T, k, H, y);
+  unpermute_kernel<<<grid_for_warps(T * chunks, 8), 256, 0, st>>>(o, row_of, probs, T, k, H, y,
+                                                                  n_rows, err);
   return cudaGetLastError();
 }
 
@@ -1045,7 +1054,8 @@ cudaError_t launch_quantize_cols_blocked(const __nv_bfloat16* in, int rows, int 
 // pass covers 32 blocks with four loads in flight per lane.
 __global__ void __launch_bounds__(256) permute_quantize_kernel(
     const __nv_bfloat16* __restrict__ x, int64_t T, int H, int k,
-    const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_tok) {
+    const int32_t* __restrict__ row_of, uint8_t* __restrict__ xq, uint8_t* __restrict__ xs_tok,
+    int64_t n_rows, int* err) {
   constexpr int kU = 4;                      // groups of 8 blocks per pass
   const int lane = lane_id();
   const int part = lane & 3;                 // which 8 elements of the block
@@ -1087,7 +1097,7 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
       }
       for (int j = 0; j < k; ++j) {
         const int r = __shfl_sync(0xffffffffu, my_row, j);
-        if (r < 0) continue;                   // warp-uniform
+        if (r < 0 || !dbg_row_ok(r, n_rows, err)) continue;   // warp-uniform
         uint8_t* dst = xq + static_cast<int64_t>(r) * H + part * 8;
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
@@ -1101,9 +1111,10 @@ __global__ void __launch_bounds__(256) permute_quantize_kernel(
 
 cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, int k,
                                     const int32_t* row_of, uint8_t* xq, uint8_t* xs_tok,
-                                    cudaStream_t st) {
+                                    cudaStream_t st, int64_t n_rows, int* err) {
   if (T == 0) return cudaSuccess;
-  permute_quantize_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(x, T, H, k, row_of, xq, xs_tok);
+  permute_quantize_kernel<<<grid_for_warps(T, 8), 256, 0, st>>>(x, T, H, k, row_of, xq, xs_tok,
+                                                                 n_rows, err);
   return cudaGetLastError();
 }
 

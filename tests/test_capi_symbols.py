@@ -37,6 +37,18 @@ def test_every_declared_symbol_is_exported(lib):
     assert not missing, missing
 
 
+def test_debug_build_exports_the_same_symbols(lib):
+    """The MOE_DEBUG library (device-side bounds checks) is built beside the
+    release one and offers the same entry points; it maps its own error bit
+    to a status of its own."""
+    path = os.path.join(ROOT, "moe_expert_dispatch_gb300", "libmoe_gb300_debug.so")
+    dbg = ctypes.CDLL(path)
+    missing = [n for n in declared_functions() if not hasattr(dbg, n)]
+    assert not missing, missing
+    dbg.moe_status_string.restype = ctypes.c_char_p
+    assert b"debug build" in dbg.moe_status_string(7)
+
+
 def test_host_side_queries(lib):
     import moe_expert_dispatch_gb300 as m
     assert m.moe_padded_rows(8192, 8, 128) == 9216
