@@ -42,33 +42,21 @@ import synth  # noqa: E402
 BF16_GEMM_SOURCES = ("gemm_bf16.cu", "common.cuh", "internal.h")
 MXFP8_GEMM_SOURCES = ("gemm_mxfp8.cu", "mx.cuh", "common.cuh", "internal.h")
 TRAFFIC = {
-    # fc1 on the Mixtral-shaped workload (CTA pairs): the 2-expert capture
-    # (643.7 MB for 620.8 MB algorithmic) scaled by the algorithmic bytes of
-    # the full launch (2181 MB); profiles/grouped_gemm_mixtral_2experts_ncu_full.md
-    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2262e6, "sources": BF16_GEMM_SOURCES,
-                                     "src_sha": "e59fc33167276ef4"},
-    # fc1 on the skewed workload (CTA pairs), captured at full size;
-    # profiles/grouped_gemm_skewed_bf16_ncu_full.md
-    ("skewed_bf16", "fc1_swiglu"): {"bytes": 1179.4e6, "sources": BF16_GEMM_SOURCES,
-                                    "src_sha": "e59fc33167276ef4"},
-    # MXFP8 fc1: the 16-expert capture (727.3 MB for 718.1 MB algorithmic)
-    # scaled to the full launch (2871.9 MB); profiles/mx_gemm_mxfp8_16experts_ncu_full.md
-    ("mxfp8", "fc1_swiglu"): {"bytes": 2909e6, "sources": MXFP8_GEMM_SOURCES,
-                              "src_sha": "d2f44ac20132c16e"},
-    # dW1 of the training step (CTA pairs): the 2-expert capture (1168.4 MB for
-    # 1208.4 MB algorithmic) scaled to the full launch (5905.5 MB);
-    # profiles/grouped_gemm_backward_train_2experts_ncu_full.md
-    ("train_bf16", "dW1"): {"bytes": 5710e6, "sources": BF16_GEMM_SOURCES,
-                            "src_sha": "e59fc33167276ef4"},
-    # fc1 with its bf16 saves in the MXFP8 training step: the 2-expert capture
-    # (626.0 MB for 672.3 MB algorithmic) scaled to the full launch (4410 MB);
-    # profiles/mx_gemm_train_mxfp8_2experts_ncu_full.md
-    ("train_mxfp8", "fc1_swiglu"): {"bytes": 4106e6, "sources": MXFP8_GEMM_SOURCES,
-                                    "src_sha": "d2f44ac20132c16e"},
-    # dW1 of the MXFP8 training step: the 2-expert capture (1023.5 MB for
-    # 1077.9 MB algorithmic) scaled to the full launch (4865.4 MB); same file
-    ("train_mxfp8", "dW1"): {"bytes": 4620e6, "sources": MXFP8_GEMM_SOURCES,
-                             "src_sha": "d2f44ac20132c16e"},
+    # DRAM bytes per launch of each workload's dominant GEMM, from counters of
+    # small cases scaled to the full launch by the algorithmic bytes;
+    # profiles/gemm_dram_traffic.md has the captures and the arithmetic
+    ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2158e6, "sources": BF16_GEMM_SOURCES,
+                                     "src_sha": "68ddcfddb25e5d7e"},
+    ("skewed_bf16", "fc1_swiglu"): {"bytes": 1175.4e6, "sources": BF16_GEMM_SOURCES,
+                                    "src_sha": "68ddcfddb25e5d7e"},
+    ("train_bf16", "dW1"): {"bytes": 5684e6, "sources": BF16_GEMM_SOURCES,
+                            "src_sha": "68ddcfddb25e5d7e"},
+    ("mxfp8", "fc1_swiglu"): {"bytes": 2912e6, "sources": MXFP8_GEMM_SOURCES,
+                              "src_sha": "a438201b20843ea3"},
+    ("train_mxfp8", "fc1_swiglu"): {"bytes": 4103e6, "sources": MXFP8_GEMM_SOURCES,
+                                    "src_sha": "a438201b20843ea3"},
+    ("train_mxfp8", "dW1"): {"bytes": 4604e6, "sources": MXFP8_GEMM_SOURCES,
+                             "src_sha": "a438201b20843ea3"},
 }
 FP8_OVER_BF16 = 2.0   # nominal dense FP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 
