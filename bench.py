@@ -43,8 +43,9 @@ BF16_GEMM_SOURCES = ("gemm_bf16.cu", "common.cuh", "internal.h")
 MXFP8_GEMM_SOURCES = ("gemm_mxfp8.cu", "mx.cuh", "common.cuh", "internal.h")
 TRAFFIC = {
     # DRAM bytes per launch of each workload's dominant GEMM, from counters of
-    # small cases scaled to the full launch by the algorithmic bytes;
-    # profiles/gemm_dram_traffic.md has the captures and the arithmetic
+    # small cases (dram__bytes_read.sum + dram__bytes_write.sum) scaled to the
+    # full launch by the algorithmic bytes; the captures and the arithmetic are
+    # summarised under profiles/
     ("mixtral_bf16", "fc1_swiglu"): {"bytes": 2158e6, "sources": BF16_GEMM_SOURCES,
                                      "src_sha": "68ddcfddb25e5d7e"},
     ("skewed_bf16", "fc1_swiglu"): {"bytes": 1175.4e6, "sources": BF16_GEMM_SOURCES,
