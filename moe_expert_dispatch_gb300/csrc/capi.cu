@@ -316,6 +316,18 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_scale_maps(MxScaleMaps* m, const uint8_t* sfa, uint64_t sfa_bytes, const uint8_t* sfb,
+                     uint64_t sfb_bytes, const uint8_t* sfb1, uint64_t sfb1_bytes) {
+  if (!make_tmap_scale_rows(&m->map[0], sfa, sfa_bytes) ||
+      !make_tmap_scale_rows(&m->map[1], sfb, sfb_bytes))
+    return false;
+  if (!sfb1) {
+    m->map[2] = m->map[1];
+    return true;
+  }
+  return make_tmap_scale_rows(&m->map[2], sfb1, sfb1_bytes);
+}
+
 bool make_tmap_scale_rows(CUtensorMap* map, const void* base, uint64_t bytes) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || bytes % 512 != 0 || bytes == 0) return false;
@@ -1090,10 +1102,9 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
     return MOE_ERR_CUDA;
   mark(1);
 
-  // CTA pairs only when asked for: measured on the MXFP8 workloads with
-  // 256-wide N tiles they are no faster (the block-scaled GEMMs are not
-  // bound by their operand traffic). A pair's CTA reads N / 2 rows of B,
-  // and the pairs' scale atoms arrive through tensor maps.
+  // CTA pairs only when asked for: measured on the MXFP8 workloads they are
+  // no faster (the pair's copies of the scale atoms into tensor memory cost
+  // it about a fifth of its tensor pipe). A pair's CTA reads N / 2 rows of B.
   const bool pairs = c.cta_pairs == 2;
   const uint32_t b_box = (pairs && mx_bn == 128) ? 64 : 128;
   CUtensorMap ta, tg, tu, th, td;
@@ -1132,15 +1143,12 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
   g1.pair = pairs ? 1 : 0;
   MxScaleMaps s1, s2;
-  if (pairs &&
-      (!make_tmap_scale_rows(&s1.map[0], xs, static_cast<uint64_t>(L.cap) * H / 32) ||
-       !make_tmap_scale_rows(&s1.map[1], wgu_s, static_cast<uint64_t>(E) * 2 * F * H / 32) ||
-       !make_tmap_scale_rows(&s2.map[0], hs, static_cast<uint64_t>(L.cap) * F / 32) ||
-       !make_tmap_scale_rows(&s2.map[1], wd_st, static_cast<uint64_t>(E) * H * F / 32)))
+  if (!make_scale_maps(&s1, xs, static_cast<uint64_t>(L.cap) * H / 32, wgu_s,
+                       static_cast<uint64_t>(E) * 2 * F * H / 32) ||
+      !make_scale_maps(&s2, hs, static_cast<uint64_t>(L.cap) * F / 32, wd_st,
+                       static_cast<uint64_t>(E) * H * F / 32))
     return MOE_ERR_CUDA;
-  s1.map[2] = s1.map[1];
-  s2.map[2] = s2.map[1];
-  if (launch_mx_fc1(ta, tg, tu, o1, g1, grid, st, pairs ? &s1 : nullptr) != cudaSuccess)
+  if (launch_mx_fc1(ta, tg, tu, o1, g1, grid, st, s1) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(2);
   MxGemmArgs g2 = g1;
@@ -1157,7 +1165,7 @@ moe_status moe_expert_forward_mxfp8(const void* x, const uint8_t* wg_q, const ui
   if (!make_out_tmap(&o2.map[0], o, H, L.cap, static_cast<uint64_t>(H) * 2, false))
     return MOE_ERR_CUDA;
   o2.map[1] = o2.map[2] = o2.map[0];
-  if (launch_mx_fc2(th, td, o2, g2, grid, st, pairs ? &s2 : nullptr) != cudaSuccess)
+  if (launch_mx_fc2(th, td, o2, g2, grid, st, s2) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(3);
   const cudaError_t ue =
@@ -1292,22 +1300,20 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   GemmOut od;
   od.map[0] = od.map[1] = od.map[2] = t_doq;     // unused
   g.keep_a = keep(static_cast<uint64_t>(cap) * H);
-  MxScaleMaps sh, sx;
-  const bool pair_h = pairs, pair_x = pairs;
-  if ((pair_h && (!make_tmap_scale_rows(&sh.map[0], at<uint8_t>(ws, B.dos),
-                                        static_cast<uint64_t>(cap) * H / 32) ||
-                  !make_tmap_scale_rows(&sh.map[1], at<uint8_t>(ws, B.w2_st),
-                                        static_cast<uint64_t>(E) * F * H / 32))) ||
-      (pair_x && (!make_tmap_scale_rows(&sx.map[0], at<uint8_t>(ws, B.das),
-                                        static_cast<uint64_t>(cap) * 2 * F / 32) ||
-                  !make_tmap_scale_rows(&sx.map[1], at<uint8_t>(ws, B.w1g_st),
-                                        static_cast<uint64_t>(E) * H * F / 32) ||
-                  !make_tmap_scale_rows(&sx.map[2], at<uint8_t>(ws, B.w1u_st),
-                                        static_cast<uint64_t>(E) * H * F / 32))))
+  MxScaleMaps sh, sx, sw1, sw2;
+  if (!make_scale_maps(&sh, at<uint8_t>(ws, B.dos), static_cast<uint64_t>(cap) * H / 32,
+                       at<uint8_t>(ws, B.w2_st), static_cast<uint64_t>(E) * F * H / 32) ||
+      !make_scale_maps(&sx, at<uint8_t>(ws, B.das), static_cast<uint64_t>(cap) * 2 * F / 32,
+                       at<uint8_t>(ws, B.w1g_st), static_cast<uint64_t>(E) * H * F / 32,
+                       at<uint8_t>(ws, B.w1u_st), static_cast<uint64_t>(E) * H * F / 32) ||
+      !make_scale_maps(&sw1, at<uint8_t>(ws, B.dats), static_cast<uint64_t>(cap) * 2 * F / 32,
+                       at<uint8_t>(ws, B.xpts), static_cast<uint64_t>(cap) * H / 32) ||
+      !make_scale_maps(&sw2, at<uint8_t>(ws, B.dots), static_cast<uint64_t>(cap) * H / 32,
+                       at<uint8_t>(ws, B.hts), static_cast<uint64_t>(cap) * F / 32))
     return MOE_ERR_CUDA;
-  sh.map[2] = sh.map[1];
+  const bool pair_h = pairs, pair_x = pairs;
   g.pair = pair_h ? 1 : 0;
-  if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st, pair_h ? &sh : nullptr)))
+  if (!ok(launch_mx_dh(t_doq, t_w2, od, g, grid, st, sh)))
     return MOE_ERR_CUDA;
   mark(2);
 
@@ -1337,7 +1343,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   ox.map[1] = ox.map[2] = ox.map[0];
   g.keep_a = keep(static_cast<uint64_t>(cap) * 2 * F);
   g.pair = pair_x ? 1 : 0;
-  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st, pair_x ? &sx : nullptr)))
+  if (!ok(launch_mx_dxp(t_daq, t_w1g, t_w1u, ox, g, grid, st, sx)))
     return MOE_ERR_CUDA;
   mark(4);
   if (!ok(launch_unpermute(d_xp, row_of, nullptr, T, k, H, static_cast<__nv_bfloat16*>(dx), st,
@@ -1376,7 +1382,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
   ow2.map[1] = ow2.map[2] = ow2.map[0];
   g.out_split = F;
   g.accumulate = accumulate_dw;
-  if (!ok(launch_mx_wgrad(t_daT, t_xpT, ow1, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_wgrad(t_daT, t_xpT, ow1, g, grid, st, sw1))) return MOE_ERR_CUDA;
   mark(7);
   g = base;
   g.M = H;
@@ -1389,7 +1395,7 @@ moe_status moe_expert_backward_mxfp8(const void* dy, const void* x, const uint8_
 
   g.out_split = 0;
   g.accumulate = accumulate_dw;
-  if (!ok(launch_mx_wgrad(t_doT, t_hT, ow2, g, grid, st))) return MOE_ERR_CUDA;
+  if (!ok(launch_mx_wgrad(t_doT, t_hT, ow2, g, grid, st, sw2))) return MOE_ERR_CUDA;
   mark(8);
   return MOE_OK;
 }

@@ -353,14 +353,16 @@ __global__ void __launch_bounds__(num_threads<kEpi>(), 1)
               for (int j = 0; j < kTileN; j += 128)
                 tma_load_2d(sb + j * BK, mb, full, kbb * BK + tl.k0, static_cast<int>(b_row + j));
             }
-            bulk_copy_g2s(ssf, p.sfa + ((static_cast<int64_t>(a_row) >> 7) * kgroups_a + kg0 + kb) * kSfBytes,
-                          kSfBytes, full);
-            const uint8_t* sfb = second ? p.sfb1 : p.sfb;
+            // the scale atoms through the 2D scale maps (one atom per box): a
+            // plain bulk copy holds the issuing thread for about as long as its
+            // bytes take to arrive, a tensor-map copy does not
+            tma_load_2d(ssf, &tmSA, full, 0,
+                        static_cast<int>(2 * ((static_cast<int64_t>(a_row) >> 7) * kgroups_a + kg0 + kb)));
+            const CUtensorMap* msb = second ? &tmSB1 : &tmSB0;
 #pragma unroll
             for (int j = 0; j < G::kSfbAtoms; ++j)
-              bulk_copy_g2s(ssf + (1 + j) * kSfBytes,
-                            sfb + (((vrow >> 7) + j) * kgroups_b + kg0 + kbb) * kSfBytes, kSfBytes,
-                            full);
+              tma_load_2d(ssf + (1 + j) * kSfBytes, msb, full, 0,
+                          static_cast<int>(2 * (((vrow >> 7) + j) * kgroups_b + kg0 + kbb)));
             ++fills;
             if (++stage == S) {
               stage = 0;
@@ -835,52 +837,49 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
                             sc.map[1], sc.map[2], p);
 }
 
-// CTA pairs run tiles of the Rows schedule when asked for and given the scale
-// maps (a pair's B maps then have boxes of N / 2 rows); everything else runs
-// one CTA per tile.
+// CTA pairs run tiles of the Rows schedule when asked for (a pair's B maps
+// then have boxes of N / 2 rows); everything else runs one CTA per tile.
 template <MxEpi kEpi, Sched kSched>
 cudaError_t launch_mx_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                          const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
-                         const MxScaleMaps* sc) {
-  MxScaleMaps none;
-  none.map[0] = none.map[1] = none.map[2] = a;   // unused by one-CTA tiles
+                         const MxScaleMaps& sc) {
   if constexpr (kSched == Sched::Rows) {
-    if (p.pair && sc)
-      return p.bn == 256 ? launch_mx<kEpi, kSched, 256, true>(a, b0, b1, o, *sc, p, grid, st)
-                         : launch_mx<kEpi, kSched, 128, true>(a, b0, b1, o, *sc, p, grid, st);
+    if (p.pair)
+      return p.bn == 256 ? launch_mx<kEpi, kSched, 256, true>(a, b0, b1, o, sc, p, grid, st)
+                         : launch_mx<kEpi, kSched, 128, true>(a, b0, b1, o, sc, p, grid, st);
   }
-  return p.bn == 256 ? launch_mx<kEpi, kSched, 256, false>(a, b0, b1, o, none, p, grid, st)
-                     : launch_mx<kEpi, kSched, 128, false>(a, b0, b1, o, none, p, grid, st);
+  return p.bn == 256 ? launch_mx<kEpi, kSched, 256, false>(a, b0, b1, o, sc, p, grid, st)
+                     : launch_mx<kEpi, kSched, 128, false>(a, b0, b1, o, sc, p, grid, st);
 }
 
 }  // namespace
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc) {
+                          const MxScaleMaps& sc) {
   return p.save ? launch_mx_bn<MxEpi::Fc1Save, Sched::Rows>(a, wg, wu, o, p, grid, st, sc)
                 : launch_mx_bn<MxEpi::Fc1, Sched::Rows>(a, wg, wu, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,
-                          const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps* sc) {
+                          const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc) {
   return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, wd, wd, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
-                         const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps* sc) {
+                         const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc) {
   return launch_mx_bn<MxEpi::SwigluBwd, Sched::Rows>(a, w2, w2, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc) {
+                          const MxScaleMaps& sc) {
   return launch_mx_bn<MxEpi::Bf16, Sched::Rows>(a, w1g, w1u, o, p, grid, st, sc);
 }
 
 cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
-                            const MxGemmArgs& p, int grid, cudaStream_t st) {
-  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, o, p, grid, st, nullptr);
+                            const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc) {
+  return launch_mx_bn<MxEpi::F32, Sched::WGrad>(a, b, b, o, p, grid, st, sc);
 }
 
 }  // namespace moe

@@ -265,20 +265,23 @@ struct MxGemmArgs {
   int out_split;           // WGrad: rows r < out_split of each expert go to output map 0
                            // (row e * out_split + r), the rest to map 1; 0 means M
   int accumulate;          // WGrad: add to the outputs instead of overwriting
-  int pair;                // Rows, bn = 256: CTA pairs share M = 256 tiles; the scale
-                           // atoms then arrive through the MxScaleMaps
+  int pair;                // Rows: CTA pairs share M = 256 tiles
   int* err;
   unsigned long long wait_ns;
 };
 
 // Tensor maps over the tiled scale arrays (sfa, sfb, sfb1) as rows of 256
-// bytes, one 512-byte atom per box of two rows (make_tmap_scale_rows): the
-// scale loads of CTA pairs, whose copies must complete on the leader's
-// barrier. Unused entries may repeat a used one.
+// bytes, one 512-byte atom per box of two rows (make_tmap_scale_rows): every
+// MXFP8 GEMM loads its scale atoms through them (a tensor-map copy is cheap
+// to issue; a CTA pair's copies can complete on the leader's barrier).
 struct MxScaleMaps {
   CUtensorMap map[3];
 };
 bool make_tmap_scale_rows(CUtensorMap* map, const void* base, uint64_t bytes);
+// The maps of one GEMM's scale arrays (sizes in bytes); without sfb1, map 2
+// repeats map 1.
+bool make_scale_maps(MxScaleMaps* m, const uint8_t* sfa, uint64_t sfa_bytes, const uint8_t* sfb,
+                     uint64_t sfb_bytes, const uint8_t* sfb1 = nullptr, uint64_t sfb1_bytes = 0);
 
 // The forward keeps A_g and A_u [rows, N] (rows, N % 32 == 0) in 32 x 32
 // blocks of 2 KB, block (row / 32, col / 32) at ((row / 32) * (N / 32) +
@@ -297,21 +300,19 @@ bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_
 
 cudaError_t launch_mx_fc1(const CUtensorMap& a, const CUtensorMap& wg, const CUtensorMap& wu,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc = nullptr);
+                          const MxScaleMaps& sc);
 // dH with the SwiGLU backward epilogue (Rows; B = W2 as [E*F, H] along H).
 cudaError_t launch_mx_dh(const CUtensorMap& a, const CUtensorMap& w2, const GemmOut& o,
-                         const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc = nullptr);
+                         const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc);
 // dXp = bf16(dA_g W1g^T + dA_u W1u^T) (Rows; K = 2F split over B0, B1).
 cudaError_t launch_mx_dxp(const CUtensorMap& a, const CUtensorMap& w1g, const CUtensorMap& w1u,
                           const GemmOut& o, const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc = nullptr);
+                          const MxScaleMaps& sc);
 // Weight gradients (WGrad: K = each expert's padded rows), float out.
 cudaError_t launch_mx_wgrad(const CUtensorMap& a, const CUtensorMap& b, const GemmOut& o,
-                            const MxGemmArgs& p, int grid, cudaStream_t st);
+                            const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc);
 cudaError_t launch_mx_fc2(const CUtensorMap& a, const CUtensorMap& wd, const GemmOut& o,
-                          const MxGemmArgs& p, int grid, cudaStream_t st,
-                          const MxScaleMaps* sc = nullptr);
+                          const MxGemmArgs& p, int grid, cudaStream_t st, const MxScaleMaps& sc);
 
 int device_sm_count();
 // The current CUDA device, or -1; launchers keep per-device state indexed by
