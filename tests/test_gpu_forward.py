@@ -1,8 +1,9 @@
 """GPU parity of the fused forward (counts -> permute -> fc1+SwiGLU -> fc2 ->
 unpermute) against the CPU oracle, within |y - y_ref| <= 1e-2 + 1e-2 |y_ref|,
 on small ragged shapes, the tiny and skewed workloads in full, the
-Mixtral-shaped workload on sampled tokens, and the invariants (schedule and
-ring-depth independence, micro-batch split, empty experts, error paths)."""
+Mixtral-shaped workload on sampled tokens and, on exact-arithmetic inputs, on
+every token bit for bit, and the invariants (schedule and ring-depth
+independence, micro-batch split, empty experts, error paths)."""
 import numpy as np
 import pytest
 import torch
@@ -86,6 +87,24 @@ def test_forward_mixtral_workload_sampled():
     ref = orc.sampled_forward(to_np(case[0]), f32_slices(case[1]), f32_slices(case[2]),
                               f32_slices(case[3]), case[4].numpy(), case[5].numpy(), toks)
     assert_bf16_close(y[toks], ref, "y sampled")
+
+
+def test_forward_mixtral_workload_exact_all_tokens():
+    """The Mixtral-shaped forward at full size (T=4096, H=4096, F=14336, E=8,
+    k=2) on exact-arithmetic inputs (small integers, dyadic weights, a
+    saturated gate): y of every token within the BF16 bound and bit-equal to
+    the oracle's whole forward, on CTA pairs (the default here) and on one
+    CTA per tile."""
+    w = synth.WORKLOADS["mixtral_bf16"]
+    inp = synth.exact_inputs(w, 0)
+    case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
+    ref = orc.expert_forward(to_np(case[0]), f32_slices(case[1]), f32_slices(case[2]),
+                             f32_slices(case[3]), case[4].numpy(),
+                             case[5].numpy().astype(np.float64), num_experts=w.E)
+    for pairs in (0, 1):
+        y = to_np(_gpu(*case, cta_pairs=pairs))
+        assert_bf16_close(y, ref, f"y (cta_pairs={pairs})")
+        assert np.array_equal(y, ref), f"y: {int((y != ref).sum())} of {y.size} not bit-equal"
 
 
 def test_forward_independent_of_schedule_and_ring_depth():
