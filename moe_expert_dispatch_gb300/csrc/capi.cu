@@ -611,6 +611,7 @@ struct FwdRun {
     g1.err = error_word();
     g1.wait_ns = static_cast<unsigned long long>(c.wait_limit_ns);
     g1.gather_token = at<int32_t>(ws, L.token_of);
+    g1.gather_x = static_cast<const __nv_bfloat16*>(x);
     g1.counts = at<int32_t>(ws, L.counts);
     g1.keep_a = keep(static_cast<uint64_t>(L.R) * H * 2);
     const int grid = grid_size(c);

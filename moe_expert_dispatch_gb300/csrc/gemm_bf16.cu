@@ -171,7 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(smem_u32(&sm->full[s]), 1);
+      // gathering: the producer's expect_tx arrival and one cp.async
+      // arrival per lane of the producer warp
+      mbar_init(smem_u32(&sm->full[s]), kGather ? 33 : 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -221,23 +223,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (kGather && warp == 0) {
     // ---------------------------------------------------------- gathering producer
-    // The whole warp: lane l gathers rows 4l..4l+3 of the A tile with one TMA
-    // gather4 per k-block (4 token rows of x, 64 columns each, into 4
-    // consecutive 128-byte rows of the slot, swizzled like a tiled load);
-    // lane 0 also loads the weight boxes. This is the dispatch AllToAllv of
-    // all2all_grouped_matmul folded into the GEMM's producer.
+    // The whole warp gathers the A tile's 128 token rows of x (64 columns, 128
+    // bytes each) with cp.async: per warp instruction 4 rows of 8 lanes x 16
+    // bytes (lane l: row 4i + l / 8, chunk l % 8), written swizzled as a tiled
+    // 128B-swizzle load would (chunk c of row r at c ^ (r & 7)); each lane
+    // then arrives on the slot's barrier once its copies have landed. Lane 0
+    // also loads the weight boxes by TMA. This is the dispatch AllToAllv of
+    // all2all_grouped_matmul folded into the GEMM's producer. (TMA gather4,
+    // four rows per instruction, was bound by the TMA unit's rate at 3.4x the
+    // materialised permute.)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t fills = 0;
     bool ok = true;
+    const int chunk = lane & 7;
     for (int t = walk0; t < total && ok; t += walk_step) {
       const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
       const int real_end = p.off_al[tl.e] + p.counts[tl.e];
-      int tok[4];
+      const __nv_bfloat16* src[32];             // this lane's 32 rows, at column 0
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = tl.row0 + 4 * lane + i;
-        tok[i] = r < real_end ? __ldg(p.gather_token + r) : 0;   // padding rows: any valid row
+      for (int i = 0; i < 32; ++i) {
+        const int r = tl.row0 + 4 * i + (lane >> 3);
+        const int tok = r < real_end ? __ldg(p.gather_token + r) : 0;   // padding: any valid row
+        src[i] = p.gather_x + static_cast<int64_t>(tok) * p.K + chunk * 8;
       }
       const int krow = tl.e * static_cast<int>(p.b_rows);
       const int n0 = tl.n * (bn / 2);
@@ -250,15 +258,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sa = smem_u32(ring + stage * kStageBytes);
         const uint32_t sb = sa + kABytes;
-        if (lane == 0) mbar_arrive_expect_tx(full, stage_tx);
-        __syncwarp();
-        tma_gather4(sa + lane * 512, &tmA, full, kb * BK, tok[0], tok[1], tok[2], tok[3]);
         if (lane == 0) {
+          mbar_arrive_expect_tx(full, (bn / 64) * kBBox);
           for (int j = 0; j < bn / 128; ++j) {
             tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow + kb * BK);
             tma_load_2d(sb + (bn / 128 + j) * kBBox, &tmB1, full, n0 + 64 * j, krow + kb * BK);
           }
         }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * BK);
+        }
+        cp_async_arrive_noinc(full);
         ++fills;
         if (++stage == S) {
           stage = 0;
@@ -428,6 +440,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // a gathered A tile was written through the generic proxy (cp.async):
+          // order it before the tensor core's async-proxy reads
+          if (kGather) fence_proxy_async_shared();
           tc_fence_after();
           // K-major, 128B swizzle: 8-row groups 1024 B apart, +32 B per K=16.
           // MN-major, 128B swizzle: 64-wide atoms 8 KB apart (LBO), 8-row K

@@ -157,6 +157,7 @@ struct GroupedGemmArgs {
   int keep_a;              // L2 evict_last hint on A loads (A small enough to stay resident)
   const int32_t* gather_token;  // fc1 with fused gather: token of each padded row
   const int32_t* counts;        // fc1 with fused gather: rows of each expert
+  const __nv_bfloat16* gather_x;  // fc1 with fused gather: x [T, K], rows read by cp.async
   int pair;                // Rows: CTA pairs (cta_group::2) share M = 256 tiles; a
                            // K-major B map then has boxes of bn/2 rows
   int* err;
