@@ -636,6 +636,8 @@ struct FwdRun {
     g2.ldo = H;
     g2.save_g = g2.save_u = nullptr;
     g2.keep_a = keep(static_cast<uint64_t>(L.R) * F * 2);
+    g2.pair = use_pairs(c, L.R, E) ? 1 : 0;     // fc2 gathers nothing: pairs as usual
+    g2.stages = bf16_stages(c, g2.pair != 0);
     if (launch_fc2(th, td, o2, g2, grid, st) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }

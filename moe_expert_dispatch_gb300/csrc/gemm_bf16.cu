@@ -58,6 +58,11 @@ constexpr int stage_bytes() { return kABytes + (kPair ? 2 : 4) * kBBox; }
 template <bool kPair>
 constexpr int max_stages() { return kPair ? 6 : 4; }
 constexpr int kThreads = 192;
+// fc1 with the fused gather: warp 0 and the added warps 6.. gather, each
+// copying 128 / kGatherWarps of the tile's token rows
+constexpr int kGatherWarps = 2;
+template <bool kGather>
+constexpr int block_threads() { return kGather ? kThreads + 32 * (kGatherWarps - 1) : kThreads; }
 constexpr uint32_t kTmemCols = 512;
 constexpr unsigned long long kDrainNs = 1000000000ull;
 constexpr unsigned long long kPairDrainNs = 50000000ull;
@@ -141,7 +146,7 @@ constexpr int kSlotsPerWarp = 3;
 constexpr int kPieceArea = 4 * kSlotsPerWarp * kPieceBytes;   // 24 KB
 
 template <Epi kEpi, bool kAmn, bool kBmn, Sched kSched, bool kGather, int kBN, bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(block_threads<kGather>(), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1,
@@ -172,8 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       // gathering: the producer's expect_tx arrival and one cp.async
-      // arrival per lane of the producer warp
-      mbar_init(smem_u32(&sm->full[s]), kGather ? 33 : 1);
+      // arrival per lane of the gathering warps
+      mbar_init(smem_u32(&sm->full[s]), kGather ? 1 + 32 * kGatherWarps : 1);
       mbar_init(smem_u32(&sm->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -204,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   int total;
   if (kSched == Sched::Rows) {
-    for (int e = threadIdx.x; e < E; e += kThreads)
+    for (int e = threadIdx.x; e < E; e += block_threads<kGather>())
       ts[e + 1] = m_tiles<kPair>((p.off_al[e + 1] - p.off_al[e]) / kTileM) * n_tiles;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -221,14 +226,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   else total = E * (p.M / (kPair ? 2 * kTileM : kTileM)) * n_tiles;
   volatile int* abort_flag = &sm->abort;
 
-  if (kGather && warp == 0) {
+  if (kGather && (warp == 0 || warp >= 6)) {
     // ---------------------------------------------------------- gathering producer
-    // The whole warp gathers the A tile's 128 token rows of x (64 columns, 128
-    // bytes each) with cp.async: per warp instruction 4 rows of 8 lanes x 16
-    // bytes (lane l: row 4i + l / 8, chunk l % 8), written swizzled as a tiled
-    // 128B-swizzle load would (chunk c of row r at c ^ (r & 7)); each lane
-    // then arrives on the slot's barrier once its copies have landed. Lane 0
-    // also loads the weight boxes by TMA. This is the dispatch AllToAllv of
+    // kGatherWarps warps gather the A tile's 128 token rows of x (64 columns,
+    // 128 bytes each) with cp.async, an equal share each: per warp instruction
+    // 4 rows of 8 lanes x 16 bytes (lane l of gathering warp g: row
+    // g * 128 / kGatherWarps + 4i + l / 8, chunk l % 8), written
+    // swizzled as a tiled 128B-swizzle load would (chunk c of row r at
+    // c ^ (r & 7)); each lane then arrives on the slot's barrier once its
+    // copies have landed. Lane 0 of warp 0 also loads the weight boxes by TMA. This is the dispatch AllToAllv of
     // all2all_grouped_matmul folded into the GEMM's producer. (TMA gather4,
     // four rows per instruction, was bound by the TMA unit's rate at 3.4x the
     // materialised permute.)
@@ -237,13 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t fills = 0;
     bool ok = true;
     const int chunk = lane & 7;
+    const int g0 = (warp == 0 ? 0 : warp - 5) * (128 / kGatherWarps);   // first row of the tile
+    constexpr int kRows = 128 / kGatherWarps / 4;   // rows per lane
+    const bool lead = warp == 0 && lane == 0;
     for (int t = walk0; t < total && ok; t += walk_step) {
       const Tile tl = decode_tile<kSched, kPair>(t, ts, p);
       const int real_end = p.off_al[tl.e] + p.counts[tl.e];
-      const __nv_bfloat16* src[32];             // this lane's 32 rows, at column 0
+      const __nv_bfloat16* src[kRows];          // this lane's rows, at column 0
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int r = tl.row0 + 4 * i + (lane >> 3);
+      for (int i = 0; i < kRows; ++i) {
+        const int r = tl.row0 + g0 + 4 * i + (lane >> 3);
         const int tok = r < real_end ? __ldg(p.gather_token + r) : 0;   // padding: any valid row
         src[i] = p.gather_x + static_cast<int64_t>(tok) * p.K + chunk * 8;
       }
@@ -258,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sa = smem_u32(ring + stage * kStageBytes);
         const uint32_t sb = sa + kABytes;
-        if (lane == 0) {
+        if (lead) {
           mbar_arrive_expect_tx(full, (bn / 64) * kBBox);
           for (int j = 0; j < bn / 128; ++j) {
             tma_load_2d(sb + j * kBBox, &tmB0, full, n0 + 64 * j, krow + kb * BK);
@@ -266,8 +275,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int r = 4 * i + (lane >> 3);
+        for (int i = 0; i < kRows; ++i) {
+          const int r = g0 + 4 * i + (lane >> 3);
           cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * BK);
         }
         cp_async_arrive_noinc(full);
@@ -743,7 +752,7 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
   if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(block_threads<kGather>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -765,7 +774,7 @@ cudaError_t launch_bn(const CUtensorMap& a, const CUtensorMap& b0, const CUtenso
     configured[d] = true;
   }
   if (!kPair) {
-    kern<<<grid, kThreads, smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
+    kern<<<grid, block_threads<kGather>(), smem, st>>>(a, b0, b1, o.map[0], o.map[1], o.map[2], p);
     return cudaGetLastError();
   }
   // a persistent grid of pairs: at most one pair per two of the CTAs asked
