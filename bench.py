@@ -689,7 +689,7 @@ def run_ours(args, w):
         "dtype": run.dtype, "data": "synthetic",
         "config": {"workload": w.name, "T": w.T, "H": w.H, "F": w.F, "E": w.E, "k": w.k,
                    "step": "forward + backward" if w.backward else "forward",
-                   "dispatch": "gathered by fc1's TMA producer" if (args.fuse_gather and not
+                   "dispatch": "gathered by fc1's cp.async warps" if (args.fuse_gather and not
                                                                    w.backward and not w.mxfp8)
                    else "materialised permute",
                    "l2": "flushed before every step (512 MB write)",
