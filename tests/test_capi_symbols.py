@@ -188,6 +188,29 @@ def test_product_and_oracle_share_nothing():
         assert "moe_expert_dispatch_gb300" not in text and "libmoe" not in text, p
 
 
+def test_no_cluster_multicast_copies():
+    # every CTA loads its own operands: no bulk copy in the kernels carries
+    # .multicast::cluster. The one multicast form allowed is the MMA commit
+    # that signals both CTAs of a pair (tcgen05.commit ... multicast::cluster),
+    # which moves no data.
+    import glob
+    import re
+    srcs = glob.glob(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", "*.cu*"))
+    srcs += glob.glob(os.path.join(ROOT, "moe_expert_dispatch_gb300", "csrc", "*.h"))
+    assert srcs
+    seen = 0
+    for p in srcs:
+        text = open(p, encoding="utf-8").read()
+        # each inline-asm string: the instruction text between quotes
+        for instr in re.findall(r'"([^"\n]*)"', text):
+            if "multicast" not in instr:
+                continue
+            seen += 1
+            assert not re.search(r"cp\.async|cp\.reduce|\.bulk", instr), (p, instr)
+            assert instr.lstrip().startswith("tcgen05.commit"), (p, instr)
+    assert seen >= 1        # the scan does see the pair commit
+
+
 def test_host_side_argument_errors_of_every_entry_point(lib):
     # each call is wrong in one way the host can see; it must answer with
     # that status at once, before any device work (this machine has no GPU,
