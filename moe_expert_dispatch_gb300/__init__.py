@@ -16,7 +16,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 # MOE_GB300_DEBUG=1 loads the MOE_DEBUG build (device-side bounds checks of
 # the row indices taken from row maps, reported as MOE_ERR_BOUNDS)
 DEBUG = os.environ.get("MOE_GB300_DEBUG", "0") not in ("", "0")
-LIB_PATH = os.path.join(_HERE, "libmoe_gb300_debug.so" if DEBUG else "libmoe_gb300.so")
+# MOE_GB300_SANITIZE=1 loads the host-sanitizer build (AddressSanitizer and
+# UndefinedBehaviorSanitizer on the host code; the process must preload their
+# runtimes): it serves the host-side checks on a machine without a GPU
+SANITIZE = os.environ.get("MOE_GB300_SANITIZE", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libmoe_gb300_sanitize.so" if SANITIZE
+                        else "libmoe_gb300_debug.so" if DEBUG else "libmoe_gb300.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(

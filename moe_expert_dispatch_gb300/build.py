@@ -43,12 +43,19 @@ def _needs(obj: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
+_SAN = ["-Xcompiler", "-fsanitize=address", "-Xcompiler", "-fsanitize=undefined"]
 VARIANTS = {
     # release: the product library; debug: the same sources with MOE_DEBUG,
-    # whose kernels bounds-check the row indices they take from row maps
-    "release": (BUILD, LIB, []),
+    # whose kernels bounds-check the row indices they take from row maps;
+    # sanitize (built only on request): the host code under AddressSanitizer
+    # and UndefinedBehaviorSanitizer, for the host-side argument and size
+    # checks on a machine without a GPU (its process preloads the runtimes)
+    "release": (BUILD, LIB, [], []),
     "debug": (os.path.join(PKG, "_build_debug"), os.path.join(PKG, "libmoe_gb300_debug.so"),
-              ["-DMOE_DEBUG"]),
+              ["-DMOE_DEBUG"], []),
+    "sanitize": (os.path.join(PKG, "_build_sanitize"),
+                 os.path.join(PKG, "libmoe_gb300_sanitize.so"),
+                 _SAN + ["-Xcompiler", "-fno-omit-frame-pointer"], _SAN),
 }
 
 
@@ -59,7 +66,7 @@ def build(verbose: bool = False, force: bool = False, variants=("release", "debu
     headers.append(os.path.join(ROOT, "include", "moe_expert.h"))
     jobs, links = [], []
     for v in variants:
-        bdir, lib, extra = VARIANTS[v]
+        bdir, lib, extra, link_extra = VARIANTS[v]
         os.makedirs(bdir, exist_ok=True)
         objs = []
         for src in SOURCES:
@@ -68,7 +75,7 @@ def build(verbose: bool = False, force: bool = False, variants=("release", "debu
             objs.append(o)
             if force or _needs(o, [s] + headers):
                 jobs.append([nvcc(), *_flags(), *extra, "-c", s, "-o", o])
-        links.append((lib, objs))
+        links.append((lib, objs, link_extra))
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -80,9 +87,9 @@ def build(verbose: bool = False, force: bool = False, variants=("release", "debu
     if jobs:
         with cf.ThreadPoolExecutor(len(jobs)) as ex:
             list(ex.map(run, jobs))
-    for lib, objs in links:
+    for lib, objs, link_extra in links:
         if force or _needs(lib, objs):
-            run([nvcc(), *ARCH, "-shared", "-o", lib, *objs])
+            run([nvcc(), *ARCH, "-shared", "-o", lib, *objs, *link_extra])
     return LIB
 
 

@@ -188,6 +188,51 @@ def test_product_and_oracle_share_nothing():
         assert "moe_expert_dispatch_gb300" not in text and "libmoe" not in text, p
 
 
+def test_host_checks_under_address_and_undefined_behaviour_sanitizers(lib):
+    """The host-side argument and size checks (including the overflow guards
+    of the workspace sizes) run against the library built with
+    AddressSanitizer and UndefinedBehaviorSanitizer on its host code: every
+    check answers as in the release build, and neither sanitizer reports."""
+    import importlib.util
+    import shutil
+    import subprocess
+    import sys
+    import torch
+    if torch.cuda.is_available() or os.environ.get("MOE_GB300_SANITIZE"):
+        pytest.skip("host-only: the cases carry fake device addresses")
+    gcc = shutil.which("gcc")
+    if not gcc:
+        pytest.skip("no gcc to locate the sanitizer runtimes")
+    rts = [subprocess.run([gcc, f"-print-file-name={n}"], capture_output=True,
+                          text=True).stdout.strip() for n in ("libasan.so", "libubsan.so")]
+    if not all(os.path.isabs(r) and os.path.exists(r) for r in rts):
+        pytest.skip("sanitizer runtimes not installed")
+    spec = importlib.util.spec_from_file_location(
+        "_moe_build", os.path.join(ROOT, "moe_expert_dispatch_gb300", "build.py"))
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    b.build(variants=("sanitize",))
+    env = dict(os.environ, LD_PRELOAD=":".join(rts), MOE_GB300_SANITIZE="1",
+               ASAN_OPTIONS="detect_leaks=0:halt_on_error=1",
+               UBSAN_OPTIONS="halt_on_error=1:print_stacktrace=1")
+    probe = subprocess.run(
+        [sys.executable, "-c", "import moe_expert_dispatch_gb300 as m; "
+         "print(m.LIB_PATH); print('loaded' if 'libmoe_gb300_sanitize.so' in "
+         "open('/proc/self/maps').read() else 'missing')"],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert probe.returncode == 0, probe.stderr[-3000:]
+    assert probe.stdout.split() == [os.path.join(ROOT, "moe_expert_dispatch_gb300",
+                                                 "libmoe_gb300_sanitize.so"), "loaded"]
+    out = subprocess.run(
+        [sys.executable, "-m", "pytest", "-q", "-p", "no:cacheprovider", __file__, "-k",
+         "host_side or invalid_arguments or refuses_tensors or rejects_host"],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    log = out.stdout + out.stderr
+    assert out.returncode == 0, log[-4000:]
+    assert "5 passed" in out.stdout, log[-4000:]
+    assert "runtime error" not in log and "AddressSanitizer" not in log, log[-4000:]
+
+
 def test_no_cluster_multicast_copies():
     # every CTA loads its own operands: no bulk copy in the kernels carries
     # .multicast::cluster. The one multicast form allowed is the MMA commit
