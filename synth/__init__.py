@@ -237,7 +237,7 @@ def _sparse_columns(g: np.random.Generator, E: int, K: int, N: int, nnz: int,
 
 
 def exact_inputs(w: Workload, seed: int = 0) -> dict:
-    """Inputs of the BF16 block (with dY) whose arithmetic is exact in float32.
+    """Inputs of the block (with dY) whose arithmetic is exact in float32.
 
     Shapes and routing are the workload's (routing() draws ids as usual), but
     every value is a small integer or a dyadic fraction:
@@ -255,6 +255,11 @@ def exact_inputs(w: Workload, seed: int = 0) -> dict:
     backward is an integer or a multiple of 2^-m far below 2^24 units. Both
     sides then round the same real numbers at the same points, and any
     remaining difference is a mistake, not rounding.
+    MXFP8 workloads get the same values with the weights laid out
+    K-contiguous, as make_inputs lays them out (w_gate_t, w_up_t [E,F,H],
+    w_down_t [E,H,F]). A 32-element block of x or of a weight row then holds
+    integers of magnitude at most 44; under the E8M0 scale that its largest
+    sets, each of them is an E4M3 value, so quantising them is exact.
     """
     T, H, F, E, k = w.T, w.H, w.F, w.E, w.k
     g = _gen(seed, 200, 0)
@@ -276,8 +281,14 @@ def exact_inputs(w: Workload, seed: int = 0) -> dict:
     ids, _ = routing(w, seed, torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
                      if w.routing == "router" else None)
     bf = lambda a: torch.from_numpy(a).to(torch.bfloat16)  # noqa: E731
-    return {"workload": w, "x": bf(x), "w_gate": bf(wg), "w_up": bf(wu), "w_down": bf(wd),
-            "expert_ids": ids, "probs": torch.from_numpy(probs), "dy": bf(dy)}
+    out = {"workload": w, "x": bf(x), "expert_ids": ids, "probs": torch.from_numpy(probs),
+           "dy": bf(dy)}
+    if w.mxfp8:
+        kc = lambda a: bf(np.ascontiguousarray(a.transpose(0, 2, 1)))  # noqa: E731
+        out.update(w_gate_t=kc(wg), w_up_t=kc(wu), w_down_t=kc(wd))
+    else:
+        out.update(w_gate=bf(wg), w_up=bf(wu), w_down=bf(wd))
+    return out
 
 
 class F32Slices:

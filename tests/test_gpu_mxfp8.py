@@ -129,6 +129,32 @@ def test_mxfp8_workload_sampled():
     assert np.all(np.isfinite(y))
 
 
+def test_mxfp8_workload_exact_arithmetic_bit_equal():
+    """The MXFP8 workload at full size on exact-arithmetic inputs
+    (synth.exact_inputs: small integers that quantise to E4M3 x E8M0 exactly,
+    a gate pre-activation of at least 40 so that silu is the identity in
+    float32 and float64, dyadic routing weights). Every product and partial
+    sum is then exact on both sides, which round the same real numbers at
+    the same points: h to bf16, h to its E4M3 codes and E8M0 scales, O and y
+    to bf16. Sampled tokens that reach all 64 experts must be bit-equal."""
+    w = synth.WORKLOADS["mxfp8"]
+    inp = synth.exact_inputs(w, 0)
+    x, wg, wu, wd = inp["x"], inp["w_gate_t"], inp["w_up_t"], inp["w_down_t"]
+    ids, probs = inp["expert_ids"], inp["probs"]
+    y, _ = _gpu(x, wg, wu, wd, ids, probs)
+    y = to_np(y)
+    rng = np.random.default_rng(1)
+    toks = tokens_covering_experts(ids.numpy(), w.E,
+                                   extra=tuple(rng.choice(w.T, 40, replace=False).tolist()))
+    assert set(ids.numpy()[toks].reshape(-1).tolist()) == set(range(w.E))
+    f32 = lambda t: synth.F32Slices(t)  # noqa: E731
+    ref = orc.sampled_forward_mxfp8(to_np(x), f32(wg), f32(wu), f32(wd), ids.numpy(), probs.numpy(), toks)
+    assert np.abs(ref).max() > 256          # past bf16's exact integers: rounding is exercised
+    diff = int((y[toks] != ref).sum())
+    print(f"{len(toks)} tokens reach all {w.E} experts; {diff} of {ref.size} outputs differ")
+    assert diff == 0
+
+
 def _with_nonfinite(shape, seed):
     """N(0,1) bf16 values with about one element in 400 replaced by +inf,
     -inf or NaN."""

@@ -74,3 +74,23 @@ def test_router_logits_reproduce_workload_routing(name):
     assert np.array_equal(ids, inp["expert_ids"].numpy())
     np.testing.assert_allclose(probs, inp["probs"].numpy(), rtol=1e-6, atol=1e-7)
     assert synth.router_logits(synth.WORKLOADS["skewed_bf16"], 0) is None
+
+
+def test_exact_inputs_quantise_exactly_to_mxfp8():
+    # the MXFP8 layout of the exact-arithmetic inputs: K-contiguous weights
+    # holding the BF16 layout's values, and every 32-element block of x and
+    # of each weight row an exact E4M3 x E8M0 encoding (the oracle's
+    # quantiser round-trips it unchanged)
+    w = synth.WORKLOADS["mxfp8"].resized(T=96, H=256, F=384, E=3, k=2)
+    mx = synth.exact_inputs(w, 0)
+    bf = synth.exact_inputs(w.resized(mxfp8=False), 0)
+    assert torch.equal(mx["x"], bf["x"]) and torch.equal(mx["expert_ids"], bf["expert_ids"])
+    assert torch.equal(mx["w_gate_t"], bf["w_gate"].transpose(1, 2))
+    assert torch.equal(mx["w_up_t"], bf["w_up"].transpose(1, 2))
+    assert torch.equal(mx["w_down_t"], bf["w_down"].transpose(1, 2))
+    assert mx["w_gate_t"].shape == (3, 384, 256) and mx["w_down_t"].shape == (3, 256, 384)
+    mats = [mx["x"]] + [mx[n][e] for n in ("w_gate_t", "w_up_t", "w_down_t") for e in range(3)]
+    for a in mats:
+        a = a.float().numpy()
+        np.testing.assert_array_equal(orc.dequantize_mxfp8(*orc.quantize_mxfp8(a)), a)
+    assert mx["w_gate_t"][:, :, 0].eq(synth.EXACT_GATE_BIAS).all()
