@@ -89,19 +89,21 @@ def test_forward_mixtral_workload_sampled():
     assert_bf16_close(y[toks], ref, "y sampled")
 
 
-def test_forward_mixtral_workload_exact_all_tokens():
-    """The Mixtral-shaped forward at full size (T=4096, H=4096, F=14336, E=8,
-    k=2) on exact-arithmetic inputs (small integers, dyadic weights, a
-    saturated gate): y of every token within the BF16 bound and bit-equal to
-    the oracle's whole forward, on CTA pairs (the default here) and on one
-    CTA per tile."""
-    w = synth.WORKLOADS["mixtral_bf16"]
+@pytest.mark.parametrize("name", ["mixtral_bf16", "tiny_bf16", "skewed_bf16"])
+def test_forward_workload_exact_all_tokens(name):
+    """The BF16 forward workloads at full size (the Mixtral-shaped one: T=4096,
+    H=4096, F=14336, E=8, k=2; the tiny one; the skewed one with its empty
+    experts and k=8) on exact-arithmetic inputs (small integers, dyadic
+    weights, a saturated gate): y of every token within the BF16 bound and
+    bit-equal to the oracle's whole forward, on one CTA per tile and on CTA
+    pairs."""
+    w = synth.WORKLOADS[name]
     inp = synth.exact_inputs(w, 0)
     case = (inp["x"], inp["w_gate"], inp["w_up"], inp["w_down"], inp["expert_ids"], inp["probs"])
     ref = orc.expert_forward(to_np(case[0]), f32_slices(case[1]), f32_slices(case[2]),
                              f32_slices(case[3]), case[4].numpy(),
                              case[5].numpy().astype(np.float64), num_experts=w.E)
-    for pairs in (0, 1):
+    for pairs in (1, 2):
         y = to_np(_gpu(*case, cta_pairs=pairs))
         assert_bf16_close(y, ref, f"y (cta_pairs={pairs})")
         assert np.array_equal(y, ref), f"y: {int((y != ref).sum())} of {y.size} not bit-equal"
