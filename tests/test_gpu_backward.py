@@ -280,12 +280,15 @@ def _check_reduction_over_rows(got, ref, what):
     return int((err > 1e-2 + 1e-2 * np.abs(ref)).sum())
 
 
-def test_backward_train_workload_microbatch_splits():
+@pytest.mark.parametrize("exact", [False, True])
+def test_backward_train_workload_microbatch_splits(exact):
     """Micro-batch splits 1, 4 and 8 of the full training workload (T=16384):
     y, dX and dprobs bit-identical to the unsplit step (1: the step run
     again), dW summed over the chunks within the BF16 bound of the unsplit
-    dW (only the order of its float sums over rows changes)."""
-    w, case, dy = _train_case(exact=False)
+    dW (only the order of its float sums over rows changes). On
+    exact-arithmetic inputs those sums are exact in any order, so there dW
+    too must equal the unsplit dW bit for bit."""
+    w, case, dy = _train_case(exact=exact)
     full = _gpu_fwd_bwd(*case, dy)
     full = {k: v.cpu() for k, v in full.items()}
     torch.cuda.empty_cache()
@@ -295,8 +298,8 @@ def test_backward_train_workload_microbatch_splits():
             assert torch.equal(acc[key].cpu(), full[key]), (splits, key)
         for key in ("dw_gate", "dw_up", "dw_down"):
             got = acc[key].cpu()
-            if splits == 1:
-                assert torch.equal(got, full[key]), key
+            if splits == 1 or exact:
+                assert torch.equal(got, full[key]), (splits, key)
             else:
                 assert_bf16_close(to_np(got), to_np(full[key]), f"{key} at {splits} splits")
         del acc
