@@ -129,6 +129,25 @@ def test_forward_microbatch_split_bit_identical(splits):
     assert torch.equal(torch.cat(parts), y)
 
 
+@pytest.mark.parametrize("name", ["tiny_bf16", "mixtral_bf16", "skewed_bf16"])
+def test_forward_workload_microbatch_splits_full_size(name):
+    """The BF16 forward workloads at full size split into 2, 4 and 8
+    contiguous token chunks, each chunk a call of its own: the concatenated
+    y equals the unsplit call's y bit for bit (a token's output depends only
+    on its own rows, which keep their K order in every GEMM)."""
+    w = synth.WORKLOADS[name]
+    inp = synth.make_inputs(w, 0)
+    x, wg, wu, wd, ids, probs = (dev(inp[k]) for k in ("x", "w_gate", "w_up", "w_down",
+                                                        "expert_ids", "probs"))
+    y, _ = m.moe_expert_forward(x, wg, wu, wd, ids, probs)
+    for splits in (2, 4, 8):
+        n = w.T // splits
+        parts = [m.moe_expert_forward(x[i * n:(i + 1) * n], wg, wu, wd, ids[i * n:(i + 1) * n],
+                                      probs[i * n:(i + 1) * n])[0] for i in range(splits)]
+        assert torch.equal(torch.cat(parts), y), splits
+    assert m.moe_get_error() == 0
+
+
 def test_forward_zero_tokens():
     x, wg, wu, wd, ids, probs = _case(4, 128, 128, 4, 2)
     y, _ = m.moe_expert_forward(dev(x[:0]), dev(wg), dev(wu), dev(wd), dev(ids[:0]), dev(probs[:0]))

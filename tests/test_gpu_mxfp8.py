@@ -155,6 +155,24 @@ def test_mxfp8_workload_exact_arithmetic_bit_equal():
     assert diff == 0
 
 
+def test_mxfp8_workload_microbatch_splits_full_size():
+    """The MXFP8 workload at full size split into 2, 4 and 8 contiguous token
+    chunks, each chunk a call of its own: the concatenated y equals the
+    unsplit call's y bit for bit (x is quantised per token, so a chunk's
+    codes and scales are the unsplit call's rows)."""
+    w = synth.WORKLOADS["mxfp8"]
+    inp = synth.make_inputs(w, 0)
+    wq = _gpu_weights(inp["w_gate_t"], inp["w_up_t"], inp["w_down_t"])
+    x, ids, probs = dev(inp["x"]), dev(inp["expert_ids"]), dev(inp["probs"])
+    y, _ = m.moe_expert_forward_mxfp8(x, *wq, ids, probs)
+    for splits in (2, 4, 8):
+        n = w.T // splits
+        parts = [m.moe_expert_forward_mxfp8(x[i * n:(i + 1) * n], *wq, ids[i * n:(i + 1) * n],
+                                            probs[i * n:(i + 1) * n])[0] for i in range(splits)]
+        assert torch.equal(torch.cat(parts), y), splits
+    assert m.moe_get_error() == 0
+
+
 def _with_nonfinite(shape, seed):
     """N(0,1) bf16 values with about one element in 400 replaced by +inf,
     -inf or NaN."""
