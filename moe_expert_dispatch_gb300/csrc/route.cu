@@ -1118,15 +1118,21 @@ cudaError_t launch_permute_quantize(const __nv_bfloat16* x, int64_t T, int H, in
   return cudaGetLastError();
 }
 
-// One CTA per 128 permuted rows (one row block of the tiled layout): thread
-// i gathers the token-order scale row of permuted row i (zeros for padding
-// rows), drops its words into the block's atoms in shared memory, and the CTA
-// writes the K/128 atoms (K/32 x 128 bytes) out contiguously.
+// One CTA per 128 permuted rows (one row block of the tiled layout). Each
+// warp reads the token-order scale rows of 32 permuted rows (zeros for
+// padding rows), 32 words of all 32 rows at a time with its lanes on
+// consecutive words, so every load is one contiguous run of a row and 32 of
+// them are in flight per lane. The words land row by row in shared memory
+// with an odd row stride, and the CTA then writes the K/128 atoms (K/32 x
+// 128 bytes) out contiguously, each thread assembling 16 bytes of an atom
+// from four rows (atom word q holds row (q >> 2) + 32 (q & 3)).
+// The odd stride keeps both the row writes and the atom reads free of bank
+// conflicts.
 __global__ void __launch_bounds__(128) gather_tile_scales_kernel(
     const uint8_t* __restrict__ xs_tok, const int32_t* __restrict__ token_of,
     const int32_t* __restrict__ off_al, const int32_t* __restrict__ counts, int E, int K,
     uint8_t* __restrict__ xs_tiled) {
-  extern __shared__ uint32_t atoms[];        // [K/128][128] words
+  extern __shared__ uint32_t rows_w[];       // [128][stride] words
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTileM;
   if (r0 >= off_al[E]) return;               // capacity beyond the padded rows
   int lo = 0, hi = E - 1;                    // the expert that owns this row block
@@ -1135,23 +1141,41 @@ __global__ void __launch_bounds__(128) gather_tile_scales_kernel(
     if (off_al[mid] <= r0) lo = mid; else hi = mid - 1;
   }
   const int64_t real_end = static_cast<int64_t>(off_al[lo]) + counts[lo];
-  const int i = threadIdx.x;
-  const int64_t r = r0 + i;
-  const int tok = r < real_end ? __ldg(token_of + r) : -1;
   const int kgroups = K >> 7, nb = K >> 5;
-  const uint32_t* src = reinterpret_cast<const uint32_t*>(xs_tok + static_cast<int64_t>(tok) * nb);
-  const int word = (i & 31) * 4 + (i >> 5);  // (m % 32) * 16 + (m / 32) * 4 bytes
-  for (int kg = 0; kg < kgroups; ++kg) atoms[kg * 128 + word] = tok >= 0 ? __ldg(src + kg) : 0u;
+  const int stride = kgroups | 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t my_r = r0 + warp * 32 + lane;          // lane i: the token of row i
+  const int my_tok = my_r < real_end ? __ldg(token_of + my_r) : -1;
+  for (int c = 0; c < kgroups; c += 32) {              // 32 words of each of the 32 rows
+    const int w = c + lane;
+    uint32_t v[32];                                    // all 32 loads in flight at once
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int tok = __shfl_sync(0xffffffffu, my_tok, i);
+      v[i] = (tok >= 0 && w < kgroups)
+                 ? __ldg(reinterpret_cast<const uint32_t*>(xs_tok + static_cast<int64_t>(tok) * nb) + w)
+                 : 0u;
+    }
+    if (w < kgroups) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) rows_w[(warp * 32 + i) * stride + w] = v[i];
+    }
+  }
   __syncthreads();
   int4* dst = reinterpret_cast<int4*>(xs_tiled + static_cast<int64_t>(blockIdx.x) * kgroups * 512);
-  const int4* s4 = reinterpret_cast<const int4*>(atoms);
-  for (int j = i; j < kgroups * 32; j += blockDim.x) dst[j] = s4[j];
+  for (int j = threadIdx.x; j < kgroups * 32; j += blockDim.x) {
+    const int kg = j >> 5, p = j & 31;       // atom kg, words 4p .. 4p + 3
+    dst[j] = make_int4(static_cast<int>(rows_w[p * stride + kg]),
+                       static_cast<int>(rows_w[(p + 32) * stride + kg]),
+                       static_cast<int>(rows_w[(p + 64) * stride + kg]),
+                       static_cast<int>(rows_w[(p + 96) * stride + kg]));
+  }
 }
 
 cudaError_t launch_gather_tile_scales(const uint8_t* xs_tok, const int32_t* token_of,
                                       const int32_t* off_al, const int32_t* counts, int E, int K,
                                       int64_t cap, uint8_t* xs_tiled, cudaStream_t st) {
-  const int smem = (K >> 5) * kTileM;
+  const int smem = ((K >> 7) | 1) * kTileM * static_cast<int>(sizeof(uint32_t));
   static int configured[kMaxDevices] = {};    // per device: the largest size set so far
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return cudaErrorInvalidDevice;
